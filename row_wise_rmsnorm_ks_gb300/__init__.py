@@ -1,0 +1,6 @@
+"""Row-wise RMSNorm and fused residual-add RMSNorm for NVIDIA GB300 (sm_103a).
+
+The compute runs in hand-written CUDA kernels behind the C ABI of ``libks`` (include/ks.h).
+This package is the thin Python binding over it: it marshals torch tensors into pointers and
+sizes and never computes anything itself. There is no CPU fallback.
+"""
