@@ -1,0 +1,508 @@
+"""Benchmark: RMSNorm and fused residual-add RMSNorm on GB300, HBM GB/s against the roofline.
+
+One step is one pass of the whole hot path over one batch: ks_rms_norm (x -> y) and
+ks_fused_add_rms_norm (x2, residual in place) on the large prefill shape [32768, 8192] bf16,
+eps 1e-5, x and residual ~ N(0,1), weight = 1 + 0.1 N(0,1) (seeded, drawn on the device).
+Every tensor (512 MiB) is larger than the 129 MB L2, so no flush is needed between steps.
+
+Bytes counted per step are the algorithmic bytes (each element read once and written once):
+rms_norm 2*R*H*e + H*e, fused 4*R*H*e + H*e (Triton Kernels, "Kernels" table and "Benchmark
+results"; Triton Kernel Lab, "Decode Kernel Results" counts the same four tensor passes plus
+the weight for its residual RMSNorm).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ks|reference]
+
+Under torchrun each rank runs one full batch on its own GPU (rows are independent, so no
+collective touches the data; weak scaling); rank 0 prints one JSON line with the max time
+over ranks. Timing follows the pages' method: CUDA events on the launching stream, warm-up
+first, p50 per launch, and no timing is published unless the oracle agrees on sampled rows
+(Triton Kernel Lab, "Quick Start": the benchmark refuses to publish when a correctness case
+fails). The oracle runs only in the CPU-baseline leg (and in --impl reference).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "RMSNorm / fused-add RMSNorm HBM GB/s (% of GB300 peak) and p50 µs"
+WORKLOAD = ("large prefill bf16: rms_norm + fused_add_rms_norm on x, residual [32768,8192] "
+            "(512 MiB per tensor), weight 1+0.1N(0,1), eps=1e-5")
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["row_wise_rmsnorm_ks_gb300/csrc/ks_kernels.cuh",
+                  "row_wise_rmsnorm_ks_gb300/csrc/ks_abi.cu"]
+
+
+def algorithmic_bytes(op: str, rows: int, hidden: int, elem: int) -> int:
+    """Bytes an ideal kernel moves: each row element read once and written once, the weight
+    read once per launch."""
+    passes = 2 if op == "rms_norm" else 4
+    return passes * rows * hidden * elem + hidden * elem
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured (MEASURED_PEAKS.json)"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback 6.8 TB/s"}
+
+
+def recorded_traffic(op: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the current
+    kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.md")
+    if not os.path.exists(path):
+        return None
+    sha, val = None, None
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line.startswith("kernel_sources_sha:"):
+                sha = line.split(":", 1)[1].strip()
+            if line.startswith(f"{op}_dram_bytes_per_launch_full:"):
+                val = line.split(":", 1)[1].strip()
+    if sha != kernel_source_sha() or val in (None, "", "null"):
+        return None
+    return int(float(val))
+
+
+# --------------------------------------------------------------------------- clock sampler
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.6)  # let the first samples arrive before the timed region
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = list(csv.reader(io.StringIO(out)))
+        load, reasons, maxes, allsm = [], set(), [], []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 10:
+                continue
+            r = [c.strip() for c in r]
+            try:
+                ts = time.mktime(time.strptime(r[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                sm, smmax = float(r[2]), float(r[3])
+            except ValueError:
+                continue
+            allsm.append(sm)
+            maxes.append(smmax)
+            if self.t0 is not None and self.t0 - 1 <= ts <= self.t1 + 1:
+                load.append(sm)
+                for n, v in zip(names, r[6:10]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        samples = load or allsm
+        return {"sm_mhz": statistics.median(samples) if samples else None,
+                "sm_max_mhz": max(maxes) if maxes else None,
+                "reasons": sorted(reasons), "samples": len(load)}
+
+
+# ------------------------------------------------------------------------------ ks arm
+
+def run_ks(args) -> int:
+    import torch
+    import torch.distributed as dist
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    _abi.load()
+
+    R, H, e = args.rows, args.hidden, 2
+    eps = 1e-5
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    # Inputs, resident in HBM before the timed region. Each rank draws its own batch.
+    seed_off = 1000 * rank
+    x = synth.cast(synth.normal_dev((R, H), synth.SEED_X + seed_off, dev), "bf16")
+    xf = x.clone()
+    r = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL + seed_off, dev), "bf16")
+    w = synth.weight(H, "bf16").to(dev)
+    y = torch.empty_like(x)
+    torch.cuda.synchronize()
+
+    # Pristine copies of the rows the CPU-baseline leg will recompute.
+    S = min(R, args.cpu_rows_max)
+    host_in = {"x": x[:S].cpu(), "xf": xf[:S].cpu(), "r": r[:S].cpu(), "w": w.cpu()}
+
+    def ks_plain():
+        return _abi.ks_rms_norm(y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H, eps,
+                                _abi.KS_DTYPE_BF16, sh)
+
+    def ks_fused():
+        return _abi.ks_fused_add_rms_norm(xf.data_ptr(), r.data_ptr(), w.data_ptr(), R, H, eps,
+                                          _abi.KS_DTYPE_BF16, sh)
+
+    # First step on pristine inputs: its outputs are what the oracle is compared with.
+    _abi.check(ks_plain())
+    _abi.check(ks_fused())
+    torch.cuda.synchronize()
+    gpu_out = {"y": y[:S].cpu(), "x": xf[:S].cpu(), "r": r[:S].cpu()}
+    for _ in range(max(0, args.warmup - 1)):
+        ks_plain()
+        ks_fused()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly K steps, barrier + synchronize on both sides
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_begin()
+    t_start.record(stream)
+    for k in range(args.steps):
+        ev[k][0].record(stream)
+        ks_plain()
+        ev[k][1].record(stream)
+        ks_fused()
+        ev[k][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    sampler.mark_end()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    plain_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
+    fused_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    b_plain = algorithmic_bytes("rms_norm", R, H, e)
+    b_fused = algorithmic_bytes("fused_add_rms_norm", R, H, e)
+    step_bytes = b_plain + b_fused
+    ms_per_step = elapsed_ms / args.steps
+    value = world * step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+
+    peaks = measured_peaks()
+    fused_avg_s = statistics.fmean(fused_ms) * 1e-3
+    plain_avg_s = statistics.fmean(plain_ms) * 1e-3
+    achieved = b_fused / fused_avg_s / 1e9
+    ops = {
+        "rms_norm": {"bytes_per_launch": b_plain, "p50_us": statistics.median(plain_ms) * 1e3,
+                     "avg_us": plain_avg_s * 1e6, "gbs": b_plain / plain_avg_s / 1e9,
+                     "frac_of_peak": b_plain / plain_avg_s / 1e9 / peaks["hbm_gbs"]},
+        "fused_add_rms_norm": {"bytes_per_launch": b_fused,
+                               "p50_us": statistics.median(fused_ms) * 1e3,
+                               "avg_us": fused_avg_s * 1e6, "gbs": achieved,
+                               "frac_of_peak": achieved / peaks["hbm_gbs"]},
+    }
+
+    result = {}
+    if rank == 0:
+        # decode shape (launch-bound): p50 of single cache-cold launches, and graph replay
+        ops["decode_fused_add_rms_norm_4x1536"] = decode_latency(dev, args)
+        e2e = run_e2e(dev, args, R, H, eps) if not args.no_e2e else None
+        cpu = cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args)
+        if not cpu["parity"]["ok"]:
+            print(json.dumps({"error": "parity check failed; no timing published",
+                              "parity": cpu["parity"]}))
+            return 1
+        traffic = recorded_traffic("fused_add_rms_norm")
+        result = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) drawn on the device)",
+            "config": {"workload": WORKLOAD, "rows": R, "hidden": H, "eps": eps,
+                       "accumulate": "f32",
+                       "l2": "no flush: every tensor (512 MiB) is larger than L2",
+                       "parallelism": f"rows: one independent batch per GPU x{world}",
+                       "kernel_plan": {
+                           "rms_norm": _abi.ks_plan_launch(0, R, H, 2, True, 152, 0)[1].as_dict()["kernel_name"],
+                           "fused_add_rms_norm": _abi.ks_plan_launch(1, R, H, 2, True, 152, 0)[1].as_dict()["kernel_name"]}},
+            "roofline": {"bound": "hbm", "kernel": "fused_add_rms_norm (bf16 [32768,8192])",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "algorithmic_bytes": b_fused, "peak_source": peaks["source"]},
+            "cpu_baseline": cpu["baseline"],
+            "parity": cpu["parity"],
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks,
+            "ops": ops,
+        }
+        print(json.dumps(result))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def decode_latency(dev, args) -> dict:
+    """Fused op on the decode shape [4, 1536] bf16: single launches after an L2 flush (CUDA
+    events around each launch, the flush outside), and the per-launch time of a CUDA graph of
+    100 back-to-back launches."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    wl = synth.decode()
+    x, r, w = wl.x.to(dev), wl.residual.to(dev), wl.weight.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def launch(s):
+        return _abi.ks_fused_add_rms_norm(x.data_ptr(), r.data_ptr(), w.data_ptr(), 4, 1536,
+                                          wl.eps, _abi.KS_DTYPE_BF16, s)
+
+    for _ in range(20):
+        launch(stream.cuda_stream)
+    samples = []
+    for _ in range(args.decode_samples):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        launch(stream.cuda_stream)
+        b.record(stream)
+        b.synchronize()
+        samples.append(a.elapsed_time(b) * 1e3)
+    samples.sort()
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(stream)
+    with torch.cuda.stream(cs):
+        launch(cs.cuda_stream)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=cs):
+        for _ in range(100):
+            launch(cs.cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    reps = 20
+    for _ in range(reps):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    per_launch = a.elapsed_time(b) * 1e3 / (reps * 100)
+    nbytes = algorithmic_bytes("fused_add_rms_norm", 4, 1536, 2)
+    q = lambda p: samples[min(len(samples) - 1, int(p * len(samples)))]
+    return {"bytes_per_launch": nbytes, "p50_us_cold_event": q(0.5), "p95_us_cold_event": q(0.95),
+            "p99_us_cold_event": q(0.99), "us_per_launch_graph_replay": per_launch,
+            "samples": len(samples)}
+
+
+def run_e2e(dev, args, R, H, eps) -> dict:
+    """The same step through the public API with host buffers: pinned host -> device copies of
+    every input, both ops, device -> host copies of every output, all inside the timed region."""
+    import torch
+
+    import row_wise_rmsnorm_ks_gb300 as ks
+    from row_wise_rmsnorm_ks_gb300 import synth
+
+    stream = torch.cuda.current_stream(dev)
+    xd = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), "bf16")
+    rd = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev), "bf16")
+    xh = xd.cpu().pin_memory()
+    x2h = xh.clone().pin_memory()
+    rh = rd.cpu().pin_memory()
+    yh, xoh, roh = (torch.empty_like(xh).pin_memory() for _ in range(3))
+    w = synth.weight(H, "bf16").to(dev)
+    xdev, x2dev, rdev, ydev = xd, torch.empty_like(xd), rd, torch.empty_like(xd)
+
+    def step():
+        xdev.copy_(xh, non_blocking=True)
+        x2dev.copy_(x2h, non_blocking=True)
+        rdev.copy_(rh, non_blocking=True)
+        ks.rms_norm(xdev, w, eps, out=ydev)
+        ks.fused_add_rms_norm(x2dev, rdev, w, eps)
+        yh.copy_(ydev, non_blocking=True)
+        xoh.copy_(x2dev, non_blocking=True)
+        roh.copy_(rdev, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.e2e_steps
+    nbytes = algorithmic_bytes("rms_norm", R, H, 2) + algorithmic_bytes("fused_add_rms_norm", R, H, 2)
+    return {"value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+            "steps": args.e2e_steps, "h2d_bytes_per_step": 3 * R * H * 2,
+            "d2h_bytes_per_step": 3 * R * H * 2}
+
+
+def cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args) -> dict:
+    """The oracle, as it stands (single-threaded C), on the first rows of the same batch until
+    about `cpu_seconds` of work is done; its outputs are also compared with the GPU's."""
+    import torch
+
+    import oracle
+    from tests.helpers import bits_equal, ulp_dist, within_tol
+
+    S = host_in["x"].shape[0]
+    chunk = 256
+    done, t_plain, t_fused = 0, 0.0, 0.0
+    max_ulp, res_ok, tol_ok = 0, True, True
+    while done < S:
+        sl = slice(done, min(S, done + chunk))
+        t0 = time.perf_counter()
+        y_ref, _ = oracle.rms_norm(host_in["x"][sl], host_in["w"], eps)
+        t1 = time.perf_counter()
+        x_ref, r_ref, _ = oracle.fused_add_rms_norm(host_in["xf"][sl], host_in["r"][sl],
+                                                    host_in["w"], eps)
+        t2 = time.perf_counter()
+        t_plain += t1 - t0
+        t_fused += t2 - t1
+        res_ok &= bits_equal(gpu_out["r"][sl], r_ref)
+        for out, ref in ((gpu_out["y"][sl], y_ref), (gpu_out["x"][sl], x_ref)):
+            max_ulp = max(max_ulp, int(ulp_dist(out, ref).max()))
+            tol_ok &= within_tol(out, ref, 1e-2, 1e-3)[0]
+        done = sl.stop
+        if t_plain + t_fused >= args.cpu_seconds:
+            break
+    nb = algorithmic_bytes("rms_norm", done, H, 2) + algorithmic_bytes("fused_add_rms_norm", done, H, 2)
+    secs = t_plain + t_fused
+    return {
+        "baseline": {"value": nb / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                     "sample": f"first {done} of {R} rows of both ops ([{done},{H}] bf16), "
+                               f"{secs:.1f} s single-threaded",
+                     "host_cores_total": os.cpu_count()},
+        "parity": {"rows_checked": done, "max_ulp": max_ulp, "residual_bit_exact": res_ok,
+                   "within_tolerance": tol_ok, "ok": bool(res_ok and tol_ok and max_ulp <= 1)},
+    }
+
+
+# ------------------------------------------------------------------------ reference arm
+
+def run_reference(args) -> int:
+    """The oracle (the plain CPU definition) timed on the host cores on bounded samples of the
+    same workload. Rank 0 only; other ranks exit without work."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import torch
+
+    import oracle
+    from row_wise_rmsnorm_ks_gb300 import synth
+
+    R, H, eps = args.rows, args.hidden, 1e-5
+    budget = args.reference_seconds
+    # calibrate one row of each op, then size each step's sample to fit the budget
+    x1 = synth.cast(synth.normal_np((1, H), synth.SEED_X), "bf16")
+    w = synth.weight(H, "bf16")
+    t0 = time.perf_counter()
+    oracle.rms_norm(x1, w, eps)
+    oracle.fused_add_rms_norm(x1, x1.clone(), w, eps)
+    per_row = time.perf_counter() - t0
+    rows = max(1, min(R, int(budget / (args.steps + args.warmup) / per_row)))
+    x = synth.cast(synth.normal_np((rows, H), synth.SEED_X), "bf16")
+    r = synth.cast(synth.normal_np((rows, H), synth.SEED_RESIDUAL), "bf16")
+
+    def step():
+        oracle.rms_norm(x, w, eps)
+        oracle.fused_add_rms_norm(x, r, w, eps)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    secs = time.perf_counter() - t0
+    nb = algorithmic_bytes("rms_norm", rows, H, 2) + algorithmic_bytes("fused_add_rms_norm", rows, H, 2)
+    value = nb * args.steps / secs / 1e9
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1), host draw)",
+        "config": {"workload": WORKLOAD, "rows": R, "hidden": H, "eps": eps},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows} of {R} rows of both ops per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ks", "reference"], default="ks")
+    ap.add_argument("--rows", type=int, default=32768)
+    ap.add_argument("--hidden", type=int, default=8192)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-samples", type=int, default=300)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-rows-max", type=int, default=8192)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ks(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

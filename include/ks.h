@@ -1,0 +1,136 @@
+/*
+ * ks.h -- C ABI of libks: row-wise RMSNorm and fused residual-add RMSNorm on NVIDIA GB300
+ * (sm_103a).
+ *
+ * Boundary style (kernel-set, "Operators"): every entry point returns a ks_status_t and takes
+ * device pointers plus a ks_stream_t. No torch or C++ types cross this boundary.
+ *
+ * Semantics (Kernscope, "Numerical contract" and "API contract / Inputs"):
+ *
+ *   rms_norm:            for each row i of x viewed as [rows, hidden] (row-major, contiguous)
+ *                          x32   = fp32(x[i, :])
+ *                          scale = rsqrt(sum_j(x32_j^2) / hidden + eps)          (FP32)
+ *                          out[i, j] = cast((x32_j * scale) * fp32(weight[j]))
+ *   fused_add_rms_norm:  s = fp32(x[i, :]) + fp32(residual[i, :])                (one FP32 add)
+ *                          residual[i, :] = cast(s)                               (in place)
+ *                          x[i, :] = cast((s_j * rsqrt(mean(s^2) + eps)) * fp32(weight[j]))
+ *                        normalising the FP32 s, not the value rounded into residual.
+ *
+ * cast() rounds to nearest, ties to even, to the element type (+-inf on fp16 overflow, NaN
+ * stays NaN). rsqrt is the correctly rounded FP32 reciprocal square root; the sum of squares is
+ * accumulated in FP32 in an order of the library's choosing (a warp-shuffle tree).
+ *
+ * Ownership and threading: the caller owns all memory; the library never allocates device or
+ * pinned memory and keeps no state apart from a per-device cache of SM counts and kernel
+ * occupancies. Calls are asynchronous on `stream`: a successful return means the work was
+ * enqueued, and a fault in the kernel surfaces at the caller's next synchronisation. All entry
+ * points are thread-safe. weight is read-only.
+ *
+ * Error behaviour: every argument check happens before any CUDA call, so an invalid call returns
+ * its status without touching the device (and works on a machine without a GPU). The statuses:
+ *   KS_ERR_INVALID_ARGUMENT   hidden <= 0, rows < 0, a NULL pointer with rows > 0, eps not
+ *                             finite or not > 0, or a byte size that overflows int64;
+ *   KS_ERR_UNSUPPORTED_DTYPE  dtype outside ks_dtype_t;
+ *   KS_ERR_OVERLAP            fused: any two of the x, residual, weight byte ranges overlap;
+ *                             plain: out overlaps weight, or overlaps x without being exactly x;
+ *   KS_ERR_CUDA               querying the device or launching failed (see ks_last_error()).
+ * rows == 0 is legal (empty input) and returns KS_SUCCESS with no launch.
+ */
+#ifndef KS_H_
+#define KS_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of x, residual, out and weight (all four share it). */
+typedef enum ks_dtype {
+    KS_DTYPE_F32 = 0,
+    KS_DTYPE_F16 = 1,
+    KS_DTYPE_BF16 = 2
+} ks_dtype_t;
+
+typedef enum ks_status {
+    KS_SUCCESS = 0,
+    KS_ERR_INVALID_ARGUMENT = 1,
+    KS_ERR_UNSUPPORTED_DTYPE = 2,
+    KS_ERR_OVERLAP = 3,
+    KS_ERR_CUDA = 4
+} ks_status_t;
+
+/* A cudaStream_t passed as an opaque handle; NULL is the legacy default stream. */
+typedef void *ks_stream_t;
+
+/*
+ * RMSNorm (Kernscope, "Numerical contract / RMSNorm"; inputs per "API contract / Inputs").
+ *   out     device pointer, [rows, hidden] elements of dtype; may be exactly x (in place).
+ *   x       device pointer, [rows, hidden] elements of dtype, read-only unless out == x.
+ *   weight  device pointer, [hidden] elements of dtype, read-only.
+ *   rows    number of rows (the flattened leading dimensions); >= 0.
+ *   hidden  row width (the last dimension); > 0.
+ *   eps     finite, > 0; added to the mean square in FP32.
+ * Any alignment is accepted; 16-byte aligned pointers with hidden*sizeof(element) a multiple of
+ * 16 take the vectorised kernels, anything else a scalar kernel with the same arithmetic.
+ */
+ks_status_t ks_rms_norm(void *out, const void *x, const void *weight, int64_t rows,
+                        int64_t hidden, float eps, ks_dtype_t dtype, ks_stream_t stream);
+
+/*
+ * Fused residual-add RMSNorm, in place on both x and residual (Kernscope, "Numerical contract /
+ * Fused residual-add RMSNorm"; "API contract / Inputs": same shape, storage regions that do not
+ * overlap, x and residual modified in place, inference only).
+ *   x         device pointer, [rows, hidden]: input x; on return the normalised output.
+ *   residual  device pointer, [rows, hidden]: input residual; on return cast(x + residual).
+ *   weight    device pointer, [hidden], read-only.
+ *   rows, hidden, eps, dtype, stream as for ks_rms_norm.
+ */
+ks_status_t ks_fused_add_rms_norm(void *x, void *residual, const void *weight, int64_t rows,
+                                  int64_t hidden, float eps, ks_dtype_t dtype,
+                                  ks_stream_t stream);
+
+/* Static, human-readable name of a status ("KS_SUCCESS", ...); "KS_UNKNOWN_STATUS" otherwise. */
+const char *ks_status_string(ks_status_t status);
+
+/* Detail of the most recent non-success status returned on the calling thread (which check
+ * failed, or the CUDA error string). Valid until the next ks_* call on that thread. */
+const char *ks_last_error(void);
+
+/*
+ * Launch plan, for introspection and tests. A pure host function: no CUDA call.
+ *   op              0 = rms_norm, 1 = fused_add_rms_norm.
+ *   aligned16       non-zero when every pointer of the call is 16-byte aligned.
+ *   sm_count        multiprocessors of the device (152 on GB300).
+ *   blocks_per_sm   resident CTAs per SM for the chosen kernel (0: plan the CTA shape only and
+ *                   leave grid at the number of CTAs one pass over the rows needs).
+ * On success *plan describes the launch the entry points would make.
+ */
+typedef struct ks_plan {
+    int32_t kernel;         /* KS_KERNEL_* below */
+    int32_t vec_per_thread; /* 16-byte vectors per thread and tensor (vector kernels) */
+    int32_t team;           /* threads per row: 32 (warp per row) or block (CTA per row) */
+    int32_t block;          /* threads per CTA */
+    int64_t grid;           /* CTAs launched */
+    int64_t rows_per_pass;  /* rows in flight per pass over the grid (grid * rows per CTA) */
+} ks_plan_t;
+
+enum {
+    KS_KERNEL_NONE = 0,     /* rows == 0: nothing is launched */
+    KS_KERNEL_WARP_ROW = 1, /* one warp per row, row in registers, 16-byte vectors */
+    KS_KERNEL_CTA_ROW = 2,  /* one CTA per row, row in registers, 16-byte vectors */
+    KS_KERNEL_SCALAR = 3    /* one CTA per row, element loads, two passes over the row */
+};
+
+ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t dtype,
+                           int32_t aligned16, int32_t sm_count, int32_t blocks_per_sm,
+                           ks_plan_t *plan);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t ks_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KS_H_ */

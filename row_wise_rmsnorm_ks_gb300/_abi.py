@@ -1,0 +1,116 @@
+"""ctypes binding of libks's C ABI (include/ks.h), one Python function per C entry point, with
+the same names. Argument marshalling only: pointers and sizes in, a status out.
+
+The library is loaded on first use. If it has not been built there is no fallback: the call
+raises ``KsLibraryMissing``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libks.so")
+
+KS_DTYPE_F32, KS_DTYPE_F16, KS_DTYPE_BF16 = 0, 1, 2
+KS_SUCCESS, KS_ERR_INVALID_ARGUMENT, KS_ERR_UNSUPPORTED_DTYPE, KS_ERR_OVERLAP, KS_ERR_CUDA = range(5)
+KS_KERNEL_NONE, KS_KERNEL_WARP_ROW, KS_KERNEL_CTA_ROW, KS_KERNEL_SCALAR = range(4)
+KERNEL_NAMES = {0: "none", 1: "warp_row", 2: "cta_row", 3: "scalar"}
+
+# Every symbol include/ks.h declares (checked by the CPU test of the boundary).
+EXPORTED = ("ks_rms_norm", "ks_fused_add_rms_norm", "ks_status_string", "ks_last_error",
+            "ks_plan_launch", "ks_version")
+
+
+class KsLibraryMissing(RuntimeError):
+    pass
+
+
+class KsError(RuntimeError):
+    def __init__(self, status: int, name: str, detail: str):
+        super().__init__(f"{name}: {detail}")
+        self.status = status
+        self.name = name
+        self.detail = detail
+
+
+class ks_plan_t(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("vec_per_thread", ctypes.c_int32),
+                ("team", ctypes.c_int32), ("block", ctypes.c_int32), ("grid", ctypes.c_int64),
+                ("rows_per_pass", ctypes.c_int64)]
+
+    def as_dict(self) -> dict:
+        d = {f: getattr(self, f) for f, _ in self._fields_}
+        d["kernel_name"] = KERNEL_NAMES.get(self.kernel, "?")
+        return d
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str | None = None):
+    """Load libks (once). Raises KsLibraryMissing if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise KsLibraryMissing(
+                f"{p} is missing: build it with `python -m row_wise_rmsnorm_ks_gb300.build` "
+                "(there is no CPU fallback)")
+        lib = ctypes.CDLL(p)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        lib.ks_rms_norm.argtypes = [vp, vp, vp, i64, i64, f32, ctypes.c_int, vp]
+        lib.ks_rms_norm.restype = ctypes.c_int
+        lib.ks_fused_add_rms_norm.argtypes = [vp, vp, vp, i64, i64, f32, ctypes.c_int, vp]
+        lib.ks_fused_add_rms_norm.restype = ctypes.c_int
+        lib.ks_status_string.argtypes = [ctypes.c_int]
+        lib.ks_status_string.restype = ctypes.c_char_p
+        lib.ks_last_error.argtypes = []
+        lib.ks_last_error.restype = ctypes.c_char_p
+        lib.ks_plan_launch.argtypes = [i32, i64, i64, ctypes.c_int, i32, i32, i32,
+                                       ctypes.POINTER(ks_plan_t)]
+        lib.ks_plan_launch.restype = ctypes.c_int
+        lib.ks_version.argtypes = []
+        lib.ks_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def ks_rms_norm(out: int, x: int, weight: int, rows: int, hidden: int, eps: float, dtype: int,
+                stream: int | None) -> int:
+    return load().ks_rms_norm(out, x, weight, rows, hidden, eps, dtype, stream)
+
+
+def ks_fused_add_rms_norm(x: int, residual: int, weight: int, rows: int, hidden: int,
+                          eps: float, dtype: int, stream: int | None) -> int:
+    return load().ks_fused_add_rms_norm(x, residual, weight, rows, hidden, eps, dtype, stream)
+
+
+def ks_status_string(status: int) -> str:
+    return load().ks_status_string(status).decode()
+
+
+def ks_last_error() -> str:
+    return load().ks_last_error().decode()
+
+
+def ks_plan_launch(op: int, rows: int, hidden: int, dtype: int, aligned16: bool, sm_count: int,
+                   blocks_per_sm: int) -> tuple[int, ks_plan_t]:
+    plan = ks_plan_t()
+    st = load().ks_plan_launch(op, rows, hidden, dtype, int(bool(aligned16)), sm_count,
+                               blocks_per_sm, ctypes.byref(plan))
+    return st, plan
+
+
+def ks_version() -> int:
+    return load().ks_version()
+
+
+def check(status: int) -> None:
+    """Raise KsError for a non-success status, with the library's detail string."""
+    if status != KS_SUCCESS:
+        raise KsError(status, ks_status_string(status), ks_last_error())

@@ -1,0 +1,37 @@
+// Declarations shared by the translation units of libks (host side only).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ks.h"
+
+namespace ks {
+
+// Arguments every row kernel receives, passed by value in the kernel parameter space.
+struct RowArgs {
+    void *out;          // plain: y (may be exactly x); fused: x, written in place
+    const void *x;      // the input rows
+    void *res;          // fused: residual, read then written in place; plain: unused
+    const void *w;      // weight [hidden]
+    int64_t rows;
+    int64_t hidden;     // H, the real row width (the divisor of the mean)
+    int64_t hv;         // H / elements-per-16-byte-vector (vector kernels)
+    float eps;
+};
+
+// Host heuristic: fills *p from the shape, the element size and the device's SM count.
+// blocks_per_sm == 0 leaves grid at one pass over the rows.
+ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem_bytes, bool aligned16,
+                 int sm_count, int blocks_per_sm, ks_plan_t *p);
+
+// Per-dtype launchers (one translation unit each). `blocks_per_sm` queries the occupancy of the
+// kernel the plan names; `launch` enqueues it.
+int blocks_per_sm_bf16(const ks_plan_t &p, bool fused);
+int blocks_per_sm_f16(const ks_plan_t &p, bool fused);
+int blocks_per_sm_f32(const ks_plan_t &p, bool fused);
+cudaError_t launch_bf16(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);
+cudaError_t launch_f16(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);
+cudaError_t launch_f32(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);
+
+}  // namespace ks

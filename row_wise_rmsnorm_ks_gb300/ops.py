@@ -1,0 +1,85 @@
+"""Tensor-level API over the C ABI, with Kernscope's signatures ("API contract"):
+
+    rms_norm(x, weight, eps=1e-6) -> y
+    fused_add_rms_norm(x, residual, weight, eps=1e-6) -> None   (x and residual updated in place)
+
+Checks follow Kernscope "API contract / Inputs": x is (..., hidden) with a non-empty last
+dimension, weight is (hidden,), tensors are contiguous CUDA tensors of one dtype (fp16, bf16 or
+fp32) on one device, eps is finite and positive, the fused op's residual has x's shape and the
+storage of x, residual and weight does not overlap; tensors that require grad are rejected
+(inference only). The leading dimensions are flattened into rows. Every launch goes through
+libks on the tensor's device and the current torch stream; nothing is computed here.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _abi
+
+_DTYPES = {torch.float32: _abi.KS_DTYPE_F32, torch.float16: _abi.KS_DTYPE_F16,
+           torch.bfloat16: _abi.KS_DTYPE_BF16}
+
+
+def _check(x: torch.Tensor, weight: torch.Tensor, eps: float, names=("x", "weight")):
+    if not isinstance(x, torch.Tensor) or not isinstance(weight, torch.Tensor):
+        raise TypeError("x and weight must be torch tensors")
+    if x.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {x.dtype}; use float16, bfloat16 or float32")
+    if weight.dtype != x.dtype:
+        raise TypeError(f"{names[1]} dtype {weight.dtype} differs from {names[0]} dtype {x.dtype}")
+    if x.device.type != "cuda" or weight.device != x.device:
+        raise ValueError("tensors must be CUDA tensors on one device (there is no CPU path)")
+    if x.dim() < 1 or x.shape[-1] == 0:
+        raise ValueError("the last dimension of x must be non-empty")
+    if weight.dim() != 1 or weight.shape[0] != x.shape[-1]:
+        raise ValueError(f"weight must have shape ({x.shape[-1]},), got {tuple(weight.shape)}")
+    if not x.is_contiguous() or not weight.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    if torch.is_grad_enabled() and (x.requires_grad or weight.requires_grad):
+        raise RuntimeError("these kernels are inference-only: inputs must not require grad")
+    if not (isinstance(eps, (int, float)) and math.isfinite(eps) and eps > 0):
+        raise ValueError("eps must be finite and positive")
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def rms_norm(x: torch.Tensor, weight: torch.Tensor, eps: float = 1e-6, *,
+             out: torch.Tensor | None = None) -> torch.Tensor:
+    """y = cast(fp32(x) * rsqrt(mean(fp32(x)^2) + eps) * fp32(weight)) per row. `out` may be x
+    itself (in place) or a new contiguous tensor of x's shape and dtype."""
+    _check(x, weight, eps)
+    if out is None:
+        out = torch.empty_like(x)
+    elif (out.shape != x.shape or out.dtype != x.dtype or out.device != x.device
+          or not out.is_contiguous()):
+        raise ValueError("out must be a contiguous tensor with x's shape, dtype and device")
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden
+    with torch.cuda.device(x.device):
+        _abi.check(_abi.ks_rms_norm(out.data_ptr(), x.data_ptr(), weight.data_ptr(), rows, hidden,
+                                    float(eps), _DTYPES[x.dtype], _stream(x.device)))
+    return out
+
+
+def fused_add_rms_norm(x: torch.Tensor, residual: torch.Tensor, weight: torch.Tensor,
+                       eps: float = 1e-6) -> None:
+    """In place: residual <- cast(fp32(x) + fp32(residual)); x <- RMSNorm of the FP32 sum
+    times fp32(weight). Returns None."""
+    _check(x, weight, eps)
+    if not isinstance(residual, torch.Tensor) or residual.shape != x.shape:
+        raise ValueError("residual must have the same shape as x")
+    if residual.dtype != x.dtype or residual.device != x.device or not residual.is_contiguous():
+        raise ValueError("residual must be contiguous, with x's dtype and device")
+    if torch.is_grad_enabled() and residual.requires_grad:
+        raise RuntimeError("these kernels are inference-only: inputs must not require grad")
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden
+    with torch.cuda.device(x.device):
+        _abi.check(_abi.ks_fused_add_rms_norm(x.data_ptr(), residual.data_ptr(),
+                                              weight.data_ptr(), rows, hidden, float(eps),
+                                              _DTYPES[x.dtype], _stream(x.device)))
+    return None

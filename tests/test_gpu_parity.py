@@ -1,0 +1,225 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, element by element, on the
+same seeded inputs. Residual outputs must be bit-exact; normalised outputs within 1 ulp and the
+stated tolerance (bf16 1e-2*|ref| + 1e-3, fp16 2e-3*|ref| + 1e-4).
+
+Workloads follow the pages' shapes (Kernscope "CUDA performance", Triton Kernel Lab "Measured
+Result" and "Decode Kernel Results", Triton Kernels "Benchmark results") widened to GB300 sizes;
+the multi-gigabyte cases are compared on sampled rows plus properties checked on every row.
+"""
+import pytest
+import torch
+
+import oracle
+import row_wise_rmsnorm_ks_gb300 as ks
+from gpu_common import compare_output, record, run_and_check, sample_rows
+from helpers import bits_equal, ulp_dist
+from row_wise_rmsnorm_ks_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def test_small_bf16(cuda_device):
+    run_and_check(synth.small(), cuda_device)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_medium_with_constant_and_zero_rows(cuda_device, dtype):
+    w = synth.medium(dtype)
+    out = run_and_check(w, cuda_device)
+    y = out["y"].cpu()
+    zi, ci, c = w.notes["zero_row"], w.notes["const_row"], w.notes["c"]
+    assert (y[zi].double() == 0).all()
+    # closed form for the constant row: c * w_j / sqrt(c^2 + eps), within 1 ulp
+    eps32 = float(torch.tensor(w.eps, dtype=torch.float32))
+    exact = (c * w.weight.double() / (c * c + eps32) ** 0.5)
+    ref = oracle.encode(exact, w.dtype)
+    assert int(ulp_dist(y[ci], ref).max()) <= 1
+
+
+def test_fused_bf16(cuda_device):
+    run_and_check(synth.fused(), cuda_device)
+
+
+def test_fused_decode_shape(cuda_device):
+    run_and_check(synth.decode(), cuda_device)
+
+
+@pytest.mark.parametrize("rows", [1024, 4096, 32768])
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
+def test_prefill_sampled(cuda_device, op, rows):
+    """The large prefill shape [rows, 8192] bf16, eps 1e-5 (rows up to 32768: 512 MiB a tensor),
+    in the launch configuration the bench times. Sampled rows against the oracle; every row's
+    residual against the rounded sum, computed independently with torch on the device."""
+    w = synth.prefill_device(op, rows, 8192, "bf16", cuda_device)
+    idx = sample_rows(rows)
+    x_in = w.x.clone()
+    r_in = w.residual.clone() if w.residual is not None else None
+    out = run_and_check(w, cuda_device, rows_idx=idx, name=f"prefill {op} [{rows},8192]")
+    if op != "rms_norm":
+        assert bits_equal(out["r"], (x_in.float() + r_in.float()).to(torch.bfloat16))
+    else:
+        assert bool(torch.isfinite(out["y"].float()).all())
+
+
+WIDE_H = [1536, 5120, 7168, 14336, 16384]
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
+@pytest.mark.parametrize("hidden", WIDE_H)
+@pytest.mark.parametrize("rows", [1, 7, 333])
+def test_wide_sweep_full(cuda_device, rows, hidden, op, dtype):
+    """Heavy-tailed Student-t(3) rows, 1% of rows scaled by 1e3; every row compared."""
+    w = synth.wide_device(op, hidden, rows, dtype, cuda_device)
+    run_and_check(w, cuda_device, name=f"wide {op} {dtype} [{rows},{hidden}]")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
+@pytest.mark.parametrize("hidden", WIDE_H)
+def test_wide_sweep_65536_rows_sampled(cuda_device, hidden, op, dtype):
+    rows = 65536
+    w = synth.wide_device(op, hidden, rows, dtype, cuda_device)
+    outl = w.notes["outlier_rows"]
+    idx = sample_rows(rows, extra=outl[:16] + outl[-4:])
+    x_in = w.x.clone()
+    r_in = w.residual.clone() if w.residual is not None else None
+    out = run_and_check(w, cuda_device, rows_idx=idx, name=f"wide {op} {dtype} [65536,{hidden}]")
+    if op != "rms_norm":
+        assert bits_equal(out["r"], (x_in.float() + r_in.float()).to(w.dtype))
+    del x_in, r_in, out, w
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------------------ edge cases
+
+EDGE_H = [1, 2, 3, 5, 7, 8, 16, 17, 64, 255, 1000, 1001, 4095, 4097, 12289, 20000, 40000]
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
+@pytest.mark.parametrize("hidden", EDGE_H)
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
+def test_edge_widths(cuda_device, hidden, dtype, op):
+    """Ragged and odd widths (scalar path), widths around vector and team boundaries, and rows
+    wider than the register-resident kernels hold."""
+    rows = 5 if hidden < 20000 else 2
+    dt = synth.dtype_of(dtype)
+    x = synth.cast(synth.normal_np((rows, hidden), 31), dt)
+    wt = synth.weight(hidden, dt)
+    r = synth.cast(synth.normal_np((rows, hidden), 32), dt) if op != "rms_norm" else None
+    w = synth.Workload(f"edge {op} {dtype} [{rows},{hidden}]", op, dt, x, wt, 1e-6, residual=r)
+    run_and_check(w, cuda_device)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
+def test_unaligned_pointers(cuda_device, dtype, op):
+    """Views starting one element into their storage are not 16-byte aligned: the scalar kernel
+    must take them and give the same answers."""
+    dt = synth.dtype_of(dtype)
+    rows, hidden = 9, 1024
+    base = synth.cast(synth.normal_np((rows * hidden + 1,), 41), dt).to(cuda_device)
+    x = base[1:].view(rows, hidden)
+    wbase = synth.weight(hidden + 1, dt).to(cuda_device)
+    wt = wbase[1:]
+    assert x.data_ptr() % 16 != 0 and wt.data_ptr() % 16 != 0
+    x_host, w_host = x.cpu(), wt.cpu()
+    if op == "rms_norm":
+        y = ks.rms_norm(x, wt, 1e-6)
+        ref, _ = oracle.rms_norm(x_host, w_host, 1e-6)
+        compare_output(y.cpu(), ref, dt, hidden, f"unaligned {op} {dtype}")
+    else:
+        rbase = synth.cast(synth.normal_np((rows * hidden + 1,), 42), dt).to(cuda_device)
+        r = rbase[1:].view(rows, hidden)
+        r_host = r.cpu()
+        ks.fused_add_rms_norm(x, r, wt, 1e-6)
+        ref_x, ref_r, _ = oracle.fused_add_rms_norm(x_host, r_host, w_host, 1e-6)
+        assert bits_equal(r.cpu(), ref_r)
+        compare_output(x.cpu(), ref_x, dt, hidden, f"unaligned {op} {dtype}")
+
+
+@pytest.mark.parametrize("hidden", [1024, 4096, 5000])
+def test_in_place_plain(cuda_device, hidden):
+    """out == x is allowed: each row is read completely before it is written."""
+    x = synth.cast(synth.normal_np((64, hidden), 51), torch.bfloat16)
+    wt = synth.weight(hidden, torch.bfloat16)
+    ref, _ = oracle.rms_norm(x, wt, 1e-6)
+    xd = x.to(cuda_device)
+    y = ks.rms_norm(xd, wt.to(cuda_device), 1e-6, out=xd)
+    assert y.data_ptr() == xd.data_ptr()
+    compare_output(xd.cpu(), ref, torch.bfloat16, hidden, f"in-place rms_norm [64,{hidden}]")
+
+
+def test_empty_and_batched_shapes(cuda_device):
+    wt = synth.weight(64, torch.bfloat16).to(cuda_device)
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device=cuda_device)
+    assert ks.rms_norm(x, wt).shape == (0, 64)
+    r = torch.empty_like(x)
+    assert ks.fused_add_rms_norm(x, r, wt) is None
+    # leading dimensions are flattened: Kernscope's (2, 3, 5)-style shapes
+    x3 = synth.cast(synth.normal_np((2, 3, 64), 3), torch.bfloat16)
+    y3 = ks.rms_norm(x3.to(cuda_device), wt).cpu()
+    ref, _ = oracle.rms_norm(x3, wt.cpu())
+    compare_output(y3, ref, torch.bfloat16, 64, "batched (2,3,64)")
+
+
+def test_fused_with_zero_residual_equals_plain_on_gpu(cuda_device):
+    x = synth.cast(synth.normal_np((333, 4096), 61), torch.bfloat16).to(cuda_device)
+    wt = synth.weight(4096, torch.bfloat16).to(cuda_device)
+    y = ks.rms_norm(x, wt)
+    xf = x.clone()
+    r = torch.zeros_like(x)
+    ks.fused_add_rms_norm(xf, r, wt)
+    assert bits_equal(xf.cpu(), y.cpu()) and bits_equal(r.cpu(), x.cpu())
+
+
+def test_nonfinite_matches_oracle(cuda_device):
+    x = torch.tensor([[1.0, float("inf"), 2.0, 3.0, 0.5, 0.25, 1.5, 2.5],
+                      [1.0, float("nan"), 1.0, 1.0, 1.0, 1.0, 1.0, 1.0],
+                      [1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0, 8.0]], dtype=torch.float32)
+    wt = torch.ones(8)
+    y = ks.rms_norm(x.to(cuda_device), wt.to(cuda_device)).cpu()
+    ref, _ = oracle.rms_norm(x, wt)
+    assert bits_equal(y[:2], ref[:2])
+
+
+def test_deterministic_and_guard_bands(cuda_device):
+    """Two launches give identical bits; bytes just past the output are never written."""
+    rows, hidden = 1000, 4096
+    x = synth.cast(synth.normal_np((rows, hidden), 71), torch.bfloat16).to(cuda_device)
+    wt = synth.weight(hidden, torch.bfloat16).to(cuda_device)
+    buf = torch.full((rows * hidden + 4096,), 7.0, dtype=torch.bfloat16, device=cuda_device)
+    out = buf[:rows * hidden].view(rows, hidden)
+    ks.rms_norm(x, wt, out=out)
+    y2 = ks.rms_norm(x, wt)
+    assert bits_equal(out.cpu(), y2.cpu())
+    assert (buf[rows * hidden:].float() == 7.0).all()
+    record("guard bands", ok=True)
+
+
+def test_rejects_requires_grad_and_cpu(cuda_device):
+    x = torch.randn(4, 64, device=cuda_device, requires_grad=True)
+    with pytest.raises(RuntimeError):
+        ks.rms_norm(x, torch.ones(64, device=cuda_device))
+    with pytest.raises(ValueError):
+        ks.rms_norm(torch.randn(4, 64), torch.ones(64))
+
+
+def test_overlap_rejected_before_launch(cuda_device):
+    x = torch.randn(8, 64, device=cuda_device)
+    with pytest.raises(ks.KsError) as e:
+        ks.fused_add_rms_norm(x, x, torch.ones(64, device=cuda_device))
+    assert e.value.name == "KS_ERR_OVERLAP"
+
+
+def test_streams_are_honoured(cuda_device):
+    """The launch goes to torch's current stream."""
+    s = torch.cuda.Stream()
+    x = synth.cast(synth.normal_np((256, 4096), 81), torch.bfloat16).to(cuda_device)
+    wt = synth.weight(4096, torch.bfloat16).to(cuda_device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        y = ks.rms_norm(x, wt)
+    s.synchronize()
+    ref, _ = oracle.rms_norm(x.cpu(), wt.cpu())
+    compare_output(y.cpu(), ref, torch.bfloat16, 4096, "side stream")
