@@ -51,6 +51,27 @@ def algorithmic_bytes(op: str, rows: int, hidden: int, elem: int) -> int:
     return passes * rows * hidden * elem + hidden * elem
 
 
+def whole_job_gbs(world: int, step_bytes: int, steps: int, elapsed_ms: float) -> float:
+    """Aggregate throughput: the bytes every rank moved over the slowest rank's time."""
+    return world * step_bytes * steps / (elapsed_ms * 1e-3) / 1e9
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws an independent batch (rows shard across GPUs with no exchange)."""
+    return base + 1000 * rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The maximum of `value` over all ranks of the default process group (or `value` alone)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -171,10 +192,9 @@ def run_ks(args) -> int:
     sh = stream.cuda_stream
 
     # Inputs, resident in HBM before the timed region. Each rank draws its own batch.
-    seed_off = 1000 * rank
-    x = synth.cast(synth.normal_dev((R, H), synth.SEED_X + seed_off, dev), "bf16")
+    x = synth.cast(synth.normal_dev((R, H), rank_seed(synth.SEED_X, rank), dev), "bf16")
     xf = x.clone()
-    r = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL + seed_off, dev), "bf16")
+    r = synth.cast(synth.normal_dev((R, H), rank_seed(synth.SEED_RESIDUAL, rank), dev), "bf16")
     w = synth.weight(H, "bf16").to(dev)
     y = torch.empty_like(x)
     torch.cuda.synchronize()
@@ -223,11 +243,7 @@ def run_ks(args) -> int:
         dist.barrier()
     sampler.mark_end()
     clocks = sampler.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
 
     plain_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
     fused_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
@@ -235,7 +251,7 @@ def run_ks(args) -> int:
     b_fused = algorithmic_bytes("fused_add_rms_norm", R, H, e)
     step_bytes = b_plain + b_fused
     ms_per_step = elapsed_ms / args.steps
-    value = world * step_bytes * args.steps / (elapsed_ms * 1e-3) / 1e9
+    value = whole_job_gbs(world, step_bytes, args.steps, elapsed_ms)
 
     peaks = measured_peaks()
     fused_avg_s = statistics.fmean(fused_ms) * 1e-3
@@ -254,7 +270,8 @@ def run_ks(args) -> int:
     result = {}
     if rank == 0:
         # decode shape (launch-bound): p50 of single cache-cold launches, and graph replay
-        ops["decode_fused_add_rms_norm_4x1536"] = decode_latency(dev, args)
+        if not args.no_decode:
+            ops["decode_fused_add_rms_norm_4x1536"] = decode_latency(dev, args)
         e2e = run_e2e(dev, args, R, H, eps) if not args.no_e2e else None
         cpu = cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args)
         if not cpu["parity"]["ok"]:
@@ -493,6 +510,7 @@ def main() -> int:
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--decode-samples", type=int, default=300)
+    ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-rows-max", type=int, default=8192)
     ap.add_argument("--reference-seconds", type=float, default=90.0)

@@ -1,0 +1,187 @@
+"""The C-ABI boundary on CPU (no GPU needed): libks builds for sm_103a, loads, exports every
+symbol include/ks.h declares, and rejects invalid calls with the documented status before any
+CUDA call. Only invalid calls are made here: a valid call would launch a kernel.
+
+Also the host-side launch heuristic (after Triton Kernels' CPU tests of its launch-config
+heuristics, "Running the tests"), checked through ks_plan_launch.
+"""
+import os
+import re
+import subprocess
+
+import pytest
+
+from row_wise_rmsnorm_ks_gb300 import _abi
+from row_wise_rmsnorm_ks_gb300 import build as ks_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ks.h")
+
+BF16, F16, F32 = _abi.KS_DTYPE_BF16, _abi.KS_DTYPE_F16, _abi.KS_DTYPE_F32
+FAKE = 0x10000  # a non-NULL address that is never dereferenced (every call below fails first)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    ks_build.build()
+    return _abi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ks_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_exactly_the_binding_surface():
+    assert declared_functions() == sorted(_abi.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", ks_build.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (ks_[a-z0-9_]+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_library_is_built_for_sm103a():
+    with open(os.path.join(ks_build.OUT_DIR, "ptxas_report.txt")) as f:
+        rep = f.read()
+    assert "for 'sm_103a'" in rep
+    assert "rows_vec_kernel" in rep and "rows_scalar_kernel" in rep
+
+
+def test_status_strings():
+    names = ["KS_SUCCESS", "KS_ERR_INVALID_ARGUMENT", "KS_ERR_UNSUPPORTED_DTYPE",
+             "KS_ERR_OVERLAP", "KS_ERR_CUDA"]
+    for code, name in enumerate(names):
+        assert _abi.ks_status_string(code) == name
+    assert _abi.ks_status_string(99) == "KS_UNKNOWN_STATUS"
+    assert _abi.ks_version() >= 100
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_invalid_arguments_rejected_before_any_cuda_call(fused):
+    call = _abi.ks_fused_add_rms_norm if fused else _abi.ks_rms_norm
+    a, b, w = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    assert call(a, b, w, 4, 0, 1e-6, BF16, None) == E            # hidden == 0
+    assert call(a, b, w, 4, -3, 1e-6, BF16, None) == E           # hidden < 0
+    assert call(a, b, w, -1, 64, 1e-6, BF16, None) == E          # rows < 0
+    for eps in (0.0, -1e-6, float("nan"), float("inf")):
+        assert call(a, b, w, 4, 64, eps, BF16, None) == E, eps   # eps not finite and > 0
+    assert call(0, b, w, 4, 64, 1e-6, BF16, None) == E           # NULL with rows > 0
+    assert call(a, 0, w, 4, 64, 1e-6, BF16, None) == E
+    assert call(a, b, 0, 4, 64, 1e-6, BF16, None) == E
+    assert call(a, b, w, 1 << 62, 1 << 20, 1e-6, BF16, None) == E  # byte size overflows
+    assert "eps" in _abi.ks_last_error() or "overflow" in _abi.ks_last_error()
+    assert call(a, b, w, 4, 64, 1e-6, 7, None) == _abi.KS_ERR_UNSUPPORTED_DTYPE
+    assert call(a, b, w, 4, 64, 1e-6, -1, None) == _abi.KS_ERR_UNSUPPORTED_DTYPE
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_empty_input_is_success_without_launch(fused):
+    call = _abi.ks_fused_add_rms_norm if fused else _abi.ks_rms_norm
+    # rows == 0: legal, nothing launched, pointers may be NULL
+    assert call(0, 0, 0, 0, 64, 1e-6, BF16, None) == _abi.KS_SUCCESS
+
+
+def test_overlap_rules_fused():
+    rows, hidden, e = 4, 64, 2
+    n = rows * hidden * e
+    x, w = FAKE, FAKE + 10 * n
+    O = _abi.KS_ERR_OVERLAP
+    assert _abi.ks_fused_add_rms_norm(x, x, w, rows, hidden, 1e-6, BF16, None) == O
+    assert _abi.ks_fused_add_rms_norm(x, x + n - 2, w, rows, hidden, 1e-6, BF16, None) == O
+    assert _abi.ks_fused_add_rms_norm(x, x + 5 * n, x + 2, rows, hidden, 1e-6, BF16, None) == O
+    assert _abi.ks_fused_add_rms_norm(x, x + 5 * n, x + 5 * n + 64, rows, hidden, 1e-6, BF16,
+                                      None) == O
+    assert "overlap" in _abi.ks_last_error()
+
+
+def test_overlap_rules_plain():
+    rows, hidden, e = 4, 64, 2
+    n = rows * hidden * e
+    x, w = FAKE, FAKE + 10 * n
+    O = _abi.KS_ERR_OVERLAP
+    assert _abi.ks_rms_norm(x + 2, x, w, rows, hidden, 1e-6, BF16, None) == O   # partial overlap
+    assert _abi.ks_rms_norm(w - 2, x, w, rows, hidden, 1e-6, BF16, None) == O   # out over weight
+
+
+# -------------------------------------------------------------------------- plan heuristic
+
+def plan(op, rows, hidden, dtype=BF16, aligned=True, sms=152, bps=0):
+    st, p = _abi.ks_plan_launch(op, rows, hidden, dtype, aligned, sms, bps)
+    assert st == _abi.KS_SUCCESS, _abi.ks_last_error()
+    return p
+
+
+@pytest.mark.parametrize("hidden,v", [(256, 1), (512, 2), (1024, 4)])
+def test_narrow_rows_take_warp_per_row(hidden, v):
+    p = plan(0, 32768, hidden)
+    assert p.kernel == _abi.KS_KERNEL_WARP_ROW and p.vec_per_thread == v and p.team == 32
+    assert p.block == 256  # 8 rows per CTA once there are enough rows
+
+
+def test_warp_per_row_spreads_few_rows_over_sms():
+    p = plan(0, 128, 1024)
+    assert p.block == 32 and p.grid == 128  # 128 rows on 128 SMs
+
+
+@pytest.mark.parametrize("hidden,block", [(1536, 64), (4096, 128), (5120, 160), (7168, 224),
+                                          (8192, 256), (14336, 448), (16384, 512)])
+def test_wide_rows_take_cta_per_row(hidden, block):
+    for op in (0, 1):
+        p = plan(op, 32768, hidden)
+        assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == block and p.team == block
+        assert p.vec_per_thread * 8 * p.block >= hidden
+
+
+def test_fp32_counts_four_elements_per_vector():
+    p = plan(0, 10, 4096, dtype=F32)
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 256
+
+
+@pytest.mark.parametrize("hidden,aligned", [(17, True), (1001, True), (4096, False),
+                                            (20000, True), (65536, True)])
+def test_scalar_fallback(hidden, aligned):
+    p = plan(1, 7, hidden, aligned=aligned)
+    assert p.kernel == _abi.KS_KERNEL_SCALAR
+    assert p.block % 32 == 0 and 32 <= p.block <= 1024
+
+
+def test_persistent_grid_is_capped_by_residency():
+    p = plan(0, 32768, 8192, bps=2)
+    assert p.grid == 304 and p.rows_per_pass == 304
+    p = plan(0, 100, 8192, bps=2)
+    assert p.grid == 100
+    p = plan(0, 32768, 1024, bps=3)
+    assert p.grid == 152 * 3 and p.rows_per_pass == 152 * 3 * 8
+
+
+def test_empty_plan_and_bad_arguments():
+    assert plan(0, 0, 64).kernel == _abi.KS_KERNEL_NONE
+    st, _ = _abi.ks_plan_launch(2, 1, 64, BF16, True, 152, 0)
+    assert st == _abi.KS_ERR_INVALID_ARGUMENT
+    st, _ = _abi.ks_plan_launch(0, 1, 0, BF16, True, 152, 0)
+    assert st == _abi.KS_ERR_INVALID_ARGUMENT
+    st, _ = _abi.ks_plan_launch(0, 1, 64, 5, True, 152, 0)
+    assert st == _abi.KS_ERR_UNSUPPORTED_DTYPE
+
+
+@pytest.mark.parametrize("dtype", [BF16, F16, F32])
+def test_plan_invariants_over_a_sweep(dtype):
+    e = 4 if dtype == F32 else 2
+    for hidden in [1, 3, 8, 64, 100, 128, 1000, 1024, 1536, 2048, 3000, 4096, 8192, 12288,
+                   16384, 16392, 32768, 100000]:
+        for rows in [1, 7, 152, 333, 65536]:
+            p = plan(1, rows, hidden, dtype=dtype, bps=2)
+            assert p.block % 32 == 0 and 32 <= p.block <= 1024
+            assert 1 <= p.grid <= max(rows, 1)
+            if p.kernel in (_abi.KS_KERNEL_WARP_ROW, _abi.KS_KERNEL_CTA_ROW):
+                assert hidden * e % 16 == 0
+                assert p.team * p.vec_per_thread * (16 // e) >= hidden
+                if p.kernel == _abi.KS_KERNEL_CTA_ROW:
+                    assert p.block <= 512  # the launch bound of the 4-vector CTA kernel

@@ -1,0 +1,89 @@
+"""Host-side logic of bench.py on CPU: the byte model against the pages' printed figures
+(tests/golden/pages_bandwidth.txt), and the multi-rank path (max over ranks, whole-job
+aggregate, independent per-rank batches) on two gloo ranks."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                      "pages_bandwidth.txt")
+
+
+def golden_rows():
+    out = []
+    for line in open(GOLDEN):
+        if line.startswith("#") or not line.strip():
+            continue
+        f = [c.strip() for c in line.split("|")]
+        out.append(dict(source=f[0], op=f[1], rows=int(f[2]), hidden=int(f[3]), e=int(f[4]),
+                        ms=float(f[5]), digits=int(f[6]), gbs=float(f[7]),
+                        expect=f[8].split()[0]))
+    return out
+
+
+@pytest.mark.parametrize("row", golden_rows(), ids=lambda r: r["source"][:40])
+def test_byte_model_against_printed_figures(row):
+    nbytes = bench.algorithmic_bytes(row["op"], row["rows"], row["hidden"], row["e"])
+    half = 0.5 * 10.0 ** -row["digits"]
+    lo_ms, hi_ms = row["ms"] - half, row["ms"] + half
+    implied_ms = nbytes / (row["gbs"] * 1e9) * 1e3
+    consistent = lo_ms <= implied_ms <= hi_ms
+    assert consistent == (row["expect"] == "consistent"), (implied_ms, lo_ms, hi_ms)
+
+
+def test_byte_model_values():
+    # the large prefill step: 1,073,758,208 B plain, 2,147,500,032 B fused
+    assert bench.algorithmic_bytes("rms_norm", 32768, 8192, 2) == 1073758208
+    assert bench.algorithmic_bytes("fused_add_rms_norm", 32768, 8192, 2) == 2147500032
+    assert bench.algorithmic_bytes("fused_add_rms_norm", 4, 1536, 2) == 52224
+
+
+def test_whole_job_aggregate():
+    assert bench.whole_job_gbs(1, 10 ** 9, 1000, 1000.0) == pytest.approx(1000.0)
+    assert bench.whole_job_gbs(4, 10 ** 9, 1000, 1000.0) == pytest.approx(4000.0)
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        local_ms = 10.0 + 5.0 * rank            # rank 1 is the slower one
+        worst = bench.max_over_ranks(local_ms)
+        seeds = [torch.tensor([bench.rank_seed(1234, rank)]) for _ in range(world)]
+        dist.all_gather(seeds, torch.tensor([bench.rank_seed(1234, rank)]))
+        dist.barrier()
+        q.put((rank, worst, [int(s) for s in seeds]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_max_and_draw_independent_batches():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, worst, seeds in results:
+        assert worst == 15.0
+        assert len(set(seeds)) == world  # every rank draws its own batch
+
+
+def test_single_process_max_is_identity():
+    assert bench.max_over_ranks(3.5) == 3.5
