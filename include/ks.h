@@ -113,18 +113,57 @@ typedef struct ks_plan {
     int32_t block;          /* threads per CTA */
     int64_t grid;           /* CTAs launched */
     int64_t rows_per_pass;  /* rows in flight per pass over the grid (grid * rows per CTA) */
+    int32_t stages;         /* staged kernel: rows in each CTA's shared-memory ring (else 0) */
+    int32_t smem_bytes;     /* staged kernel: dynamic shared memory per CTA (else 0) */
+    int32_t flags;          /* KS_PLAN_* bits below */
+    int32_t reserved;       /* zero */
 } ks_plan_t;
+
+/* Plan flags. KS_PLAN_NO_PREFETCH: the register kernels (warp and CTA rows) load each row when
+ * they reach it instead of loading the next row before reducing the current one (fewer
+ * registers, so more resident CTAs). */
+#define KS_PLAN_NO_PREFETCH 1
 
 enum {
     KS_KERNEL_NONE = 0,     /* rows == 0: nothing is launched */
     KS_KERNEL_WARP_ROW = 1, /* one warp per row, row in registers, 16-byte vectors */
     KS_KERNEL_CTA_ROW = 2,  /* one CTA per row, row in registers, 16-byte vectors */
-    KS_KERNEL_SCALAR = 3    /* one CTA per row, element loads, two passes over the row */
+    KS_KERNEL_SCALAR = 3,   /* one CTA per row, element loads, two passes over the row */
+    KS_KERNEL_BULK_ROW = 4  /* one CTA per row, rows streamed through a shared-memory ring by
+                               bulk asynchronous copies, 4 vectors per thread */
 };
 
 ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t dtype,
                            int32_t aligned16, int32_t sm_count, int32_t blocks_per_sm,
                            ks_plan_t *plan);
+
+/*
+ * The same two operations with an explicit launch plan instead of the built-in heuristic (a
+ * tuning hook: a plan from ks_plan_launch, edited). Semantics, arguments and errors are those of
+ * ks_rms_norm / ks_fused_add_rms_norm, plus KS_ERR_INVALID_ARGUMENT when the plan does not fit
+ * the call: a vector kernel on unaligned pointers or on a width that is not a multiple of 16
+ * bytes, team * vec_per_thread vectors short of the row, a block that is not a multiple of 32 or
+ * exceeds the kernel's bound (warp rows 256, CTA rows 1024 at 2 vectors and 512 at 4, staged
+ * rows 512, scalar 1024), or a staged ring (stages 1..16) over 226 KB of shared memory. grid <= 0
+ * lets the library size the persistent grid; smem_bytes and rows_per_pass are recomputed. The
+ * plan is read, never written.
+ */
+ks_status_t ks_rms_norm_planned(void *out, const void *x, const void *weight, int64_t rows,
+                                int64_t hidden, float eps, ks_dtype_t dtype,
+                                const ks_plan_t *plan, ks_stream_t stream);
+ks_status_t ks_fused_add_rms_norm_planned(void *x, void *residual, const void *weight,
+                                          int64_t rows, int64_t hidden, float eps,
+                                          ks_dtype_t dtype, const ks_plan_t *plan,
+                                          ks_stream_t stream);
+
+/*
+ * Device-side faults of the current device: the OR of the fault words the kernels set (bit 0,
+ * KS_FAULT_WAIT_TIMEOUT: a staged kernel gave up waiting for a bulk copy after about 2 s, left
+ * its row loop and returned; its outputs are then incomplete). Reading synchronises with the
+ * device. clear != 0 zeroes the words after reading. KS_ERR_CUDA if the read fails.
+ */
+#define KS_FAULT_WAIT_TIMEOUT 1
+ks_status_t ks_device_faults(int32_t *flags, int32_t clear);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t ks_version(void);

@@ -15,12 +15,15 @@ LIB_PATH = os.path.join(_HERE, "_build", "libks.so")
 
 KS_DTYPE_F32, KS_DTYPE_F16, KS_DTYPE_BF16 = 0, 1, 2
 KS_SUCCESS, KS_ERR_INVALID_ARGUMENT, KS_ERR_UNSUPPORTED_DTYPE, KS_ERR_OVERLAP, KS_ERR_CUDA = range(5)
-KS_KERNEL_NONE, KS_KERNEL_WARP_ROW, KS_KERNEL_CTA_ROW, KS_KERNEL_SCALAR = range(4)
-KERNEL_NAMES = {0: "none", 1: "warp_row", 2: "cta_row", 3: "scalar"}
+KS_KERNEL_NONE, KS_KERNEL_WARP_ROW, KS_KERNEL_CTA_ROW, KS_KERNEL_SCALAR, KS_KERNEL_BULK_ROW = range(5)
+KERNEL_NAMES = {0: "none", 1: "warp_row", 2: "cta_row", 3: "scalar", 4: "bulk_row"}
+KS_FAULT_WAIT_TIMEOUT = 1
+KS_PLAN_NO_PREFETCH = 1
 
 # Every symbol include/ks.h declares (checked by the CPU test of the boundary).
 EXPORTED = ("ks_rms_norm", "ks_fused_add_rms_norm", "ks_status_string", "ks_last_error",
-            "ks_plan_launch", "ks_version")
+            "ks_plan_launch", "ks_rms_norm_planned", "ks_fused_add_rms_norm_planned",
+            "ks_device_faults", "ks_version")
 
 
 class KsLibraryMissing(RuntimeError):
@@ -38,7 +41,9 @@ class KsError(RuntimeError):
 class ks_plan_t(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("vec_per_thread", ctypes.c_int32),
                 ("team", ctypes.c_int32), ("block", ctypes.c_int32), ("grid", ctypes.c_int64),
-                ("rows_per_pass", ctypes.c_int64)]
+                ("rows_per_pass", ctypes.c_int64), ("stages", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {f: getattr(self, f) for f, _ in self._fields_}
@@ -74,6 +79,14 @@ def load(path: str | None = None):
         lib.ks_plan_launch.argtypes = [i32, i64, i64, ctypes.c_int, i32, i32, i32,
                                        ctypes.POINTER(ks_plan_t)]
         lib.ks_plan_launch.restype = ctypes.c_int
+        PP = ctypes.POINTER(ks_plan_t)
+        lib.ks_rms_norm_planned.argtypes = [vp, vp, vp, i64, i64, f32, ctypes.c_int, PP, vp]
+        lib.ks_rms_norm_planned.restype = ctypes.c_int
+        lib.ks_fused_add_rms_norm_planned.argtypes = [vp, vp, vp, i64, i64, f32, ctypes.c_int,
+                                                      PP, vp]
+        lib.ks_fused_add_rms_norm_planned.restype = ctypes.c_int
+        lib.ks_device_faults.argtypes = [ctypes.POINTER(i32), i32]
+        lib.ks_device_faults.restype = ctypes.c_int
         lib.ks_version.argtypes = []
         lib.ks_version.restype = i32
         _lib = lib
@@ -104,6 +117,35 @@ def ks_plan_launch(op: int, rows: int, hidden: int, dtype: int, aligned16: bool,
     st = load().ks_plan_launch(op, rows, hidden, dtype, int(bool(aligned16)), sm_count,
                                blocks_per_sm, ctypes.byref(plan))
     return st, plan
+
+
+def make_plan(kernel: int, vec_per_thread: int, block: int, stages: int = 0,
+              grid: int = 0, flags: int = 0) -> ks_plan_t:
+    """A plan for the *_planned entry points (derived fields are recomputed by the library)."""
+    p = ks_plan_t()
+    p.kernel, p.vec_per_thread, p.block, p.stages, p.grid, p.flags = (
+        kernel, vec_per_thread, block, stages, grid, flags)
+    return p
+
+
+def ks_rms_norm_planned(out: int, x: int, weight: int, rows: int, hidden: int, eps: float,
+                        dtype: int, plan: ks_plan_t, stream: int | None) -> int:
+    return load().ks_rms_norm_planned(out, x, weight, rows, hidden, eps, dtype,
+                                      ctypes.byref(plan), stream)
+
+
+def ks_fused_add_rms_norm_planned(x: int, residual: int, weight: int, rows: int, hidden: int,
+                                  eps: float, dtype: int, plan: ks_plan_t,
+                                  stream: int | None) -> int:
+    return load().ks_fused_add_rms_norm_planned(x, residual, weight, rows, hidden, eps, dtype,
+                                                ctypes.byref(plan), stream)
+
+
+def ks_device_faults(clear: bool = True) -> tuple[int, int]:
+    """(status, flags): the device fault words of the current device, OR-ed."""
+    flags = ctypes.c_int32(0)
+    st = load().ks_device_faults(ctypes.byref(flags), int(bool(clear)))
+    return st, flags.value
 
 
 def ks_version() -> int:

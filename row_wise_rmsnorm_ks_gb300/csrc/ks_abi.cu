@@ -62,8 +62,67 @@ std::mutex g_occ_mu;
 std::unordered_map<uint64_t, int> g_occ;  // (device, dtype, fused, kernel, vec, block) -> CTAs/SM
 
 uint64_t occ_key(int dev, ks_dtype_t d, bool fused, const ks_plan_t &p) {
-    return ((uint64_t)dev << 48) | ((uint64_t)d << 44) | ((uint64_t)fused << 43) |
-           ((uint64_t)p.kernel << 36) | ((uint64_t)p.vec_per_thread << 24) | (uint64_t)p.block;
+    return ((uint64_t)dev << 52) | ((uint64_t)d << 48) | ((uint64_t)fused << 47) |
+           ((uint64_t)p.kernel << 40) | ((uint64_t)p.vec_per_thread << 32) |
+           ((uint64_t)(p.flags & 0xFF) << 24) | ((uint64_t)p.stages << 16) | (uint64_t)p.block;
+}
+
+constexpr int kSmemLimit = 226 * 1024;  // dynamic ring; static smem and reserve fit in 227 KB
+constexpr int kRingHeader = 128;  // the staged kernel's mbarriers, ahead of its ring
+
+// Checks that a plan fits the call (see ks_rms_norm_planned) and fills the derived fields.
+ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, int e,
+                       bool aligned16) {
+    const int per_vec = 16 / e;
+    const bool vec_ok = aligned16 && hidden % per_vec == 0;
+    const int64_t hv = vec_ok ? hidden / per_vec : 0;
+    if (p.block < 32 || p.block % 32 != 0)
+        return fail(KS_ERR_INVALID_ARGUMENT, "plan block %d is not a positive multiple of 32", p.block);
+    p.stages = p.kernel == KS_KERNEL_BULK_ROW ? p.stages : 0;
+    p.smem_bytes = 0;
+    p.reserved = 0;
+    if (p.flags & ~KS_PLAN_NO_PREFETCH)
+        return fail(KS_ERR_INVALID_ARGUMENT, "unknown plan flags 0x%x", (unsigned)p.flags);
+    int64_t rows_per_cta = 1;
+    switch (p.kernel) {
+    case KS_KERNEL_WARP_ROW:
+        if (!vec_ok) return fail(KS_ERR_INVALID_ARGUMENT, "vector kernel needs 16-byte rows and pointers");
+        if (p.vec_per_thread != 1 && p.vec_per_thread != 2 && p.vec_per_thread != 4)
+            return fail(KS_ERR_INVALID_ARGUMENT, "warp-row kernel takes 1, 2 or 4 vectors");
+        if (32LL * p.vec_per_thread < hv || p.block > 256)
+            return fail(KS_ERR_INVALID_ARGUMENT, "warp-row plan does not cover the row or block > 256");
+        p.team = 32;
+        rows_per_cta = p.block / 32;
+        break;
+    case KS_KERNEL_CTA_ROW:
+    case KS_KERNEL_BULK_ROW: {
+        if (!vec_ok) return fail(KS_ERR_INVALID_ARGUMENT, "vector kernel needs 16-byte rows and pointers");
+        const bool bulk = p.kernel == KS_KERNEL_BULK_ROW;
+        if (bulk ? p.vec_per_thread != 4 : (p.vec_per_thread != 2 && p.vec_per_thread != 4))
+            return fail(KS_ERR_INVALID_ARGUMENT, "unsupported vectors per thread %d", p.vec_per_thread);
+        const int bound = bulk ? 512 : (p.vec_per_thread == 2 ? 1024 : 512);
+        if ((int64_t)p.block * p.vec_per_thread < hv || p.block > bound)
+            return fail(KS_ERR_INVALID_ARGUMENT, "CTA-row plan does not cover the row or block > %d", bound);
+        p.team = p.block;
+        if (bulk) {
+            const int64_t stage = hv * 16 * (fused ? 2 : 1);
+            if (p.stages < 1 || p.stages > 16 || kRingHeader + stage * p.stages > kSmemLimit)
+                return fail(KS_ERR_INVALID_ARGUMENT, "staged ring of %d stages does not fit", p.stages);
+            p.smem_bytes = (int32_t)(kRingHeader + stage * p.stages);
+        }
+        break;
+    }
+    case KS_KERNEL_SCALAR:
+        if (p.block > 1024) return fail(KS_ERR_INVALID_ARGUMENT, "scalar block > 1024");
+        p.vec_per_thread = 0;
+        p.team = p.block;
+        break;
+    default:
+        return fail(KS_ERR_INVALID_ARGUMENT, "unknown kernel %d", p.kernel);
+    }
+    p.rows_per_pass = rows_per_cta;  // per CTA here; scaled by the grid once it is known
+    (void)rows;
+    return KS_SUCCESS;
 }
 
 int query_blocks_per_sm(ks_dtype_t d, const ks_plan_t &p, bool fused) {
@@ -75,7 +134,8 @@ int query_blocks_per_sm(ks_dtype_t d, const ks_plan_t &p, bool fused) {
 }
 
 ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, int64_t rows,
-                int64_t hidden, float eps, ks_dtype_t dtype, ks_stream_t stream) {
+                int64_t hidden, float eps, ks_dtype_t dtype, ks_stream_t stream,
+                const ks_plan_t *forced) {
     // ---- argument checks: no CUDA call before all of them pass
     const int e = elem_bytes(dtype);
     if (e == 0) return fail(KS_ERR_UNSUPPORTED_DTYPE, "dtype code %d is not a ks_dtype_t", (int)dtype);
@@ -102,6 +162,16 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         if (overlaps(out, nbytes, w, wbytes)) return fail(KS_ERR_OVERLAP, "out and weight storage overlap");
     }
 
+    const uintptr_t align = (uintptr_t)out | (uintptr_t)x | (uintptr_t)w | (fused ? (uintptr_t)res : 0);
+    const bool aligned16 = (align & 15u) == 0;
+    ks_plan_t p;
+    ks_status_t st;
+    if (forced) {  // an explicit plan is an argument too: checked before any CUDA call
+        p = *forced;
+        st = check_plan(p, fused, rows, hidden, e, aligned16);
+        if (st != KS_SUCCESS) return st;
+    }
+
     // ---- device facts (cached per device)
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
@@ -113,12 +183,10 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
     });
     if (slot.err != cudaSuccess)
         return fail(KS_ERR_CUDA, "querying the SM count: %s", cudaGetErrorString(slot.err));
-
-    const uintptr_t align = (uintptr_t)out | (uintptr_t)x | (uintptr_t)w | (fused ? (uintptr_t)res : 0);
-    const bool aligned16 = (align & 15u) == 0;
-    ks_plan_t p;
-    ks_status_t st = plan(fused ? 1 : 0, rows, hidden, e, aligned16, slot.sm_count, 0, &p);
-    if (st != KS_SUCCESS) return st;
+    if (!forced) {
+        st = plan(fused ? 1 : 0, rows, hidden, e, aligned16, slot.sm_count, 0, &p);
+        if (st != KS_SUCCESS) return st;
+    }
 
     int bps;
     {
@@ -133,8 +201,16 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         }
     }
     if (bps <= 0) return fail(KS_ERR_CUDA, "kernel %d (block %d) cannot be resident", p.kernel, p.block);
-    st = plan(fused ? 1 : 0, rows, hidden, e, aligned16, slot.sm_count, bps, &p);
-    if (st != KS_SUCCESS) return st;
+    if (forced) {
+        const int64_t per_cta = p.rows_per_pass;
+        const int64_t ctas = ceil_div(rows, per_cta);
+        const int64_t cap = (int64_t)slot.sm_count * bps;
+        p.grid = forced->grid > 0 ? (forced->grid < ctas ? forced->grid : ctas) : (ctas < cap ? ctas : cap);
+        p.rows_per_pass = p.grid * per_cta;
+    } else {
+        st = plan(fused ? 1 : 0, rows, hidden, e, aligned16, slot.sm_count, bps, &p);
+        if (st != KS_SUCCESS) return st;
+    }
 
     RowArgs a;
     a.out = fused ? const_cast<void *>(x) : out;
@@ -145,6 +221,7 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
     a.hidden = hidden;
     a.hv = (p.kernel == KS_KERNEL_SCALAR) ? 0 : hidden / (16 / e);
     a.eps = eps;
+    a.stages = p.stages;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (dtype) {
     case KS_DTYPE_BF16: ce = launch_bf16(p, fused, a, s); break;
@@ -158,12 +235,17 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 }  // namespace
 
 // Host heuristic (after the pages' rule of sizing the launch from the row width: Triton
-// Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"):
-//  * rows of at most 128 16-byte vectors (bf16/fp16 H <= 1024, fp32 H <= 512): one warp per row,
-//    1/2/4 vectors per lane, up to 8 rows per CTA but never fewer CTAs than SMs when the rows
-//    allow it;
+// Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"), set from a sweep of
+// every variant on GB300 over widths 512..16384 at HBM-bound row counts:
+//  * rows of at most 128 16-byte vectors (bf16/fp16 H <= 1024, fp32 H <= 512): one warp per
+//    row, 1/2/4 vectors per lane, next row prefetched, up to 8 rows per CTA but never fewer CTAs
+//    than SMs when the rows allow it;
 //  * rows of up to 2048 vectors (bf16/fp16 H <= 16384, fp32 H <= 8192): one CTA per row, 4
-//    vectors per thread, the CTA as wide as the row needs (a multiple of 32 threads);
+//    vectors per thread, the CTA as wide as the row needs (a multiple of 32 threads). The fused
+//    op prefetches the next row (two tensors in flight per row hide the barrier); the plain op
+//    does not, which lowers its registers enough to keep more CTAs resident. Plain rows wider
+//    than 1536 vectors stream through the staged shared-memory ring instead, when there are
+//    enough rows to fill it;
 //  * anything else (H not a multiple of the vector, unaligned pointers, wider rows): the scalar
 //    two-pass kernel.
 // The grid is persistent: at most sm_count * blocks_per_sm CTAs.
@@ -192,10 +274,20 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem, bool aligned16,
         rows_per_cta = teams;
         p->block = (int32_t)(32 * teams);
     } else if (vec_ok && hv <= 2048) {
-        p->kernel = KS_KERNEL_CTA_ROW;
         p->vec_per_thread = 4;
         p->block = (int32_t)round_up(ceil_div(hv, 4), 32);
         p->team = p->block;
+        p->kernel = KS_KERNEL_CTA_ROW;
+        if (op == 0) p->flags = KS_PLAN_NO_PREFETCH;
+        const int64_t stage = hv * 16;
+        if (op == 0 && hv > 1536 && rows >= 4 * (int64_t)sm_count) {
+            int64_t st = (96 * 1024) / stage;
+            st = st < 2 ? 2 : (st > 8 ? 8 : st);
+            p->kernel = KS_KERNEL_BULK_ROW;
+            p->flags = 0;
+            p->stages = (int32_t)st;
+            p->smem_bytes = (int32_t)(kRingHeader + st * stage);
+        }
     } else {
         p->kernel = KS_KERNEL_SCALAR;
         int64_t b = round_up(ceil_div(hidden, 8), 32);
@@ -215,13 +307,40 @@ extern "C" {
 
 ks_status_t ks_rms_norm(void *out, const void *x, const void *weight, int64_t rows,
                         int64_t hidden, float eps, ks_dtype_t dtype, ks_stream_t stream) {
-    return ks::run(false, out, x, nullptr, weight, rows, hidden, eps, dtype, stream);
+    return ks::run(false, out, x, nullptr, weight, rows, hidden, eps, dtype, stream, nullptr);
 }
 
 ks_status_t ks_fused_add_rms_norm(void *x, void *residual, const void *weight, int64_t rows,
                                   int64_t hidden, float eps, ks_dtype_t dtype,
                                   ks_stream_t stream) {
-    return ks::run(true, x, x, residual, weight, rows, hidden, eps, dtype, stream);
+    return ks::run(true, x, x, residual, weight, rows, hidden, eps, dtype, stream, nullptr);
+}
+
+ks_status_t ks_rms_norm_planned(void *out, const void *x, const void *weight, int64_t rows,
+                                int64_t hidden, float eps, ks_dtype_t dtype,
+                                const ks_plan_t *plan, ks_stream_t stream) {
+    if (!plan) return ks::fail(KS_ERR_INVALID_ARGUMENT, "plan is NULL");
+    return ks::run(false, out, x, nullptr, weight, rows, hidden, eps, dtype, stream, plan);
+}
+
+ks_status_t ks_fused_add_rms_norm_planned(void *x, void *residual, const void *weight,
+                                          int64_t rows, int64_t hidden, float eps,
+                                          ks_dtype_t dtype, const ks_plan_t *plan,
+                                          ks_stream_t stream) {
+    if (!plan) return ks::fail(KS_ERR_INVALID_ARGUMENT, "plan is NULL");
+    return ks::run(true, x, x, residual, weight, rows, hidden, eps, dtype, stream, plan);
+}
+
+ks_status_t ks_device_faults(int32_t *flags, int32_t clear) {
+    if (!flags) return ks::fail(KS_ERR_INVALID_ARGUMENT, "flags is NULL");
+    *flags = 0;
+    const int parts[3] = {ks::fault_flags_bf16(clear != 0), ks::fault_flags_f16(clear != 0),
+                          ks::fault_flags_f32(clear != 0)};
+    for (int v : parts) {
+        if (v < 0) return ks::fail(KS_ERR_CUDA, "reading the device fault words failed");
+        *flags |= v;
+    }
+    return KS_SUCCESS;
 }
 
 const char *ks_status_string(ks_status_t status) {

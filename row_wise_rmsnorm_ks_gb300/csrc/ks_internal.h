@@ -18,6 +18,7 @@ struct RowArgs {
     int64_t hidden;     // H, the real row width (the divisor of the mean)
     int64_t hv;         // H / elements-per-16-byte-vector (vector kernels)
     float eps;
+    int32_t stages;     // staged kernel: rows in the shared-memory ring
 };
 
 // Host heuristic: fills *p from the shape, the element size and the device's SM count.
@@ -30,6 +31,11 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem_bytes, bool alig
 int blocks_per_sm_bf16(const ks_plan_t &p, bool fused);
 int blocks_per_sm_f16(const ks_plan_t &p, bool fused);
 int blocks_per_sm_f32(const ks_plan_t &p, bool fused);
+// Reads (and with `clear`, zeroes) the device fault word of each translation unit's kernels on
+// the current device; returns the OR of them, or -1 if the read failed.
+int fault_flags_bf16(bool clear);
+int fault_flags_f16(bool clear);
+int fault_flags_f32(bool clear);
 cudaError_t launch_bf16(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);
 cudaError_t launch_f16(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);
 cudaError_t launch_f32(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);

@@ -13,6 +13,9 @@
 // streaming stores; the weight slice a thread needs is loaded once and kept in registers for
 // every row it touches; the grid is persistent and each team loads its next row before it
 // reduces the current one, so a row's loads are in flight during the previous row's reduction.
+// The staged kernel instead streams whole rows into a ring of shared-memory stages with bulk
+// asynchronous copies (one issuing thread, an mbarrier per stage), so several rows per CTA are in
+// flight without spending registers on them.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -21,6 +24,7 @@
 #include <string.h>
 
 #include "ks_internal.h"
+#include "ks_ptx.cuh"
 
 namespace ks {
 
@@ -139,6 +143,20 @@ __device__ __forceinline__ float row_scale(float ss, float h, float eps) {
     return __frsqrt_rn(__fadd_rn(__fdiv_rn(ss, h), eps));
 }
 
+// Four independent FMA chains per thread (element e feeds chain e % 4), added pairwise at the end:
+// a single chain would serialise on the FMA latency.
+struct SumSq {
+    float a[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    template <int N>
+    __device__ __forceinline__ void add(const float (&f)[N]) {
+#pragma unroll
+        for (int e = 0; e < N; ++e) a[e & 3] = __fmaf_rn(f[e], f[e], a[e & 3]);
+    }
+    __device__ __forceinline__ float total() const {
+        return __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
+    }
+};
+
 // --------------------------------------------------------------- vectorised row kernel
 
 // Register budget per thread grows with V (current + prefetched rows, weight slice); the
@@ -162,7 +180,14 @@ __device__ __forceinline__ void load_row(const uint4 *base, int t, int g, int64_
 // One team (a warp, or the whole CTA) per row; row r's 16-byte vector c (of hv) is handled by
 // thread c % G of the team, as its (c / G)-th vector. Teams stride over rows by the number of
 // teams in the grid.
-template <typename T, int V, bool kFused, bool kWarpTeam>
+// Hides a register's value from the optimiser, so values derived from it before this point are
+// not reused after it (the second pass unpacks the raw 16-bit vectors again instead of keeping
+// 8 floats per vector live across the row's reduction).
+__device__ __forceinline__ void opaque(uint4 &v) {
+    asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
+}
+
+template <typename T, int V, bool kFused, bool kWarpTeam, bool kPrefetch>
 __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
     rows_vec_kernel(const RowArgs a) {
     using E = Elem<T>;
@@ -193,7 +218,7 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
     int64_t row = (int64_t)blockIdx.x * teams + team;
     const int64_t stride = (int64_t)gridDim.x * teams;
     uint4 xc[V], rc[V];
-    if (row < a.rows) {
+    if (kPrefetch && row < a.rows) {
         load_row<V>(xg + row * hv, t, g, hv, xc);
         if (kFused) load_row<V>(rg + row * hv, t, g, hv, rc);
     }
@@ -203,13 +228,16 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
         uint4 xn[V], rn[V];
 #pragma unroll
         for (int k = 0; k < V; ++k) xn[k] = rn[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (next < a.rows) {
+        if (!kPrefetch) {
+            load_row<V>(xg + row * hv, t, g, hv, xc);
+            if (kFused) load_row<V>(rg + row * hv, t, g, hv, rc);
+        } else if (next < a.rows) {
             load_row<V>(xg + next * hv, t, g, hv, xn);
             if (kFused) load_row<V>(rg + next * hv, t, g, hv, rn);
         }
 
         // Sum of squares; the fused op also forms s and stores cast(s) into the residual.
-        float ss = 0.0f;
+        SumSq acc;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
@@ -223,15 +251,22 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
                     for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
                     __stcs(rg + row * hv + c, E::pack(f));
                 }
-#pragma unroll
-                for (int e = 0; e < N; ++e) ss = __fmaf_rn(f[e], f[e], ss);
+                acc.add(f);
             }
         }
-        ss = team_sum<kWarpTeam>(ss, red[parity]);
+        const float ss = team_sum<kWarpTeam>(acc.total(), red[parity]);
         parity ^= 1;
         const float scale = row_scale(ss, h, a.eps);
 
         // Normalise, weight, cast, store.
+        if (!kPrefetch) {  // measured: helps without prefetch, costs with it
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                opaque(xc[k]);
+                if (kFused) opaque(rc[k]);
+                opaque(wv[k]);
+            }
+        }
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
@@ -252,10 +287,12 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
         }
 
         row = next;
+        if (kPrefetch) {
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            xc[k] = xn[k];
-            rc[k] = rn[k];
+            for (int k = 0; k < V; ++k) {
+                xc[k] = xn[k];
+                rc[k] = rn[k];
+            }
         }
     }
 }
@@ -274,13 +311,24 @@ __global__ void __launch_bounds__(1024) rows_scalar_kernel(const RowArgs a) {
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const int64_t base = row * H;
-        float ss = 0.0f;
-        for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
-            float v = E::load1(a.x, base + j);
-            if (kFused) v = __fadd_rn(v, E::load1(a.res, base + j));
-            ss = __fmaf_rn(v, v, ss);
+        SumSq acc;
+        int64_t j = threadIdx.x;
+        for (; j + 3 * (int64_t)blockDim.x < H; j += 4 * (int64_t)blockDim.x) {
+            float v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t jj = j + u * (int64_t)blockDim.x;
+                v[u] = E::load1(a.x, base + jj);
+                if (kFused) v[u] = __fadd_rn(v[u], E::load1(a.res, base + jj));
+            }
+            acc.add(v);
         }
-        ss = team_sum<false>(ss, red[parity]);
+        for (; j < H; j += blockDim.x) {
+            float v[1] = {E::load1(a.x, base + j)};
+            if (kFused) v[0] = __fadd_rn(v[0], E::load1(a.res, base + j));
+            acc.add(v);
+        }
+        const float ss = team_sum<false>(acc.total(), red[parity]);
         parity ^= 1;
         const float scale = row_scale(ss, h, a.eps);
         for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
@@ -294,37 +342,240 @@ __global__ void __launch_bounds__(1024) rows_scalar_kernel(const RowArgs a) {
     }
 }
 
+
+// ------------------------------------------------------------------- staged row kernel
+
+// One CTA per row (team = the CTA, V vectors per thread, as in the CTA-team vector kernel), but
+// rows arrive through a ring of `a.stages` shared-memory stages. Thread 0 issues one bulk copy per
+// row and tensor (L2 evict-first) and arms the stage's mbarrier with the byte count; every thread
+// waits on the barrier, copies its vectors to registers, and computes as before. The row's
+// barrier in the CTA reduction is also the point after which the stage is free, so thread 0
+// refills it with the row `stages` iterations ahead right after that barrier.
+// Shared memory: 128 bytes of barriers, then stages x (1 or 2) x H*e bytes.
+// Every wait is bounded: on a time-out the CTA records kFaultWaitTimeout, waits (bounded) for the
+// copies it still has in flight, and returns.
+template <typename T, int V, bool kFused>
+__global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[2][32];
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *ring = smem + 128;
+    const int g = blockDim.x;
+    const int t = threadIdx.x;
+    const int64_t hv = a.hv;
+    const int stages = a.stages;
+    const uint32_t row_bytes = (uint32_t)(hv * 16);
+    const uint32_t stage_bytes = kFused ? 2u * row_bytes : row_bytes;
+    const float h = (float)a.hidden;
+    const int64_t step = gridDim.x;
+
+    const uint4 *xg = static_cast<const uint4 *>(a.x);
+    uint4 *og = static_cast<uint4 *>(a.out);
+    uint4 *rg = static_cast<uint4 *>(a.res);
+
+    uint4 wv[V];
+    {
+        const uint4 *wg = static_cast<const uint4 *>(a.w);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            wv[k] = (c < hv) ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
+    uint64_t policy = 0;
+    if (t == 0) {
+        for (int s = 0; s < stages; ++s) mbar_init(&bars[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int s, int64_t row) {
+        unsigned char *dst = ring + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&bars[s], stage_bytes);
+        bulk_g2s(dst, xg + row * hv, row_bytes, &bars[s], policy);
+        if (kFused) bulk_g2s(dst + row_bytes, rg + row * hv, row_bytes, &bars[s], policy);
+    };
+    if (t == 0) {
+        policy = l2_evict_first_policy();
+        for (int s = 0; s < stages; ++s) {
+            const int64_t row = blockIdx.x + (int64_t)s * step;
+            if (row >= a.rows) break;
+            issue(s, row);
+        }
+    }
+
+    int s = 0;
+    uint32_t phase = 0;
+    int parity = 0;
+    int64_t row = blockIdx.x;
+    bool fault = false;
+    for (; row < a.rows; row += step) {
+        const bool ok = mbar_wait_bounded(&bars[s], phase);
+        const unsigned char *sx = ring + (size_t)s * stage_bytes;
+        uint4 xv[V], rv[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            const bool in = ok && c < hv;
+            xv[k] = in ? ld_shared_v4(sx + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+            if (kFused) rv[k] = in ? ld_shared_v4(sx + row_bytes + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+        }
+
+        SumSq acc;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (ok && c < hv) {
+                float f[N];
+                E::unpack(xv[k], f);
+                if (kFused) {
+                    float q[N];
+                    E::unpack(rv[k], q);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
+                    __stcs(rg + row * hv + c, E::pack(f));
+                }
+                acc.add(f);
+            }
+        }
+        const float part = warp_sum(acc.total());
+        if ((t & 31) == 0) red[parity][t >> 5] = part;
+        // The CTA barrier of this row: partial sums are visible, every thread has its stage data
+        // in registers (so the stage may be refilled), and a time-out anywhere is seen by all.
+        if (__syncthreads_or(!ok)) {
+            fault = true;
+            break;
+        }
+        if (t == 0) {
+            const int64_t ahead = row + (int64_t)stages * step;
+            if (ahead < a.rows) issue(s, ahead);
+        }
+        float ss = 0.0f;
+        const int nw = g >> 5;
+        for (int i = 0; i < nw; ++i) ss += red[parity][i];
+        parity ^= 1;
+        const float scale = row_scale(ss, h, a.eps);
+
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            opaque(xv[k]);
+            if (kFused) opaque(rv[k]);
+            opaque(wv[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < hv) {
+                float f[N], wf[N];
+                E::unpack(xv[k], f);
+                if (kFused) {
+                    float q[N];
+                    E::unpack(rv[k], q);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
+                }
+                E::unpack(wv[k], wf);
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
+                __stcs(og + row * hv + c, E::pack(f));
+            }
+        }
+        if (++s == stages) {
+            s = 0;
+            phase ^= 1u;
+        }
+    }
+    if (fault && t == 0) {
+        atomicOr(&g_fault_flags, kFaultWaitTimeout);
+        // Drain what this CTA issued and did not consume: the rows from `row` up to `stages`
+        // iterations ahead, stage s onwards, before the CTA's shared memory is released.
+        for (int i = 0; i < stages; ++i) {
+            if (row + (int64_t)i * step >= a.rows) break;
+            mbar_wait_bounded(&bars[s], phase);
+            if (++s == stages) {
+                s = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
 // ----------------------------------------------------------------------- kernel selection
 
 template <typename T, bool kFused>
 const void *pick_kernel(const ks_plan_t &p) {
     switch (p.kernel) {
-    case KS_KERNEL_WARP_ROW:
+    case KS_KERNEL_WARP_ROW: {
+        const bool pf = !(p.flags & KS_PLAN_NO_PREFETCH);
         switch (p.vec_per_thread) {
-        case 1: return (const void *)rows_vec_kernel<T, 1, kFused, true>;
-        case 2: return (const void *)rows_vec_kernel<T, 2, kFused, true>;
-        case 4: return (const void *)rows_vec_kernel<T, 4, kFused, true>;
+        case 1: return pf ? (const void *)rows_vec_kernel<T, 1, kFused, true, true>
+                          : (const void *)rows_vec_kernel<T, 1, kFused, true, false>;
+        case 2: return pf ? (const void *)rows_vec_kernel<T, 2, kFused, true, true>
+                          : (const void *)rows_vec_kernel<T, 2, kFused, true, false>;
+        case 4: return pf ? (const void *)rows_vec_kernel<T, 4, kFused, true, true>
+                          : (const void *)rows_vec_kernel<T, 4, kFused, true, false>;
         default: return nullptr;
         }
-    case KS_KERNEL_CTA_ROW:
+    }
+    case KS_KERNEL_CTA_ROW: {
+        const bool pf = !(p.flags & KS_PLAN_NO_PREFETCH);
         switch (p.vec_per_thread) {
-        case 2: return (const void *)rows_vec_kernel<T, 2, kFused, false>;
-        case 4: return (const void *)rows_vec_kernel<T, 4, kFused, false>;
+        case 2: return pf ? (const void *)rows_vec_kernel<T, 2, kFused, false, true>
+                          : (const void *)rows_vec_kernel<T, 2, kFused, false, false>;
+        case 4: return pf ? (const void *)rows_vec_kernel<T, 4, kFused, false, true>
+                          : (const void *)rows_vec_kernel<T, 4, kFused, false, false>;
         default: return nullptr;
         }
+    }
     case KS_KERNEL_SCALAR: return (const void *)rows_scalar_kernel<T, kFused>;
+    case KS_KERNEL_BULK_ROW:
+        return p.vec_per_thread == 4 ? (const void *)rows_bulk_kernel<T, 4, kFused> : nullptr;
     default: return nullptr;
     }
+}
+
+// Dynamic shared memory of a launch (the staged kernel's barriers and ring; 0 otherwise).
+inline size_t dynamic_smem(const ks_plan_t &p) {
+    return p.kernel == KS_KERNEL_BULK_ROW ? (size_t)p.smem_bytes : 0;
 }
 
 template <typename T>
 int blocks_per_sm_t(const ks_plan_t &p, bool fused) {
     const void *f = fused ? pick_kernel<T, true>(p) : pick_kernel<T, false>(p);
     if (!f) return -1;
+    if (p.kernel == KS_KERNEL_BULK_ROW) {
+        // Allow the largest ring the device takes next to the kernel's static shared memory.
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaFuncGetAttributes(&fa, f) != cudaSuccess)
+            return -1;
+        const int max_dynamic = optin - (int)fa.sharedSizeBytes;
+        if (p.smem_bytes > max_dynamic ||
+            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic) !=
+                cudaSuccess)
+            return -1;
+    }
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, p.block, 0) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, p.block, dynamic_smem(p)) !=
+        cudaSuccess)
         return -1;
     return n;
+}
+
+inline int fault_flags_t(bool clear) {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_fault_flags, sizeof v) != cudaSuccess) return -1;
+    if (clear && v != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(g_fault_flags, &zero, sizeof zero) != cudaSuccess) return -1;
+    }
+    return (int)v;
 }
 
 template <typename T>
@@ -333,7 +584,8 @@ cudaError_t launch_t(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStrea
     if (!f) return cudaErrorInvalidConfiguration;
     RowArgs copy = a;
     void *args[] = {&copy};
-    return cudaLaunchKernel(f, dim3((unsigned)p.grid), dim3((unsigned)p.block), args, 0, s);
+    return cudaLaunchKernel(f, dim3((unsigned)p.grid), dim3((unsigned)p.block), args,
+                            dynamic_smem(p), s);
 }
 
 }  // namespace ks
@@ -348,4 +600,5 @@ cudaError_t launch_t(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStrea
                                 cudaStream_t s) {                                             \
         return launch_t<TYPE>(p, fused, a, s);                                                \
     }                                                                                         \
+    int fault_flags_##SUFFIX(bool clear) { return fault_flags_t(clear); }                     \
     }

@@ -133,14 +133,27 @@ def test_warp_per_row_spreads_few_rows_over_sms():
 @pytest.mark.parametrize("hidden,block", [(1536, 64), (4096, 128), (5120, 160), (7168, 224),
                                           (8192, 256), (14336, 448), (16384, 512)])
 def test_wide_rows_take_cta_per_row(hidden, block):
-    for op in (0, 1):
-        p = plan(op, 32768, hidden)
-        assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == block and p.team == block
-        assert p.vec_per_thread * 8 * p.block >= hidden
+    # fused: registers, next row prefetched
+    p = plan(1, 32768, hidden)
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == block and p.team == block
+    assert p.vec_per_thread * 8 * p.block >= hidden and p.stages == 0 and p.flags == 0
+    # plain: registers without prefetch, or the staged ring for the widest rows with many rows
+    p = plan(0, 32768, hidden)
+    assert p.block == block and p.team == block
+    if hidden > 1536 * 8:
+        assert p.kernel == _abi.KS_KERNEL_BULK_ROW and p.flags == 0
+        assert 2 <= p.stages <= 8 and p.smem_bytes == 128 + p.stages * hidden * 2
+        assert p.smem_bytes <= 226 * 1024
+    else:
+        assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.flags == _abi.KS_PLAN_NO_PREFETCH
+    # few rows: never the staged ring
+    assert plan(0, 100, hidden).kernel == _abi.KS_KERNEL_CTA_ROW
 
 
 def test_fp32_counts_four_elements_per_vector():
     p = plan(0, 10, 4096, dtype=F32)
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 256
+    p = plan(1, 1000, 4096, dtype=F32)
     assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 256
 
 
@@ -180,8 +193,37 @@ def test_plan_invariants_over_a_sweep(dtype):
             p = plan(1, rows, hidden, dtype=dtype, bps=2)
             assert p.block % 32 == 0 and 32 <= p.block <= 1024
             assert 1 <= p.grid <= max(rows, 1)
-            if p.kernel in (_abi.KS_KERNEL_WARP_ROW, _abi.KS_KERNEL_CTA_ROW):
+            if p.kernel in (_abi.KS_KERNEL_WARP_ROW, _abi.KS_KERNEL_CTA_ROW,
+                            _abi.KS_KERNEL_BULK_ROW):
                 assert hidden * e % 16 == 0
                 assert p.team * p.vec_per_thread * (16 // e) >= hidden
-                if p.kernel == _abi.KS_KERNEL_CTA_ROW:
-                    assert p.block <= 512  # the launch bound of the 4-vector CTA kernel
+                if p.kernel != _abi.KS_KERNEL_WARP_ROW:
+                    assert p.block <= 512  # the launch bound of the 4-vector CTA kernels
+                if p.kernel == _abi.KS_KERNEL_BULK_ROW:
+                    assert p.smem_bytes <= 226 * 1024 and p.stages >= 2
+
+
+def test_planned_entry_points_reject_plans_that_do_not_fit():
+    """Explicit plans are arguments: checked before any CUDA call."""
+    a, b, w = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    mk = _abi.make_plan
+    bad = [
+        mk(_abi.KS_KERNEL_CTA_ROW, 4, 96),          # 96 threads x 4 vectors < 1024 vectors
+        mk(_abi.KS_KERNEL_CTA_ROW, 4, 1024),        # over the 512-thread bound at 4 vectors
+        mk(_abi.KS_KERNEL_CTA_ROW, 3, 512),         # unsupported vector count
+        mk(_abi.KS_KERNEL_WARP_ROW, 4, 64),         # a warp cannot cover 1024 vectors
+        mk(_abi.KS_KERNEL_BULK_ROW, 4, 256, 0),     # no stages
+        mk(_abi.KS_KERNEL_BULK_ROW, 4, 256, 15),    # 15 x 16 KB > 227 KB
+        mk(_abi.KS_KERNEL_SCALAR, 0, 48),           # not a multiple of 32
+        mk(9, 4, 256),                              # unknown kernel
+    ]
+    for p in bad:
+        assert _abi.ks_rms_norm_planned(a, b, w, 64, 8192, 1e-6, BF16, p, None) == E
+    # a vector plan on an unaligned pointer
+    p = mk(_abi.KS_KERNEL_CTA_ROW, 4, 256)
+    assert _abi.ks_rms_norm_planned(a, b + 2, w, 64, 8192, 1e-6, BF16, p, None) == E
+    # fused rings hold two rows per stage: 8 x 32 KB does not fit
+    p = mk(_abi.KS_KERNEL_BULK_ROW, 4, 256, 8)
+    assert _abi.ks_fused_add_rms_norm_planned(a, b, w, 64, 8192, 1e-6, BF16, p, None) == E
+    assert _abi.load().ks_rms_norm_planned(a, b, w, 64, 8192, 1e-6, BF16, None, None) == E

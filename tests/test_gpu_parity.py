@@ -223,3 +223,79 @@ def test_streams_are_honoured(cuda_device):
     s.synchronize()
     ref, _ = oracle.rms_norm(x.cpu(), wt.cpu())
     compare_output(y.cpu(), ref, torch.bfloat16, 4096, "side stream")
+
+
+# ------------------------------------------------- every kernel variant, via explicit plans
+
+def _variant_plan(name, hidden, elem):
+    from row_wise_rmsnorm_ks_gb300 import _abi as A
+    hv = hidden * elem // 16
+    up32 = lambda n: -(-n // 32) * 32
+    if name == "scalar":
+        return A.make_plan(A.KS_KERNEL_SCALAR, 0, 256)
+    if hidden * elem % 16:
+        return None
+    flags = A.KS_PLAN_NO_PREFETCH if name.endswith("_np") else 0
+    if name.startswith("warp_row"):
+        v = next((v for v in (1, 2, 4) if 32 * v >= hv), None)
+        return A.make_plan(A.KS_KERNEL_WARP_ROW, v, 128, flags=flags) if v else None
+    v = 2 if name.startswith("cta_row_v2") else 4
+    block = max(32, up32(-(-hv // v)))
+    if block > (1024 if v == 2 else 512):
+        return None
+    if name.startswith("bulk_row"):
+        stages = int(name.split("_s")[1])
+        return A.make_plan(A.KS_KERNEL_BULK_ROW, 4, block, stages)
+    return A.make_plan(A.KS_KERNEL_CTA_ROW, v, block, flags=flags)
+
+
+VARIANTS = ["warp_row", "warp_row_np", "cta_row_v2", "cta_row_v2_np", "cta_row_v4",
+            "cta_row_v4_np", "bulk_row_s1", "bulk_row_s2", "bulk_row_s5", "scalar"]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
+@pytest.mark.parametrize("rows,hidden", [(333, 1024), (1000, 1536), (457, 4096), (300, 8192),
+                                         (155, 16384)])
+def test_every_kernel_variant_matches_oracle(cuda_device, variant, dtype, op, rows, hidden):
+    from row_wise_rmsnorm_ks_gb300 import _abi as A
+    dt = synth.dtype_of(dtype)
+    elem = 4 if dt == torch.float32 else 2
+    plan = _variant_plan(variant, hidden, elem)
+    if plan is None:
+        pytest.skip("variant does not fit this width")
+    if plan.kernel == A.KS_KERNEL_BULK_ROW:
+        stage = hidden * elem * (2 if op != "rms_norm" else 1)
+        if 128 + plan.stages * stage > 226 * 1024:
+            pytest.skip("ring does not fit")
+    x = synth.cast(synth.normal_np((rows, hidden), 91), dt)
+    wt = synth.weight(hidden, dt)
+    code = {torch.bfloat16: A.KS_DTYPE_BF16, torch.float16: A.KS_DTYPE_F16,
+            torch.float32: A.KS_DTYPE_F32}[dt]
+    xd, wd = x.to(cuda_device), wt.to(cuda_device)
+    s = torch.cuda.current_stream().cuda_stream
+    name = f"variant {variant} {op} {dtype} [{rows},{hidden}]"
+    if op == "rms_norm":
+        yd = torch.empty_like(xd)
+        A.check(A.ks_rms_norm_planned(yd.data_ptr(), xd.data_ptr(), wd.data_ptr(), rows, hidden,
+                                      1e-6, code, plan, s))
+        ref, _ = oracle.rms_norm(x, wt, 1e-6)
+        compare_output(yd.cpu(), ref, dt, hidden, name)
+    else:
+        r = synth.cast(synth.normal_np((rows, hidden), 92, std=2.0), dt)
+        rd = r.to(cuda_device)
+        A.check(A.ks_fused_add_rms_norm_planned(xd.data_ptr(), rd.data_ptr(), wd.data_ptr(), rows,
+                                                hidden, 1e-6, code, plan, s))
+        ref_x, ref_r, _ = oracle.fused_add_rms_norm(x, r, wt, 1e-6)
+        assert bits_equal(rd.cpu(), ref_r), name
+        compare_output(xd.cpu(), ref_x, dt, hidden, name)
+    st, flags = A.ks_device_faults(clear=True)
+    assert st == A.KS_SUCCESS and flags == 0
+
+
+def test_no_device_faults_recorded(cuda_device):
+    from row_wise_rmsnorm_ks_gb300 import _abi as A
+    torch.cuda.synchronize()
+    st, flags = A.ks_device_faults(clear=False)
+    assert st == A.KS_SUCCESS and flags == 0
