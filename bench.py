@@ -365,47 +365,83 @@ def decode_latency(dev, args) -> dict:
 
 
 def run_e2e(dev, args, R, H, eps) -> dict:
-    """The same step through the public API with host buffers: pinned host -> device copies of
-    every input, both ops, device -> host copies of every output, all inside the timed region."""
+    """The same step through the public API with host buffers: ks.rms_norm_host and
+    ks.fused_add_rms_norm_host take pinned host rows. Two modes are timed: direct (the kernels
+    read and write the pinned rows over the host link) and staged (chunks copied through a device
+    workspace, copies overlapping kernels). Either way every input byte crosses host->device and
+    every output byte device->host inside the timed region; the faster mode is the e2e value."""
     import torch
 
     import row_wise_rmsnorm_ks_gb300 as ks
     from row_wise_rmsnorm_ks_gb300 import synth
 
     stream = torch.cuda.current_stream(dev)
-    xd = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), "bf16")
-    rd = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev), "bf16")
-    xh = xd.cpu().pin_memory()
+    xh = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), "bf16").cpu().pin_memory()
     x2h = xh.clone().pin_memory()
-    rh = rd.cpu().pin_memory()
-    yh, xoh, roh = (torch.empty_like(xh).pin_memory() for _ in range(3))
+    rh = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev), "bf16").cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
     w = synth.weight(H, "bf16").to(dev)
-    xdev, x2dev, rdev, ydev = xd, torch.empty_like(xd), rd, torch.empty_like(xd)
-
-    def step():
-        xdev.copy_(xh, non_blocking=True)
-        x2dev.copy_(x2h, non_blocking=True)
-        rdev.copy_(rh, non_blocking=True)
-        ks.rms_norm(xdev, w, eps, out=ydev)
-        ks.fused_add_rms_norm(x2dev, rdev, w, eps)
-        yh.copy_(ydev, non_blocking=True)
-        xoh.copy_(x2dev, non_blocking=True)
-        roh.copy_(rdev, non_blocking=True)
-
-    for _ in range(2):
-        step()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(args.e2e_steps):
-        step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / args.e2e_steps
     nbytes = algorithmic_bytes("rms_norm", R, H, 2) + algorithmic_bytes("fused_add_rms_norm", R, H, 2)
+
+    def timed(ws):
+        def step():
+            ks.rms_norm_host(xh, w, eps, workspace=ws, out=yh)
+            ks.fused_add_rms_norm_host(x2h, rh, w, eps, workspace=ws)
+
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.e2e_steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.e2e_steps
+
+    # The host link's own ceiling: pinned copies of 512 MiB one way, the other way, and both at
+    # once on two streams (the e2e step moves equal bytes each way).
+    blk = 256 << 20  # bf16 elements = 512 MiB
+    hsrc = xh.view(-1)[:blk]
+    hdst = torch.empty(blk, dtype=torch.bfloat16).pin_memory()
+    dbuf = torch.empty(blk, dtype=torch.bfloat16, device=dev)
+    dbuf2 = torch.empty(blk, dtype=torch.bfloat16, device=dev)
+    s2 = torch.cuda.Stream(dev)
+
+    def copy_time(h2d, d2h, reps=3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            if h2d:
+                dbuf.copy_(hsrc, non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s2):
+                    hdst.copy_(dbuf2, non_blocking=True)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    nblk = blk * 2
+    link = {"h2d_gbs": nblk / copy_time(True, False) / 1e9,
+            "d2h_gbs": nblk / copy_time(False, True) / 1e9,
+            "bidirectional_gbs": 2 * nblk / copy_time(True, True) / 1e9,
+            "how": "pinned 512 MiB copies (torch copy_), wall clock over 3 repetitions"}
+    del hdst, dbuf, dbuf2
+
+    ms_direct = timed(None)
+    ws = torch.empty(args.e2e_workspace_mb << 20, dtype=torch.uint8, device=dev)
+    ms_staged = timed(ws)
+    del ws
+    best = "direct" if ms_direct <= ms_staged else "staged"
+    ms = min(ms_direct, ms_staged)
     return {"value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
             "steps": args.e2e_steps, "h2d_bytes_per_step": 3 * R * H * 2,
-            "d2h_bytes_per_step": 3 * R * H * 2}
+            "d2h_bytes_per_step": 3 * R * H * 2, "mode": best, "host_link": link,
+            "frac_of_link": (nbytes / (ms * 1e-3) / 1e9) / link["bidirectional_gbs"],
+            "direct_gbs": nbytes / (ms_direct * 1e-3) / 1e9,
+            "staged_gbs": nbytes / (ms_staged * 1e-3) / 1e9,
+            "api": "rms_norm_host + fused_add_rms_norm_host on pinned host rows (direct: kernels "
+                   "address the host rows; staged: chunks through a "
+                   f"{args.e2e_workspace_mb} MiB device workspace)"}
 
 
 def cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args) -> dict:
@@ -508,6 +544,7 @@ def main() -> int:
     ap.add_argument("--rows", type=int, default=32768)
     ap.add_argument("--hidden", type=int, default=8192)
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-workspace-mb", type=int, default=192)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--decode-samples", type=int, default=300)
     ap.add_argument("--no-decode", action="store_true")

@@ -165,6 +165,45 @@ ks_status_t ks_fused_add_rms_norm_planned(void *x, void *residual, const void *w
 #define KS_FAULT_WAIT_TIMEOUT 1
 ks_status_t ks_device_faults(int32_t *flags, int32_t clear);
 
+/*
+ * The same two operations on rows held in host memory, for callers whose activations are not on
+ * the device. Two modes:
+ *   - direct (workspace == NULL): every host buffer must be page-locked memory mapped into the
+ *     device's address space (cudaHostAlloc / cudaHostRegister; on Grace-Blackwell the GPU
+ *     reaches it over the coherent NVLink-C2C link). The kernels read and write the host rows in
+ *     place, on `stream`, with no staging copy. The library checks both ends of each buffer with
+ *     cudaPointerGetAttributes first and returns KS_ERR_INVALID_ARGUMENT, launching nothing, if
+ *     any is not page-locked, mapped and contiguous.
+ *   - staged (workspace != NULL): any memory cudaMemcpy reads (pinned for the copies to overlap).
+ *     The rows go in chunks through `workspace`, device memory the caller owns, split into 3
+ *     slots; a chunk is as many rows as a slot holds (fused: x rows, then residual rows at the
+ *     next 256-byte boundary; see ks_host_chunk_rows). Chunk i's copy to the device, the kernel
+ *     on chunk i-1 and chunk i-2's copy back run at once on three streams the library creates
+ *     once per device; the caller's `stream` is joined at entry (work queued on it earlier
+ *     happens first) and at exit (work queued on it later waits for the last copy back).
+ *     Calls that share a workspace must be ordered on one stream.
+ * Both modes return once the work is queued: host buffers must stay valid and are complete only
+ * after `stream` reaches that point.
+ *   out, x, residual  host pointers, [rows, hidden]; rms_norm allows out == x; fused updates x
+ *                     and residual in place.
+ *   weight            device pointer, [hidden], read-only; must not overlap the workspace.
+ *   workspace         device pointer or NULL (direct mode); workspace_bytes its size.
+ * Errors as for the device entry points, plus KS_ERR_INVALID_ARGUMENT when a staged slot cannot
+ * hold one row or a direct-mode buffer is not mapped, and KS_ERR_CUDA when the library's streams
+ * cannot be created or a copy fails.
+ */
+ks_status_t ks_rms_norm_host(void *out, const void *x, const void *weight, int64_t rows,
+                             int64_t hidden, float eps, ks_dtype_t dtype, void *workspace,
+                             int64_t workspace_bytes, ks_stream_t stream);
+ks_status_t ks_fused_add_rms_norm_host(void *x, void *residual, const void *weight, int64_t rows,
+                                       int64_t hidden, float eps, ks_dtype_t dtype,
+                                       void *workspace, int64_t workspace_bytes,
+                                       ks_stream_t stream);
+
+/* Rows per chunk the *_host entry points use for this workspace size (op 0 = rms_norm, 1 =
+ * fused); 0 if a slot holds no row, -1 for invalid arguments. Pure host function. */
+int64_t ks_host_chunk_rows(int32_t op, int64_t hidden, ks_dtype_t dtype, int64_t workspace_bytes);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t ks_version(void);
 

@@ -23,7 +23,8 @@ KS_PLAN_NO_PREFETCH = 1
 # Every symbol include/ks.h declares (checked by the CPU test of the boundary).
 EXPORTED = ("ks_rms_norm", "ks_fused_add_rms_norm", "ks_status_string", "ks_last_error",
             "ks_plan_launch", "ks_rms_norm_planned", "ks_fused_add_rms_norm_planned",
-            "ks_device_faults", "ks_version")
+            "ks_device_faults", "ks_rms_norm_host", "ks_fused_add_rms_norm_host",
+            "ks_host_chunk_rows", "ks_version")
 
 
 class KsLibraryMissing(RuntimeError):
@@ -87,6 +88,13 @@ def load(path: str | None = None):
         lib.ks_fused_add_rms_norm_planned.restype = ctypes.c_int
         lib.ks_device_faults.argtypes = [ctypes.POINTER(i32), i32]
         lib.ks_device_faults.restype = ctypes.c_int
+        lib.ks_rms_norm_host.argtypes = [vp, vp, vp, i64, i64, f32, ctypes.c_int, vp, i64, vp]
+        lib.ks_rms_norm_host.restype = ctypes.c_int
+        lib.ks_fused_add_rms_norm_host.argtypes = [vp, vp, vp, i64, i64, f32, ctypes.c_int, vp,
+                                                   i64, vp]
+        lib.ks_fused_add_rms_norm_host.restype = ctypes.c_int
+        lib.ks_host_chunk_rows.argtypes = [i32, i64, ctypes.c_int, i64]
+        lib.ks_host_chunk_rows.restype = i64
         lib.ks_version.argtypes = []
         lib.ks_version.restype = i32
         _lib = lib
@@ -146,6 +154,23 @@ def ks_device_faults(clear: bool = True) -> tuple[int, int]:
     flags = ctypes.c_int32(0)
     st = load().ks_device_faults(ctypes.byref(flags), int(bool(clear)))
     return st, flags.value
+
+
+def ks_rms_norm_host(out: int, x: int, weight: int, rows: int, hidden: int, eps: float,
+                     dtype: int, workspace: int, workspace_bytes: int, stream: int | None) -> int:
+    return load().ks_rms_norm_host(out, x, weight, rows, hidden, eps, dtype, workspace,
+                                   workspace_bytes, stream)
+
+
+def ks_fused_add_rms_norm_host(x: int, residual: int, weight: int, rows: int, hidden: int,
+                               eps: float, dtype: int, workspace: int, workspace_bytes: int,
+                               stream: int | None) -> int:
+    return load().ks_fused_add_rms_norm_host(x, residual, weight, rows, hidden, eps, dtype,
+                                             workspace, workspace_bytes, stream)
+
+
+def ks_host_chunk_rows(op: int, hidden: int, dtype: int, workspace_bytes: int) -> int:
+    return load().ks_host_chunk_rows(op, hidden, dtype, workspace_bytes)
 
 
 def ks_version() -> int:

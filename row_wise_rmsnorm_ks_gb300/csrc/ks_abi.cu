@@ -18,8 +18,8 @@
 
 namespace ks {
 namespace {
-
 thread_local char g_detail[256] = "";
+}  // namespace
 
 ks_status_t fail(ks_status_t s, const char *fmt, ...) {
     va_list ap;
@@ -232,7 +232,6 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
     return KS_SUCCESS;
 }
 
-}  // namespace
 
 // Host heuristic (after the pages' rule of sizing the launch from the row width: Triton
 // Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"), set from a sweep of

@@ -21,6 +21,17 @@ struct RowArgs {
     int32_t stages;     // staged kernel: rows in the shared-memory ring
 };
 
+// Records a failure detail for ks_last_error() on this thread and returns `s`.
+ks_status_t fail(ks_status_t s, const char *fmt, ...);
+// Element size of a dtype in bytes (0 for an unknown code).
+int elem_bytes(ks_dtype_t d);
+// Whether [a, a+na) and [b, b+nb) share a byte.
+bool overlaps(const void *a, int64_t na, const void *b, int64_t nb);
+// The checked launch path behind every device-pointer entry point (forced == NULL: heuristic).
+ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, int64_t rows,
+                int64_t hidden, float eps, ks_dtype_t dtype, ks_stream_t stream,
+                const ks_plan_t *forced);
+
 // Host heuristic: fills *p from the shape, the element size and the device's SM count.
 // blocks_per_sm == 0 leaves grid at one pass over the rows.
 ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem_bytes, bool aligned16,

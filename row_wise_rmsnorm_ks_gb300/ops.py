@@ -3,6 +3,12 @@
     rms_norm(x, weight, eps=1e-6) -> y
     fused_add_rms_norm(x, residual, weight, eps=1e-6) -> None   (x and residual updated in place)
 
+    rms_norm_host(x, weight, eps=1e-6, *, out=None, workspace=None) -> out
+    fused_add_rms_norm_host(x, residual, weight, eps=1e-6, *, workspace=None) -> None
+(the last two take rows in host memory: without a workspace the kernels read and write pinned
+host rows directly over the host link; with a device workspace the library copies them through
+it in overlapping chunks).
+
 Checks follow Kernscope "API contract / Inputs": x is (..., hidden) with a non-empty last
 dimension, weight is (hidden,), tensors are contiguous CUDA tensors of one dtype (fp16, bf16 or
 fp32) on one device, eps is finite and positive, the fused op's residual has x's shape and the
@@ -82,4 +88,69 @@ def fused_add_rms_norm(x: torch.Tensor, residual: torch.Tensor, weight: torch.Te
         _abi.check(_abi.ks_fused_add_rms_norm(x.data_ptr(), residual.data_ptr(),
                                               weight.data_ptr(), rows, hidden, float(eps),
                                               _DTYPES[x.dtype], _stream(x.device)))
+    return None
+
+
+def _check_host(x: torch.Tensor, weight: torch.Tensor, workspace: torch.Tensor, eps: float):
+    if not isinstance(x, torch.Tensor) or x.device.type != "cpu":
+        raise ValueError("x must be a CPU tensor (pin it for the copies to overlap)")
+    if x.dtype not in _DTYPES or weight.dtype != x.dtype:
+        raise TypeError("x and weight must share a dtype: float16, bfloat16 or float32")
+    if weight.device.type != "cuda" or weight.dim() != 1 or weight.shape[0] != x.shape[-1]:
+        raise ValueError("weight must be a CUDA tensor of shape (hidden,)")
+    if workspace is not None and (not isinstance(workspace, torch.Tensor)
+                                  or workspace.device != weight.device
+                                  or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor on weight's device")
+    if workspace is None and not x.is_pinned():
+        raise ValueError("without a workspace the host rows must be pinned")
+    if not (x.is_contiguous() and weight.is_contiguous()):
+        raise ValueError("tensors must be contiguous")
+    if x.dim() < 1 or x.shape[-1] == 0:
+        raise ValueError("the last dimension of x must be non-empty")
+    if not (isinstance(eps, (int, float)) and math.isfinite(eps) and eps > 0):
+        raise ValueError("eps must be finite and positive")
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+
+
+def rms_norm_host(x: torch.Tensor, weight: torch.Tensor, eps: float = 1e-6, *,
+                  workspace: torch.Tensor | None = None,
+                  out: torch.Tensor | None = None) -> torch.Tensor:
+    """RMSNorm of host rows through the device: returns `out` (a host tensor, x's shape; may be
+    x). Ordered on the current stream of weight's device; synchronise it before reading `out`."""
+    _check_host(x, weight, workspace, eps)
+    if out is None:
+        out = torch.empty(x.shape, dtype=x.dtype, pin_memory=x.is_pinned())
+    elif out.shape != x.shape or out.dtype != x.dtype or out.device.type != "cpu":
+        raise ValueError("out must be a CPU tensor with x's shape and dtype")
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden
+    with torch.cuda.device(weight.device):
+        _abi.check(_abi.ks_rms_norm_host(out.data_ptr(), x.data_ptr(), weight.data_ptr(), rows,
+                                         hidden, float(eps), _DTYPES[x.dtype], *_ws(workspace),
+                                         _stream(weight.device)))
+    return out
+
+
+def fused_add_rms_norm_host(x: torch.Tensor, residual: torch.Tensor, weight: torch.Tensor,
+                            eps: float = 1e-6, *, workspace: torch.Tensor | None = None) -> None:
+    """Fused residual-add RMSNorm of host rows through the device, in place on both host
+    tensors. Ordered on the current stream of weight's device; synchronise before reading."""
+    _check_host(x, weight, workspace, eps)
+    if (not isinstance(residual, torch.Tensor) or residual.shape != x.shape
+            or residual.dtype != x.dtype or residual.device.type != "cpu"
+            or not residual.is_contiguous()):
+        raise ValueError("residual must be a contiguous CPU tensor with x's shape and dtype")
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden
+    with torch.cuda.device(weight.device):
+        _abi.check(_abi.ks_fused_add_rms_norm_host(x.data_ptr(), residual.data_ptr(),
+                                                   weight.data_ptr(), rows, hidden, float(eps),
+                                                   _DTYPES[x.dtype], *_ws(workspace),
+                                                   _stream(weight.device)))
     return None

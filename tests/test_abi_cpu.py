@@ -227,3 +227,30 @@ def test_planned_entry_points_reject_plans_that_do_not_fit():
     p = mk(_abi.KS_KERNEL_BULK_ROW, 4, 256, 8)
     assert _abi.ks_fused_add_rms_norm_planned(a, b, w, 64, 8192, 1e-6, BF16, p, None) == E
     assert _abi.load().ks_rms_norm_planned(a, b, w, 64, 8192, 1e-6, BF16, None, None) == E
+
+
+def test_host_chunk_rows():
+    # plain: a slot (workspace / 3, rounded down to 256 bytes) of whole rows
+    assert _abi.ks_host_chunk_rows(0, 8192, BF16, 3 * 16384 * 100) == 100
+    # fused: x rows then residual rows at the next 256-byte boundary
+    assert _abi.ks_host_chunk_rows(1, 8192, BF16, 3 * 16384 * 100) == 50
+    # 200-byte rows in a 1024-byte slot: 2 fit (x at 0..400, residual at 512..912); 3 need 768 + 600
+    assert _abi.ks_host_chunk_rows(1, 100, BF16, 3 * 1024) == 2
+    assert _abi.ks_host_chunk_rows(0, 8192, BF16, 3 * 16383) == 0
+    assert _abi.ks_host_chunk_rows(2, 8192, BF16, 1 << 20) == -1
+    assert _abi.ks_host_chunk_rows(0, 8192, 9, 1 << 20) == -1
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_host_entry_points_reject_invalid_arguments(fused):
+    call = _abi.ks_fused_add_rms_norm_host if fused else _abi.ks_rms_norm_host
+    a, b, w, ws = FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30)
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    assert call(a, b, w, 4, 0, 1e-6, BF16, ws, 1 << 20, None) == E
+    assert call(a, b, w, 4, 64, float("nan"), BF16, ws, 1 << 20, None) == E
+    assert call(a, b, w, 4, 64, 1e-6, BF16, ws, 0, None) == E               # empty workspace
+    assert call(a, b, w, 4, 8192, 1e-6, BF16, ws, 3 * 1000, None) == E      # no row fits a slot
+    assert "holds no row" in _abi.ks_last_error()
+    assert call(a, b, w, 4, 64, 1e-6, 7, ws, 1 << 20, None) == _abi.KS_ERR_UNSUPPORTED_DTYPE
+    assert call(a, b, ws + 64, 4, 64, 1e-6, BF16, ws, 1 << 20, None) == _abi.KS_ERR_OVERLAP
+    assert call(0, 0, 0, 0, 64, 1e-6, BF16, 0, 0, None) == _abi.KS_SUCCESS   # empty input
