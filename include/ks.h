@@ -204,6 +204,32 @@ ks_status_t ks_fused_add_rms_norm_host(void *x, void *residual, const void *weig
  * fused); 0 if a slot holds no row, -1 for invalid arguments. Pure host function. */
 int64_t ks_host_chunk_rows(int32_t op, int64_t hidden, ks_dtype_t dtype, int64_t workspace_bytes);
 
+/*
+ * Fused residual-add RMSNorm of host rows, staged through device scratch memory built into the
+ * library, so the call allocates nothing. (No counterpart in the source pages: this is a
+ * convenience of this library.)
+ *
+ * For callers that cannot call cudaMalloc: code whose device memory belongs to another
+ * allocator (a plugin in a framework or serving process that accounts for every byte on the
+ * GPU) and latency-sensitive loops where cudaMalloc/cudaFree would stall the device. They have
+ * host rows and a stream but no device buffer to lend; this entry point behaves like
+ * ks_fused_add_rms_norm_host with a workspace, except that the workspace is a fixed 24 MiB array
+ * inside the library that every GPU loading the library holds until the process exits.
+ *   x, residual   host pointers (pinned for the copies to overlap), [rows, hidden], in place.
+ *   weight        device pointer, [hidden], read-only.
+ *   rows, hidden, eps, dtype, stream as for ks_fused_add_rms_norm_host.
+ * Limit: one row of x plus one of residual must fit a third of the 24 MiB (hidden up to about
+ * 2M bf16/fp16 or 1M fp32 elements); wider rows return KS_ERR_INVALID_ARGUMENT, launching
+ * nothing. Any number of rows is processed, in chunks.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture. All calls on a device
+ * share the one array and it keeps the last call's contents (nothing in it needs to start at
+ * zero); calls whose GPU work overlaps would race on it, so order them, e.g. on one stream.
+ */
+ks_status_t ks_fused_add_rms_norm_host_noalloc(void *x, void *residual, const void *weight,
+                                               int64_t rows, int64_t hidden, float eps,
+                                               ks_dtype_t dtype, ks_stream_t stream);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t ks_version(void);
 

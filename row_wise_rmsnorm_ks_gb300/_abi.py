@@ -24,7 +24,7 @@ KS_PLAN_NO_PREFETCH = 1
 EXPORTED = ("ks_rms_norm", "ks_fused_add_rms_norm", "ks_status_string", "ks_last_error",
             "ks_plan_launch", "ks_rms_norm_planned", "ks_fused_add_rms_norm_planned",
             "ks_device_faults", "ks_rms_norm_host", "ks_fused_add_rms_norm_host",
-            "ks_host_chunk_rows", "ks_version")
+            "ks_host_chunk_rows", "ks_fused_add_rms_norm_host_noalloc", "ks_version")
 
 
 class KsLibraryMissing(RuntimeError):
@@ -95,6 +95,9 @@ def load(path: str | None = None):
         lib.ks_fused_add_rms_norm_host.restype = ctypes.c_int
         lib.ks_host_chunk_rows.argtypes = [i32, i64, ctypes.c_int, i64]
         lib.ks_host_chunk_rows.restype = i64
+        lib.ks_fused_add_rms_norm_host_noalloc.argtypes = [vp, vp, vp, i64, i64, f32,
+                                                           ctypes.c_int, vp]
+        lib.ks_fused_add_rms_norm_host_noalloc.restype = ctypes.c_int
         lib.ks_version.argtypes = []
         lib.ks_version.restype = i32
         _lib = lib
@@ -171,6 +174,14 @@ def ks_fused_add_rms_norm_host(x: int, residual: int, weight: int, rows: int, hi
 
 def ks_host_chunk_rows(op: int, hidden: int, dtype: int, workspace_bytes: int) -> int:
     return load().ks_host_chunk_rows(op, hidden, dtype, workspace_bytes)
+
+
+def ks_fused_add_rms_norm_host_noalloc(x: int, residual: int, weight: int, rows: int, hidden: int,
+                                       eps: float, dtype: int, stream: int | None) -> int:
+    """The staged host-buffer fused op on the library's built-in 24 MiB device scratch, for
+    callers that may not allocate device memory themselves."""
+    return load().ks_fused_add_rms_norm_host_noalloc(x, residual, weight, rows, hidden, eps, dtype,
+                                                     stream)
 
 
 def ks_version() -> int:

@@ -32,6 +32,13 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
                 int64_t hidden, float eps, ks_dtype_t dtype, ks_stream_t stream,
                 const ks_plan_t *forced);
 
+// The host-buffer path behind ks_*_host: direct when ws is NULL, staged through ws otherwise.
+ks_status_t run_host(bool fused, void *out, const void *x, void *res, const void *w,
+                     int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype, void *ws,
+                     int64_t ws_bytes, ks_stream_t stream);
+// Rows per staged chunk for a workspace of ws_bytes (0 if a slot holds no row).
+int64_t host_chunk_rows(bool fused, int64_t hidden, int e, int64_t ws_bytes);
+
 // Host heuristic: fills *p from the shape, the element size and the device's SM count.
 // blocks_per_sm == 0 leaves grid at one pass over the rows.
 ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem_bytes, bool aligned16,
