@@ -41,7 +41,7 @@ WORKLOAD = ("large prefill bf16: rms_norm + fused_add_rms_norm on x, residual [3
             "(512 MiB per tensor), weight 1+0.1N(0,1), eps=1e-5")
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["row_wise_rmsnorm_ks_gb300/csrc/ks_kernels.cuh",
-                  "row_wise_rmsnorm_ks_gb300/csrc/ks_abi.cu"]
+                  "row_wise_rmsnorm_ks_gb300/csrc/ks_ptx.cuh"]
 
 
 def algorithmic_bytes(op: str, rows: int, hidden: int, elem: int) -> int:
@@ -420,6 +420,7 @@ def run_e2e(dev, args, R, H, eps) -> dict:
         torch.cuda.synchronize()
         return (time.perf_counter() - t0) / reps
 
+    copy_time(True, True, reps=1)  # warm both directions up
     nblk = blk * 2
     link = {"h2d_gbs": nblk / copy_time(True, False) / 1e9,
             "d2h_gbs": nblk / copy_time(False, True) / 1e9,
