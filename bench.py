@@ -310,9 +310,12 @@ def run_ks(args) -> int:
 
 
 def decode_latency(dev, args) -> dict:
-    """Fused op on the decode shape [4, 1536] bf16: single launches after an L2 flush (CUDA
-    events around each launch, the flush outside), and the per-launch time of a CUDA graph of
-    100 back-to-back launches."""
+    """Fused op on the decode shape [4, 1536] bf16 (launch-bound). Reported: single launches
+    timed with CUDA events around each launch, cold (an L2 flush by a 512 MiB write outside the
+    timed pair, the pages' cache-cold method; the flush keeps the GPU busy while the launch is
+    queued, so the pair times the kernel) and hot (the GPU idles, so the pair also times this
+    Python caller's launch path); and the per-launch time of a CUDA graph of 100 back-to-back
+    dependent launches, without and with programmatic dependent launch."""
     import torch
 
     from row_wise_rmsnorm_ks_gb300 import _abi, synth
@@ -328,40 +331,55 @@ def decode_latency(dev, args) -> dict:
 
     for _ in range(20):
         launch(stream.cuda_stream)
-    samples = []
-    for _ in range(args.decode_samples):
-        flush.fill_(1)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        launch(stream.cuda_stream)
-        b.record(stream)
-        b.synchronize()
-        samples.append(a.elapsed_time(b) * 1e3)
-    samples.sort()
-    g = torch.cuda.CUDAGraph()
-    cs = torch.cuda.Stream(dev)
-    cs.wait_stream(stream)
-    with torch.cuda.stream(cs):
-        launch(cs.cuda_stream)
-    torch.cuda.synchronize()
-    with torch.cuda.graph(g, stream=cs):
-        for _ in range(100):
-            launch(cs.cuda_stream)
-    g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    reps = 20
-    for _ in range(reps):
+
+    def single(cold):
+        out = []
+        for _ in range(args.decode_samples):
+            if cold:
+                flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch(stream.cuda_stream)
+            b.record(stream)
+            b.synchronize()
+            out.append(a.elapsed_time(b) * 1e3)
+        out.sort()
+        return out
+
+    def graph_per_launch(pdl):
+        _abi.ks_set_launch_options(_abi.KS_LAUNCH_PDL if pdl else 0)
+        try:
+            g = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream(dev)
+            cs.wait_stream(stream)
+            with torch.cuda.stream(cs):
+                launch(cs.cuda_stream)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=cs):
+                for _ in range(100):
+                    launch(cs.cuda_stream)
+        finally:
+            _abi.ks_set_launch_options(0)
         g.replay()
-    b.record(stream)
-    torch.cuda.synchronize()
-    per_launch = a.elapsed_time(b) * 1e3 / (reps * 100)
-    nbytes = algorithmic_bytes("fused_add_rms_norm", 4, 1536, 2)
-    q = lambda p: samples[min(len(samples) - 1, int(p * len(samples)))]
-    return {"bytes_per_launch": nbytes, "p50_us_cold_event": q(0.5), "p95_us_cold_event": q(0.95),
-            "p99_us_cold_event": q(0.99), "us_per_launch_graph_replay": per_launch,
-            "samples": len(samples)}
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 20
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * 100)
+
+    cold, hot = single(True), single(False)
+    q = lambda v, p: v[min(len(v) - 1, int(p * len(v)))]
+    return {"bytes_per_launch": algorithmic_bytes("fused_add_rms_norm", 4, 1536, 2),
+            "p50_us_cold_event": q(cold, 0.5), "p95_us_cold_event": q(cold, 0.95),
+            "p99_us_cold_event": q(cold, 0.99),
+            "p50_us_hot_event_incl_python_launch": q(hot, 0.5),
+            "us_per_launch_graph_replay": graph_per_launch(False),
+            "us_per_launch_graph_replay_pdl": graph_per_launch(True),
+            "samples": len(cold)}
 
 
 def run_e2e(dev, args, R, H, eps) -> dict:

@@ -121,8 +121,11 @@ typedef struct ks_plan {
 
 /* Plan flags. KS_PLAN_NO_PREFETCH: the register kernels (warp and CTA rows) load each row when
  * they reach it instead of loading the next row before reducing the current one (fewer
- * registers, so more resident CTAs). */
+ * registers, so more resident CTAs). KS_PLAN_PDL: launch with programmatic stream serialization
+ * (programmatic dependent launch), so the kernel may be scheduled while the previous kernel in
+ * the stream finishes; it waits for that kernel's writes before its first memory access. */
 #define KS_PLAN_NO_PREFETCH 1
+#define KS_PLAN_PDL 2
 
 enum {
     KS_KERNEL_NONE = 0,     /* rows == 0: nothing is launched */
@@ -229,6 +232,17 @@ int64_t ks_host_chunk_rows(int32_t op, int64_t hidden, ks_dtype_t dtype, int64_t
 ks_status_t ks_fused_add_rms_norm_host_noalloc(void *x, void *residual, const void *weight,
                                                int64_t rows, int64_t hidden, float eps,
                                                ks_dtype_t dtype, ks_stream_t stream);
+
+/*
+ * Process-wide launch options for the entry points that choose their own plan (all but the
+ * *_planned ones, whose plan carries its flags). KS_LAUNCH_PDL: launch every row kernel with
+ * programmatic dependent launch (see KS_PLAN_PDL), which hides launch latency in chains of small
+ * kernels such as a decode step. Off by default. Unknown bits return KS_ERR_INVALID_ARGUMENT.
+ * ks_get_launch_options returns the current bits.
+ */
+#define KS_LAUNCH_PDL 1
+ks_status_t ks_set_launch_options(int32_t options);
+int32_t ks_get_launch_options(void);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t ks_version(void);

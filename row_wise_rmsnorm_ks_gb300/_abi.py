@@ -19,12 +19,15 @@ KS_KERNEL_NONE, KS_KERNEL_WARP_ROW, KS_KERNEL_CTA_ROW, KS_KERNEL_SCALAR, KS_KERN
 KERNEL_NAMES = {0: "none", 1: "warp_row", 2: "cta_row", 3: "scalar", 4: "bulk_row"}
 KS_FAULT_WAIT_TIMEOUT = 1
 KS_PLAN_NO_PREFETCH = 1
+KS_PLAN_PDL = 2
+KS_LAUNCH_PDL = 1
 
 # Every symbol include/ks.h declares (checked by the CPU test of the boundary).
 EXPORTED = ("ks_rms_norm", "ks_fused_add_rms_norm", "ks_status_string", "ks_last_error",
             "ks_plan_launch", "ks_rms_norm_planned", "ks_fused_add_rms_norm_planned",
             "ks_device_faults", "ks_rms_norm_host", "ks_fused_add_rms_norm_host",
-            "ks_host_chunk_rows", "ks_fused_add_rms_norm_host_noalloc", "ks_version")
+            "ks_host_chunk_rows", "ks_fused_add_rms_norm_host_noalloc", "ks_set_launch_options",
+            "ks_get_launch_options", "ks_version")
 
 
 class KsLibraryMissing(RuntimeError):
@@ -98,6 +101,10 @@ def load(path: str | None = None):
         lib.ks_fused_add_rms_norm_host_noalloc.argtypes = [vp, vp, vp, i64, i64, f32,
                                                            ctypes.c_int, vp]
         lib.ks_fused_add_rms_norm_host_noalloc.restype = ctypes.c_int
+        lib.ks_set_launch_options.argtypes = [i32]
+        lib.ks_set_launch_options.restype = ctypes.c_int
+        lib.ks_get_launch_options.argtypes = []
+        lib.ks_get_launch_options.restype = i32
         lib.ks_version.argtypes = []
         lib.ks_version.restype = i32
         _lib = lib
@@ -182,6 +189,14 @@ def ks_fused_add_rms_norm_host_noalloc(x: int, residual: int, weight: int, rows:
     callers that may not allocate device memory themselves."""
     return load().ks_fused_add_rms_norm_host_noalloc(x, residual, weight, rows, hidden, eps, dtype,
                                                      stream)
+
+
+def ks_set_launch_options(options: int) -> int:
+    return load().ks_set_launch_options(options)
+
+
+def ks_get_launch_options() -> int:
+    return load().ks_get_launch_options()
 
 
 def ks_version() -> int:

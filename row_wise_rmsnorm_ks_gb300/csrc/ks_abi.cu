@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -19,6 +20,7 @@
 namespace ks {
 namespace {
 thread_local char g_detail[256] = "";
+std::atomic<int32_t> g_launch_options{0};
 }  // namespace
 
 ks_status_t fail(ks_status_t s, const char *fmt, ...) {
@@ -81,7 +83,7 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
     p.stages = p.kernel == KS_KERNEL_BULK_ROW ? p.stages : 0;
     p.smem_bytes = 0;
     p.reserved = 0;
-    if (p.flags & ~KS_PLAN_NO_PREFETCH)
+    if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL))
         return fail(KS_ERR_INVALID_ARGUMENT, "unknown plan flags 0x%x", (unsigned)p.flags);
     int64_t rows_per_cta = 1;
     switch (p.kernel) {
@@ -187,6 +189,9 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         st = plan(fused ? 1 : 0, rows, hidden, e, aligned16, slot.sm_count, 0, &p);
         if (st != KS_SUCCESS) return st;
     }
+    const int32_t pdl = forced ? (p.flags & KS_PLAN_PDL)
+                               : ((g_launch_options.load(std::memory_order_relaxed) & KS_LAUNCH_PDL)
+                                      ? KS_PLAN_PDL : 0);
 
     int bps;
     {
@@ -212,6 +217,7 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         if (st != KS_SUCCESS) return st;
     }
 
+    p.flags = (p.flags & ~KS_PLAN_PDL) | pdl;
     RowArgs a;
     a.out = fused ? const_cast<void *>(x) : out;
     a.x = x;
@@ -362,6 +368,15 @@ ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t 
     if (e == 0) return ks::fail(KS_ERR_UNSUPPORTED_DTYPE, "dtype code %d is not a ks_dtype_t", (int)dtype);
     return ks::plan(op, rows, hidden, e, aligned16 != 0, sm_count, blocks_per_sm, plan);
 }
+
+ks_status_t ks_set_launch_options(int32_t options) {
+    if (options & ~KS_LAUNCH_PDL)
+        return ks::fail(KS_ERR_INVALID_ARGUMENT, "unknown launch option bits 0x%x", (unsigned)options);
+    ks::g_launch_options.store(options, std::memory_order_relaxed);
+    return KS_SUCCESS;
+}
+
+int32_t ks_get_launch_options(void) { return ks::g_launch_options.load(std::memory_order_relaxed); }
 
 int32_t ks_version(void) { return 100; }
 

@@ -205,6 +205,8 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
     uint4 *og = static_cast<uint4 *>(a.out);
     uint4 *rg = static_cast<uint4 *>(a.res);
 
+    grid_dependency_wait();
+    allow_dependents_launch();
     uint4 wv[V];
     {
         const uint4 *wg = static_cast<const uint4 *>(a.w);
@@ -309,6 +311,8 @@ __global__ void __launch_bounds__(1024) rows_scalar_kernel(const RowArgs a) {
     const int64_t H = a.hidden;
     const float h = (float)H;
     int parity = 0;
+    grid_dependency_wait();
+    allow_dependents_launch();
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const int64_t base = row * H;
         SumSq acc;
@@ -376,6 +380,8 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
     uint4 *og = static_cast<uint4 *>(a.out);
     uint4 *rg = static_cast<uint4 *>(a.res);
 
+    grid_dependency_wait();
+    allow_dependents_launch();
     uint4 wv[V];
     {
         const uint4 *wg = static_cast<const uint4 *>(a.w);
@@ -584,8 +590,20 @@ cudaError_t launch_t(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStrea
     if (!f) return cudaErrorInvalidConfiguration;
     RowArgs copy = a;
     void *args[] = {&copy};
-    return cudaLaunchKernel(f, dim3((unsigned)p.grid), dim3((unsigned)p.block), args,
-                            dynamic_smem(p), s);
+    if (!(p.flags & KS_PLAN_PDL))
+        return cudaLaunchKernel(f, dim3((unsigned)p.grid), dim3((unsigned)p.block), args,
+                                dynamic_smem(p), s);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid);
+    cfg.blockDim = dim3((unsigned)p.block);
+    cfg.dynamicSmemBytes = dynamic_smem(p);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 }  // namespace ks

@@ -16,6 +16,19 @@ constexpr unsigned int kFaultWaitTimeout = 1u;
 // microsecond.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// Programmatic dependent launch. Every row kernel calls grid_dependency_wait() before its first
+// global-memory access: when the kernel was launched with the programmatic-serialization
+// attribute it waits there until the preceding kernel in the stream has completed and its writes
+// are visible; otherwise it returns at once. allow_dependents_launch() lets a kernel queued
+// after this one (and launched with the attribute) be scheduled early; that kernel still waits
+// for this one to finish before touching memory.
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

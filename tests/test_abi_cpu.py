@@ -254,3 +254,19 @@ def test_host_entry_points_reject_invalid_arguments(fused):
     assert call(a, b, w, 4, 64, 1e-6, 7, ws, 1 << 20, None) == _abi.KS_ERR_UNSUPPORTED_DTYPE
     assert call(a, b, ws + 64, 4, 64, 1e-6, BF16, ws, 1 << 20, None) == _abi.KS_ERR_OVERLAP
     assert call(0, 0, 0, 0, 64, 1e-6, BF16, 0, 0, None) == _abi.KS_SUCCESS   # empty input
+
+
+def test_launch_options():
+    assert _abi.ks_get_launch_options() == 0  # off by default
+    assert _abi.ks_set_launch_options(4) == _abi.KS_ERR_INVALID_ARGUMENT
+    assert _abi.ks_set_launch_options(_abi.KS_LAUNCH_PDL) == _abi.KS_SUCCESS
+    assert _abi.ks_get_launch_options() == _abi.KS_LAUNCH_PDL
+    assert _abi.ks_set_launch_options(0) == _abi.KS_SUCCESS
+    assert _abi.ks_get_launch_options() == 0
+
+
+def test_planned_flags_validated():
+    a, b, w = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    p = _abi.make_plan(_abi.KS_KERNEL_CTA_ROW, 4, 256, flags=8)
+    assert _abi.ks_rms_norm_planned(a, b, w, 64, 8192, 1e-6, BF16, p, None) == \
+        _abi.KS_ERR_INVALID_ARGUMENT
