@@ -18,7 +18,11 @@
  *
  * cast() rounds to nearest, ties to even, to the element type (+-inf on fp16 overflow, NaN
  * stays NaN). rsqrt is the correctly rounded FP32 reciprocal square root; the sum of squares is
- * accumulated in FP32 in an order of the library's choosing (a warp-shuffle tree).
+ * accumulated in FP32 in an order of the library's choosing (per-thread chains, a warp-shuffle
+ * tree, then warps in order). That order follows the launch shape the heuristic picks from
+ * (rows, hidden, dtype): results are bitwise reproducible for a given call shape on a given
+ * device, but two calls whose row counts select different launch shapes may differ in the last
+ * bit of some outputs (never in the residual, whose rounding is unique).
  *
  * Ownership and threading: the caller owns all memory; the library never allocates device or
  * pinned memory and keeps no state apart from a per-device cache of SM counts and kernel
@@ -116,7 +120,7 @@ typedef struct ks_plan {
     int32_t stages;         /* staged kernel: rows in each CTA's shared-memory ring (else 0) */
     int32_t smem_bytes;     /* staged kernel: dynamic shared memory per CTA (else 0) */
     int32_t flags;          /* KS_PLAN_* bits below */
-    int32_t reserved;       /* zero */
+    int32_t cluster;        /* cluster-row kernel: CTAs per cluster (one cluster per row) */
 } ks_plan_t;
 
 /* Plan flags. KS_PLAN_NO_PREFETCH: the register kernels (warp and CTA rows) load each row when
@@ -132,8 +136,10 @@ enum {
     KS_KERNEL_WARP_ROW = 1, /* one warp per row, row in registers, 16-byte vectors */
     KS_KERNEL_CTA_ROW = 2,  /* one CTA per row, row in registers, 16-byte vectors */
     KS_KERNEL_SCALAR = 3,   /* one CTA per row, element loads, two passes over the row */
-    KS_KERNEL_BULK_ROW = 4  /* one CTA per row, rows streamed through a shared-memory ring by
+    KS_KERNEL_BULK_ROW = 4, /* one CTA per row, rows streamed through a shared-memory ring by
                                bulk asynchronous copies, 4 vectors per thread */
+    KS_KERNEL_CLUSTER_ROW = 5 /* one cluster of `cluster` CTAs per row (few wide rows): each CTA
+                                 reduces a slice, partials exchanged in distributed shared memory */
 };
 
 ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t dtype,
@@ -147,7 +153,9 @@ ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t 
  * the call: a vector kernel on unaligned pointers or on a width that is not a multiple of 16
  * bytes, team * vec_per_thread vectors short of the row, a block that is not a multiple of 32 or
  * exceeds the kernel's bound (warp rows 256, CTA rows 1024 at 2 vectors and 512 at 4, staged
- * rows 512, scalar 1024), or a staged ring (stages 1..16) over 226 KB of shared memory. grid <= 0
+ * rows 512, cluster rows 512, scalar 1024), a staged ring (stages 1..16) over 226 KB of shared
+ * memory, or a cluster outside 2..8 CTAs whose slices (block * vec_per_thread vectors each) do
+ * not cover the row. grid <= 0
  * lets the library size the persistent grid; smem_bytes and rows_per_pass are recomputed. The
  * plan is read, never written.
  */

@@ -15,8 +15,10 @@ LIB_PATH = os.path.join(_HERE, "_build", "libks.so")
 
 KS_DTYPE_F32, KS_DTYPE_F16, KS_DTYPE_BF16 = 0, 1, 2
 KS_SUCCESS, KS_ERR_INVALID_ARGUMENT, KS_ERR_UNSUPPORTED_DTYPE, KS_ERR_OVERLAP, KS_ERR_CUDA = range(5)
-KS_KERNEL_NONE, KS_KERNEL_WARP_ROW, KS_KERNEL_CTA_ROW, KS_KERNEL_SCALAR, KS_KERNEL_BULK_ROW = range(5)
-KERNEL_NAMES = {0: "none", 1: "warp_row", 2: "cta_row", 3: "scalar", 4: "bulk_row"}
+(KS_KERNEL_NONE, KS_KERNEL_WARP_ROW, KS_KERNEL_CTA_ROW, KS_KERNEL_SCALAR, KS_KERNEL_BULK_ROW,
+ KS_KERNEL_CLUSTER_ROW) = range(6)
+KERNEL_NAMES = {0: "none", 1: "warp_row", 2: "cta_row", 3: "scalar", 4: "bulk_row",
+                5: "cluster_row"}
 KS_FAULT_WAIT_TIMEOUT = 1
 KS_PLAN_NO_PREFETCH = 1
 KS_PLAN_PDL = 2
@@ -47,7 +49,7 @@ class ks_plan_t(ctypes.Structure):
                 ("team", ctypes.c_int32), ("block", ctypes.c_int32), ("grid", ctypes.c_int64),
                 ("rows_per_pass", ctypes.c_int64), ("stages", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("flags", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("cluster", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {f: getattr(self, f) for f, _ in self._fields_}
@@ -138,11 +140,11 @@ def ks_plan_launch(op: int, rows: int, hidden: int, dtype: int, aligned16: bool,
 
 
 def make_plan(kernel: int, vec_per_thread: int, block: int, stages: int = 0,
-              grid: int = 0, flags: int = 0) -> ks_plan_t:
+              grid: int = 0, flags: int = 0, cluster: int = 0) -> ks_plan_t:
     """A plan for the *_planned entry points (derived fields are recomputed by the library)."""
     p = ks_plan_t()
-    p.kernel, p.vec_per_thread, p.block, p.stages, p.grid, p.flags = (
-        kernel, vec_per_thread, block, stages, grid, flags)
+    p.kernel, p.vec_per_thread, p.block, p.stages, p.grid, p.flags, p.cluster = (
+        kernel, vec_per_thread, block, stages, grid, flags, cluster)
     return p
 
 

@@ -82,7 +82,7 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
         return fail(KS_ERR_INVALID_ARGUMENT, "plan block %d is not a positive multiple of 32", p.block);
     p.stages = p.kernel == KS_KERNEL_BULK_ROW ? p.stages : 0;
     p.smem_bytes = 0;
-    p.reserved = 0;
+    p.cluster = p.kernel == KS_KERNEL_CLUSTER_ROW ? p.cluster : 0;
     if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL))
         return fail(KS_ERR_INVALID_ARGUMENT, "unknown plan flags 0x%x", (unsigned)p.flags);
     int64_t rows_per_cta = 1;
@@ -112,6 +112,18 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
                 return fail(KS_ERR_INVALID_ARGUMENT, "staged ring of %d stages does not fit", p.stages);
             p.smem_bytes = (int32_t)(kRingHeader + stage * p.stages);
         }
+        break;
+    }
+    case KS_KERNEL_CLUSTER_ROW: {
+        if (!vec_ok) return fail(KS_ERR_INVALID_ARGUMENT, "vector kernel needs 16-byte rows and pointers");
+        if (p.vec_per_thread != 1 && p.vec_per_thread != 2 && p.vec_per_thread != 4)
+            return fail(KS_ERR_INVALID_ARGUMENT, "cluster-row kernel takes 1, 2 or 4 vectors");
+        if (p.cluster < 2 || p.cluster > 8)
+            return fail(KS_ERR_INVALID_ARGUMENT, "cluster of %d CTAs (2..8 supported)", p.cluster);
+        const int64_t slice = ceil_div(hv, p.cluster);
+        if ((int64_t)p.block * p.vec_per_thread < slice || p.block > 512)
+            return fail(KS_ERR_INVALID_ARGUMENT, "cluster-row plan does not cover its slice or block > 512");
+        p.team = p.block * p.cluster;
         break;
     }
     case KS_KERNEL_SCALAR:
@@ -206,7 +218,15 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         }
     }
     if (bps <= 0) return fail(KS_ERR_CUDA, "kernel %d (block %d) cannot be resident", p.kernel, p.block);
-    if (forced) {
+    if (forced && p.kernel == KS_KERNEL_CLUSTER_ROW) {
+        // whole clusters: one row per cluster per pass
+        const int64_t cap = (int64_t)slot.sm_count * bps / p.cluster;
+        int64_t clusters = forced->grid > 0 ? forced->grid / p.cluster : cap;
+        clusters = clusters < 1 ? 1 : clusters;
+        clusters = clusters < rows ? clusters : rows;
+        p.grid = clusters * p.cluster;
+        p.rows_per_pass = clusters;
+    } else if (forced) {
         const int64_t per_cta = p.rows_per_pass;
         const int64_t ctas = ceil_div(rows, per_cta);
         const int64_t cap = (int64_t)slot.sm_count * bps;
@@ -251,6 +271,9 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 //    does not, which lowers its registers enough to keep more CTAs resident. Plain rows wider
 //    than 1536 vectors stream through the staged shared-memory ring instead, when there are
 //    enough rows to fill it;
+//    In the latency regime (rows <= SMs, so each CTA gets at most one row) the widest fused rows
+//    (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8 CTAs per row, and plain rows of
+//    at most 1024 vectors take 2 vectors per thread;
 //  * anything else (H not a multiple of the vector, unaligned pointers, wider rows): the scalar
 //    two-pass kernel.
 // The grid is persistent: at most sm_count * blocks_per_sm CTAs.
@@ -292,12 +315,37 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem, bool aligned16,
             p->flags = 0;
             p->stages = (int32_t)st;
             p->smem_bytes = (int32_t)(kRingHeader + st * stage);
+        } else if (rows <= sm_count) {
+            // Latency regime (at most one row per CTA), from a graph-replay sweep of few rows:
+            // the widest fused rows split over a cluster of 8 CTAs; narrower plain rows take
+            // twice the threads at 2 vectors each.
+            if (op == 1 && hv >= 1792 && rows * 8 <= sm_count) {
+                p->kernel = KS_KERNEL_CLUSTER_ROW;
+                p->cluster = 8;
+                p->vec_per_thread = 1;
+                p->block = (int32_t)round_up(ceil_div(hv, 8), 32);
+                p->team = p->block * 8;
+                p->flags = 0;
+            } else if (op == 0 && hv <= 1024) {
+                p->vec_per_thread = 2;
+                p->block = (int32_t)round_up(ceil_div(hv, 2), 32);
+                p->team = p->block;
+                p->flags = 0;
+            }
         }
     } else {
         p->kernel = KS_KERNEL_SCALAR;
         int64_t b = round_up(ceil_div(hidden, 8), 32);
         p->block = (int32_t)(b < 32 ? 32 : (b > 1024 ? 1024 : b));
         p->team = p->block;
+    }
+    if (p->kernel == KS_KERNEL_CLUSTER_ROW) {  // whole clusters, one row each per pass
+        int64_t clusters = rows;
+        const int64_t cap = (int64_t)sm_count * blocks_per_sm / p->cluster;
+        if (blocks_per_sm > 0 && clusters > cap) clusters = cap < 1 ? 1 : cap;
+        p->grid = clusters * p->cluster;
+        p->rows_per_pass = clusters;
+        return KS_SUCCESS;
     }
     const int64_t ctas = ceil_div(rows, rows_per_cta);
     const int64_t cap = (int64_t)sm_count * blocks_per_sm;

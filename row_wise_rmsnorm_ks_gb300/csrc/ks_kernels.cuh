@@ -18,6 +18,7 @@
 // flight without spending registers on them.
 #pragma once
 
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -509,6 +510,116 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ cluster row kernel
+
+// One thread-block cluster of C CTAs per row, for few rows of wide rows, where one CTA per row
+// would leave most SMs idle. CTA rank q of the cluster owns the row's 16-byte vectors
+// [q*S, min(hv, (q+1)*S)), S = ceil(hv / C); its thread t owns vectors q*S + t + k*G (k < V).
+// Each CTA reduces its slice (warp shuffles, then its warps in order), publishes the partial in
+// its own shared memory, and after one cluster barrier every thread adds the C partials in rank
+// order, read through distributed shared memory, so every CTA of the cluster computes the same
+// scale. Partials alternate between two slots per row, so one cluster barrier per row suffices
+// (a CTA can overwrite a slot only after the next row's barrier, which every peer reaches only
+// after reading it); a last cluster barrier keeps each CTA's shared memory alive until its peers
+// have read it. Clusters stride over rows. No global scratch, no spin-waits.
+template <typename T, int V, bool kFused>
+__global__ void __launch_bounds__(512) rows_cluster_kernel(const RowArgs a) {
+    namespace cg = cooperative_groups;
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    __shared__ float red[2][32];
+    __shared__ float part[2];
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int q = (int)cluster.block_rank();
+    const int g = blockDim.x;
+    const int t = threadIdx.x;
+    const int64_t hv = a.hv;
+    const int64_t S = (hv + C - 1) / C;
+    const int64_t lo = q * S;
+    const int64_t hi = (lo + S < hv) ? lo + S : hv;
+    const float h = (float)a.hidden;
+
+    const uint4 *xg = static_cast<const uint4 *>(a.x);
+    uint4 *og = static_cast<uint4 *>(a.out);
+    uint4 *rg = static_cast<uint4 *>(a.res);
+
+    grid_dependency_wait();
+    allow_dependents_launch();
+    uint4 wv[V];
+    {
+        const uint4 *wg = static_cast<const uint4 *>(a.w);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = lo + t + (int64_t)k * g;
+            wv[k] = (c < hi) ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+
+    const int64_t nclusters = gridDim.x / C;
+    int parity = 0;
+    for (int64_t row = blockIdx.x / C; row < a.rows; row += nclusters) {
+        uint4 xv[V], rv[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = lo + t + (int64_t)k * g;
+            xv[k] = (c < hi) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+            if (kFused) rv[k] = (c < hi) ? __ldcs(rg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        SumSq acc;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = lo + t + (int64_t)k * g;
+            if (c < hi) {
+                float f[N];
+                E::unpack(xv[k], f);
+                if (kFused) {
+                    float r[N];
+                    E::unpack(rv[k], r);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], r[e]);
+                    __stcs(rg + row * hv + c, E::pack(f));
+                }
+                acc.add(f);
+            }
+        }
+        // CTA partial: warps in order, by thread 0, into this row's slot
+        const float wsum = warp_sum(acc.total());
+        if ((t & 31) == 0) red[parity][t >> 5] = wsum;
+        __syncthreads();
+        if (t == 0) {
+            float cta = 0.0f;
+            for (int i = 0; i < (g >> 5); ++i) cta += red[parity][i];
+            part[parity] = cta;
+        }
+        cluster.sync();  // every CTA's partial for this row is published
+        float ss = 0.0f;
+        for (int r = 0; r < C; ++r) ss += *cluster.map_shared_rank(&part[parity], r);
+        parity ^= 1;
+        const float scale = row_scale(ss, h, a.eps);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = lo + t + (int64_t)k * g;
+            if (c < hi) {
+                float f[N], wf[N];
+                E::unpack(xv[k], f);
+                if (kFused) {
+                    float r[N];
+                    E::unpack(rv[k], r);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], r[e]);
+                }
+                E::unpack(wv[k], wf);
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
+                __stcs(og + row * hv + c, E::pack(f));
+            }
+        }
+    }
+    cluster.sync();  // peers may still be reading this CTA's partials
+}
+
 // ----------------------------------------------------------------------- kernel selection
 
 template <typename T, bool kFused>
@@ -539,6 +650,13 @@ const void *pick_kernel(const ks_plan_t &p) {
     case KS_KERNEL_SCALAR: return (const void *)rows_scalar_kernel<T, kFused>;
     case KS_KERNEL_BULK_ROW:
         return p.vec_per_thread == 4 ? (const void *)rows_bulk_kernel<T, 4, kFused> : nullptr;
+    case KS_KERNEL_CLUSTER_ROW:
+        switch (p.vec_per_thread) {
+        case 1: return (const void *)rows_cluster_kernel<T, 1, kFused>;
+        case 2: return (const void *)rows_cluster_kernel<T, 2, kFused>;
+        case 4: return (const void *)rows_cluster_kernel<T, 4, kFused>;
+        default: return nullptr;
+        }
     default: return nullptr;
     }
 }
@@ -590,7 +708,8 @@ cudaError_t launch_t(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStrea
     if (!f) return cudaErrorInvalidConfiguration;
     RowArgs copy = a;
     void *args[] = {&copy};
-    if (!(p.flags & KS_PLAN_PDL))
+    const bool cluster = p.kernel == KS_KERNEL_CLUSTER_ROW;
+    if (!(p.flags & KS_PLAN_PDL) && !cluster)
         return cudaLaunchKernel(f, dim3((unsigned)p.grid), dim3((unsigned)p.block), args,
                                 dynamic_smem(p), s);
     cudaLaunchConfig_t cfg = {};
@@ -598,11 +717,22 @@ cudaError_t launch_t(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStrea
     cfg.blockDim = dim3((unsigned)p.block);
     cfg.dynamicSmemBytes = dynamic_smem(p);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (p.flags & KS_PLAN_PDL) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)p.cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelExC(&cfg, f, args);
 }
 

@@ -151,8 +151,9 @@ def test_wide_rows_take_cta_per_row(hidden, block):
 
 
 def test_fp32_counts_four_elements_per_vector():
+    # 4096 fp32 = 1024 vectors: few rows take 2 vectors per thread (512 threads)
     p = plan(0, 10, 4096, dtype=F32)
-    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 256
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 512 and p.vec_per_thread == 2
     p = plan(1, 1000, 4096, dtype=F32)
     assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 256
 
@@ -192,13 +193,15 @@ def test_plan_invariants_over_a_sweep(dtype):
         for rows in [1, 7, 152, 333, 65536]:
             p = plan(1, rows, hidden, dtype=dtype, bps=2)
             assert p.block % 32 == 0 and 32 <= p.block <= 1024
-            assert 1 <= p.grid <= max(rows, 1)
+            assert 1 <= p.grid <= max(rows, 1) * max(p.cluster, 1)
             if p.kernel in (_abi.KS_KERNEL_WARP_ROW, _abi.KS_KERNEL_CTA_ROW,
-                            _abi.KS_KERNEL_BULK_ROW):
+                            _abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_CLUSTER_ROW):
                 assert hidden * e % 16 == 0
                 assert p.team * p.vec_per_thread * (16 // e) >= hidden
                 if p.kernel != _abi.KS_KERNEL_WARP_ROW:
-                    assert p.block <= 512  # the launch bound of the 4-vector CTA kernels
+                    assert p.block <= (1024 if p.vec_per_thread <= 2 else 512)
+                if p.kernel == _abi.KS_KERNEL_CLUSTER_ROW:
+                    assert p.grid % p.cluster == 0 and 2 <= p.cluster <= 8
                 if p.kernel == _abi.KS_KERNEL_BULK_ROW:
                     assert p.smem_bytes <= 226 * 1024 and p.stages >= 2
 
@@ -270,3 +273,20 @@ def test_planned_flags_validated():
     p = _abi.make_plan(_abi.KS_KERNEL_CTA_ROW, 4, 256, flags=8)
     assert _abi.ks_rms_norm_planned(a, b, w, 64, 8192, 1e-6, BF16, p, None) == \
         _abi.KS_ERR_INVALID_ARGUMENT
+
+
+def test_latency_regime_choices():
+    # widest fused rows, few of them: a cluster of 8 CTAs per row, 1 vector per thread
+    for hidden in (14336, 16384):
+        p = plan(1, 7, hidden, bps=2)
+        assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == 8 and p.vec_per_thread == 1
+        assert p.block * 8 * p.cluster >= hidden and p.grid == 7 * 8 and p.rows_per_pass == 7
+        assert p.team == p.block * 8
+    # too many rows for clusters of 8 on 152 SMs: the CTA kernel
+    assert plan(1, 20, 16384).kernel == _abi.KS_KERNEL_CTA_ROW
+    # narrower plain rows, few of them: 2 vectors per thread, twice the threads
+    p = plan(0, 33, 4096)
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.vec_per_thread == 2 and p.block == 256
+    # plain rows wider than 1024 vectors keep 4 vectors per thread
+    p = plan(0, 33, 16384)
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.vec_per_thread == 4 and p.block == 512

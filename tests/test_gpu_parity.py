@@ -246,11 +246,16 @@ def _variant_plan(name, hidden, elem):
     if name.startswith("bulk_row"):
         stages = int(name.split("_s")[1])
         return A.make_plan(A.KS_KERNEL_BULK_ROW, 4, block, stages)
+    if name.startswith("cluster_row"):
+        c = int(name.split("_c")[1])
+        block = max(32, up32(-(-(-(-hv // c)) // 4)))
+        return A.make_plan(A.KS_KERNEL_CLUSTER_ROW, 4, block, cluster=c)
     return A.make_plan(A.KS_KERNEL_CTA_ROW, v, block, flags=flags)
 
 
 VARIANTS = ["warp_row", "warp_row_np", "cta_row_v2", "cta_row_v2_np", "cta_row_v4",
-            "cta_row_v4_np", "bulk_row_s1", "bulk_row_s2", "bulk_row_s5", "scalar"]
+            "cta_row_v4_np", "bulk_row_s1", "bulk_row_s2", "bulk_row_s5", "cluster_row_c2",
+            "cluster_row_c3", "cluster_row_c8", "scalar"]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -299,3 +304,36 @@ def test_no_device_faults_recorded(cuda_device):
     torch.cuda.synchronize()
     st, flags = A.ks_device_faults(clear=False)
     assert st == A.KS_SUCCESS and flags == 0
+
+
+@pytest.mark.parametrize("cluster", [2, 4, 8])
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
+@pytest.mark.parametrize("rows,hidden", [(1, 16384), (7, 14336), (3, 5120), (500, 4096)])
+def test_cluster_rows_wide_sweep(cuda_device, cluster, op, rows, hidden):
+    """The cluster kernel on the wide sweep's heavy-tailed rows, few rows and many (grid capped
+    to resident clusters, clusters striding over rows)."""
+    from row_wise_rmsnorm_ks_gb300 import _abi as A
+    w = synth.wide_device(op, hidden, rows, "bf16", cuda_device)
+    hv = hidden // 8
+    slice_vectors = -(-hv // cluster)
+    threads = -(-slice_vectors // 4)
+    block = max(32, -(-threads // 32) * 32)
+    plan = A.make_plan(A.KS_KERNEL_CLUSTER_ROW, 4, block, cluster=cluster)
+    s = torch.cuda.current_stream().cuda_stream
+    x_host = w.x.cpu()
+    wd = w.weight.to(cuda_device)
+    name = f"cluster c{cluster} {op} [{rows},{hidden}]"
+    if op == "rms_norm":
+        y = torch.empty_like(w.x)
+        A.check(A.ks_rms_norm_planned(y.data_ptr(), w.x.data_ptr(), wd.data_ptr(), rows, hidden,
+                                      w.eps, A.KS_DTYPE_BF16, plan, s))
+        ref, _ = oracle.rms_norm(x_host, w.weight.cpu(), w.eps)
+        compare_output(y.cpu(), ref, torch.bfloat16, hidden, name)
+    else:
+        r_host = w.residual.cpu()
+        A.check(A.ks_fused_add_rms_norm_planned(w.x.data_ptr(), w.residual.data_ptr(),
+                                                wd.data_ptr(), rows, hidden, w.eps,
+                                                A.KS_DTYPE_BF16, plan, s))
+        ref_x, ref_r, _ = oracle.fused_add_rms_norm(x_host, r_host, w.weight.cpu(), w.eps)
+        assert bits_equal(w.residual.cpu(), ref_r)
+        compare_output(w.x.cpu(), ref_x, torch.bfloat16, hidden, name)

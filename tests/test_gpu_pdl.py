@@ -37,6 +37,8 @@ KERNELS = {
                                            flags=f | _abi.KS_PLAN_NO_PREFETCH),
     "bulk_row": lambda f: _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 64, stages=2, flags=f),
     "scalar": lambda f: _abi.make_plan(_abi.KS_KERNEL_SCALAR, 0, 128, flags=f),
+    "cluster_row": lambda f: _abi.make_plan(_abi.KS_KERNEL_CLUSTER_ROW, 2, 32, flags=f,
+                                            cluster=4),
 }
 
 

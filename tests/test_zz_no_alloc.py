@@ -49,6 +49,10 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device, dtype, rows, h
         assert ok, f"call {call}: normalised output beyond tolerance by {worst}"
         if dtype != torch.float32:
             assert int(ulp_dist(xb, xa).max()) <= 1
+        # the next call starts both paths from the same rows (the scratch still holds this
+        # call's chunks): its results must again agree
+        xb.copy_(xa)
+        rb.copy_(ra)
 
 
 def test_noalloc_rejects_rows_wider_than_its_scratch(cuda_device):
