@@ -8,8 +8,10 @@ method's arithmetic.
 
 The arithmetic lives in ``ks_oracle.c`` (plain C, single-threaded, built with no FMA
 contraction). This module only marshals CPU torch tensors into it. Each function follows
-Kernscope, "Numerical contract" (RMSNorm; Fused residual-add RMSNorm); the readings taken where
-the contract is silent are listed at the top of ``ks_oracle.c``.
+Kernscope, "Numerical contract" (RMSNorm; Fused residual-add RMSNorm; SwiGLU activation;
+Softmax) or, for LayerNorm (only named on kernel-set's operator list), the standard definition
+with the same FP32 discipline; the readings taken where a contract is silent are listed at the
+top of ``ks_oracle.c`` and beside each function.
 
 Parity pins: every function here is pinned by the ``-m "not gpu"`` tests
 (tests/test_oracle_*.py) against exact rationals, closed forms, invariants, a float64 brute
@@ -47,6 +49,12 @@ def _load():
         lib.oracle_encode.restype = None
         lib.oracle_rsqrt.argtypes = [p, p, i64]
         lib.oracle_rsqrt.restype = None
+        lib.oracle_silu_and_mul.argtypes = [p, p, p, i64, i64, c_int]
+        lib.oracle_silu_and_mul.restype = None
+        lib.oracle_softmax.argtypes = [p, p, p, i64, i64, c_int]
+        lib.oracle_softmax.restype = None
+        lib.oracle_layer_norm.argtypes = [p, p, p, p, p, i64, i64, f32, c_int]
+        lib.oracle_layer_norm.restype = None
         lib.oracle_version.restype = c_int
         _lib = lib
     return _lib
@@ -117,6 +125,56 @@ def fused_add_rms_norm_f64(x: torch.Tensor, residual: torch.Tensor, weight: torc
     lib.oracle_fused_add_rms_norm_f64(x2.data_ptr(), r2.data_ptr(), w.data_ptr(), yd.data_ptr(),
                                       sd.data_ptr(), x2.shape[0], H, eps32, _CODES[x.dtype])
     return yd.reshape(x.shape), sd.reshape(x.shape)
+
+
+def silu_and_mul(x: torch.Tensor):
+    """SwiGLU per Kernscope's contract on x of shape (..., 2d). Returns (out, u): out of shape
+    (..., d) in x's dtype, u the fp32 values before the cast."""
+    lib = _load()
+    if x.device.type != "cpu" or x.dtype not in _CODES or x.shape[-1] % 2:
+        raise ValueError("x must be a CPU fp16/bf16/fp32 tensor with an even last dimension")
+    d = x.shape[-1] // 2
+    x2 = x.reshape(-1, 2 * d).contiguous()
+    out = torch.empty((x2.shape[0], d), dtype=x.dtype)
+    u = torch.empty((x2.shape[0], d), dtype=torch.float32)
+    lib.oracle_silu_and_mul(x2.data_ptr(), out.data_ptr(), u.data_ptr(), x2.shape[0], d,
+                            _CODES[x.dtype])
+    shape = tuple(x.shape[:-1]) + (d,)
+    return out.reshape(shape), u.reshape(shape)
+
+
+def softmax(x: torch.Tensor):
+    """Softmax over the last axis per Kernscope's contract. Returns (out, u)."""
+    lib = _load()
+    if x.device.type != "cpu" or x.dtype not in _CODES or x.shape[-1] == 0:
+        raise ValueError("x must be a CPU fp16/bf16/fp32 tensor with a non-empty last dimension")
+    H = x.shape[-1]
+    x2 = x.reshape(-1, H).contiguous()
+    out = torch.empty_like(x2)
+    u = torch.empty(x2.shape, dtype=torch.float32)
+    lib.oracle_softmax(x2.data_ptr(), out.data_ptr(), u.data_ptr(), x2.shape[0], H,
+                       _CODES[x.dtype])
+    return out.reshape(x.shape), u.reshape(x.shape)
+
+
+def layer_norm(x: torch.Tensor, weight: torch.Tensor | None, bias: torch.Tensor | None,
+               eps: float = 1e-5):
+    """LayerNorm over the last axis (the standard definition, FP32 steps). Returns (out, u)."""
+    lib = _load()
+    H = x.shape[-1]
+    for t in (weight, bias):
+        if t is not None and (t.dtype != x.dtype or t.numel() != H or t.device.type != "cpu"):
+            raise ValueError("weight and bias must be CPU tensors of x's dtype and shape (H,)")
+    x2 = x.reshape(-1, H).contiguous()
+    out = torch.empty_like(x2)
+    u = torch.empty(x2.shape, dtype=torch.float32)
+    keep = (weight.contiguous() if weight is not None else None,
+            bias.contiguous() if bias is not None else None)
+    wp = keep[0].data_ptr() if keep[0] is not None else None
+    bp = keep[1].data_ptr() if keep[1] is not None else None
+    lib.oracle_layer_norm(x2.data_ptr(), wp, bp, out.data_ptr(), u.data_ptr(), x2.shape[0], H,
+                          float(eps), _CODES[x.dtype])
+    return out.reshape(x.shape), u.reshape(x.shape)
 
 
 def decode(t: torch.Tensor) -> torch.Tensor:

@@ -1,5 +1,6 @@
 /*
- * ks_oracle.c -- the CPU oracle for row-wise RMSNorm and the fused residual-add RMSNorm.
+ * ks_oracle.c -- the CPU oracle for row-wise RMSNorm and the fused residual-add RMSNorm, and for
+ * the next operators of the same library: SwiGLU (silu_and_mul), Softmax and LayerNorm.
  *
  * TEST INFRASTRUCTURE. This file is the plain, slow, single-threaded definition that the CUDA
  * path is checked against. Only the test suite, the smoke check and the CPU-baseline leg of
@@ -300,6 +301,102 @@ void oracle_fused_add_rms_norm_f64(const void *x, const void *r, const void *w, 
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* The next operators of the same library (Kernscope, "Numerical contract": SwiGLU activation,  */
+/* Softmax; kernel-set, "Operators": LayerNorm, named only).                                   */
+/* ------------------------------------------------------------------------------------------ */
+
+/* fp32 exp, read as the correctly rounded value of e^v: exp in double rounded once to fp32 (a
+ * double rounding could differ only within 2^-29 of a midpoint). */
+static float exp_rn(float v) { return (float)exp((double)v); }
+
+/*
+ * SwiGLU, Kernscope "Numerical contract / SwiGLU activation": for x of shape [rows, 2d],
+ * gate = fp32(x[:, :d]), up = fp32(x[:, d:]), out = cast(gate * sigmoid(gate) * up), FP32
+ * intermediates. Read as sigmoid(g) = 1 / (1 + exp(-g)) and the products left to right:
+ * ((g * sigmoid(g)) * up). u (optional) receives the fp32 value before the cast.
+ */
+void oracle_silu_and_mul(const void *x, void *out, float *u, int64_t rows, int64_t d, int dtype) {
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t j = 0; j < d; ++j) {
+            float g = (float)load_elem(x, i * 2 * d + j, dtype);
+            float up = (float)load_elem(x, i * 2 * d + d + j, dtype);
+            float e = exp_rn(-g);
+            float den = 1.0f + e;
+            float sig = 1.0f / den;
+            float a = g * sig;
+            float o = a * up;
+            if (u) u[i * d + j] = o;
+            store_elem(out, i * d + j, dtype, (double)o);
+        }
+    }
+}
+
+/*
+ * Softmax over the last axis, Kernscope "Numerical contract / Softmax":
+ * z = fp32(x) - max(fp32(x)); out = cast(exp(z) / sum(exp(z))). The maximum propagates NaN (as
+ * the reference's torch.softmax does), which yields the stated non-finite rules literally: a row
+ * with NaN or +inf, or a row that is all -inf, comes out NaN; -inf entries of a row with finite
+ * values come out 0. The sum runs left to right in fp32.
+ */
+void oracle_softmax(const void *x, void *out, float *u, int64_t rows, int64_t H, int dtype) {
+    for (int64_t i = 0; i < rows; ++i) {
+        const int64_t base = i * H;
+        float m = -INFINITY;
+        int nan = 0;
+        for (int64_t j = 0; j < H; ++j) {
+            float v = (float)load_elem(x, base + j, dtype);
+            if (isnan(v)) nan = 1;
+            else if (v > m) m = v;
+        }
+        if (nan) m = NAN;
+        float sum = 0.0f;
+        for (int64_t j = 0; j < H; ++j) {
+            float z = (float)load_elem(x, base + j, dtype) - m;
+            sum = sum + exp_rn(z);
+        }
+        for (int64_t j = 0; j < H; ++j) {
+            float z = (float)load_elem(x, base + j, dtype) - m;
+            float o = exp_rn(z) / sum;
+            if (u) u[base + j] = o;
+            store_elem(out, base + j, dtype, (double)o);
+        }
+    }
+}
+
+/*
+ * LayerNorm over the last axis (named on kernel-set's operator list; the contract is read as the
+ * standard definition with the RMSNorm contract's FP32 discipline): mean = sum(x)/H, var =
+ * sum((x - mean)^2)/H (two passes, population variance), rstd = rsqrt(var + eps), and
+ * out = cast((((x - mean) * rstd) * w) + b), every step one fp32 rounding, sums left to right.
+ * w and b may be NULL (then 1 and 0).
+ */
+void oracle_layer_norm(const void *x, const void *w, const void *b, void *out, float *u,
+                       int64_t rows, int64_t H, float eps, int dtype) {
+    for (int64_t i = 0; i < rows; ++i) {
+        const int64_t base = i * H;
+        float s = 0.0f;
+        for (int64_t j = 0; j < H; ++j) s = s + (float)load_elem(x, base + j, dtype);
+        float mean = s / (float)H;
+        float q = 0.0f;
+        for (int64_t j = 0; j < H; ++j) {
+            float dlt = (float)load_elem(x, base + j, dtype) - mean;
+            float sq = dlt * dlt;
+            q = q + sq;
+        }
+        float var = q / (float)H;
+        float rstd = rsqrt_rn(var + eps);
+        for (int64_t j = 0; j < H; ++j) {
+            float dlt = (float)load_elem(x, base + j, dtype) - mean;
+            float t = dlt * rstd;
+            if (w) t = t * (float)load_elem(w, j, dtype);
+            if (b) t = t + (float)load_elem(b, j, dtype);
+            if (u) u[base + j] = t;
+            store_elem(out, base + j, dtype, (double)t);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Array helpers exposed for the pins.                                                         */
 /* ------------------------------------------------------------------------------------------ */
 
@@ -316,4 +413,4 @@ void oracle_rsqrt(const float *v, float *out, int64_t n) {
 }
 
 /* Bumped whenever the arithmetic above changes, so stale builds are detected. */
-int oracle_version(void) { return 1; }
+int oracle_version(void) { return 2; }
