@@ -252,6 +252,42 @@ ks_status_t ks_fused_add_rms_norm_host_noalloc(void *x, void *residual, const vo
 ks_status_t ks_set_launch_options(int32_t options);
 int32_t ks_get_launch_options(void);
 
+/*
+ * SwiGLU activation (Kernscope, "Numerical contract / SwiGLU activation"): for x of shape
+ * [rows, 2d], gate = fp32(x[:, :d]), up = fp32(x[:, d:]),
+ * out[:, j] = cast((gate_j * sigmoid(gate_j)) * up_j) with sigmoid(g) = 1 / (1 + exp(-g)), FP32
+ * throughout (exp within 2 ulp, the reciprocal an IEEE division).
+ *   out  device pointer, [rows, d], must not overlap x.
+ *   x    device pointer, [rows, 2d], read-only.
+ *   rows >= 0 (0: nothing launched); d > 0 (it may be odd).
+ * Errors as for ks_rms_norm (KS_ERR_OVERLAP if out overlaps x).
+ */
+ks_status_t ks_silu_and_mul(void *out, const void *x, int64_t rows, int64_t d, ks_dtype_t dtype,
+                            ks_stream_t stream);
+
+/*
+ * Softmax over the last axis (Kernscope, "Numerical contract / Softmax"):
+ * z = fp32(x) - max(fp32(x)), out = cast(exp(z) / sum(exp(z))). A row with NaN or +inf, or a
+ * row that is all -inf, comes out NaN; -inf entries of a row with finite values come out 0.
+ *   out  device pointer, [rows, hidden]; may be exactly x.
+ *   x    device pointer, [rows, hidden].
+ *   rows >= 0, hidden > 0. Errors as for ks_rms_norm.
+ */
+ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, ks_dtype_t dtype,
+                       ks_stream_t stream);
+
+/*
+ * LayerNorm over the last axis (named on kernel-set's operator list, "Operators"; read as the
+ * standard definition with FP32 steps): mean = sum(x)/H, var = sum((x - mean)^2)/H, rstd =
+ * rsqrt(var + eps) correctly rounded, out = cast((((x - mean) * rstd) * w) + b).
+ *   out           device pointer, [rows, hidden]; may be exactly x.
+ *   weight, bias  device pointers, [hidden], or NULL (then 1 and 0); read-only.
+ *   eps           finite, > 0. Errors as for ks_rms_norm.
+ */
+ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const void *bias,
+                          int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype,
+                          ks_stream_t stream);
+
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t ks_version(void);
 

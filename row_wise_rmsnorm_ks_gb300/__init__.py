@@ -6,8 +6,8 @@ sizes and never computes anything itself. There is no CPU fallback: without the 
 every op raises ``KsLibraryMissing``.
 """
 from ._abi import KsError, KsLibraryMissing  # noqa: F401
-from .ops import (fused_add_rms_norm, fused_add_rms_norm_host, rms_norm,  # noqa: F401
-                  rms_norm_host)
+from .ops import (fused_add_rms_norm, fused_add_rms_norm_host, layer_norm,  # noqa: F401
+                  rms_norm, rms_norm_host, silu_and_mul, softmax)
 
 __all__ = ["rms_norm", "fused_add_rms_norm", "rms_norm_host", "fused_add_rms_norm_host",
-           "KsError", "KsLibraryMissing"]
+           "silu_and_mul", "softmax", "layer_norm", "KsError", "KsLibraryMissing"]

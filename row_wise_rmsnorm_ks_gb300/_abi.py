@@ -29,7 +29,8 @@ EXPORTED = ("ks_rms_norm", "ks_fused_add_rms_norm", "ks_status_string", "ks_last
             "ks_plan_launch", "ks_rms_norm_planned", "ks_fused_add_rms_norm_planned",
             "ks_device_faults", "ks_rms_norm_host", "ks_fused_add_rms_norm_host",
             "ks_host_chunk_rows", "ks_fused_add_rms_norm_host_noalloc", "ks_set_launch_options",
-            "ks_get_launch_options", "ks_version")
+            "ks_get_launch_options", "ks_silu_and_mul", "ks_softmax", "ks_layer_norm",
+            "ks_version")
 
 
 class KsLibraryMissing(RuntimeError):
@@ -107,6 +108,12 @@ def load(path: str | None = None):
         lib.ks_set_launch_options.restype = ctypes.c_int
         lib.ks_get_launch_options.argtypes = []
         lib.ks_get_launch_options.restype = i32
+        lib.ks_silu_and_mul.argtypes = [vp, vp, i64, i64, ctypes.c_int, vp]
+        lib.ks_silu_and_mul.restype = ctypes.c_int
+        lib.ks_softmax.argtypes = [vp, vp, i64, i64, ctypes.c_int, vp]
+        lib.ks_softmax.restype = ctypes.c_int
+        lib.ks_layer_norm.argtypes = [vp, vp, vp, vp, i64, i64, f32, ctypes.c_int, vp]
+        lib.ks_layer_norm.restype = ctypes.c_int
         lib.ks_version.argtypes = []
         lib.ks_version.restype = i32
         _lib = lib
@@ -199,6 +206,19 @@ def ks_set_launch_options(options: int) -> int:
 
 def ks_get_launch_options() -> int:
     return load().ks_get_launch_options()
+
+
+def ks_silu_and_mul(out: int, x: int, rows: int, d: int, dtype: int, stream: int | None) -> int:
+    return load().ks_silu_and_mul(out, x, rows, d, dtype, stream)
+
+
+def ks_softmax(out: int, x: int, rows: int, hidden: int, dtype: int, stream: int | None) -> int:
+    return load().ks_softmax(out, x, rows, hidden, dtype, stream)
+
+
+def ks_layer_norm(out: int, x: int, weight: int | None, bias: int | None, rows: int, hidden: int,
+                  eps: float, dtype: int, stream: int | None) -> int:
+    return load().ks_layer_norm(out, x, weight, bias, rows, hidden, eps, dtype, stream)
 
 
 def ks_version() -> int:

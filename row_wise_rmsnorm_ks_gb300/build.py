@@ -19,8 +19,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libks.so")
-SOURCES = ["ks_abi.cu", "ks_host.cu", "ks_noalloc.cu", "ks_launch_bf16.cu", "ks_launch_f16.cu",
-           "ks_launch_f32.cu"]
+SOURCES = ["ks_abi.cu", "ks_host.cu", "ks_noalloc.cu", "ks_ops.cu", "ks_launch_bf16.cu",
+           "ks_launch_f16.cu", "ks_launch_f32.cu"]
 HEADERS = ["ks_kernels.cuh", "ks_internal.h", "ks_ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

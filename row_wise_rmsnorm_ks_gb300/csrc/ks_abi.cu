@@ -47,6 +47,10 @@ bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool launch_pdl_enabled() {
+    return (g_launch_options.load(std::memory_order_relaxed) & KS_LAUNCH_PDL) != 0;
+}
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // ---------------------------------------------------------------- per-device caches

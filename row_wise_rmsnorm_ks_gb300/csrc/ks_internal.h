@@ -39,6 +39,9 @@ ks_status_t run_host(bool fused, void *out, const void *x, void *res, const void
 // Rows per staged chunk for a workspace of ws_bytes (0 if a slot holds no row).
 int64_t host_chunk_rows(bool fused, int64_t hidden, int e, int64_t ws_bytes);
 
+// Whether ks_set_launch_options turned programmatic dependent launch on.
+bool launch_pdl_enabled();
+
 // Host heuristic: fills *p from the shape, the element size and the device's SM count.
 // blocks_per_sm == 0 leaves grid at one pass over the rows.
 ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem_bytes, bool aligned16,

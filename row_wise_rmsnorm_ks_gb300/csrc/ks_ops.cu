@@ -1,0 +1,532 @@
+// The next operators of the library on sm_103a: SwiGLU (silu_and_mul), row-wise Softmax and
+// LayerNorm, with their C entry points. All three are memory-bound row or element streams; they
+// reuse the RMSNorm kernels' element traits, streaming loads and stores, and the two-slot CTA
+// reductions.
+//
+// Arithmetic:
+//  * SwiGLU (Kernscope, "Numerical contract / SwiGLU activation"): gate = fp32(x[:, :d]),
+//    up = fp32(x[:, d:]), out = cast((gate * (1 / (1 + exp(-gate)))) * up), FP32 throughout;
+//    exp is CUDA's expf (within 2 ulp), the reciprocal an IEEE division.
+//  * Softmax (Kernscope, "Numerical contract / Softmax"): z = fp32(x) - max(fp32(x)),
+//    out = cast(exp(z) / sum(exp(z))). The row maximum propagates NaN, which gives the contract's
+//    non-finite rules directly: a row with NaN or +inf, or a row all -inf, comes out NaN; -inf
+//    entries of a row with finite values come out 0. exp(z) is computed once per element and kept
+//    in registers; each output is one IEEE division.
+//  * LayerNorm (named on kernel-set's operator list; read as the standard definition with FP32
+//    steps): mean = sum(x)/H, var = sum((x-mean)^2)/H (two reductions over the register-resident
+//    row), rstd = correctly rounded rsqrt(var + eps), out = cast((((x-mean)*rstd)*w) + b); w and b
+//    optional.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+#include <unordered_map>
+
+#include "ks_kernels.cuh"
+
+namespace ks {
+namespace {
+
+// ---------------------------------------------------------------------------- reductions
+
+__device__ __forceinline__ float nan_max(float a, float b) {
+    return (a != a) ? a : ((b != b) ? b : fmaxf(a, b));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = nan_max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// CTA-wide sum / NaN-propagating max; every thread returns the same value. `slot` alternates
+// between two 32-float rows of `red` on every reduction: a warp writes a slot again only after
+// the next reduction's barrier, which every warp passes only after reading this one.
+__device__ __forceinline__ float cta_sum(float v, float (*red)[32], int &slot) {
+    v = warp_sum(v);
+    if ((threadIdx.x & 31) == 0) red[slot][threadIdx.x >> 5] = v;
+    __syncthreads();
+    float s = 0.0f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s += red[slot][i];
+    slot ^= 1;
+    return s;
+}
+
+__device__ __forceinline__ float cta_max(float v, float (*red)[32], int &slot) {
+    v = warp_max(v);
+    if ((threadIdx.x & 31) == 0) red[slot][threadIdx.x >> 5] = v;
+    __syncthreads();
+    float m = -INFINITY;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = nan_max(m, red[slot][i]);
+    slot ^= 1;
+    return m;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float up) {
+    const float sig = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+    return __fmul_rn(__fmul_rn(g, sig), up);
+}
+
+// ------------------------------------------------------------------------------- SwiGLU
+
+// Vector path: rows of d elements as dv = d / E 16-byte vectors in the gate half and the up half
+// of each input row. blockIdx.y strides over rows, the x dimension over a row's vectors.
+template <typename T>
+__global__ void __launch_bounds__(256) silu_mul_vec_kernel(void *out, const void *x, int64_t rows,
+                                                           int64_t dv) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const uint4 *xg = static_cast<const uint4 *>(x);
+    uint4 *og = static_cast<uint4 *>(out);
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+        const uint4 *gate = xg + row * 2 * dv;
+        const uint4 *up = gate + dv;
+        uint4 *o = og + row * dv;
+        int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        // two vectors per thread per iteration, loads issued before the math
+        for (; c + step < dv; c += 2 * step) {
+            const uint4 g0 = __ldcs(gate + c), u0 = __ldcs(up + c);
+            const uint4 g1 = __ldcs(gate + c + step), u1 = __ldcs(up + c + step);
+            float a[N], b[N], r[N];
+            E::unpack(g0, a);
+            E::unpack(u0, b);
+#pragma unroll
+            for (int e = 0; e < N; ++e) r[e] = silu_mul(a[e], b[e]);
+            __stcs(o + c, E::pack(r));
+            E::unpack(g1, a);
+            E::unpack(u1, b);
+#pragma unroll
+            for (int e = 0; e < N; ++e) r[e] = silu_mul(a[e], b[e]);
+            __stcs(o + c + step, E::pack(r));
+        }
+        if (c < dv) {
+            float a[N], b[N], r[N];
+            E::unpack(__ldcs(gate + c), a);
+            E::unpack(__ldcs(up + c), b);
+#pragma unroll
+            for (int e = 0; e < N; ++e) r[e] = silu_mul(a[e], b[e]);
+            __stcs(o + c, E::pack(r));
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) silu_mul_scalar_kernel(void *out, const void *x,
+                                                              int64_t rows, int64_t d) {
+    using E = Elem<T>;
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+        for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < d; j += step) {
+            const float g = E::load1(x, row * 2 * d + j);
+            const float up = E::load1(x, row * 2 * d + d + j);
+            E::store1(out, row * d + j, silu_mul(g, up));
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------ Softmax
+
+// One CTA per row, V 16-byte vectors per thread held in registers; persistent over rows.
+template <typename T, int V>
+__global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void *x, int64_t rows,
+                                                          int64_t hv) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    __shared__ float red[2][32];
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const uint4 *xg = static_cast<const uint4 *>(x);
+    uint4 *og = static_cast<uint4 *>(out);
+    const int t = threadIdx.x, g = blockDim.x;
+    int slot = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        float f[V][N];
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < hv) {
+                E::unpack(__ldcs(xg + row * hv + c), f[k]);
+#pragma unroll
+                for (int e = 0; e < N; ++e) m = nan_max(m, f[k][e]);
+            }
+        }
+        m = cta_max(m, red, slot);
+        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < hv) {
+#pragma unroll
+                for (int e = 0; e < N; ++e) {
+                    f[k][e] = expf(__fsub_rn(f[k][e], m));
+                    s[e & 3] = __fadd_rn(s[e & 3], f[k][e]);
+                }
+            }
+        }
+        const float sum = cta_sum(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])), red, slot);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < hv) {
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[k][e] = __fdiv_rn(f[k][e], sum);
+                __stcs(og + row * hv + c, E::pack(f[k]));
+            }
+        }
+    }
+}
+
+// Any width and alignment: one CTA per row, three passes over the row (max, sum, write); the
+// second and third mostly hit L2. out may be exactly x: each element is read by the thread that
+// writes it, after the row's last read by any other thread (the sum's barrier).
+template <typename T>
+__global__ void __launch_bounds__(1024) softmax_scalar_kernel(void *out, const void *x,
+                                                              int64_t rows, int64_t H) {
+    using E = Elem<T>;
+    __shared__ float red[2][32];
+    grid_dependency_wait();
+    allow_dependents_launch();
+    int slot = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t base = row * H;
+        float m = -INFINITY;
+        for (int64_t j = threadIdx.x; j < H; j += blockDim.x) m = nan_max(m, E::load1(x, base + j));
+        m = cta_max(m, red, slot);
+        float s = 0.0f;
+        for (int64_t j = threadIdx.x; j < H; j += blockDim.x)
+            s = __fadd_rn(s, expf(__fsub_rn(E::load1(x, base + j), m)));
+        const float sum = cta_sum(s, red, slot);
+        for (int64_t j = threadIdx.x; j < H; j += blockDim.x)
+            E::store1(out, base + j, __fdiv_rn(expf(__fsub_rn(E::load1(x, base + j), m)), sum));
+    }
+}
+
+// ---------------------------------------------------------------------------- LayerNorm
+
+template <typename T, int V>
+__global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const void *x,
+                                                             const void *w, const void *b,
+                                                             int64_t rows, int64_t hidden,
+                                                             int64_t hv, float eps) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    __shared__ float red[2][32];
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const uint4 *xg = static_cast<const uint4 *>(x);
+    uint4 *og = static_cast<uint4 *>(out);
+    const int t = threadIdx.x, g = blockDim.x;
+    const float h = (float)hidden;
+    uint4 wv[V], bv[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        const int64_t c = t + (int64_t)k * g;
+        wv[k] = (w && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
+        bv[k] = (b && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    int slot = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        uint4 xv[V];
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            xv[k] = (c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+            float f[N];
+            E::unpack(xv[k], f);
+#pragma unroll
+            for (int e = 0; e < N; ++e) s4[e & 3] = __fadd_rn(s4[e & 3], f[e]);
+        }
+        const float mean = __fdiv_rn(
+            cta_sum(__fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3])), red, slot), h);
+        SumSq q;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < hv) {
+                float f[N];
+                E::unpack(xv[k], f);
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[e] = __fsub_rn(f[e], mean);
+                q.add(f);
+            }
+        }
+        const float var = __fdiv_rn(cta_sum(q.total(), red, slot), h);
+        const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < hv) {
+                float f[N], wf[N], bf[N];
+                E::unpack(xv[k], f);
+                E::unpack(wv[k], wf);
+                E::unpack(bv[k], bf);
+#pragma unroll
+                for (int e = 0; e < N; ++e) {
+                    float v = __fmul_rn(__fsub_rn(f[e], mean), rstd);
+                    if (w) v = __fmul_rn(v, wf[e]);
+                    if (b) v = __fadd_rn(v, bf[e]);
+                    f[e] = v;
+                }
+                __stcs(og + row * hv + c, E::pack(f));
+            }
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(1024) layer_norm_scalar_kernel(void *out, const void *x,
+                                                                 const void *w, const void *b,
+                                                                 int64_t rows, int64_t H,
+                                                                 float eps) {
+    using E = Elem<T>;
+    __shared__ float red[2][32];
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const float h = (float)H;
+    int slot = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const int64_t base = row * H;
+        float s = 0.0f;
+        for (int64_t j = threadIdx.x; j < H; j += blockDim.x) s = __fadd_rn(s, E::load1(x, base + j));
+        const float mean = __fdiv_rn(cta_sum(s, red, slot), h);
+        float q = 0.0f;
+        for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
+            const float d = __fsub_rn(E::load1(x, base + j), mean);
+            q = __fmaf_rn(d, d, q);
+        }
+        const float var = __fdiv_rn(cta_sum(q, red, slot), h);
+        const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
+        for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
+            float v = __fmul_rn(__fsub_rn(E::load1(x, base + j), mean), rstd);
+            if (w) v = __fmul_rn(v, E::load1(w, j));
+            if (b) v = __fadd_rn(v, E::load1(b, j));
+            E::store1(out, base + j, v);
+        }
+    }
+}
+
+// ------------------------------------------------------------------------ launch planning
+
+int g_sm_count[64];
+std::once_flag g_sm_once[64];
+
+ks_status_t sm_count(int *out) {
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
+    if (dev < 0 || dev >= 64) return fail(KS_ERR_CUDA, "device ordinal %d out of range", dev);
+    cudaError_t err = cudaSuccess;
+    std::call_once(g_sm_once[dev], [&] {
+        err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    });
+    if (err != cudaSuccess || g_sm_count[dev] <= 0)
+        return fail(KS_ERR_CUDA, "querying the SM count failed");
+    *out = g_sm_count[dev];
+    return KS_SUCCESS;
+}
+
+int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up64(int64_t a, int64_t b) { return ceil_div64(a, b) * b; }
+
+// Vectors per thread and block for a register-resident row of hv vectors: 1 vector below 64,
+// 2 below 512, else 4; the block a multiple of 32 (at most 512). 0 if the row does not fit.
+int row_vec_plan(int64_t hv, int *block) {
+    const int v = hv < 64 ? 1 : (hv < 512 ? 2 : 4);
+    const int64_t b = round_up64(ceil_div64(hv, v), 32);
+    if (b > 512) return 0;
+    *block = (int)b;
+    return v;
+}
+
+ks_status_t check_common(int64_t rows, int64_t width, ks_dtype_t dtype, int *e) {
+    *e = elem_bytes(dtype);
+    if (*e == 0) return fail(KS_ERR_UNSUPPORTED_DTYPE, "dtype code %d is not a ks_dtype_t", (int)dtype);
+    if (width <= 0) return fail(KS_ERR_INVALID_ARGUMENT, "the last dimension must be > 0 (got %lld)", (long long)width);
+    if (rows < 0) return fail(KS_ERR_INVALID_ARGUMENT, "rows must be >= 0 (got %lld)", (long long)rows);
+    if (width > INT64_MAX / (4 * *e) || (rows > 0 && rows > INT64_MAX / (4 * width * *e)))
+        return fail(KS_ERR_INVALID_ARGUMENT, "rows*width*element size overflows int64");
+    return KS_SUCCESS;
+}
+
+cudaError_t launch(const void *f, dim3 grid, dim3 block, void **args, cudaStream_t s) {
+    if (launch_pdl_enabled()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelExC(&cfg, f, args);
+    }
+    return cudaLaunchKernel(f, grid, block, args, 0, s);
+}
+
+template <typename T>
+cudaError_t silu_dispatch(bool vec, void *out, const void *x, int64_t rows, int64_t d, int sms,
+                          cudaStream_t s) {
+    const int64_t per_row = vec ? d / Elem<T>::kPerVec : d;
+    const int block = 256;
+    // columns: enough CTAs to cover a row's vectors twice per thread; rows: fill ~8 waves of SMs
+    int64_t gx = ceil_div64(per_row, (int64_t)block * (vec ? 2 : 1));
+    gx = gx < 1 ? 1 : gx;
+    int64_t gy = (int64_t)sms * 8 / gx;
+    gy = gy < 1 ? 1 : (gy > rows ? rows : gy);
+    gy = gy > 65535 ? 65535 : gy;
+    int64_t nr = rows, dd = per_row;
+    void *args[] = {&out, const_cast<void **>(&x), &nr, &dd};
+    const void *f = vec ? (const void *)silu_mul_vec_kernel<T> : (const void *)silu_mul_scalar_kernel<T>;
+    return launch(f, dim3((unsigned)gx, (unsigned)gy), dim3(block), args, s);
+}
+
+template <typename T>
+cudaError_t softmax_dispatch(int v, int block, void *out, const void *x, int64_t rows,
+                             int64_t width, int sms, cudaStream_t s) {
+    int64_t nr = rows, wd = width;
+    void *args[] = {&out, const_cast<void **>(&x), &nr, &wd};
+    const void *f;
+    switch (v) {
+    case 1: f = (const void *)softmax_vec_kernel<T, 1>; break;
+    case 2: f = (const void *)softmax_vec_kernel<T, 2>; break;
+    case 4: f = (const void *)softmax_vec_kernel<T, 4>; break;
+    default:
+        f = (const void *)softmax_scalar_kernel<T>;
+        block = (int)round_up64(ceil_div64(width, 8), 32);
+        block = block < 32 ? 32 : (block > 1024 ? 1024 : block);
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, 0) != cudaSuccess || n < 1) n = 1;
+    int64_t grid = (int64_t)sms * n;
+    grid = grid > rows ? rows : grid;
+    return launch(f, dim3((unsigned)grid), dim3(block), args, s);
+}
+
+template <typename T>
+cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, const void *w,
+                                const void *b, int64_t rows, int64_t hidden, int64_t hv,
+                                float eps, int sms, cudaStream_t s) {
+    int64_t nr = rows, hd = hidden, hvv = hv;
+    float ep = eps;
+    const void *f;
+    void *vec_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
+                        const_cast<void **>(&b), &nr, &hd, &hvv, &ep};
+    void *sc_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
+                       const_cast<void **>(&b), &nr, &hd, &ep};
+    void **args = vec_args;
+    switch (v) {
+    case 1: f = (const void *)layer_norm_vec_kernel<T, 1>; break;
+    case 2: f = (const void *)layer_norm_vec_kernel<T, 2>; break;
+    case 4: f = (const void *)layer_norm_vec_kernel<T, 4>; break;
+    default:
+        f = (const void *)layer_norm_scalar_kernel<T>;
+        args = sc_args;
+        block = (int)round_up64(ceil_div64(hidden, 8), 32);
+        block = block < 32 ? 32 : (block > 1024 ? 1024 : block);
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, 0) != cudaSuccess || n < 1) n = 1;
+    int64_t grid = (int64_t)sms * n;
+    grid = grid > rows ? rows : grid;
+    return launch(f, dim3((unsigned)grid), dim3(block), args, s);
+}
+
+}  // namespace
+}  // namespace ks
+
+using namespace ks;
+
+extern "C" {
+
+ks_status_t ks_silu_and_mul(void *out, const void *x, int64_t rows, int64_t d, ks_dtype_t dtype,
+                            ks_stream_t stream) {
+    int e = 0;
+    ks_status_t st = check_common(rows, d, dtype, &e);
+    if (st != KS_SUCCESS) return st;
+    if (rows == 0) return KS_SUCCESS;
+    if (!out || !x) return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    if (overlaps(out, rows * d * e, x, rows * 2 * d * e))
+        return fail(KS_ERR_OVERLAP, "out and x storage overlap");
+    int sms = 0;
+    if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
+    const bool vec = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0 && (d * e) % 16 == 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t ce;
+    switch (dtype) {
+    case KS_DTYPE_BF16: ce = silu_dispatch<__nv_bfloat16>(vec, out, x, rows, d, sms, s); break;
+    case KS_DTYPE_F16: ce = silu_dispatch<__half>(vec, out, x, rows, d, sms, s); break;
+    default: ce = silu_dispatch<float>(vec, out, x, rows, d, sms, s); break;
+    }
+    if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
+    return KS_SUCCESS;
+}
+
+ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, ks_dtype_t dtype,
+                       ks_stream_t stream) {
+    int e = 0;
+    ks_status_t st = check_common(rows, hidden, dtype, &e);
+    if (st != KS_SUCCESS) return st;
+    if (rows == 0) return KS_SUCCESS;
+    if (!out || !x) return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    const int64_t nbytes = rows * hidden * e;
+    if (out != x && overlaps(out, nbytes, x, nbytes))
+        return fail(KS_ERR_OVERLAP, "out partially overlaps x (only out == x is allowed)");
+    int sms = 0;
+    if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
+    const bool aligned = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0 && (hidden * e) % 16 == 0;
+    int block = 0, v = 0;
+    int64_t width = hidden;
+    if (aligned && (v = row_vec_plan(hidden * e / 16, &block)) > 0) width = hidden * e / 16;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t ce;
+    switch (dtype) {
+    case KS_DTYPE_BF16: ce = softmax_dispatch<__nv_bfloat16>(v, block, out, x, rows, width, sms, s); break;
+    case KS_DTYPE_F16: ce = softmax_dispatch<__half>(v, block, out, x, rows, width, sms, s); break;
+    default: ce = softmax_dispatch<float>(v, block, out, x, rows, width, sms, s); break;
+    }
+    if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
+    return KS_SUCCESS;
+}
+
+ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const void *bias,
+                          int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype,
+                          ks_stream_t stream) {
+    int e = 0;
+    ks_status_t st = check_common(rows, hidden, dtype, &e);
+    if (st != KS_SUCCESS) return st;
+    if (!std::isfinite(eps) || !(eps > 0.0f))
+        return fail(KS_ERR_INVALID_ARGUMENT, "eps must be finite and > 0 (got %g)", (double)eps);
+    if (rows == 0) return KS_SUCCESS;
+    if (!out || !x) return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    const int64_t nbytes = rows * hidden * e, pbytes = hidden * e;
+    if (out != x && overlaps(out, nbytes, x, nbytes))
+        return fail(KS_ERR_OVERLAP, "out partially overlaps x (only out == x is allowed)");
+    if ((weight && overlaps(out, nbytes, weight, pbytes)) || (bias && overlaps(out, nbytes, bias, pbytes)))
+        return fail(KS_ERR_OVERLAP, "out overlaps weight or bias storage");
+    int sms = 0;
+    if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
+    const uintptr_t al = (uintptr_t)out | (uintptr_t)x | (uintptr_t)weight | (uintptr_t)bias;
+    const bool aligned = (al & 15u) == 0 && (hidden * e) % 16 == 0;
+    int block = 0, v = 0;
+    const int64_t hv = hidden * e / 16;
+    if (aligned) v = row_vec_plan(hv, &block);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t ce;
+    switch (dtype) {
+    case KS_DTYPE_BF16: ce = layer_norm_dispatch<__nv_bfloat16>(v, block, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
+    case KS_DTYPE_F16: ce = layer_norm_dispatch<__half>(v, block, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
+    default: ce = layer_norm_dispatch<float>(v, block, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
+    }
+    if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
+    return KS_SUCCESS;
+}
+
+}  // extern "C"

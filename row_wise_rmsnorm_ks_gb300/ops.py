@@ -154,3 +154,73 @@ def fused_add_rms_norm_host(x: torch.Tensor, residual: torch.Tensor, weight: tor
                                                    _DTYPES[x.dtype], *_ws(workspace),
                                                    _stream(weight.device)))
     return None
+
+
+# ------------------------------------------------------------------ the next operators
+
+def _check_plain(x: torch.Tensor, name="x"):
+    if not isinstance(x, torch.Tensor) or x.dtype not in _DTYPES:
+        raise TypeError(f"{name} must be a float16, bfloat16 or float32 tensor")
+    if x.device.type != "cuda":
+        raise ValueError("tensors must be CUDA tensors (there is no CPU path)")
+    if not x.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    if x.dim() < 1 or x.shape[-1] == 0:
+        raise ValueError("the last dimension must be non-empty")
+    if torch.is_grad_enabled() and x.requires_grad:
+        raise RuntimeError("these kernels are inference-only: inputs must not require grad")
+
+
+def silu_and_mul(x: torch.Tensor) -> torch.Tensor:
+    """SwiGLU (Kernscope, "Numerical contract / SwiGLU activation"): x of shape (..., 2D) gives
+    cast(gate * sigmoid(gate) * up) of shape (..., D), gate = x[..., :D], up = x[..., D:], FP32
+    throughout. x is read-only; D may be odd; leading dimensions may be empty."""
+    _check_plain(x)
+    if x.shape[-1] % 2:
+        raise ValueError("the last dimension of x must be even")
+    d = x.shape[-1] // 2
+    out = torch.empty(tuple(x.shape[:-1]) + (d,), dtype=x.dtype, device=x.device)
+    rows = x.numel() // x.shape[-1]
+    with torch.cuda.device(x.device):
+        _abi.check(_abi.ks_silu_and_mul(out.data_ptr(), x.data_ptr(), rows, d, _DTYPES[x.dtype],
+                                        _stream(x.device)))
+    return out
+
+
+def softmax(x: torch.Tensor, *, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Softmax over the last dimension (Kernscope, "Numerical contract / Softmax"), FP32
+    max/exp/sum/divide, cast back; rows with NaN or +inf, or all -inf, come out NaN."""
+    _check_plain(x)
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype or out.device != x.device:
+        raise ValueError("out must match x in shape, dtype and device")
+    hidden = x.shape[-1]
+    with torch.cuda.device(x.device):
+        _abi.check(_abi.ks_softmax(out.data_ptr(), x.data_ptr(), x.numel() // hidden, hidden,
+                                   _DTYPES[x.dtype], _stream(x.device)))
+    return out
+
+
+def layer_norm(x: torch.Tensor, weight: torch.Tensor | None = None,
+               bias: torch.Tensor | None = None, eps: float = 1e-5, *,
+               out: torch.Tensor | None = None) -> torch.Tensor:
+    """LayerNorm over the last dimension with FP32 steps:
+    cast((((x - mean) * rsqrt(var + eps)) * weight) + bias); weight and bias optional."""
+    _check_plain(x)
+    hidden = x.shape[-1]
+    for t, n in ((weight, "weight"), (bias, "bias")):
+        if t is not None and (t.dtype != x.dtype or t.device != x.device or t.dim() != 1
+                              or t.shape[0] != hidden or not t.is_contiguous()):
+            raise ValueError(f"{n} must be a contiguous ({hidden},) tensor of x's dtype and device")
+    if not (isinstance(eps, (int, float)) and math.isfinite(eps) and eps > 0):
+        raise ValueError("eps must be finite and positive")
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(x.device):
+        _abi.check(_abi.ks_layer_norm(out.data_ptr(), x.data_ptr(),
+                                      weight.data_ptr() if weight is not None else None,
+                                      bias.data_ptr() if bias is not None else None,
+                                      x.numel() // hidden, hidden, float(eps), _DTYPES[x.dtype],
+                                      _stream(x.device)))
+    return out

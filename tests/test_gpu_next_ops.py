@@ -1,0 +1,163 @@
+"""GPU parity of SwiGLU, Softmax and LayerNorm (through the C ABI) against the oracle.
+
+Shapes from the pages: SwiGLU 8 x 2*4096 (Kernscope "Quick start"), 512 x 8192 in / 512 x 4096
+out and rows 1..512 x widths 1024..8192 (Kernscope "SwiGLU baseline"), 128 x 1024 .. 2048 x 4096
+(Triton Kernel Lab "Measured Result"); Softmax 512 x 128 .. 512 x 1024 (Kernscope "Softmax
+measurements"), widths 1..16384 and a 65536-column fp16 row, non-finite rows (Kernscope
+"Correctness"); LayerNorm on the RMSNorm shapes. Outputs within 1 ulp and the tolerance gate
+(LayerNorm: 1 ulp away from zero, the gate near it, where the bias cancels).
+"""
+import pytest
+import torch
+
+import oracle
+import row_wise_rmsnorm_ks_gb300 as ks
+from gpu_common import compare_output, record
+from helpers import bits_equal, tol_for, ulp_dist, within_tol
+from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+pytestmark = pytest.mark.gpu
+DT = ["bf16", "fp16", "fp32"]
+
+
+# ----------------------------------------------------------------------------------- SwiGLU
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("rows,d", [(8, 4096), (512, 4096), (1, 1024), (16, 8192), (128, 1024),
+                                    (3, 7), (5, 1), (33, 1001), (0, 16), (2048, 4096)])
+def test_silu_and_mul(cuda_device, dtype, rows, d):
+    dt = synth.dtype_of(dtype)
+    x = synth.cast(synth.normal_np((rows, 2 * d), 801, std=2.0), dt)
+    y = ks.silu_and_mul(x.to(cuda_device))
+    assert y.shape == (rows, d)
+    if rows:
+        ref, _ = oracle.silu_and_mul(x)
+        # fp32 bound (8+4)*2^-24: expf within 2 ulp plus three roundings
+        compare_output(y.cpu(), ref, dt, 8, f"silu_and_mul {dtype} [{rows},{d}]")
+
+
+def test_silu_and_mul_extremes_and_views(cuda_device):
+    g = torch.tensor([[0.0, 30.0, -30.0, 100.0, -100.0, float("inf"), float("-inf"), 2.0]])
+    up = torch.tensor([[7.0, 3.0, 5.0, -2.0, 4.0, 1.0, 1.0, 0.0]])
+    x = torch.cat([g, up], dim=1)
+    y = ks.silu_and_mul(x.to(cuda_device)).cpu()
+    ref, _ = oracle.silu_and_mul(x)
+    assert torch.equal(torch.isnan(y), torch.isnan(ref))
+    fin = ~torch.isnan(ref)
+    ok, worst, _ = within_tol(y[fin], ref[fin], 1e-6, 1e-30)
+    assert ok, worst
+    # a contiguous view that starts one element in: unaligned, scalar path
+    base = synth.cast(synth.normal_np((4 * 2 * 64 + 1,), 5), torch.bfloat16).to(cuda_device)
+    xv = base[1:].view(4, 128)
+    yv = ks.silu_and_mul(xv).cpu()
+    refv, _ = oracle.silu_and_mul(xv.cpu())
+    compare_output(yv, refv, torch.bfloat16, 1, "silu_and_mul unaligned view")
+
+
+# ----------------------------------------------------------------------------------- Softmax
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("rows,h", [(512, 1024), (512, 128), (2, 5), (7, 1), (3, 63), (100, 4096),
+                                    (4, 16384), (33, 1000), (0, 8), (64, 2048)])
+def test_softmax(cuda_device, dtype, rows, h):
+    dt = synth.dtype_of(dtype)
+    x = synth.cast(synth.normal_np((rows, h), 802, std=3.0), dt)
+    y = ks.softmax(x.to(cuda_device))
+    if rows:
+        ref, _ = oracle.softmax(x)
+        compare_output(y.cpu(), ref, dt, h, f"softmax {dtype} [{rows},{h}]")
+
+
+def test_softmax_wide_fp16(cuda_device):
+    x = synth.cast(synth.normal_np((3, 65536), 803), torch.float16)
+    y = ks.softmax(x.to(cuda_device)).cpu()
+    ref, _ = oracle.softmax(x)
+    compare_output(y, ref, torch.float16, 65536, "softmax fp16 [3,65536]")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("h", [8, 1000])
+def test_softmax_nonfinite_rows(cuda_device, dtype, h):
+    dt = synth.dtype_of(dtype)
+    x = synth.normal_np((6, h), 804)
+    inf, nan = float("inf"), float("nan")
+    x[0, 1] = -inf; x[0, 3] = -inf        # masked entries
+    x[1, 2] = nan                          # NaN row
+    x[2, 0] = inf                          # +inf row
+    x[3, :] = -inf                         # all -inf row
+    x[4, :] = 0.0                          # uniform row
+    xt = synth.cast(x, dt)
+    y = ks.softmax(xt.to(cuda_device)).cpu()
+    ref, _ = oracle.softmax(xt)
+    assert torch.equal(torch.isnan(y), torch.isnan(ref))
+    assert torch.isnan(y[1:4]).all() and (y[0, [1, 3]] == 0).all()
+    fin = ~torch.isnan(ref)
+    rtol, atol = tol_for(dt, h)
+    assert within_tol(y[fin], ref[fin], rtol, atol)[0]
+
+
+def test_softmax_in_place(cuda_device):
+    x = synth.cast(synth.normal_np((64, 4096), 805), torch.bfloat16)
+    ref, _ = oracle.softmax(x)
+    xd = x.to(cuda_device)
+    ks.softmax(xd, out=xd)
+    compare_output(xd.cpu(), ref, torch.bfloat16, 4096, "softmax in place")
+
+
+# --------------------------------------------------------------------------------- LayerNorm
+
+def _ln_check(out, ref, dt, h, name):
+    away = ref.double().abs() > 0.05
+    if dt != torch.float32 and bool(away.any()):
+        assert int(ulp_dist(out[away], ref[away]).max()) <= 1, name
+    rtol, atol = tol_for(dt, h)
+    if dt == torch.float32:
+        # fp32: the mean's rounding error (about H * 2^-24 * |mean|) moves every output by
+        # itself times rstd, whatever the output's size: an absolute term of the same order
+        atol = rtol * 4.0
+    ok, worst, _ = within_tol(out, ref, rtol, atol)
+    record(name, worst_excess=worst, n=out.numel())
+    assert ok, f"{name}: {worst}"
+
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("rows,h", [(128, 1024), (2048, 4096), (512, 4096), (4, 1536), (333, 8192),
+                                    (7, 16384), (5, 17), (3, 1000), (2, 20000)])
+@pytest.mark.parametrize("affine", [True, False])
+def test_layer_norm(cuda_device, dtype, rows, h, affine):
+    dt = synth.dtype_of(dtype)
+    x = synth.cast(synth.normal_np((rows, h), 806) + 0.25, dt)
+    w = synth.weight(h, dt) if affine else None
+    b = synth.cast(synth.normal_np((h,), 807, std=0.1), dt) if affine else None
+    y = ks.layer_norm(x.to(cuda_device), w.to(cuda_device) if affine else None,
+                      b.to(cuda_device) if affine else None, 1e-5).cpu()
+    ref, _ = oracle.layer_norm(x, w, b, 1e-5)
+    _ln_check(y, ref, dt, h, f"layer_norm {dtype} [{rows},{h}] affine={affine}")
+
+
+def test_layer_norm_constant_row_and_in_place(cuda_device):
+    h = 4096
+    x = synth.cast(synth.normal_np((16, h), 808), torch.bfloat16)
+    x[3] = 0.75
+    w = synth.weight(h, torch.bfloat16)
+    b = synth.cast(synth.normal_np((h,), 809), torch.bfloat16)
+    ref, _ = oracle.layer_norm(x, w, b, 1e-5)
+    xd = x.to(cuda_device)
+    ks.layer_norm(xd, w.to(cuda_device), b.to(cuda_device), 1e-5, out=xd)
+    y = xd.cpu()
+    assert torch.equal(y[3].float(), b.float())       # constant row: exactly the bias
+    _ln_check(y, ref, torch.bfloat16, h, "layer_norm in place")
+
+
+def test_next_ops_reject_bad_arguments(cuda_device):
+    x = torch.randn(4, 8, device=cuda_device)
+    assert _abi.ks_silu_and_mul(x.data_ptr(), x.data_ptr(), 4, 4, _abi.KS_DTYPE_F32, None) == \
+        _abi.KS_ERR_OVERLAP
+    assert _abi.ks_softmax(x.data_ptr(), x.data_ptr(), 4, 0, _abi.KS_DTYPE_F32, None) == \
+        _abi.KS_ERR_INVALID_ARGUMENT
+    assert _abi.ks_layer_norm(x.data_ptr(), x.data_ptr(), None, None, 4, 8, 0.0,
+                              _abi.KS_DTYPE_F32, None) == _abi.KS_ERR_INVALID_ARGUMENT
+    with pytest.raises(ValueError):
+        ks.silu_and_mul(torch.randn(4, 7, device=cuda_device))
+    st, flags = _abi.ks_device_faults(clear=False)
+    assert st == _abi.KS_SUCCESS and flags == 0
