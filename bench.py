@@ -272,6 +272,8 @@ def run_ks(args) -> int:
         # decode shape (launch-bound): p50 of single cache-cold launches, and graph replay
         if not args.no_decode:
             ops["decode_fused_add_rms_norm_4x1536"] = decode_latency(dev, args)
+        if not args.no_next_ops:
+            ops["next_ops"] = next_ops(dev, args)
         e2e = run_e2e(dev, args, R, H, eps) if not args.no_e2e else None
         cpu = cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args)
         if not cpu["parity"]["ok"]:
@@ -380,6 +382,87 @@ def decode_latency(dev, args) -> dict:
             "us_per_launch_graph_replay": graph_per_launch(False),
             "us_per_launch_graph_replay_pdl": graph_per_launch(True),
             "samples": len(cold)}
+
+
+def next_ops(dev, args) -> dict:
+    """SwiGLU, Softmax and LayerNorm (the library's next operators): HBM GB/s on large bf16
+    shapes (CUDA events over back-to-back launches; every tensor larger than L2) and the
+    per-launch time of a CUDA graph on the pages' small shapes."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    s = torch.cuda.current_stream(dev)
+    peak = measured_peaks()["hbm_gbs"]
+    BF = _abi.KS_DTYPE_BF16
+
+    def events(fn, n):
+        for _ in range(3):
+            fn(s.cuda_stream)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(n):
+            fn(s.cuda_stream)
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e-3 / n
+
+    def graph_us(fn, n=100, reps=10):
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(s)
+        with torch.cuda.stream(cs):
+            fn(cs.cuda_stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(n):
+                fn(cs.cuda_stream)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        for _ in range(reps):
+            g.replay()
+        b.record(s)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) * 1e3 / (n * reps)
+
+    out = {}
+    R, D = 32768, 8192
+    x = synth.cast(synth.normal_dev((R, 2 * D), 11, dev), "bf16")
+    y = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
+    nb = 3 * R * D * 2
+    t = events(lambda st: _abi.ks_silu_and_mul(y.data_ptr(), x.data_ptr(), R, D, BF, st), 100)
+    xs = synth.cast(synth.normal_dev((512, 8192), 12, dev), "bf16")
+    ys = torch.empty((512, 4096), dtype=torch.bfloat16, device=dev)
+    out["silu_and_mul"] = {
+        "shape": f"[{R},{2 * D}] -> [{R},{D}] bf16", "bytes_per_launch": nb, "avg_us": t * 1e6,
+        "gbs": nb / t / 1e9, "frac_of_peak": nb / t / 1e9 / peak,
+        "us_per_launch_graph_512x8192": graph_us(
+            lambda st: _abi.ks_silu_and_mul(ys.data_ptr(), xs.data_ptr(), 512, 4096, BF, st))}
+    del x, y
+    H = 8192
+    x = synth.cast(synth.normal_dev((R, H), 13, dev), "bf16")
+    y = torch.empty_like(x)
+    nb = 2 * R * H * 2
+    t = events(lambda st: _abi.ks_softmax(y.data_ptr(), x.data_ptr(), R, H, BF, st), 100)
+    xs = synth.cast(synth.normal_dev((512, 1024), 14, dev), "bf16")
+    ys = torch.empty_like(xs)
+    out["softmax"] = {
+        "shape": f"[{R},{H}] bf16", "bytes_per_launch": nb, "avg_us": t * 1e6,
+        "gbs": nb / t / 1e9, "frac_of_peak": nb / t / 1e9 / peak,
+        "us_per_launch_graph_512x1024": graph_us(
+            lambda st: _abi.ks_softmax(ys.data_ptr(), xs.data_ptr(), 512, 1024, BF, st))}
+    w = synth.weight(H, "bf16").to(dev)
+    bias = synth.cast(synth.normal_dev((H,), 15, dev, std=0.1), "bf16")
+    nb = 2 * R * H * 2 + 2 * H * 2
+    t = events(lambda st: _abi.ks_layer_norm(y.data_ptr(), x.data_ptr(), w.data_ptr(),
+                                             bias.data_ptr(), R, H, 1e-5, BF, st), 100)
+    out["layer_norm"] = {"shape": f"[{R},{H}] bf16, weight and bias", "bytes_per_launch": nb,
+                         "avg_us": t * 1e6, "gbs": nb / t / 1e9,
+                         "frac_of_peak": nb / t / 1e9 / peak}
+    return out
 
 
 def run_e2e(dev, args, R, H, eps) -> dict:
@@ -567,6 +650,7 @@ def main() -> int:
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--decode-samples", type=int, default=300)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-next-ops", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-rows-max", type=int, default=8192)
     ap.add_argument("--reference-seconds", type=float, default=90.0)

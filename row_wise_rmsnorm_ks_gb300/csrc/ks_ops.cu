@@ -6,12 +6,13 @@
 // Arithmetic:
 //  * SwiGLU (Kernscope, "Numerical contract / SwiGLU activation"): gate = fp32(x[:, :d]),
 //    up = fp32(x[:, d:]), out = cast((gate * (1 / (1 + exp(-gate)))) * up), FP32 throughout;
-//    exp is CUDA's expf (within 2 ulp), the reciprocal an IEEE division.
+//    exp is CUDA's expf for fp32 and the SFU intrinsic for 16-bit types (see exp_for), the
+//    reciprocal correctly rounded (equal to the IEEE quotient).
 //  * Softmax (Kernscope, "Numerical contract / Softmax"): z = fp32(x) - max(fp32(x)),
-//    out = cast(exp(z) / sum(exp(z))). The row maximum propagates NaN, which gives the contract's
-//    non-finite rules directly: a row with NaN or +inf, or a row all -inf, comes out NaN; -inf
-//    entries of a row with finite values come out 0. exp(z) is computed once per element and kept
-//    in registers; each output is one IEEE division.
+//    out = cast(exp(z) / sum(exp(z))). The contract's non-finite rules follow from IEEE
+//    arithmetic: a NaN or +inf in a row makes its sum (and so every output) NaN, a row of only
+//    -inf has max -inf and z = NaN, and -inf entries of a row with finite values give exp = 0. exp(z) is computed once per element and kept
+//    in registers; each output is exp(z) times the correctly rounded reciprocal of the sum.
 //  * LayerNorm (named on kernel-set's operator list; read as the standard definition with FP32
 //    steps): mean = sum(x)/H, var = sum((x-mean)^2)/H (two reductions over the register-resident
 //    row), rstd = correctly rounded rsqrt(var + eps), out = cast((((x-mean)*rstd)*w) + b); w and b
@@ -29,17 +30,13 @@ namespace {
 
 // ---------------------------------------------------------------------------- reductions
 
-__device__ __forceinline__ float nan_max(float a, float b) {
-    return (a != a) ? a : ((b != b) ? b : fmaxf(a, b));
-}
-
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = nan_max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
     return v;
 }
 
-// CTA-wide sum / NaN-propagating max; every thread returns the same value. `slot` alternates
+// CTA-wide sum / max (fmaxf: NaN-ignoring); every thread returns the same value. `slot` alternates
 // between two 32-float rows of `red` on every reduction: a warp writes a slot again only after
 // the next reduction's barrier, which every warp passes only after reading this one.
 __device__ __forceinline__ float cta_sum(float v, float (*red)[32], int &slot) {
@@ -57,13 +54,27 @@ __device__ __forceinline__ float cta_max(float v, float (*red)[32], int &slot) {
     if ((threadIdx.x & 31) == 0) red[slot][threadIdx.x >> 5] = v;
     __syncthreads();
     float m = -INFINITY;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = nan_max(m, red[slot][i]);
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[slot][i]);
     slot ^= 1;
     return m;
 }
 
+// e^v. For 16-bit outputs the SFU-based intrinsic (error a few fp32 ulps, growing with |v|,
+// far below half a bf16/fp16 ulp); for fp32 outputs CUDA's expf (within 2 ulp).
+template <typename T>
+__device__ __forceinline__ float exp_for(float v) {
+    return __expf(v);
+}
+template <>
+__device__ __forceinline__ float exp_for<float>(float v) {
+    return expf(v);
+}
+
+// (g * sigmoid(g)) * up with sigmoid(g) = 1 / (1 + e^-g); the correctly rounded reciprocal is
+// the IEEE quotient 1 / (1 + e^-g) exactly.
+template <typename T>
 __device__ __forceinline__ float silu_mul(float g, float up) {
-    const float sig = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+    const float sig = __frcp_rn(__fadd_rn(1.0f, exp_for<T>(-g)));
     return __fmul_rn(__fmul_rn(g, sig), up);
 }
 
@@ -94,12 +105,12 @@ __global__ void __launch_bounds__(256) silu_mul_vec_kernel(void *out, const void
             E::unpack(g0, a);
             E::unpack(u0, b);
 #pragma unroll
-            for (int e = 0; e < N; ++e) r[e] = silu_mul(a[e], b[e]);
+            for (int e = 0; e < N; ++e) r[e] = silu_mul<T>(a[e], b[e]);
             __stcs(o + c, E::pack(r));
             E::unpack(g1, a);
             E::unpack(u1, b);
 #pragma unroll
-            for (int e = 0; e < N; ++e) r[e] = silu_mul(a[e], b[e]);
+            for (int e = 0; e < N; ++e) r[e] = silu_mul<T>(a[e], b[e]);
             __stcs(o + c + step, E::pack(r));
         }
         if (c < dv) {
@@ -107,7 +118,7 @@ __global__ void __launch_bounds__(256) silu_mul_vec_kernel(void *out, const void
             E::unpack(__ldcs(gate + c), a);
             E::unpack(__ldcs(up + c), b);
 #pragma unroll
-            for (int e = 0; e < N; ++e) r[e] = silu_mul(a[e], b[e]);
+            for (int e = 0; e < N; ++e) r[e] = silu_mul<T>(a[e], b[e]);
             __stcs(o + c, E::pack(r));
         }
     }
@@ -124,14 +135,17 @@ __global__ void __launch_bounds__(256) silu_mul_scalar_kernel(void *out, const v
         for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < d; j += step) {
             const float g = E::load1(x, row * 2 * d + j);
             const float up = E::load1(x, row * 2 * d + d + j);
-            E::store1(out, row * d + j, silu_mul(g, up));
+            E::store1(out, row * d + j, silu_mul<T>(g, up));
         }
     }
 }
 
 // ------------------------------------------------------------------------------ Softmax
 
-// One CTA per row, V 16-byte vectors per thread held in registers; persistent over rows.
+// One CTA per row, V 16-byte vectors per thread held in registers; persistent over rows, the
+// next row's vectors loaded before the current row's two reductions. The maximum is a plain
+// fmaxf (NaN-ignoring): a NaN or +inf in the row still makes the sum, and so every output, NaN,
+// and a row of only -inf still gets max -inf and z = NaN, so the contract's non-finite rules hold.
 template <typename T, int V>
 __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void *x, int64_t rows,
                                                           int64_t hv) {
@@ -144,16 +158,30 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
     uint4 *og = static_cast<uint4 *>(out);
     const int t = threadIdx.x, g = blockDim.x;
     int slot = 0;
-    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    int64_t row = blockIdx.x;
+    uint4 cur[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        const int64_t c = t + (int64_t)k * g;
+        cur[k] = (row < rows && c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (; row < rows; row += gridDim.x) {
+        const int64_t next = row + gridDim.x;
+        uint4 nxt[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            nxt[k] = (next < rows && c < hv) ? __ldcs(xg + next * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
         float f[V][N];
         float m = -INFINITY;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
+            E::unpack(cur[k], f[k]);
             if (c < hv) {
-                E::unpack(__ldcs(xg + row * hv + c), f[k]);
 #pragma unroll
-                for (int e = 0; e < N; ++e) m = nan_max(m, f[k][e]);
+                for (int e = 0; e < N; ++e) m = fmaxf(m, f[k][e]);
             }
         }
         m = cta_max(m, red, slot);
@@ -164,21 +192,26 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
             if (c < hv) {
 #pragma unroll
                 for (int e = 0; e < N; ++e) {
-                    f[k][e] = expf(__fsub_rn(f[k][e], m));
+                    f[k][e] = exp_for<T>(__fsub_rn(f[k][e], m));
                     s[e & 3] = __fadd_rn(s[e & 3], f[k][e]);
                 }
             }
         }
         const float sum = cta_sum(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])), red, slot);
+        // e / sum as e * (1 / sum): one correctly rounded reciprocal per row, then a product
+        // per element (within 1 fp32 ulp of the quotient)
+        const float inv = __frcp_rn(sum);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
             if (c < hv) {
 #pragma unroll
-                for (int e = 0; e < N; ++e) f[k][e] = __fdiv_rn(f[k][e], sum);
+                for (int e = 0; e < N; ++e) f[k][e] = __fmul_rn(f[k][e], inv);
                 __stcs(og + row * hv + c, E::pack(f[k]));
             }
         }
+#pragma unroll
+        for (int k = 0; k < V; ++k) cur[k] = nxt[k];
     }
 }
 
@@ -196,19 +229,25 @@ __global__ void __launch_bounds__(1024) softmax_scalar_kernel(void *out, const v
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
         const int64_t base = row * H;
         float m = -INFINITY;
-        for (int64_t j = threadIdx.x; j < H; j += blockDim.x) m = nan_max(m, E::load1(x, base + j));
+        for (int64_t j = threadIdx.x; j < H; j += blockDim.x) m = fmaxf(m, E::load1(x, base + j));
         m = cta_max(m, red, slot);
         float s = 0.0f;
         for (int64_t j = threadIdx.x; j < H; j += blockDim.x)
-            s = __fadd_rn(s, expf(__fsub_rn(E::load1(x, base + j), m)));
-        const float sum = cta_sum(s, red, slot);
+            s = __fadd_rn(s, exp_for<T>(__fsub_rn(E::load1(x, base + j), m)));
+        const float inv = __frcp_rn(cta_sum(s, red, slot));
         for (int64_t j = threadIdx.x; j < H; j += blockDim.x)
-            E::store1(out, base + j, __fdiv_rn(expf(__fsub_rn(E::load1(x, base + j), m)), sum));
+            E::store1(out, base + j,
+                      __fmul_rn(exp_for<T>(__fsub_rn(E::load1(x, base + j), m)), inv));
     }
 }
 
 // ---------------------------------------------------------------------------- LayerNorm
 
+// One CTA per row, V 16-byte vectors per thread in registers, persistent over rows; the weight
+// and bias slices a thread needs stay in registers for every row it visits, and the next row's
+// vectors are loaded before the current row's two reductions. (Measured on GB300 at [32768,
+// 8192] bf16: 74 % of the copy peak; weight and bias in shared memory, with or without the
+// prefetch, were slower at 58-64 %.)
 template <typename T, int V>
 __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const void *x,
                                                              const void *w, const void *b,
@@ -231,13 +270,24 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
         bv[k] = (b && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
     }
     int slot = 0;
-    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-        uint4 xv[V];
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int64_t row = blockIdx.x;
+    uint4 xv[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        const int64_t c = t + (int64_t)k * g;
+        xv[k] = (row < rows && c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (; row < rows; row += gridDim.x) {
+        const int64_t next = row + gridDim.x;
+        uint4 nxt[V];
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            xv[k] = (c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+            nxt[k] = (next < rows && c < hv) ? __ldcs(xg + next * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
             float f[N];
             E::unpack(xv[k], f);
 #pragma unroll
@@ -277,6 +327,8 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
                 __stcs(og + row * hv + c, E::pack(f));
             }
         }
+#pragma unroll
+        for (int k = 0; k < V; ++k) xv[k] = nxt[k];
     }
 }
 

@@ -161,3 +161,16 @@ def test_next_ops_reject_bad_arguments(cuda_device):
         ks.silu_and_mul(torch.randn(4, 7, device=cuda_device))
     st, flags = _abi.ks_device_faults(clear=False)
     assert st == _abi.KS_SUCCESS and flags == 0
+
+
+@pytest.mark.parametrize("dtype", DT)
+def test_softmax_extreme_spread(cuda_device, dtype):
+    """exp(z) down to fp32 subnormals (z to -103): bf16 keeps fp32's exponent range, so tiny
+    probabilities survive the cast and must still be within the gate."""
+    dt = synth.dtype_of(dtype)
+    row = [0.0, -1.0, -20.0, -50.0, -87.0, -88.0, -90.0, -95.0, -100.0, -103.0, -3.0, -0.5,
+           -60.0, -70.0, -80.0, -86.0]
+    x = synth.cast(torch.tensor([row, [v / 2 for v in row]], dtype=torch.float32), dt)
+    y = ks.softmax(x.to(cuda_device)).cpu()
+    ref, _ = oracle.softmax(x)
+    compare_output(y, ref, dt, 16, f"softmax extreme spread {dtype}")
