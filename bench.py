@@ -429,7 +429,7 @@ def next_ops(dev, args) -> dict:
         return a.elapsed_time(b) * 1e3 / (n * reps)
 
     out = {}
-    R, D = 32768, 8192
+    R, D = args.next_rows, 8192
     x = synth.cast(synth.normal_dev((R, 2 * D), 11, dev), "bf16")
     y = torch.empty((R, D), dtype=torch.bfloat16, device=dev)
     nb = 3 * R * D * 2
@@ -651,6 +651,8 @@ def main() -> int:
     ap.add_argument("--decode-samples", type=int, default=300)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-next-ops", action="store_true")
+    ap.add_argument("--next-rows", type=int, default=32768,
+                    help="rows of the next operators' large shapes (width 8192)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-rows-max", type=int, default=8192)
     ap.add_argument("--reference-seconds", type=float, default=90.0)

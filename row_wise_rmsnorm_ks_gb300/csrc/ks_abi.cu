@@ -391,8 +391,8 @@ ks_status_t ks_fused_add_rms_norm_planned(void *x, void *residual, const void *w
 ks_status_t ks_device_faults(int32_t *flags, int32_t clear) {
     if (!flags) return ks::fail(KS_ERR_INVALID_ARGUMENT, "flags is NULL");
     *flags = 0;
-    const int parts[3] = {ks::fault_flags_bf16(clear != 0), ks::fault_flags_f16(clear != 0),
-                          ks::fault_flags_f32(clear != 0)};
+    const int parts[4] = {ks::fault_flags_bf16(clear != 0), ks::fault_flags_f16(clear != 0),
+                          ks::fault_flags_f32(clear != 0), ks::fault_flags_ops(clear != 0)};
     for (int v : parts) {
         if (v < 0) return ks::fail(KS_ERR_CUDA, "reading the device fault words failed");
         *flags |= v;

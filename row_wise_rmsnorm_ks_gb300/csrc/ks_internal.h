@@ -57,6 +57,7 @@ int blocks_per_sm_f32(const ks_plan_t &p, bool fused);
 int fault_flags_bf16(bool clear);
 int fault_flags_f16(bool clear);
 int fault_flags_f32(bool clear);
+int fault_flags_ops(bool clear);
 cudaError_t launch_bf16(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);
 cudaError_t launch_f16(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);
 cudaError_t launch_f32(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStream_t s);

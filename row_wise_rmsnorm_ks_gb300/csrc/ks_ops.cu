@@ -16,7 +16,8 @@
 //  * LayerNorm (named on kernel-set's operator list; read as the standard definition with FP32
 //    steps): mean = sum(x)/H, var = sum((x-mean)^2)/H (two reductions over the register-resident
 //    row), rstd = correctly rounded rsqrt(var + eps), out = cast((((x-mean)*rstd)*w) + b); w and b
-//    optional.
+//    optional. The output pass evaluates it as fma(x, rstd, -mean*rstd), then fma(., w, b):
+//    the same value with fewer roundings (within the stated tolerance of the oracle's order).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -70,11 +71,36 @@ __device__ __forceinline__ float exp_for<float>(float v) {
     return expf(v);
 }
 
-// (g * sigmoid(g)) * up with sigmoid(g) = 1 / (1 + e^-g); the correctly rounded reciprocal is
-// the IEEE quotient 1 / (1 + e^-g) exactly.
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTwoPowM64 = 5.421010862427522e-20f;          // 2^-64
+
+// 2^v on the special-function unit (relative error about 2^-22; results below 2^-126 flush to
+// zero, which the callers keep out of the range that matters by a power-of-two bias).
+__device__ __forceinline__ float ex2_sfu(float v) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+__device__ __forceinline__ float rcp_sfu(float v) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// (g * sigmoid(g)) * up with sigmoid(g) = 1 / (1 + e^-g).
+//  fp32 outputs: e^-g by expf, the correctly rounded reciprocal (bitwise the IEEE quotient).
+//  16-bit outputs: g * up / (1 + e^-g) on the SFU, everything scaled by 2^-64 so that neither
+//  e^-g * 2^-64 nor the reciprocal of (1 + e^-g) * 2^-64 leaves the normal range for any
+//  finite gate (the flush-to-zero SFU ops then lose nothing a 16-bit output can show):
+//  t = (-g) log2(e) - 64, den' = 2^t + 2^-64, out = ((g * up) * rcp(den')) * 2^-64.
 template <typename T>
 __device__ __forceinline__ float silu_mul(float g, float up) {
-    const float sig = __frcp_rn(__fadd_rn(1.0f, exp_for<T>(-g)));
+    const float den = __fadd_rn(ex2_sfu(__fmaf_rn(-g, kLog2e, -64.0f)), kTwoPowM64);
+    return __fmul_rn(__fmul_rn(__fmul_rn(g, up), rcp_sfu(den)), kTwoPowM64);
+}
+template <>
+__device__ __forceinline__ float silu_mul<float>(float g, float up) {
+    const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-g)));
     return __fmul_rn(__fmul_rn(g, sig), up);
 }
 
@@ -185,6 +211,11 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
             }
         }
         m = cta_max(m, red, slot);
+        // 16-bit outputs: e_j * 2^64 = 2^(x_j log2(e) + (64 - m log2(e))), one FMA and one SFU op
+        // per element; the 2^64 cancels in e_j / sum and keeps every exp above 2^-190 normal
+        // (smaller ones are below any fp32 output anyway). For m = +-inf or NaN the bias is
+        // -inf/+inf/NaN, which gives NaN rows exactly as the formula does.
+        const float bias = __fmaf_rn(-m, kLog2e, 64.0f);
         float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int k = 0; k < V; ++k) {
@@ -192,7 +223,8 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
             if (c < hv) {
 #pragma unroll
                 for (int e = 0; e < N; ++e) {
-                    f[k][e] = exp_for<T>(__fsub_rn(f[k][e], m));
+                    f[k][e] = sizeof(T) == 4 ? expf(__fsub_rn(f[k][e], m))
+                                             : ex2_sfu(__fmaf_rn(f[k][e], kLog2e, bias));
                     s[e & 3] = __fadd_rn(s[e & 3], f[k][e]);
                 }
             }
@@ -309,6 +341,7 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
         }
         const float var = __fdiv_rn(cta_sum(q.total(), red, slot), h);
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
+        const float shift = -__fmul_rn(mean, rstd);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
@@ -319,9 +352,9 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
                 E::unpack(bv[k], bf);
 #pragma unroll
                 for (int e = 0; e < N; ++e) {
-                    float v = __fmul_rn(__fsub_rn(f[e], mean), rstd);
-                    if (w) v = __fmul_rn(v, wf[e]);
-                    if (b) v = __fadd_rn(v, bf[e]);
+                    float v = __fmaf_rn(f[e], rstd, shift);  // (x - mean) * rstd
+                    if (w) v = b ? __fmaf_rn(v, wf[e], bf[e]) : __fmul_rn(v, wf[e]);
+                    else if (b) v = __fadd_rn(v, bf[e]);
                     f[e] = v;
                 }
                 __stcs(og + row * hv + c, E::pack(f));
@@ -329,6 +362,149 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
         }
 #pragma unroll
         for (int k = 0; k < V; ++k) xv[k] = nxt[k];
+    }
+}
+
+// Staged LayerNorm for many rows: rows stream into a ring of `stages` shared-memory stages by
+// bulk asynchronous copies (thread 0 issues one per row, L2 evict-first, completing on the
+// stage's mbarrier), so several rows per CTA are in flight. Every thread copies its vectors of
+// the stage into registers in the first pass; the row's first reduction barrier is therefore
+// also the point after which thread 0 refills the stage with the row `stages` iterations ahead.
+// (Reading the stage in all three passes instead freed registers but measured slower.) Waits
+// are bounded (about 2 s); on a time-out the CTA records KS_FAULT_WAIT_TIMEOUT, drains its copies
+// in flight (bounded) and returns.
+template <typename T, int V>
+__global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const void *x,
+                                                              const void *w, const void *b,
+                                                              int64_t rows, int64_t hidden,
+                                                              int64_t hv, float eps, int stages) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[2][32];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *ring = smem + 128;
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const uint4 *xg = static_cast<const uint4 *>(x);
+    uint4 *og = static_cast<uint4 *>(out);
+    const int t = threadIdx.x, g = blockDim.x;
+    const float h = (float)hidden;
+    const uint32_t row_bytes = (uint32_t)(hv * 16);
+    const int64_t step = gridDim.x;
+    uint4 wv[V], bv[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        const int64_t c = t + (int64_t)k * g;
+        wv[k] = (w && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
+        bv[k] = (b && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint64_t policy = 0;
+    if (t == 0) {
+        for (int i = 0; i < stages; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int st, int64_t r) {
+        mbar_arrive_expect_tx(&bars[st], row_bytes);
+        bulk_g2s(ring + (size_t)st * row_bytes, xg + r * hv, row_bytes, &bars[st], policy);
+    };
+    if (t == 0) {
+        policy = l2_evict_first_policy();
+        for (int i = 0; i < stages; ++i) {
+            const int64_t r = blockIdx.x + (int64_t)i * step;
+            if (r >= rows) break;
+            issue(i, r);
+        }
+    }
+    int st = 0, slot = 0;
+    uint32_t phase = 0;
+    bool fault = false;
+    int64_t row = blockIdx.x;
+    for (; row < rows; row += step) {
+        const bool ok = mbar_wait_bounded(&bars[st], phase);
+        const unsigned char *sx = ring + (size_t)st * row_bytes;
+        uint4 xv[V];
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            xv[k] = (ok && c < hv) ? ld_shared_v4(sx + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+            float f[N];
+            E::unpack(xv[k], f);
+#pragma unroll
+            for (int e = 0; e < N; ++e) s4[e & 3] = __fadd_rn(s4[e & 3], f[e]);
+        }
+        // first reduction: every thread holds its vectors, so the stage is free, and a time-out
+        // anywhere is seen by all
+        const float part = warp_sum(__fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3])));
+        if ((t & 31) == 0) red[slot][t >> 5] = part;
+        if (__syncthreads_or(!ok)) {
+            fault = true;
+            break;
+        }
+        if (t == 0) {
+            const int64_t ahead = row + (int64_t)stages * step;
+            if (ahead < rows) issue(st, ahead);
+        }
+        float tot = 0.0f;
+        for (int i = 0; i < (g >> 5); ++i) tot += red[slot][i];
+        slot ^= 1;
+        const float mean = __fdiv_rn(tot, h);
+        SumSq q;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < hv) {
+                float f[N];
+                E::unpack(xv[k], f);
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[e] = __fsub_rn(f[e], mean);
+                q.add(f);
+            }
+        }
+        const float var = __fdiv_rn(cta_sum(q.total(), red, slot), h);
+        const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
+        const float shift = -__fmul_rn(mean, rstd);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {  // unpack weight and bias per row, not hoisted as floats
+            opaque(wv[k]);
+            opaque(bv[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < hv) {
+                float f[N], wf[N], bf[N];
+                E::unpack(xv[k], f);
+                E::unpack(wv[k], wf);
+                E::unpack(bv[k], bf);
+#pragma unroll
+                for (int e = 0; e < N; ++e) {
+                    float v = __fmaf_rn(f[e], rstd, shift);  // (x - mean) * rstd
+                    if (w) v = b ? __fmaf_rn(v, wf[e], bf[e]) : __fmul_rn(v, wf[e]);
+                    else if (b) v = __fadd_rn(v, bf[e]);
+                    f[e] = v;
+                }
+                __stcs(og + row * hv + c, E::pack(f));
+            }
+        }
+        if (++st == stages) {
+            st = 0;
+            phase ^= 1u;
+        }
+    }
+    if (fault && t == 0) {
+        atomicOr(&g_fault_flags, kFaultWaitTimeout);
+        // copies still in flight: this row's stage and the ones after it
+        for (int i = 0; i < stages; ++i) {
+            if (row + (int64_t)i * step >= rows) break;
+            mbar_wait_bounded(&bars[st], phase);
+            if (++st == stages) {
+                st = 0;
+                phase ^= 1u;
+            }
+        }
     }
 }
 
@@ -462,6 +638,11 @@ cudaError_t softmax_dispatch(int v, int block, void *out, const void *x, int64_t
     return launch(f, dim3((unsigned)grid), dim3(block), args, s);
 }
 
+// Bytes of rows in each CTA's LayerNorm ring (a tuning constant, set from a GB300 measurement).
+#ifndef KS_LN_RING_BYTES
+#define KS_LN_RING_BYTES (64 * 1024)
+#endif
+
 template <typename T>
 cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, const void *w,
                                 const void *b, int64_t rows, int64_t hidden, int64_t hv,
@@ -474,24 +655,65 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
     void *sc_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
                        const_cast<void **>(&b), &nr, &hd, &ep};
     void **args = vec_args;
-    switch (v) {
+    // Many rows of a vectorisable width: the staged ring (KS_LN_RING_BYTES of rows per CTA, 2..8
+    // stages) keeps enough bytes in flight; otherwise the register kernel.
+    int stages = 0;
+    if (v == 4 && rows >= 4 * (int64_t)sms) {
+        int64_t n_st = (KS_LN_RING_BYTES) / (hv * 16);
+        stages = (int)(n_st < 2 ? 2 : (n_st > 8 ? 8 : n_st));
+    }
+    void *bulk_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
+                         const_cast<void **>(&b), &nr, &hd, &hvv, &ep, &stages};
+    size_t smem = 0;
+    switch (stages ? 8 : v) {
     case 1: f = (const void *)layer_norm_vec_kernel<T, 1>; break;
     case 2: f = (const void *)layer_norm_vec_kernel<T, 2>; break;
     case 4: f = (const void *)layer_norm_vec_kernel<T, 4>; break;
+    case 8:
+        f = (const void *)layer_norm_bulk_kernel<T, 4>;
+        args = bulk_args;
+        smem = 128 + (size_t)stages * (size_t)hv * 16;
+        break;
     default:
         f = (const void *)layer_norm_scalar_kernel<T>;
         args = sc_args;
         block = (int)round_up64(ceil_div64(hidden, 8), 32);
         block = block < 32 ? 32 : (block > 1024 ? 1024 : block);
     }
+    if (smem > 0) {
+        // allow the largest ring the device takes beside the kernel's static shared memory
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaFuncGetAttributes(&fa, f) != cudaSuccess)
+            return cudaErrorInvalidConfiguration;
+        const int max_dynamic = optin - (int)fa.sharedSizeBytes;
+        if ((int64_t)smem > max_dynamic ||
+            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic) != cudaSuccess)
+            return cudaErrorInvalidConfiguration;
+    }
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, 0) != cudaSuccess || n < 1) n = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, smem) != cudaSuccess || n < 1) n = 1;
     int64_t grid = (int64_t)sms * n;
     grid = grid > rows ? rows : grid;
-    return launch(f, dim3((unsigned)grid), dim3(block), args, s);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = launch_pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, f, args);
 }
 
 }  // namespace
+
+int fault_flags_ops(bool clear) { return fault_flags_t(clear); }
+
 }  // namespace ks
 
 using namespace ks;

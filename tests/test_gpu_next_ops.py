@@ -174,3 +174,24 @@ def test_softmax_extreme_spread(cuda_device, dtype):
     y = ks.softmax(x.to(cuda_device)).cpu()
     ref, _ = oracle.softmax(x)
     compare_output(y, ref, dt, 16, f"softmax extreme spread {dtype}")
+
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("h", [1024, 4096, 8192, 16384])
+@pytest.mark.parametrize("affine", [True, False])
+def test_layer_norm_many_rows_staged(cuda_device, dtype, h, affine):
+    """Enough rows for the staged ring (>= 4 rows per SM): sampled rows against the oracle, and
+    the ring's fault word stays clear."""
+    dt = synth.dtype_of(dtype)
+    if dt == torch.float32 and h > 8192:
+        pytest.skip("fp32 rows wider than 2048 vectors take the scalar kernel")
+    rows = 1000
+    x = synth.cast(synth.normal_np((rows, h), 811) - 0.5, dt)
+    w = synth.weight(h, dt) if affine else None
+    b = synth.cast(synth.normal_np((h,), 812, std=0.1), dt) if affine else None
+    y = ks.layer_norm(x.to(cuda_device), w.to(cuda_device) if affine else None,
+                      b.to(cuda_device) if affine else None, 1e-5).cpu()
+    ref, _ = oracle.layer_norm(x, w, b, 1e-5)
+    _ln_check(y, ref, dt, h, f"layer_norm staged {dtype} [{rows},{h}] affine={affine}")
+    st, flags = _abi.ks_device_faults(clear=False)
+    assert st == _abi.KS_SUCCESS and flags == 0
