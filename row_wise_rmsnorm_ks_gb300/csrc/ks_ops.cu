@@ -22,7 +22,6 @@
 
 #include <cmath>
 #include <mutex>
-#include <unordered_map>
 
 #include "ks_kernels.cuh"
 

@@ -13,7 +13,7 @@ import torch
 import oracle
 import row_wise_rmsnorm_ks_gb300 as ks
 from gpu_common import compare_output, record
-from helpers import bits_equal, tol_for, ulp_dist, within_tol
+from helpers import tol_for, ulp_dist, within_tol
 from row_wise_rmsnorm_ks_gb300 import _abi, synth
 
 pytestmark = pytest.mark.gpu
