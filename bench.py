@@ -636,6 +636,212 @@ def run_reference(args) -> int:
     return 0
 
 
+def run_sweep(args) -> int:
+    """The configuration sweeps (one JSON line per case; not the contract's line): the large bf16
+    shape's rows 1024..32768 at H = 8192, and the odd/wide sweep H in {1536, 5120, 7168, 14336,
+    16384} x rows in {1, 7, 333, 65536} x {fp16, bf16}, both ops, on the sweep's own inputs
+    (N(0,1) rows for the first, heavy-tailed Student-t rows with 1% scaled by 1e3 for the second).
+    Each case: the median of single launches timed with CUDA events, the L2 emptied before each
+    (outside the timed pair) by reading a 512 MiB buffer, so no dirty line of another tensor is
+    left to write back; algorithmic GB/s and the fraction of the measured copy peak. Cases of at
+    most 333 rows also report the per-launch time of 20 back-to-back launches replayed from a
+    CUDA graph (inputs hot in L2), the launch-bound figure for decode-sized batches."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    side = torch.cuda.Stream(dev)
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    peak = measured_peaks()["hbm_gbs"]
+    codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16}
+
+    def median_us(fn, n):
+        s = torch.cuda.current_stream(dev)
+        fn(s.cuda_stream)
+        out = []
+        for _ in range(n):
+            flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn(s.cuda_stream)
+            b.record(s)
+            b.synchronize()
+            out.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(out)
+
+    def graph_us(fn, launches=20, replays=20):
+        with torch.cuda.stream(side):
+            fn(side.cuda_stream)
+            side.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _ in range(launches):
+                    fn(torch.cuda.current_stream(dev).cuda_stream)
+            g.replay()
+            side.synchronize()
+            out = []
+            for _ in range(replays):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(side)
+                g.replay()
+                b.record(side)
+                b.synchronize()
+                out.append(a.elapsed_time(b) * 1e3 / launches)
+        return statistics.median(out)
+
+    def case(tag, dt, R, H, op, x, r, w, eps):
+        code = codes[dt]
+        if op == "rms_norm":
+            y = torch.empty_like(x)
+            fn = lambda st: _abi.check(_abi.ks_rms_norm(y.data_ptr(), x.data_ptr(), w.data_ptr(),
+                                                        R, H, eps, code, st))
+        else:
+            fn = lambda st: _abi.check(_abi.ks_fused_add_rms_norm(x.data_ptr(), r.data_ptr(),
+                                                                  w.data_ptr(), R, H, eps, code, st))
+        us = median_us(fn, args.sweep_samples)
+        nb = algorithmic_bytes(op, R, H, 2)
+        plan = _abi.ks_plan_launch(0 if op == "rms_norm" else 1, R, H, code, True, 152, 0)[1]
+        line = {"sweep": tag, "op": op, "dtype": dt, "rows": R, "hidden": H, "p50_us": us,
+                "gbs": nb / (us * 1e-6) / 1e9, "frac_of_peak": nb / (us * 1e-6) / 1e9 / peak,
+                "kernel": plan.as_dict()["kernel_name"], "vec_per_thread": plan.vec_per_thread,
+                "prefetch": not plan.flags & _abi.KS_PLAN_NO_PREFETCH}
+        if R <= 333:
+            line["graph_us"] = graph_us(fn)
+        print(json.dumps(line), flush=True)
+
+    for R in (1024, 2048, 4096, 8192, 16384, 32768):
+        x = synth.cast(synth.normal_dev((R, 8192), synth.SEED_X, dev), "bf16")
+        r = synth.cast(synth.normal_dev((R, 8192), synth.SEED_RESIDUAL, dev), "bf16")
+        w = synth.weight(8192, "bf16").to(dev)
+        for op in ("rms_norm", "fused_add_rms_norm"):
+            case("prefill rows", "bf16", R, 8192, op, x, r, w, 1e-5)
+        del x, r
+    for dt in ("bf16", "fp16"):
+        for H in (1536, 5120, 7168, 14336, 16384):
+            for R in (1, 7, 333, 65536):
+                for op in ("rms_norm", "fused_add_rms_norm"):
+                    wl = synth.wide_device(op, H, R, dt, dev)
+                    case("wide", dt, R, H, op, wl.x, wl.residual, wl.weight, wl.eps)
+                    del wl
+    torch.cuda.empty_cache()
+    return 0
+
+
+def plan_candidates(op: str, hv: int, elem: int):
+    """Every launch plan the heuristic chooses among for a row of hv 16-byte vectors, named as in
+    the plan-sweep tables: w4/w4n (warp per row, 4 vectors per lane, with/without prefetch),
+    p2/n2/p4/n4 (CTA per row, 2 or 4 vectors per thread, with/without prefetch), b2 (staged ring,
+    2 stages), and for rows wider than 2048 vectors cC (register-resident cluster of C CTAs, 4
+    vectors per thread) and bCsS (staged ring split over C CTAs, S stages)."""
+    from row_wise_rmsnorm_ks_gb300 import _abi
+
+    up32 = lambda n: -(-n // 32) * 32
+    fused = op == "fused_add_rms_norm"
+    out = []
+    if hv <= 128:
+        out += [("w4", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, 4, 256)),
+                ("w4n", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, 4, 256,
+                                       flags=_abi.KS_PLAN_NO_PREFETCH))]
+    for v in (2, 4):
+        b = up32(-(-hv // v))
+        if b <= (1024 if v == 2 else 512):
+            out += [(f"p{v}", _abi.make_plan(_abi.KS_KERNEL_CTA_ROW, v, b)),
+                    (f"n{v}", _abi.make_plan(_abi.KS_KERNEL_CTA_ROW, v, b,
+                                             flags=_abi.KS_PLAN_NO_PREFETCH))]
+    b = up32(-(-hv // 4))
+    if b <= 512 and 128 + 2 * hv * 16 * (2 if fused else 1) <= 226 * 1024:
+        out.append(("b2", _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, b, 2)))
+    if hv > 2048:
+        for c in (2, 4, 8):
+            sl = -(-hv // c)
+            b = up32(-(-sl // 4))
+            if b > 512:
+                continue
+            out.append((f"c{c}", _abi.make_plan(_abi.KS_KERNEL_CLUSTER_ROW, 4, b, cluster=c)))
+            for st in (2, 3):
+                if 128 + st * sl * 16 * (2 if fused else 1) <= 226 * 1024:
+                    out.append((f"b{c}s{st}", _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, b, st,
+                                                             cluster=c)))
+    return out
+
+
+def run_plan_sweep(args) -> int:
+    """The sweep behind the launch heuristic (one JSON line per dtype, op and width; not the
+    contract's line): for rows of hv = 128..2048 16-byte vectors in steps of 64, and 2560, 3072,
+    4096, 8192, 16384, every candidate plan of plan_candidates() and the default, at an HBM-bound
+    row count (384 MiB per tensor), N(0,1) inputs, back-to-back launches timed with CUDA events;
+    the candidates are interleaved over --plan-sweep-rounds rounds and the median kept, as a
+    fraction of the measured copy peak."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    peak = measured_peaks()["hbm_gbs"]
+    codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
+
+    def timeit(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fn()
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n * 1e-3
+
+    widths = list(range(128, 2049, 64)) + [2560, 3072, 4096, 8192, 16384]
+    for dt in args.plan_sweep_dtypes.split(","):
+        elem = 4 if dt == "fp32" else 2
+        code = codes[dt]
+        for hv in widths:
+            H = hv * 16 // elem
+            R = max(64, (384 << 20) // (H * elem))
+            x = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), dt)
+            r = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev), dt)
+            y = torch.empty_like(x)
+            w = synth.weight(H, dt).to(dev)
+            for op in ("rms_norm", "fused_add_rms_norm"):
+                nb = algorithmic_bytes(op, R, H, elem)
+                fns = []
+                for name, p in [("default", None)] + plan_candidates(op, hv, elem):
+                    if op == "rms_norm":
+                        fn = ((lambda p=p: _abi.ks_rms_norm_planned(
+                            y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H, 1e-5, code, p, s))
+                            if p else (lambda: _abi.ks_rms_norm(
+                                y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H, 1e-5, code, s)))
+                    else:
+                        fn = ((lambda p=p: _abi.ks_fused_add_rms_norm_planned(
+                            x.data_ptr(), r.data_ptr(), w.data_ptr(), R, H, 1e-5, code, p, s))
+                            if p else (lambda: _abi.ks_fused_add_rms_norm(
+                                x.data_ptr(), r.data_ptr(), w.data_ptr(), R, H, 1e-5, code, s)))
+                    if fn() == _abi.KS_SUCCESS:  # a plan that does not fit is left out
+                        fns.append((name, fn))
+                n = max(10, min(60, int(1.5e-2 / (nb / 6e12))))
+                res = {name: [] for name, _ in fns}
+                for _ in range(args.plan_sweep_rounds):
+                    for name, fn in fns:
+                        res[name].append(nb / timeit(fn, n) / 1e9 / peak)
+                dp = _abi.ks_plan_launch(0 if op == "rms_norm" else 1, R, H, code, True, 152,
+                                         0)[1].as_dict()
+                line = {"plan_sweep": dt, "op": op, "hv": hv, "hidden": H, "rows": R,
+                        "default_plan": {k: dp[k] for k in ("kernel_name", "vec_per_thread",
+                                                            "flags", "stages", "cluster")}}
+                line.update({k: round(statistics.median(v), 4) for k, v in res.items()})
+                print(json.dumps(line), flush=True)
+            del x, r, y
+            torch.cuda.empty_cache()
+    st, flags = _abi.ks_device_faults(clear=True)
+    if st != _abi.KS_SUCCESS or flags:
+        print(json.dumps({"plan_sweep": "device faults", "status": st, "flags": flags}))
+        return 1
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -650,6 +856,13 @@ def main() -> int:
     ap.add_argument("--decode-samples", type=int, default=300)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-next-ops", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print the configuration sweeps, one JSON line per case, and exit")
+    ap.add_argument("--sweep-samples", type=int, default=15)
+    ap.add_argument("--plan-sweep", action="store_true",
+                    help="time every candidate launch plan per dtype, op and width, and exit")
+    ap.add_argument("--plan-sweep-rounds", type=int, default=3)
+    ap.add_argument("--plan-sweep-dtypes", default="bf16,fp16,fp32")
     ap.add_argument("--next-rows", type=int, default=32768,
                     help="rows of the next operators' large shapes (width 8192)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -660,6 +873,10 @@ def main() -> int:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    if args.plan_sweep:
+        return run_plan_sweep(args)
     return run_ks(args)
 
 

@@ -65,12 +65,17 @@ struct DeviceSlot {
 DeviceSlot g_devices[kMaxDevices];
 
 std::mutex g_occ_mu;
-std::unordered_map<uint64_t, int> g_occ;  // (device, dtype, fused, kernel, vec, block) -> CTAs/SM
+std::unordered_map<uint64_t, int> g_occ;  // occupancy facts per (device, kernel, plan shape)
 
-uint64_t occ_key(int dev, ks_dtype_t d, bool fused, const ks_plan_t &p) {
-    return ((uint64_t)dev << 52) | ((uint64_t)d << 48) | ((uint64_t)fused << 47) |
-           ((uint64_t)p.kernel << 40) | ((uint64_t)p.vec_per_thread << 32) |
-           ((uint64_t)(p.flags & 0xFF) << 24) | ((uint64_t)p.stages << 16) | (uint64_t)p.block;
+// Key of an occupancy fact: the device, what is asked (CTAs per SM or resident clusters), and
+// every plan field that selects the kernel or changes its residency.
+uint64_t occ_key(int dev, ks_dtype_t d, bool fused, const ks_plan_t &p, bool clusters) {
+    return ((uint64_t)(dev & 0x3F) << 58) | ((uint64_t)clusters << 57) |
+           ((uint64_t)(d & 0x3) << 55) | ((uint64_t)fused << 54) |
+           ((uint64_t)(p.kernel & 0x7) << 51) | ((uint64_t)(p.vec_per_thread & 0x7) << 48) |
+           ((uint64_t)(p.cluster & 0xF) << 44) | ((uint64_t)(p.flags & 0x3) << 42) |
+           ((uint64_t)(p.stages & 0x1F) << 37) | ((uint64_t)(p.block & 0x7FF) << 26) |
+           (uint64_t)(p.smem_bytes & 0x3FFFFFF);
 }
 
 constexpr int kSmemLimit = 226 * 1024;  // dynamic ring; static smem and reserve fit in 227 KB
@@ -86,7 +91,8 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
         return fail(KS_ERR_INVALID_ARGUMENT, "plan block %d is not a positive multiple of 32", p.block);
     p.stages = p.kernel == KS_KERNEL_BULK_ROW ? p.stages : 0;
     p.smem_bytes = 0;
-    p.cluster = p.kernel == KS_KERNEL_CLUSTER_ROW ? p.cluster : 0;
+    const bool split_bulk = p.kernel == KS_KERNEL_BULK_ROW && p.cluster >= 2;
+    p.cluster = (p.kernel == KS_KERNEL_CLUSTER_ROW || split_bulk) ? p.cluster : 0;
     if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL))
         return fail(KS_ERR_INVALID_ARGUMENT, "unknown plan flags 0x%x", (unsigned)p.flags);
     int64_t rows_per_cta = 1;
@@ -106,12 +112,18 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
         const bool bulk = p.kernel == KS_KERNEL_BULK_ROW;
         if (bulk ? p.vec_per_thread != 4 : (p.vec_per_thread != 2 && p.vec_per_thread != 4))
             return fail(KS_ERR_INVALID_ARGUMENT, "unsupported vectors per thread %d", p.vec_per_thread);
+        if (split_bulk && p.cluster > 8)
+            return fail(KS_ERR_INVALID_ARGUMENT, "cluster of %d CTAs (2..8 supported)", p.cluster);
+        const int C = split_bulk ? p.cluster : 1;
+        const int64_t slice = ceil_div(hv, C);
+        if ((C - 1) * slice >= hv)
+            return fail(KS_ERR_INVALID_ARGUMENT, "a cluster of %d leaves a CTA without vectors", C);
         const int bound = bulk ? 512 : (p.vec_per_thread == 2 ? 1024 : 512);
-        if ((int64_t)p.block * p.vec_per_thread < hv || p.block > bound)
+        if ((int64_t)p.block * p.vec_per_thread < slice || p.block > bound)
             return fail(KS_ERR_INVALID_ARGUMENT, "CTA-row plan does not cover the row or block > %d", bound);
-        p.team = p.block;
+        p.team = p.block * C;
         if (bulk) {
-            const int64_t stage = hv * 16 * (fused ? 2 : 1);
+            const int64_t stage = slice * 16 * (fused ? 2 : 1);
             if (p.stages < 1 || p.stages > 16 || kRingHeader + stage * p.stages > kSmemLimit)
                 return fail(KS_ERR_INVALID_ARGUMENT, "staged ring of %d stages does not fit", p.stages);
             p.smem_bytes = (int32_t)(kRingHeader + stage * p.stages);
@@ -149,6 +161,26 @@ int query_blocks_per_sm(ks_dtype_t d, const ks_plan_t &p, bool fused) {
     case KS_DTYPE_F16: return blocks_per_sm_f16(p, fused);
     default: return blocks_per_sm_f32(p, fused);
     }
+}
+
+int query_max_clusters(ks_dtype_t d, const ks_plan_t &p, bool fused) {
+    switch (d) {
+    case KS_DTYPE_BF16: return max_clusters_bf16(p, fused);
+    case KS_DTYPE_F16: return max_clusters_f16(p, fused);
+    default: return max_clusters_f32(p, fused);
+    }
+}
+
+// Cached occupancy facts of a plan's kernel on a device: CTAs per SM, and for cluster plans the
+// clusters that can be resident at once (0 = the query failed).
+int cached_query(int dev, ks_dtype_t dtype, bool fused, const ks_plan_t &p, bool clusters) {
+    const uint64_t key = occ_key(dev, dtype, fused, p, clusters);
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+    const int v = clusters ? query_max_clusters(dtype, p, fused) : query_blocks_per_sm(dtype, p, fused);
+    if (v > 0) g_occ.emplace(key, v);
+    return v;
 }
 
 ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, int64_t rows,
@@ -202,27 +234,16 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
     if (slot.err != cudaSuccess)
         return fail(KS_ERR_CUDA, "querying the SM count: %s", cudaGetErrorString(slot.err));
     if (!forced) {
-        st = plan(fused ? 1 : 0, rows, hidden, e, aligned16, slot.sm_count, 0, &p);
+        st = plan(fused ? 1 : 0, rows, hidden, dtype, aligned16, slot.sm_count, 0, &p);
         if (st != KS_SUCCESS) return st;
     }
     const int32_t pdl = forced ? (p.flags & KS_PLAN_PDL)
                                : ((g_launch_options.load(std::memory_order_relaxed) & KS_LAUNCH_PDL)
                                       ? KS_PLAN_PDL : 0);
 
-    int bps;
-    {
-        const uint64_t key = occ_key(dev, dtype, fused, p);
-        std::lock_guard<std::mutex> lock(g_occ_mu);
-        auto it = g_occ.find(key);
-        if (it != g_occ.end()) {
-            bps = it->second;
-        } else {
-            bps = query_blocks_per_sm(dtype, p, fused);
-            if (bps > 0) g_occ.emplace(key, bps);
-        }
-    }
+    const int bps = cached_query(dev, dtype, fused, p, false);
     if (bps <= 0) return fail(KS_ERR_CUDA, "kernel %d (block %d) cannot be resident", p.kernel, p.block);
-    if (forced && p.kernel == KS_KERNEL_CLUSTER_ROW) {
+    if (forced && p.cluster >= 2) {
         // whole clusters: one row per cluster per pass
         const int64_t cap = (int64_t)slot.sm_count * bps / p.cluster;
         int64_t clusters = forced->grid > 0 ? forced->grid / p.cluster : cap;
@@ -237,8 +258,21 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         p.grid = forced->grid > 0 ? (forced->grid < ctas ? forced->grid : ctas) : (ctas < cap ? ctas : cap);
         p.rows_per_pass = p.grid * per_cta;
     } else {
-        st = plan(fused ? 1 : 0, rows, hidden, e, aligned16, slot.sm_count, bps, &p);
+        st = plan(fused ? 1 : 0, rows, hidden, dtype, aligned16, slot.sm_count, bps, &p);
         if (st != KS_SUCCESS) return st;
+    }
+    if (p.cluster >= 2) {
+        // A persistent grid of clusters must be resident at once (a cluster left for a second
+        // wave would start only after a resident one has finished all its rows): cap it by the
+        // device's own count, which the placement of clusters on GPCs can make smaller than
+        // SMs * CTAs per SM / cluster.
+        const int resident = cached_query(dev, dtype, fused, p, true);
+        if (resident <= 0)
+            return fail(KS_ERR_CUDA, "no cluster of %d x %d threads can be resident", p.cluster, p.block);
+        if (p.grid / p.cluster > resident) {
+            p.grid = (int64_t)resident * p.cluster;
+            p.rows_per_pass = resident;
+        }
     }
 
     p.flags = (p.flags & ~KS_PLAN_PDL) | pdl;
@@ -265,37 +299,75 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 
 // Host heuristic (after the pages' rule of sizing the launch from the row width: Triton
 // Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"), set from a sweep of
-// every variant on GB300 over widths 512..16384 at HBM-bound row counts:
-//  * rows of at most 128 16-byte vectors (bf16/fp16 H <= 1024, fp32 H <= 512): one warp per
-//    row, 1/2/4 vectors per lane, next row prefetched, up to 8 rows per CTA but never fewer CTAs
-//    than SMs when the rows allow it;
-//  * rows of up to 2048 vectors (bf16/fp16 H <= 16384, fp32 H <= 8192): one CTA per row, 4
-//    vectors per thread, the CTA as wide as the row needs (a multiple of 32 threads). The fused
-//    op prefetches the next row (two tensors in flight per row hide the barrier); the plain op
-//    does not, which lowers its registers enough to keep more CTAs resident. Plain rows wider
-//    than 1536 vectors stream through the staged shared-memory ring instead, when there are
-//    enough rows to fill it;
-//    In the latency regime (rows <= SMs, so each CTA gets at most one row) the widest fused rows
-//    (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8 CTAs per row, and plain rows of
-//    at most 1024 vectors take 2 vectors per thread;
+// every variant on GB300 over row widths of 128..2048 16-byte vectors in steps of 64, for each
+// dtype and op, at HBM-bound row counts (3 interleaved rounds, the median of each):
+//  * rows of at most 128 vectors (bf16/fp16 H <= 1024, fp32 H <= 512): one warp per row, 1/2/4
+//    vectors per lane, next row prefetched, up to 8 rows per CTA but never fewer CTAs than SMs
+//    when the rows allow it;
+//  * rows of up to 2048 vectors (bf16/fp16 H <= 16384, fp32 H <= 8192): one CTA per row, as wide
+//    as the row needs (a multiple of 32 threads). Which variant sustains the most bandwidth
+//    depends on the width, and the sweep picks:
+//      plain: 4 vectors per thread, no prefetch (fp32 rows of at most 384 vectors: 2 vectors,
+//        next row prefetched); rows wider than 1536 vectors stream through the staged
+//        shared-memory ring when there are enough rows to fill it;
+//      fused: no prefetch, 2 vectors per thread for rows of at most 768 vectors and for 961..1152
+//        vectors, 4 vectors per thread for 769..960 and 1153..1536 (fp32 rows of at most 384
+//        vectors: 2 vectors, next row prefetched). Wider rows: fp16, and bf16 below 1792 vectors,
+//        take the staged ring (2 stages) when there are enough rows; bf16 from 1792 vectors on
+//        prefetches at 4 vectors per thread; fp32 keeps 4 vectors without prefetch up to 1792
+//        vectors and takes the ring beyond.
+//    In the latency regime (rows <= SMs, so each CTA gets at most one row) prefetch has nothing
+//    to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8
+//    CTAs per row, plain rows of at most 1024 vectors take 2 vectors per thread, and the rest 4;
+//  * rows of 2049..16384 vectors (wider than one CTA's registers): a cluster of 2, 4 or 8 CTAs
+//    per row, each with at most 2048 vectors: the staged ring split over the cluster (fused, and
+//    plain rows of at most 3072 vectors) or the register-resident cluster kernel (wider plain
+//    rows, and at most SMs/8 rows of any kind);
 //  * anything else (H not a multiple of the vector, unaligned pointers, wider rows): the scalar
 //    two-pass kernel.
-// The grid is persistent: at most sm_count * blocks_per_sm CTAs.
-ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem, bool aligned16, int sm_count,
-                 int blocks_per_sm, ks_plan_t *p) {
+// The grid is persistent: at most sm_count * blocks_per_sm CTAs (for cluster plans, whole
+// clusters, which the launch caps again by the device's count of resident clusters).
+namespace {
+
+void cta_row(ks_plan_t *p, int64_t hv, int v, bool prefetch) {
+    p->kernel = KS_KERNEL_CTA_ROW;
+    p->vec_per_thread = v;
+    p->block = (int32_t)round_up(ceil_div(hv, v), 32);
+    p->team = p->block;
+    p->flags = prefetch ? 0 : KS_PLAN_NO_PREFETCH;
+}
+
+void bulk_row(ks_plan_t *p, int64_t hv, bool fused, int64_t stages) {
+    const int64_t stage = hv * 16 * (fused ? 2 : 1);
+    p->kernel = KS_KERNEL_BULK_ROW;
+    p->vec_per_thread = 4;
+    p->block = (int32_t)round_up(ceil_div(hv, 4), 32);
+    p->team = p->block;
+    p->flags = 0;
+    p->stages = (int32_t)stages;
+    p->smem_bytes = (int32_t)(kRingHeader + stages * stage);
+}
+
+}  // namespace
+
+ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
+                 int sm_count, int blocks_per_sm, ks_plan_t *p) {
     if (!p) return fail(KS_ERR_INVALID_ARGUMENT, "plan pointer is NULL");
     memset(p, 0, sizeof *p);
+    const int elem = elem_bytes(dtype);
+    if (elem == 0) return fail(KS_ERR_UNSUPPORTED_DTYPE, "dtype code %d is not a ks_dtype_t", (int)dtype);
     if (op != 0 && op != 1) return fail(KS_ERR_INVALID_ARGUMENT, "op must be 0 or 1");
-    if (hidden <= 0 || rows < 0 || sm_count <= 0 || blocks_per_sm < 0 ||
-        (elem != 2 && elem != 4))
+    if (hidden <= 0 || rows < 0 || sm_count <= 0 || blocks_per_sm < 0)
         return fail(KS_ERR_INVALID_ARGUMENT, "bad plan arguments");
     if (rows == 0) {
         p->kernel = KS_KERNEL_NONE;
         return KS_SUCCESS;
     }
+    const bool fused = op == 1;
     const int per_vec = 16 / elem;
     const bool vec_ok = aligned16 && hidden % per_vec == 0;
     const int64_t hv = vec_ok ? hidden / per_vec : 0;
+    const bool ring_rows = rows >= 4 * (int64_t)sm_count;  // enough rows to keep a ring busy
     int64_t rows_per_cta = 1;
     if (vec_ok && hv <= 128) {
         p->kernel = KS_KERNEL_WARP_ROW;
@@ -305,37 +377,69 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem, bool aligned16,
         teams = teams < 1 ? 1 : (teams > 8 ? 8 : teams);
         rows_per_cta = teams;
         p->block = (int32_t)(32 * teams);
+    } else if (vec_ok && hv <= 2048 && rows <= sm_count) {
+        // Latency regime, from a graph-replay sweep of few rows.
+        if (fused && hv >= 1792 && rows * 8 <= sm_count) {
+            p->kernel = KS_KERNEL_CLUSTER_ROW;
+            p->cluster = 8;
+            p->vec_per_thread = 1;
+            p->block = (int32_t)round_up(ceil_div(hv, 8), 32);
+            p->team = p->block * 8;
+        } else if (!fused && hv <= 1024) {
+            cta_row(p, hv, 2, true);
+        } else {
+            cta_row(p, hv, 4, fused);
+        }
     } else if (vec_ok && hv <= 2048) {
-        p->vec_per_thread = 4;
-        p->block = (int32_t)round_up(ceil_div(hv, 4), 32);
-        p->team = p->block;
-        p->kernel = KS_KERNEL_CTA_ROW;
-        if (op == 0) p->flags = KS_PLAN_NO_PREFETCH;
-        const int64_t stage = hv * 16;
-        if (op == 0 && hv > 1536 && rows >= 4 * (int64_t)sm_count) {
-            int64_t st = (96 * 1024) / stage;
-            st = st < 2 ? 2 : (st > 8 ? 8 : st);
-            p->kernel = KS_KERNEL_BULK_ROW;
-            p->flags = 0;
-            p->stages = (int32_t)st;
-            p->smem_bytes = (int32_t)(kRingHeader + st * stage);
-        } else if (rows <= sm_count) {
-            // Latency regime (at most one row per CTA), from a graph-replay sweep of few rows:
-            // the widest fused rows split over a cluster of 8 CTAs; narrower plain rows take
-            // twice the threads at 2 vectors each.
-            if (op == 1 && hv >= 1792 && rows * 8 <= sm_count) {
-                p->kernel = KS_KERNEL_CLUSTER_ROW;
-                p->cluster = 8;
-                p->vec_per_thread = 1;
-                p->block = (int32_t)round_up(ceil_div(hv, 8), 32);
-                p->team = p->block * 8;
-                p->flags = 0;
-            } else if (op == 0 && hv <= 1024) {
-                p->vec_per_thread = 2;
-                p->block = (int32_t)round_up(ceil_div(hv, 2), 32);
-                p->team = p->block;
-                p->flags = 0;
+        const bool f32 = dtype == KS_DTYPE_F32;
+        if (f32 && hv <= 384) {
+            cta_row(p, hv, 2, true);
+        } else if (!fused) {
+            if (hv > 1536 && ring_rows) {
+                int64_t st = (96 * 1024) / (hv * 16);
+                bulk_row(p, hv, false, st < 2 ? 2 : (st > 8 ? 8 : st));
+            } else {
+                cta_row(p, hv, 4, false);
             }
+        } else if (hv <= 1536) {
+            const bool two = hv <= 768 || (hv > 960 && hv <= 1152);
+            cta_row(p, hv, two ? 2 : 4, false);
+        } else if (dtype == KS_DTYPE_BF16 && hv >= 1792) {
+            cta_row(p, hv, 4, true);
+        } else if (f32 && hv <= 1792) {
+            cta_row(p, hv, 4, false);
+        } else if (ring_rows) {
+            bulk_row(p, hv, true, 2);
+        } else {
+            cta_row(p, hv, 4, true);
+        }
+    } else if (vec_ok && hv <= 16384) {
+        // Wider than one CTA's registers: split each row over a cluster of CTAs, each owning at
+        // most 2048 vectors (a probe of the variants at 2560..16384 vectors, many rows):
+        //   fused: the staged ring split over C = 2, 4 or 8 CTAs, 2 stages per CTA (two stages
+        //     beat deeper rings: two CTAs per SM hide more than one CTA's deeper ring);
+        //   plain: the same ring over 2 CTAs up to 3072 vectors, wider rows the register-resident
+        //     cluster kernel at 4 vectors per thread over 4 CTAs (8 beyond 8192 vectors).
+        // Few rows (at most SMs/8) take the register-resident cluster kernel with 8 CTAs per row.
+        int C = 2;
+        while (ceil_div(hv, C) > 2048) C *= 2;
+        if (rows * 8 <= sm_count) {
+            const int64_t slice = ceil_div(hv, 8);
+            p->kernel = KS_KERNEL_CLUSTER_ROW;
+            p->cluster = 8;
+            p->vec_per_thread = slice <= 512 ? 1 : (slice <= 1024 ? 2 : 4);
+            p->block = (int32_t)round_up(ceil_div(slice, p->vec_per_thread), 32);
+            p->team = p->block * 8;
+        } else if (fused || hv <= 3072) {
+            bulk_row(p, ceil_div(hv, C), fused, 2);
+            p->cluster = C;
+            p->team = p->block * C;
+        } else {
+            p->cluster = hv <= 8192 ? 4 : 8;
+            p->kernel = KS_KERNEL_CLUSTER_ROW;
+            p->vec_per_thread = 4;
+            p->block = (int32_t)round_up(ceil_div(ceil_div(hv, p->cluster), 4), 32);
+            p->team = p->block * p->cluster;
         }
     } else {
         p->kernel = KS_KERNEL_SCALAR;
@@ -343,7 +447,7 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem, bool aligned16,
         p->block = (int32_t)(b < 32 ? 32 : (b > 1024 ? 1024 : b));
         p->team = p->block;
     }
-    if (p->kernel == KS_KERNEL_CLUSTER_ROW) {  // whole clusters, one row each per pass
+    if (p->cluster >= 2) {  // whole clusters, one row each per pass
         int64_t clusters = rows;
         const int64_t cap = (int64_t)sm_count * blocks_per_sm / p->cluster;
         if (blocks_per_sm > 0 && clusters > cap) clusters = cap < 1 ? 1 : cap;
@@ -418,7 +522,7 @@ ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t 
                            ks_plan_t *plan) {
     const int e = ks::elem_bytes(dtype);
     if (e == 0) return ks::fail(KS_ERR_UNSUPPORTED_DTYPE, "dtype code %d is not a ks_dtype_t", (int)dtype);
-    return ks::plan(op, rows, hidden, e, aligned16 != 0, sm_count, blocks_per_sm, plan);
+    return ks::plan(op, rows, hidden, dtype, aligned16 != 0, sm_count, blocks_per_sm, plan);
 }
 
 ks_status_t ks_set_launch_options(int32_t options) {

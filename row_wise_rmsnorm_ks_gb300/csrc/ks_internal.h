@@ -42,16 +42,20 @@ int64_t host_chunk_rows(bool fused, int64_t hidden, int e, int64_t ws_bytes);
 // Whether ks_set_launch_options turned programmatic dependent launch on.
 bool launch_pdl_enabled();
 
-// Host heuristic: fills *p from the shape, the element size and the device's SM count.
+// Host heuristic: fills *p from the shape, the dtype and the device's SM count.
 // blocks_per_sm == 0 leaves grid at one pass over the rows.
-ks_status_t plan(int op, int64_t rows, int64_t hidden, int elem_bytes, bool aligned16,
+ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
                  int sm_count, int blocks_per_sm, ks_plan_t *p);
 
 // Per-dtype launchers (one translation unit each). `blocks_per_sm` queries the occupancy of the
-// kernel the plan names; `launch` enqueues it.
+// kernel the plan names; `max_clusters` how many of its clusters can be resident at once (plans
+// with cluster >= 2; 0 if the query fails); `launch` enqueues it.
 int blocks_per_sm_bf16(const ks_plan_t &p, bool fused);
 int blocks_per_sm_f16(const ks_plan_t &p, bool fused);
 int blocks_per_sm_f32(const ks_plan_t &p, bool fused);
+int max_clusters_bf16(const ks_plan_t &p, bool fused);
+int max_clusters_f16(const ks_plan_t &p, bool fused);
+int max_clusters_f32(const ks_plan_t &p, bool fused);
 // Reads (and with `clear`, zeroes) the device fault word of each translation unit's kernels on
 // the current device; returns the OR of them, or -1 if the read failed.
 int fault_flags_bf16(bool clear);

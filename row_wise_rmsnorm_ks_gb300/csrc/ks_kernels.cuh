@@ -178,9 +178,6 @@ __device__ __forceinline__ void load_row(const uint4 *base, int t, int g, int64_
     }
 }
 
-// One team (a warp, or the whole CTA) per row; row r's 16-byte vector c (of hv) is handled by
-// thread c % G of the team, as its (c / G)-th vector. Teams stride over rows by the number of
-// teams in the grid.
 // Hides a register's value from the optimiser, so values derived from it before this point are
 // not reused after it (the second pass unpacks the raw 16-bit vectors again instead of keeping
 // 8 floats per vector live across the row's reduction).
@@ -188,11 +185,77 @@ __device__ __forceinline__ void opaque(uint4 &v) {
     asm volatile("" : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w));
 }
 
+// One row of the vector kernel, its vectors already in registers (xc, and rc for the fused op):
+// the sum of squares (the fused op also forms s and stores cast(s) into the residual), the team
+// reduction through `red`, then normalise, weight, cast and store.
+template <typename T, int V, bool kFused, bool kWarpTeam, bool kOpaque>
+__device__ __forceinline__ void vec_row(const RowArgs &a, int64_t row, int t, int g,
+                                        uint4 (&xc)[V], uint4 (&rc)[V], uint4 (&wv)[V],
+                                        float *red) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    const int64_t hv = a.hv;
+    uint4 *og = static_cast<uint4 *>(a.out) + row * hv;
+    uint4 *rg = kFused ? static_cast<uint4 *>(a.res) + row * hv : nullptr;
+
+    SumSq acc;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        const int64_t c = t + (int64_t)k * g;
+        if (c < hv) {
+            float f[N];
+            E::unpack(xc[k], f);
+            if (kFused) {
+                float q[N];
+                E::unpack(rc[k], q);
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
+                __stcs(rg + c, E::pack(f));
+            }
+            acc.add(f);
+        }
+    }
+    const float ss = team_sum<kWarpTeam>(acc.total(), red);
+    const float scale = row_scale(ss, (float)a.hidden, a.eps);
+
+    if (kOpaque) {
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            opaque(xc[k]);
+            if (kFused) opaque(rc[k]);
+            opaque(wv[k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+        const int64_t c = t + (int64_t)k * g;
+        if (c < hv) {
+            float f[N], wf[N];
+            E::unpack(xc[k], f);
+            if (kFused) {
+                float q[N];
+                E::unpack(rc[k], q);
+#pragma unroll
+                for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
+            }
+            E::unpack(wv[k], wf);
+#pragma unroll
+            for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
+            __stcs(og + c, E::pack(f));
+        }
+    }
+}
+
+// One team (a warp, or the whole CTA) per row; row r's 16-byte vector c (of hv) is handled by
+// thread c % G of the team, as its (c / G)-th vector. Teams stride over rows by the number of
+// teams in the grid. With kPrefetch a team loads its next row while it works on the current one,
+// into two register buffers used in turn (the loop body is written out for both, so no buffer
+// is ever copied into the other: a copy would wait for the prefetched data at the end of every
+// row). Without it, each row is loaded when its turn comes, and the raw vectors are hidden from
+// the optimiser across the reduction (measured: this helps without prefetch, costs with it).
 template <typename T, int V, bool kFused, bool kWarpTeam, bool kPrefetch>
 __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
     rows_vec_kernel(const RowArgs a) {
-    using E = Elem<T>;
-    constexpr int N = E::kPerVec;
     __shared__ float red[2][32];
 
     const int g = kWarpTeam ? 32 : (int)blockDim.x;
@@ -200,11 +263,9 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
     const int teams = kWarpTeam ? (int)(blockDim.x >> 5) : 1;
     const int team = kWarpTeam ? (int)(threadIdx.x >> 5) : 0;
     const int64_t hv = a.hv;
-    const float h = (float)a.hidden;
 
     const uint4 *xg = static_cast<const uint4 *>(a.x);
-    uint4 *og = static_cast<uint4 *>(a.out);
-    uint4 *rg = static_cast<uint4 *>(a.res);
+    const uint4 *rg = static_cast<const uint4 *>(a.res);
 
     grid_dependency_wait();
     allow_dependents_launch();
@@ -220,83 +281,39 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
 
     int64_t row = (int64_t)blockIdx.x * teams + team;
     const int64_t stride = (int64_t)gridDim.x * teams;
-    uint4 xc[V], rc[V];
-    if (kPrefetch && row < a.rows) {
-        load_row<V>(xg + row * hv, t, g, hv, xc);
-        if (kFused) load_row<V>(rg + row * hv, t, g, hv, rc);
-    }
-    int parity = 0;
-    while (row < a.rows) {
-        const int64_t next = row + stride;
-        uint4 xn[V], rn[V];
-#pragma unroll
-        for (int k = 0; k < V; ++k) xn[k] = rn[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (!kPrefetch) {
+    if (!kPrefetch) {
+        int parity = 0;
+        for (; row < a.rows; row += stride) {
+            uint4 xc[V], rc[V];
             load_row<V>(xg + row * hv, t, g, hv, xc);
             if (kFused) load_row<V>(rg + row * hv, t, g, hv, rc);
-        } else if (next < a.rows) {
-            load_row<V>(xg + next * hv, t, g, hv, xn);
-            if (kFused) load_row<V>(rg + next * hv, t, g, hv, rn);
+            vec_row<T, V, kFused, kWarpTeam, true>(a, row, t, g, xc, rc, wv, red[parity]);
+            parity ^= 1;
         }
+        return;
+    }
 
-        // Sum of squares; the fused op also forms s and stores cast(s) into the residual.
-        SumSq acc;
-#pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
-                float f[N];
-                E::unpack(xc[k], f);
-                if (kFused) {
-                    float q[N];
-                    E::unpack(rc[k], q);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
-                    __stcs(rg + row * hv + c, E::pack(f));
-                }
-                acc.add(f);
-            }
+    uint4 xa[V], ra[V], xb[V], rb[V];
+    if (row < a.rows) {
+        load_row<V>(xg + row * hv, t, g, hv, xa);
+        if (kFused) load_row<V>(rg + row * hv, t, g, hv, ra);
+    }
+    while (row < a.rows) {
+        int64_t next = row + stride;
+        if (next < a.rows) {
+            load_row<V>(xg + next * hv, t, g, hv, xb);
+            if (kFused) load_row<V>(rg + next * hv, t, g, hv, rb);
         }
-        const float ss = team_sum<kWarpTeam>(acc.total(), red[parity]);
-        parity ^= 1;
-        const float scale = row_scale(ss, h, a.eps);
-
-        // Normalise, weight, cast, store.
-        if (!kPrefetch) {  // measured: helps without prefetch, costs with it
-#pragma unroll
-            for (int k = 0; k < V; ++k) {
-                opaque(xc[k]);
-                if (kFused) opaque(rc[k]);
-                opaque(wv[k]);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
-                float f[N], wf[N];
-                E::unpack(xc[k], f);
-                if (kFused) {
-                    float q[N];
-                    E::unpack(rc[k], q);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
-                }
-                E::unpack(wv[k], wf);
-#pragma unroll
-                for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
-                __stcs(og + row * hv + c, E::pack(f));
-            }
-        }
-
+        vec_row<T, V, kFused, kWarpTeam, false>(a, row, t, g, xa, ra, wv, red[0]);
         row = next;
-        if (kPrefetch) {
-#pragma unroll
-            for (int k = 0; k < V; ++k) {
-                xc[k] = xn[k];
-                rc[k] = rn[k];
-            }
+        if (row >= a.rows) break;
+        next = row + stride;
+        if (next < a.rows) {
+            load_row<V>(xg + next * hv, t, g, hv, xa);
+            if (kFused) load_row<V>(rg + next * hv, t, g, hv, ra);
         }
+        vec_row<T, V, kFused, kWarpTeam, false>(a, row, t, g, xb, rb, wv, red[1]);
+        row = next;
     }
 }
 
@@ -356,40 +373,65 @@ __global__ void __launch_bounds__(1024) rows_scalar_kernel(const RowArgs a) {
 // waits on the barrier, copies its vectors to registers, and computes as before. The row's
 // barrier in the CTA reduction is also the point after which the stage is free, so thread 0
 // refills it with the row `stages` iterations ahead right after that barrier.
-// Shared memory: 128 bytes of barriers, then stages x (1 or 2) x H*e bytes.
-// Every wait is bounded: on a time-out the CTA records kFaultWaitTimeout, waits (bounded) for the
-// copies it still has in flight, and returns.
-template <typename T, int V, bool kFused>
+//
+// kCluster: rows too wide for one CTA's registers are split over a thread-block cluster of C
+// CTAs. CTA rank q owns the row's vectors [q*S, min(hv, (q+1)*S)), S = ceil(hv / C), and streams
+// that slice through its own ring; each CTA publishes its partial sum of squares (and whether a
+// wait of its timed out) in its shared memory, and after one cluster barrier every thread adds
+// the C partials in rank order through distributed shared memory, so the whole cluster computes
+// one scale. Partials alternate between two slots per row (a CTA overwrites a slot only after the
+// next row's cluster barrier, which its peers reach only after reading it). Stages are refilled
+// only after the cluster barrier, once the row is known to be good everywhere.
+//
+// Shared memory: 128 bytes of barriers, then stages x (1 or 2) x S*16 bytes.
+// Every wait is bounded: on a time-out the CTA records kFaultWaitTimeout; the CTA (with kCluster,
+// the whole cluster, which learns of it at the row's cluster barrier) stops at that row, each CTA
+// waits (bounded) for the copies it still has in flight, and returns.
+template <typename T, int V, bool kFused, bool kCluster>
 __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
+    namespace cg = cooperative_groups;
     using E = Elem<T>;
     constexpr int N = E::kPerVec;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[2][32];
+    __shared__ float part[2];
+    __shared__ int bad_slot[2];
 
+    int C = 1, q = 0;
+    if (kCluster) {
+        cg::cluster_group cluster = cg::this_cluster();
+        C = (int)cluster.num_blocks();
+        q = (int)cluster.block_rank();
+    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     unsigned char *ring = smem + 128;
     const int g = blockDim.x;
     const int t = threadIdx.x;
     const int64_t hv = a.hv;
+    const int64_t S = kCluster ? (hv + C - 1) / C : hv;
+    const int64_t lo = kCluster ? q * S : 0;
+    const int64_t nv = (lo + S < hv ? lo + S : hv) - lo;  // this CTA's vectors (>= 1)
     const int stages = a.stages;
-    const uint32_t row_bytes = (uint32_t)(hv * 16);
-    const uint32_t stage_bytes = kFused ? 2u * row_bytes : row_bytes;
+    const uint32_t copy_bytes = (uint32_t)(nv * 16);
+    const uint32_t slot_bytes = (uint32_t)(S * 16);  // the residual's slice follows the x slice
+    const uint32_t stage_bytes = kFused ? 2u * slot_bytes : slot_bytes;
     const float h = (float)a.hidden;
-    const int64_t step = gridDim.x;
+    const int64_t first = kCluster ? blockIdx.x / C : blockIdx.x;
+    const int64_t step = kCluster ? gridDim.x / C : gridDim.x;
 
-    const uint4 *xg = static_cast<const uint4 *>(a.x);
-    uint4 *og = static_cast<uint4 *>(a.out);
-    uint4 *rg = static_cast<uint4 *>(a.res);
+    const uint4 *xg = static_cast<const uint4 *>(a.x) + lo;
+    uint4 *og = static_cast<uint4 *>(a.out) + lo;
+    uint4 *rg = kFused ? static_cast<uint4 *>(a.res) + lo : nullptr;
 
     grid_dependency_wait();
     allow_dependents_launch();
     uint4 wv[V];
     {
-        const uint4 *wg = static_cast<const uint4 *>(a.w);
+        const uint4 *wg = static_cast<const uint4 *>(a.w) + lo;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            wv[k] = (c < hv) ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+            wv[k] = (c < nv) ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
         }
     }
 
@@ -401,14 +443,14 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
     __syncthreads();
     auto issue = [&](int s, int64_t row) {
         unsigned char *dst = ring + (size_t)s * stage_bytes;
-        mbar_arrive_expect_tx(&bars[s], stage_bytes);
-        bulk_g2s(dst, xg + row * hv, row_bytes, &bars[s], policy);
-        if (kFused) bulk_g2s(dst + row_bytes, rg + row * hv, row_bytes, &bars[s], policy);
+        mbar_arrive_expect_tx(&bars[s], kFused ? 2u * copy_bytes : copy_bytes);
+        bulk_g2s(dst, xg + row * hv, copy_bytes, &bars[s], policy);
+        if (kFused) bulk_g2s(dst + slot_bytes, rg + row * hv, copy_bytes, &bars[s], policy);
     };
     if (t == 0) {
         policy = l2_evict_first_policy();
         for (int s = 0; s < stages; ++s) {
-            const int64_t row = blockIdx.x + (int64_t)s * step;
+            const int64_t row = first + (int64_t)s * step;
             if (row >= a.rows) break;
             issue(s, row);
         }
@@ -417,7 +459,7 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
     int s = 0;
     uint32_t phase = 0;
     int parity = 0;
-    int64_t row = blockIdx.x;
+    int64_t row = first;
     bool fault = false;
     for (; row < a.rows; row += step) {
         const bool ok = mbar_wait_bounded(&bars[s], phase);
@@ -426,43 +468,68 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            const bool in = ok && c < hv;
+            const bool in = ok && c < nv;
             xv[k] = in ? ld_shared_v4(sx + c * 16) : make_uint4(0u, 0u, 0u, 0u);
-            if (kFused) rv[k] = in ? ld_shared_v4(sx + row_bytes + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+            if (kFused) rv[k] = in ? ld_shared_v4(sx + slot_bytes + c * 16) : make_uint4(0u, 0u, 0u, 0u);
         }
 
         SumSq acc;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            if (ok && c < hv) {
+            if (ok && c < nv) {
                 float f[N];
                 E::unpack(xv[k], f);
                 if (kFused) {
-                    float q[N];
-                    E::unpack(rv[k], q);
+                    float q2[N];
+                    E::unpack(rv[k], q2);
 #pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
+                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q2[e]);
                     __stcs(rg + row * hv + c, E::pack(f));
                 }
                 acc.add(f);
             }
         }
-        const float part = warp_sum(acc.total());
-        if ((t & 31) == 0) red[parity][t >> 5] = part;
+        const float wsum = warp_sum(acc.total());
+        if ((t & 31) == 0) red[parity][t >> 5] = wsum;
         // The CTA barrier of this row: partial sums are visible, every thread has its stage data
         // in registers (so the stage may be refilled), and a time-out anywhere is seen by all.
-        if (__syncthreads_or(!ok)) {
-            fault = true;
-            break;
-        }
-        if (t == 0) {
-            const int64_t ahead = row + (int64_t)stages * step;
-            if (ahead < a.rows) issue(s, ahead);
-        }
+        const bool bad = __syncthreads_or(!ok);
         float ss = 0.0f;
         const int nw = g >> 5;
-        for (int i = 0; i < nw; ++i) ss += red[parity][i];
+        if (!kCluster) {
+            if (bad) {
+                fault = true;
+                break;
+            }
+            if (t == 0) {
+                const int64_t ahead = row + (int64_t)stages * step;
+                if (ahead < a.rows) issue(s, ahead);
+            }
+            for (int i = 0; i < nw; ++i) ss += red[parity][i];
+        } else {
+            cg::cluster_group cluster = cg::this_cluster();
+            if (t == 0) {
+                float cta = 0.0f;
+                for (int i = 0; i < nw; ++i) cta += red[parity][i];
+                part[parity] = cta;
+                bad_slot[parity] = bad ? 1 : 0;
+            }
+            cluster.sync();  // every CTA's partial and time-out flag for this row is published
+            int any_bad = 0;
+            for (int r = 0; r < C; ++r) {
+                ss += *cluster.map_shared_rank(&part[parity], r);
+                any_bad |= *cluster.map_shared_rank(&bad_slot[parity], r);
+            }
+            if (any_bad) {
+                fault = true;
+                break;
+            }
+            if (t == 0) {
+                const int64_t ahead = row + (int64_t)stages * step;
+                if (ahead < a.rows) issue(s, ahead);
+            }
+        }
         parity ^= 1;
         const float scale = row_scale(ss, h, a.eps);
 
@@ -475,14 +542,14 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
+            if (c < nv) {
                 float f[N], wf[N];
                 E::unpack(xv[k], f);
                 if (kFused) {
-                    float q[N];
-                    E::unpack(rv[k], q);
+                    float q2[N];
+                    E::unpack(rv[k], q2);
 #pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
+                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q2[e]);
                 }
                 E::unpack(wv[k], wf);
 #pragma unroll
@@ -508,6 +575,7 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
             }
         }
     }
+    if (kCluster) cg::this_cluster().sync();  // peers may still be reading this CTA's partials
 }
 
 // ------------------------------------------------------------------ cluster row kernel
@@ -649,7 +717,9 @@ const void *pick_kernel(const ks_plan_t &p) {
     }
     case KS_KERNEL_SCALAR: return (const void *)rows_scalar_kernel<T, kFused>;
     case KS_KERNEL_BULK_ROW:
-        return p.vec_per_thread == 4 ? (const void *)rows_bulk_kernel<T, 4, kFused> : nullptr;
+        if (p.vec_per_thread != 4) return nullptr;
+        return p.cluster >= 2 ? (const void *)rows_bulk_kernel<T, 4, kFused, true>
+                              : (const void *)rows_bulk_kernel<T, 4, kFused, false>;
     case KS_KERNEL_CLUSTER_ROW:
         switch (p.vec_per_thread) {
         case 1: return (const void *)rows_cluster_kernel<T, 1, kFused>;
@@ -692,6 +762,28 @@ int blocks_per_sm_t(const ks_plan_t &p, bool fused) {
     return n;
 }
 
+// Clusters of the plan's kernel that can be resident at once on the current device (0 when the
+// query fails), so a persistent grid of clusters never waits for a second wave.
+template <typename T>
+int max_clusters_t(const ks_plan_t &p, bool fused) {
+    const void *f = fused ? pick_kernel<T, true>(p) : pick_kernel<T, false>(p);
+    if (!f || p.cluster < 2 || blocks_per_sm_t<T>(p, fused) < 0) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.cluster);
+    cfg.blockDim = dim3((unsigned)p.block);
+    cfg.dynamicSmemBytes = dynamic_smem(p);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)p.cluster;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
 inline int fault_flags_t(bool clear) {
     unsigned int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_fault_flags, sizeof v) != cudaSuccess) return -1;
@@ -708,7 +800,7 @@ cudaError_t launch_t(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStrea
     if (!f) return cudaErrorInvalidConfiguration;
     RowArgs copy = a;
     void *args[] = {&copy};
-    const bool cluster = p.kernel == KS_KERNEL_CLUSTER_ROW;
+    const bool cluster = p.cluster >= 2;  // the cluster-row kernel, or the staged one split
     if (!(p.flags & KS_PLAN_PDL) && !cluster)
         return cudaLaunchKernel(f, dim3((unsigned)p.grid), dim3((unsigned)p.block), args,
                                 dynamic_smem(p), s);
@@ -743,6 +835,9 @@ cudaError_t launch_t(const ks_plan_t &p, bool fused, const RowArgs &a, cudaStrea
     namespace ks {                                                                            \
     int blocks_per_sm_##SUFFIX(const ks_plan_t &p, bool fused) {                              \
         return blocks_per_sm_t<TYPE>(p, fused);                                               \
+    }                                                                                         \
+    int max_clusters_##SUFFIX(const ks_plan_t &p, bool fused) {                               \
+        return max_clusters_t<TYPE>(p, fused);                                                \
     }                                                                                         \
     cudaError_t launch_##SUFFIX(const ks_plan_t &p, bool fused, const RowArgs &a,             \
                                 cudaStream_t s) {                                             \

@@ -49,7 +49,9 @@ int main(void) {
     ks_plan_t p;
     expect(ks_plan_launch(1, 32768, 8192, KS_DTYPE_BF16, 1, 152, 2, &p), KS_SUCCESS, "plan");
     expect(p.kernel, KS_KERNEL_CTA_ROW, "plan kernel");
-    expect(p.block, 256, "plan block");
+    expect(p.vec_per_thread, 2, "plan vectors per thread");
+    expect(p.block, 512, "plan block");
+    expect(p.flags, KS_PLAN_NO_PREFETCH, "plan flags");
     expect(ks_set_launch_options(KS_LAUNCH_PDL), KS_SUCCESS, "options on");
     expect(ks_get_launch_options(), KS_LAUNCH_PDL, "options read");
     expect(ks_set_launch_options(0), KS_SUCCESS, "options off");

@@ -130,36 +130,71 @@ def test_warp_per_row_spreads_few_rows_over_sms():
     assert p.block == 32 and p.grid == 128  # 128 rows on 128 SMs
 
 
-@pytest.mark.parametrize("hidden,block", [(1536, 64), (4096, 128), (5120, 160), (7168, 224),
-                                          (8192, 256), (14336, 448), (16384, 512)])
-def test_wide_rows_take_cta_per_row(hidden, block):
-    # fused: registers, next row prefetched
-    p = plan(1, 32768, hidden)
-    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == block and p.team == block
-    assert p.vec_per_thread * 8 * p.block >= hidden and p.stages == 0 and p.flags == 0
-    # plain: registers without prefetch, or the staged ring for the widest rows with many rows
-    p = plan(0, 32768, hidden)
-    assert p.block == block and p.team == block
-    if hidden > 1536 * 8:
-        assert p.kernel == _abi.KS_KERNEL_BULK_ROW and p.flags == 0
-        assert 2 <= p.stages <= 8 and p.smem_bytes == 128 + p.stages * hidden * 2
-        assert p.smem_bytes <= 226 * 1024
-    else:
-        assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.flags == _abi.KS_PLAN_NO_PREFETCH
+# bf16 widths and the plan the sweep picks at HBM-bound row counts: (kernel, vectors/thread,
+# prefetch) for the fused op, then for the plain op.
+CTA, BULK = _abi.KS_KERNEL_CTA_ROW, _abi.KS_KERNEL_BULK_ROW
+WIDE_BF16 = [
+    (1536, (CTA, 2, False), (CTA, 4, False)),
+    (4096, (CTA, 2, False), (CTA, 4, False)),
+    (5120, (CTA, 2, False), (CTA, 4, False)),
+    (7168, (CTA, 4, False), (CTA, 4, False)),
+    (8192, (CTA, 2, False), (CTA, 4, False)),
+    (9216, (CTA, 2, False), (CTA, 4, False)),
+    (12288, (CTA, 4, False), (CTA, 4, False)),
+    (13312, (BULK, 4, True), (BULK, 4, True)),
+    (14336, (CTA, 4, True), (BULK, 4, True)),
+    (16384, (CTA, 4, True), (BULK, 4, True)),
+]
+
+
+@pytest.mark.parametrize("hidden,fused_plan,plain_plan", WIDE_BF16)
+def test_wide_rows_take_cta_per_row(hidden, fused_plan, plain_plan):
+    for op, want in ((1, fused_plan), (0, plain_plan)):
+        p = plan(op, 32768, hidden)
+        kernel, v, prefetch = want
+        assert (p.kernel, p.vec_per_thread) == (kernel, v), (op, hidden)
+        assert p.block == -(-hidden // (8 * v) // 32) * 32 and p.team == p.block
+        assert p.vec_per_thread * 8 * p.block >= hidden
+        if kernel == BULK:
+            stage = hidden * 2 * (2 if op == 1 else 1)
+            assert p.flags == 0 and 2 <= p.stages <= 8
+            assert p.smem_bytes == 128 + p.stages * stage <= 226 * 1024
+        else:
+            assert p.stages == 0
+            assert p.flags == (0 if prefetch else _abi.KS_PLAN_NO_PREFETCH)
     # few rows: never the staged ring
-    assert plan(0, 100, hidden).kernel == _abi.KS_KERNEL_CTA_ROW
+    assert plan(0, 100, hidden).kernel == CTA
+    assert plan(1, 300, hidden).kernel == CTA
+
+
+def test_fp16_wide_fused_rows_take_the_ring():
+    p = plan(1, 32768, 14336, dtype=F16)
+    assert p.kernel == BULK and p.stages == 2 and p.block == 448
+    p = plan(1, 32768, 7168, dtype=F16)
+    assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags == _abi.KS_PLAN_NO_PREFETCH
+
+
+def test_latency_regime_keeps_one_row_per_cta_plans():
+    p = plan(1, 100, 8192)  # fused, few rows: 4 vectors, prefetch on (nothing to fetch)
+    assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags == 0
+    p = plan(0, 100, 8192)  # plain, <= 1024 vectors: 2 vectors per thread
+    assert p.kernel == CTA and p.vec_per_thread == 2 and p.block == 512
+    p = plan(1, 4, 16384)  # fused, widest rows, few rows: a cluster of 8 CTAs per row
+    assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == 8
 
 
 def test_fp32_counts_four_elements_per_vector():
     # 4096 fp32 = 1024 vectors: few rows take 2 vectors per thread (512 threads)
     p = plan(0, 10, 4096, dtype=F32)
     assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 512 and p.vec_per_thread == 2
-    p = plan(1, 1000, 4096, dtype=F32)
-    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 256
+    p = plan(1, 1000, 4096, dtype=F32)  # 1024 vectors, fused: 2 vectors per thread
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 512 and p.vec_per_thread == 2
+    p = plan(0, 32768, 1024, dtype=F32)  # 256 vectors: 2 vectors, next row prefetched
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.vec_per_thread == 2 and p.flags == 0
 
 
 @pytest.mark.parametrize("hidden,aligned", [(17, True), (1001, True), (4096, False),
-                                            (20000, True), (65536, True)])
+                                            (20004, True), (140000, True)])
 def test_scalar_fallback(hidden, aligned):
     p = plan(1, 7, hidden, aligned=aligned)
     assert p.kernel == _abi.KS_KERNEL_SCALAR
@@ -204,6 +239,61 @@ def test_plan_invariants_over_a_sweep(dtype):
                     assert p.grid % p.cluster == 0 and 2 <= p.cluster <= 8
                 if p.kernel == _abi.KS_KERNEL_BULK_ROW:
                     assert p.smem_bytes <= 226 * 1024 and p.stages >= 2
+                    assert p.cluster == 0 or (p.grid % p.cluster == 0 and 2 <= p.cluster <= 8)
+
+
+@pytest.mark.parametrize("hidden,dtype,cluster", [(20000, BF16, 2), (32768, BF16, 2),
+                                                  (65536, BF16, 4), (131072, BF16, 8),
+                                                  (12288, F32, 2), (16384, F32, 2),
+                                                  (32768, F32, 4)])
+def test_rows_wider_than_registers_split_over_a_cluster(hidden, dtype, cluster):
+    e = 4 if dtype == F32 else 2
+    hv = hidden * e // 16
+    slice_ = -(-hv // cluster)
+    assert slice_ <= 2048 and (cluster == 2 or -(-hv // (cluster // 2)) > 2048)
+    for op in (0, 1):
+        p = plan(op, 65536, hidden, dtype=dtype, bps=1)
+        if op == 1 or hv <= 3072:
+            # many rows: each CTA streams its slice through its own staged ring (2 stages)
+            assert p.kernel == _abi.KS_KERNEL_BULK_ROW and p.cluster == cluster
+            assert p.vec_per_thread == 4 and p.block == -(-slice_ // 4 // 32) * 32 <= 512
+            stage = slice_ * 16 * (2 if op else 1)
+            assert p.stages == 2 and p.smem_bytes == 128 + 2 * stage <= 226 * 1024
+        else:
+            # wide plain rows: the register-resident cluster kernel, 4 or 8 CTAs
+            c = 4 if hv <= 8192 else 8
+            assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == c
+            assert p.vec_per_thread == 4 and p.block * 4 * c >= hv and p.block <= 512
+        assert p.team == p.block * p.cluster and p.grid % p.cluster == 0
+        assert p.grid == 152 // p.cluster * p.cluster and p.rows_per_pass == 152 // p.cluster
+        # few rows: the register-resident cluster kernel, 8 CTAs per row
+        p = plan(op, 3, hidden, dtype=dtype, bps=1)
+        assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == 8
+        assert p.block * p.vec_per_thread * 8 >= hv and p.grid == 24
+
+
+def test_split_staged_plans_are_checked():
+    a, b, w = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    mk = _abi.make_plan
+    rows, hidden = 64, 32768  # 4096 vectors of bf16
+    ok = mk(_abi.KS_KERNEL_BULK_ROW, 4, 512, 2, cluster=2)
+    bad = [
+        mk(_abi.KS_KERNEL_BULK_ROW, 4, 256, 2, cluster=2),   # 256 x 4 < the 2048-vector slice
+        mk(_abi.KS_KERNEL_BULK_ROW, 4, 512, 2, cluster=9),   # cluster over 8
+        mk(_abi.KS_KERNEL_BULK_ROW, 4, 512, 8, cluster=2),   # 8 x 32 KB > 226 KB
+        mk(_abi.KS_KERNEL_BULK_ROW, 4, 512, 2, cluster=1),   # one CTA cannot hold 4096 vectors
+    ]
+    for p in bad:
+        assert _abi.ks_rms_norm_planned(a, b, w, rows, hidden, 1e-6, BF16, p, None) == E
+    # fused: two slices per stage, 4 x 64 KB does not fit
+    p = mk(_abi.KS_KERNEL_BULK_ROW, 4, 512, 4, cluster=2)
+    assert _abi.ks_fused_add_rms_norm_planned(a, b, w, rows, hidden, 1e-6, BF16, p, None) == E
+    # a cluster so large that one of its CTAs would own no vector (8 CTAs, 7 vectors)
+    p = mk(_abi.KS_KERNEL_BULK_ROW, 4, 32, 2, cluster=8)
+    assert _abi.ks_rms_norm_planned(a, b, w, rows, 56, 1e-6, BF16, p, None) == E
+    assert "without vectors" in _abi.ks_last_error()
+    del ok
 
 
 def test_planned_entry_points_reject_plans_that_do_not_fit():
