@@ -312,10 +312,9 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 //        shared-memory ring when there are enough rows to fill it;
 //      fused: no prefetch, 2 vectors per thread for rows of at most 768 vectors and for 961..1152
 //        vectors, 4 vectors per thread for 769..960 and 1153..1536 (fp32 rows of at most 384
-//        vectors: 2 vectors, next row prefetched). Wider rows: fp16, and bf16 below 1792 vectors,
-//        take the staged ring (2 stages) when there are enough rows; bf16 from 1792 vectors on
-//        prefetches at 4 vectors per thread; fp32 keeps 4 vectors without prefetch up to 1792
-//        vectors and takes the ring beyond.
+//        vectors: 2 vectors, next row prefetched). Wider rows: bf16 prefetches at 4 vectors per
+//        thread; fp16 takes the staged ring (2 stages) when there are enough rows; fp32 keeps 4
+//        vectors without prefetch up to 1792 vectors and takes the ring beyond.
 //    In the latency regime (rows <= SMs, so each CTA gets at most one row) prefetch has nothing
 //    to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8
 //    CTAs per row, plain rows of at most 1024 vectors take 2 vectors per thread, and the rest 4;
@@ -404,7 +403,7 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         } else if (hv <= 1536) {
             const bool two = hv <= 768 || (hv > 960 && hv <= 1152);
             cta_row(p, hv, two ? 2 : 4, false);
-        } else if (dtype == KS_DTYPE_BF16 && hv >= 1792) {
+        } else if (dtype == KS_DTYPE_BF16) {
             cta_row(p, hv, 4, true);
         } else if (f32 && hv <= 1792) {
             cta_row(p, hv, 4, false);

@@ -248,11 +248,12 @@ __device__ __forceinline__ void vec_row(const RowArgs &a, int64_t row, int t, in
 
 // One team (a warp, or the whole CTA) per row; row r's 16-byte vector c (of hv) is handled by
 // thread c % G of the team, as its (c / G)-th vector. Teams stride over rows by the number of
-// teams in the grid. With kPrefetch a team loads its next row while it works on the current one,
-// into two register buffers used in turn (the loop body is written out for both, so no buffer
-// is ever copied into the other: a copy would wait for the prefetched data at the end of every
-// row). Without it, each row is loaded when its turn comes, and the raw vectors are hidden from
-// the optimiser across the reduction (measured: this helps without prefetch, costs with it).
+// teams in the grid. With kPrefetch a team loads its next row while it works on the current one
+// and moves it into the current buffer at the end of the row. (Writing the loop body out twice
+// for two buffers used in turn, with no copy, measured 2-20 points slower for bf16 on GB300 and
+// no faster for fp16.) Without it, each row is loaded when its turn comes, and the raw vectors
+// are hidden from the optimiser across the reduction (measured: this helps without prefetch,
+// costs with it).
 template <typename T, int V, bool kFused, bool kWarpTeam, bool kPrefetch>
 __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
     rows_vec_kernel(const RowArgs a) {
@@ -293,27 +294,29 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
         return;
     }
 
-    uint4 xa[V], ra[V], xb[V], rb[V];
+    uint4 xc[V], rc[V];
     if (row < a.rows) {
-        load_row<V>(xg + row * hv, t, g, hv, xa);
-        if (kFused) load_row<V>(rg + row * hv, t, g, hv, ra);
+        load_row<V>(xg + row * hv, t, g, hv, xc);
+        if (kFused) load_row<V>(rg + row * hv, t, g, hv, rc);
     }
+    int parity = 0;
     while (row < a.rows) {
-        int64_t next = row + stride;
+        const int64_t next = row + stride;
+        uint4 xn[V], rn[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k) xn[k] = rn[k] = make_uint4(0u, 0u, 0u, 0u);
         if (next < a.rows) {
-            load_row<V>(xg + next * hv, t, g, hv, xb);
-            if (kFused) load_row<V>(rg + next * hv, t, g, hv, rb);
+            load_row<V>(xg + next * hv, t, g, hv, xn);
+            if (kFused) load_row<V>(rg + next * hv, t, g, hv, rn);
         }
-        vec_row<T, V, kFused, kWarpTeam, false>(a, row, t, g, xa, ra, wv, red[0]);
+        vec_row<T, V, kFused, kWarpTeam, false>(a, row, t, g, xc, rc, wv, red[parity]);
+        parity ^= 1;
         row = next;
-        if (row >= a.rows) break;
-        next = row + stride;
-        if (next < a.rows) {
-            load_row<V>(xg + next * hv, t, g, hv, xa);
-            if (kFused) load_row<V>(rg + next * hv, t, g, hv, ra);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            xc[k] = xn[k];
+            rc[k] = rn[k];
         }
-        vec_row<T, V, kFused, kWarpTeam, false>(a, row, t, g, xb, rb, wv, red[1]);
-        row = next;
     }
 }
 

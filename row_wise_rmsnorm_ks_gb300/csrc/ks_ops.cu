@@ -167,11 +167,13 @@ __global__ void __launch_bounds__(256) silu_mul_scalar_kernel(void *out, const v
 
 // ------------------------------------------------------------------------------ Softmax
 
-// One CTA per row, V 16-byte vectors per thread held in registers; persistent over rows, the
-// next row's vectors loaded before the current row's two reductions. The maximum is a plain
-// fmaxf (NaN-ignoring): a NaN or +inf in the row still makes the sum, and so every output, NaN,
-// and a row of only -inf still gets max -inf and z = NaN, so the contract's non-finite rules hold.
-template <typename T, int V>
+// One CTA per row, V 16-byte vectors per thread held in registers; persistent over rows. With
+// kPrefetch the next row's vectors are loaded before the current row's two reductions; without
+// it each row is loaded when its turn comes (fewer registers, more resident warps: faster up to
+// 1024 vectors per row on GB300, slower beyond). The maximum is a plain fmaxf (NaN-ignoring): a
+// NaN or +inf in the row still makes the sum, and so every output, NaN, and a row of only -inf
+// still gets max -inf and z = NaN, so the contract's non-finite rules hold.
+template <typename T, int V, bool kPrefetch>
 __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void *x, int64_t rows,
                                                           int64_t hv) {
     using E = Elem<T>;
@@ -188,7 +190,8 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
 #pragma unroll
     for (int k = 0; k < V; ++k) {
         const int64_t c = t + (int64_t)k * g;
-        cur[k] = (row < rows && c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+        cur[k] = (kPrefetch && row < rows && c < hv) ? __ldcs(xg + row * hv + c)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
     }
     for (; row < rows; row += gridDim.x) {
         const int64_t next = row + gridDim.x;
@@ -196,7 +199,10 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            nxt[k] = (next < rows && c < hv) ? __ldcs(xg + next * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+            if (kPrefetch)
+                nxt[k] = (next < rows && c < hv) ? __ldcs(xg + next * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+            else
+                cur[k] = (c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
         }
         float f[V][N];
         float m = -INFINITY;
@@ -241,8 +247,10 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
                 __stcs(og + row * hv + c, E::pack(f[k]));
             }
         }
+        if (kPrefetch) {
 #pragma unroll
-        for (int k = 0; k < V; ++k) cur[k] = nxt[k];
+            for (int k = 0; k < V; ++k) cur[k] = nxt[k];
+        }
     }
 }
 
@@ -563,9 +571,11 @@ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up64(int64_t a, int64_t b) { return ceil_div64(a, b) * b; }
 
 // Vectors per thread and block for a register-resident row of hv vectors: 1 vector below 64,
-// 2 below 512, else 4; the block a multiple of 32 (at most 512). 0 if the row does not fit.
+// 2 below 128, else 4 (measured on GB300 for Softmax and LayerNorm at 128..512 vectors: 4
+// vectors per thread beat 2 by 2-12 points); the block a multiple of 32 (at most 512). 0 if the
+// row does not fit.
 int row_vec_plan(int64_t hv, int *block) {
-    const int v = hv < 64 ? 1 : (hv < 512 ? 2 : 4);
+    const int v = hv < 64 ? 1 : (hv < 128 ? 2 : 4);
     const int64_t b = round_up64(ceil_div64(hv, v), 32);
     if (b > 512) return 0;
     *block = (int)b;
@@ -622,9 +632,14 @@ cudaError_t softmax_dispatch(int v, int block, void *out, const void *x, int64_t
     void *args[] = {&out, const_cast<void **>(&x), &nr, &wd};
     const void *f;
     switch (v) {
-    case 1: f = (const void *)softmax_vec_kernel<T, 1>; break;
-    case 2: f = (const void *)softmax_vec_kernel<T, 2>; break;
-    case 4: f = (const void *)softmax_vec_kernel<T, 4>; break;
+    case 1: f = (const void *)softmax_vec_kernel<T, 1, true>; break;
+    case 2: f = (const void *)softmax_vec_kernel<T, 2, true>; break;
+    case 4:
+        // measured on GB300 (bf16, HBM-bound rows): without prefetch 0.92-0.97 of the copy peak
+        // for rows of 128..1024 vectors against 0.85-0.93 with it; beyond, prefetch wins
+        f = width <= 1024 ? (const void *)softmax_vec_kernel<T, 4, false>
+                          : (const void *)softmax_vec_kernel<T, 4, true>;
+        break;
     default:
         f = (const void *)softmax_scalar_kernel<T>;
         block = (int)round_up64(ceil_div64(width, 8), 32);
@@ -654,10 +669,11 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
     void *sc_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
                        const_cast<void **>(&b), &nr, &hd, &ep};
     void **args = vec_args;
-    // Many rows of a vectorisable width: the staged ring (KS_LN_RING_BYTES of rows per CTA, 2..8
-    // stages) keeps enough bytes in flight; otherwise the register kernel.
+    // Many rows wider than 512 vectors: the staged ring (KS_LN_RING_BYTES of rows per CTA, 2..8
+    // stages) keeps enough bytes in flight; otherwise the register kernel, which measured faster
+    // for rows of at most 512 vectors (0.74-0.82 of the copy peak against 0.65-0.69 for the ring).
     int stages = 0;
-    if (v == 4 && rows >= 4 * (int64_t)sms) {
+    if (v == 4 && hv > 512 && rows >= 4 * (int64_t)sms) {
         int64_t n_st = (KS_LN_RING_BYTES) / (hv * 16);
         stages = (int)(n_st < 2 ? 2 : (n_st > 8 ? 8 : n_st));
     }

@@ -141,7 +141,7 @@ WIDE_BF16 = [
     (8192, (CTA, 2, False), (CTA, 4, False)),
     (9216, (CTA, 2, False), (CTA, 4, False)),
     (12288, (CTA, 4, False), (CTA, 4, False)),
-    (13312, (BULK, 4, True), (BULK, 4, True)),
+    (13312, (CTA, 4, True), (BULK, 4, True)),
     (14336, (CTA, 4, True), (BULK, 4, True)),
     (16384, (CTA, 4, True), (BULK, 4, True)),
 ]
