@@ -282,18 +282,24 @@ __global__ void __launch_bounds__(1024) softmax_scalar_kernel(void *out, const v
 
 // ---------------------------------------------------------------------------- LayerNorm
 
+// Which of weight and bias a LayerNorm kernel applies, fixed at compile time: a run-time test per
+// element in the output pass measured 7-10 points of the copy peak slower on GB300 (the compiler
+// did not hoist it out of the unrolled loop).
+constexpr int kAffineWeight = 1, kAffineBias = 2;
+
 // One CTA per row, V 16-byte vectors per thread in registers, persistent over rows; the weight
 // and bias slices a thread needs stay in registers for every row it visits, and the next row's
 // vectors are loaded before the current row's two reductions. (Measured on GB300 at [32768,
 // 8192] bf16: 74 % of the copy peak; weight and bias in shared memory, with or without the
 // prefetch, were slower at 58-64 %.)
-template <typename T, int V>
+template <typename T, int V, int kAffine>
 __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const void *x,
                                                              const void *w, const void *b,
                                                              int64_t rows, int64_t hidden,
                                                              int64_t hv, float eps) {
     using E = Elem<T>;
     constexpr int N = E::kPerVec;
+    constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
     __shared__ float red[2][32];
     grid_dependency_wait();
     allow_dependents_launch();
@@ -305,8 +311,8 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
 #pragma unroll
     for (int k = 0; k < V; ++k) {
         const int64_t c = t + (int64_t)k * g;
-        wv[k] = (w && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
-        bv[k] = (b && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
+        wv[k] = (kW && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
+        bv[k] = (kB && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
     }
     int slot = 0;
     int64_t row = blockIdx.x;
@@ -355,13 +361,14 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
             if (c < hv) {
                 float f[N], wf[N], bf[N];
                 E::unpack(xv[k], f);
-                E::unpack(wv[k], wf);
-                E::unpack(bv[k], bf);
+                if (kW) E::unpack(wv[k], wf);
+                if (kB) E::unpack(bv[k], bf);
 #pragma unroll
                 for (int e = 0; e < N; ++e) {
                     float v = __fmaf_rn(f[e], rstd, shift);  // (x - mean) * rstd
-                    if (w) v = b ? __fmaf_rn(v, wf[e], bf[e]) : __fmul_rn(v, wf[e]);
-                    else if (b) v = __fadd_rn(v, bf[e]);
+                    if (kW && kB) v = __fmaf_rn(v, wf[e], bf[e]);
+                    else if (kW) v = __fmul_rn(v, wf[e]);
+                    else if (kB) v = __fadd_rn(v, bf[e]);
                     f[e] = v;
                 }
                 __stcs(og + row * hv + c, E::pack(f));
@@ -380,13 +387,14 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
 // (Reading the stage in all three passes instead freed registers but measured slower.) Waits
 // are bounded (about 2 s); on a time-out the CTA records KS_FAULT_WAIT_TIMEOUT, drains its copies
 // in flight (bounded) and returns.
-template <typename T, int V>
+template <typename T, int V, int kAffine>
 __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const void *x,
                                                               const void *w, const void *b,
                                                               int64_t rows, int64_t hidden,
                                                               int64_t hv, float eps, int stages) {
     using E = Elem<T>;
     constexpr int N = E::kPerVec;
+    constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[2][32];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
@@ -403,8 +411,8 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
 #pragma unroll
     for (int k = 0; k < V; ++k) {
         const int64_t c = t + (int64_t)k * g;
-        wv[k] = (w && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
-        bv[k] = (b && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
+        wv[k] = (kW && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
+        bv[k] = (kB && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
     }
     uint64_t policy = 0;
     if (t == 0) {
@@ -484,13 +492,14 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
             if (c < hv) {
                 float f[N], wf[N], bf[N];
                 E::unpack(xv[k], f);
-                E::unpack(wv[k], wf);
-                E::unpack(bv[k], bf);
+                if (kW) E::unpack(wv[k], wf);
+                if (kB) E::unpack(bv[k], bf);
 #pragma unroll
                 for (int e = 0; e < N; ++e) {
                     float v = __fmaf_rn(f[e], rstd, shift);  // (x - mean) * rstd
-                    if (w) v = b ? __fmaf_rn(v, wf[e], bf[e]) : __fmul_rn(v, wf[e]);
-                    else if (b) v = __fadd_rn(v, bf[e]);
+                    if (kW && kB) v = __fmaf_rn(v, wf[e], bf[e]);
+                    else if (kW) v = __fmul_rn(v, wf[e]);
+                    else if (kB) v = __fadd_rn(v, bf[e]);
                     f[e] = v;
                 }
                 __stcs(og + row * hv + c, E::pack(f));
@@ -515,12 +524,13 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
     }
 }
 
-template <typename T>
+template <typename T, int kAffine>
 __global__ void __launch_bounds__(1024) layer_norm_scalar_kernel(void *out, const void *x,
                                                                  const void *w, const void *b,
                                                                  int64_t rows, int64_t H,
                                                                  float eps) {
     using E = Elem<T>;
+    constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
     __shared__ float red[2][32];
     grid_dependency_wait();
     allow_dependents_launch();
@@ -540,8 +550,8 @@ __global__ void __launch_bounds__(1024) layer_norm_scalar_kernel(void *out, cons
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
         for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
             float v = __fmul_rn(__fsub_rn(E::load1(x, base + j), mean), rstd);
-            if (w) v = __fmul_rn(v, E::load1(w, j));
-            if (b) v = __fadd_rn(v, E::load1(b, j));
+            if (kW) v = __fmul_rn(v, E::load1(w, j));
+            if (kB) v = __fadd_rn(v, E::load1(b, j));
             E::store1(out, base + j, v);
         }
     }
@@ -657,6 +667,17 @@ cudaError_t softmax_dispatch(int v, int block, void *out, const void *x, int64_t
 #define KS_LN_RING_BYTES (64 * 1024)
 #endif
 
+// The instantiation of a LayerNorm kernel for the weight/bias combination of the call.
+template <typename T, typename K>
+const void *layer_norm_pick(int affine, K none, K weight, K bias, K both) {
+    switch (affine) {
+    case kAffineWeight: return (const void *)weight;
+    case kAffineBias: return (const void *)bias;
+    case kAffineWeight | kAffineBias: return (const void *)both;
+    default: return (const void *)none;
+    }
+}
+
 template <typename T>
 cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, const void *w,
                                 const void *b, int64_t rows, int64_t hidden, int64_t hv,
@@ -680,17 +701,23 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
     void *bulk_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
                          const_cast<void **>(&b), &nr, &hd, &hvv, &ep, &stages};
     size_t smem = 0;
+    const int affine = (w ? kAffineWeight : 0) | (b ? kAffineBias : 0);
     switch (stages ? 8 : v) {
-    case 1: f = (const void *)layer_norm_vec_kernel<T, 1>; break;
-    case 2: f = (const void *)layer_norm_vec_kernel<T, 2>; break;
-    case 4: f = (const void *)layer_norm_vec_kernel<T, 4>; break;
+    case 1: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 1, 0>, layer_norm_vec_kernel<T, 1, 1>,
+                                   layer_norm_vec_kernel<T, 1, 2>, layer_norm_vec_kernel<T, 1, 3>); break;
+    case 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0>, layer_norm_vec_kernel<T, 2, 1>,
+                                   layer_norm_vec_kernel<T, 2, 2>, layer_norm_vec_kernel<T, 2, 3>); break;
+    case 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0>, layer_norm_vec_kernel<T, 4, 1>,
+                                   layer_norm_vec_kernel<T, 4, 2>, layer_norm_vec_kernel<T, 4, 3>); break;
     case 8:
-        f = (const void *)layer_norm_bulk_kernel<T, 4>;
+        f = layer_norm_pick<T>(affine, layer_norm_bulk_kernel<T, 4, 0>, layer_norm_bulk_kernel<T, 4, 1>,
+                               layer_norm_bulk_kernel<T, 4, 2>, layer_norm_bulk_kernel<T, 4, 3>);
         args = bulk_args;
         smem = 128 + (size_t)stages * (size_t)hv * 16;
         break;
     default:
-        f = (const void *)layer_norm_scalar_kernel<T>;
+        f = layer_norm_pick<T>(affine, layer_norm_scalar_kernel<T, 0>, layer_norm_scalar_kernel<T, 1>,
+                               layer_norm_scalar_kernel<T, 2>, layer_norm_scalar_kernel<T, 3>);
         args = sc_args;
         block = (int)round_up64(ceil_div64(hidden, 8), 32);
         block = block < 32 ? 32 : (block > 1024 ? 1024 : block);

@@ -120,17 +120,28 @@ def _ln_check(out, ref, dt, h, name):
     assert ok, f"{name}: {worst}"
 
 
+AFFINE = ["both", "none", "weight", "bias"]  # each combination is its own kernel instantiation
+
+
+def _affine(affine, h, dt, seed):
+    w = synth.weight(h, dt) if affine in ("both", "weight") else None
+    b = synth.cast(synth.normal_np((h,), seed, std=0.1), dt) if affine in ("both", "bias") else None
+    return w, b
+
+
+def _dev(t, device):
+    return t.to(device) if t is not None else None
+
+
 @pytest.mark.parametrize("dtype", DT)
 @pytest.mark.parametrize("rows,h", [(128, 1024), (2048, 4096), (512, 4096), (4, 1536), (333, 8192),
                                     (7, 16384), (5, 17), (3, 1000), (2, 20000)])
-@pytest.mark.parametrize("affine", [True, False])
+@pytest.mark.parametrize("affine", AFFINE)
 def test_layer_norm(cuda_device, dtype, rows, h, affine):
     dt = synth.dtype_of(dtype)
     x = synth.cast(synth.normal_np((rows, h), 806) + 0.25, dt)
-    w = synth.weight(h, dt) if affine else None
-    b = synth.cast(synth.normal_np((h,), 807, std=0.1), dt) if affine else None
-    y = ks.layer_norm(x.to(cuda_device), w.to(cuda_device) if affine else None,
-                      b.to(cuda_device) if affine else None, 1e-5).cpu()
+    w, b = _affine(affine, h, dt, 807)
+    y = ks.layer_norm(x.to(cuda_device), _dev(w, cuda_device), _dev(b, cuda_device), 1e-5).cpu()
     ref, _ = oracle.layer_norm(x, w, b, 1e-5)
     _ln_check(y, ref, dt, h, f"layer_norm {dtype} [{rows},{h}] affine={affine}")
 
@@ -178,7 +189,7 @@ def test_softmax_extreme_spread(cuda_device, dtype):
 
 @pytest.mark.parametrize("dtype", DT)
 @pytest.mark.parametrize("h", [1024, 4096, 8192, 16384])
-@pytest.mark.parametrize("affine", [True, False])
+@pytest.mark.parametrize("affine", AFFINE)
 def test_layer_norm_many_rows_staged(cuda_device, dtype, h, affine):
     """Enough rows for the staged ring (>= 4 rows per SM): sampled rows against the oracle, and
     the ring's fault word stays clear."""
@@ -187,10 +198,8 @@ def test_layer_norm_many_rows_staged(cuda_device, dtype, h, affine):
         pytest.skip("fp32 rows wider than 2048 vectors take the scalar kernel")
     rows = 1000
     x = synth.cast(synth.normal_np((rows, h), 811) - 0.5, dt)
-    w = synth.weight(h, dt) if affine else None
-    b = synth.cast(synth.normal_np((h,), 812, std=0.1), dt) if affine else None
-    y = ks.layer_norm(x.to(cuda_device), w.to(cuda_device) if affine else None,
-                      b.to(cuda_device) if affine else None, 1e-5).cpu()
+    w, b = _affine(affine, h, dt, 812)
+    y = ks.layer_norm(x.to(cuda_device), _dev(w, cuda_device), _dev(b, cuda_device), 1e-5).cpu()
     ref, _ = oracle.layer_norm(x, w, b, 1e-5)
     _ln_check(y, ref, dt, h, f"layer_norm staged {dtype} [{rows},{h}] affine={affine}")
     st, flags = _abi.ks_device_faults(clear=False)
