@@ -102,7 +102,10 @@ const char *ks_status_string(ks_status_t status);
 const char *ks_last_error(void);
 
 /*
- * Launch plan, for introspection and tests. A pure host function: no CUDA call.
+ * Launch plan, for introspection and tests. A pure host function: no CUDA call. The plan
+ * depends on the dtype (the heuristic was set per dtype from a sweep of every variant), the row
+ * width in 16-byte vectors and the row count; grid is an upper bound when cluster >= 2 (the
+ * launch caps whole clusters by what the device can hold resident).
  *   op              0 = rms_norm, 1 = fused_add_rms_norm.
  *   aligned16       non-zero when every pointer of the call is 16-byte aligned.
  *   sm_count        multiprocessors of the device (152 on GB300).
@@ -120,7 +123,9 @@ typedef struct ks_plan {
     int32_t stages;         /* staged kernel: rows in each CTA's shared-memory ring (else 0) */
     int32_t smem_bytes;     /* staged kernel: dynamic shared memory per CTA (else 0) */
     int32_t flags;          /* KS_PLAN_* bits below */
-    int32_t cluster;        /* cluster-row kernel: CTAs per cluster (one cluster per row) */
+    int32_t cluster;        /* CTAs per cluster, one cluster per row: the cluster-row kernel
+                               (2..8), or the staged kernel split over a cluster (2..8; 0 or 1:
+                               one CTA per row); 0 for the other kernels */
 } ks_plan_t;
 
 /* Plan flags. KS_PLAN_NO_PREFETCH: the register kernels (warp and CTA rows) load each row when
@@ -137,9 +142,14 @@ enum {
     KS_KERNEL_CTA_ROW = 2,  /* one CTA per row, row in registers, 16-byte vectors */
     KS_KERNEL_SCALAR = 3,   /* one CTA per row, element loads, two passes over the row */
     KS_KERNEL_BULK_ROW = 4, /* one CTA per row, rows streamed through a shared-memory ring by
-                               bulk asynchronous copies, 4 vectors per thread */
-    KS_KERNEL_CLUSTER_ROW = 5 /* one cluster of `cluster` CTAs per row (few wide rows): each CTA
-                                 reduces a slice, partials exchanged in distributed shared memory */
+                               bulk asynchronous copies, 4 vectors per thread; with cluster >= 2
+                               the row is split over a cluster, each CTA streaming its slice of
+                               ceil(hv / cluster) vectors through its own ring, partial sums
+                               exchanged in distributed shared memory (rows too wide for one
+                               CTA's registers) */
+    KS_KERNEL_CLUSTER_ROW = 5 /* one cluster of `cluster` CTAs per row (few wide rows, wide plain
+                                 rows): each CTA holds a slice in registers and reduces it,
+                                 partials exchanged in distributed shared memory */
 };
 
 ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t dtype,
@@ -154,10 +164,11 @@ ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t 
  * bytes, team * vec_per_thread vectors short of the row, a block that is not a multiple of 32 or
  * exceeds the kernel's bound (warp rows 256, CTA rows 1024 at 2 vectors and 512 at 4, staged
  * rows 512, cluster rows 512, scalar 1024), a staged ring (stages 1..16) over 226 KB of shared
- * memory, or a cluster outside 2..8 CTAs whose slices (block * vec_per_thread vectors each) do
- * not cover the row. grid <= 0
- * lets the library size the persistent grid; smem_bytes and rows_per_pass are recomputed. The
- * plan is read, never written.
+ * memory (per CTA: stages * slice * 16 bytes, twice that for the fused op), or a cluster outside
+ * 2..8 CTAs whose slices (ceil(hv / cluster) vectors, at most block * vec_per_thread each) do not
+ * cover the row or leave a CTA without vectors. grid <= 0 lets the library size the persistent
+ * grid; cluster grids are whole clusters, capped by the number the device can hold resident at
+ * once. smem_bytes and rows_per_pass are recomputed. The plan is read, never written.
  */
 ks_status_t ks_rms_norm_planned(void *out, const void *x, const void *weight, int64_t rows,
                                 int64_t hidden, float eps, ks_dtype_t dtype,

@@ -11,11 +11,12 @@
 // so HBM bandwidth bounds it; no tensor cores apply): each row is read once with 16-byte
 // coalesced loads (streaming, evict-first) into registers, written once with 16-byte
 // streaming stores; the weight slice a thread needs is loaded once and kept in registers for
-// every row it touches; the grid is persistent and each team loads its next row before it
-// reduces the current one, so a row's loads are in flight during the previous row's reduction.
-// The staged kernel instead streams whole rows into a ring of shared-memory stages with bulk
-// asynchronous copies (one issuing thread, an mbarrier per stage), so several rows per CTA are in
-// flight without spending registers on them.
+// every row it touches; the grid is persistent. Teams either load their next row before they
+// reduce the current one (prefetch) or load each row in turn with fewer registers and more
+// resident warps; the launch heuristic picks per width. The staged kernel instead streams whole
+// rows (or, split over a cluster, row slices) into a ring of shared-memory stages with bulk
+// asynchronous copies (one issuing thread, an mbarrier per stage), so several rows per CTA are
+// in flight without spending registers on them.
 #pragma once
 
 #include <cooperative_groups.h>

@@ -87,3 +87,14 @@ def test_two_gloo_ranks_take_the_max_and_draw_independent_batches():
 
 def test_single_process_max_is_identity():
     assert bench.max_over_ranks(3.5) == 3.5
+
+
+def test_kernel_hash_ignores_comments_and_layout():
+    """The recorded DRAM traffic stays valid across comment edits, not across code edits."""
+    src = 'int f(int a) { // sum\n  return a + 1; /* one */\n}\nconst char *s = "// kept";\n'
+    same = '/* header */\nint f(int a)   {\n\n  return a + 1;\n}  // trailing\nconst char *s = "// kept";'
+    changed = 'int f(int a) { return a + 2; }\nconst char *s = "// kept";'
+    assert bench.code_only(src) == bench.code_only(same)
+    assert bench.code_only(src) != bench.code_only(changed)
+    assert '"// kept"' in bench.code_only(src)
+
