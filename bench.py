@@ -295,6 +295,7 @@ def run_ks(args) -> int:
         # decode shape (launch-bound): p50 of single cache-cold launches, and graph replay
         if not args.no_decode:
             ops["decode_fused_add_rms_norm_4x1536"] = decode_latency(dev, args)
+            ops["pages_latency_shapes"] = pages_shapes_latency(dev, args)
         if not args.no_next_ops:
             ops["next_ops"] = next_ops(dev, args)
         e2e = run_e2e(dev, args, R, H, eps) if not args.no_e2e else None
@@ -405,6 +406,107 @@ def decode_latency(dev, args) -> dict:
             "us_per_launch_graph_replay": graph_per_launch(False),
             "us_per_launch_graph_replay_pdl": graph_per_launch(True),
             "samples": len(cold)}
+
+
+# The pages' latency table (Triton Kernel Lab, "Measured Result" and "Decode Kernel Results"; RTX
+# 5070 Ti, cache-cold CUDA events, 100 warm-ups, 500 samples, p50), shape for shape: op, dtype,
+# rows, hidden, and the pages' p50 in microseconds (context: another GPU).
+PAGES_LATENCY_SHAPES = [("rms_norm", "fp16", 128, 1024, 5.8), ("rms_norm", "fp16", 512, 4096, 13.5),
+                        ("rms_norm", "fp16", 2048, 4096, 42.7),
+                        ("fused_add_rms_norm", "bf16", 4, 1536, 5.1)]
+
+
+def pages_shapes_latency(dev, args) -> dict:
+    """The pages' latency shapes by their method: 100 warm-up launches, then single launches timed
+    with CUDA events, each after the L2 is flushed (a 512 MiB write outside the timed pair);
+    p50/p95 over --decode-samples samples. Also the per-launch time of 100 back-to-back launches
+    replayed from a CUDA graph (inputs hot in L2). N(0,1) inputs; fused residual N(0, var 4)."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16}
+    out = {}
+    for op, dt, R, H, pages_us in PAGES_LATENCY_SHAPES:
+        code = codes[dt]
+        x = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), dt)
+        r = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev, std=2.0), dt)
+        w = synth.weight(H, dt).to(dev)
+        y = torch.empty_like(x)
+        if op == "rms_norm":
+            launch = lambda st: _abi.ks_rms_norm(y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H,
+                                                 1e-6, code, st)
+        else:
+            launch = lambda st: _abi.ks_fused_add_rms_norm(x.data_ptr(), r.data_ptr(),
+                                                           w.data_ptr(), R, H, 1e-6, code, st)
+        for _ in range(100):
+            launch(stream.cuda_stream)
+        samples = []
+        for _ in range(args.decode_samples):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch(stream.cuda_stream)
+            b.record(stream)
+            b.synchronize()
+            samples.append(a.elapsed_time(b) * 1e3)
+        samples.sort()
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(100):
+                launch(cs.cuda_stream)
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(10):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        q = lambda p: samples[min(len(samples) - 1, int(p * len(samples)))]
+        nb = algorithmic_bytes(op, R, H, 2)
+        out[f"{op} {dt} [{R},{H}]"] = {
+            "bytes_per_launch": nb, "p50_us_cold_event": q(0.5), "p95_us_cold_event": q(0.95),
+            "gbs_at_p50": nb / (q(0.5) * 1e-6) / 1e9,
+            "us_per_launch_graph_replay": a.elapsed_time(b) * 1e3 / 1000,
+            "pages_p50_us_other_gpu": pages_us, "samples": len(samples)}
+        del x, r, w, y
+    # The floor of this method on this GPU: the same protocol around a one-element torch fill
+    one = torch.empty(1, device=dev)
+    for _ in range(100):
+        one.fill_(0)
+    floor = []
+    for _ in range(args.decode_samples):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one.fill_(0)
+        b.record(stream)
+        b.synchronize()
+        floor.append(a.elapsed_time(b) * 1e3)
+    floor.sort()
+    cs = torch.cuda.Stream(dev)
+    cs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        for _ in range(100):
+            one.fill_(0)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(10):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    out["method floor: one-element torch fill, same protocol"] = {
+        "p50_us_cold_event": floor[len(floor) // 2], "samples": len(floor),
+        "us_per_launch_graph_replay": a.elapsed_time(b) * 1e3 / 1000}
+    return out
 
 
 def next_ops(dev, args) -> dict:
