@@ -319,9 +319,9 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 //    to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8
 //    CTAs per row, plain rows of at most 1024 vectors take 2 vectors per thread, and the rest 4;
 //  * rows of 2049..16384 vectors (wider than one CTA's registers): a cluster of 2, 4 or 8 CTAs
-//    per row, each with at most 2048 vectors: the staged ring split over the cluster (fused, and
-//    plain rows of at most 3072 vectors) or the register-resident cluster kernel (wider plain
-//    rows, and at most SMs/8 rows of any kind);
+//    per row, each with at most 2048 vectors: the staged ring split over the cluster (16-bit
+//    fused rows above 2560 vectors, fp32 fused rows above 8192, plain rows of at most 3072) or
+//    the register-resident cluster kernel (the other rows, and at most SMs/8 rows of any kind);
 //  * anything else (H not a multiple of the vector, unaligned pointers, wider rows): the scalar
 //    two-pass kernel.
 // The grid is persistent: at most sm_count * blocks_per_sm CTAs (for cluster plans, whole
@@ -414,14 +414,18 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         }
     } else if (vec_ok && hv <= 16384) {
         // Wider than one CTA's registers: split each row over a cluster of CTAs, each owning at
-        // most 2048 vectors (a probe of the variants at 2560..16384 vectors, many rows):
-        //   fused: the staged ring split over C = 2, 4 or 8 CTAs, 2 stages per CTA (two stages
-        //     beat deeper rings: two CTAs per SM hide more than one CTA's deeper ring);
-        //   plain: the same ring over 2 CTAs up to 3072 vectors, wider rows the register-resident
+        // most 2048 vectors (from the plan sweep at 2560..16384 vectors, many rows):
+        //   fused: fp32 rows of at most 8192 vectors, and 16-bit rows of at most 2560, take the
+        //     register-resident cluster kernel (4 CTAs, 8 beyond 4096 vectors); the rest the
+        //     staged ring split over C = 2, 4 or 8 CTAs, 2 stages per CTA (two stages beat
+        //     deeper rings: two CTAs per SM hide more than one CTA's deeper ring);
+        //   plain: the split ring over 2 CTAs up to 3072 vectors, wider rows the register-resident
         //     cluster kernel at 4 vectors per thread over 4 CTAs (8 beyond 8192 vectors).
         // Few rows (at most SMs/8) take the register-resident cluster kernel with 8 CTAs per row.
         int C = 2;
         while (ceil_div(hv, C) > 2048) C *= 2;
+        const bool f32 = dtype == KS_DTYPE_F32;
+        const bool split = fused ? !(f32 ? hv <= 8192 : hv <= 2560) : hv <= 3072;
         if (rows * 8 <= sm_count) {
             const int64_t slice = ceil_div(hv, 8);
             p->kernel = KS_KERNEL_CLUSTER_ROW;
@@ -429,12 +433,12 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
             p->vec_per_thread = slice <= 512 ? 1 : (slice <= 1024 ? 2 : 4);
             p->block = (int32_t)round_up(ceil_div(slice, p->vec_per_thread), 32);
             p->team = p->block * 8;
-        } else if (fused || hv <= 3072) {
+        } else if (split) {
             bulk_row(p, ceil_div(hv, C), fused, 2);
             p->cluster = C;
             p->team = p->block * C;
         } else {
-            p->cluster = hv <= 8192 ? 4 : 8;
+            p->cluster = (fused ? hv <= 4096 : hv <= 8192) ? 4 : 8;
             p->kernel = KS_KERNEL_CLUSTER_ROW;
             p->vec_per_thread = 4;
             p->block = (int32_t)round_up(ceil_div(ceil_div(hv, p->cluster), 4), 32);

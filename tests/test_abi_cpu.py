@@ -253,7 +253,13 @@ def test_rows_wider_than_registers_split_over_a_cluster(hidden, dtype, cluster):
     assert slice_ <= 2048 and (cluster == 2 or -(-hv // (cluster // 2)) > 2048)
     for op in (0, 1):
         p = plan(op, 65536, hidden, dtype=dtype, bps=1)
-        if op == 1 or hv <= 3072:
+        if op == 1 and hv <= (8192 if dtype == F32 else 2560):
+            # wide fused fp32 rows (and 16-bit rows of at most 2560 vectors): the register-
+            # resident cluster kernel over 4 CTAs (8 beyond 4096 vectors)
+            c = 4 if hv <= 4096 else 8
+            assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == c
+            assert p.vec_per_thread == 4 and p.block * 4 * c >= hv and p.block <= 512
+        elif op == 1 or hv <= 3072:
             # many rows: each CTA streams its slice through its own staged ring (2 stages)
             assert p.kernel == _abi.KS_KERNEL_BULK_ROW and p.cluster == cluster
             assert p.vec_per_thread == 4 and p.block == -(-slice_ // 4 // 32) * 32 <= 512
