@@ -859,8 +859,9 @@ def plan_candidates(op: str, hv: int, elem: int):
     """Every launch plan the heuristic chooses among for a row of hv 16-byte vectors, named as in
     the plan-sweep tables: w4/w4n (warp per row, 4 vectors per lane, with/without prefetch),
     p2/n2/p4/n4 (CTA per row, 2 or 4 vectors per thread, with/without prefetch), b2 (staged ring,
-    2 stages), and for rows wider than 2048 vectors cC (register-resident cluster of C CTAs, 4
-    vectors per thread) and bCsS (staged ring split over C CTAs, S stages)."""
+    2 stages), tBuU (the two-pass kernel, B threads, U vectors per thread per step; rows of at
+    least 512 vectors), and for rows wider than 2048 vectors cC (register-resident cluster of C
+    CTAs, 4 vectors per thread) and bCsS (staged ring split over C CTAs, S stages)."""
     from row_wise_rmsnorm_ks_gb300 import _abi
 
     up32 = lambda n: -(-n // 32) * 32
@@ -879,6 +880,9 @@ def plan_candidates(op: str, hv: int, elem: int):
     b = up32(-(-hv // 4))
     if b <= 512 and 128 + 2 * hv * 16 * (2 if fused else 1) <= 226 * 1024:
         out.append(("b2", _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, b, 2)))
+    if hv >= 512:
+        for blk, u in ((256, 4), (512, 2), (512, 4), (1024, 2), (1024, 4)):
+            out.append((f"t{blk}u{u}", _abi.make_plan(_abi.KS_KERNEL_TWOPASS_ROW, u, blk)))
     if hv > 2048:
         for c in (2, 4, 8):
             sl = -(-hv // c)
@@ -920,7 +924,7 @@ def run_plan_sweep(args) -> int:
         torch.cuda.synchronize()
         return a.elapsed_time(b) / n * 1e-3
 
-    widths = list(range(128, 2049, 64)) + [2560, 3072, 4096, 8192, 16384]
+    widths = list(range(128, 2049, 64)) + [2560, 3072, 4096, 8192, 16384, 32768]
     for dt in args.plan_sweep_dtypes.split(","):
         elem = 4 if dt == "fp32" else 2
         code = codes[dt]
@@ -956,7 +960,8 @@ def run_plan_sweep(args) -> int:
                                          0)[1].as_dict()
                 line = {"plan_sweep": dt, "op": op, "hv": hv, "hidden": H, "rows": R,
                         "default_plan": {k: dp[k] for k in ("kernel_name", "vec_per_thread",
-                                                            "flags", "stages", "cluster")}}
+                                                            "block", "flags", "stages",
+                                                            "cluster")}}
                 line.update({k: round(statistics.median(v), 4) for k, v in res.items()})
                 print(json.dumps(line), flush=True)
             del x, r, y

@@ -147,9 +147,13 @@ enum {
                                ceil(hv / cluster) vectors through its own ring, partial sums
                                exchanged in distributed shared memory (rows too wide for one
                                CTA's registers) */
-    KS_KERNEL_CLUSTER_ROW = 5 /* one cluster of `cluster` CTAs per row (few wide rows, wide plain
-                                 rows): each CTA holds a slice in registers and reduces it,
-                                 partials exchanged in distributed shared memory */
+    KS_KERNEL_CLUSTER_ROW = 5, /* one cluster of `cluster` CTAs per row (few wide rows): each CTA
+                                  holds a slice in registers and reduces it, partials exchanged
+                                  in distributed shared memory */
+    KS_KERNEL_TWOPASS_ROW = 6  /* one CTA per row, any width: the row read twice with 16-byte
+                                  vectors (sum of squares, then outputs; the second pass from
+                                  L2), vec_per_thread (2 or 4) vectors per thread in flight per
+                                  step; the grid is capped so the rows in flight fit in L2 */
 };
 
 ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t dtype,

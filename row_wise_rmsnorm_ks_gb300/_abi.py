@@ -16,9 +16,9 @@ LIB_PATH = os.path.join(_HERE, "_build", "libks.so")
 KS_DTYPE_F32, KS_DTYPE_F16, KS_DTYPE_BF16 = 0, 1, 2
 KS_SUCCESS, KS_ERR_INVALID_ARGUMENT, KS_ERR_UNSUPPORTED_DTYPE, KS_ERR_OVERLAP, KS_ERR_CUDA = range(5)
 (KS_KERNEL_NONE, KS_KERNEL_WARP_ROW, KS_KERNEL_CTA_ROW, KS_KERNEL_SCALAR, KS_KERNEL_BULK_ROW,
- KS_KERNEL_CLUSTER_ROW) = range(6)
+ KS_KERNEL_CLUSTER_ROW, KS_KERNEL_TWOPASS_ROW) = range(7)
 KERNEL_NAMES = {0: "none", 1: "warp_row", 2: "cta_row", 3: "scalar", 4: "bulk_row",
-                5: "cluster_row"}
+                5: "cluster_row", 6: "twopass_row"}
 KS_FAULT_WAIT_TIMEOUT = 1
 KS_PLAN_NO_PREFETCH = 1
 KS_PLAN_PDL = 2

@@ -79,6 +79,15 @@ uint64_t occ_key(int dev, ks_dtype_t d, bool fused, const ks_plan_t &p, bool clu
 }
 
 constexpr int kSmemLimit = 226 * 1024;  // dynamic ring; static smem and reserve fit in 227 KB
+// Bytes of rows the two-pass kernel's CTAs may have in flight together: the second pass re-reads
+// each row from L2 (129 MB), so the grid keeps the first pass's rows well inside it.
+constexpr int64_t kTwoPassL2Budget = 48ll << 20;
+
+int64_t twopass_grid_cap(int64_t hv, bool fused) {
+    const int64_t per_cta = hv * 16 * (fused ? 2 : 1);
+    const int64_t cap = kTwoPassL2Budget / (per_cta > 0 ? per_cta : 1);
+    return cap < 1 ? 1 : cap;
+}
 constexpr int kRingHeader = 128;  // the staged kernel's mbarriers, ahead of its ring
 
 // Checks that a plan fits the call (see ks_rms_norm_planned) and fills the derived fields.
@@ -142,6 +151,13 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
         p.team = p.block * p.cluster;
         break;
     }
+    case KS_KERNEL_TWOPASS_ROW:
+        if (!vec_ok) return fail(KS_ERR_INVALID_ARGUMENT, "vector kernel needs 16-byte rows and pointers");
+        if (p.vec_per_thread != 2 && p.vec_per_thread != 4)
+            return fail(KS_ERR_INVALID_ARGUMENT, "two-pass kernel takes 2 or 4 vectors per step");
+        if (p.block > 1024) return fail(KS_ERR_INVALID_ARGUMENT, "two-pass block > 1024");
+        p.team = p.block;
+        break;
     case KS_KERNEL_SCALAR:
         if (p.block > 1024) return fail(KS_ERR_INVALID_ARGUMENT, "scalar block > 1024");
         p.vec_per_thread = 0;
@@ -256,6 +272,10 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         const int64_t ctas = ceil_div(rows, per_cta);
         const int64_t cap = (int64_t)slot.sm_count * bps;
         p.grid = forced->grid > 0 ? (forced->grid < ctas ? forced->grid : ctas) : (ctas < cap ? ctas : cap);
+        if (forced->grid <= 0 && p.kernel == KS_KERNEL_TWOPASS_ROW) {
+            const int64_t l2cap = twopass_grid_cap(hidden / (16 / e), fused);
+            if (p.grid > l2cap) p.grid = l2cap;
+        }
         p.rows_per_pass = p.grid * per_cta;
     } else {
         st = plan(fused ? 1 : 0, rows, hidden, dtype, aligned16, slot.sm_count, bps, &p);
@@ -308,24 +328,23 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 //    as the row needs (a multiple of 32 threads). Which variant sustains the most bandwidth
 //    depends on the width, and the sweep picks:
 //      plain: 4 vectors per thread, no prefetch (fp32 rows of at most 384 vectors: 2 vectors,
-//        next row prefetched); rows wider than 1536 vectors stream through the staged
-//        shared-memory ring when there are enough rows to fill it;
+//        next row prefetched); 16-bit rows wider than 1536 vectors take the two-pass kernel;
 //      fused: no prefetch, 2 vectors per thread for rows of at most 768 vectors and for 961..1152
 //        vectors, 4 vectors per thread for 769..960 and 1153..1536 (fp32 rows of at most 384
 //        vectors: 2 vectors, next row prefetched). Wider rows: bf16 prefetches at 4 vectors per
-//        thread; fp16 takes the staged ring (2 stages) when there are enough rows; fp32 keeps 4
-//        vectors without prefetch up to 1792 vectors and takes the ring beyond.
+//        thread; fp16 takes the staged ring (2 stages) up to 1728 vectors when there are enough
+//        rows, the two-pass kernel beyond; fp32 takes the two-pass kernel.
 //    In the latency regime (rows <= SMs, so each CTA gets at most one row) prefetch has nothing
 //    to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8
 //    CTAs per row, plain rows of at most 1024 vectors take 2 vectors per thread, and the rest 4;
-//  * rows of 2049..16384 vectors (wider than one CTA's registers): a cluster of 2, 4 or 8 CTAs
-//    per row, each with at most 2048 vectors: the staged ring split over the cluster (16-bit
-//    fused rows above 2560 vectors, fp32 fused rows above 8192, plain rows of at most 3072) or
-//    the register-resident cluster kernel (the other rows, and at most SMs/8 rows of any kind);
-//  * anything else (H not a multiple of the vector, unaligned pointers, wider rows): the scalar
-//    two-pass kernel.
+//  * rows wider than 2048 vectors (bf16/fp16 H > 16384, fp32 H > 8192): the two-pass kernel,
+//    one CTA per row reading it twice (the second time from L2), any width; few rows (at most
+//    SMs/8) of up to 16384 vectors split over a cluster of 8 CTAs instead;
+//  * anything else (H not a multiple of the vector, unaligned pointers): the scalar two-pass
+//    kernel.
 // The grid is persistent: at most sm_count * blocks_per_sm CTAs (for cluster plans, whole
-// clusters, which the launch caps again by the device's count of resident clusters).
+// clusters, which the launch caps again by the device's count of resident clusters; for the
+// two-pass kernel, no more CTAs than keep their rows in flight within 48 MiB of L2).
 namespace {
 
 void cta_row(ks_plan_t *p, int64_t hv, int v, bool prefetch) {
@@ -345,6 +364,25 @@ void bulk_row(ks_plan_t *p, int64_t hv, bool fused, int64_t stages) {
     p->flags = 0;
     p->stages = (int32_t)stages;
     p->smem_bytes = (int32_t)(kRingHeader + stages * stage);
+}
+
+// The two-pass kernel's launch shape, from the plan sweep: plain rows 4 vectors per thread per
+// step on 256 threads up to 4096 vectors, 512 up to 8192, 1024 beyond; fused rows 2 vectors on
+// 512 threads up to 4096 vectors and 1024 beyond (fp32 rows of at most 2048 vectors: 4 on 256).
+void twopass_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
+    p->kernel = KS_KERNEL_TWOPASS_ROW;
+    if (!fused) {
+        p->vec_per_thread = 4;
+        p->block = hv <= 4096 ? 256 : (hv <= 8192 ? 512 : 1024);
+    } else if (dtype == KS_DTYPE_F32 && hv <= 2048) {
+        p->vec_per_thread = 4;
+        p->block = 256;
+    } else {
+        p->vec_per_thread = 2;
+        p->block = hv <= 4096 ? 512 : 1024;
+    }
+    p->team = p->block;
+    p->flags = 0;
 }
 
 }  // namespace
@@ -394,56 +432,32 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         if (f32 && hv <= 384) {
             cta_row(p, hv, 2, true);
         } else if (!fused) {
-            if (hv > 1536 && ring_rows) {
-                int64_t st = (96 * 1024) / (hv * 16);
-                bulk_row(p, hv, false, st < 2 ? 2 : (st > 8 ? 8 : st));
-            } else {
+            if (hv > 1536 && !f32)
+                twopass_row(p, hv, false, dtype);
+            else
                 cta_row(p, hv, 4, false);
-            }
         } else if (hv <= 1536) {
             const bool two = hv <= 768 || (hv > 960 && hv <= 1152);
             cta_row(p, hv, two ? 2 : 4, false);
         } else if (dtype == KS_DTYPE_BF16) {
             cta_row(p, hv, 4, true);
-        } else if (f32 && hv <= 1792) {
-            cta_row(p, hv, 4, false);
-        } else if (ring_rows) {
+        } else if (!f32 && hv <= 1728 && ring_rows) {
             bulk_row(p, hv, true, 2);
         } else {
-            cta_row(p, hv, 4, true);
+            twopass_row(p, hv, true, dtype);
         }
-    } else if (vec_ok && hv <= 16384) {
-        // Wider than one CTA's registers: split each row over a cluster of CTAs, each owning at
-        // most 2048 vectors (from the plan sweep at 2560..16384 vectors, many rows):
-        //   fused: fp32 rows of at most 8192 vectors, and 16-bit rows of at most 2560, take the
-        //     register-resident cluster kernel (4 CTAs, 8 beyond 4096 vectors); the rest the
-        //     staged ring split over C = 2, 4 or 8 CTAs, 2 stages per CTA (two stages beat
-        //     deeper rings: two CTAs per SM hide more than one CTA's deeper ring);
-        //   plain: the split ring over 2 CTAs up to 3072 vectors, wider rows the register-resident
-        //     cluster kernel at 4 vectors per thread over 4 CTAs (8 beyond 8192 vectors).
-        // Few rows (at most SMs/8) take the register-resident cluster kernel with 8 CTAs per row.
-        int C = 2;
-        while (ceil_div(hv, C) > 2048) C *= 2;
-        const bool f32 = dtype == KS_DTYPE_F32;
-        const bool split = fused ? !(f32 ? hv <= 8192 : hv <= 2560) : hv <= 3072;
-        if (rows * 8 <= sm_count) {
-            const int64_t slice = ceil_div(hv, 8);
-            p->kernel = KS_KERNEL_CLUSTER_ROW;
-            p->cluster = 8;
-            p->vec_per_thread = slice <= 512 ? 1 : (slice <= 1024 ? 2 : 4);
-            p->block = (int32_t)round_up(ceil_div(slice, p->vec_per_thread), 32);
-            p->team = p->block * 8;
-        } else if (split) {
-            bulk_row(p, ceil_div(hv, C), fused, 2);
-            p->cluster = C;
-            p->team = p->block * C;
-        } else {
-            p->cluster = (fused ? hv <= 4096 : hv <= 8192) ? 4 : 8;
-            p->kernel = KS_KERNEL_CLUSTER_ROW;
-            p->vec_per_thread = 4;
-            p->block = (int32_t)round_up(ceil_div(ceil_div(hv, p->cluster), 4), 32);
-            p->team = p->block * p->cluster;
-        }
+    } else if (vec_ok && hv > 2048 && rows * 8 <= sm_count && hv <= 16384) {
+        // Few rows wider than one CTA's registers: each row split over a cluster of 8 CTAs (the
+        // register-resident cluster kernel), so the row's bytes come in over 8 SMs.
+        const int64_t slice = ceil_div(hv, 8);
+        p->kernel = KS_KERNEL_CLUSTER_ROW;
+        p->cluster = 8;
+        p->vec_per_thread = slice <= 512 ? 1 : (slice <= 1024 ? 2 : 4);
+        p->block = (int32_t)round_up(ceil_div(slice, p->vec_per_thread), 32);
+        p->team = p->block * 8;
+    } else if (vec_ok && hv > 2048) {
+        // Wider rows, more of them: the two-pass kernel (no width limit; the second pass from L2).
+        twopass_row(p, hv, fused, dtype);
     } else {
         p->kernel = KS_KERNEL_SCALAR;
         int64_t b = round_up(ceil_div(hidden, 8), 32);
@@ -461,6 +475,8 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
     const int64_t ctas = ceil_div(rows, rows_per_cta);
     const int64_t cap = (int64_t)sm_count * blocks_per_sm;
     p->grid = (blocks_per_sm > 0 && ctas > cap) ? cap : ctas;
+    if (p->kernel == KS_KERNEL_TWOPASS_ROW && p->grid > twopass_grid_cap(hv, fused))
+        p->grid = twopass_grid_cap(hv, fused);
     p->rows_per_pass = p->grid * rows_per_cta;
     return KS_SUCCESS;
 }

@@ -321,6 +321,100 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
     }
 }
 
+// ------------------------------------------------------------------ two-pass row kernel
+
+// One CTA per row, the row read twice from global memory with 16-byte vectors, U vectors per
+// thread in flight in each loop step. The first pass forms the sum of squares (the fused op from
+// s = x + r, writing nothing); the second re-reads the row and writes the outputs (the fused op
+// recomputes s from the untouched inputs and writes both tensors). The second pass reads from
+// L2: the launch sizes the grid so that the rows all CTAs have in flight fit in a share of it,
+// so DRAM still sees each element read once and written once. Nothing but the loop bounds the
+// row width: no row is held in registers, shared memory or a cluster. The first pass loads
+// with the default L2 policy (the row is read again), the second with evict-first (last use).
+template <typename T, bool kFused, int U, int kMaxBlock>
+__global__ void __launch_bounds__(kMaxBlock) rows_twopass_kernel(const RowArgs a) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    __shared__ float red[2][32];
+    const int g = blockDim.x, t = threadIdx.x;
+    const int64_t hv = a.hv;
+    const int64_t chunk = (int64_t)g * U;
+    const uint4 *xg = static_cast<const uint4 *>(a.x);
+    uint4 *og = static_cast<uint4 *>(a.out);
+    uint4 *rg = static_cast<uint4 *>(a.res);
+    const uint4 *wg = static_cast<const uint4 *>(a.w);
+    grid_dependency_wait();
+    allow_dependents_launch();
+    int parity = 0;
+    for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
+        const uint4 *xr = xg + row * hv;
+        uint4 *rr = kFused ? rg + row * hv : nullptr;
+        SumSq acc;
+        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+            uint4 xv[U], rv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                xv[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+                if (kFused) rv[u] = c < hv ? rr[c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float f[N];
+                E::unpack(xv[u], f);
+                if (kFused) {
+                    float q[N];
+                    E::unpack(rv[u], q);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
+                }
+                acc.add(f);
+            }
+        }
+        const float ss = team_sum<false>(acc.total(), red[parity]);
+        parity ^= 1;
+        const float scale = row_scale(ss, (float)a.hidden, a.eps);
+        uint4 *orow = og + row * hv;
+        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+            uint4 xv[U], rv[U], wv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                const bool in = c < hv;
+                xv[u] = in ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+                if (kFused) rv[u] = in ? __ldcs(rr + c) : make_uint4(0u, 0u, 0u, 0u);
+                wv[u] = in ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                if (c < hv) {
+                    float f[N], wf[N];
+                    E::unpack(xv[u], f);
+                    if (kFused) {
+                        float q[N];
+                        E::unpack(rv[u], q);
+#pragma unroll
+                        for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
+                        __stcs(rr + c, E::pack(f));
+                    }
+                    E::unpack(wv[u], wf);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
+                    __stcs(orow + c, E::pack(f));
+                }
+            }
+        }
+    }
+}
+
+template <typename T, bool kFused, int U>
+const void *pick_twopass(int block) {
+    if (block <= 256) return (const void *)rows_twopass_kernel<T, kFused, U, 256>;
+    if (block <= 512) return (const void *)rows_twopass_kernel<T, kFused, U, 512>;
+    return (const void *)rows_twopass_kernel<T, kFused, U, 1024>;
+}
+
 // ------------------------------------------------------------------- scalar row kernel
 
 // Any width and any alignment: one CTA per row, element loads, two passes over the row (the
@@ -720,6 +814,12 @@ const void *pick_kernel(const ks_plan_t &p) {
         }
     }
     case KS_KERNEL_SCALAR: return (const void *)rows_scalar_kernel<T, kFused>;
+    case KS_KERNEL_TWOPASS_ROW:
+        switch (p.vec_per_thread) {
+        case 2: return pick_twopass<T, kFused, 2>(p.block);
+        case 4: return pick_twopass<T, kFused, 4>(p.block);
+        default: return nullptr;
+        }
     case KS_KERNEL_BULK_ROW:
         if (p.vec_per_thread != 4) return nullptr;
         return p.cluster >= 2 ? (const void *)rows_bulk_kernel<T, 4, kFused, true>

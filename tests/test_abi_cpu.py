@@ -132,7 +132,7 @@ def test_warp_per_row_spreads_few_rows_over_sms():
 
 # bf16 widths and the plan the sweep picks at HBM-bound row counts: (kernel, vectors/thread,
 # prefetch) for the fused op, then for the plain op.
-CTA, BULK = _abi.KS_KERNEL_CTA_ROW, _abi.KS_KERNEL_BULK_ROW
+CTA, BULK, TWO = _abi.KS_KERNEL_CTA_ROW, _abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_TWOPASS_ROW
 WIDE_BF16 = [
     (1536, (CTA, 2, False), (CTA, 4, False)),
     (4096, (CTA, 2, False), (CTA, 4, False)),
@@ -141,9 +141,9 @@ WIDE_BF16 = [
     (8192, (CTA, 2, False), (CTA, 4, False)),
     (9216, (CTA, 2, False), (CTA, 4, False)),
     (12288, (CTA, 4, False), (CTA, 4, False)),
-    (13312, (CTA, 4, True), (BULK, 4, True)),
-    (14336, (CTA, 4, True), (BULK, 4, True)),
-    (16384, (CTA, 4, True), (BULK, 4, True)),
+    (13312, (CTA, 4, True), (TWO, 4, 256)),
+    (14336, (CTA, 4, True), (TWO, 4, 256)),
+    (16384, (CTA, 4, True), (TWO, 4, 256)),
 ]
 
 
@@ -151,27 +151,31 @@ WIDE_BF16 = [
 def test_wide_rows_take_cta_per_row(hidden, fused_plan, plain_plan):
     for op, want in ((1, fused_plan), (0, plain_plan)):
         p = plan(op, 32768, hidden)
-        kernel, v, prefetch = want
+        kernel, v, third = want
         assert (p.kernel, p.vec_per_thread) == (kernel, v), (op, hidden)
-        assert p.block == -(-hidden // (8 * v) // 32) * 32 and p.team == p.block
-        assert p.vec_per_thread * 8 * p.block >= hidden
-        if kernel == BULK:
-            stage = hidden * 2 * (2 if op == 1 else 1)
-            assert p.flags == 0 and 2 <= p.stages <= 8
-            assert p.smem_bytes == 128 + p.stages * stage <= 226 * 1024
-        else:
-            assert p.stages == 0
-            assert p.flags == (0 if prefetch else _abi.KS_PLAN_NO_PREFETCH)
-    # few rows: never the staged ring
-    assert plan(0, 100, hidden).kernel == CTA
+        assert p.team == p.block and p.stages == 0
+        if kernel == TWO:  # (TWO, vectors per step, block)
+            assert p.block == third and p.flags == 0
+        else:  # (CTA, vectors per thread, prefetch)
+            assert p.block == -(-hidden // (8 * v) // 32) * 32
+            assert p.vec_per_thread * 8 * p.block >= hidden
+            assert p.flags == (0 if third else _abi.KS_PLAN_NO_PREFETCH)
+    # few rows: never a staged ring
+    assert plan(0, 100, hidden).kernel in (CTA, TWO)
     assert plan(1, 300, hidden).kernel == CTA
 
 
-def test_fp16_wide_fused_rows_take_the_ring():
-    p = plan(1, 32768, 14336, dtype=F16)
-    assert p.kernel == BULK and p.stages == 2 and p.block == 448
+def test_fp16_and_fp32_wide_rows():
+    p = plan(1, 32768, 13312, dtype=F16)  # 1664 vectors: the staged ring
+    assert p.kernel == BULK and p.stages == 2 and p.block == 416
+    p = plan(1, 32768, 14336, dtype=F16)  # 1792 vectors: two-pass, 2 vectors on 512 threads
+    assert (p.kernel, p.vec_per_thread, p.block) == (TWO, 2, 512)
     p = plan(1, 32768, 7168, dtype=F16)
     assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags == _abi.KS_PLAN_NO_PREFETCH
+    p = plan(0, 32768, 7168, dtype=F32)  # 1792 vectors of fp32, plain: registers
+    assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags == _abi.KS_PLAN_NO_PREFETCH
+    p = plan(1, 32768, 7168, dtype=F32)  # fused: two-pass, 4 vectors on 256 threads
+    assert (p.kernel, p.vec_per_thread, p.block) == (TWO, 4, 256)
 
 
 def test_latency_regime_keeps_one_row_per_cta_plans():
@@ -194,7 +198,7 @@ def test_fp32_counts_four_elements_per_vector():
 
 
 @pytest.mark.parametrize("hidden,aligned", [(17, True), (1001, True), (4096, False),
-                                            (20004, True), (140000, True)])
+                                            (20004, True), (140001, True)])
 def test_scalar_fallback(hidden, aligned):
     p = plan(1, 7, hidden, aligned=aligned)
     assert p.kernel == _abi.KS_KERNEL_SCALAR
@@ -229,8 +233,10 @@ def test_plan_invariants_over_a_sweep(dtype):
             p = plan(1, rows, hidden, dtype=dtype, bps=2)
             assert p.block % 32 == 0 and 32 <= p.block <= 1024
             assert 1 <= p.grid <= max(rows, 1) * max(p.cluster, 1)
-            if p.kernel in (_abi.KS_KERNEL_WARP_ROW, _abi.KS_KERNEL_CTA_ROW,
-                            _abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_CLUSTER_ROW):
+            if p.kernel == _abi.KS_KERNEL_TWOPASS_ROW:
+                assert hidden * e % 16 == 0 and p.vec_per_thread in (2, 4)
+            elif p.kernel in (_abi.KS_KERNEL_WARP_ROW, _abi.KS_KERNEL_CTA_ROW,
+                              _abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_CLUSTER_ROW):
                 assert hidden * e % 16 == 0
                 assert p.team * p.vec_per_thread * (16 // e) >= hidden
                 if p.kernel != _abi.KS_KERNEL_WARP_ROW:
@@ -242,40 +248,41 @@ def test_plan_invariants_over_a_sweep(dtype):
                     assert p.cluster == 0 or (p.grid % p.cluster == 0 and 2 <= p.cluster <= 8)
 
 
-@pytest.mark.parametrize("hidden,dtype,cluster", [(20000, BF16, 2), (32768, BF16, 2),
-                                                  (65536, BF16, 4), (131072, BF16, 8),
-                                                  (12288, F32, 2), (16384, F32, 2),
-                                                  (32768, F32, 4)])
-def test_rows_wider_than_registers_split_over_a_cluster(hidden, dtype, cluster):
+@pytest.mark.parametrize("hidden,dtype", [(20000, BF16), (32768, BF16), (65536, BF16),
+                                          (131072, BF16), (140000, BF16), (12288, F32),
+                                          (16384, F32), (32768, F32)])
+def test_rows_wider_than_registers_take_the_two_pass_kernel(hidden, dtype):
     e = 4 if dtype == F32 else 2
     hv = hidden * e // 16
-    slice_ = -(-hv // cluster)
-    assert slice_ <= 2048 and (cluster == 2 or -(-hv // (cluster // 2)) > 2048)
     for op in (0, 1):
+        # many rows: one CTA per row, two passes over the row (the second from L2)
         p = plan(op, 65536, hidden, dtype=dtype, bps=1)
-        if op == 1 and hv <= (8192 if dtype == F32 else 2560):
-            # wide fused fp32 rows (and 16-bit rows of at most 2560 vectors): the register-
-            # resident cluster kernel over 4 CTAs (8 beyond 4096 vectors)
-            c = 4 if hv <= 4096 else 8
-            assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == c
-            assert p.vec_per_thread == 4 and p.block * 4 * c >= hv and p.block <= 512
-        elif op == 1 or hv <= 3072:
-            # many rows: each CTA streams its slice through its own staged ring (2 stages)
-            assert p.kernel == _abi.KS_KERNEL_BULK_ROW and p.cluster == cluster
-            assert p.vec_per_thread == 4 and p.block == -(-slice_ // 4 // 32) * 32 <= 512
-            stage = slice_ * 16 * (2 if op else 1)
-            assert p.stages == 2 and p.smem_bytes == 128 + 2 * stage <= 226 * 1024
+        assert p.kernel == _abi.KS_KERNEL_TWOPASS_ROW and p.cluster == 0 and p.team == p.block
+        assert p.vec_per_thread == (2 if op else 4)
+        if op:
+            assert p.block == (512 if hv <= 4096 else 1024)
         else:
-            # wide plain rows: the register-resident cluster kernel, 4 or 8 CTAs
-            c = 4 if hv <= 8192 else 8
-            assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == c
-            assert p.vec_per_thread == 4 and p.block * 4 * c >= hv and p.block <= 512
-        assert p.team == p.block * p.cluster and p.grid % p.cluster == 0
-        assert p.grid == 152 // p.cluster * p.cluster and p.rows_per_pass == 152 // p.cluster
-        # few rows: the register-resident cluster kernel, 8 CTAs per row
+            assert p.block == (256 if hv <= 4096 else 512 if hv <= 8192 else 1024)
+        # the grid keeps the rows in flight within 48 MiB of L2
+        assert p.grid <= max(1, (48 << 20) // (hv * 16 * (2 if op else 1))) and p.grid <= 152
+        # few rows: the register-resident cluster kernel, 8 CTAs per row (up to 16384 vectors)
         p = plan(op, 3, hidden, dtype=dtype, bps=1)
-        assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == 8
-        assert p.block * p.vec_per_thread * 8 >= hv and p.grid == 24
+        if hv <= 16384:
+            assert p.kernel == _abi.KS_KERNEL_CLUSTER_ROW and p.cluster == 8
+            assert p.block * p.vec_per_thread * 8 >= hv and p.grid == 24
+        else:
+            assert p.kernel == _abi.KS_KERNEL_TWOPASS_ROW and p.grid == 3
+
+
+def test_two_pass_plans_are_checked():
+    a, b, w = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    mk = _abi.make_plan
+    for p in (mk(_abi.KS_KERNEL_TWOPASS_ROW, 3, 256), mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, 2048),
+              mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, 100)):
+        assert _abi.ks_rms_norm_planned(a, b, w, 64, 32768, 1e-6, BF16, p, None) == E
+    p = mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, 256)
+    assert _abi.ks_rms_norm_planned(a, b + 2, w, 64, 32768, 1e-6, BF16, p, None) == E  # unaligned
 
 
 def test_split_staged_plans_are_checked():

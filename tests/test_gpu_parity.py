@@ -251,6 +251,9 @@ def _variant_plan(name, hidden, elem):
         return A.make_plan(A.KS_KERNEL_SCALAR, 0, 256)
     if hidden * elem % 16:
         return None
+    if name.startswith("twopass"):  # twopass_b<block>_u<vectors per step>
+        block, u = name.split("_b")[1].split("_u")
+        return A.make_plan(A.KS_KERNEL_TWOPASS_ROW, int(u), int(block))
     flags = A.KS_PLAN_NO_PREFETCH if name.endswith("_np") else 0
     if name.startswith("warp_row"):
         v = next((v for v in (1, 2, 4) if 32 * v >= hv), None)
@@ -276,7 +279,8 @@ def _variant_plan(name, hidden, elem):
 VARIANTS = ["warp_row", "warp_row_np", "cta_row_v2", "cta_row_v2_np", "cta_row_v4",
             "cta_row_v4_np", "bulk_row_s1", "bulk_row_s2", "bulk_row_s5", "bulk_row_c2_s2",
             "bulk_row_c3_s1", "bulk_row_c8_s3", "cluster_row_c2", "cluster_row_c3",
-            "cluster_row_c8", "scalar"]
+            "cluster_row_c8", "twopass_b256_u4", "twopass_b512_u2", "twopass_b1024_u4",
+            "twopass_b96_u2", "scalar"]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -335,7 +339,8 @@ def test_rows_wider_than_registers_match_oracle(cuda_device, op, dtype, hidden, 
     code = {torch.bfloat16: A.KS_DTYPE_BF16, torch.float16: A.KS_DTYPE_F16,
             torch.float32: A.KS_DTYPE_F32}[dt]
     p = A.ks_plan_launch(0 if op == "rms_norm" else 1, rows, hidden, code, True, 152, 1)[1]
-    assert p.kernel in (A.KS_KERNEL_BULK_ROW, A.KS_KERNEL_CLUSTER_ROW) and p.cluster >= 2
+    assert p.kernel == A.KS_KERNEL_TWOPASS_ROW or (p.kernel == A.KS_KERNEL_CLUSTER_ROW
+                                                    and p.cluster == 8)
     x = synth.cast(synth.student_t3_np((rows, hidden), 95), dt)
     wt = synth.weight(hidden, dt)
     xd, wd = x.to(cuda_device), wt.to(cuda_device)
