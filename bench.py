@@ -925,6 +925,8 @@ def run_plan_sweep(args) -> int:
         return a.elapsed_time(b) / n * 1e-3
 
     widths = list(range(128, 2049, 64)) + [2560, 3072, 4096, 8192, 16384, 32768]
+    if args.plan_sweep_widths:
+        widths = [int(v) for v in args.plan_sweep_widths.split(",")]
     for dt in args.plan_sweep_dtypes.split(","):
         elem = 4 if dt == "fp32" else 2
         code = codes[dt]
@@ -994,6 +996,8 @@ def main() -> int:
                     help="time every candidate launch plan per dtype, op and width, and exit")
     ap.add_argument("--plan-sweep-rounds", type=int, default=3)
     ap.add_argument("--plan-sweep-dtypes", default="bf16,fp16,fp32")
+    ap.add_argument("--plan-sweep-widths", default="",
+                    help="comma-separated row widths in 16-byte vectors (default: the full grid)")
     ap.add_argument("--next-rows", type=int, default=32768,
                     help="rows of the next operators' large shapes (width 8192)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -153,7 +153,8 @@ enum {
     KS_KERNEL_TWOPASS_ROW = 6  /* one CTA per row, any width: the row read twice with 16-byte
                                   vectors (sum of squares, then outputs; the second pass from
                                   L2), vec_per_thread (2 or 4) vectors per thread in flight per
-                                  step; the grid is capped so the rows in flight fit in L2 */
+                                  step; the grid is capped so the rows in flight fit in L2,
+                                  down to one CTA per SM */
 };
 
 ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t dtype,

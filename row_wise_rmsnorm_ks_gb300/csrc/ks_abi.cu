@@ -80,13 +80,15 @@ uint64_t occ_key(int dev, ks_dtype_t d, bool fused, const ks_plan_t &p, bool clu
 
 constexpr int kSmemLimit = 226 * 1024;  // dynamic ring; static smem and reserve fit in 227 KB
 // Bytes of rows the two-pass kernel's CTAs may have in flight together: the second pass re-reads
-// each row from L2 (129 MB), so the grid keeps the first pass's rows well inside it.
-constexpr int64_t kTwoPassL2Budget = 48ll << 20;
+// each row from L2 (129 MB), so the grid keeps the first pass's rows inside it, but never drops
+// below one CTA per SM (for rows of 16384 vectors and more, measured: a full grid with some L2
+// misses beats fewer CTAs, 0.66-0.81 of the copy peak against 0.39-0.68 for fused rows).
+constexpr int64_t kTwoPassL2Budget = 96ll << 20;
 
-int64_t twopass_grid_cap(int64_t hv, bool fused) {
+int64_t twopass_grid_cap(int64_t hv, bool fused, int sm_count) {
     const int64_t per_cta = hv * 16 * (fused ? 2 : 1);
     const int64_t cap = kTwoPassL2Budget / (per_cta > 0 ? per_cta : 1);
-    return cap < 1 ? 1 : cap;
+    return cap < sm_count ? sm_count : cap;
 }
 constexpr int kRingHeader = 128;  // the staged kernel's mbarriers, ahead of its ring
 
@@ -273,7 +275,7 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         const int64_t cap = (int64_t)slot.sm_count * bps;
         p.grid = forced->grid > 0 ? (forced->grid < ctas ? forced->grid : ctas) : (ctas < cap ? ctas : cap);
         if (forced->grid <= 0 && p.kernel == KS_KERNEL_TWOPASS_ROW) {
-            const int64_t l2cap = twopass_grid_cap(hidden / (16 / e), fused);
+            const int64_t l2cap = twopass_grid_cap(hidden / (16 / e), fused, slot.sm_count);
             if (p.grid > l2cap) p.grid = l2cap;
         }
         p.rows_per_pass = p.grid * per_cta;
@@ -344,7 +346,8 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 //    kernel.
 // The grid is persistent: at most sm_count * blocks_per_sm CTAs (for cluster plans, whole
 // clusters, which the launch caps again by the device's count of resident clusters; for the
-// two-pass kernel, no more CTAs than keep their rows in flight within 48 MiB of L2).
+// two-pass kernel, no more CTAs than keep their rows in flight within 96 MiB of L2, but at
+// least one per SM).
 namespace {
 
 void cta_row(ks_plan_t *p, int64_t hv, int v, bool prefetch) {
@@ -475,8 +478,8 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
     const int64_t ctas = ceil_div(rows, rows_per_cta);
     const int64_t cap = (int64_t)sm_count * blocks_per_sm;
     p->grid = (blocks_per_sm > 0 && ctas > cap) ? cap : ctas;
-    if (p->kernel == KS_KERNEL_TWOPASS_ROW && p->grid > twopass_grid_cap(hv, fused))
-        p->grid = twopass_grid_cap(hv, fused);
+    if (p->kernel == KS_KERNEL_TWOPASS_ROW && p->grid > twopass_grid_cap(hv, fused, sm_count))
+        p->grid = twopass_grid_cap(hv, fused, sm_count);
     p->rows_per_pass = p->grid * rows_per_cta;
     return KS_SUCCESS;
 }

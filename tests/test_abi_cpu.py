@@ -263,8 +263,10 @@ def test_rows_wider_than_registers_take_the_two_pass_kernel(hidden, dtype):
             assert p.block == (512 if hv <= 4096 else 1024)
         else:
             assert p.block == (256 if hv <= 4096 else 512 if hv <= 8192 else 1024)
-        # the grid keeps the rows in flight within 48 MiB of L2
-        assert p.grid <= max(1, (48 << 20) // (hv * 16 * (2 if op else 1))) and p.grid <= 152
+        # the grid keeps the rows in flight within 96 MiB of L2, but takes at least every SM
+        assert p.grid == min(152, max(152, (96 << 20) // (hv * 16 * (2 if op else 1))))
+        p2 = plan(op, 65536, hidden, dtype=dtype, bps=4)
+        assert p2.grid == min(608, max(152, (96 << 20) // (hv * 16 * (2 if op else 1))))
         # few rows: the register-resident cluster kernel, 8 CTAs per row (up to 16384 vectors)
         p = plan(op, 3, hidden, dtype=dtype, bps=1)
         if hv <= 16384:
