@@ -32,8 +32,9 @@
  *
  * Error behaviour: every argument check happens before any CUDA call, so an invalid call returns
  * its status without touching the device (and works on a machine without a GPU). The statuses:
- *   KS_ERR_INVALID_ARGUMENT   hidden <= 0, rows < 0, a NULL pointer with rows > 0, eps not
- *                             finite or not > 0, or a byte size that overflows int64;
+ *   KS_ERR_INVALID_ARGUMENT   hidden <= 0, rows < 0, a NULL pointer with rows > 0, a pointer
+ *                             that is not a multiple of the element size (2 or 4 bytes), eps
+ *                             not finite or not > 0, or a byte size that overflows int64;
  *   KS_ERR_UNSUPPORTED_DTYPE  dtype outside ks_dtype_t;
  *   KS_ERR_OVERLAP            fused: any two of the x, residual, weight byte ranges overlap;
  *                             plain: out overlaps weight, or overlaps x without being exactly x;
@@ -75,8 +76,9 @@ typedef void *ks_stream_t;
  *   rows    number of rows (the flattened leading dimensions); >= 0.
  *   hidden  row width (the last dimension); > 0.
  *   eps     finite, > 0; added to the mean square in FP32.
- * Any alignment is accepted; 16-byte aligned pointers with hidden*sizeof(element) a multiple of
- * 16 take the vectorised kernels, anything else a scalar kernel with the same arithmetic.
+ * Pointers must be aligned to the element size (else KS_ERR_INVALID_ARGUMENT); 16-byte aligned
+ * pointers with hidden*sizeof(element) a multiple of 16 take the vectorised kernels, anything
+ * else a scalar kernel with the same arithmetic.
  */
 ks_status_t ks_rms_norm(void *out, const void *x, const void *weight, int64_t rows,
                         int64_t hidden, float eps, ks_dtype_t dtype, ks_stream_t stream);

@@ -41,6 +41,11 @@ int elem_bytes(ks_dtype_t d) {
 }
 
 // [a, a+na) and [b, b+nb) share a byte.
+bool misaligned(int e, const void *a, const void *b, const void *c, const void *d) {
+    const uintptr_t m = (uintptr_t)e - 1;
+    return (((uintptr_t)a | (uintptr_t)b | (uintptr_t)c | (uintptr_t)d) & m) != 0;
+}
+
 bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
     const uintptr_t pa = (uintptr_t)a, pb = (uintptr_t)b;
     return pa < pb + (uintptr_t)nb && pb < pa + (uintptr_t)na;
@@ -217,6 +222,8 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
     if (rows == 0) return KS_SUCCESS;  // empty input: legal, nothing to launch
     if (!out || !x || !w || (fused && !res))
         return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    if (misaligned(e, out, x, w, fused ? res : nullptr))
+        return fail(KS_ERR_INVALID_ARGUMENT, "a pointer is not aligned to the %d-byte element", e);
     const int64_t nbytes = rows * hidden * e, wbytes = hidden * e;
     if (fused) {
         if (overlaps(x, nbytes, res, nbytes))

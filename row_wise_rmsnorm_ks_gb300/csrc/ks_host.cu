@@ -109,6 +109,8 @@ ks_status_t run_host(bool fused, void *out, const void *x, void *res, const void
     if (rows == 0) return KS_SUCCESS;
     if (!out || !x || !w || (fused && !res))
         return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    if (misaligned(e, out, x, w, fused ? res : nullptr))
+        return fail(KS_ERR_INVALID_ARGUMENT, "a pointer is not aligned to the %d-byte element", e);
     const int64_t row_bytes = hidden * e, nbytes = rows * row_bytes;
     if (fused) {
         if (overlaps(x, nbytes, res, nbytes))
@@ -128,6 +130,8 @@ ks_status_t run_host(bool fused, void *out, const void *x, void *res, const void
         return run(fused, od, xd, rd, w, rows, hidden, eps, dtype, stream, nullptr);
     }
     if (ws_bytes <= 0) return fail(KS_ERR_INVALID_ARGUMENT, "workspace_bytes must be > 0");
+    if (misaligned(e, ws))
+        return fail(KS_ERR_INVALID_ARGUMENT, "the workspace is not aligned to the %d-byte element", e);
     if (overlaps(ws, ws_bytes, w, row_bytes))
         return fail(KS_ERR_OVERLAP, "workspace and weight storage overlap");
     const int64_t chunk = host_chunk_rows(fused, hidden, e, ws_bytes);

@@ -27,6 +27,10 @@ ks_status_t fail(ks_status_t s, const char *fmt, ...);
 int elem_bytes(ks_dtype_t d);
 // Whether [a, a+na) and [b, b+nb) share a byte.
 bool overlaps(const void *a, int64_t na, const void *b, int64_t nb);
+// True when any of the (non-NULL) pointers is not a multiple of the element size e: every kernel
+// accesses whole elements, so such a pointer is an argument error.
+bool misaligned(int e, const void *a, const void *b = nullptr, const void *c = nullptr,
+                const void *d = nullptr);
 // The checked launch path behind every device-pointer entry point (forced == NULL: heuristic).
 ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, int64_t rows,
                 int64_t hidden, float eps, ks_dtype_t dtype, ks_stream_t stream,

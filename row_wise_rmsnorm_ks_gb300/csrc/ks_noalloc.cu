@@ -59,6 +59,8 @@ extern "C" ks_status_t ks_fused_add_rms_norm_host_noalloc(void *x, void *residua
                     (long long)hidden, (long long)(2 * hidden * e), (long long)kScratchBytes);
     if (rows == 0) return KS_SUCCESS;
     if (!x || !residual || !weight) return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    if (misaligned(e, x, residual, weight))
+        return fail(KS_ERR_INVALID_ARGUMENT, "a pointer is not aligned to the %d-byte element", e);
 
     // Set-up, once per device, with that device current: the scratch array's device address.
     int dev = 0;

@@ -557,6 +557,195 @@ __global__ void __launch_bounds__(1024) layer_norm_scalar_kernel(void *out, cons
     }
 }
 
+// ----------------------------------------------------------------------- wide rows
+
+// Rows too wide for the register kernels (more than 2048 16-byte vectors): one CTA per row, the
+// row read once per pass with 16-byte vectors, U vectors per thread in flight per step; every
+// pass after the first re-reads the row from L2, as the grid keeps the rows all CTAs have in
+// flight inside it (wide_grid_cap), so DRAM still sees each element read once. Same arithmetic
+// as the register kernels above. The first passes load with the default L2 policy, the last with
+// evict-first (last use).
+
+// Softmax: max, sum of exponentials, outputs.
+template <typename T, int U>
+__global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const void *x,
+                                                            int64_t rows, int64_t hv) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    __shared__ float red[2][32];
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const uint4 *xg = static_cast<const uint4 *>(x);
+    uint4 *og = static_cast<uint4 *>(out);
+    const int t = threadIdx.x, g = blockDim.x;
+    const int64_t chunk = (int64_t)g * U;
+    int slot = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const uint4 *xr = xg + row * hv;
+        float m = -INFINITY;
+        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                v[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (c0 + (int64_t)u * g < hv) {
+                    float f[N];
+                    E::unpack(v[u], f);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) m = fmaxf(m, f[e]);
+                }
+            }
+        }
+        m = cta_max(m, red, slot);
+        const float bias = __fmaf_rn(-m, kLog2e, 64.0f);  // see softmax_vec_kernel
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                v[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (c0 + (int64_t)u * g < hv) {
+                    float f[N];
+                    E::unpack(v[u], f);
+#pragma unroll
+                    for (int e = 0; e < N; ++e)
+                        s4[e & 3] = __fadd_rn(s4[e & 3], sizeof(T) == 4 ? expf(__fsub_rn(f[e], m))
+                                                         : ex2_sfu(__fmaf_rn(f[e], kLog2e, bias)));
+                }
+            }
+        }
+        const float inv = __frcp_rn(
+            cta_sum(__fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3])), red, slot));
+        uint4 *orow = og + row * hv;
+        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                v[u] = c < hv ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                if (c < hv) {
+                    float f[N];
+                    E::unpack(v[u], f);
+#pragma unroll
+                    for (int e = 0; e < N; ++e)
+                        f[e] = __fmul_rn(sizeof(T) == 4 ? expf(__fsub_rn(f[e], m))
+                                                        : ex2_sfu(__fmaf_rn(f[e], kLog2e, bias)),
+                                         inv);
+                    __stcs(orow + c, E::pack(f));
+                }
+            }
+        }
+    }
+}
+
+// LayerNorm: mean, variance, outputs.
+template <typename T, int U, int kAffine>
+__global__ void __launch_bounds__(512) layer_norm_wide_kernel(void *out, const void *x,
+                                                               const void *w, const void *b,
+                                                               int64_t rows, int64_t hidden,
+                                                               int64_t hv, float eps) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
+    __shared__ float red[2][32];
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const uint4 *xg = static_cast<const uint4 *>(x);
+    uint4 *og = static_cast<uint4 *>(out);
+    const uint4 *wg = static_cast<const uint4 *>(w);
+    const uint4 *bg = static_cast<const uint4 *>(b);
+    const int t = threadIdx.x, g = blockDim.x;
+    const int64_t chunk = (int64_t)g * U;
+    const float h = (float)hidden;
+    int slot = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        const uint4 *xr = xg + row * hv;
+        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                v[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float f[N];
+                E::unpack(v[u], f);
+#pragma unroll
+                for (int e = 0; e < N; ++e) s4[e & 3] = __fadd_rn(s4[e & 3], f[e]);
+            }
+        }
+        const float mean = __fdiv_rn(
+            cta_sum(__fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3])), red, slot), h);
+        SumSq q;
+        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                v[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (c0 + (int64_t)u * g < hv) {
+                    float f[N];
+                    E::unpack(v[u], f);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) f[e] = __fsub_rn(f[e], mean);
+                    q.add(f);
+                }
+            }
+        }
+        const float var = __fdiv_rn(cta_sum(q.total(), red, slot), h);
+        const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
+        const float shift = -__fmul_rn(mean, rstd);
+        uint4 *orow = og + row * hv;
+        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+            uint4 v[U], wv[U], bv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                const bool in = c < hv;
+                v[u] = in ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+                wv[u] = (kW && in) ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+                bv[u] = (kB && in) ? __ldg(bg + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                if (c < hv) {
+                    float f[N], wf[N], bf[N];
+                    E::unpack(v[u], f);
+                    if (kW) E::unpack(wv[u], wf);
+                    if (kB) E::unpack(bv[u], bf);
+#pragma unroll
+                    for (int e = 0; e < N; ++e) {
+                        float o = __fmaf_rn(f[e], rstd, shift);  // (x - mean) * rstd
+                        if (kW && kB) o = __fmaf_rn(o, wf[e], bf[e]);
+                        else if (kW) o = __fmul_rn(o, wf[e]);
+                        else if (kB) o = __fadd_rn(o, bf[e]);
+                        f[e] = o;
+                    }
+                    __stcs(orow + c, E::pack(f));
+                }
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------------ launch planning
 
 int g_sm_count[64];
@@ -590,6 +779,27 @@ int row_vec_plan(int64_t hv, int *block) {
     if (b > 512) return 0;
     *block = (int)b;
     return v;
+}
+
+// Rows wider than the register kernels hold take the wide multi-pass kernels (marked by this
+// vector count), 4 vectors per thread per step. Small CTAs keep more rows in flight per SM;
+// measured on GB300 (bf16, HBM-bound rows), the best block grows with the width: Softmax 128
+// threads up to 3072 vectors, 256 up to 6144, 512 beyond (0.66-0.87 of the copy peak, against
+// 0.62-0.79 at a fixed 512); LayerNorm 128 up to 3072, 256 up to 12288, 512 beyond (0.52-0.86,
+// against 0.38-0.62).
+constexpr int kWideRows = 16;
+
+int wide_row_block(int64_t hv, bool layer_norm) {
+    if (hv <= 3072) return 128;
+    if (hv <= (layer_norm ? 12288 : 6144)) return 256;
+    return 512;
+}
+
+// The wide kernels re-read each row from L2: no more CTAs than keep their rows in flight within
+// 96 MiB of it, but at least one per SM (as for the two-pass RMSNorm kernel).
+int64_t wide_grid_cap(int64_t hv, int sms) {
+    const int64_t cap = (96ll << 20) / (hv * 16);
+    return cap < sms ? sms : cap;
 }
 
 ks_status_t check_common(int64_t rows, int64_t width, ks_dtype_t dtype, int *e) {
@@ -650,6 +860,7 @@ cudaError_t softmax_dispatch(int v, int block, void *out, const void *x, int64_t
         f = width <= 1024 ? (const void *)softmax_vec_kernel<T, 4, false>
                           : (const void *)softmax_vec_kernel<T, 4, true>;
         break;
+    case kWideRows: f = (const void *)softmax_wide_kernel<T, 4>; break;
     default:
         f = (const void *)softmax_scalar_kernel<T>;
         block = (int)round_up64(ceil_div64(width, 8), 32);
@@ -658,6 +869,7 @@ cudaError_t softmax_dispatch(int v, int block, void *out, const void *x, int64_t
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, 0) != cudaSuccess || n < 1) n = 1;
     int64_t grid = (int64_t)sms * n;
+    if (v == kWideRows && grid > wide_grid_cap(width, sms)) grid = wide_grid_cap(width, sms);
     grid = grid > rows ? rows : grid;
     return launch(f, dim3((unsigned)grid), dim3(block), args, s);
 }
@@ -709,6 +921,10 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
                                    layer_norm_vec_kernel<T, 2, 2>, layer_norm_vec_kernel<T, 2, 3>); break;
     case 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0>, layer_norm_vec_kernel<T, 4, 1>,
                                    layer_norm_vec_kernel<T, 4, 2>, layer_norm_vec_kernel<T, 4, 3>); break;
+    case kWideRows:
+        f = layer_norm_pick<T>(affine, layer_norm_wide_kernel<T, 4, 0>, layer_norm_wide_kernel<T, 4, 1>,
+                               layer_norm_wide_kernel<T, 4, 2>, layer_norm_wide_kernel<T, 4, 3>);
+        break;
     case 8:
         f = layer_norm_pick<T>(affine, layer_norm_bulk_kernel<T, 4, 0>, layer_norm_bulk_kernel<T, 4, 1>,
                                layer_norm_bulk_kernel<T, 4, 2>, layer_norm_bulk_kernel<T, 4, 3>);
@@ -738,6 +954,7 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, smem) != cudaSuccess || n < 1) n = 1;
     int64_t grid = (int64_t)sms * n;
+    if (v == kWideRows && !stages && grid > wide_grid_cap(hv, sms)) grid = wide_grid_cap(hv, sms);
     grid = grid > rows ? rows : grid;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
@@ -769,6 +986,8 @@ ks_status_t ks_silu_and_mul(void *out, const void *x, int64_t rows, int64_t d, k
     if (st != KS_SUCCESS) return st;
     if (rows == 0) return KS_SUCCESS;
     if (!out || !x) return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    if (misaligned(e, out, x))
+        return fail(KS_ERR_INVALID_ARGUMENT, "a pointer is not aligned to the %d-byte element", e);
     if (overlaps(out, rows * d * e, x, rows * 2 * d * e))
         return fail(KS_ERR_OVERLAP, "out and x storage overlap");
     int sms = 0;
@@ -792,6 +1011,8 @@ ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, k
     if (st != KS_SUCCESS) return st;
     if (rows == 0) return KS_SUCCESS;
     if (!out || !x) return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    if (misaligned(e, out, x))
+        return fail(KS_ERR_INVALID_ARGUMENT, "a pointer is not aligned to the %d-byte element", e);
     const int64_t nbytes = rows * hidden * e;
     if (out != x && overlaps(out, nbytes, x, nbytes))
         return fail(KS_ERR_OVERLAP, "out partially overlaps x (only out == x is allowed)");
@@ -800,7 +1021,14 @@ ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, k
     const bool aligned = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0 && (hidden * e) % 16 == 0;
     int block = 0, v = 0;
     int64_t width = hidden;
-    if (aligned && (v = row_vec_plan(hidden * e / 16, &block)) > 0) width = hidden * e / 16;
+    if (aligned) {
+        width = hidden * e / 16;
+        v = row_vec_plan(width, &block);
+        if (v == 0) {
+            v = kWideRows;
+            block = wide_row_block(width, false);
+        }
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce;
     switch (dtype) {
@@ -822,6 +1050,8 @@ ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const vo
         return fail(KS_ERR_INVALID_ARGUMENT, "eps must be finite and > 0 (got %g)", (double)eps);
     if (rows == 0) return KS_SUCCESS;
     if (!out || !x) return fail(KS_ERR_INVALID_ARGUMENT, "NULL pointer with rows > 0");
+    if (misaligned(e, out, x, weight, bias))
+        return fail(KS_ERR_INVALID_ARGUMENT, "a pointer is not aligned to the %d-byte element", e);
     const int64_t nbytes = rows * hidden * e, pbytes = hidden * e;
     if (out != x && overlaps(out, nbytes, x, nbytes))
         return fail(KS_ERR_OVERLAP, "out partially overlaps x (only out == x is allowed)");
@@ -833,7 +1063,13 @@ ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const vo
     const bool aligned = (al & 15u) == 0 && (hidden * e) % 16 == 0;
     int block = 0, v = 0;
     const int64_t hv = hidden * e / 16;
-    if (aligned) v = row_vec_plan(hv, &block);
+    if (aligned) {
+        v = row_vec_plan(hv, &block);
+        if (v == 0) {
+            v = kWideRows;
+            block = wide_row_block(hv, true);  // at most 512: the kernel's bound
+        }
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce;
     switch (dtype) {

@@ -395,3 +395,29 @@ def test_latency_regime_choices():
     # plain rows wider than 1024 vectors keep 4 vectors per thread
     p = plan(0, 33, 16384)
     assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.vec_per_thread == 4 and p.block == 512
+
+
+@pytest.mark.parametrize("dtype,off", [(F32, 2), (F32, 1), (BF16, 1), (F16, 1)])
+def test_pointers_not_aligned_to_the_element_are_rejected(dtype, off):
+    """Every kernel accesses whole elements: a pointer that is not a multiple of the element size
+    is an argument error for every entry point, found before any CUDA call."""
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    a, b, w, c = FAKE, FAKE + (1 << 30), FAKE + (2 << 30), FAKE + (3 << 30)
+    rows, h = 8, 64
+    for args in ((a + off, b, w), (a, b + off, w), (a, b, w + off)):
+        assert _abi.ks_rms_norm(*args, rows, h, 1e-6, dtype, None) == E
+        assert "aligned to the" in _abi.ks_last_error()
+        assert _abi.ks_fused_add_rms_norm(*args, rows, h, 1e-6, dtype, None) == E
+        p = _abi.make_plan(_abi.KS_KERNEL_SCALAR, 0, 64)
+        assert _abi.ks_rms_norm_planned(*args, rows, h, 1e-6, dtype, p, None) == E
+        assert _abi.ks_rms_norm_host(*args, rows, h, 1e-6, dtype, c, 1 << 24, None) == E
+        assert _abi.ks_fused_add_rms_norm_host(*args, rows, h, 1e-6, dtype, c, 1 << 24, None) == E
+        assert _abi.ks_fused_add_rms_norm_host_noalloc(*args, rows, h, 1e-6, dtype, None) == E
+    assert _abi.ks_rms_norm_host(a, b, w, rows, h, 1e-6, dtype, c + off, 1 << 24, None) == E
+    assert _abi.ks_silu_and_mul(a + off, b, rows, h, dtype, None) == E
+    assert _abi.ks_silu_and_mul(a, b + off, rows, h, dtype, None) == E
+    assert _abi.ks_softmax(a + off, b, rows, h, dtype, None) == E
+    assert _abi.ks_softmax(a, b + off, rows, h, dtype, None) == E
+    assert _abi.ks_layer_norm(a + off, b, w, c, rows, h, 1e-5, dtype, None) == E
+    assert _abi.ks_layer_norm(a, b, w + off, None, rows, h, 1e-5, dtype, None) == E
+    assert _abi.ks_layer_norm(a, b, None, c + off, rows, h, 1e-5, dtype, None) == E

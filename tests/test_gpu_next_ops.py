@@ -204,3 +204,31 @@ def test_layer_norm_many_rows_staged(cuda_device, dtype, h, affine):
     _ln_check(y, ref, dt, h, f"layer_norm staged {dtype} [{rows},{h}] affine={affine}")
     st, flags = _abi.ks_device_faults(clear=False)
     assert st == _abi.KS_SUCCESS and flags == 0
+
+
+# --------------------------------------------------------------- rows wider than 2048 vectors
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("rows,h", [(300, 20480), (97, 65536), (5, 40000)])
+def test_softmax_rows_wider_than_registers(cuda_device, dtype, rows, h):
+    """The wide multi-pass kernel (max, sum, outputs; later passes from L2)."""
+    dt = synth.dtype_of(dtype)
+    x = synth.cast(synth.normal_np((rows, h), 831, std=3.0), dt)
+    y = ks.softmax(x.to(cuda_device)).cpu()
+    ref, _ = oracle.softmax(x)
+    compare_output(y, ref, dt, h, f"softmax wide {dtype} [{rows},{h}]")
+
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("rows,h", [(300, 20480), (97, 65536), (5, 40000)])
+@pytest.mark.parametrize("affine", AFFINE)
+def test_layer_norm_rows_wider_than_registers(cuda_device, dtype, rows, h, affine):
+    """The wide multi-pass kernel (mean, variance, outputs; later passes from L2)."""
+    dt = synth.dtype_of(dtype)
+    x = synth.cast(synth.normal_np((rows, h), 832) + 0.5, dt)
+    w, b = _affine(affine, h, dt, 833)
+    y = ks.layer_norm(x.to(cuda_device), _dev(w, cuda_device), _dev(b, cuda_device), 1e-5).cpu()
+    ref, _ = oracle.layer_norm(x, w, b, 1e-5)
+    _ln_check(y, ref, dt, h, f"layer_norm wide {dtype} [{rows},{h}] affine={affine}")
+    st, flags = _abi.ks_device_faults(clear=False)
+    assert st == _abi.KS_SUCCESS and flags == 0
