@@ -292,13 +292,103 @@ constexpr int kAffineWeight = 1, kAffineBias = 2;
 // vectors are loaded before the current row's two reductions. (Measured on GB300 at [32768,
 // 8192] bf16: 74 % of the copy peak; weight and bias in shared memory, with or without the
 // prefetch, were slower at 58-64 %.)
+// LayerNorm element steps. Four running sums per thread: element e of a vector feeds sum e % 4,
+// held as lane e % 2 of FP32 pair (e / 2) % 2, and a row's partial sum is the pairwise total.
+// Element types with Elem::kPairMath run the steps on packed FP32 pairs (bit-identical to the
+// scalar steps, half the instructions; for bf16 LayerNorm rows of 768..4096 vectors that
+// measured 4-8 points of the copy peak faster on GB300).
+template <typename T>
+__device__ __forceinline__ void ln_add_sum(const uint4 &v, float2 (&s)[2]) {
+    if constexpr (Elem<T>::kPairMath) {
+        float2 f[4];
+        Elem<T>::unpack2(v, f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s[i & 1] = __fadd2_rn(s[i & 1], f[i]);
+    } else {
+        constexpr int N = Elem<T>::kPerVec;
+        float f[N];
+        Elem<T>::unpack(v, f);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            float &acc = (e & 1) ? s[(e >> 1) & 1].y : s[(e >> 1) & 1].x;
+            acc = __fadd_rn(acc, f[e]);
+        }
+    }
+}
+
+// the squares of x - mean, summed as above (x - mean formed as x + (-mean), which is exact)
+template <typename T>
+__device__ __forceinline__ void ln_add_sq(const uint4 &v, float neg_mean, float2 (&q)[2]) {
+    if constexpr (Elem<T>::kPairMath) {
+        float2 f[4];
+        Elem<T>::unpack2(v, f);
+        const float2 m = make_float2(neg_mean, neg_mean);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 d = __fadd2_rn(f[i], m);
+            q[i & 1] = __ffma2_rn(d, d, q[i & 1]);
+        }
+    } else {
+        constexpr int N = Elem<T>::kPerVec;
+        float f[N];
+        Elem<T>::unpack(v, f);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            const float d = __fadd_rn(f[e], neg_mean);
+            float &acc = (e & 1) ? q[(e >> 1) & 1].y : q[(e >> 1) & 1].x;
+            acc = __fmaf_rn(d, d, acc);
+        }
+    }
+}
+
+__device__ __forceinline__ float ln_total(const float2 (&s)[2]) {
+    return __fadd_rn(__fadd_rn(s[0].x, s[0].y), __fadd_rn(s[1].x, s[1].y));
+}
+
+// One output vector: (x - mean) * rstd as one FMA with shift = -mean * rstd, then the affine
+// step (weight and bias, weight alone or bias alone, as kAffine says).
+template <typename T, int kAffine>
+__device__ __forceinline__ uint4 ln_out(const uint4 &v, const uint4 &wv, const uint4 &bv,
+                                        float rstd, float shift) {
+    constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
+    if constexpr (Elem<T>::kPairMath) {
+        float2 f[4], wf[4], bf[4];
+        Elem<T>::unpack2(v, f);
+        if (kW) Elem<T>::unpack2(wv, wf);
+        if (kB) Elem<T>::unpack2(bv, bf);
+        const float2 r2 = make_float2(rstd, rstd), s2 = make_float2(shift, shift);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 o = __ffma2_rn(f[i], r2, s2);
+            if (kW && kB) o = __ffma2_rn(o, wf[i], bf[i]);
+            else if (kW) o = __fmul2_rn(o, wf[i]);
+            else if (kB) o = __fadd2_rn(o, bf[i]);
+            f[i] = o;
+        }
+        return Elem<T>::pack2(f);
+    } else {
+        constexpr int N = Elem<T>::kPerVec;
+        float f[N], wf[N], bf[N];
+        Elem<T>::unpack(v, f);
+        if (kW) Elem<T>::unpack(wv, wf);
+        if (kB) Elem<T>::unpack(bv, bf);
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            float o = __fmaf_rn(f[e], rstd, shift);
+            if (kW && kB) o = __fmaf_rn(o, wf[e], bf[e]);
+            else if (kW) o = __fmul_rn(o, wf[e]);
+            else if (kB) o = __fadd_rn(o, bf[e]);
+            f[e] = o;
+        }
+        return Elem<T>::pack(f);
+    }
+}
+
 template <typename T, int V, int kAffine>
 __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const void *x,
                                                              const void *w, const void *b,
                                                              int64_t rows, int64_t hidden,
                                                              int64_t hv, float eps) {
-    using E = Elem<T>;
-    constexpr int N = E::kPerVec;
     constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
     __shared__ float red[2][32];
     grid_dependency_wait();
@@ -330,49 +420,21 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
             const int64_t c = t + (int64_t)k * g;
             nxt[k] = (next < rows && c < hv) ? __ldcs(xg + next * hv + c) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            float f[N];
-            E::unpack(xv[k], f);
+        for (int k = 0; k < V; ++k) ln_add_sum<T>(xv[k], s2);
+        const float mean = __fdiv_rn(cta_sum(ln_total(s2), red, slot), h);
+        float2 q2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-            for (int e = 0; e < N; ++e) s4[e & 3] = __fadd_rn(s4[e & 3], f[e]);
-        }
-        const float mean = __fdiv_rn(
-            cta_sum(__fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3])), red, slot), h);
-        SumSq q;
-#pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
-                float f[N];
-                E::unpack(xv[k], f);
-#pragma unroll
-                for (int e = 0; e < N; ++e) f[e] = __fsub_rn(f[e], mean);
-                q.add(f);
-            }
-        }
-        const float var = __fdiv_rn(cta_sum(q.total(), red, slot), h);
+        for (int k = 0; k < V; ++k)
+            if (t + (int64_t)k * g < hv) ln_add_sq<T>(xv[k], -mean, q2);
+        const float var = __fdiv_rn(cta_sum(ln_total(q2), red, slot), h);
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
         const float shift = -__fmul_rn(mean, rstd);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
-                float f[N], wf[N], bf[N];
-                E::unpack(xv[k], f);
-                if (kW) E::unpack(wv[k], wf);
-                if (kB) E::unpack(bv[k], bf);
-#pragma unroll
-                for (int e = 0; e < N; ++e) {
-                    float v = __fmaf_rn(f[e], rstd, shift);  // (x - mean) * rstd
-                    if (kW && kB) v = __fmaf_rn(v, wf[e], bf[e]);
-                    else if (kW) v = __fmul_rn(v, wf[e]);
-                    else if (kB) v = __fadd_rn(v, bf[e]);
-                    f[e] = v;
-                }
-                __stcs(og + row * hv + c, E::pack(f));
-            }
+            if (c < hv) __stcs(og + row * hv + c, ln_out<T, kAffine>(xv[k], wv[k], bv[k], rstd, shift));
         }
 #pragma unroll
         for (int k = 0; k < V; ++k) xv[k] = nxt[k];
@@ -392,8 +454,6 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
                                                               const void *w, const void *b,
                                                               int64_t rows, int64_t hidden,
                                                               int64_t hv, float eps, int stages) {
-    using E = Elem<T>;
-    constexpr int N = E::kPerVec;
     constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[2][32];
@@ -440,19 +500,16 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
         const bool ok = mbar_wait_bounded(&bars[st], phase);
         const unsigned char *sx = ring + (size_t)st * row_bytes;
         uint4 xv[V];
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
             xv[k] = (ok && c < hv) ? ld_shared_v4(sx + c * 16) : make_uint4(0u, 0u, 0u, 0u);
-            float f[N];
-            E::unpack(xv[k], f);
-#pragma unroll
-            for (int e = 0; e < N; ++e) s4[e & 3] = __fadd_rn(s4[e & 3], f[e]);
+            ln_add_sum<T>(xv[k], s2);
         }
         // first reduction: every thread holds its vectors, so the stage is free, and a time-out
         // anywhere is seen by all
-        const float part = warp_sum(__fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3])));
+        const float part = warp_sum(ln_total(s2));
         if ((t & 31) == 0) red[slot][t >> 5] = part;
         if (__syncthreads_or(!ok)) {
             fault = true;
@@ -466,19 +523,11 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
         for (int i = 0; i < (g >> 5); ++i) tot += red[slot][i];
         slot ^= 1;
         const float mean = __fdiv_rn(tot, h);
-        SumSq q;
+        float2 q2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
-                float f[N];
-                E::unpack(xv[k], f);
-#pragma unroll
-                for (int e = 0; e < N; ++e) f[e] = __fsub_rn(f[e], mean);
-                q.add(f);
-            }
-        }
-        const float var = __fdiv_rn(cta_sum(q.total(), red, slot), h);
+        for (int k = 0; k < V; ++k)
+            if (t + (int64_t)k * g < hv) ln_add_sq<T>(xv[k], -mean, q2);
+        const float var = __fdiv_rn(cta_sum(ln_total(q2), red, slot), h);
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
         const float shift = -__fmul_rn(mean, rstd);
 #pragma unroll
@@ -489,21 +538,7 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
-                float f[N], wf[N], bf[N];
-                E::unpack(xv[k], f);
-                if (kW) E::unpack(wv[k], wf);
-                if (kB) E::unpack(bv[k], bf);
-#pragma unroll
-                for (int e = 0; e < N; ++e) {
-                    float v = __fmaf_rn(f[e], rstd, shift);  // (x - mean) * rstd
-                    if (kW && kB) v = __fmaf_rn(v, wf[e], bf[e]);
-                    else if (kW) v = __fmul_rn(v, wf[e]);
-                    else if (kB) v = __fadd_rn(v, bf[e]);
-                    f[e] = v;
-                }
-                __stcs(og + row * hv + c, E::pack(f));
-            }
+            if (c < hv) __stcs(og + row * hv + c, ln_out<T, kAffine>(xv[k], wv[k], bv[k], rstd, shift));
         }
         if (++st == stages) {
             st = 0;
@@ -656,8 +691,6 @@ __global__ void __launch_bounds__(512) layer_norm_wide_kernel(void *out, const v
                                                                const void *w, const void *b,
                                                                int64_t rows, int64_t hidden,
                                                                int64_t hv, float eps) {
-    using E = Elem<T>;
-    constexpr int N = E::kPerVec;
     constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
     __shared__ float red[2][32];
     grid_dependency_wait();
@@ -672,7 +705,7 @@ __global__ void __launch_bounds__(512) layer_norm_wide_kernel(void *out, const v
     int slot = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
         const uint4 *xr = xg + row * hv;
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
         for (int64_t c0 = t; c0 < hv; c0 += chunk) {
             uint4 v[U];
 #pragma unroll
@@ -681,16 +714,10 @@ __global__ void __launch_bounds__(512) layer_norm_wide_kernel(void *out, const v
                 v[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float f[N];
-                E::unpack(v[u], f);
-#pragma unroll
-                for (int e = 0; e < N; ++e) s4[e & 3] = __fadd_rn(s4[e & 3], f[e]);
-            }
+            for (int u = 0; u < U; ++u) ln_add_sum<T>(v[u], s2);
         }
-        const float mean = __fdiv_rn(
-            cta_sum(__fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3])), red, slot), h);
-        SumSq q;
+        const float mean = __fdiv_rn(cta_sum(ln_total(s2), red, slot), h);
+        float2 q2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
         for (int64_t c0 = t; c0 < hv; c0 += chunk) {
             uint4 v[U];
 #pragma unroll
@@ -699,17 +726,10 @@ __global__ void __launch_bounds__(512) layer_norm_wide_kernel(void *out, const v
                 v[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (c0 + (int64_t)u * g < hv) {
-                    float f[N];
-                    E::unpack(v[u], f);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fsub_rn(f[e], mean);
-                    q.add(f);
-                }
-            }
+            for (int u = 0; u < U; ++u)
+                if (c0 + (int64_t)u * g < hv) ln_add_sq<T>(v[u], -mean, q2);
         }
-        const float var = __fdiv_rn(cta_sum(q.total(), red, slot), h);
+        const float var = __fdiv_rn(cta_sum(ln_total(q2), red, slot), h);
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
         const float shift = -__fmul_rn(mean, rstd);
         uint4 *orow = og + row * hv;
@@ -726,21 +746,7 @@ __global__ void __launch_bounds__(512) layer_norm_wide_kernel(void *out, const v
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int64_t c = c0 + (int64_t)u * g;
-                if (c < hv) {
-                    float f[N], wf[N], bf[N];
-                    E::unpack(v[u], f);
-                    if (kW) E::unpack(wv[u], wf);
-                    if (kB) E::unpack(bv[u], bf);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) {
-                        float o = __fmaf_rn(f[e], rstd, shift);  // (x - mean) * rstd
-                        if (kW && kB) o = __fmaf_rn(o, wf[e], bf[e]);
-                        else if (kW) o = __fmul_rn(o, wf[e]);
-                        else if (kB) o = __fadd_rn(o, bf[e]);
-                        f[e] = o;
-                    }
-                    __stcs(orow + c, E::pack(f));
-                }
+                if (c < hv) __stcs(orow + c, ln_out<T, kAffine>(v[u], wv[u], bv[u], rstd, shift));
             }
         }
     }
@@ -905,10 +911,20 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
     // Many rows wider than 512 vectors: the staged ring (KS_LN_RING_BYTES of rows per CTA, 2..8
     // stages) keeps enough bytes in flight; otherwise the register kernel, which measured faster
     // for rows of at most 512 vectors (0.74-0.82 of the copy peak against 0.65-0.69 for the ring).
+    // Between 1024 and 2048 vectors the ring's CTA (a thread per 4 vectors, ~105 registers for
+    // 16-bit types) leaves one CTA of 8-14 warps per SM; the wide kernel's 128-thread CTAs keep
+    // more warps resident and measured faster on GB300 for many rows: bf16 1280..1792 vectors
+    // 0.76-0.83 of the copy peak against 0.65-0.78, fp32 1024..1792 0.88-0.95 against 0.76-0.86
+    // (at 1024 bf16 vectors the ring measured 0.96 against 0.81, so 16-bit rows start above it).
     int stages = 0;
     if (v == 4 && hv > 512 && rows >= 4 * (int64_t)sms) {
-        int64_t n_st = (KS_LN_RING_BYTES) / (hv * 16);
-        stages = (int)(n_st < 2 ? 2 : (n_st > 8 ? 8 : n_st));
+        if (hv < 2048 && hv >= (sizeof(T) == 4 ? 1024 : 1025)) {
+            v = kWideRows;
+            block = 128;
+        } else {
+            int64_t n_st = (KS_LN_RING_BYTES) / (hv * 16);
+            stages = (int)(n_st < 2 ? 2 : (n_st > 8 ? 8 : n_st));
+        }
     }
     void *bulk_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
                          const_cast<void **>(&b), &nr, &hd, &hvv, &ep, &stages};

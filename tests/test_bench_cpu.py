@@ -98,3 +98,16 @@ def test_kernel_hash_ignores_comments_and_layout():
     assert bench.code_only(src) != bench.code_only(changed)
     assert '"// kept"' in bench.code_only(src)
 
+
+
+def test_recorded_traffic_only_for_the_recorded_shape():
+    """The committed ncu bytes are per launch of the full workload: a smaller --rows/--hidden
+    case reports no traffic, and its config names its own shape."""
+    full = bench.recorded_traffic("fused_add_rms_norm")
+    assert full is None or full > 0
+    assert bench.recorded_traffic("fused_add_rms_norm", 8192, 8192) is None
+    assert bench.recorded_traffic("rms_norm", bench.FULL_ROWS, 4096) is None
+    assert "[8192,8192]" in bench.workload(8192, 8192) and "128 MiB" in bench.workload(8192, 8192)
+    assert bench.workload(bench.FULL_ROWS, bench.FULL_HIDDEN).startswith("large prefill bf16")
+    assert "larger than L2" in bench.l2_note(bench.FULL_ROWS, bench.FULL_HIDDEN)
+    assert "not a bench figure" in bench.l2_note(1024, 1024)

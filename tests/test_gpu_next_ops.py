@@ -188,14 +188,13 @@ def test_softmax_extreme_spread(cuda_device, dtype):
 
 
 @pytest.mark.parametrize("dtype", DT)
-@pytest.mark.parametrize("h", [1024, 4096, 8192, 16384])
+@pytest.mark.parametrize("h", [1024, 4096, 8192, 10240, 12288, 16384])
 @pytest.mark.parametrize("affine", AFFINE)
 def test_layer_norm_many_rows_staged(cuda_device, dtype, h, affine):
-    """Enough rows for the staged ring (>= 4 rows per SM): sampled rows against the oracle, and
-    the ring's fault word stays clear."""
+    """Enough rows (>= 4 rows per SM) for the staged ring, or, for rows of 1024..2047 vectors,
+    the wide kernel's 128-thread CTAs: every row against the oracle, and the ring's fault word
+    stays clear."""
     dt = synth.dtype_of(dtype)
-    if dt == torch.float32 and h > 8192:
-        pytest.skip("fp32 rows wider than 2048 vectors take the scalar kernel")
     rows = 1000
     x = synth.cast(synth.normal_np((rows, h), 811) - 0.5, dt)
     w, b = _affine(affine, h, dt, 812)
