@@ -35,13 +35,15 @@ namespace ks {
 template <typename T>
 struct Elem;
 
-// kPairMath: the row kernels run the element steps on packed FP32 pairs (the FADD2/FMUL2/FFMA2
-// instructions of sm_100 and later). Each lane is one IEEE round-to-nearest operation, so with
-// the same sums in the same order the results are bit-identical to the scalar steps, in half the
-// floating-point instructions. Measured on GB300 for bf16 (RMSNorm 1024..8192 elements per row:
-// 0-1 point of the copy peak faster; LayerNorm 768..4096 vectors: 4-8 points); for fp16 (whose
-// conversions are not plain shifts) it measured between 2 points slower and 1 faster, and FP32
-// rows (4 elements per vector) gained nothing, so those keep the scalar steps.
+// Vectors are unpacked to FP32 pairs (element 2i, 2i + 1; unpack2/pack2), and the row kernels run
+// each element step on a pair (pair_add, pair_mul, pair_fma below). kPairMath: the step is one
+// packed FP32 instruction (FADD2/FMUL2/FFMA2, sm_100 and later); otherwise two scalar operations.
+// Either way each element gets one IEEE round-to-nearest operation, so the two forms give the
+// same bits, and the packed one takes half the floating-point instructions. Measured on GB300 for
+// bf16: RMSNorm rows of 1024..8192 elements 0-1 point of the copy peak faster, LayerNorm rows of
+// 768..4096 vectors 4-8 points. fp16 (whose conversions are not plain shifts) measured between 2
+// points slower and 1 faster, and fp32 rows (2 pairs per vector) gained nothing, so those two
+// keep scalar operations.
 template <>
 struct Elem<__nv_bfloat16> {
     static constexpr int kPerVec = 8;
@@ -111,6 +113,24 @@ struct Elem<__half> {
         }
         return make_uint4(w[0], w[1], w[2], w[3]);
     }
+    __device__ __forceinline__ static void unpack2(const uint4 &v, float2 (&f)[4]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h;
+            memcpy(&h, &w[i], sizeof(uint32_t));
+            f[i] = __half22float2(h);
+        }
+    }
+    __device__ __forceinline__ static uint4 pack2(const float2 (&f)[4]) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 h = __float22half2_rn(f[i]);
+            memcpy(&w[i], &h, sizeof(uint32_t));
+        }
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
     __device__ __forceinline__ static float load1(const void *p, int64_t i) {
         return __half2float(static_cast<const __half *>(p)[i]);
     }
@@ -132,6 +152,14 @@ struct Elem<float> {
     __device__ __forceinline__ static uint4 pack(const float (&f)[4]) {
         return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                           __float_as_uint(f[3]));
+    }
+    __device__ __forceinline__ static void unpack2(const uint4 &v, float2 (&f)[2]) {
+        f[0] = make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+        f[1] = make_float2(__uint_as_float(v.z), __uint_as_float(v.w));
+    }
+    __device__ __forceinline__ static uint4 pack2(const float2 (&f)[2]) {
+        return make_uint4(__float_as_uint(f[0].x), __float_as_uint(f[0].y), __float_as_uint(f[1].x),
+                          __float_as_uint(f[1].y));
     }
     __device__ __forceinline__ static float load1(const void *p, int64_t i) {
         return static_cast<const float *>(p)[i];
@@ -185,6 +213,67 @@ struct SumSq {
     }
 };
 
+// ------------------------------------------------------------- element steps on FP32 pairs
+
+template <bool kPair>
+__device__ __forceinline__ float2 pair_add(float2 a, float2 b) {
+    if constexpr (kPair) return __fadd2_rn(a, b);
+    else return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y));
+}
+
+template <bool kPair>
+__device__ __forceinline__ float2 pair_mul(float2 a, float2 b) {
+    if constexpr (kPair) return __fmul2_rn(a, b);
+    else return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y));
+}
+
+template <bool kPair>
+__device__ __forceinline__ float2 pair_fma(float2 a, float2 b, float2 c) {
+    if constexpr (kPair) return __ffma2_rn(a, b, c);
+    else return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
+}
+
+// The four FMA chains of SumSq held as two pairs: element e feeds chain e % 4, which is lane
+// e % 2 of pair (e / 2) % 2; the total adds the chains in the same order.
+template <bool kPair>
+struct PairSumSq {
+    float2 a[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    template <int P>
+    __device__ __forceinline__ void add(const float2 (&f)[P]) {
+#pragma unroll
+        for (int i = 0; i < P; ++i) a[i & 1] = pair_fma<kPair>(f[i], f[i], a[i & 1]);
+    }
+    __device__ __forceinline__ float total() const {
+        return __fadd_rn(__fadd_rn(a[0].x, a[0].y), __fadd_rn(a[1].x, a[1].y));
+    }
+};
+
+// One vector's values: fp32(x), or for the fused op s = fp32(x) + fp32(r) (one FP32 add each).
+template <typename T, bool kFused>
+__device__ __forceinline__ void row_values(const uint4 &x, const uint4 &r,
+                                           float2 (&s)[Elem<T>::kPerVec / 2]) {
+    Elem<T>::unpack2(x, s);
+    if (kFused) {
+        float2 q[Elem<T>::kPerVec / 2];
+        Elem<T>::unpack2(r, q);
+#pragma unroll
+        for (int i = 0; i < Elem<T>::kPerVec / 2; ++i) s[i] = pair_add<Elem<T>::kPairMath>(s[i], q[i]);
+    }
+}
+
+// One output vector: cast((s * scale) * w), the products in that order.
+template <typename T>
+__device__ __forceinline__ uint4 scaled_weighted(float2 (&s)[Elem<T>::kPerVec / 2], float scale,
+                                                 const uint4 &w) {
+    constexpr bool kPair = Elem<T>::kPairMath;
+    float2 wf[Elem<T>::kPerVec / 2];
+    Elem<T>::unpack2(w, wf);
+    const float2 s2 = make_float2(scale, scale);
+#pragma unroll
+    for (int i = 0; i < Elem<T>::kPerVec / 2; ++i) s[i] = pair_mul<kPair>(pair_mul<kPair>(s[i], s2), wf[i]);
+    return Elem<T>::pack2(s);
+}
+
 // --------------------------------------------------------------- vectorised row kernel
 
 // Register budget per thread grows with V (current + prefetched rows, weight slice); the
@@ -220,55 +309,23 @@ __device__ __forceinline__ void vec_row(const RowArgs &a, int64_t row, int t, in
                                         uint4 (&xc)[V], uint4 (&rc)[V], uint4 (&wv)[V],
                                         float *red) {
     using E = Elem<T>;
-    constexpr int N = E::kPerVec;
-    // packed pairs (Elem::kPairMath): element e feeds chain e % 4, lane e % 2 of pair (e / 2) % 2
-    constexpr bool kPairs = E::kPairMath;
+    constexpr int P = E::kPerVec / 2;
     const int64_t hv = a.hv;
     uint4 *og = static_cast<uint4 *>(a.out) + row * hv;
     uint4 *rg = kFused ? static_cast<uint4 *>(a.res) + row * hv : nullptr;
 
-    float ssum;
-    if constexpr (kPairs) {
-        float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    PairSumSq<E::kPairMath> acc;
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
-                float2 f[4];
-                E::unpack2(xc[k], f);
-                if (kFused) {
-                    float2 q[4];
-                    E::unpack2(rc[k], q);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) f[i] = __fadd2_rn(f[i], q[i]);
-                    __stcs(rg + c, E::pack2(f));
-                }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) acc2[i & 1] = __ffma2_rn(f[i], f[i], acc2[i & 1]);
-            }
+    for (int k = 0; k < V; ++k) {
+        const int64_t c = t + (int64_t)k * g;
+        if (c < hv) {
+            float2 f[P];
+            row_values<T, kFused>(xc[k], rc[k], f);
+            if (kFused) __stcs(rg + c, E::pack2(f));
+            acc.add(f);
         }
-        ssum = __fadd_rn(__fadd_rn(acc2[0].x, acc2[0].y), __fadd_rn(acc2[1].x, acc2[1].y));
-    } else {
-        SumSq acc;
-#pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
-                float f[N];
-                E::unpack(xc[k], f);
-                if (kFused) {
-                    float q[N];
-                    E::unpack(rc[k], q);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
-                    __stcs(rg + c, E::pack(f));
-                }
-                acc.add(f);
-            }
-        }
-        ssum = acc.total();
     }
-    const float ss = team_sum<kWarpTeam>(ssum, red);
+    const float ss = team_sum<kWarpTeam>(acc.total(), red);
     const float scale = row_scale(ss, (float)a.hidden, a.eps);
 
     if (kOpaque) {
@@ -283,34 +340,9 @@ __device__ __forceinline__ void vec_row(const RowArgs &a, int64_t row, int t, in
     for (int k = 0; k < V; ++k) {
         const int64_t c = t + (int64_t)k * g;
         if (c < hv) {
-            if constexpr (kPairs) {
-                float2 f[4], wf[4];
-                E::unpack2(xc[k], f);
-                if (kFused) {
-                    float2 q[4];
-                    E::unpack2(rc[k], q);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) f[i] = __fadd2_rn(f[i], q[i]);
-                }
-                E::unpack2(wv[k], wf);
-                const float2 s2 = make_float2(scale, scale);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) f[i] = __fmul2_rn(__fmul2_rn(f[i], s2), wf[i]);
-                __stcs(og + c, E::pack2(f));
-            } else {
-                float f[N], wf[N];
-                E::unpack(xc[k], f);
-                if (kFused) {
-                    float q[N];
-                    E::unpack(rc[k], q);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
-                }
-                E::unpack(wv[k], wf);
-#pragma unroll
-                for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
-                __stcs(og + c, E::pack(f));
-            }
+            float2 f[P];
+            row_values<T, kFused>(xc[k], rc[k], f);
+            __stcs(og + c, scaled_weighted<T>(f, scale, wv[k]));
         }
     }
 }
@@ -402,7 +434,7 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
 template <typename T, bool kFused, int U, int kMaxBlock>
 __global__ void __launch_bounds__(kMaxBlock) rows_twopass_kernel(const RowArgs a) {
     using E = Elem<T>;
-    constexpr int N = E::kPerVec;
+    constexpr int P = E::kPerVec / 2;
     __shared__ float red[2][32];
     const int g = blockDim.x, t = threadIdx.x;
     const int64_t hv = a.hv;
@@ -417,7 +449,7 @@ __global__ void __launch_bounds__(kMaxBlock) rows_twopass_kernel(const RowArgs a
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const uint4 *xr = xg + row * hv;
         uint4 *rr = kFused ? rg + row * hv : nullptr;
-        SumSq acc;
+        PairSumSq<E::kPairMath> acc;
         for (int64_t c0 = t; c0 < hv; c0 += chunk) {
             uint4 xv[U], rv[U];
 #pragma unroll
@@ -428,14 +460,8 @@ __global__ void __launch_bounds__(kMaxBlock) rows_twopass_kernel(const RowArgs a
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                float f[N];
-                E::unpack(xv[u], f);
-                if (kFused) {
-                    float q[N];
-                    E::unpack(rv[u], q);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
-                }
+                float2 f[P];
+                row_values<T, kFused>(xv[u], rv[u], f);
                 acc.add(f);
             }
         }
@@ -457,19 +483,10 @@ __global__ void __launch_bounds__(kMaxBlock) rows_twopass_kernel(const RowArgs a
             for (int u = 0; u < U; ++u) {
                 const int64_t c = c0 + (int64_t)u * g;
                 if (c < hv) {
-                    float f[N], wf[N];
-                    E::unpack(xv[u], f);
-                    if (kFused) {
-                        float q[N];
-                        E::unpack(rv[u], q);
-#pragma unroll
-                        for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q[e]);
-                        __stcs(rr + c, E::pack(f));
-                    }
-                    E::unpack(wv[u], wf);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
-                    __stcs(orow + c, E::pack(f));
+                    float2 f[P];
+                    row_values<T, kFused>(xv[u], rv[u], f);
+                    if (kFused) __stcs(rr + c, E::pack2(f));
+                    __stcs(orow + c, scaled_weighted<T>(f, scale, wv[u]));
                 }
             }
         }
@@ -557,7 +574,7 @@ template <typename T, int V, bool kFused, bool kCluster>
 __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
     namespace cg = cooperative_groups;
     using E = Elem<T>;
-    constexpr int N = E::kPerVec;
+    constexpr int P = E::kPerVec / 2;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[2][32];
     __shared__ float part[2];
@@ -639,20 +656,14 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
             if (kFused) rv[k] = in ? ld_shared_v4(sx + slot_bytes + c * 16) : make_uint4(0u, 0u, 0u, 0u);
         }
 
-        SumSq acc;
+        PairSumSq<E::kPairMath> acc;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
             if (ok && c < nv) {
-                float f[N];
-                E::unpack(xv[k], f);
-                if (kFused) {
-                    float q2[N];
-                    E::unpack(rv[k], q2);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q2[e]);
-                    __stcs(rg + row * hv + c, E::pack(f));
-                }
+                float2 f[P];
+                row_values<T, kFused>(xv[k], rv[k], f);
+                if (kFused) __stcs(rg + row * hv + c, E::pack2(f));
                 acc.add(f);
             }
         }
@@ -709,18 +720,9 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
             if (c < nv) {
-                float f[N], wf[N];
-                E::unpack(xv[k], f);
-                if (kFused) {
-                    float q2[N];
-                    E::unpack(rv[k], q2);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], q2[e]);
-                }
-                E::unpack(wv[k], wf);
-#pragma unroll
-                for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
-                __stcs(og + row * hv + c, E::pack(f));
+                float2 f[P];
+                row_values<T, kFused>(xv[k], rv[k], f);
+                __stcs(og + row * hv + c, scaled_weighted<T>(f, scale, wv[k]));
             }
         }
         if (++s == stages) {
@@ -760,7 +762,7 @@ template <typename T, int V, bool kFused>
 __global__ void __launch_bounds__(512) rows_cluster_kernel(const RowArgs a) {
     namespace cg = cooperative_groups;
     using E = Elem<T>;
-    constexpr int N = E::kPerVec;
+    constexpr int P = E::kPerVec / 2;
     __shared__ float red[2][32];
     __shared__ float part[2];
 
@@ -801,20 +803,14 @@ __global__ void __launch_bounds__(512) rows_cluster_kernel(const RowArgs a) {
             xv[k] = (c < hi) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
             if (kFused) rv[k] = (c < hi) ? __ldcs(rg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
         }
-        SumSq acc;
+        PairSumSq<E::kPairMath> acc;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = lo + t + (int64_t)k * g;
             if (c < hi) {
-                float f[N];
-                E::unpack(xv[k], f);
-                if (kFused) {
-                    float r[N];
-                    E::unpack(rv[k], r);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], r[e]);
-                    __stcs(rg + row * hv + c, E::pack(f));
-                }
+                float2 f[P];
+                row_values<T, kFused>(xv[k], rv[k], f);
+                if (kFused) __stcs(rg + row * hv + c, E::pack2(f));
                 acc.add(f);
             }
         }
@@ -836,18 +832,9 @@ __global__ void __launch_bounds__(512) rows_cluster_kernel(const RowArgs a) {
         for (int k = 0; k < V; ++k) {
             const int64_t c = lo + t + (int64_t)k * g;
             if (c < hi) {
-                float f[N], wf[N];
-                E::unpack(xv[k], f);
-                if (kFused) {
-                    float r[N];
-                    E::unpack(rv[k], r);
-#pragma unroll
-                    for (int e = 0; e < N; ++e) f[e] = __fadd_rn(f[e], r[e]);
-                }
-                E::unpack(wv[k], wf);
-#pragma unroll
-                for (int e = 0; e < N; ++e) f[e] = __fmul_rn(__fmul_rn(f[e], scale), wf[e]);
-                __stcs(og + row * hv + c, E::pack(f));
+                float2 f[P];
+                row_values<T, kFused>(xv[k], rv[k], f);
+                __stcs(og + row * hv + c, scaled_weighted<T>(f, scale, wv[k]));
             }
         }
     }

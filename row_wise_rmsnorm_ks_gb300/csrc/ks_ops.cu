@@ -292,52 +292,28 @@ constexpr int kAffineWeight = 1, kAffineBias = 2;
 // vectors are loaded before the current row's two reductions. (Measured on GB300 at [32768,
 // 8192] bf16: 74 % of the copy peak; weight and bias in shared memory, with or without the
 // prefetch, were slower at 58-64 %.)
-// LayerNorm element steps. Four running sums per thread: element e of a vector feeds sum e % 4,
-// held as lane e % 2 of FP32 pair (e / 2) % 2, and a row's partial sum is the pairwise total.
-// Element types with Elem::kPairMath run the steps on packed FP32 pairs (bit-identical to the
-// scalar steps, half the instructions; for bf16 LayerNorm rows of 768..4096 vectors that
-// measured 4-8 points of the copy peak faster on GB300).
+// LayerNorm element steps, on FP32 pairs (packed instructions where Elem::kPairMath). Four running
+// sums per thread: element e of a vector feeds sum e % 4, held as lane e % 2 of pair (e / 2) % 2,
+// and a row's partial sum is the pairwise total (ln_total).
 template <typename T>
 __device__ __forceinline__ void ln_add_sum(const uint4 &v, float2 (&s)[2]) {
-    if constexpr (Elem<T>::kPairMath) {
-        float2 f[4];
-        Elem<T>::unpack2(v, f);
+    float2 f[Elem<T>::kPerVec / 2];
+    Elem<T>::unpack2(v, f);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) s[i & 1] = __fadd2_rn(s[i & 1], f[i]);
-    } else {
-        constexpr int N = Elem<T>::kPerVec;
-        float f[N];
-        Elem<T>::unpack(v, f);
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-            float &acc = (e & 1) ? s[(e >> 1) & 1].y : s[(e >> 1) & 1].x;
-            acc = __fadd_rn(acc, f[e]);
-        }
-    }
+    for (int i = 0; i < Elem<T>::kPerVec / 2; ++i) s[i & 1] = pair_add<Elem<T>::kPairMath>(s[i & 1], f[i]);
 }
 
 // the squares of x - mean, summed as above (x - mean formed as x + (-mean), which is exact)
 template <typename T>
 __device__ __forceinline__ void ln_add_sq(const uint4 &v, float neg_mean, float2 (&q)[2]) {
-    if constexpr (Elem<T>::kPairMath) {
-        float2 f[4];
-        Elem<T>::unpack2(v, f);
-        const float2 m = make_float2(neg_mean, neg_mean);
+    constexpr bool kPair = Elem<T>::kPairMath;
+    float2 f[Elem<T>::kPerVec / 2];
+    Elem<T>::unpack2(v, f);
+    const float2 m = make_float2(neg_mean, neg_mean);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 d = __fadd2_rn(f[i], m);
-            q[i & 1] = __ffma2_rn(d, d, q[i & 1]);
-        }
-    } else {
-        constexpr int N = Elem<T>::kPerVec;
-        float f[N];
-        Elem<T>::unpack(v, f);
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-            const float d = __fadd_rn(f[e], neg_mean);
-            float &acc = (e & 1) ? q[(e >> 1) & 1].y : q[(e >> 1) & 1].x;
-            acc = __fmaf_rn(d, d, acc);
-        }
+    for (int i = 0; i < Elem<T>::kPerVec / 2; ++i) {
+        const float2 d = pair_add<kPair>(f[i], m);
+        q[i & 1] = pair_fma<kPair>(d, d, q[i & 1]);
     }
 }
 
@@ -351,37 +327,22 @@ template <typename T, int kAffine>
 __device__ __forceinline__ uint4 ln_out(const uint4 &v, const uint4 &wv, const uint4 &bv,
                                         float rstd, float shift) {
     constexpr bool kW = kAffine & kAffineWeight, kB = kAffine & kAffineBias;
-    if constexpr (Elem<T>::kPairMath) {
-        float2 f[4], wf[4], bf[4];
-        Elem<T>::unpack2(v, f);
-        if (kW) Elem<T>::unpack2(wv, wf);
-        if (kB) Elem<T>::unpack2(bv, bf);
-        const float2 r2 = make_float2(rstd, rstd), s2 = make_float2(shift, shift);
+    constexpr bool kPair = Elem<T>::kPairMath;
+    constexpr int P = Elem<T>::kPerVec / 2;
+    float2 f[P], wf[P], bf[P];
+    Elem<T>::unpack2(v, f);
+    if (kW) Elem<T>::unpack2(wv, wf);
+    if (kB) Elem<T>::unpack2(bv, bf);
+    const float2 r2 = make_float2(rstd, rstd), s2 = make_float2(shift, shift);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float2 o = __ffma2_rn(f[i], r2, s2);
-            if (kW && kB) o = __ffma2_rn(o, wf[i], bf[i]);
-            else if (kW) o = __fmul2_rn(o, wf[i]);
-            else if (kB) o = __fadd2_rn(o, bf[i]);
-            f[i] = o;
-        }
-        return Elem<T>::pack2(f);
-    } else {
-        constexpr int N = Elem<T>::kPerVec;
-        float f[N], wf[N], bf[N];
-        Elem<T>::unpack(v, f);
-        if (kW) Elem<T>::unpack(wv, wf);
-        if (kB) Elem<T>::unpack(bv, bf);
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-            float o = __fmaf_rn(f[e], rstd, shift);
-            if (kW && kB) o = __fmaf_rn(o, wf[e], bf[e]);
-            else if (kW) o = __fmul_rn(o, wf[e]);
-            else if (kB) o = __fadd_rn(o, bf[e]);
-            f[e] = o;
-        }
-        return Elem<T>::pack(f);
+    for (int i = 0; i < P; ++i) {
+        float2 o = pair_fma<kPair>(f[i], r2, s2);
+        if (kW && kB) o = pair_fma<kPair>(o, wf[i], bf[i]);
+        else if (kW) o = pair_mul<kPair>(o, wf[i]);
+        else if (kB) o = pair_add<kPair>(o, bf[i]);
+        f[i] = o;
     }
+    return Elem<T>::pack2(f);
 }
 
 template <typename T, int V, int kAffine>
