@@ -86,6 +86,18 @@ __device__ __forceinline__ float rcp_sfu(float v) {
     return r;
 }
 
+// Softmax numerators for a pair of elements: fp32 outputs e^(v - m) by expf; 16-bit outputs
+// 2^(v log2(e) + bias) with bias = 64 - m log2(e) (e^(v - m) * 2^64; see softmax_vec_kernel).
+template <typename T, bool kPair>
+__device__ __forceinline__ float2 softmax_exp_pair(float2 v, float m, float bias) {
+    if constexpr (sizeof(T) == 4) {
+        return make_float2(expf(__fsub_rn(v.x, m)), expf(__fsub_rn(v.y, m)));
+    } else {
+        const float2 z = pair_fma<kPair>(v, make_float2(kLog2e, kLog2e), make_float2(bias, bias));
+        return make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
+    }
+}
+
 // (g * sigmoid(g)) * up with sigmoid(g) = 1 / (1 + e^-g).
 //  fp32 outputs: e^-g by expf, the correctly rounded reciprocal (bitwise the IEEE quotient).
 //  16-bit outputs: g * up / (1 + e^-g) on the SFU, everything scaled by 2^-64 so that neither
@@ -177,7 +189,11 @@ template <typename T, int V, bool kPrefetch>
 __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void *x, int64_t rows,
                                                           int64_t hv) {
     using E = Elem<T>;
-    constexpr int N = E::kPerVec;
+    constexpr int P = E::kPerVec / 2;
+    // packed pair instructions (bit-identical) where they measured faster on GB300: bf16 without
+    // prefetch, 0.3-0.6 point of the copy peak; with prefetch they took the register count from
+    // 64 to 74 and lost 7 points at 2048 vectors
+    constexpr bool kPair = E::kPairMath && !kPrefetch;
     __shared__ float red[2][32];
     grid_dependency_wait();
     allow_dependents_launch();
@@ -204,15 +220,15 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
             else
                 cur[k] = (c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float f[V][N];
+        float2 f[V][P];
         float m = -INFINITY;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            E::unpack(cur[k], f[k]);
+            E::unpack2(cur[k], f[k]);
             if (c < hv) {
 #pragma unroll
-                for (int e = 0; e < N; ++e) m = fmaxf(m, f[k][e]);
+                for (int i = 0; i < P; ++i) m = fmaxf(fmaxf(m, f[k][i].x), f[k][i].y);
             }
         }
         m = cta_max(m, red, slot);
@@ -221,30 +237,31 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
         // (smaller ones are below any fp32 output anyway). For m = +-inf or NaN the bias is
         // -inf/+inf/NaN, which gives NaN rows exactly as the formula does.
         const float bias = __fmaf_rn(-m, kLog2e, 64.0f);
-        float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // four running sums: element e feeds lane e % 2 of s[(e / 2) % 2]
+        float2 s[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
             if (c < hv) {
 #pragma unroll
-                for (int e = 0; e < N; ++e) {
-                    f[k][e] = sizeof(T) == 4 ? expf(__fsub_rn(f[k][e], m))
-                                             : ex2_sfu(__fmaf_rn(f[k][e], kLog2e, bias));
-                    s[e & 3] = __fadd_rn(s[e & 3], f[k][e]);
+                for (int i = 0; i < P; ++i) {
+                    f[k][i] = softmax_exp_pair<T, kPair>(f[k][i], m, bias);
+                    s[i & 1] = pair_add<kPair>(s[i & 1], f[k][i]);
                 }
             }
         }
-        const float sum = cta_sum(__fadd_rn(__fadd_rn(s[0], s[1]), __fadd_rn(s[2], s[3])), red, slot);
+        const float sum = cta_sum(__fadd_rn(__fadd_rn(s[0].x, s[0].y), __fadd_rn(s[1].x, s[1].y)), red, slot);
         // e / sum as e * (1 / sum): one correctly rounded reciprocal per row, then a product
         // per element (within 1 fp32 ulp of the quotient)
         const float inv = __frcp_rn(sum);
+        const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
             if (c < hv) {
 #pragma unroll
-                for (int e = 0; e < N; ++e) f[k][e] = __fmul_rn(f[k][e], inv);
-                __stcs(og + row * hv + c, E::pack(f[k]));
+                for (int i = 0; i < P; ++i) f[k][i] = pair_mul<kPair>(f[k][i], inv2);
+                __stcs(og + row * hv + c, E::pack2(f[k]));
             }
         }
         if (kPrefetch) {
@@ -567,7 +584,8 @@ template <typename T, int U>
 __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const void *x,
                                                             int64_t rows, int64_t hv) {
     using E = Elem<T>;
-    constexpr int N = E::kPerVec;
+    constexpr int P = E::kPerVec / 2;
+    constexpr bool kPair = E::kPairMath;
     __shared__ float red[2][32];
     grid_dependency_wait();
     allow_dependents_launch();
@@ -589,16 +607,16 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (c0 + (int64_t)u * g < hv) {
-                    float f[N];
-                    E::unpack(v[u], f);
+                    float2 f[P];
+                    E::unpack2(v[u], f);
 #pragma unroll
-                    for (int e = 0; e < N; ++e) m = fmaxf(m, f[e]);
+                    for (int i = 0; i < P; ++i) m = fmaxf(fmaxf(m, f[i].x), f[i].y);
                 }
             }
         }
         m = cta_max(m, red, slot);
         const float bias = __fmaf_rn(-m, kLog2e, 64.0f);  // see softmax_vec_kernel
-        float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
         for (int64_t c0 = t; c0 < hv; c0 += chunk) {
             uint4 v[U];
 #pragma unroll
@@ -609,17 +627,17 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 if (c0 + (int64_t)u * g < hv) {
-                    float f[N];
-                    E::unpack(v[u], f);
+                    float2 f[P];
+                    E::unpack2(v[u], f);
 #pragma unroll
-                    for (int e = 0; e < N; ++e)
-                        s4[e & 3] = __fadd_rn(s4[e & 3], sizeof(T) == 4 ? expf(__fsub_rn(f[e], m))
-                                                         : ex2_sfu(__fmaf_rn(f[e], kLog2e, bias)));
+                    for (int i = 0; i < P; ++i)
+                        s2[i & 1] = pair_add<kPair>(s2[i & 1], softmax_exp_pair<T, kPair>(f[i], m, bias));
                 }
             }
         }
         const float inv = __frcp_rn(
-            cta_sum(__fadd_rn(__fadd_rn(s4[0], s4[1]), __fadd_rn(s4[2], s4[3])), red, slot));
+            cta_sum(__fadd_rn(__fadd_rn(s2[0].x, s2[0].y), __fadd_rn(s2[1].x, s2[1].y)), red, slot));
+        const float2 inv2 = make_float2(inv, inv);
         uint4 *orow = og + row * hv;
         for (int64_t c0 = t; c0 < hv; c0 += chunk) {
             uint4 v[U];
@@ -632,14 +650,11 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
             for (int u = 0; u < U; ++u) {
                 const int64_t c = c0 + (int64_t)u * g;
                 if (c < hv) {
-                    float f[N];
-                    E::unpack(v[u], f);
+                    float2 f[P];
+                    E::unpack2(v[u], f);
 #pragma unroll
-                    for (int e = 0; e < N; ++e)
-                        f[e] = __fmul_rn(sizeof(T) == 4 ? expf(__fsub_rn(f[e], m))
-                                                        : ex2_sfu(__fmaf_rn(f[e], kLog2e, bias)),
-                                         inv);
-                    __stcs(orow + c, E::pack(f));
+                    for (int i = 0; i < P; ++i) f[i] = pair_mul<kPair>(softmax_exp_pair<T, kPair>(f[i], m, bias), inv2);
+                    __stcs(orow + c, E::pack2(f));
                 }
             }
         }
