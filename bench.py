@@ -992,6 +992,106 @@ def run_plan_sweep(args) -> int:
     return 0
 
 
+def run_plan_contexts(args) -> int:
+    """The register-kernel candidates (warp and CTA rows, 2 or 4 vectors, with and without
+    prefetch; plus the two-pass kernel and the staged ring where they apply) against the default
+    plan, per dtype, op and width, in two contexts (one JSON line each; not the contract's line):
+    steady (the same plan launched back to back, after 5 untimed launches) and right after one
+    launch of the staged ring, a kernel with a large shared-memory carveout, as after a GEMM in a
+    model (each launch timed alone). 384 MiB per tensor, N(0,1) inputs; the plans alternate over
+    --plan-sweep-rounds rounds and the median is kept, as a fraction of the measured copy peak.
+    The plan-sweep mode instead interleaves every candidate, so each block of launches follows a
+    different kernel."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    peak = measured_peaks()["hbm_gbs"]
+    codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
+    keep = ("w4", "w4n", "p2", "n2", "p4", "n4", "t256u4", "t512u2", "b2")
+
+    def steady(fn, n=30):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(5):
+            fn()
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n * 1e-3
+
+    def after(fn, pre, n=12):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(n):
+            pre()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b) * 1e-3
+        return tot / n
+
+    widths = [int(v) for v in (args.plan_sweep_widths or "128,256,512,640,768,1024,1280,1536,2048").split(",")]
+    for dt in args.plan_sweep_dtypes.split(","):
+        elem = 4 if dt == "fp32" else 2
+        code = codes[dt]
+        for hv in widths:
+            H = hv * 16 // elem
+            R = (384 << 20) // (H * elem)
+            x = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), dt)
+            r = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev), dt)
+            w = synth.weight(H, dt).to(dev)
+            y = torch.empty_like(x)
+            ring = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, -(-(-(-hv // 4)) // 32) * 32, 2)
+            pre = (lambda: _abi.check(_abi.ks_rms_norm_planned(
+                y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H, 1e-5, code, ring, s)))
+            if 128 + 2 * hv * 16 > 226 * 1024:
+                pre = None  # no ring of two stages fits: steady context only
+            for op in ("rms_norm", "fused_add_rms_norm"):
+                fused = op == "fused_add_rms_norm"
+                nb = algorithmic_bytes(op, R, H, elem)
+
+                def mk(p):
+                    if fused:
+                        return lambda: _abi.check(_abi.ks_fused_add_rms_norm_planned(
+                            x.data_ptr(), r.data_ptr(), w.data_ptr(), R, H, 1e-5, code, p, s))
+                    return lambda: _abi.check(_abi.ks_rms_norm_planned(
+                        y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H, 1e-5, code, p, s))
+                def default():
+                    if fused:
+                        _abi.check(_abi.ks_fused_add_rms_norm(x.data_ptr(), r.data_ptr(),
+                                                              w.data_ptr(), R, H, 1e-5, code, s))
+                    else:
+                        _abi.check(_abi.ks_rms_norm(y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H,
+                                                    1e-5, code, s))
+                _, dp = _abi.ks_plan_launch(int(fused), R, H, code, True, 152, 0)
+                fns = [("default", default)] + [(n, mk(p)) for n, p in plan_candidates(op, hv, elem)
+                                                if n in keep]
+                line = {"plan_contexts": dt, "op": op, "hv": hv, "hidden": H, "rows": R,
+                        "default_plan": {k: dp.as_dict()[k] for k in ("kernel_name", "vec_per_thread",
+                                                                       "block", "flags")}}
+                for ctx in ("steady", "after_ring") if pre else ("steady",):
+                    res = {name: [] for name, _ in fns}
+                    for _ in range(args.plan_sweep_rounds):
+                        for name, fn in fns:
+                            t = steady(fn) if ctx == "steady" else after(fn, pre)
+                            res[name].append(nb / t / 1e9 / peak)
+                    line[ctx] = {k: round(statistics.median(v), 4) for k, v in res.items()}
+                print(json.dumps(line), flush=True)
+            del x, r, w, y
+            torch.cuda.empty_cache()
+    st, flags = _abi.ks_device_faults(clear=False)
+    if st != _abi.KS_SUCCESS or flags:
+        print(json.dumps({"plan_contexts": "device faults", "status": st, "flags": flags}))
+        return 1
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1011,6 +1111,9 @@ def main() -> int:
     ap.add_argument("--sweep-samples", type=int, default=15)
     ap.add_argument("--plan-sweep", action="store_true",
                     help="time every candidate launch plan per dtype, op and width, and exit")
+    ap.add_argument("--plan-contexts", action="store_true",
+                    help="compare the register-kernel plans per width in steady state and right "
+                         "after a large-shared-memory kernel, and exit")
     ap.add_argument("--plan-sweep-rounds", type=int, default=3)
     ap.add_argument("--plan-sweep-dtypes", default="bf16,fp16,fp32")
     ap.add_argument("--plan-sweep-widths", default="",
@@ -1029,6 +1132,8 @@ def main() -> int:
         return run_sweep(args)
     if args.plan_sweep:
         return run_plan_sweep(args)
+    if args.plan_contexts:
+        return run_plan_contexts(args)
     return run_ks(args)
 
 

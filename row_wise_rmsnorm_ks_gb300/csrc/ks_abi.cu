@@ -357,6 +357,17 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 // least one per SM).
 namespace {
 
+// bf16 plain rows of many CTAs (4 vectors per thread) that load their next row while reducing
+// the current one: within 32 vectors of 256, 512 and 640, and 1185..1312 vectors. There the
+// no-prefetch kernel measured 0.89-0.93 of the copy peak and the prefetching one 0.95-0.98 on
+// GB300, at every tensor size and placement tried (256-512 MiB), and by more right after a kernel
+// with a large shared-memory carveout; at the other widths the no-prefetch kernel was as fast or
+// faster (prefetch lost up to 14 points, e.g. at 832 vectors).
+bool bf16_plain_prefetch(int64_t hv) {
+    return (hv > 224 && hv <= 288) || (hv > 480 && hv <= 544) || (hv > 608 && hv <= 672) ||
+           (hv > 1184 && hv <= 1312);
+}
+
 void cta_row(ks_plan_t *p, int64_t hv, int v, bool prefetch) {
     p->kernel = KS_KERNEL_CTA_ROW;
     p->vec_per_thread = v;
@@ -415,8 +426,13 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
     const bool vec_ok = aligned16 && hidden % per_vec == 0;
     const int64_t hv = vec_ok ? hidden / per_vec : 0;
     const bool ring_rows = rows >= 4 * (int64_t)sm_count;  // enough rows to keep a ring busy
+    const bool bf16 = dtype == KS_DTYPE_BF16, f16 = dtype == KS_DTYPE_F16;
+    // Many rows of 97..128 vectors: a CTA per row with prefetch beat a warp per row for bf16 plain
+    // (2 vectors per thread: 0.96 of the copy peak against 0.92) and fp16 fused (4 vectors: 0.97-0.99
+    // against 0.95-0.98), whatever kernel ran before.
+    const bool cta_narrow = rows > sm_count && hv > 96 && ((bf16 && !fused) || (f16 && fused));
     int64_t rows_per_cta = 1;
-    if (vec_ok && hv <= 128) {
+    if (vec_ok && hv <= 128 && !cta_narrow) {
         p->kernel = KS_KERNEL_WARP_ROW;
         p->vec_per_thread = hv <= 32 ? 1 : (hv <= 64 ? 2 : 4);
         p->team = 32;
@@ -438,18 +454,35 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
             cta_row(p, hv, 4, fused);
         }
     } else if (vec_ok && hv <= 2048) {
+        // Many rows. Besides the general rules, 16-bit exceptions measured on GB300 with every
+        // candidate plan timed in steady state and right after a kernel with a large shared-memory
+        // carveout (each gains 1-4 points of the copy peak there): bf16 plain prefetches at the
+        // widths of bf16_plain_prefetch; bf16 fused prefetches at 4 vectors at 161..224 vectors
+        // and from 1473 (the general rule prefetches from 1537); fp16 fused takes 4 vectors
+        // without prefetch at 161..224 and 2 with prefetch at 225..288; 16-bit fused rows of
+        // 609..672 vectors take 4 vectors without prefetch.
         const bool f32 = dtype == KS_DTYPE_F32;
-        if (f32 && hv <= 384) {
+        if (hv <= 128) {  // cta_narrow
+            cta_row(p, hv, fused ? 4 : 2, true);
+        } else if (f32 && hv <= 384) {
             cta_row(p, hv, 2, true);
         } else if (!fused) {
             if (hv > 1536 && !f32)
                 twopass_row(p, hv, false, dtype);
             else
-                cta_row(p, hv, 4, false);
-        } else if (hv <= 1536) {
+                cta_row(p, hv, 4, bf16 && bf16_plain_prefetch(hv));
+        } else if (bf16 && hv > 160 && hv <= 224) {
+            cta_row(p, hv, 4, true);
+        } else if (f16 && hv > 160 && hv <= 224) {
+            cta_row(p, hv, 4, false);
+        } else if (f16 && hv > 224 && hv <= 288) {
+            cta_row(p, hv, 2, true);
+        } else if (!f32 && hv > 608 && hv <= 672) {
+            cta_row(p, hv, 4, false);
+        } else if (hv <= 1472 || (!bf16 && hv <= 1536)) {
             const bool two = hv <= 768 || (hv > 960 && hv <= 1152);
             cta_row(p, hv, two ? 2 : 4, false);
-        } else if (dtype == KS_DTYPE_BF16) {
+        } else if (bf16) {
             cta_row(p, hv, 4, true);
         } else if (!f32 && hv <= 1728 && ring_rows) {
             bulk_row(p, hv, true, 2);

@@ -118,11 +118,61 @@ def plan(op, rows, hidden, dtype=BF16, aligned=True, sms=152, bps=0):
     return p
 
 
-@pytest.mark.parametrize("hidden,v", [(256, 1), (512, 2), (1024, 4)])
-def test_narrow_rows_take_warp_per_row(hidden, v):
-    p = plan(0, 32768, hidden)
+@pytest.mark.parametrize("op,hidden,dtype,v", [(0, 256, BF16, 1), (0, 512, BF16, 2), (0, 1024, F16, 4),
+                                               (1, 1024, BF16, 4), (0, 512, F32, 4)])
+def test_narrow_rows_take_warp_per_row(op, hidden, dtype, v):
+    p = plan(op, 32768, hidden, dtype)
     assert p.kernel == _abi.KS_KERNEL_WARP_ROW and p.vec_per_thread == v and p.team == 32
     assert p.block == 256  # 8 rows per CTA once there are enough rows
+
+
+# The measured exceptions for 16-bit rows with many rows (op, hidden, dtype) -> (vectors per thread,
+# prefetch), and the neighbouring widths that keep the general rule.
+NO_PF = _abi.KS_PLAN_NO_PREFETCH
+EXCEPTIONS = [
+    ((0, 1024, BF16), (2, True)),     # 128 vectors: CTA at 2 vectors, not a warp
+    ((1, 1024, F16), (4, True)),
+    ((0, 2048, BF16), (4, True)),     # 256 vectors
+    ((0, 3072, BF16), (4, False)),    # 384: general rule
+    ((0, 4096, BF16), (4, True)),     # 512
+    ((0, 5120, BF16), (4, True)),     # 640
+    ((0, 6144, BF16), (4, False)),    # 768: general rule
+    ((0, 8192, BF16), (4, False)),    # 1024: general rule (the headline shape)
+    ((0, 10240, BF16), (4, True)),    # 1280
+    ((0, 4096, F16), (4, False)),     # fp16 plain keeps the general rule
+    ((1, 1536, BF16), (4, True)),     # 192
+    ((1, 1536, F16), (4, False)),
+    ((1, 2048, F16), (2, True)),      # 256
+    ((1, 2048, BF16), (2, False)),    # general rule
+    ((1, 12288, BF16), (4, True)),    # 1536
+    ((1, 8192, BF16), (2, False)),    # general rule (the headline shape)
+    ((1, 5120, BF16), (4, False)),    # 640 vectors, fused: 4 without prefetch
+    ((1, 5120, F16), (4, False)),
+    ((1, 4096, F16), (2, False)),     # 512: general rule
+]
+
+
+@pytest.mark.parametrize("args,want", EXCEPTIONS)
+def test_measured_16bit_plan_exceptions(args, want):
+    op, hidden, dtype = args
+    p = plan(op, 32768, hidden, dtype)
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW
+    assert (p.vec_per_thread, not (p.flags & NO_PF)) == want
+
+
+def test_bf16_fused_prefetch_starts_at_1473_vectors():
+    p = plan(1, 32768, 11776, BF16)  # 1472 vectors: the general rule (4 vectors, no prefetch)
+    assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags & NO_PF
+    for hidden in (11784, 12288, 16384):  # 1473, 1536, 2048 vectors: prefetch at 4 vectors
+        p = plan(1, 32768, hidden, BF16)
+        assert p.kernel == CTA and p.vec_per_thread == 4 and not (p.flags & NO_PF)
+
+
+def test_few_rows_keep_the_latency_rules():
+    # rows <= SMs: the exceptions above apply only to many rows
+    assert plan(0, 100, 1024, BF16).kernel == _abi.KS_KERNEL_WARP_ROW
+    p = plan(0, 100, 4096, BF16)
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.vec_per_thread == 2
 
 
 def test_warp_per_row_spreads_few_rows_over_sms():
@@ -134,13 +184,13 @@ def test_warp_per_row_spreads_few_rows_over_sms():
 # prefetch) for the fused op, then for the plain op.
 CTA, BULK, TWO = _abi.KS_KERNEL_CTA_ROW, _abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_TWOPASS_ROW
 WIDE_BF16 = [
-    (1536, (CTA, 2, False), (CTA, 4, False)),
-    (4096, (CTA, 2, False), (CTA, 4, False)),
-    (5120, (CTA, 2, False), (CTA, 4, False)),
+    (1536, (CTA, 4, True), (CTA, 4, False)),
+    (4096, (CTA, 2, False), (CTA, 4, True)),
+    (5120, (CTA, 4, False), (CTA, 4, True)),
     (7168, (CTA, 4, False), (CTA, 4, False)),
     (8192, (CTA, 2, False), (CTA, 4, False)),
     (9216, (CTA, 2, False), (CTA, 4, False)),
-    (12288, (CTA, 4, False), (CTA, 4, False)),
+    (12288, (CTA, 4, True), (CTA, 4, False)),
     (13312, (CTA, 4, True), (TWO, 4, 256)),
     (14336, (CTA, 4, True), (TWO, 4, 256)),
     (16384, (CTA, 4, True), (TWO, 4, 256)),
@@ -162,7 +212,7 @@ def test_wide_rows_take_cta_per_row(hidden, fused_plan, plain_plan):
             assert p.flags == (0 if third else _abi.KS_PLAN_NO_PREFETCH)
     # few rows: never a staged ring
     assert plan(0, 100, hidden).kernel in (CTA, TWO)
-    assert plan(1, 300, hidden).kernel == CTA
+    assert plan(1, 300, hidden).kernel in (CTA, TWO)
 
 
 def test_fp16_and_fp32_wide_rows():
@@ -210,7 +260,7 @@ def test_persistent_grid_is_capped_by_residency():
     assert p.grid == 304 and p.rows_per_pass == 304
     p = plan(0, 100, 8192, bps=2)
     assert p.grid == 100
-    p = plan(0, 32768, 1024, bps=3)
+    p = plan(0, 32768, 1024, F16, bps=3)  # warp per row: 8 rows per CTA
     assert p.grid == 152 * 3 and p.rows_per_pass == 152 * 3 * 8
 
 
