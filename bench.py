@@ -261,32 +261,33 @@ def run_ks(args) -> int:
         ks_fused()
     torch.cuda.synchronize()
 
-    # ---- timed region: exactly K steps, barrier + synchronize on both sides
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- timed region: exactly K steps, barrier + synchronize on both sides. One event per
+    # kernel boundary: ev[2k] before step k's rms_norm, ev[2k+1] between its two kernels,
+    # ev[2k+2] after its fused kernel (and before step k+1's rms_norm); ev[0] and ev[2K] bound
+    # the region. Each event record costs the stream about a microsecond on this part, so no
+    # boundary carries two.
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.mark_begin()
-    t_start.record(stream)
+    ev[0].record(stream)
     for k in range(args.steps):
-        ev[k][0].record(stream)
         ks_plain()
-        ev[k][1].record(stream)
+        ev[2 * k + 1].record(stream)
         ks_fused()
-        ev[k][2].record(stream)
-    t_end.record(stream)
+        ev[2 * k + 2].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     sampler.mark_end()
     clocks = sampler.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), dev)
+    elapsed_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
 
-    plain_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(args.steps)]
-    fused_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
+    plain_ms = [ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(args.steps)]
+    fused_ms = [ev[2 * k + 1].elapsed_time(ev[2 * k + 2]) for k in range(args.steps)]
     b_plain = algorithmic_bytes("rms_norm", R, H, e)
     b_fused = algorithmic_bytes("fused_add_rms_norm", R, H, e)
     step_bytes = b_plain + b_fused
@@ -309,6 +310,8 @@ def run_ks(args) -> int:
 
     result = {}
     if rank == 0:
+        ops["step_chain"] = step_chain(ks_plain, ks_fused, stream, step_bytes,
+                                       measured_peaks()["hbm_gbs"])
         # decode shape (launch-bound): p50 of single cache-cold launches, and graph replay
         if not args.no_decode:
             ops["decode_fused_add_rms_norm_4x1536"] = decode_latency(dev, args)
@@ -350,6 +353,40 @@ def run_ks(args) -> int:
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def step_chain(ks_plain, ks_fused, stream, step_bytes: int, peak_gbs: float,
+               steps: int = 200) -> dict:
+    """The bench step with no event between its kernels, as a model runs it: `steps` steps timed
+    by one pair of events, with the library's default launches and with programmatic dependent
+    launch (KS_LAUNCH_PDL: each kernel is scheduled while the previous one drains and waits for
+    its writes before its first memory access). Reported beside the timed region, whose events
+    at every kernel boundary keep each launch apart; this shows what those boundaries cost."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi
+
+    out = {"steps": steps}
+    for key, opt in (("no_events", 0), ("no_events_pdl", _abi.KS_LAUNCH_PDL)):
+        _abi.check(_abi.ks_set_launch_options(opt))
+        try:
+            for _ in range(3):
+                _abi.check(ks_plain())
+                _abi.check(ks_fused())
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(steps):
+                ks_plain()
+                ks_fused()
+            b.record(stream)
+            torch.cuda.synchronize()
+        finally:
+            _abi.ks_set_launch_options(0)
+        us = a.elapsed_time(b) * 1e3 / steps
+        out[f"us_per_step_{key}"] = us
+        out[f"frac_of_peak_{key}"] = step_bytes / us / 1e3 / peak_gbs
+    return out
 
 
 def decode_latency(dev, args) -> dict:
@@ -874,7 +911,8 @@ def run_sweep(args) -> int:
 
 def plan_candidates(op: str, hv: int, elem: int):
     """Every launch plan the heuristic chooses among for a row of hv 16-byte vectors, named as in
-    the plan-sweep tables: w4/w4n (warp per row, 4 vectors per lane, with/without prefetch),
+    the plan-sweep tables: w4/w4n (warp per row, 4 vectors per lane, with/without prefetch;
+    w6/w6n and w8/w8n: 6 or 8 vectors per lane for rows of 129..192 and 193..256 vectors),
     p2/n2/p4/n4 (CTA per row, 2 or 4 vectors per thread, with/without prefetch), b2 (staged ring,
     2 stages), tBuU (the two-pass kernel, B threads, U vectors per thread per step; rows of at
     least 512 vectors), and for rows wider than 2048 vectors cC (register-resident cluster of C
@@ -888,6 +926,11 @@ def plan_candidates(op: str, hv: int, elem: int):
         out += [("w4", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, 4, 256)),
                 ("w4n", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, 4, 256,
                                        flags=_abi.KS_PLAN_NO_PREFETCH))]
+    for v in (6, 8):  # a warp covers rows of up to 32 * v vectors; 4 rows per 128-thread CTA
+        if 32 * (v - 2) < hv <= 32 * v:
+            out += [(f"w{v}", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, v, 128)),
+                    (f"w{v}n", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, v, 128,
+                                              flags=_abi.KS_PLAN_NO_PREFETCH))]
     for v in (2, 4):
         b = up32(-(-hv // v))
         if b <= (1024 if v == 2 else 512):
@@ -1011,7 +1054,8 @@ def run_plan_contexts(args) -> int:
     s = torch.cuda.current_stream(dev).cuda_stream
     peak = measured_peaks()["hbm_gbs"]
     codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
-    keep = ("w4", "w4n", "p2", "n2", "p4", "n4", "t256u4", "t512u2", "b2")
+    keep = ("w4", "w4n", "w6", "w6n", "w8", "w8n", "p2", "n2", "p4", "n4", "t256u4", "t512u2",
+            "b2")
 
     def steady(fn, n=30):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -117,7 +117,9 @@ const char *ks_last_error(void);
  */
 typedef struct ks_plan {
     int32_t kernel;         /* KS_KERNEL_* below */
-    int32_t vec_per_thread; /* 16-byte vectors per thread and tensor (vector kernels) */
+    int32_t vec_per_thread; /* 16-byte vectors per thread and tensor (vector kernels): warp
+                               rows 1, 2, 4, 6 or 8; CTA rows 2 or 4; staged rows 4; cluster
+                               rows 1, 2 or 4; two-pass 2 or 4 per step */
     int32_t team;           /* threads per row: 32 (warp per row) or block (CTA per row) */
     int32_t block;          /* threads per CTA */
     int64_t grid;           /* CTAs launched */

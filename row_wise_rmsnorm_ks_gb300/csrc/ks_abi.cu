@@ -115,8 +115,9 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
     switch (p.kernel) {
     case KS_KERNEL_WARP_ROW:
         if (!vec_ok) return fail(KS_ERR_INVALID_ARGUMENT, "vector kernel needs 16-byte rows and pointers");
-        if (p.vec_per_thread != 1 && p.vec_per_thread != 2 && p.vec_per_thread != 4)
-            return fail(KS_ERR_INVALID_ARGUMENT, "warp-row kernel takes 1, 2 or 4 vectors");
+        if (p.vec_per_thread != 1 && p.vec_per_thread != 2 && p.vec_per_thread != 4 &&
+            p.vec_per_thread != 6 && p.vec_per_thread != 8)
+            return fail(KS_ERR_INVALID_ARGUMENT, "warp-row kernel takes 1, 2, 4, 6 or 8 vectors");
         if (32LL * p.vec_per_thread < hv || p.block > 256)
             return fail(KS_ERR_INVALID_ARGUMENT, "warp-row plan does not cover the row or block > 256");
         p.team = 32;
@@ -327,25 +328,33 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 
 
 // Host heuristic (after the pages' rule of sizing the launch from the row width: Triton
-// Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"), set from a sweep of
-// every variant on GB300 over row widths of 128..2048 16-byte vectors in steps of 64, for each
-// dtype and op, at HBM-bound row counts (3 interleaved rounds, the median of each):
+// Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"), set from sweeps of
+// every variant on GB300 at HBM-bound row counts (384 MiB per tensor), each plan timed in steady
+// state and right after a kernel with a large shared-memory carveout, the worse of the two kept:
+// rows of 129..384 16-byte vectors in steps of 8 (two runs averaged), 416..2048 in steps of 32.
 //  * rows of at most 128 vectors (bf16/fp16 H <= 1024, fp32 H <= 512): one warp per row, 1/2/4
 //    vectors per lane, next row prefetched, up to 8 rows per CTA but never fewer CTAs than SMs
 //    when the rows allow it;
+//  * many rows of 129..384 vectors: the plan of kNarrowPlans for the row's 8-vector bucket
+//    (a warp per row at 6 or 8 vectors per lane for most plain rows up to 256 vectors, where a
+//    CTA row of 33..64 threads pays a barrier per row for 4 vectors a thread; CTA rows otherwise);
 //  * rows of up to 2048 vectors (bf16/fp16 H <= 16384, fp32 H <= 8192): one CTA per row, as wide
 //    as the row needs (a multiple of 32 threads). Which variant sustains the most bandwidth
 //    depends on the width, and the sweep picks:
-//      plain: 4 vectors per thread, no prefetch (fp32 rows of at most 384 vectors: 2 vectors,
-//        next row prefetched); 16-bit rows wider than 1536 vectors take the two-pass kernel;
+//      plain: 4 vectors per thread, no prefetch, except at the widths where that plan dips and
+//        the prefetching one does not (bf16 512, 640 and 1184..1280 vectors: 4 vectors with
+//        prefetch; fp32 512 and 640: 2 vectors with prefetch); 16-bit rows wider than 1536
+//        vectors and fp32 rows of 1537..1696 take the two-pass kernel;
 //      fused: no prefetch, 2 vectors per thread for rows of at most 768 vectors and for 961..1152
-//        vectors, 4 vectors per thread for 769..960 and 1153..1536 (fp32 rows of at most 384
-//        vectors: 2 vectors, next row prefetched). Wider rows: bf16 prefetches at 4 vectors per
-//        thread; fp16 takes the staged ring (2 stages) up to 1728 vectors when there are enough
-//        rows, the two-pass kernel beyond; fp32 takes the two-pass kernel.
+//        vectors, 4 vectors per thread for 769..960 and 1153..1536, and for 16-bit rows of
+//        545..672. Wider rows: bf16 prefetches at 4 vectors per thread (from 1473) and takes the
+//        two-pass kernel from 1985; fp16 takes the staged ring (2 stages) up to 1696 vectors when
+//        there are enough rows, the two-pass kernel beyond; fp32 takes the two-pass kernel at
+//        769..928 and from 1409, and 2 vectors per thread at 929..960.
 //    In the latency regime (rows <= SMs, so each CTA gets at most one row) prefetch has nothing
 //    to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8
-//    CTAs per row, plain rows of at most 1024 vectors take 2 vectors per thread, and the rest 4;
+//    CTAs per row, plain rows of at most 1024 vectors take 2 vectors per thread, and the rest 4
+//    (a graph-replay sweep of 1..333 rows found no gain in warp rows there);
 //  * rows wider than 2048 vectors (bf16/fp16 H > 16384, fp32 H > 8192): the two-pass kernel,
 //    one CTA per row reading it twice (the second time from L2), any width; few rows (at most
 //    SMs/8) of up to 16384 vectors split over a cluster of 8 CTAs instead;
@@ -357,16 +366,22 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 // least one per SM).
 namespace {
 
-// bf16 plain rows of many CTAs (4 vectors per thread) that load their next row while reducing
-// the current one: within 32 vectors of 256, 512 and 640, and 1185..1312 vectors. There the
-// no-prefetch kernel measured 0.89-0.93 of the copy peak and the prefetching one 0.95-0.98 on
-// GB300, at every tensor size and placement tried (256-512 MiB), and by more right after a kernel
-// with a large shared-memory carveout; at the other widths the no-prefetch kernel was as fast or
-// faster (prefetch lost up to 14 points, e.g. at 832 vectors).
-bool bf16_plain_prefetch(int64_t hv) {
-    return (hv > 224 && hv <= 288) || (hv > 480 && hv <= 544) || (hv > 608 && hv <= 672) ||
-           (hv > 1184 && hv <= 1312);
-}
+// Many rows of 129..384 vectors: one plan per 8-vector bucket (bucket b holds rows of
+// 129 + 8b .. 136 + 8b vectors), measured at the bucket's widest row. A plan switched away from
+// the general rules only where another won by at least a point of the copy peak in both
+// contexts (steady, and after a large-carveout kernel). Codes: W / w a warp per row with (W) or
+// without (w) prefetch, 6 vectors per lane up to 192 vectors and 8 up to 256, 4 rows per
+// 128-thread CTA; T / t a CTA per row at 2 vectors per thread with / without prefetch; F / f the
+// same at 4 vectors. Indexed [dtype code][op].
+constexpr int kNarrowLo = 129, kNarrowHi = 384, kNarrowStep = 8;
+const char *const kNarrowPlans[3][2] = {
+    // fp32: plain, fused
+    {"wwwffffWfWWWWWWTfffffffffffffffT", "tttTTTTTtTTTTTTWtttTTTTTtttTTTTT"},
+    // fp16
+    {"wwwwwwwffffffffWffffffffffffffff", "wttttfffttttttTTtttttttttttttttt"},
+    // bf16
+    {"wWWWWWWfwffffWWWffffffffffffffff", "tttttFFFFttttttttttttttFtttttttt"},
+};
 
 void cta_row(ks_plan_t *p, int64_t hv, int v, bool prefetch) {
     p->kernel = KS_KERNEL_CTA_ROW;
@@ -374,6 +389,21 @@ void cta_row(ks_plan_t *p, int64_t hv, int v, bool prefetch) {
     p->block = (int32_t)round_up(ceil_div(hv, v), 32);
     p->team = p->block;
     p->flags = prefetch ? 0 : KS_PLAN_NO_PREFETCH;
+}
+
+// The kNarrowPlans plan for a row of hv (129..384) vectors; returns the rows each CTA handles.
+int64_t narrow_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
+    const char c = kNarrowPlans[(int)dtype][fused ? 1 : 0][(hv - kNarrowLo) / kNarrowStep];
+    if (c == 'W' || c == 'w') {
+        p->kernel = KS_KERNEL_WARP_ROW;
+        p->vec_per_thread = hv <= 192 ? 6 : 8;
+        p->team = 32;
+        p->block = 128;
+        p->flags = c == 'W' ? 0 : KS_PLAN_NO_PREFETCH;
+        return 4;
+    }
+    cta_row(p, hv, (c == 'T' || c == 't') ? 2 : 4, c == 'T' || c == 'F');
+    return 1;
 }
 
 void bulk_row(ks_plan_t *p, int64_t hv, bool fused, int64_t stages) {
@@ -454,37 +484,31 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
             cta_row(p, hv, 4, fused);
         }
     } else if (vec_ok && hv <= 2048) {
-        // Many rows. Besides the general rules, 16-bit exceptions measured on GB300 with every
-        // candidate plan timed in steady state and right after a kernel with a large shared-memory
-        // carveout (each gains 1-4 points of the copy peak there): bf16 plain prefetches at the
-        // widths of bf16_plain_prefetch; bf16 fused prefetches at 4 vectors at 161..224 vectors
-        // and from 1473 (the general rule prefetches from 1537); fp16 fused takes 4 vectors
-        // without prefetch at 161..224 and 2 with prefetch at 225..288; 16-bit fused rows of
-        // 609..672 vectors take 4 vectors without prefetch.
+        // Many rows.
         const bool f32 = dtype == KS_DTYPE_F32;
         if (hv <= 128) {  // cta_narrow
             cta_row(p, hv, fused ? 4 : 2, true);
-        } else if (f32 && hv <= 384) {
-            cta_row(p, hv, 2, true);
+        } else if (hv <= kNarrowHi) {
+            rows_per_cta = narrow_row(p, hv, fused, dtype);
         } else if (!fused) {
-            if (hv > 1536 && !f32)
+            if (f32 && (hv == 512 || hv == 640))
+                cta_row(p, hv, 2, true);
+            else if ((hv > 1536 && !f32) || (f32 && hv > 1536 && hv <= 1696))
                 twopass_row(p, hv, false, dtype);
             else
-                cta_row(p, hv, 4, bf16 && bf16_plain_prefetch(hv));
-        } else if (bf16 && hv > 160 && hv <= 224) {
-            cta_row(p, hv, 4, true);
-        } else if (f16 && hv > 160 && hv <= 224) {
-            cta_row(p, hv, 4, false);
-        } else if (f16 && hv > 224 && hv <= 288) {
-            cta_row(p, hv, 2, true);
-        } else if (!f32 && hv > 608 && hv <= 672) {
+                cta_row(p, hv, 4, bf16 && (hv == 512 || hv == 640 || (hv >= 1184 && hv <= 1280)));
+        } else if (f32 && ((hv > 768 && hv <= 928) || hv > 1408)) {
+            twopass_row(p, hv, true, dtype);
+        } else if (f32 && hv > 928 && hv <= 960) {
+            cta_row(p, hv, 2, false);
+        } else if (!f32 && hv > 544 && hv <= 672) {
             cta_row(p, hv, 4, false);
         } else if (hv <= 1472 || (!bf16 && hv <= 1536)) {
             const bool two = hv <= 768 || (hv > 960 && hv <= 1152);
             cta_row(p, hv, two ? 2 : 4, false);
-        } else if (bf16) {
+        } else if (bf16 && hv <= 1984) {
             cta_row(p, hv, 4, true);
-        } else if (!f32 && hv <= 1728 && ring_rows) {
+        } else if (f16 && hv <= 1696 && ring_rows) {
             bulk_row(p, hv, true, 2);
         } else {
             twopass_row(p, hv, true, dtype);

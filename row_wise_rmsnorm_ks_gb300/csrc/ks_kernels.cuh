@@ -855,6 +855,10 @@ const void *pick_kernel(const ks_plan_t &p) {
                           : (const void *)rows_vec_kernel<T, 2, kFused, true, false>;
         case 4: return pf ? (const void *)rows_vec_kernel<T, 4, kFused, true, true>
                           : (const void *)rows_vec_kernel<T, 4, kFused, true, false>;
+        case 6: return pf ? (const void *)rows_vec_kernel<T, 6, kFused, true, true>
+                          : (const void *)rows_vec_kernel<T, 6, kFused, true, false>;
+        case 8: return pf ? (const void *)rows_vec_kernel<T, 8, kFused, true, true>
+                          : (const void *)rows_vec_kernel<T, 8, kFused, true, false>;
         default: return nullptr;
         }
     }

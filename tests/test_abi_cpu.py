@@ -129,16 +129,19 @@ def test_narrow_rows_take_warp_per_row(op, hidden, dtype, v):
 # The measured exceptions for 16-bit rows with many rows (op, hidden, dtype) -> (vectors per thread,
 # prefetch), and the neighbouring widths that keep the general rule.
 NO_PF = _abi.KS_PLAN_NO_PREFETCH
+CTA, BULK, TWO = _abi.KS_KERNEL_CTA_ROW, _abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_TWOPASS_ROW
 EXCEPTIONS = [
     ((0, 1024, BF16), (2, True)),     # 128 vectors: CTA at 2 vectors, not a warp
     ((1, 1024, F16), (4, True)),
-    ((0, 2048, BF16), (4, True)),     # 256 vectors
+    ((0, 2304, BF16), (4, False)),    # 288 vectors (H = 2304): no prefetch (it lost 10 points)
     ((0, 3072, BF16), (4, False)),    # 384: general rule
     ((0, 4096, BF16), (4, True)),     # 512
     ((0, 5120, BF16), (4, True)),     # 640
     ((0, 6144, BF16), (4, False)),    # 768: general rule
     ((0, 8192, BF16), (4, False)),    # 1024: general rule (the headline shape)
     ((0, 10240, BF16), (4, True)),    # 1280
+    ((0, 10496, BF16), (4, False)),   # 1312: no prefetch (it lost 19 points)
+    ((0, 4352, BF16), (4, False)),    # 544: no prefetch
     ((0, 4096, F16), (4, False)),     # fp16 plain keeps the general rule
     ((1, 1536, BF16), (4, True)),     # 192
     ((1, 1536, F16), (4, False)),
@@ -149,6 +152,8 @@ EXCEPTIONS = [
     ((1, 5120, BF16), (4, False)),    # 640 vectors, fused: 4 without prefetch
     ((1, 5120, F16), (4, False)),
     ((1, 4096, F16), (2, False)),     # 512: general rule
+    ((1, 4864, BF16), (4, False)),    # 608 vectors, fused: 4 without prefetch
+    ((1, 2304, F16), (2, False)),     # 288 vectors, fp16 fused: no prefetch (+8 points)
 ]
 
 
@@ -163,9 +168,63 @@ def test_measured_16bit_plan_exceptions(args, want):
 def test_bf16_fused_prefetch_starts_at_1473_vectors():
     p = plan(1, 32768, 11776, BF16)  # 1472 vectors: the general rule (4 vectors, no prefetch)
     assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags & NO_PF
-    for hidden in (11784, 12288, 16384):  # 1473, 1536, 2048 vectors: prefetch at 4 vectors
+    for hidden in (11784, 12288, 15872):  # 1473, 1536, 1984 vectors: prefetch at 4 vectors
         p = plan(1, 32768, hidden, BF16)
         assert p.kernel == CTA and p.vec_per_thread == 4 and not (p.flags & NO_PF)
+    for hidden in (15880, 16384):  # 1985, 2048 vectors: the two-pass kernel
+        p = plan(1, 32768, hidden, BF16)
+        assert (p.kernel, p.vec_per_thread, p.block) == (TWO, 2, 512)
+
+
+# Many rows of 129..384 vectors: the measured per-bucket table. (op, hidden, dtype) ->
+# (kernel, vectors per thread or lane, prefetch).
+WARP = _abi.KS_KERNEL_WARP_ROW
+NARROW = [
+    ((0, 1088, BF16), (WARP, 6, False)),   # 136 vectors
+    ((0, 1280, BF16), (WARP, 6, True)),    # 160 (H = 1280)
+    ((0, 1536, BF16), (CTA, 4, False)),    # 192 (H = 1536): the CTA row stays
+    ((0, 2048, BF16), (WARP, 8, True)),    # 256
+    ((0, 1280, F16), (WARP, 6, False)),
+    ((0, 2048, F16), (WARP, 8, True)),
+    ((0, 640, F32), (CTA, 4, False)),      # 160 fp32 vectors
+    ((0, 896, F32), (WARP, 8, True)),      # 224
+    ((0, 1024, F32), (CTA, 2, True)),      # 256
+    ((0, 1280, F32), (CTA, 4, False)),     # 320
+    ((1, 1792, BF16), (CTA, 2, False)),    # 224
+    ((1, 2560, BF16), (CTA, 4, True)),     # 320 (H = 2560)
+    ((1, 1088, F16), (WARP, 6, False)),    # 136
+    ((1, 1792, F16), (CTA, 2, False)),     # 224
+    ((1, 2048, F32), (CTA, 2, False)),     # 512 fp32 vectors: general rule (above the table)
+    ((1, 1024, F32), (WARP, 8, True)),     # 256
+    ((1, 1088, F32), (CTA, 2, False)),     # 272
+]
+
+
+@pytest.mark.parametrize("args,want", NARROW)
+def test_narrow_rows_take_the_measured_table(args, want):
+    op, hidden, dtype = args
+    p = plan(op, 32768, hidden, dtype)
+    kernel, v, pf = want
+    assert (p.kernel, p.vec_per_thread, not (p.flags & NO_PF)) == (kernel, v, pf)
+    if kernel == WARP:
+        assert p.team == 32 and p.block == 128 and p.rows_per_pass == p.grid * 4
+
+
+@pytest.mark.parametrize("dtype", [BF16, F16, F32])
+@pytest.mark.parametrize("op", [0, 1])
+def test_every_narrow_width_gets_a_plan_the_library_accepts(dtype, op):
+    # the rules of the planned entry points' check, for every width the table covers
+    per = 4 if dtype == F32 else 8
+    for hv in range(129, 385):
+        p = plan(op, 32768, hv * per, dtype, bps=4)
+        if p.kernel == WARP:
+            assert p.vec_per_thread in (6, 8) and 32 * p.vec_per_thread >= hv
+            assert p.block == 128 and p.team == 32
+        else:
+            assert p.kernel == CTA and p.vec_per_thread in (2, 4)
+            assert p.block * p.vec_per_thread >= hv and p.block % 32 == 0
+            assert p.block <= (1024 if p.vec_per_thread == 2 else 512)
+        assert p.grid == 152 * 4
 
 
 def test_few_rows_keep_the_latency_rules():
@@ -182,7 +241,6 @@ def test_warp_per_row_spreads_few_rows_over_sms():
 
 # bf16 widths and the plan the sweep picks at HBM-bound row counts: (kernel, vectors/thread,
 # prefetch) for the fused op, then for the plain op.
-CTA, BULK, TWO = _abi.KS_KERNEL_CTA_ROW, _abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_TWOPASS_ROW
 WIDE_BF16 = [
     (1536, (CTA, 4, True), (CTA, 4, False)),
     (4096, (CTA, 2, False), (CTA, 4, True)),
@@ -193,7 +251,7 @@ WIDE_BF16 = [
     (12288, (CTA, 4, True), (CTA, 4, False)),
     (13312, (CTA, 4, True), (TWO, 4, 256)),
     (14336, (CTA, 4, True), (TWO, 4, 256)),
-    (16384, (CTA, 4, True), (TWO, 4, 256)),
+    (16384, (TWO, 2, 512), (TWO, 4, 256)),
 ]
 
 
@@ -371,6 +429,8 @@ def test_planned_entry_points_reject_plans_that_do_not_fit():
         mk(_abi.KS_KERNEL_CTA_ROW, 4, 1024),        # over the 512-thread bound at 4 vectors
         mk(_abi.KS_KERNEL_CTA_ROW, 3, 512),         # unsupported vector count
         mk(_abi.KS_KERNEL_WARP_ROW, 4, 64),         # a warp cannot cover 1024 vectors
+        mk(_abi.KS_KERNEL_WARP_ROW, 8, 64),         # nor at 8 vectors per lane (256)
+        mk(_abi.KS_KERNEL_WARP_ROW, 3, 64),         # unsupported vector count
         mk(_abi.KS_KERNEL_BULK_ROW, 4, 256, 0),     # no stages
         mk(_abi.KS_KERNEL_BULK_ROW, 4, 256, 15),    # 15 x 16 KB > 227 KB
         mk(_abi.KS_KERNEL_SCALAR, 0, 48),           # not a multiple of 32

@@ -111,6 +111,31 @@ def test_edge_widths(cuda_device, hidden, dtype, op):
     run_and_check(w, cuda_device)
 
 
+# Row widths (16-byte vectors) at which the launch heuristic changes plan for many rows: the
+# edges of the measured 8-vector buckets of rows of 129..384 vectors, the widths with their own
+# rule above them, and the edges of the two-pass and staged ranges.
+PLAN_EDGE_HV = [129, 136, 137, 160, 184, 185, 192, 193, 200, 224, 232, 233, 248, 256, 257, 288,
+                320, 384, 385, 512, 544, 545, 608, 640, 672, 800, 928, 929, 960, 1184, 1280,
+                1312, 1408, 1409, 1440, 1537, 1568, 1696, 1697, 1984, 1985, 2048]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
+@pytest.mark.parametrize("hv", PLAN_EDGE_HV)
+def test_default_plans_at_heuristic_edges(cuda_device, hv, op, dtype):
+    """The default entry points on many rows (333: more rows than SMs, and ragged) at every
+    width where the launch heuristic switches plan, so each plan it can pick is checked."""
+    dt = synth.dtype_of(dtype)
+    hidden = hv * (4 if dt == torch.float32 else 8)
+    rows = 333
+    x = synth.cast(synth.normal_np((rows, hidden), 41), dt)
+    wt = synth.weight(hidden, dt)
+    r = synth.cast(synth.normal_np((rows, hidden), 42, std=2.0), dt) if op != "rms_norm" else None
+    w = synth.Workload(f"plan edge {op} {dtype} [{rows},{hidden}]", op, dt, x, wt, 1e-6,
+                       residual=r)
+    run_and_check(w, cuda_device)
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
 def test_unaligned_pointers(cuda_device, dtype, op):
@@ -256,7 +281,7 @@ def _variant_plan(name, hidden, elem):
         return A.make_plan(A.KS_KERNEL_TWOPASS_ROW, int(u), int(block))
     flags = A.KS_PLAN_NO_PREFETCH if name.endswith("_np") else 0
     if name.startswith("warp_row"):
-        v = next((v for v in (1, 2, 4) if 32 * v >= hv), None)
+        v = next((v for v in (1, 2, 4, 6, 8) if 32 * v >= hv), None)
         return A.make_plan(A.KS_KERNEL_WARP_ROW, v, 128, flags=flags) if v else None
     v = 2 if name.startswith("cta_row_v2") else 4
     block = max(32, up32(-(-hv // v)))
@@ -286,8 +311,8 @@ VARIANTS = ["warp_row", "warp_row_np", "cta_row_v2", "cta_row_v2_np", "cta_row_v
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
-@pytest.mark.parametrize("rows,hidden", [(333, 1024), (1000, 1536), (457, 4096), (300, 8192),
-                                         (155, 16384)])
+@pytest.mark.parametrize("rows,hidden", [(333, 1024), (1000, 1536), (77, 1400), (457, 4096),
+                                         (300, 8192), (155, 16384)])
 def test_every_kernel_variant_matches_oracle(cuda_device, variant, dtype, op, rows, hidden):
     from row_wise_rmsnorm_ks_gb300 import _abi as A
     dt = synth.dtype_of(dtype)
