@@ -1136,6 +1136,95 @@ def run_plan_contexts(args) -> int:
     return 0
 
 
+def run_ops_scan(args) -> int:
+    """The next operators' default launches over row widths (one JSON line per dtype and width;
+    not the contract's line): Softmax, LayerNorm (weight and bias) and SwiGLU on rows of
+    --plan-sweep-widths 16-byte vectors (SwiGLU: d of that many vectors), 384 MiB per input
+    tensor, N(0,1) inputs, each timed in steady state (back-to-back launches) and right after one
+    launch of the staged RMSNorm ring, a kernel with a large shared-memory carveout (each launch
+    timed alone); the median of --plan-sweep-rounds rounds, as a fraction of the measured copy
+    peak."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    peak = measured_peaks()["hbm_gbs"]
+    codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
+
+    def steady(fn, n=25):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(4):
+            fn()
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n * 1e-3
+
+    def after(fn, pre, n=10):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(n):
+            pre()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b) * 1e-3
+        return tot / n
+
+    widths = [int(v) for v in (args.plan_sweep_widths or "64,96,128,160,192,256,512,1024,2048").split(",")]
+    for dt in args.plan_sweep_dtypes.split(","):
+        e = 4 if dt == "fp32" else 2
+        code = codes[dt]
+        for hv in widths:
+            H = hv * 16 // e
+            R = (384 << 20) // (H * e)
+            x = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), dt)
+            y = torch.empty_like(x)
+            w = synth.weight(H, dt).to(dev)
+            b = synth.weight(H, dt).to(dev)
+            ring = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, -(-(-(-hv // 4)) // 32) * 32, 2)
+            pre = (lambda: _abi.check(_abi.ks_rms_norm_planned(
+                y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H, 1e-5, code, ring, s)))
+            if 128 + 2 * hv * 16 > 226 * 1024 or hv > 2048:
+                pre = None  # no ring of two stages fits: steady context only
+            R2 = R // 2  # SwiGLU reads x as [R2, 2H] and writes [R2, H] into y
+            ops = {
+                "softmax": (2 * R * H * e,
+                            lambda: _abi.check(_abi.ks_softmax(y.data_ptr(), x.data_ptr(), R, H,
+                                                               code, s))),
+                "layer_norm": (2 * R * H * e + 2 * H * e,
+                               lambda: _abi.check(_abi.ks_layer_norm(
+                                   y.data_ptr(), x.data_ptr(), w.data_ptr(), b.data_ptr(), R, H,
+                                   1e-5, code, s))),
+                "silu_and_mul": (3 * R2 * H * e,
+                                 lambda: _abi.check(_abi.ks_silu_and_mul(
+                                     y.data_ptr(), x.data_ptr(), R2, H, code, s))),
+            }
+            line = {"ops_scan": dt, "hv": hv, "hidden": H, "rows": R}
+            for name, (nb, fn) in ops.items():
+                st, af = [], []
+                for _ in range(args.plan_sweep_rounds):
+                    st.append(nb / steady(fn) / 1e9 / peak)
+                    if pre:
+                        af.append(nb / after(fn, pre) / 1e9 / peak)
+                line[name] = {"steady": round(statistics.median(st), 4),
+                              "after_ring": round(statistics.median(af), 4) if af else None}
+            print(json.dumps(line), flush=True)
+            del x, y, w, b
+            torch.cuda.empty_cache()
+    st, flags = _abi.ks_device_faults(clear=False)
+    if st != _abi.KS_SUCCESS or flags:
+        print(json.dumps({"ops_scan": "device faults", "status": st, "flags": flags}))
+        return 1
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1158,6 +1247,9 @@ def main() -> int:
     ap.add_argument("--plan-contexts", action="store_true",
                     help="compare the register-kernel plans per width in steady state and right "
                          "after a large-shared-memory kernel, and exit")
+    ap.add_argument("--ops-scan", action="store_true",
+                    help="time the next operators' default launches per dtype and width, in steady "
+                         "state and right after a large-shared-memory kernel, and exit")
     ap.add_argument("--plan-sweep-rounds", type=int, default=3)
     ap.add_argument("--plan-sweep-dtypes", default="bf16,fp16,fp32")
     ap.add_argument("--plan-sweep-widths", default="",
@@ -1178,6 +1270,8 @@ def main() -> int:
         return run_plan_sweep(args)
     if args.plan_contexts:
         return run_plan_contexts(args)
+    if args.ops_scan:
+        return run_ops_scan(args)
     return run_ks(args)
 
 

@@ -350,7 +350,11 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 //        545..672. Wider rows: bf16 prefetches at 4 vectors per thread (from 1473) and takes the
 //        two-pass kernel from 1985; fp16 takes the staged ring (2 stages) up to 1696 vectors when
 //        there are enough rows, the two-pass kernel beyond; fp32 takes the two-pass kernel at
-//        769..928 and from 1409, and 2 vectors per thread at 929..960.
+//        769..928 and from 1409, and 2 vectors per thread at 929..960. The two-pass switches that
+//        came from the dense sweep (bf16 fused from 1985, fp32 fused at 769..928 and 1409..1536,
+//        fp32 plain at 1537..1696) need at least 4 rows per SM, as the sweep had: with fewer rows,
+//        e.g. 333 bf16 fused rows of 2048 vectors, the one-pass plan measured faster (7.5 against
+//        7.9 us a launch under graph replay), so those take the previous rules.
 //    In the latency regime (rows <= SMs, so each CTA gets at most one row) prefetch has nothing
 //    to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8
 //    CTAs per row, plain rows of at most 1024 vectors take 2 vectors per thread, and the rest 4
@@ -493,11 +497,11 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         } else if (!fused) {
             if (f32 && (hv == 512 || hv == 640))
                 cta_row(p, hv, 2, true);
-            else if ((hv > 1536 && !f32) || (f32 && hv > 1536 && hv <= 1696))
+            else if ((hv > 1536 && !f32) || (f32 && ring_rows && hv > 1536 && hv <= 1696))
                 twopass_row(p, hv, false, dtype);
             else
                 cta_row(p, hv, 4, bf16 && (hv == 512 || hv == 640 || (hv >= 1184 && hv <= 1280)));
-        } else if (f32 && ((hv > 768 && hv <= 928) || hv > 1408)) {
+        } else if (f32 && ring_rows && ((hv > 768 && hv <= 928) || hv > 1408)) {
             twopass_row(p, hv, true, dtype);
         } else if (f32 && hv > 928 && hv <= 960) {
             cta_row(p, hv, 2, false);
@@ -506,7 +510,7 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         } else if (hv <= 1472 || (!bf16 && hv <= 1536)) {
             const bool two = hv <= 768 || (hv > 960 && hv <= 1152);
             cta_row(p, hv, two ? 2 : 4, false);
-        } else if (bf16 && hv <= 1984) {
+        } else if (bf16 && (hv <= 1984 || !ring_rows)) {
             cta_row(p, hv, 4, true);
         } else if (f16 && hv <= 1696 && ring_rows) {
             bulk_row(p, hv, true, 2);

@@ -59,6 +59,18 @@ __device__ __forceinline__ float cta_max(float v, float (*red)[32], int &slot) {
     return m;
 }
 
+// Reductions over a row's team: a warp (kWarp: shuffles only, no barrier, so the warps of a CTA
+// work on their own rows independently) or the whole CTA.
+template <bool kWarp>
+__device__ __forceinline__ float team_sum(float v, float (*red)[32], int &slot) {
+    return kWarp ? warp_sum(v) : cta_sum(v, red, slot);
+}
+
+template <bool kWarp>
+__device__ __forceinline__ float team_max(float v, float (*red)[32], int &slot) {
+    return kWarp ? warp_max(v) : cta_max(v, red, slot);
+}
+
 // e^v. For 16-bit outputs the SFU-based intrinsic (error a few fp32 ulps, growing with |v|,
 // far below half a bf16/fp16 ulp); for fp32 outputs CUDA's expf (within 2 ulp).
 template <typename T>
@@ -117,11 +129,16 @@ __device__ __forceinline__ float silu_mul<float>(float g, float up) {
 
 // ------------------------------------------------------------------------------- SwiGLU
 
-// Vector path: rows of d elements as dv = d / E 16-byte vectors in the gate half and the up half
-// of each input row. blockIdx.y strides over rows, the x dimension over a row's vectors.
+// Vector paths: rows of d elements as dv = d / E 16-byte vectors in the gate half and the up half
+// of each input row.
+//
+// Row-structured: blockIdx.y and threadIdx.y over rows, the x dimensions over a row's vectors,
+// two vectors per thread per iteration with the loads issued before the math. The launch fits the
+// block to the row (a multiple of 32 threads covering half the row's vectors per column of CTAs)
+// and stacks narrow rows several to a CTA, so few threads sit idle.
 template <typename T>
-__global__ void __launch_bounds__(256) silu_mul_vec_kernel(void *out, const void *x, int64_t rows,
-                                                           int64_t dv) {
+__global__ void __launch_bounds__(256) silu_mul_rows_kernel(void *out, const void *x,
+                                                            int64_t rows, int64_t dv) {
     using E = Elem<T>;
     constexpr int N = E::kPerVec;
     grid_dependency_wait();
@@ -129,12 +146,12 @@ __global__ void __launch_bounds__(256) silu_mul_vec_kernel(void *out, const void
     const uint4 *xg = static_cast<const uint4 *>(x);
     uint4 *og = static_cast<uint4 *>(out);
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t row = blockIdx.y; row < rows; row += gridDim.y) {
+    const int64_t rstep = (int64_t)gridDim.y * blockDim.y;
+    for (int64_t row = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; row < rows; row += rstep) {
         const uint4 *gate = xg + row * 2 * dv;
         const uint4 *up = gate + dv;
         uint4 *o = og + row * dv;
         int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-        // two vectors per thread per iteration, loads issued before the math
         for (; c + step < dv; c += 2 * step) {
             const uint4 g0 = __ldcs(gate + c), u0 = __ldcs(up + c);
             const uint4 g1 = __ldcs(gate + c + step), u1 = __ldcs(up + c + step);
@@ -161,6 +178,73 @@ __global__ void __launch_bounds__(256) silu_mul_vec_kernel(void *out, const void
     }
 }
 
+// Flat: the output [rows, dv] walked as one run of rows * dv vectors, grid-stride, two vectors
+// per thread per iteration, so every thread has work whatever the row width (a 256-thread block laid across a row of
+// 64 vectors left 7 of its 8 warps idle: bf16 d = 512 ran at 0.54 of the copy peak). It spends
+// more integer instructions per vector than the row-structured kernel. Output vector i is input
+// vector i + row * dv of the gate half (row = i / dv) and dv further on of the up half; each
+// thread divides once, then carries (row, column) forward by the stride.
+template <typename T>
+__global__ void __launch_bounds__(256) silu_mul_flat_kernel(void *out, const void *x, int64_t rows,
+                                                           int64_t dv) {
+    using E = Elem<T>;
+    constexpr int N = E::kPerVec;
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const uint4 *xg = static_cast<const uint4 *>(x);
+    uint4 *og = static_cast<uint4 *>(out);
+    const int64_t total = rows * dv;
+    const int64_t step = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= total) return;
+    // (row, column) of flat vector i, of i + step, and the increments of 2 * step
+    int64_t r0 = i / dv, c0 = i - r0 * dv;
+    const int64_t sr = step / dv, sc = step - sr * dv;
+    const int64_t sr2 = (2 * step) / dv, sc2 = 2 * step - sr2 * dv;
+    int64_t r1 = r0 + sr, c1 = c0 + sc;
+    if (c1 >= dv) {
+        c1 -= dv;
+        ++r1;
+    }
+    for (; i + step < total; i += 2 * step) {
+        const uint4 *p0 = xg + i + r0 * dv, *p1 = xg + i + step + r1 * dv;
+        const uint4 g0 = __ldcs(p0), u0 = __ldcs(p0 + dv);
+        const uint4 g1 = __ldcs(p1), u1 = __ldcs(p1 + dv);
+        float a[N], b[N], r[N];
+        E::unpack(g0, a);
+        E::unpack(u0, b);
+#pragma unroll
+        for (int e = 0; e < N; ++e) r[e] = silu_mul<T>(a[e], b[e]);
+        __stcs(og + i, E::pack(r));
+        E::unpack(g1, a);
+        E::unpack(u1, b);
+#pragma unroll
+        for (int e = 0; e < N; ++e) r[e] = silu_mul<T>(a[e], b[e]);
+        __stcs(og + i + step, E::pack(r));
+        r0 += sr2;
+        c0 += sc2;
+        if (c0 >= dv) {
+            c0 -= dv;
+            ++r0;
+        }
+        r1 += sr2;
+        c1 += sc2;
+        if (c1 >= dv) {
+            c1 -= dv;
+            ++r1;
+        }
+    }
+    if (i < total) {
+        const uint4 *p0 = xg + i + r0 * dv;
+        float a[N], b[N], r[N];
+        E::unpack(__ldcs(p0), a);
+        E::unpack(__ldcs(p0 + dv), b);
+#pragma unroll
+        for (int e = 0; e < N; ++e) r[e] = silu_mul<T>(a[e], b[e]);
+        __stcs(og + i, E::pack(r));
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) silu_mul_scalar_kernel(void *out, const void *x,
                                                               int64_t rows, int64_t d) {
@@ -179,14 +263,15 @@ __global__ void __launch_bounds__(256) silu_mul_scalar_kernel(void *out, const v
 
 // ------------------------------------------------------------------------------ Softmax
 
-// One CTA per row, V 16-byte vectors per thread held in registers; persistent over rows. With
+// One CTA per row (or with kWarp one warp per row, the CTA's warps on rows of their own), V
+// 16-byte vectors per thread held in registers; persistent over rows. With
 // kPrefetch the next row's vectors are loaded before the current row's two reductions; without
 // it each row is loaded when its turn comes (fewer registers, more resident warps: faster up to
 // 1024 vectors per row on GB300, slower beyond). The maximum is a plain fmaxf (NaN-ignoring): a
 // NaN or +inf in the row still makes the sum, and so every output, NaN, and a row of only -inf
 // still gets max -inf and z = NaN, so the contract's non-finite rules hold.
-template <typename T, int V, bool kPrefetch>
-__global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void *x, int64_t rows,
+template <typename T, int V, bool kPrefetch, bool kWarp = false>
+__global__ void __launch_bounds__(kWarp ? 128 : 512) softmax_vec_kernel(void *out, const void *x, int64_t rows,
                                                           int64_t hv) {
     using E = Elem<T>;
     constexpr int P = E::kPerVec / 2;
@@ -199,9 +284,12 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
     allow_dependents_launch();
     const uint4 *xg = static_cast<const uint4 *>(x);
     uint4 *og = static_cast<uint4 *>(out);
-    const int t = threadIdx.x, g = blockDim.x;
+    const int t = kWarp ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
+    const int g = kWarp ? 32 : (int)blockDim.x;
+    const int teams = kWarp ? (int)(blockDim.x >> 5) : 1;
+    const int64_t stride = (int64_t)gridDim.x * teams;
     int slot = 0;
-    int64_t row = blockIdx.x;
+    int64_t row = (int64_t)blockIdx.x * teams + (kWarp ? (int)(threadIdx.x >> 5) : 0);
     uint4 cur[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) {
@@ -209,8 +297,8 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
         cur[k] = (kPrefetch && row < rows && c < hv) ? __ldcs(xg + row * hv + c)
                                                      : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (; row < rows; row += gridDim.x) {
-        const int64_t next = row + gridDim.x;
+    for (; row < rows; row += stride) {
+        const int64_t next = row + stride;
         uint4 nxt[V];
 #pragma unroll
         for (int k = 0; k < V; ++k) {
@@ -231,7 +319,7 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
                 for (int i = 0; i < P; ++i) m = fmaxf(fmaxf(m, f[k][i].x), f[k][i].y);
             }
         }
-        m = cta_max(m, red, slot);
+        m = team_max<kWarp>(m, red, slot);
         // 16-bit outputs: e_j * 2^64 = 2^(x_j log2(e) + (64 - m log2(e))), one FMA and one SFU op
         // per element; the 2^64 cancels in e_j / sum and keeps every exp above 2^-190 normal
         // (smaller ones are below any fp32 output anyway). For m = +-inf or NaN the bias is
@@ -250,7 +338,7 @@ __global__ void __launch_bounds__(512) softmax_vec_kernel(void *out, const void 
                 }
             }
         }
-        const float sum = cta_sum(__fadd_rn(__fadd_rn(s[0].x, s[0].y), __fadd_rn(s[1].x, s[1].y)), red, slot);
+        const float sum = team_sum<kWarp>(__fadd_rn(__fadd_rn(s[0].x, s[0].y), __fadd_rn(s[1].x, s[1].y)), red, slot);
         // e / sum as e * (1 / sum): one correctly rounded reciprocal per row, then a product
         // per element (within 1 fp32 ulp of the quotient)
         const float inv = __frcp_rn(sum);
@@ -304,9 +392,10 @@ __global__ void __launch_bounds__(1024) softmax_scalar_kernel(void *out, const v
 // did not hoist it out of the unrolled loop).
 constexpr int kAffineWeight = 1, kAffineBias = 2;
 
-// One CTA per row, V 16-byte vectors per thread in registers, persistent over rows; the weight
-// and bias slices a thread needs stay in registers for every row it visits, and the next row's
-// vectors are loaded before the current row's two reductions. (Measured on GB300 at [32768,
+// One CTA per row (or with kWarp one warp per row, the CTA's warps on rows of their own), V
+// 16-byte vectors per thread in registers, persistent over rows; the weight and bias slices a
+// thread needs stay in registers for every row it visits, and the next row's vectors are loaded
+// before the current row's two reductions. (Measured on GB300 at [32768,
 // 8192] bf16: 74 % of the copy peak; weight and bias in shared memory, with or without the
 // prefetch, were slower at 58-64 %.)
 // LayerNorm element steps, on FP32 pairs (packed instructions where Elem::kPairMath). Four running
@@ -362,8 +451,8 @@ __device__ __forceinline__ uint4 ln_out(const uint4 &v, const uint4 &wv, const u
     return Elem<T>::pack2(f);
 }
 
-template <typename T, int V, int kAffine>
-__global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const void *x,
+template <typename T, int V, int kAffine, bool kWarp = false>
+__global__ void __launch_bounds__(kWarp ? 128 : 512) layer_norm_vec_kernel(void *out, const void *x,
                                                              const void *w, const void *b,
                                                              int64_t rows, int64_t hidden,
                                                              int64_t hv, float eps) {
@@ -373,7 +462,10 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
     allow_dependents_launch();
     const uint4 *xg = static_cast<const uint4 *>(x);
     uint4 *og = static_cast<uint4 *>(out);
-    const int t = threadIdx.x, g = blockDim.x;
+    const int t = kWarp ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
+    const int g = kWarp ? 32 : (int)blockDim.x;
+    const int teams = kWarp ? (int)(blockDim.x >> 5) : 1;
+    const int64_t stride = (int64_t)gridDim.x * teams;
     const float h = (float)hidden;
     uint4 wv[V], bv[V];
 #pragma unroll
@@ -383,15 +475,15 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
         bv[k] = (kB && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
     }
     int slot = 0;
-    int64_t row = blockIdx.x;
+    int64_t row = (int64_t)blockIdx.x * teams + (kWarp ? (int)(threadIdx.x >> 5) : 0);
     uint4 xv[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) {
         const int64_t c = t + (int64_t)k * g;
         xv[k] = (row < rows && c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (; row < rows; row += gridDim.x) {
-        const int64_t next = row + gridDim.x;
+    for (; row < rows; row += stride) {
+        const int64_t next = row + stride;
         uint4 nxt[V];
 #pragma unroll
         for (int k = 0; k < V; ++k) {
@@ -401,12 +493,12 @@ __global__ void __launch_bounds__(512) layer_norm_vec_kernel(void *out, const vo
         float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
         for (int k = 0; k < V; ++k) ln_add_sum<T>(xv[k], s2);
-        const float mean = __fdiv_rn(cta_sum(ln_total(s2), red, slot), h);
+        const float mean = __fdiv_rn(team_sum<kWarp>(ln_total(s2), red, slot), h);
         float2 q2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
         for (int k = 0; k < V; ++k)
             if (t + (int64_t)k * g < hv) ln_add_sq<T>(xv[k], -mean, q2);
-        const float var = __fdiv_rn(cta_sum(ln_total(q2), red, slot), h);
+        const float var = __fdiv_rn(team_sum<kWarp>(ln_total(q2), red, slot), h);
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
         const float shift = -__fmul_rn(mean, rstd);
 #pragma unroll
@@ -810,50 +902,213 @@ cudaError_t launch(const void *f, dim3 grid, dim3 block, void **args, cudaStream
     return cudaLaunchKernel(f, grid, block, args, 0, s);
 }
 
+// SwiGLU launch shapes. kSiluRows: the row-structured kernel with its block fitted to the row,
+// at most `max_block` threads; kSiluFlat: the flat walk over all rows' vectors; kSiluScalar:
+// element loads (rows that cannot be vectorised).
+enum SiluKind { kSiluScalar, kSiluRows, kSiluFlat };
+
+struct SiluPlan {
+    SiluKind kind;
+    int max_block;
+};
+
+// Measured on GB300 over widths of 16..2048 vectors (144..512 in steps of 8 to 32), many rows,
+// each plan timed in steady state and right after a kernel with a large shared-memory carveout
+// (as after a GEMM), the worse of the two kept. The flat walk held 0.81-0.88 of the copy peak for
+// 16-bit types at every width and 0.93-0.98 for fp32, whose rows it serves best throughout. The
+// row-structured kernel beats it for 16-bit rows of 160 and 192 vectors (0.88-0.93) and of
+// 288..447 (0.86-0.94), and from 448 vectors with its block capped at 96 threads (0.86-0.95;
+// with 128..256-thread CTAs some of those widths fell to 0.77-0.84, e.g. bf16 dv = 1024: 0.82);
+// at the other widths below 288 it fell as low as 0.59.
+SiluPlan silu_plan(bool vec, int64_t dv, ks_dtype_t dtype) {
+    if (!vec) return {kSiluScalar, 256};
+    if (dtype == KS_DTYPE_F32) return {kSiluFlat, 256};
+    if (dv >= 448) return {kSiluRows, 96};
+    if (dv >= 288 || dv == 160 || dv == 192) return {kSiluRows, 256};
+    return {kSiluFlat, 256};
+}
+
 template <typename T>
-cudaError_t silu_dispatch(bool vec, void *out, const void *x, int64_t rows, int64_t d, int sms,
-                          cudaStream_t s) {
-    const int64_t per_row = vec ? d / Elem<T>::kPerVec : d;
-    const int block = 256;
-    // columns: enough CTAs to cover a row's vectors twice per thread; rows: fill ~8 waves of SMs
-    int64_t gx = ceil_div64(per_row, (int64_t)block * (vec ? 2 : 1));
+cudaError_t silu_dispatch(SiluPlan plan, void *out, const void *x, int64_t rows, int64_t d,
+                          int sms, cudaStream_t s) {
+    const SiluKind kind = plan.kind;
+    int64_t nr = rows, dd = kind == kSiluScalar ? d : d / Elem<T>::kPerVec;
+    void *args[] = {&out, const_cast<void **>(&x), &nr, &dd};
+    if (kind == kSiluFlat) {
+        // a persistent grid of as many 256-thread CTAs as are resident at once (fewer if the
+        // vectors run out), two vectors per thread per iteration
+        const void *f = (const void *)silu_mul_flat_kernel<T>;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, 256, 0) != cudaSuccess || n < 1)
+            n = 1;
+        int64_t grid = ceil_div64(rows * dd, 512);
+        grid = grid > (int64_t)sms * n ? (int64_t)sms * n : grid;
+        return launch(f, dim3((unsigned)grid), dim3(256), args, s);
+    }
+    if (kind == kSiluRows) {
+        // gx CTAs across a row, each of bx threads covering two vectors a thread (bx a multiple
+        // of 32, at most plan.max_block); narrow rows stack 256 / bx rows per CTA; about 8 CTAs
+        // per SM in all
+        const int64_t gx = ceil_div64(dd, 2 * (int64_t)plan.max_block);
+        const int bx = (int)round_up64(ceil_div64(dd, 2 * gx), 32);
+        int64_t by = 256 / bx;
+        by = by > rows ? rows : by;
+        int64_t gy = ceil_div64(rows, by);
+        const int64_t cap = (int64_t)sms * 8 / gx;
+        gy = gy > cap ? cap : gy;
+        gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
+        return launch((const void *)silu_mul_rows_kernel<T>, dim3((unsigned)gx, (unsigned)gy),
+                      dim3((unsigned)bx, (unsigned)by), args, s);
+    }
+    // scalar: enough CTAs to cover a row once; rows: fill ~8 waves of SMs
+    int64_t gx = ceil_div64(d, 256);
     gx = gx < 1 ? 1 : gx;
     int64_t gy = (int64_t)sms * 8 / gx;
     gy = gy < 1 ? 1 : (gy > rows ? rows : gy);
     gy = gy > 65535 ? 65535 : gy;
-    int64_t nr = rows, dd = per_row;
-    void *args[] = {&out, const_cast<void **>(&x), &nr, &dd};
-    const void *f = vec ? (const void *)silu_mul_vec_kernel<T> : (const void *)silu_mul_scalar_kernel<T>;
-    return launch(f, dim3((unsigned)gx, (unsigned)gy), dim3(block), args, s);
+    return launch((const void *)silu_mul_scalar_kernel<T>, dim3((unsigned)gx, (unsigned)gy),
+                  dim3(256), args, s);
+}
+
+// A register-row launch for Softmax and LayerNorm: V 16-byte vectors per thread, one CTA of
+// `block` threads per row or (warp) one warp per row with block / 32 rows per CTA; prefetch:
+// load the next row before reducing the current one. v == kWideRows: the multi-pass wide kernel;
+// v == 0: the scalar kernel. Warp plans launch 128-thread CTAs (the warp kernels' launch bound,
+// which leaves them up to 255 registers for two rows of up to 8 vectors a lane).
+struct RegPlan {
+    int v;
+    int block;
+    bool warp;
+    bool prefetch;
+};
+
+// Grid of a register-row launch: as many CTAs as are resident at once, no more than the rows
+// need.
+int64_t reg_grid(const void *f, const RegPlan &p, size_t smem, int64_t rows, int sms) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, p.block, smem) != cudaSuccess || n < 1)
+        n = 1;
+    const int64_t per_cta = p.warp ? p.block / 32 : 1;
+    const int64_t need = ceil_div64(rows, per_cta);
+    const int64_t grid = (int64_t)sms * n;
+    return grid > need ? need : grid;
+}
+
+// Width bands for many rows (more rows than SMs) of at most 256 vectors, measured on GB300 per
+// dtype, each plan timed in steady state and right after a kernel with a large shared-memory
+// carveout, the worse of the two kept: rows up to `hi` vectors take one warp per row at `v`
+// vectors per lane (kind 'w'), a CTA per row at 4 vectors with prefetch (kind 'c'), or the
+// general rule (kind 'g'). A CTA per row of 33..64 threads, most of them idle or split across
+// two partly filled warps, paid two CTA barriers per row; warp rows reduce with shuffles alone
+// and fill their lanes. Gains over the general rule at the narrowest widths were 20-39 points of
+// the copy peak (Softmax bf16 72 vectors: 0.52 -> 0.91; LayerNorm fp16 96 vectors: 0.53 -> 0.85).
+struct Band {
+    int16_t hi;
+    char kind;
+    int8_t v;
+    bool prefetch;
+};
+
+constexpr int16_t kBandEnd = 32767;
+constexpr Band kSoftmax16[] = {{32, 'w', 2, false}, {63, 'w', 2, true}, {127, 'w', 4, true},
+                               {128, 'g', 0, false}, {192, 'w', 6, false}, {224, 'w', 8, false},
+                               {kBandEnd, 'g', 0, false}};
+constexpr Band kSoftmax32[] = {{44, 'w', 2, false}, {52, 'w', 2, true}, {63, 'w', 4, false},
+                               {64, 'g', 0, false}, {80, 'w', 4, true}, {128, 'w', 4, false},
+                               {168, 'w', 6, false}, {176, 'g', 0, false}, {216, 'c', 4, true},
+                               {256, 'w', 8, false}, {kBandEnd, 'g', 0, false}};
+constexpr Band kLayerNormBf16[] = {{64, 'w', 2, true}, {127, 'w', 4, true}, {128, 'g', 0, true},
+                                   {192, 'w', 6, true}, {256, 'w', 8, true},
+                                   {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF16[] = {{64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true},
+                                  {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF32[] = {{63, 'w', 2, true}, {64, 'g', 0, true}, {128, 'w', 4, true},
+                                  {192, 'w', 6, true}, {224, 'w', 8, true}, {kBandEnd, 'g', 0, true}};
+
+// Applies the band of a row of hv vectors to p (the general rule's plan) when there are more rows
+// than SMs; warp plans take 128-thread CTAs (4 rows each).
+void apply_band(const Band *bands, int64_t hv, int64_t rows, int sms, RegPlan *p) {
+    if (rows <= sms || hv > 256) return;
+    const Band *b = bands;
+    while (hv > b->hi) ++b;
+    if (b->kind == 'w') {
+        *p = RegPlan{b->v, 128, true, b->prefetch};
+    } else if (b->kind == 'c') {
+        *p = RegPlan{b->v, (int)round_up64(ceil_div64(hv, b->v), 32), false, b->prefetch};
+    }
+}
+
+// Softmax: rows of up to 512 threads x V vectors in registers (V from row_vec_plan; at 4 vectors
+// no prefetch up to 1024 vectors: measured on GB300 (bf16, HBM-bound rows) 0.92-0.97 of the copy
+// peak for rows of 128..1024 vectors against 0.85-0.93 with it; beyond, prefetch wins), the wide
+// kernel for wider rows, the scalar kernel for rows that cannot be vectorised; many rows of at
+// most 256 vectors by the bands above.
+RegPlan softmax_plan(bool aligned, int64_t width, int64_t rows, int sms, ks_dtype_t dtype) {
+    RegPlan p{0, 0, false, true};
+    if (!aligned) return p;
+    p.v = row_vec_plan(width, &p.block);
+    if (p.v == 0) {
+        p.v = kWideRows;
+        p.block = wide_row_block(width, false);
+    } else if (p.v == 4) {
+        p.prefetch = width > 1024;
+    }
+    apply_band(dtype == KS_DTYPE_F32 ? kSoftmax32 : kSoftmax16, width, rows, sms, &p);
+    return p;
+}
+
+// LayerNorm: register rows (V from row_vec_plan, next row always prefetched: without it the two
+// reductions per row left it at 0.50-0.66 of the copy peak), the staged ring and the wide kernel
+// for many wider rows (layer_norm_dispatch), the scalar kernel for rows that cannot be
+// vectorised; many rows of at most 256 vectors by the bands above.
+RegPlan layer_norm_plan(bool aligned, int64_t hv, int64_t rows, int sms, ks_dtype_t dtype) {
+    RegPlan p{0, 0, false, true};
+    if (!aligned) return p;
+    p.v = row_vec_plan(hv, &p.block);
+    if (p.v == 0) {
+        p.v = kWideRows;
+        p.block = wide_row_block(hv, true);  // at most 512: the kernel's bound
+    }
+    apply_band(dtype == KS_DTYPE_BF16 ? kLayerNormBf16
+               : dtype == KS_DTYPE_F16 ? kLayerNormF16 : kLayerNormF32, hv, rows, sms, &p);
+    return p;
 }
 
 template <typename T>
-cudaError_t softmax_dispatch(int v, int block, void *out, const void *x, int64_t rows,
-                             int64_t width, int sms, cudaStream_t s) {
+cudaError_t softmax_dispatch(RegPlan p, void *out, const void *x, int64_t rows, int64_t width,
+                             int sms, cudaStream_t s) {
     int64_t nr = rows, wd = width;
     void *args[] = {&out, const_cast<void **>(&x), &nr, &wd};
-    const void *f;
-    switch (v) {
-    case 1: f = (const void *)softmax_vec_kernel<T, 1, true>; break;
-    case 2: f = (const void *)softmax_vec_kernel<T, 2, true>; break;
-    case 4:
-        // measured on GB300 (bf16, HBM-bound rows): without prefetch 0.92-0.97 of the copy peak
-        // for rows of 128..1024 vectors against 0.85-0.93 with it; beyond, prefetch wins
-        f = width <= 1024 ? (const void *)softmax_vec_kernel<T, 4, false>
-                          : (const void *)softmax_vec_kernel<T, 4, true>;
-        break;
-    case kWideRows: f = (const void *)softmax_wide_kernel<T, 4>; break;
-    default:
-        f = (const void *)softmax_scalar_kernel<T>;
-        block = (int)round_up64(ceil_div64(width, 8), 32);
-        block = block < 32 ? 32 : (block > 1024 ? 1024 : block);
+    const void *f = nullptr;
+    if (p.warp) {
+        if (32 * (int64_t)p.v < width) return cudaErrorInvalidConfiguration;  // a warp must cover the row
+        switch (p.v) {
+        case 2: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 2, true, true>
+                               : (const void *)softmax_vec_kernel<T, 2, false, true>; break;
+        case 4: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 4, true, true>
+                               : (const void *)softmax_vec_kernel<T, 4, false, true>; break;
+        case 6: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 6, true, true>
+                               : (const void *)softmax_vec_kernel<T, 6, false, true>; break;
+        case 8: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 8, true, true>
+                               : (const void *)softmax_vec_kernel<T, 8, false, true>; break;
+        default: return cudaErrorInvalidConfiguration;
+        }
+    } else {
+        switch (p.v) {
+        case 1: f = (const void *)softmax_vec_kernel<T, 1, true>; break;
+        case 2: f = (const void *)softmax_vec_kernel<T, 2, true>; break;
+        case 4: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 4, true>
+                               : (const void *)softmax_vec_kernel<T, 4, false>; break;
+        case kWideRows: f = (const void *)softmax_wide_kernel<T, 4>; break;
+        default:
+            f = (const void *)softmax_scalar_kernel<T>;
+            p.block = (int)round_up64(ceil_div64(width, 8), 32);
+            p.block = p.block < 32 ? 32 : (p.block > 1024 ? 1024 : p.block);
+        }
     }
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, 0) != cudaSuccess || n < 1) n = 1;
-    int64_t grid = (int64_t)sms * n;
-    if (v == kWideRows && grid > wide_grid_cap(width, sms)) grid = wide_grid_cap(width, sms);
-    grid = grid > rows ? rows : grid;
-    return launch(f, dim3((unsigned)grid), dim3(block), args, s);
+    int64_t grid = reg_grid(f, p, 0, rows, sms);
+    if (p.v == kWideRows && grid > wide_grid_cap(width, sms)) grid = wide_grid_cap(width, sms);
+    return launch(f, dim3((unsigned)grid), dim3(p.block), args, s);
 }
 
 // Bytes of rows in each CTA's LayerNorm ring (a tuning constant, set from a GB300 measurement).
@@ -873,9 +1128,11 @@ const void *layer_norm_pick(int affine, K none, K weight, K bias, K both) {
 }
 
 template <typename T>
-cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, const void *w,
+cudaError_t layer_norm_dispatch(RegPlan p, void *out, const void *x, const void *w,
                                 const void *b, int64_t rows, int64_t hidden, int64_t hv,
                                 float eps, int sms, cudaStream_t s) {
+    int v = p.v, block = p.block;
+    if (p.warp && 32 * (int64_t)v < hv) return cudaErrorInvalidConfiguration;  // a warp must cover the row
     int64_t nr = rows, hd = hidden, hvv = hv;
     float ep = eps;
     const void *f;
@@ -893,7 +1150,7 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
     // 0.76-0.83 of the copy peak against 0.65-0.78, fp32 1024..1792 0.88-0.95 against 0.76-0.86
     // (at 1024 bf16 vectors the ring measured 0.96 against 0.81, so 16-bit rows start above it).
     int stages = 0;
-    if (v == 4 && hv > 512 && rows >= 4 * (int64_t)sms) {
+    if (!p.warp && v == 4 && hv > 512 && rows >= 4 * (int64_t)sms) {
         if (hv < 2048 && hv >= (sizeof(T) == 4 ? 1024 : 1025)) {
             v = kWideRows;
             block = 128;
@@ -906,7 +1163,15 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
                          const_cast<void **>(&b), &nr, &hd, &hvv, &ep, &stages};
     size_t smem = 0;
     const int affine = (w ? kAffineWeight : 0) | (b ? kAffineBias : 0);
-    switch (stages ? 8 : v) {
+    switch (p.warp ? -v : (stages ? 8 : v)) {
+    case -2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0, true>, layer_norm_vec_kernel<T, 2, 1, true>,
+                                    layer_norm_vec_kernel<T, 2, 2, true>, layer_norm_vec_kernel<T, 2, 3, true>); break;
+    case -4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0, true>, layer_norm_vec_kernel<T, 4, 1, true>,
+                                    layer_norm_vec_kernel<T, 4, 2, true>, layer_norm_vec_kernel<T, 4, 3, true>); break;
+    case -6: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 6, 0, true>, layer_norm_vec_kernel<T, 6, 1, true>,
+                                    layer_norm_vec_kernel<T, 6, 2, true>, layer_norm_vec_kernel<T, 6, 3, true>); break;
+    case -8: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 8, 0, true>, layer_norm_vec_kernel<T, 8, 1, true>,
+                                    layer_norm_vec_kernel<T, 8, 2, true>, layer_norm_vec_kernel<T, 8, 3, true>); break;
     case 1: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 1, 0>, layer_norm_vec_kernel<T, 1, 1>,
                                    layer_norm_vec_kernel<T, 1, 2>, layer_norm_vec_kernel<T, 1, 3>); break;
     case 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0>, layer_norm_vec_kernel<T, 2, 1>,
@@ -943,11 +1208,10 @@ cudaError_t layer_norm_dispatch(int v, int block, void *out, const void *x, cons
             cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic) != cudaSuccess)
             return cudaErrorInvalidConfiguration;
     }
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, smem) != cudaSuccess || n < 1) n = 1;
-    int64_t grid = (int64_t)sms * n;
+    p.v = v;
+    p.block = block;
+    int64_t grid = reg_grid(f, p, smem, rows, sms);
     if (v == kWideRows && !stages && grid > wide_grid_cap(hv, sms)) grid = wide_grid_cap(hv, sms);
-    grid = grid > rows ? rows : grid;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(block);
@@ -985,12 +1249,13 @@ ks_status_t ks_silu_and_mul(void *out, const void *x, int64_t rows, int64_t d, k
     int sms = 0;
     if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
     const bool vec = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0 && (d * e) % 16 == 0;
+    const SiluPlan plan = silu_plan(vec, vec ? d * e / 16 : 0, dtype);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce;
     switch (dtype) {
-    case KS_DTYPE_BF16: ce = silu_dispatch<__nv_bfloat16>(vec, out, x, rows, d, sms, s); break;
-    case KS_DTYPE_F16: ce = silu_dispatch<__half>(vec, out, x, rows, d, sms, s); break;
-    default: ce = silu_dispatch<float>(vec, out, x, rows, d, sms, s); break;
+    case KS_DTYPE_BF16: ce = silu_dispatch<__nv_bfloat16>(plan, out, x, rows, d, sms, s); break;
+    case KS_DTYPE_F16: ce = silu_dispatch<__half>(plan, out, x, rows, d, sms, s); break;
+    default: ce = silu_dispatch<float>(plan, out, x, rows, d, sms, s); break;
     }
     if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
     return KS_SUCCESS;
@@ -1011,22 +1276,14 @@ ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, k
     int sms = 0;
     if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
     const bool aligned = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0 && (hidden * e) % 16 == 0;
-    int block = 0, v = 0;
-    int64_t width = hidden;
-    if (aligned) {
-        width = hidden * e / 16;
-        v = row_vec_plan(width, &block);
-        if (v == 0) {
-            v = kWideRows;
-            block = wide_row_block(width, false);
-        }
-    }
+    const int64_t width = aligned ? hidden * e / 16 : hidden;
+    const RegPlan p = softmax_plan(aligned, width, rows, sms, dtype);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce;
     switch (dtype) {
-    case KS_DTYPE_BF16: ce = softmax_dispatch<__nv_bfloat16>(v, block, out, x, rows, width, sms, s); break;
-    case KS_DTYPE_F16: ce = softmax_dispatch<__half>(v, block, out, x, rows, width, sms, s); break;
-    default: ce = softmax_dispatch<float>(v, block, out, x, rows, width, sms, s); break;
+    case KS_DTYPE_BF16: ce = softmax_dispatch<__nv_bfloat16>(p, out, x, rows, width, sms, s); break;
+    case KS_DTYPE_F16: ce = softmax_dispatch<__half>(p, out, x, rows, width, sms, s); break;
+    default: ce = softmax_dispatch<float>(p, out, x, rows, width, sms, s); break;
     }
     if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
     return KS_SUCCESS;
@@ -1053,21 +1310,14 @@ ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const vo
     if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
     const uintptr_t al = (uintptr_t)out | (uintptr_t)x | (uintptr_t)weight | (uintptr_t)bias;
     const bool aligned = (al & 15u) == 0 && (hidden * e) % 16 == 0;
-    int block = 0, v = 0;
     const int64_t hv = hidden * e / 16;
-    if (aligned) {
-        v = row_vec_plan(hv, &block);
-        if (v == 0) {
-            v = kWideRows;
-            block = wide_row_block(hv, true);  // at most 512: the kernel's bound
-        }
-    }
+    const RegPlan p = layer_norm_plan(aligned, hv, rows, sms, dtype);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce;
     switch (dtype) {
-    case KS_DTYPE_BF16: ce = layer_norm_dispatch<__nv_bfloat16>(v, block, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
-    case KS_DTYPE_F16: ce = layer_norm_dispatch<__half>(v, block, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
-    default: ce = layer_norm_dispatch<float>(v, block, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
+    case KS_DTYPE_BF16: ce = layer_norm_dispatch<__nv_bfloat16>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
+    case KS_DTYPE_F16: ce = layer_norm_dispatch<__half>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
+    default: ce = layer_norm_dispatch<float>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
     }
     if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
     return KS_SUCCESS;

@@ -174,6 +174,16 @@ def test_bf16_fused_prefetch_starts_at_1473_vectors():
     for hidden in (15880, 16384):  # 1985, 2048 vectors: the two-pass kernel
         p = plan(1, 32768, hidden, BF16)
         assert (p.kernel, p.vec_per_thread, p.block) == (TWO, 2, 512)
+        p = plan(1, 333, hidden, BF16)  # fewer than 4 rows per SM: the one-pass plan stays
+        assert p.kernel == CTA and p.vec_per_thread == 4 and not (p.flags & NO_PF)
+
+
+def test_fp32_two_pass_switches_need_many_rows():
+    for hidden, rows, want in ((3200, 32768, TWO), (3200, 333, CTA),     # fused, 800 vectors
+                               (6000, 32768, TWO), (6000, 333, CTA)):    # fused, 1500 vectors
+        assert plan(1, rows, hidden, F32).kernel == want, (hidden, rows)
+    assert plan(0, 32768, 6400, F32).kernel == TWO   # plain, 1600 vectors
+    assert plan(0, 333, 6400, F32).kernel == CTA
 
 
 # Many rows of 129..384 vectors: the measured per-bucket table. (op, hidden, dtype) ->

@@ -24,7 +24,11 @@ DT = ["bf16", "fp16", "fp32"]
 
 @pytest.mark.parametrize("dtype", DT)
 @pytest.mark.parametrize("rows,d", [(8, 4096), (512, 4096), (1, 1024), (16, 8192), (128, 1024),
-                                    (3, 7), (5, 1), (33, 1001), (0, 16), (2048, 4096)])
+                                    (3, 7), (5, 1), (33, 1001), (0, 16), (2048, 4096),
+                                    # narrow rows, many of them: the flat walk crosses rows
+                                    # inside a warp and leaves a ragged tail
+                                    (3000, 8), (1000, 64), (777, 520), (20000, 96),
+                                    (4099, 1408)])
 def test_silu_and_mul(cuda_device, dtype, rows, d):
     dt = synth.dtype_of(dtype)
     x = synth.cast(synth.normal_np((rows, 2 * d), 801, std=2.0), dt)
@@ -231,3 +235,68 @@ def test_layer_norm_rows_wider_than_registers(cuda_device, dtype, rows, h, affin
     _ln_check(y, ref, dt, h, f"layer_norm wide {dtype} [{rows},{h}] affine={affine}")
     st, flags = _abi.ks_device_faults(clear=False)
     assert st == _abi.KS_SUCCESS and flags == 0
+
+
+# ------------------------------------------- plan bands: warp rows and the SwiGLU launch shapes
+
+# Row widths in 16-byte vectors at the edges of the measured plan bands for many rows (warp rows
+# at 2, 4, 6 or 8 vectors per lane, CTA rows, the general rule), for every dtype.
+BAND_HV = [16, 32, 33, 44, 45, 52, 53, 63, 64, 65, 72, 80, 81, 127, 128, 129, 168, 169, 176, 177,
+           192, 193, 216, 217, 224, 225, 256, 257]
+
+
+def _elems(dt, hv):
+    return hv * (4 if dt == torch.float32 else 8)
+
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("hv", BAND_HV)
+def test_softmax_at_plan_band_edges(cuda_device, dtype, hv):
+    """Many rows (1001: more than SMs, not a multiple of a CTA's 4 warp rows) at each band edge;
+    also one row with NaN, +inf, all -inf and masked entries, which the warp kernels must treat
+    as the CTA kernels do."""
+    dt = synth.dtype_of(dtype)
+    h = _elems(dt, hv)
+    x = synth.normal_np((1001, h), 810, std=3.0)
+    inf, nan = float("inf"), float("nan")
+    x[5, 1] = -inf; x[5, 3] = -inf         # masked entries
+    x[6, 2] = nan                            # NaN row
+    x[7, 0] = inf                            # +inf row
+    x[8, :] = -inf                           # all -inf row
+    # torch's cast keeps the infinities (the input recipe's fp16 cast saturates them)
+    xt = torch.tensor(x, dtype=torch.float32).to(dt)
+    y = ks.softmax(xt.to(cuda_device)).cpu()
+    ref, _ = oracle.softmax(xt)
+    assert torch.equal(torch.isnan(y), torch.isnan(ref))
+    assert torch.isnan(y[6:9]).all() and (y[5, [1, 3]] == 0).all()
+    fin = ~torch.isnan(ref).any(dim=1)
+    compare_output(y[fin], ref[fin], dt, h, f"softmax band {dtype} [1001,{h}]")
+
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("hv", BAND_HV)
+@pytest.mark.parametrize("affine", AFFINE)
+def test_layer_norm_at_plan_band_edges(cuda_device, dtype, hv, affine):
+    dt = synth.dtype_of(dtype)
+    h = _elems(dt, hv)
+    x = synth.cast(synth.normal_np((1001, h), 811) + 0.25, dt)
+    x[9] = 0.75  # a constant row
+    w, b = _affine(affine, h, dt, 812)
+    y = ks.layer_norm(x.to(cuda_device), _dev(w, cuda_device), _dev(b, cuda_device), 1e-5).cpu()
+    ref, _ = oracle.layer_norm(x, w, b, 1e-5)
+    _ln_check(y, ref, dt, h, f"layer_norm band {dtype} [1001,{h}] affine={affine}")
+
+
+@pytest.mark.parametrize("dtype", DT)
+@pytest.mark.parametrize("dv", [64, 159, 160, 161, 191, 192, 193, 256, 287, 288, 447, 448, 512,
+                                1024, 1280, 2048])
+def test_silu_and_mul_at_plan_band_edges(cuda_device, dtype, dv):
+    """SwiGLU on many rows at the edges of its launch shapes: the flat walk, and the row kernel
+    with its block fitted to the row (at most 256 or 96 threads)."""
+    dt = synth.dtype_of(dtype)
+    d = _elems(dt, dv)
+    rows = 700 if dv <= 512 else 150
+    x = synth.cast(synth.normal_np((rows, 2 * d), 813, std=2.0), dt)
+    y = ks.silu_and_mul(x.to(cuda_device)).cpu()
+    ref, _ = oracle.silu_and_mul(x)
+    compare_output(y, ref, dt, 8, f"silu_and_mul band {dtype} [{rows},{d}]")
