@@ -22,6 +22,7 @@
 
 #include <cmath>
 #include <mutex>
+#include <type_traits>
 
 #include "ks_kernels.cuh"
 
@@ -179,11 +180,11 @@ __global__ void __launch_bounds__(256) silu_mul_rows_kernel(void *out, const voi
 }
 
 // Flat: the output [rows, dv] walked as one run of rows * dv vectors, grid-stride, two vectors
-// per thread per iteration, so every thread has work whatever the row width (a 256-thread block laid across a row of
-// 64 vectors left 7 of its 8 warps idle: bf16 d = 512 ran at 0.54 of the copy peak). It spends
-// more integer instructions per vector than the row-structured kernel. Output vector i is input
-// vector i + row * dv of the gate half (row = i / dv) and dv further on of the up half; each
-// thread divides once, then carries (row, column) forward by the stride.
+// per thread per iteration, so every thread has work whatever the row width (a 256-thread block
+// laid across a row of 64 vectors left 7 of its 8 warps idle: bf16 d = 512 ran at 0.54 of the
+// copy peak). It spends more integer instructions per vector than the row-structured kernel.
+// Output vector i is input vector i + row * dv of the gate half (row = i / dv) and dv further on
+// of the up half; each thread divides once, then carries (row, column) forward by the stride.
 template <typename T>
 __global__ void __launch_bounds__(256) silu_mul_flat_kernel(void *out, const void *x, int64_t rows,
                                                            int64_t dv) {
@@ -271,8 +272,8 @@ __global__ void __launch_bounds__(256) silu_mul_scalar_kernel(void *out, const v
 // NaN or +inf in the row still makes the sum, and so every output, NaN, and a row of only -inf
 // still gets max -inf and z = NaN, so the contract's non-finite rules hold.
 template <typename T, int V, bool kPrefetch, bool kWarp = false>
-__global__ void __launch_bounds__(kWarp ? 128 : 512) softmax_vec_kernel(void *out, const void *x, int64_t rows,
-                                                          int64_t hv) {
+__global__ void __launch_bounds__(kWarp ? 128 : 512)
+    softmax_vec_kernel(void *out, const void *x, int64_t rows, int64_t hv) {
     using E = Elem<T>;
     constexpr int P = E::kPerVec / 2;
     // packed pair instructions (bit-identical) where they measured faster on GB300: bf16 without
@@ -338,7 +339,8 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512) softmax_vec_kernel(void *ou
                 }
             }
         }
-        const float sum = team_sum<kWarp>(__fadd_rn(__fadd_rn(s[0].x, s[0].y), __fadd_rn(s[1].x, s[1].y)), red, slot);
+        const float sum = team_sum<kWarp>(
+            __fadd_rn(__fadd_rn(s[0].x, s[0].y), __fadd_rn(s[1].x, s[1].y)), red, slot);
         // e / sum as e * (1 / sum): one correctly rounded reciprocal per row, then a product
         // per element (within 1 fp32 ulp of the quotient)
         const float inv = __frcp_rn(sum);
@@ -467,12 +469,30 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512) layer_norm_vec_kernel(void 
     const int teams = kWarp ? (int)(blockDim.x >> 5) : 1;
     const int64_t stride = (int64_t)gridDim.x * teams;
     const float h = (float)hidden;
+    // Weight and bias slices: in registers for every row a thread visits, except bf16 warp rows
+    // of up to 6 vectors a lane, whose CTA keeps one copy in shared memory (every warp of the CTA
+    // needs the same slices; filled once, before any warp starts its rows). That frees 8
+    // registers per vector a lane holds (bf16, 4 vectors, weight and bias: 136 -> 80) and measured
+    // on GB300 0.76 -> 0.94 of the copy peak at 96 vectors, 0.74 -> 0.94 at 160, 0.80 -> 0.92 at
+    // 192; for bf16 at 8 vectors and for fp16 and fp32, whose rows already held more warps, it
+    // measured up to 8 points slower.
+    constexpr bool kSmemAffine = kWarp && std::is_same<T, __nv_bfloat16>::value && V <= 6;
     uint4 wv[V], bv[V];
+    __shared__ uint4 sw[kSmemAffine && kW ? 32 * V : 1], sb[kSmemAffine && kB ? 32 * V : 1];
+    if (kSmemAffine) {
+        const int n = hv < 32 * V ? (int)hv : 32 * V;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            if (kW) sw[i] = __ldg(static_cast<const uint4 *>(w) + i);
+            if (kB) sb[i] = __ldg(static_cast<const uint4 *>(b) + i);
+        }
+        __syncthreads();
+    } else {
 #pragma unroll
-    for (int k = 0; k < V; ++k) {
-        const int64_t c = t + (int64_t)k * g;
-        wv[k] = (kW && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
-        bv[k] = (kB && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            wv[k] = (kW && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
+            bv[k] = (kB && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     int slot = 0;
     int64_t row = (int64_t)blockIdx.x * teams + (kWarp ? (int)(threadIdx.x >> 5) : 0);
@@ -504,7 +524,11 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512) layer_norm_vec_kernel(void 
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            if (c < hv) __stcs(og + row * hv + c, ln_out<T, kAffine>(xv[k], wv[k], bv[k], rstd, shift));
+            if (c < hv) {
+                const uint4 wk = kSmemAffine ? (kW ? sw[c] : make_uint4(0u, 0u, 0u, 0u)) : wv[k];
+                const uint4 bk = kSmemAffine ? (kB ? sb[c] : make_uint4(0u, 0u, 0u, 0u)) : bv[k];
+                __stcs(og + row * hv + c, ln_out<T, kAffine>(xv[k], wk, bk, rstd, shift));
+            }
         }
 #pragma unroll
         for (int k = 0; k < V; ++k) xv[k] = nxt[k];
