@@ -725,6 +725,30 @@ def run_e2e(dev, args, R, H, eps) -> dict:
                    f"{args.e2e_workspace_mb} MiB device workspace)"}
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model name, best effort (/proc/cpuinfo on x86; on Arm hosts, whose cpuinfo
+    names no model, the implementer and part numbers), else the platform's processor string."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key, val = key.strip().lower(), val.strip()
+                if key and val and key not in fields:
+                    fields[key] = val
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu implementer" in fields and "cpu part" in fields:
+        parts = {("0x41", "0xd4f"): "Arm Neoverse V2", ("0x41", "0xd40"): "Arm Neoverse V1",
+                 ("0x41", "0xd0c"): "Arm Neoverse N1", ("0x41", "0xd49"): "Arm Neoverse N2"}
+        key = (fields["cpu implementer"].lower(), fields["cpu part"].lower())
+        return parts.get(key, f"Arm CPU (implementer {key[0]}, part {key[1]})")
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args) -> dict:
     """The oracle, as it stands (single-threaded C), on the first rows of the same batch until
     about `cpu_seconds` of work is done; its outputs are also compared with the GPU's."""
@@ -760,7 +784,7 @@ def cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args) -> dict:
         "baseline": {"value": nb / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                      "sample": f"first {done} of {R} rows of both ops ([{done},{H}] bf16), "
                                f"{secs:.1f} s single-threaded",
-                     "host_cores_total": os.cpu_count()},
+                     "host_cores_total": os.cpu_count(), "host_cpu": host_cpu_model()},
         "parity": {"rows_checked": done, "max_ulp": max_ulp, "residual_bit_exact": res_ok,
                    "within_tolerance": tol_ok, "ok": bool(res_ok and tol_ok and max_ulp <= 1)},
     }
@@ -810,7 +834,8 @@ def run_reference(args) -> int:
         "data": "synthetic (seeded N(0,1), host draw)",
         "config": {"workload": workload(R, H), "rows": R, "hidden": H, "eps": eps},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{rows} of {R} rows of both ops per step"},
+                         "sample": f"{rows} of {R} rows of both ops per step",
+                         "host_cores_total": os.cpu_count(), "host_cpu": host_cpu_model()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))
     return 0

@@ -111,3 +111,9 @@ def test_recorded_traffic_only_for_the_recorded_shape():
     assert bench.workload(bench.FULL_ROWS, bench.FULL_HIDDEN).startswith("large prefill bf16")
     assert "larger than L2" in bench.l2_note(bench.FULL_ROWS, bench.FULL_HIDDEN)
     assert "not a bench figure" in bench.l2_note(1024, 1024)
+
+
+def test_host_cpu_model_names_the_cpu():
+    import bench
+    name = bench.host_cpu_model()
+    assert isinstance(name, str) and name.strip()
