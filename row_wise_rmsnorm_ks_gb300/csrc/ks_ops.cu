@@ -21,8 +21,11 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <type_traits>
+#include <utility>
 
 #include "ks_kernels.cuh"
 
@@ -849,6 +852,57 @@ __global__ void __launch_bounds__(512) layer_norm_wide_kernel(void *out, const v
 int g_sm_count[64];
 std::once_flag g_sm_once[64];
 
+// Per-device launch facts, cached: without the cache every launch would repeat the same
+// occupancy query (and, for the staged LayerNorm ring, three attribute calls), host work that
+// adds to small launches' latency.
+std::mutex g_launch_facts_mu;
+std::map<std::tuple<int, const void *, int, size_t>, int> g_occupancy;  // CTAs per SM
+std::map<std::pair<int, const void *>, int> g_max_dynamic_smem;  // set on the kernel already
+
+// CTAs of kernel f resident per SM at `block` threads and `smem` bytes of dynamic shared memory
+// on the current device; 1 when the query fails (not cached then).
+int cached_occupancy(const void *f, int block, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    const auto key = std::make_tuple(dev, f, block, smem);
+    {
+        std::lock_guard<std::mutex> lock(g_launch_facts_mu);
+        const auto it = g_occupancy.find(key);
+        if (it != g_occupancy.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, block, smem) != cudaSuccess || n < 1)
+        return 1;
+    std::lock_guard<std::mutex> lock(g_launch_facts_mu);
+    g_occupancy.emplace(key, n);
+    return n;
+}
+
+// Lets kernel f use the largest dynamic shared memory the current device takes beside its static
+// shared memory (once per device and kernel); false if `smem` does not fit or a call fails.
+bool allow_dynamic_smem(const void *f, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const auto key = std::make_pair(dev, f);
+    {
+        std::lock_guard<std::mutex> lock(g_launch_facts_mu);
+        const auto it = g_max_dynamic_smem.find(key);
+        if (it != g_max_dynamic_smem.end()) return (int64_t)smem <= it->second;
+    }
+    int optin = 0;
+    cudaFuncAttributes fa;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaFuncGetAttributes(&fa, f) != cudaSuccess)
+        return false;
+    const int max_dynamic = optin - (int)fa.sharedSizeBytes;
+    if ((int64_t)smem > max_dynamic ||
+        cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic) != cudaSuccess)
+        return false;
+    std::lock_guard<std::mutex> lock(g_launch_facts_mu);
+    g_max_dynamic_smem.emplace(key, max_dynamic);
+    return true;
+}
+
 ks_status_t sm_count(int *out) {
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
@@ -962,9 +1016,7 @@ cudaError_t silu_dispatch(SiluPlan plan, void *out, const void *x, int64_t rows,
         // a persistent grid of as many 256-thread CTAs as are resident at once (fewer if the
         // vectors run out), two vectors per thread per iteration
         const void *f = (const void *)silu_mul_flat_kernel<T>;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, 256, 0) != cudaSuccess || n < 1)
-            n = 1;
+        const int n = cached_occupancy(f, 256, 0);
         int64_t grid = ceil_div64(rows * dd, 512);
         grid = grid > (int64_t)sms * n ? (int64_t)sms * n : grid;
         return launch(f, dim3((unsigned)grid), dim3(256), args, s);
@@ -1009,9 +1061,7 @@ struct RegPlan {
 // Grid of a register-row launch: as many CTAs as are resident at once, no more than the rows
 // need.
 int64_t reg_grid(const void *f, const RegPlan &p, size_t smem, int64_t rows, int sms) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, p.block, smem) != cudaSuccess || n < 1)
-        n = 1;
+    const int n = cached_occupancy(f, p.block, smem);
     const int64_t per_cta = p.warp ? p.block / 32 : 1;
     const int64_t need = ceil_div64(rows, per_cta);
     const int64_t grid = (int64_t)sms * n;
@@ -1219,19 +1269,8 @@ cudaError_t layer_norm_dispatch(RegPlan p, void *out, const void *x, const void 
         block = (int)round_up64(ceil_div64(hidden, 8), 32);
         block = block < 32 ? 32 : (block > 1024 ? 1024 : block);
     }
-    if (smem > 0) {
-        // allow the largest ring the device takes beside the kernel's static shared memory
-        int dev = 0, optin = 0;
-        cudaFuncAttributes fa;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
-            cudaFuncGetAttributes(&fa, f) != cudaSuccess)
-            return cudaErrorInvalidConfiguration;
-        const int max_dynamic = optin - (int)fa.sharedSizeBytes;
-        if ((int64_t)smem > max_dynamic ||
-            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic) != cudaSuccess)
-            return cudaErrorInvalidConfiguration;
-    }
+    // allow the largest ring the device takes beside the kernel's static shared memory
+    if (smem > 0 && !allow_dynamic_smem(f, smem)) return cudaErrorInvalidConfiguration;
     p.v = v;
     p.block = block;
     int64_t grid = reg_grid(f, p, smem, rows, sms);
