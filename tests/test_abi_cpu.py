@@ -541,3 +541,42 @@ def test_pointers_not_aligned_to_the_element_are_rejected(dtype, off):
     assert _abi.ks_layer_norm(a + off, b, w, c, rows, h, 1e-5, dtype, None) == E
     assert _abi.ks_layer_norm(a, b, w + off, None, rows, h, 1e-5, dtype, None) == E
     assert _abi.ks_layer_norm(a, b, None, c + off, rows, h, 1e-5, dtype, None) == E
+
+
+@pytest.mark.parametrize("dtype", [BF16, F16, F32])
+@pytest.mark.parametrize("op", [0, 1])
+def test_every_width_gets_a_valid_plan(dtype, op):
+    """Every row width from 1 to 2100 16-byte vectors (and an element more, which cannot be
+    vectorised), at row counts around the heuristic's thresholds (SMs, 4 x SMs): the plan obeys
+    the rules the planned entry points enforce, so the default path never builds a launch the
+    library would refuse."""
+    per = 4 if dtype == F32 else 8
+    for rows in (1, 19, 152, 153, 607, 608, 65536):
+        for hv in range(1, 2101):
+            for hidden in (hv * per, hv * per + 1):
+                p = plan(op, rows, hidden, dtype, bps=4)
+                assert p.block % 32 == 0 and 32 <= p.block <= 1024, (rows, hidden, p.as_dict())
+                assert p.grid >= 1
+                if hidden % per:
+                    assert p.kernel == _abi.KS_KERNEL_SCALAR
+                    continue
+                if p.kernel == WARP:
+                    assert p.vec_per_thread in (1, 2, 4, 6, 8) and p.block <= 256
+                    assert 32 * p.vec_per_thread >= hv, (rows, hidden)
+                elif p.kernel == CTA:
+                    assert p.vec_per_thread in (2, 4)
+                    assert p.block <= (1024 if p.vec_per_thread == 2 else 512)
+                    assert p.block * p.vec_per_thread >= hv, (rows, hidden)
+                elif p.kernel == TWO:
+                    assert p.vec_per_thread in (2, 4) and p.block <= 1024
+                elif p.kernel == BULK:
+                    assert p.vec_per_thread == 4 and p.block <= 512 and 1 <= p.stages <= 16
+                    assert p.block * 4 >= hv and p.smem_bytes <= 226 * 1024
+                    assert p.cluster in (0, 1)
+                elif p.kernel == _abi.KS_KERNEL_CLUSTER_ROW:
+                    assert 2 <= p.cluster <= 8 and p.grid % p.cluster == 0
+                    assert p.vec_per_thread in (1, 2, 4) and p.block <= 512
+                    slice_ = -(-hv // p.cluster)
+                    assert p.block * p.vec_per_thread >= slice_ and (p.cluster - 1) * slice_ < hv
+                else:
+                    raise AssertionError(f"unexpected kernel {p.kernel} for {rows} x {hidden}")
