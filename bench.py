@@ -749,6 +749,34 @@ def host_cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
+def oracle_all_cores(host_in, rows: int, H: int, eps: float) -> dict:
+    """The same oracle on the first `rows` rows of both ops, the rows split evenly over every
+    host core (one thread each; the C oracle keeps no shared state and its calls release the
+    interpreter lock). A second, separately labelled CPU figure beside the single-threaded
+    baseline."""
+    import concurrent.futures as cf
+
+    import oracle
+
+    n = max(1, min(os.cpu_count() or 1, rows))
+    per = -(-rows // n)
+    chunks = [slice(i, min(rows, i + per)) for i in range(0, rows, per)]
+
+    def work(sl):
+        oracle.rms_norm(host_in["x"][sl], host_in["w"], eps)
+        oracle.fused_add_rms_norm(host_in["xf"][sl], host_in["r"][sl], host_in["w"], eps)
+
+    oracle.rms_norm(host_in["x"][:1], host_in["w"], eps)  # load the library before the threads
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(len(chunks)) as ex:
+        list(ex.map(work, chunks))
+    secs = time.perf_counter() - t0
+    nb = algorithmic_bytes("rms_norm", rows, H, 2) + algorithmic_bytes("fused_add_rms_norm", rows, H, 2)
+    return {"value": nb / secs / 1e9, "unit": "GB/s", "cores": len(chunks),
+            "kind": "oracle, rows split over threads",
+            "sample": f"first {rows} rows of both ops ([{rows},{H}] bf16), {secs:.2f} s"}
+
+
 def cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args) -> dict:
     """The oracle, as it stands (single-threaded C), on the first rows of the same batch until
     about `cpu_seconds` of work is done; its outputs are also compared with the GPU's."""
@@ -784,7 +812,8 @@ def cpu_baseline_and_parity(host_in, gpu_out, R, H, eps, args) -> dict:
         "baseline": {"value": nb / secs / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                      "sample": f"first {done} of {R} rows of both ops ([{done},{H}] bf16), "
                                f"{secs:.1f} s single-threaded",
-                     "host_cores_total": os.cpu_count(), "host_cpu": host_cpu_model()},
+                     "host_cores_total": os.cpu_count(), "host_cpu": host_cpu_model(),
+                     "all_cores": oracle_all_cores(host_in, done, H, eps)},
         "parity": {"rows_checked": done, "max_ulp": max_ulp, "residual_bit_exact": res_ok,
                    "within_tolerance": tol_ok, "ok": bool(res_ok and tol_ok and max_ulp <= 1)},
     }

@@ -117,3 +117,17 @@ def test_host_cpu_model_names_the_cpu():
     import bench
     name = bench.host_cpu_model()
     assert isinstance(name, str) and name.strip()
+
+
+def test_oracle_all_cores_figure():
+    """The all-cores CPU figure runs the oracle on row slices in threads; it must cover the
+    requested rows and report the threads it used."""
+    import bench
+    from row_wise_rmsnorm_ks_gb300 import synth
+    R, H = 40, 256
+    x = synth.cast(synth.normal_np((R, H), 5), "bf16")
+    r = synth.cast(synth.normal_np((R, H), 6), "bf16")
+    w = synth.weight(H, "bf16")
+    d = bench.oracle_all_cores({"x": x, "xf": x.clone(), "r": r, "w": w}, R, H, 1e-5)
+    assert d["value"] > 0 and 1 <= d["cores"] <= min(R, os.cpu_count())
+    assert d["sample"].startswith(f"first {R} rows")
