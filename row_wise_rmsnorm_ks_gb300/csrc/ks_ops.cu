@@ -102,28 +102,40 @@ __device__ __forceinline__ float rcp_sfu(float v) {
     return r;
 }
 
-// Softmax numerators for a pair of elements: fp32 outputs e^(v - m) by expf; 16-bit outputs
-// 2^(v log2(e) + bias) with bias = 64 - m log2(e) (e^(v - m) * 2^64; see softmax_vec_kernel).
+// Softmax numerators for a pair of elements. Both forms first take the contract's FP32 difference
+// z = v - m (as v + (-m): the same IEEE operation), so z is bitwise the contract's whatever the
+// magnitude of m. fp32 outputs: e^z by expf. 16-bit outputs: e^z * 2^64 = 2^(z log2(e) + 64), one
+// FMA and one SFU op; the 2^64 cancels in e / sum and keeps every exp above 2^-190 normal
+// (smaller ones are below any fp32 output anyway). Folding -m log2(e) into one rounded bias
+// instead loses the row once |m log2(e)| passes 2^31: that bias's rounding error alone then
+// exceeds the 64 of exponent headroom.
 template <typename T, bool kPair>
-__device__ __forceinline__ float2 softmax_exp_pair(float2 v, float m, float bias) {
+__device__ __forceinline__ float2 softmax_exp_pair(float2 v, float neg_m) {
     if constexpr (sizeof(T) == 4) {
-        return make_float2(expf(__fsub_rn(v.x, m)), expf(__fsub_rn(v.y, m)));
+        return make_float2(expf(__fadd_rn(v.x, neg_m)), expf(__fadd_rn(v.y, neg_m)));
     } else {
-        const float2 z = pair_fma<kPair>(v, make_float2(kLog2e, kLog2e), make_float2(bias, bias));
-        return make_float2(ex2_sfu(z.x), ex2_sfu(z.y));
+        const float2 z = pair_add<kPair>(v, make_float2(neg_m, neg_m));
+        const float2 t = pair_fma<kPair>(z, make_float2(kLog2e, kLog2e), make_float2(64.0f, 64.0f));
+        return make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
     }
 }
 
-// (g * sigmoid(g)) * up with sigmoid(g) = 1 / (1 + e^-g).
+// (g * sigmoid(g)) * up with sigmoid(g) = 1 / (1 + e^-g), the products in the contract's order,
+// so no intermediate is larger than the contract's own.
 //  fp32 outputs: e^-g by expf, the correctly rounded reciprocal (bitwise the IEEE quotient).
-//  16-bit outputs: g * up / (1 + e^-g) on the SFU, everything scaled by 2^-64 so that neither
-//  e^-g * 2^-64 nor the reciprocal of (1 + e^-g) * 2^-64 leaves the normal range for any
-//  finite gate (the flush-to-zero SFU ops then lose nothing a 16-bit output can show):
-//  t = (-g) log2(e) - 64, den' = 2^t + 2^-64, out = ((g * up) * rcp(den')) * 2^-64.
+//  16-bit outputs: the sigmoid on the SFU. Its flush-to-zero ex2 and rcp would lose sigmoids
+//  below 2^-126 (gates in [-88.7, -87.3]), which a large `up` still carries into a 16-bit
+//  output, so the reciprocal is taken of den' = (1 + e^-g) * 2^-64 = 2^(-g log2(e) - 64) + 2^-64,
+//  which is normal for every gate that matters, and scaled back by an IEEE multiply (subnormal
+//  results kept): sigmoid = rcp(den') * 2^-64 <= 1. Where e^-g overflows FP32 (-g log2(e) >=
+//  128) the contract's sigmoid is 1/(1 + inf) = 0 exactly, and so is this one; a NaN gate keeps
+//  the NaN through g * 0.
 template <typename T>
 __device__ __forceinline__ float silu_mul(float g, float up) {
-    const float den = __fadd_rn(ex2_sfu(__fmaf_rn(-g, kLog2e, -64.0f)), kTwoPowM64);
-    return __fmul_rn(__fmul_rn(__fmul_rn(g, up), rcp_sfu(den)), kTwoPowM64);
+    const float t = __fmul_rn(-g, kLog2e);
+    const float den = __fadd_rn(ex2_sfu(__fadd_rn(t, -64.0f)), kTwoPowM64);
+    const float sig = t < 128.0f ? __fmul_rn(rcp_sfu(den), kTwoPowM64) : 0.0f;
+    return __fmul_rn(__fmul_rn(g, sig), up);
 }
 template <>
 __device__ __forceinline__ float silu_mul<float>(float g, float up) {
@@ -324,11 +336,9 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
             }
         }
         m = team_max<kWarp>(m, red, slot);
-        // 16-bit outputs: e_j * 2^64 = 2^(x_j log2(e) + (64 - m log2(e))), one FMA and one SFU op
-        // per element; the 2^64 cancels in e_j / sum and keeps every exp above 2^-190 normal
-        // (smaller ones are below any fp32 output anyway). For m = +-inf or NaN the bias is
-        // -inf/+inf/NaN, which gives NaN rows exactly as the formula does.
-        const float bias = __fmaf_rn(-m, kLog2e, 64.0f);
+        // For m = +-inf or NaN, z is NaN or -inf where the formula's is, which gives the
+        // contract's NaN rows and masked entries.
+        const float neg_m = -m;
         // four running sums: element e feeds lane e % 2 of s[(e / 2) % 2]
         float2 s[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
@@ -337,7 +347,7 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
             if (c < hv) {
 #pragma unroll
                 for (int i = 0; i < P; ++i) {
-                    f[k][i] = softmax_exp_pair<T, kPair>(f[k][i], m, bias);
+                    f[k][i] = softmax_exp_pair<T, kPair>(f[k][i], neg_m);
                     s[i & 1] = pair_add<kPair>(s[i & 1], f[k][i]);
                 }
             }
@@ -734,7 +744,7 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
             }
         }
         m = cta_max(m, red, slot);
-        const float bias = __fmaf_rn(-m, kLog2e, 64.0f);  // see softmax_vec_kernel
+        const float neg_m = -m;
         float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
         for (int64_t c0 = t; c0 < hv; c0 += chunk) {
             uint4 v[U];
@@ -750,7 +760,7 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
                     E::unpack2(v[u], f);
 #pragma unroll
                     for (int i = 0; i < P; ++i)
-                        s2[i & 1] = pair_add<kPair>(s2[i & 1], softmax_exp_pair<T, kPair>(f[i], m, bias));
+                        s2[i & 1] = pair_add<kPair>(s2[i & 1], softmax_exp_pair<T, kPair>(f[i], neg_m));
                 }
             }
         }
@@ -772,7 +782,7 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
                     float2 f[P];
                     E::unpack2(v[u], f);
 #pragma unroll
-                    for (int i = 0; i < P; ++i) f[i] = pair_mul<kPair>(softmax_exp_pair<T, kPair>(f[i], m, bias), inv2);
+                    for (int i = 0; i < P; ++i) f[i] = pair_mul<kPair>(softmax_exp_pair<T, kPair>(f[i], neg_m), inv2);
                     __stcs(orow + c, E::pack2(f));
                 }
             }
