@@ -253,9 +253,12 @@ int64_t ks_host_chunk_rows(int32_t op, int64_t hidden, ks_dtype_t dtype, int64_t
  * 2M bf16/fp16 or 1M fp32 elements); wider rows return KS_ERR_INVALID_ARGUMENT, launching
  * nothing. Any number of rows is processed, in chunks.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture. All calls on a device
- * share the one array and it keeps the last call's contents (nothing in it needs to start at
- * zero); calls whose GPU work overlaps would race on it, so order them, e.g. on one stream.
+ * that device current (a lookup that fails is not kept: the next call tries again); make that
+ * first call before any stream capture. All calls on a device share the one array and it keeps
+ * the last call's contents (nothing in it needs to start at zero); calls whose GPU work overlaps
+ * would race on it, so order them, e.g. on one stream. The library's own per-device copy and
+ * kernel streams already queue each reuse of a third of the array after the previous copy out
+ * of it, so consecutive calls of one process, from any of its streams, do not overlap there.
  */
 ks_status_t ks_fused_add_rms_norm_host_noalloc(void *x, void *residual, const void *weight,
                                                int64_t rows, int64_t hidden, float eps,

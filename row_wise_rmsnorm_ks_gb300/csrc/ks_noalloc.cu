@@ -11,8 +11,8 @@
 // which loads this library holds until the process exits. Host code cannot use the array's name
 // as a device address (on the host it names a shadow variable), so the first call on each device
 // asks the runtime for the real address with cudaGetSymbolAddress, with that device current, and
-// keeps it. That first call should therefore come before any stream capture. Nothing here calls
-// cudaMalloc, cudaFree or any other allocating routine.
+// keeps it once the lookup succeeds. That first call should therefore come before any stream
+// capture. Nothing here calls cudaMalloc, cudaFree or any other allocating routine.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -29,10 +29,12 @@ constexpr int64_t kScratchBytes = 24ll << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
+// The scratch array's device address per device, looked up under the mutex until a lookup
+// succeeds: a failed lookup (say, an error left pending by earlier work on the device) is not
+// kept, so a later call tries again.
 struct ScratchSlot {
-    std::once_flag once;
+    std::mutex mu;
     void *ptr = nullptr;
-    cudaError_t err = cudaSuccess;
 };
 ScratchSlot g_scratch[kMaxDevices];
 
@@ -52,6 +54,9 @@ extern "C" ks_status_t ks_fused_add_rms_norm_host_noalloc(void *x, void *residua
     if (rows < 0) return fail(KS_ERR_INVALID_ARGUMENT, "rows must be >= 0 (got %lld)", (long long)rows);
     if (!std::isfinite(eps) || !(eps > 0.0f))
         return fail(KS_ERR_INVALID_ARGUMENT, "eps must be finite and > 0 (got %g)", (double)eps);
+    if (hidden > INT64_MAX / (2 * e))
+        return fail(KS_ERR_INVALID_ARGUMENT, "hidden %lld times twice the element size overflows int64",
+                    (long long)hidden);
     if (host_chunk_rows(true, hidden, e, kScratchBytes) < 1)
         return fail(KS_ERR_INVALID_ARGUMENT,
                     "hidden %lld is too wide: one row of x and one of residual (%lld bytes) do not "
@@ -62,21 +67,31 @@ extern "C" ks_status_t ks_fused_add_rms_norm_host_noalloc(void *x, void *residua
     if (misaligned(e, x, residual, weight))
         return fail(KS_ERR_INVALID_ARGUMENT, "a pointer is not aligned to the %d-byte element", e);
 
-    // Set-up, once per device, with that device current: the scratch array's device address.
+    // Set-up, once per device (until it succeeds), with that device current: the scratch array's
+    // device address.
     int dev = 0;
     cudaError_t ce = cudaGetDevice(&dev);
     if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
     if (dev < 0 || dev >= kMaxDevices) return fail(KS_ERR_CUDA, "device ordinal %d out of range", dev);
     ScratchSlot &slot = g_scratch[dev];
-    std::call_once(slot.once, [&] {
-        slot.err = cudaGetSymbolAddress(&slot.ptr, g_noalloc_scratch);
-        if (slot.err != cudaSuccess) (void)cudaGetLastError();
-    });
-    if (slot.err != cudaSuccess || !slot.ptr)
-        return fail(KS_ERR_CUDA, "locating the built-in scratch: %s", cudaGetErrorString(slot.err));
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(slot.mu);
+        if (!slot.ptr) {
+            void *p = nullptr;
+            ce = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (ce != cudaSuccess || !p) {
+                (void)cudaGetLastError();
+                return fail(KS_ERR_CUDA, "locating the built-in scratch: %s",
+                            cudaGetErrorString(ce != cudaSuccess ? ce : cudaErrorInvalidSymbol));
+            }
+            slot.ptr = p;
+        }
+        scratch = slot.ptr;
+    }
 
     // The staged path with the built-in scratch as its workspace. Each chunk's rows are copied
     // into a slot before the kernel reads them, so nothing in the scratch needs to start at zero.
-    return run_host(true, x, x, residual, weight, rows, hidden, eps, dtype, slot.ptr,
+    return run_host(true, x, x, residual, weight, rows, hidden, eps, dtype, scratch,
                     kScratchBytes, stream);
 }
