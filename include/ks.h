@@ -128,8 +128,8 @@ typedef struct ks_plan {
     int32_t smem_bytes;     /* staged kernel: dynamic shared memory per CTA (else 0) */
     int32_t flags;          /* KS_PLAN_* bits below */
     int32_t cluster;        /* CTAs per cluster, one cluster per row: the cluster-row kernel
-                               (2..8), or the staged kernel split over a cluster (2..8; 0 or 1:
-                               one CTA per row); 0 for the other kernels */
+                               (2..8), or the staged or two-pass kernel split over a cluster
+                               (2..8; 0 or 1: one CTA per row); 0 for the other kernels */
 } ks_plan_t;
 
 /* Plan flags. KS_PLAN_NO_PREFETCH: the register kernels (warp and CTA rows) load each row when
@@ -158,7 +158,10 @@ enum {
                                   vectors (sum of squares, then outputs; the second pass from
                                   L2), vec_per_thread (2 or 4) vectors per thread in flight per
                                   step; the grid is capped so the rows in flight fit in L2,
-                                  down to one CTA per SM */
+                                  down to one CTA per SM. With cluster >= 2 each row is split
+                                  over a cluster: CTA q runs both passes on its slice of
+                                  ceil(hv / cluster) vectors and the slice sums meet in
+                                  distributed shared memory, one cluster barrier per row */
 };
 
 ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t dtype,

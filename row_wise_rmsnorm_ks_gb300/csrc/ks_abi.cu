@@ -65,6 +65,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceSlot {
     std::once_flag once;
     int sm_count = 0;
+    int l2_bytes = 0;
     cudaError_t err = cudaSuccess;
 };
 DeviceSlot g_devices[kMaxDevices];
@@ -84,16 +85,32 @@ uint64_t occ_key(int dev, ks_dtype_t d, bool fused, const ks_plan_t &p, bool clu
 }
 
 constexpr int kSmemLimit = 226 * 1024;  // dynamic ring; static smem and reserve fit in 227 KB
-// Bytes of rows the two-pass kernel's CTAs may have in flight together: the second pass re-reads
-// each row from L2 (129 MB), so the grid keeps the first pass's rows inside it, but never drops
-// below one CTA per SM (for rows of 16384 vectors and more, measured: a full grid with some L2
-// misses beats fewer CTAs, 0.66-0.81 of the copy peak against 0.39-0.68 for fused rows).
-constexpr int64_t kTwoPassL2Budget = 96ll << 20;
+// Bytes of rows the two-pass kernels may have in flight together: the second pass re-reads each
+// row from L2, so the grid keeps the first pass's rows inside three quarters of the device's L2
+// (96 MiB when no device size is given, as in the pure-host ks_plan_launch). The
+// one-CTA-per-row kernel never drops below one CTA per SM (for rows of 16384 vectors and more,
+// measured: a full grid with some L2 misses beats fewer CTAs, 0.66-0.81 of the copy peak
+// against 0.39-0.68 for fused rows).
+int64_t twopass_l2_budget(int64_t l2_bytes) { return l2_bytes > 0 ? l2_bytes / 4 * 3 : 96ll << 20; }
 
-int64_t twopass_grid_cap(int64_t hv, bool fused, int sm_count) {
+int64_t twopass_grid_cap(int64_t hv, bool fused, int sm_count, int64_t l2_bytes) {
     const int64_t per_cta = hv * 16 * (fused ? 2 : 1);
-    const int64_t cap = kTwoPassL2Budget / (per_cta > 0 ? per_cta : 1);
+    const int64_t cap = twopass_l2_budget(l2_bytes) / (per_cta > 0 ? per_cta : 1);
     return cap < sm_count ? sm_count : cap;
+}
+
+// Clusters of the split two-pass kernel: no more than keep their rows in flight (one per
+// cluster) within the L2 budget; then as few as give every cluster the same number of rows (a
+// last wave that only some clusters run leaves the others' SMs idle), e.g. 768 rows on 152
+// resident clusters run as 6 rows on each of 128 clusters instead of 5 or 6 on 152.
+int64_t split_clusters(int64_t rows, int64_t resident, int64_t hv, bool fused, int64_t l2_bytes) {
+    const int64_t row_bytes = hv * 16 * (fused ? 2 : 1);
+    int64_t n = twopass_l2_budget(l2_bytes) / (row_bytes > 0 ? row_bytes : 1);
+    n = n < resident ? n : resident;
+    n = n < rows ? n : rows;
+    n = n < 1 ? 1 : n;
+    const int64_t waves = ceil_div(rows, n);
+    return ceil_div(rows, waves);
 }
 constexpr int kRingHeader = 128;  // the staged kernel's mbarriers, ahead of its ring
 
@@ -108,7 +125,8 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
     p.stages = p.kernel == KS_KERNEL_BULK_ROW ? p.stages : 0;
     p.smem_bytes = 0;
     const bool split_bulk = p.kernel == KS_KERNEL_BULK_ROW && p.cluster >= 2;
-    p.cluster = (p.kernel == KS_KERNEL_CLUSTER_ROW || split_bulk) ? p.cluster : 0;
+    const bool split_twopass = p.kernel == KS_KERNEL_TWOPASS_ROW && p.cluster >= 2;
+    p.cluster = (p.kernel == KS_KERNEL_CLUSTER_ROW || split_bulk || split_twopass) ? p.cluster : 0;
     if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL))
         return fail(KS_ERR_INVALID_ARGUMENT, "unknown plan flags 0x%x", (unsigned)p.flags);
     int64_t rows_per_cta = 1;
@@ -164,7 +182,15 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
         if (p.vec_per_thread != 2 && p.vec_per_thread != 4)
             return fail(KS_ERR_INVALID_ARGUMENT, "two-pass kernel takes 2 or 4 vectors per step");
         if (p.block > 1024) return fail(KS_ERR_INVALID_ARGUMENT, "two-pass block > 1024");
-        p.team = p.block;
+        if (split_twopass) {
+            if (p.cluster > 8)
+                return fail(KS_ERR_INVALID_ARGUMENT, "cluster of %d CTAs (2..8 supported)", p.cluster);
+            const int64_t slice = ceil_div(hv, p.cluster);
+            if ((p.cluster - 1) * slice >= hv)
+                return fail(KS_ERR_INVALID_ARGUMENT, "a cluster of %d leaves a CTA without vectors",
+                            p.cluster);
+        }
+        p.team = p.block * (split_twopass ? p.cluster : 1);
         break;
     case KS_KERNEL_SCALAR:
         if (p.block > 1024) return fail(KS_ERR_INVALID_ARGUMENT, "scalar block > 1024");
@@ -256,11 +282,13 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
     DeviceSlot &slot = g_devices[dev];
     std::call_once(slot.once, [&] {
         slot.err = cudaDeviceGetAttribute(&slot.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (slot.err == cudaSuccess)
+            slot.err = cudaDeviceGetAttribute(&slot.l2_bytes, cudaDevAttrL2CacheSize, dev);
     });
     if (slot.err != cudaSuccess)
-        return fail(KS_ERR_CUDA, "querying the SM count: %s", cudaGetErrorString(slot.err));
+        return fail(KS_ERR_CUDA, "querying the SM count and L2 size: %s", cudaGetErrorString(slot.err));
     if (!forced) {
-        st = plan(fused ? 1 : 0, rows, hidden, dtype, aligned16, slot.sm_count, 0, &p);
+        st = plan(fused ? 1 : 0, rows, hidden, dtype, aligned16, slot.sm_count, 0, slot.l2_bytes, &p);
         if (st != KS_SUCCESS) return st;
     }
     const int32_t pdl = forced ? (p.flags & KS_PLAN_PDL)
@@ -283,12 +311,13 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         const int64_t cap = (int64_t)slot.sm_count * bps;
         p.grid = forced->grid > 0 ? (forced->grid < ctas ? forced->grid : ctas) : (ctas < cap ? ctas : cap);
         if (forced->grid <= 0 && p.kernel == KS_KERNEL_TWOPASS_ROW) {
-            const int64_t l2cap = twopass_grid_cap(hidden / (16 / e), fused, slot.sm_count);
+            const int64_t l2cap = twopass_grid_cap(hidden / (16 / e), fused, slot.sm_count,
+                                                   slot.l2_bytes);
             if (p.grid > l2cap) p.grid = l2cap;
         }
         p.rows_per_pass = p.grid * per_cta;
     } else {
-        st = plan(fused ? 1 : 0, rows, hidden, dtype, aligned16, slot.sm_count, bps, &p);
+        st = plan(fused ? 1 : 0, rows, hidden, dtype, aligned16, slot.sm_count, bps, slot.l2_bytes, &p);
         if (st != KS_SUCCESS) return st;
     }
     if (p.cluster >= 2) {
@@ -303,6 +332,12 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
             p.grid = (int64_t)resident * p.cluster;
             p.rows_per_pass = resident;
         }
+        if (p.kernel == KS_KERNEL_TWOPASS_ROW && !(forced && forced->grid > 0)) {
+            const int64_t n = split_clusters(rows, p.grid / p.cluster, hidden / (16 / e), fused,
+                                             slot.l2_bytes);
+            p.grid = n * p.cluster;
+            p.rows_per_pass = n;
+        }
     }
 
     p.flags = (p.flags & ~KS_PLAN_PDL) | pdl;
@@ -316,6 +351,7 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
     a.hv = (p.kernel == KS_KERNEL_SCALAR) ? 0 : hidden / (16 / e);
     a.eps = eps;
     a.stages = p.stages;
+    a.l2_prefetch = (p.kernel == KS_KERNEL_TWOPASS_ROW && !(p.flags & KS_PLAN_NO_PREFETCH)) ? 1 : 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (dtype) {
     case KS_DTYPE_BF16: ce = launch_bf16(p, fused, a, s); break;
@@ -426,6 +462,7 @@ void bulk_row(ks_plan_t *p, int64_t hv, bool fused, int64_t stages) {
 // 512 threads up to 4096 vectors and 1024 beyond (fp32 rows of at most 2048 vectors: 4 on 256).
 void twopass_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
     p->kernel = KS_KERNEL_TWOPASS_ROW;
+    p->flags = KS_PLAN_NO_PREFETCH;
     if (!fused) {
         p->vec_per_thread = 4;
         p->block = hv <= 4096 ? 256 : (hv <= 8192 ? 512 : 1024);
@@ -437,13 +474,29 @@ void twopass_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
         p->block = hv <= 4096 ? 512 : 1024;
     }
     p->team = p->block;
-    p->flags = 0;
+}
+
+// Many wide rows: the two-pass kernel split over a cluster of C = clamp(hv / 4096, 2, 8) CTAs,
+// so each CTA's slice is about 4096 vectors (64 KiB a tensor), read 1024 vectors a step: plain
+// rows by 256 threads at 4 vectors with each slice asked into L2 as the row starts, fused rows by
+// 512 threads at 2 without. Measured on GB300 (plan sweep, 384 MiB per tensor, bf16/fp16/fp32):
+// plain rows of 16384 and 32768 vectors 0.83-0.86 of the copy peak, fused rows of 8192 0.86-0.93,
+// 16384 0.84-0.91 and 32768 0.79-0.86, against 0.66-0.81 with one CTA per row (whose last wave,
+// at 10 rows per CTA, left SMs idle, and whose rows in flight outgrew L2 for fused rows).
+void split_row(ks_plan_t *p, int64_t hv, bool fused) {
+    const int64_t c = hv / 4096;
+    p->kernel = KS_KERNEL_TWOPASS_ROW;
+    p->cluster = (int32_t)(c < 2 ? 2 : (c > 8 ? 8 : c));
+    p->vec_per_thread = fused ? 2 : 4;
+    p->block = fused ? 512 : 256;
+    p->team = p->block * p->cluster;
+    p->flags = fused ? KS_PLAN_NO_PREFETCH : 0;
 }
 
 }  // namespace
 
 ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
-                 int sm_count, int blocks_per_sm, ks_plan_t *p) {
+                 int sm_count, int blocks_per_sm, int64_t l2_bytes, ks_plan_t *p) {
     if (!p) return fail(KS_ERR_INVALID_ARGUMENT, "plan pointer is NULL");
     memset(p, 0, sizeof *p);
     const int elem = elem_bytes(dtype);
@@ -526,6 +579,9 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         p->vec_per_thread = slice <= 512 ? 1 : (slice <= 1024 ? 2 : 4);
         p->block = (int32_t)round_up(ceil_div(slice, p->vec_per_thread), 32);
         p->team = p->block * 8;
+    } else if (vec_ok && (hv > 8192 || (fused && hv > 4096))) {
+        // Very wide rows, more of them: the two-pass kernel split over a cluster.
+        split_row(p, hv, fused);
     } else if (vec_ok && hv > 2048) {
         // Wider rows, more of them: the two-pass kernel (no width limit; the second pass from L2).
         twopass_row(p, hv, fused, dtype);
@@ -539,6 +595,8 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         int64_t clusters = rows;
         const int64_t cap = (int64_t)sm_count * blocks_per_sm / p->cluster;
         if (blocks_per_sm > 0 && clusters > cap) clusters = cap < 1 ? 1 : cap;
+        if (p->kernel == KS_KERNEL_TWOPASS_ROW)
+            clusters = split_clusters(rows, clusters, hv, fused, l2_bytes);
         p->grid = clusters * p->cluster;
         p->rows_per_pass = clusters;
         return KS_SUCCESS;
@@ -546,8 +604,10 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
     const int64_t ctas = ceil_div(rows, rows_per_cta);
     const int64_t cap = (int64_t)sm_count * blocks_per_sm;
     p->grid = (blocks_per_sm > 0 && ctas > cap) ? cap : ctas;
-    if (p->kernel == KS_KERNEL_TWOPASS_ROW && p->grid > twopass_grid_cap(hv, fused, sm_count))
-        p->grid = twopass_grid_cap(hv, fused, sm_count);
+    if (p->kernel == KS_KERNEL_TWOPASS_ROW) {
+        const int64_t l2cap = twopass_grid_cap(hv, fused, sm_count, l2_bytes);
+        if (p->grid > l2cap) p->grid = l2cap;
+    }
     p->rows_per_pass = p->grid * rows_per_cta;
     return KS_SUCCESS;
 }
@@ -612,7 +672,7 @@ ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t 
                            ks_plan_t *plan) {
     const int e = ks::elem_bytes(dtype);
     if (e == 0) return ks::fail(KS_ERR_UNSUPPORTED_DTYPE, "dtype code %d is not a ks_dtype_t", (int)dtype);
-    return ks::plan(op, rows, hidden, dtype, aligned16 != 0, sm_count, blocks_per_sm, plan);
+    return ks::plan(op, rows, hidden, dtype, aligned16 != 0, sm_count, blocks_per_sm, 0, plan);
 }
 
 ks_status_t ks_set_launch_options(int32_t options) {

@@ -19,6 +19,7 @@ struct RowArgs {
     int64_t hv;         // H / elements-per-16-byte-vector (vector kernels)
     float eps;
     int32_t stages;     // staged kernel: rows in the shared-memory ring
+    int32_t l2_prefetch;  // two-pass kernels: each row's slice asked into L2 as the row starts
 };
 
 // Records a failure detail for ks_last_error() on this thread and returns `s`.
@@ -46,10 +47,10 @@ int64_t host_chunk_rows(bool fused, int64_t hidden, int e, int64_t ws_bytes);
 // Whether ks_set_launch_options turned programmatic dependent launch on.
 bool launch_pdl_enabled();
 
-// Host heuristic: fills *p from the shape, the dtype and the device's SM count.
-// blocks_per_sm == 0 leaves grid at one pass over the rows.
+// Host heuristic: fills *p from the shape, the dtype and the device's SM count and L2 size
+// (l2_bytes <= 0: a GB300's). blocks_per_sm == 0 leaves grid at one pass over the rows.
 ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
-                 int sm_count, int blocks_per_sm, ks_plan_t *p);
+                 int sm_count, int blocks_per_sm, int64_t l2_bytes, ks_plan_t *p);
 
 // Per-dtype launchers (one translation unit each). `blocks_per_sm` queries the occupancy of the
 // kernel the plan names; `max_clusters` how many of its clusters can be resident at once (plans

@@ -431,6 +431,20 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
 // so DRAM still sees each element read once and written once. Nothing but the loop bounds the
 // row width: no row is held in registers, shared memory or a cluster. The first pass loads
 // with the default L2 policy (the row is read again), the second with evict-first (last use).
+// Asks L2 for vectors [lo, hi) of a row of x (and of the residual): threads 0.. each issue one
+// bulk prefetch of at most 32 KiB.
+template <bool kFused>
+__device__ __forceinline__ void prefetch_slice(const uint4 *xr, const uint4 *rr, int64_t lo,
+                                               int64_t hi, int t) {
+    constexpr int64_t kPiece = 2048;  // vectors (32 KiB) per prefetch
+    const int64_t c = lo + (int64_t)t * kPiece;
+    if (c < hi) {
+        const uint32_t bytes = (uint32_t)(((hi - c) < kPiece ? (hi - c) : kPiece) * 16);
+        bulk_prefetch_l2(xr + c, bytes);
+        if (kFused) bulk_prefetch_l2(rr + c, bytes);
+    }
+}
+
 template <typename T, bool kFused, int U, int kMaxBlock>
 __global__ void __launch_bounds__(kMaxBlock) rows_twopass_kernel(const RowArgs a) {
     using E = Elem<T>;
@@ -445,10 +459,14 @@ __global__ void __launch_bounds__(kMaxBlock) rows_twopass_kernel(const RowArgs a
     const uint4 *wg = static_cast<const uint4 *>(a.w);
     grid_dependency_wait();
     allow_dependents_launch();
+    // With prefetch, the whole row is asked into L2 by the copy engine as it starts (see
+    // rows_split_kernel).
+    const bool prefetch = a.l2_prefetch != 0;
     int parity = 0;
     for (int64_t row = blockIdx.x; row < a.rows; row += gridDim.x) {
         const uint4 *xr = xg + row * hv;
         uint4 *rr = kFused ? rg + row * hv : nullptr;
+        if (prefetch) prefetch_slice<kFused>(xr, rr, 0, hv, t);
         PairSumSq<E::kPairMath> acc;
         for (int64_t c0 = t; c0 < hv; c0 += chunk) {
             uint4 xv[U], rv[U];
@@ -498,6 +516,144 @@ const void *pick_twopass(int block) {
     if (block <= 256) return (const void *)rows_twopass_kernel<T, kFused, U, 256>;
     if (block <= 512) return (const void *)rows_twopass_kernel<T, kFused, U, 512>;
     return (const void *)rows_twopass_kernel<T, kFused, U, 1024>;
+}
+
+// ------------------------------------------------------------ split two-pass row kernel
+
+// The two-pass scheme with each row split over a thread-block cluster of C CTAs (2..8): CTA q of
+// a cluster takes the contiguous slice [q*S, min((q+1)*S, hv)) of S = ceil(hv / C) vectors of
+// every row its cluster visits, forms the slice's sum of squares (default L2 policy), and writes
+// the slice's outputs from a second read of it (evict-first, from L2). Between the two passes
+// the slice sums meet: the CTA's first C threads each write the CTA's sum into one peer's
+// shared memory (distributed shared memory), one cluster barrier per row makes them visible,
+// and every CTA adds the C sums in rank order, so all CTAs of a row agree on its scale. The
+// barrier's arrive and wait are split, with the first loads of the second pass issued between
+// them, so its latency overlaps those loads.
+//
+// Against one CTA per row this keeps each unit of work to a slice: a persistent grid of whole
+// rows leaves SMs idle in its last wave when the rows per CTA are few (10.1 rows per CTA run as
+// 11 waves), and the rows a CTA-per-row grid has in flight at once grow with the width until
+// the second pass misses L2; here the rows in flight are one per cluster.
+template <typename T, bool kFused, int U, int kMaxBlock>
+__global__ void __launch_bounds__(kMaxBlock) rows_split_kernel(const RowArgs a) {
+    namespace cg = cooperative_groups;
+    using E = Elem<T>;
+    constexpr int P = E::kPerVec / 2;
+    __shared__ float red[32];
+    __shared__ float part[2][8];  // a row's slice sums from every CTA of the cluster, by rank
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int q = (int)cluster.block_rank();
+    const int g = blockDim.x, t = threadIdx.x;
+    const int64_t hv = a.hv;
+    const int64_t S = (hv + C - 1) / C;
+    const int64_t lo = q * S;
+    const int64_t hi = (lo + S < hv) ? lo + S : hv;
+    const int64_t chunk = (int64_t)g * U;
+    const float h = (float)a.hidden;
+    const uint4 *xg = static_cast<const uint4 *>(a.x);
+    uint4 *og = static_cast<uint4 *>(a.out);
+    uint4 *rg = static_cast<uint4 *>(a.res);
+    const uint4 *wg = static_cast<const uint4 *>(a.w);
+    grid_dependency_wait();
+    allow_dependents_launch();
+    // A peer's shared memory may be written only once that peer has started: every CTA arrives
+    // here and waits (before its first write into a peer) for all of its cluster to arrive. The
+    // row loop runs the same rows on every CTA of a cluster, so `started` is uniform.
+    cluster.barrier_arrive();
+    bool started = false;
+    const int64_t nclusters = gridDim.x / C;
+    // With prefetch, the whole slice of a row is asked into L2 by the copy engine as the row
+    // starts, so the DRAM reads of all the first pass's steps are in flight at once.
+    const bool prefetch = a.l2_prefetch != 0;
+    int parity = 0;
+    for (int64_t row = blockIdx.x / C; row < a.rows; row += nclusters) {
+        const uint4 *xr = xg + row * hv;
+        uint4 *rr = kFused ? rg + row * hv : nullptr;
+        if (prefetch) prefetch_slice<kFused>(xr, rr, lo, hi, t);
+        PairSumSq<E::kPairMath> acc;
+        for (int64_t c0 = lo + t; c0 < hi; c0 += chunk) {
+            uint4 xv[U], rv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                xv[u] = c < hi ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+                if (kFused) rv[u] = c < hi ? rr[c] : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float2 f[P];
+                row_values<T, kFused>(xv[u], rv[u], f);
+                acc.add(f);
+            }
+        }
+        // The CTA's slice sum (warps in order) into slot `parity` of every CTA of the cluster.
+        // `red` is free again once every thread has passed the previous row's cluster barrier;
+        // slot `parity` of a peer is written again two rows on, after a barrier that the peer
+        // reaches only once it has read this row's sums.
+        const float wsum = warp_sum(acc.total());
+        if ((t & 31) == 0) red[t >> 5] = wsum;
+        __syncthreads();
+        if (!started) {
+            cluster.barrier_wait();
+            started = true;
+        }
+        if (t < C) {
+            float cta = 0.0f;
+            for (int i = 0; i < (g >> 5); ++i) cta += red[i];
+            *cluster.map_shared_rank(&part[parity][q], t) = cta;
+        }
+        cluster.barrier_arrive();
+        uint4 *orow = og + row * hv;
+        uint4 xv[U], rv[U], wv[U];
+        int64_t c0 = lo + t;
+        // the second pass's first loads do not need the scale: issue them before the wait
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = c0 + (int64_t)u * g;
+            const bool in = c < hi;
+            xv[u] = in ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+            if (kFused) rv[u] = in ? __ldcs(rr + c) : make_uint4(0u, 0u, 0u, 0u);
+            wv[u] = in ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        cluster.barrier_wait();
+        float ss = 0.0f;
+        for (int r = 0; r < C; ++r) ss += part[parity][r];
+        parity ^= 1;
+        const float scale = row_scale(ss, h, a.eps);
+        for (; c0 < hi; c0 += chunk) {
+            if (c0 != lo + t) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t c = c0 + (int64_t)u * g;
+                    const bool in = c < hi;
+                    xv[u] = in ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+                    if (kFused) rv[u] = in ? __ldcs(rr + c) : make_uint4(0u, 0u, 0u, 0u);
+                    wv[u] = in ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                if (c < hi) {
+                    float2 f[P];
+                    row_values<T, kFused>(xv[u], rv[u], f);
+                    if (kFused) __stcs(rr + c, E::pack2(f));
+                    __stcs(orow + c, scaled_weighted<T>(f, scale, wv[u]));
+                }
+            }
+        }
+    }
+    if (!started) cluster.barrier_wait();
+    cluster.sync();  // no CTA leaves while a peer may still write its sums here
+}
+
+template <typename T, bool kFused, int U>
+const void *pick_split(int block) {
+    if (block <= 256) return (const void *)rows_split_kernel<T, kFused, U, 256>;
+    if (block <= 512) return (const void *)rows_split_kernel<T, kFused, U, 512>;
+    return (const void *)rows_split_kernel<T, kFused, U, 1024>;
 }
 
 // ------------------------------------------------------------------- scalar row kernel
@@ -874,6 +1030,13 @@ const void *pick_kernel(const ks_plan_t &p) {
     }
     case KS_KERNEL_SCALAR: return (const void *)rows_scalar_kernel<T, kFused>;
     case KS_KERNEL_TWOPASS_ROW:
+        if (p.cluster >= 2) {
+            switch (p.vec_per_thread) {
+            case 2: return pick_split<T, kFused, 2>(p.block);
+            case 4: return pick_split<T, kFused, 4>(p.block);
+            default: return nullptr;
+            }
+        }
         switch (p.vec_per_thread) {
         case 2: return pick_twopass<T, kFused, 2>(p.block);
         case 4: return pick_twopass<T, kFused, 4>(p.block);

@@ -95,6 +95,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// A hint to the copy engine: bring `bytes` (a multiple of 16, the address 16-byte aligned) of
+// global memory into L2, with no completion to wait for and no register or shared-memory cost.
+// Later loads of those bytes hit L2 if the lines are still there, and go to DRAM otherwise.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -273,7 +273,7 @@ def test_wide_rows_take_cta_per_row(hidden, fused_plan, plain_plan):
         assert (p.kernel, p.vec_per_thread) == (kernel, v), (op, hidden)
         assert p.team == p.block and p.stages == 0
         if kernel == TWO:  # (TWO, vectors per step, block)
-            assert p.block == third and p.flags == 0
+            assert p.block == third and p.flags == _abi.KS_PLAN_NO_PREFETCH
         else:  # (CTA, vectors per thread, prefetch)
             assert p.block == -(-hidden // (8 * v) // 32) * 32
             assert p.vec_per_thread * 8 * p.block >= hidden
@@ -373,10 +373,23 @@ def test_rows_wider_than_registers_take_the_two_pass_kernel(hidden, dtype):
     e = 4 if dtype == F32 else 2
     hv = hidden * e // 16
     for op in (0, 1):
-        # many rows: one CTA per row, two passes over the row (the second from L2)
         p = plan(op, 65536, hidden, dtype=dtype, bps=1)
-        assert p.kernel == _abi.KS_KERNEL_TWOPASS_ROW and p.cluster == 0 and p.team == p.block
+        assert p.kernel == _abi.KS_KERNEL_TWOPASS_ROW
         assert p.vec_per_thread == (2 if op else 4)
+        if hv > 8192 or (op and hv > 4096):
+            # many rows of more than 8192 vectors (fused: 4096): split over a cluster of
+            # hv / 4096 CTAs (2..8), slices of about 4096 vectors; whole clusters, as many as the
+            # SMs hold, each with the same number of rows; plain rows prefetch each slice to L2
+            c = min(8, max(2, hv // 4096))
+            assert p.cluster == c and p.team == p.block * c
+            assert p.block == (512 if op else 256)
+            assert p.flags == (_abi.KS_PLAN_NO_PREFETCH if op else 0)
+            n = 152 // c
+            waves = -(-65536 // n)
+            assert p.grid == -(-65536 // waves) * c
+            continue
+        # many rows: one CTA per row, two passes over the row (the second from L2)
+        assert p.cluster == 0 and p.team == p.block and p.flags == _abi.KS_PLAN_NO_PREFETCH
         if op:
             assert p.block == (512 if hv <= 4096 else 1024)
         else:
@@ -403,6 +416,20 @@ def test_two_pass_plans_are_checked():
         assert _abi.ks_rms_norm_planned(a, b, w, 64, 32768, 1e-6, BF16, p, None) == E
     p = mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, 256)
     assert _abi.ks_rms_norm_planned(a, b + 2, w, 64, 32768, 1e-6, BF16, p, None) == E  # unaligned
+
+
+def test_split_two_pass_plans_are_checked():
+    a, b, w = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    mk = _abi.make_plan
+    for p in (mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, 256, cluster=9),    # cluster over 8
+              mk(_abi.KS_KERNEL_TWOPASS_ROW, 3, 256, cluster=4),    # unsupported vector count
+              mk(_abi.KS_KERNEL_TWOPASS_ROW, 2, 2048, cluster=4)):  # block over 1024
+        assert _abi.ks_rms_norm_planned(a, b, w, 64, 32768, 1e-6, BF16, p, None) == E
+    # 8 CTAs over a row of 7 vectors: one would own none
+    p = mk(_abi.KS_KERNEL_TWOPASS_ROW, 2, 32, cluster=8)
+    assert _abi.ks_fused_add_rms_norm_planned(a, b, w, 64, 56, 1e-6, BF16, p, None) == E
+    assert "without vectors" in _abi.ks_last_error()
 
 
 def test_split_staged_plans_are_checked():
@@ -569,6 +596,10 @@ def test_every_width_gets_a_valid_plan(dtype, op):
                     assert p.block * p.vec_per_thread >= hv, (rows, hidden)
                 elif p.kernel == TWO:
                     assert p.vec_per_thread in (2, 4) and p.block <= 1024
+                    if p.cluster >= 2:
+                        slice_ = -(-hv // p.cluster)
+                        assert p.cluster <= 8 and p.grid % p.cluster == 0
+                        assert (p.cluster - 1) * slice_ < hv, (rows, hidden)
                 elif p.kernel == BULK:
                     assert p.vec_per_thread == 4 and p.block <= 512 and 1 <= p.stages <= 16
                     assert p.block * 4 >= hv and p.smem_bytes <= 226 * 1024

@@ -83,8 +83,9 @@ def test_host_in_place_and_stream_order(cuda_device):
     # 4000-row batch on the device, and the bits must match exactly
     ws = _workspace(cuda_device, 3 * 160 * hidden * 2)
     assert _abi.ks_host_chunk_rows(0, hidden, _abi.KS_DTYPE_BF16, ws.numel()) == 160
-    st, p_chunk = _abi.ks_plan_launch(0, 160, hidden, _abi.KS_DTYPE_BF16, True, 152, 0)
-    st, p_all = _abi.ks_plan_launch(0, rows, hidden, _abi.KS_DTYPE_BF16, True, 152, 0)
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    st, p_chunk = _abi.ks_plan_launch(0, 160, hidden, _abi.KS_DTYPE_BF16, True, sms, 0)
+    st, p_all = _abi.ks_plan_launch(0, rows, hidden, _abi.KS_DTYPE_BF16, True, sms, 0)
     assert (p_chunk.kernel, p_chunk.vec_per_thread, p_chunk.block, p_chunk.flags) == \
         (p_all.kernel, p_all.vec_per_thread, p_all.block, p_all.flags)
     wd = w.to(cuda_device)

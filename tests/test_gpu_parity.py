@@ -279,6 +279,12 @@ def _variant_plan(name, hidden, elem):
     if name.startswith("twopass"):  # twopass_b<block>_u<vectors per step>
         block, u = name.split("_b")[1].split("_u")
         return A.make_plan(A.KS_KERNEL_TWOPASS_ROW, int(u), int(block))
+    if name.startswith("split"):  # split_c<cluster>_b<block>_u<vectors per step>
+        c = int(name.split("_c")[1].split("_")[0])
+        block, u = name.split("_b")[1].split("_u")
+        if (c - 1) * -(-hv // c) >= hv:
+            return None
+        return A.make_plan(A.KS_KERNEL_TWOPASS_ROW, int(u), int(block), cluster=c)
     flags = A.KS_PLAN_NO_PREFETCH if name.endswith("_np") else 0
     if name.startswith("warp_row"):
         v = next((v for v in (1, 2, 4, 6, 8) if 32 * v >= hv), None)
@@ -305,7 +311,8 @@ VARIANTS = ["warp_row", "warp_row_np", "cta_row_v2", "cta_row_v2_np", "cta_row_v
             "cta_row_v4_np", "bulk_row_s1", "bulk_row_s2", "bulk_row_s5", "bulk_row_c2_s2",
             "bulk_row_c3_s1", "bulk_row_c8_s3", "cluster_row_c2", "cluster_row_c3",
             "cluster_row_c8", "twopass_b256_u4", "twopass_b512_u2", "twopass_b1024_u4",
-            "twopass_b96_u2", "scalar"]
+            "twopass_b96_u2", "split_c2_b256_u4", "split_c3_b96_u2", "split_c4_b512_u2",
+            "split_c8_b1024_u2", "scalar"]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -357,13 +364,15 @@ def test_every_kernel_variant_matches_oracle(cuda_device, variant, dtype, op, ro
                                                ("bf16", 131072, 21), ("bf16", 32768, 3),
                                                ("fp32", 20480, 5)])
 def test_rows_wider_than_registers_match_oracle(cuda_device, op, dtype, hidden, rows):
-    """Rows of more than 2048 vectors: split over a cluster (a staged ring per CTA with many rows,
-    the register-resident cluster kernel with few), through the default heuristic."""
+    """Rows of more than 2048 vectors through the default heuristic: the two-pass kernel (split
+    over a cluster for rows of more than 8192 vectors) with many rows, the register-resident
+    cluster kernel with few."""
     from row_wise_rmsnorm_ks_gb300 import _abi as A
     dt = synth.dtype_of(dtype)
     code = {torch.bfloat16: A.KS_DTYPE_BF16, torch.float16: A.KS_DTYPE_F16,
             torch.float32: A.KS_DTYPE_F32}[dt]
-    p = A.ks_plan_launch(0 if op == "rms_norm" else 1, rows, hidden, code, True, 152, 1)[1]
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    p = A.ks_plan_launch(0 if op == "rms_norm" else 1, rows, hidden, code, True, sms, 1)[1]
     assert p.kernel == A.KS_KERNEL_TWOPASS_ROW or (p.kernel == A.KS_KERNEL_CLUSTER_ROW
                                                     and p.cluster == 8)
     x = synth.cast(synth.student_t3_np((rows, hidden), 95), dt)
