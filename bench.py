@@ -38,7 +38,6 @@ sys.path.insert(0, ROOT)
 METRIC = "RMSNorm / fused-add RMSNorm HBM GB/s (% of GB300 peak) and p50 µs"
 # the workload the headline is quoted on; --rows/--hidden name smaller cases (profiling captures)
 FULL_ROWS, FULL_HIDDEN = 32768, 8192
-L2_BYTES = 129 * 10**6
 
 
 def workload(rows: int, hidden: int) -> str:
@@ -47,16 +46,29 @@ def workload(rows: int, hidden: int) -> str:
             f"({rows * hidden * 2 / 2**20:.0f} MiB per tensor), weight 1+0.1N(0,1), eps=1e-5")
 
 
-def l2_note(rows: int, hidden: int) -> str:
+def device_facts(dev) -> dict:
+    """The device's SM count and L2 size, as the runtime reports them."""
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    return {"sm_count": int(p.multi_processor_count), "l2_bytes": int(p.L2_cache_size)}
+
+
+def l2_note(rows: int, hidden: int, l2_bytes: int) -> str:
     mib = rows * hidden * 2 / 2**20
-    if rows * hidden * 2 > L2_BYTES:
-        return f"no flush: every tensor ({mib:.0f} MiB) is larger than L2"
-    return f"no flush, and the tensors ({mib:.1f} MiB) fit in L2: not a bench figure"
+    l2 = f"L2 ({l2_bytes / 2**20:.0f} MiB, device query)"
+    if rows * hidden * 2 > l2_bytes:
+        return f"no flush: every tensor ({mib:.0f} MiB) is larger than {l2}"
+    return f"no flush, and the tensors ({mib:.1f} MiB) fit in {l2}: not a bench figure"
 
 
 FALLBACK_HBM_GBS = 6800.0
+C2C_NOMINAL_GBS = 900.0  # NVLink-C2C between Grace and the GPU, both directions together
+# what decides the recorded launches' DRAM traffic: the kernels, and the plan code that picks
+# their launch shape (a change to either invalidates the record)
 KERNEL_SOURCES = ["row_wise_rmsnorm_ks_gb300/csrc/ks_kernels.cuh",
-                  "row_wise_rmsnorm_ks_gb300/csrc/ks_ptx.cuh"]
+                  "row_wise_rmsnorm_ks_gb300/csrc/ks_ptx.cuh",
+                  "row_wise_rmsnorm_ks_gb300/csrc/ks_abi.cu"]
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
 
 
 def algorithmic_bytes(op: str, rows: int, hidden: int, elem: int) -> int:
@@ -111,7 +123,7 @@ def code_only(src: str) -> str:
 
 
 def kernel_source_sha() -> str:
-    """Hash of the kernel sources' code (comments and layout ignored)."""
+    """Hash of the kernel and plan sources' code (comments and layout ignored)."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
@@ -129,23 +141,19 @@ def measured_peaks() -> dict:
 
 
 def recorded_traffic(op: str, rows: int = FULL_ROWS, hidden: int = FULL_HIDDEN):
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on the current
-    kernel sources and the launch has the recorded shape, bf16 [FULL_ROWS, FULL_HIDDEN]
-    (else None)."""
-    path = os.path.join(ROOT, "profiles", "ncu_dram_traffic.md")
-    if (rows, hidden) != (FULL_ROWS, FULL_HIDDEN) or not os.path.exists(path):
+    """Per-launch DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) from the
+    committed record, if it was taken on the current kernel and plan sources and the launch has
+    the recorded shape (else None)."""
+    if not os.path.exists(TRAFFIC_RECORD):
         return None
-    sha, val = None, None
-    with open(path) as f:
-        for line in f:
-            line = line.strip()
-            if line.startswith("kernel_sources_sha:"):
-                sha = line.split(":", 1)[1].strip()
-            if line.startswith(f"{op}_dram_bytes_per_launch_full:"):
-                val = line.split(":", 1)[1].strip()
-    if sha != kernel_source_sha() or val in (None, "", "null"):
+    with open(TRAFFIC_RECORD) as f:
+        rec = json.load(f)
+    if rec.get("sources_sha") != kernel_source_sha():
         return None
-    return int(float(val))
+    ent = rec.get("launches", {}).get(op)
+    if not ent or [rows, hidden] != ent.get("shape"):
+        return None
+    return int(ent["dram_read_bytes"]) + int(ent["dram_write_bytes"])
 
 
 # --------------------------------------------------------------------------- clock sampler
@@ -225,6 +233,7 @@ def run_ks(args) -> int:
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     _abi.load()
+    facts = device_facts(dev)
 
     R, H, e = args.rows, args.hidden, 2
     eps = 1e-5
@@ -332,11 +341,11 @@ def run_ks(args) -> int:
             "data": "synthetic (seeded N(0,1) drawn on the device)",
             "config": {"workload": workload(R, H), "rows": R, "hidden": H, "eps": eps,
                        "accumulate": "f32",
-                       "l2": l2_note(R, H),
+                       "l2": l2_note(R, H, facts["l2_bytes"]),
                        "parallelism": f"rows: one independent batch per GPU x{world}",
                        "kernel_plan": {
-                           "rms_norm": _abi.ks_plan_launch(0, R, H, 2, True, 152, 0)[1].as_dict()["kernel_name"],
-                           "fused_add_rms_norm": _abi.ks_plan_launch(1, R, H, 2, True, 152, 0)[1].as_dict()["kernel_name"]}},
+                           "rms_norm": _abi.ks_plan_launch(0, R, H, 2, True, facts["sm_count"], 0)[1].as_dict()["kernel_name"],
+                           "fused_add_rms_norm": _abi.ks_plan_launch(1, R, H, 2, True, facts["sm_count"], 0)[1].as_dict()["kernel_name"]}},
             "roofline": {"bound": "hbm", "kernel": f"fused_add_rms_norm (bf16 [{R},{H}])",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
@@ -702,10 +711,11 @@ def run_e2e(dev, args, R, H, eps) -> dict:
 
     copy_time(True, True, reps=1)  # warm both directions up
     nblk = blk * 2
-    link = {"h2d_gbs": nblk / copy_time(True, False) / 1e9,
-            "d2h_gbs": nblk / copy_time(False, True) / 1e9,
-            "bidirectional_gbs": 2 * nblk / copy_time(True, True) / 1e9,
-            "how": "pinned 512 MiB copies (torch copy_), wall clock over 3 repetitions"}
+    copies = {"h2d_gbs": nblk / copy_time(True, False) / 1e9,
+              "d2h_gbs": nblk / copy_time(False, True) / 1e9,
+              "both_directions_gbs": 2 * nblk / copy_time(True, True) / 1e9,
+              "how": "pinned 512 MiB torch copy_ calls, wall clock over 3 repetitions (the "
+                     "copy engines' rate, not the link's: the direct mode beats it)"}
     del hdst, dbuf, dbuf2
 
     ms_direct = timed(None)
@@ -714,10 +724,14 @@ def run_e2e(dev, args, R, H, eps) -> dict:
     del ws
     best = "direct" if ms_direct <= ms_staged else "staged"
     ms = min(ms_direct, ms_staged)
-    return {"value": nbytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": ms,
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"value": gbs, "unit": "GB/s", "ms_per_step": ms,
             "steps": args.e2e_steps, "h2d_bytes_per_step": 3 * R * H * 2,
-            "d2h_bytes_per_step": 3 * R * H * 2, "mode": best, "host_link": link,
-            "frac_of_link": (nbytes / (ms * 1e-3) / 1e9) / link["bidirectional_gbs"],
+            "d2h_bytes_per_step": 3 * R * H * 2, "mode": best, "host_copies": copies,
+            # every counted byte crosses the host link once (x, residual in; y, x, residual out)
+            "link": {"name": "NVLink-C2C", "nominal_gbs_both_directions": C2C_NOMINAL_GBS,
+                     "source": "NVIDIA's published Grace-Blackwell figure, not measured here",
+                     "frac_of_nominal": gbs / C2C_NOMINAL_GBS},
             "direct_gbs": nbytes / (ms_direct * 1e-3) / 1e9,
             "staged_gbs": nbytes / (ms_staged * 1e-3) / 1e9,
             "api": "rms_norm_host + fused_add_rms_norm_host on pinned host rows (direct: kernels "
@@ -889,6 +903,7 @@ def run_sweep(args) -> int:
     side = torch.cuda.Stream(dev)
     flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)
     peak = measured_peaks()["hbm_gbs"]
+    sms = device_facts(dev)["sm_count"]
     codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16}
 
     def median_us(fn, n):
@@ -936,7 +951,7 @@ def run_sweep(args) -> int:
                                                                   w.data_ptr(), R, H, eps, code, st))
         us = median_us(fn, args.sweep_samples)
         nb = algorithmic_bytes(op, R, H, 2)
-        plan = _abi.ks_plan_launch(0 if op == "rms_norm" else 1, R, H, code, True, 152, 0)[1]
+        plan = _abi.ks_plan_launch(0 if op == "rms_norm" else 1, R, H, code, True, sms, 0)[1]
         line = {"sweep": tag, "op": op, "dtype": dt, "rows": R, "hidden": H, "p50_us": us,
                 "gbs": nb / (us * 1e-6) / 1e9, "frac_of_peak": nb / (us * 1e-6) / 1e9 / peak,
                 "kernel": plan.as_dict()["kernel_name"], "vec_per_thread": plan.vec_per_thread,
@@ -969,8 +984,10 @@ def plan_candidates(op: str, hv: int, elem: int):
     w6/w6n and w8/w8n: 6 or 8 vectors per lane for rows of 129..192 and 193..256 vectors),
     p2/n2/p4/n4 (CTA per row, 2 or 4 vectors per thread, with/without prefetch), b2 (staged ring,
     2 stages), tBuU (the two-pass kernel, B threads, U vectors per thread per step; rows of at
-    least 512 vectors), and for rows wider than 2048 vectors cC (register-resident cluster of C
-    CTAs, 4 vectors per thread) and bCsS (staged ring split over C CTAs, S stages)."""
+    least 512 vectors), sCbBuU (the two-pass kernel split over a cluster of C CTAs; rows of at
+    least 1024 vectors), both also with a trailing n (no L2 prefetch of the next row), and for
+    rows wider than 2048 vectors cC (register-resident cluster of C CTAs, 4 vectors per thread)
+    and bCsS (staged ring split over C CTAs, S stages)."""
     from row_wise_rmsnorm_ks_gb300 import _abi
 
     up32 = lambda n: -(-n // 32) * 32
@@ -994,9 +1011,20 @@ def plan_candidates(op: str, hv: int, elem: int):
     b = up32(-(-hv // 4))
     if b <= 512 and 128 + 2 * hv * 16 * (2 if fused else 1) <= 226 * 1024:
         out.append(("b2", _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, b, 2)))
+    npf = _abi.KS_PLAN_NO_PREFETCH
     if hv >= 512:
         for blk, u in ((256, 4), (512, 2), (512, 4), (1024, 2), (1024, 4)):
             out.append((f"t{blk}u{u}", _abi.make_plan(_abi.KS_KERNEL_TWOPASS_ROW, u, blk)))
+            out.append((f"t{blk}u{u}n", _abi.make_plan(_abi.KS_KERNEL_TWOPASS_ROW, u, blk,
+                                                       flags=npf)))
+    if hv >= 1024:
+        for c in (2, 4, 8):
+            for blk, u in ((256, 4), (512, 2), (512, 4), (1024, 2)):
+                if blk * u * (c - 1) < hv:  # at least one step of work per CTA slice
+                    out.append((f"s{c}b{blk}u{u}", _abi.make_plan(_abi.KS_KERNEL_TWOPASS_ROW, u,
+                                                                  blk, cluster=c)))
+                    out.append((f"s{c}b{blk}u{u}n", _abi.make_plan(
+                        _abi.KS_KERNEL_TWOPASS_ROW, u, blk, cluster=c, flags=npf)))
     if hv > 2048:
         for c in (2, 4, 8):
             sl = -(-hv // c)
@@ -1026,6 +1054,7 @@ def run_plan_sweep(args) -> int:
     torch.cuda.set_device(dev)
     s = torch.cuda.current_stream(dev).cuda_stream
     peak = measured_peaks()["hbm_gbs"]
+    sms = device_facts(dev)["sm_count"]
     codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
 
     def timeit(fn, n):
@@ -1072,7 +1101,7 @@ def run_plan_sweep(args) -> int:
                 for _ in range(args.plan_sweep_rounds):
                     for name, fn in fns:
                         res[name].append(nb / timeit(fn, n) / 1e9 / peak)
-                dp = _abi.ks_plan_launch(0 if op == "rms_norm" else 1, R, H, code, True, 152,
+                dp = _abi.ks_plan_launch(0 if op == "rms_norm" else 1, R, H, code, True, sms,
                                          0)[1].as_dict()
                 line = {"plan_sweep": dt, "op": op, "hv": hv, "hidden": H, "rows": R,
                         "default_plan": {k: dp[k] for k in ("kernel_name", "vec_per_thread",
@@ -1107,6 +1136,7 @@ def run_plan_contexts(args) -> int:
     torch.cuda.set_device(dev)
     s = torch.cuda.current_stream(dev).cuda_stream
     peak = measured_peaks()["hbm_gbs"]
+    sms = device_facts(dev)["sm_count"]
     codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
     keep = ("w4", "w4n", "w6", "w6n", "w8", "w8n", "p2", "n2", "p4", "n4", "t256u4", "t512u2",
             "b2")
@@ -1167,7 +1197,7 @@ def run_plan_contexts(args) -> int:
                     else:
                         _abi.check(_abi.ks_rms_norm(y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H,
                                                     1e-5, code, s))
-                _, dp = _abi.ks_plan_launch(int(fused), R, H, code, True, 152, 0)
+                _, dp = _abi.ks_plan_launch(int(fused), R, H, code, True, sms, 0)
                 fns = [("default", default)] + [(n, mk(p)) for n, p in plan_candidates(op, hv, elem)
                                                 if n in keep]
                 line = {"plan_contexts": dt, "op": op, "hv": hv, "hidden": H, "rows": R,

@@ -109,8 +109,30 @@ def test_recorded_traffic_only_for_the_recorded_shape():
     assert bench.recorded_traffic("rms_norm", bench.FULL_ROWS, 4096) is None
     assert "[8192,8192]" in bench.workload(8192, 8192) and "128 MiB" in bench.workload(8192, 8192)
     assert bench.workload(bench.FULL_ROWS, bench.FULL_HIDDEN).startswith("large prefill bf16")
-    assert "larger than L2" in bench.l2_note(bench.FULL_ROWS, bench.FULL_HIDDEN)
-    assert "not a bench figure" in bench.l2_note(1024, 1024)
+    l2 = 126 << 20
+    assert "larger than L2" in bench.l2_note(bench.FULL_ROWS, bench.FULL_HIDDEN, l2)
+    assert "not a bench figure" in bench.l2_note(1024, 1024, l2)
+
+
+def test_recorded_traffic_follows_the_sources(tmp_path, monkeypatch):
+    """The DRAM-traffic record is data: it is used only while the kernel and plan sources hash
+    to the value it was taken on, and only for the shape it records."""
+    import json
+    rec = {"sources_sha": bench.kernel_source_sha(),
+           "launches": {"fused_add_rms_norm": {"shape": [bench.FULL_ROWS, bench.FULL_HIDDEN],
+                                               "dram_read_bytes": 1000,
+                                               "dram_write_bytes": 900}}}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(path))
+    assert bench.recorded_traffic("fused_add_rms_norm") == 1900
+    assert bench.recorded_traffic("rms_norm") is None
+    assert bench.recorded_traffic("fused_add_rms_norm", 4096, bench.FULL_HIDDEN) is None
+    rec["sources_sha"] = "0" * 16
+    path.write_text(json.dumps(rec))
+    assert bench.recorded_traffic("fused_add_rms_norm") is None
+    # the plan code is part of the hash
+    assert any(s.endswith("ks_abi.cu") for s in bench.KERNEL_SOURCES)
 
 
 def test_host_cpu_model_names_the_cpu():
