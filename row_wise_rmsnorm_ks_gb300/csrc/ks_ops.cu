@@ -102,17 +102,25 @@ __device__ __forceinline__ float rcp_sfu(float v) {
     return r;
 }
 
-// Softmax numerators for a pair of elements. Both forms first take the contract's FP32 difference
-// z = v - m (as v + (-m): the same IEEE operation), so z is bitwise the contract's whatever the
-// magnitude of m. fp32 outputs: e^z by expf. 16-bit outputs: e^z * 2^64 = 2^(z log2(e) + 64), one
-// FMA and one SFU op; the 2^64 cancels in e / sum and keeps every exp above 2^-190 normal
-// (smaller ones are below any fp32 output anyway). Folding -m log2(e) into one rounded bias
-// instead loses the row once |m log2(e)| passes 2^31: that bias's rounding error alone then
+// Softmax numerators for a pair of elements. fp32 outputs: e^z by expf, with z = v - m the
+// contract's FP32 difference (as v + (-m): the same IEEE operation). 16-bit outputs:
+// e^z * 2^64 = 2^(z log2(e) + 64) on the SFU; the 2^64 cancels in e / sum and keeps every exp
+// above 2^-190 normal (smaller ones are below any fp32 output anyway). Two forms, chosen per row
+// (a uniform branch): kFold, for rows with |m| <= kSoftmaxFoldMax, takes one FMA per element,
+// v log2(e) + (64 - m log2(e)), whose folded bias is off by at most half an ulp of 64 + 370,
+// 2^-16 in the exponent (1e-5 of the output, far below a 16-bit ulp); other rows first form z
+// exactly as the contract does, then z log2(e) + 64 (one operation more). Folding the bias for
+// any m would lose whole rows: once |m log2(e)| passes 2^31 the bias's rounding error alone
 // exceeds the 64 of exponent headroom.
-template <typename T, bool kPair>
-__device__ __forceinline__ float2 softmax_exp_pair(float2 v, float neg_m) {
+constexpr float kSoftmaxFoldMax = 256.0f;
+
+template <typename T, bool kPair, bool kFold>
+__device__ __forceinline__ float2 softmax_exp_pair(float2 v, float neg_m, float bias) {
     if constexpr (sizeof(T) == 4) {
         return make_float2(expf(__fadd_rn(v.x, neg_m)), expf(__fadd_rn(v.y, neg_m)));
+    } else if constexpr (kFold) {
+        const float2 t = pair_fma<kPair>(v, make_float2(kLog2e, kLog2e), make_float2(bias, bias));
+        return make_float2(ex2_sfu(t.x), ex2_sfu(t.y));
     } else {
         const float2 z = pair_add<kPair>(v, make_float2(neg_m, neg_m));
         const float2 t = pair_fma<kPair>(z, make_float2(kLog2e, kLog2e), make_float2(64.0f, 64.0f));
@@ -125,16 +133,17 @@ __device__ __forceinline__ float2 softmax_exp_pair(float2 v, float neg_m) {
 //  fp32 outputs: e^-g by expf, the correctly rounded reciprocal (bitwise the IEEE quotient).
 //  16-bit outputs: the sigmoid on the SFU. Its flush-to-zero ex2 and rcp would lose sigmoids
 //  below 2^-126 (gates in [-88.7, -87.3]), which a large `up` still carries into a 16-bit
-//  output, so the reciprocal is taken of den' = (1 + e^-g) * 2^-64 = 2^(-g log2(e) - 64) + 2^-64,
-//  which is normal for every gate that matters, and scaled back by an IEEE multiply (subnormal
-//  results kept): sigmoid = rcp(den') * 2^-64 <= 1. Where e^-g overflows FP32 (-g log2(e) >=
-//  128) the contract's sigmoid is 1/(1 + inf) = 0 exactly, and so is this one; a NaN gate keeps
-//  the NaN through g * 0.
+//  output, so the reciprocal is taken of den' = (1 + e^-g) * 2^-64 = fma(2^(-g log2(e)), 2^-64,
+//  2^-64), normal for every gate whose sigmoid is not 0, and scaled back by an IEEE multiply
+//  (subnormal results kept): sigmoid = rcp(den') * 2^-64 <= 1. Where e^-g overflows FP32
+//  (-g log2(e) >= 128, gates below about -88.72) ex2 gives inf, as the contract's exp does, so
+//  den' = inf and the sigmoid is 0 exactly, 1 / (1 + inf) as in the contract; e^-g below 2^-126
+//  flushes to 0, giving a sigmoid of 1, which 1 / (1 + e^-g) also rounds to. A NaN gate keeps
+//  the NaN.
 template <typename T>
 __device__ __forceinline__ float silu_mul(float g, float up) {
-    const float t = __fmul_rn(-g, kLog2e);
-    const float den = __fadd_rn(ex2_sfu(__fadd_rn(t, -64.0f)), kTwoPowM64);
-    const float sig = t < 128.0f ? __fmul_rn(rcp_sfu(den), kTwoPowM64) : 0.0f;
+    const float den = __fmaf_rn(ex2_sfu(__fmul_rn(-g, kLog2e)), kTwoPowM64, kTwoPowM64);
+    const float sig = __fmul_rn(rcp_sfu(den), kTwoPowM64);
     return __fmul_rn(__fmul_rn(g, sig), up);
 }
 template <>
@@ -336,19 +345,34 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
             }
         }
         m = team_max<kWarp>(m, red, slot);
-        // For m = +-inf or NaN, z is NaN or -inf where the formula's is, which gives the
-        // contract's NaN rows and masked entries.
+        // For m = +-inf or NaN, z (or the folded bias) is NaN or -inf where the formula's is,
+        // which gives the contract's NaN rows and masked entries; such rows take the exact form.
         const float neg_m = -m;
+        const float bias = __fmaf_rn(neg_m, kLog2e, 64.0f);
         // four running sums: element e feeds lane e % 2 of s[(e / 2) % 2]
         float2 s[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+        if (fabsf(m) <= kSoftmaxFoldMax) {
 #pragma unroll
-        for (int k = 0; k < V; ++k) {
-            const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
+            for (int k = 0; k < V; ++k) {
+                const int64_t c = t + (int64_t)k * g;
+                if (c < hv) {
 #pragma unroll
-                for (int i = 0; i < P; ++i) {
-                    f[k][i] = softmax_exp_pair<T, kPair>(f[k][i], neg_m);
-                    s[i & 1] = pair_add<kPair>(s[i & 1], f[k][i]);
+                    for (int i = 0; i < P; ++i) {
+                        f[k][i] = softmax_exp_pair<T, kPair, true>(f[k][i], neg_m, bias);
+                        s[i & 1] = pair_add<kPair>(s[i & 1], f[k][i]);
+                    }
+                }
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const int64_t c = t + (int64_t)k * g;
+                if (c < hv) {
+#pragma unroll
+                    for (int i = 0; i < P; ++i) {
+                        f[k][i] = softmax_exp_pair<T, kPair, false>(f[k][i], neg_m, bias);
+                        s[i & 1] = pair_add<kPair>(s[i & 1], f[k][i]);
+                    }
                 }
             }
         }
@@ -745,6 +769,8 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
         }
         m = cta_max(m, red, slot);
         const float neg_m = -m;
+        const float bias = __fmaf_rn(neg_m, kLog2e, 64.0f);
+        const bool fold = fabsf(m) <= kSoftmaxFoldMax;  // see softmax_exp_pair
         float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
         for (int64_t c0 = t; c0 < hv; c0 += chunk) {
             uint4 v[U];
@@ -760,7 +786,9 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
                     E::unpack2(v[u], f);
 #pragma unroll
                     for (int i = 0; i < P; ++i)
-                        s2[i & 1] = pair_add<kPair>(s2[i & 1], softmax_exp_pair<T, kPair>(f[i], neg_m));
+                        s2[i & 1] = pair_add<kPair>(
+                            s2[i & 1], fold ? softmax_exp_pair<T, kPair, true>(f[i], neg_m, bias)
+                                            : softmax_exp_pair<T, kPair, false>(f[i], neg_m, bias));
                 }
             }
         }
@@ -782,7 +810,10 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
                     float2 f[P];
                     E::unpack2(v[u], f);
 #pragma unroll
-                    for (int i = 0; i < P; ++i) f[i] = pair_mul<kPair>(softmax_exp_pair<T, kPair>(f[i], neg_m), inv2);
+                    for (int i = 0; i < P; ++i)
+                        f[i] = pair_mul<kPair>(fold ? softmax_exp_pair<T, kPair, true>(f[i], neg_m, bias)
+                                                    : softmax_exp_pair<T, kPair, false>(f[i], neg_m, bias),
+                                               inv2);
                     __stcs(orow + c, E::pack2(f));
                 }
             }
@@ -1033,18 +1064,19 @@ cudaError_t silu_dispatch(SiluPlan plan, void *out, const void *x, int64_t rows,
     }
     if (kind == kSiluRows) {
         // gx CTAs across a row, each of bx threads covering two vectors a thread (bx a multiple
-        // of 32, at most plan.max_block); narrow rows stack 256 / bx rows per CTA; about 8 CTAs
-        // per SM in all
+        // of 32, at most plan.max_block); narrow rows stack 256 / bx rows per CTA; as many CTAs
+        // as are resident at once (a CTA left for a second wave of this persistent grid would
+        // start only when a first-wave one has finished all its rows)
+        const void *f = (const void *)silu_mul_rows_kernel<T>;
         const int64_t gx = ceil_div64(dd, 2 * (int64_t)plan.max_block);
         const int bx = (int)round_up64(ceil_div64(dd, 2 * gx), 32);
         int64_t by = 256 / bx;
         by = by > rows ? rows : by;
         int64_t gy = ceil_div64(rows, by);
-        const int64_t cap = (int64_t)sms * 8 / gx;
+        const int64_t cap = (int64_t)sms * cached_occupancy(f, bx * (int)by, 0) / gx;
         gy = gy > cap ? cap : gy;
         gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
-        return launch((const void *)silu_mul_rows_kernel<T>, dim3((unsigned)gx, (unsigned)gy),
-                      dim3((unsigned)bx, (unsigned)by), args, s);
+        return launch(f, dim3((unsigned)gx, (unsigned)gy), dim3((unsigned)bx, (unsigned)by), args, s);
     }
     // scalar: enough CTAs to cover a row once; rows: fill ~8 waves of SMs
     int64_t gx = ceil_div64(d, 256);
