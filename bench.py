@@ -978,6 +978,130 @@ def run_sweep(args) -> int:
     return 0
 
 
+def ncu_launch_list(csv_path: str, kernel_prefix: str = "rows_"):
+    """(kernel name, gpu__time_duration in microseconds) of each launch in an ncu --csv launch
+    list, in launch order, for kernels whose name contains `kernel_prefix`."""
+    out = []
+    with open(csv_path, newline="") as f:
+        lines = [ln for ln in f if ln.startswith('"')]
+    for row in csv.DictReader(io.StringIO("".join(lines))):
+        if row.get("Metric Name") != "gpu__time_duration.sum":
+            continue
+        name = row.get("Kernel Name", "")
+        if kernel_prefix not in name:
+            continue
+        v = float(row["Metric Value"].replace(",", ""))
+        unit = row.get("Metric Unit", "ns")
+        out.append((name, v / 1e3 if unit == "ns" else v if unit == "us" else v * 1e3))
+    return out
+
+
+def kernel_times_table(jsonl_path: str, csv_path: str) -> str:
+    """A markdown table joining the kernel-times mode's JSON lines with the ncu launch list of the
+    same command: per case the median kernel time of its timed launches (ncu; caches flushed
+    before each, clocks not locked), the event p50 of the same launches, and the fraction of the
+    measured copy peak each implies."""
+    peak = measured_peaks()["hbm_gbs"]
+    cases = [json.loads(ln) for ln in open(jsonl_path) if ln.startswith('{"kernel_times"')]
+    launches = ncu_launch_list(csv_path)
+    need = sum(c["launches"] for c in cases)
+    if len(launches) != need:
+        raise SystemExit(f"the launch list has {len(launches)} launches of this library, the cases "
+                         f"made {need}: not the same command")
+    rows, i = [], 0
+    for c in cases:
+        mine = launches[i:i + c["launches"]]
+        i += c["launches"]
+        k_us = statistics.median(us for _, us in mine[1:])
+        p = c["plan"]
+        kern = p["kernel_name"] + (f" c{p['cluster']}" if p.get("cluster", 0) >= 2 else "")
+        rows.append(f"| {c['kernel_times']} | {c['dtype']} | {c['op']} | [{c['rows']}, {c['hidden']}] "
+                    f"| {kern} | {k_us:.2f} | {c['event_p50_us']:.2f} | "
+                    f"{c['bytes'] / (k_us * 1e-6) / 1e9 / peak:.3f} | {c['event_frac_of_peak']:.3f} |")
+    head = ("| case | dtype | op | [rows, H] | kernel | kernel µs (ncu) | event p50 µs | "
+            "of peak by kernel time | of peak by event |\n|---|---|---|---|---|---|---|---|---|")
+    return head + "\n" + "\n".join(rows)
+
+
+KERNEL_TIME_WIDE_H = (1536, 5120, 7168, 14336, 16384)
+
+
+def kernel_time_cases():
+    """The shapes the kernel-times mode runs, in its launch order: (tag, dtype, op, rows, hidden,
+    eps). The stated configurations (small [128, 1024]; medium [2048, 4096] fp16 and bf16; fused
+    [512, 4096] and decode [4, 1536]; prefill bf16 rows 1024..32768 at 8192; wide fp16/bf16
+    H x rows {1, 7, 333, 65536}), both ops where the configuration has both."""
+    out = [("small", "bf16", "rms_norm", 128, 1024, 1e-6)]
+    out += [("medium", dt, "rms_norm", 2048, 4096, 1e-6) for dt in ("fp16", "bf16")]
+    out += [("fused", "bf16", "fused_add_rms_norm", 512, 4096, 1e-6),
+            ("decode", "bf16", "fused_add_rms_norm", 4, 1536, 1e-6)]
+    out += [("prefill", "bf16", op, R, 8192, 1e-5) for R in (1024, 2048, 4096, 8192, 16384, 32768)
+            for op in ("rms_norm", "fused_add_rms_norm")]
+    out += [("wide", dt, op, R, H, 1e-6) for dt in ("bf16", "fp16") for H in KERNEL_TIME_WIDE_H
+            for R in (1, 7, 333, 65536) for op in ("rms_norm", "fused_add_rms_norm")]
+    return out
+
+
+def run_kernel_times(args) -> int:
+    """Every stated configuration, launched a fixed number of times in a fixed order, so that a
+    launch list taken by ncu over the same command (gpu__time_duration.sum, one pass) maps onto
+    the cases: per case one untimed launch, then --kernel-time-launches single launches, each
+    after the L2 is emptied (a 512 MiB read, outside the timed pair) and timed with CUDA events.
+    One JSON line per case (not the contract's line) with the event p50 and the number of this
+    library's launches it made, in order."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=dev)
+    peak = measured_peaks()["hbm_gbs"]
+    sms = device_facts(dev)["sm_count"]
+    codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16}
+    n = args.kernel_time_launches
+    for tag, dt, op, R, H, eps in kernel_time_cases():
+        if tag == "wide":
+            wl = synth.wide_device(op, H, R, dt, dev)
+            x, r, w = wl.x, wl.residual, wl.weight
+        else:
+            x = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), dt)
+            r = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev, std=2.0), dt)
+            w = synth.weight(H, dt).to(dev)
+        code = codes[dt]
+        st = torch.cuda.current_stream(dev)
+        if op == "rms_norm":
+            y = torch.empty_like(x)
+            fn = lambda: _abi.check(_abi.ks_rms_norm(y.data_ptr(), x.data_ptr(), w.data_ptr(), R,
+                                                     H, eps, code, st.cuda_stream))
+        else:
+            fn = lambda: _abi.check(_abi.ks_fused_add_rms_norm(x.data_ptr(), r.data_ptr(),
+                                                               w.data_ptr(), R, H, eps, code,
+                                                               st.cuda_stream))
+        fn()
+        us = []
+        for _ in range(n):
+            flush.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            fn()
+            b.record(st)
+            b.synchronize()
+            us.append(a.elapsed_time(b) * 1e3)
+        nb = algorithmic_bytes(op, R, H, 2)
+        plan = _abi.ks_plan_launch(0 if op == "rms_norm" else 1, R, H, code, True, sms, 0)[1]
+        p50 = statistics.median(us)
+        print(json.dumps({"kernel_times": tag, "dtype": dt, "op": op, "rows": R, "hidden": H,
+                          "launches": n + 1, "event_p50_us": p50,
+                          "event_frac_of_peak": nb / (p50 * 1e-6) / 1e9 / peak,
+                          "bytes": nb, "plan": plan.as_dict()}), flush=True)
+        del x, r, w
+        if tag == "wide":
+            del wl
+        torch.cuda.empty_cache()
+    return 0
+
+
 def plan_candidates(op: str, hv: int, elem: int):
     """Every launch plan the heuristic chooses among for a row of hv 16-byte vectors, named as in
     the plan-sweep tables: w4/w4n (warp per row, 4 vectors per lane, with/without prefetch;
@@ -1326,6 +1450,11 @@ def main() -> int:
     ap.add_argument("--sweep", action="store_true",
                     help="print the configuration sweeps, one JSON line per case, and exit")
     ap.add_argument("--sweep-samples", type=int, default=15)
+    ap.add_argument("--kernel-times", action="store_true",
+                    help="every stated configuration a fixed number of times, for an ncu launch list")
+    ap.add_argument("--kernel-time-launches", type=int, default=5)
+    ap.add_argument("--kernel-times-table", nargs=2, metavar=("JSONL", "NCU_CSV"),
+                    help="print the markdown table joining a kernel-times run with its ncu launch list")
     ap.add_argument("--plan-sweep", action="store_true",
                     help="time every candidate launch plan per dtype, op and width, and exit")
     ap.add_argument("--plan-contexts", action="store_true",
@@ -1350,6 +1479,11 @@ def main() -> int:
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.kernel_times:
+        return run_kernel_times(args)
+    if args.kernel_times_table:
+        print(kernel_times_table(*args.kernel_times_table))
+        return 0
     if args.plan_sweep:
         return run_plan_sweep(args)
     if args.plan_contexts:

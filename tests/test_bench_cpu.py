@@ -153,3 +153,38 @@ def test_oracle_all_cores_figure():
     d = bench.oracle_all_cores({"x": x, "xf": x.clone(), "r": r, "w": w}, R, H, 1e-5)
     assert d["value"] > 0 and 1 <= d["cores"] <= min(R, os.cpu_count())
     assert d["sample"].startswith(f"first {R} rows")
+
+
+def test_kernel_times_table_joins_the_launch_list(tmp_path):
+    """The kernel-times summary pairs each case with its own launches from an ncu launch list
+    (this library's kernels only, in order; the untimed first launch of each case left out) and
+    refuses a list from another command."""
+    import json
+    hdr = ('"ID","Process ID","Process Name","Host Name","Kernel Name","Context","Stream",'
+           '"Block Size","Grid Size","Device","CC","Section Name","Metric Name","Metric Unit",'
+           '"Metric Value"\n')
+
+    def row(i, name, ns):
+        return (f'"{i}","1","python3","h","{name}","1","7","(256, 1, 1)","(152, 1, 1)","0","10.3",'
+                f'"Command line profiler metrics","gpu__time_duration.sum","ns","{ns}"\n')
+    csv_text = "==PROF== Connected\n" + hdr
+    csv_text += row(0, "void at::native::reduce_kernel<...>", 500)  # not this library's
+    times = [9000, 2000, 2200, 2100, 30000, 10000, 10400, 10200]
+    for i, ns in enumerate(times):
+        csv_text += row(i + 1, "void rows_vec_kernel<bf16, 4, 0, 0, 0>(RowArgs)", ns)
+    (tmp_path / "l.csv").write_text(csv_text)
+    plan = {"kernel_name": "cta_row", "cluster": 0}
+    cases = [{"kernel_times": "small", "dtype": "bf16", "op": "rms_norm", "rows": 128,
+              "hidden": 1024, "launches": 4, "event_p50_us": 6.8, "event_frac_of_peak": 0.01,
+              "bytes": 526336, "plan": plan},
+             {"kernel_times": "fused", "dtype": "bf16", "op": "fused_add_rms_norm", "rows": 512,
+              "hidden": 4096, "launches": 4, "event_p50_us": 12.0, "event_frac_of_peak": 0.2,
+              "bytes": 16785408, "plan": plan}]
+    (tmp_path / "k.jsonl").write_text("".join(json.dumps(c) + "\n" for c in cases))
+    table = bench.kernel_times_table(str(tmp_path / "k.jsonl"), str(tmp_path / "l.csv"))
+    lines = table.splitlines()
+    assert len(lines) == 4
+    assert "| 2.10 | 6.80 |" in lines[2] and "| 10.20 | 12.00 |" in lines[3]
+    (tmp_path / "k.jsonl").write_text(json.dumps(cases[0]) + "\n")
+    with pytest.raises(SystemExit):
+        bench.kernel_times_table(str(tmp_path / "k.jsonl"), str(tmp_path / "l.csv"))
