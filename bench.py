@@ -1344,6 +1344,185 @@ def run_plan_contexts(args) -> int:
     return 0
 
 
+OPS_BAND_WIDTHS = {
+    # rows of 16-byte vectors at the edges of the Softmax and LayerNorm width bands
+    "softmax": (16, 32, 33, 44, 45, 52, 53, 63, 64, 65, 72, 80, 81, 96, 127, 128, 129, 168, 169,
+                176, 177, 192, 193, 216, 217, 224, 225, 256),
+    "layer_norm": (16, 32, 33, 63, 64, 65, 96, 127, 128, 129, 160, 192, 193, 224, 225, 256),
+    # the SwiGLU output row's vectors at the edges of its launch shapes
+    "silu_and_mul": (32, 64, 128, 159, 160, 161, 192, 193, 256, 287, 288, 447, 448, 512, 1024,
+                     2048),
+}
+
+
+def op_band_candidates(op: str, hv: int):
+    """The launch plans the next operators' width bands choose among for a row of hv vectors:
+    wV / wVn (a warp per row, V vectors a lane, with / without prefetch; where a warp covers the
+    row), cV / cVn (a CTA per row, V vectors a thread), and for SwiGLU flatB (the flat walk on
+    B-thread CTAs) and rowsB (the row kernel with at most B threads)."""
+    from row_wise_rmsnorm_ks_gb300 import _abi
+
+    up32 = lambda n: -(-n // 32) * 32
+    mk = _abi.make_plan
+    npf = _abi.KS_PLAN_NO_PREFETCH
+    out = []
+    if op == "silu_and_mul":
+        out += [("flat256", mk(_abi.KS_KERNEL_FLAT, 2, 256)),
+                ("flat128", mk(_abi.KS_KERNEL_FLAT, 2, 128))]
+        out += [(f"rows{b}", mk(_abi.KS_KERNEL_CTA_ROW, 2, b)) for b in (96, 128, 256)]
+        return out
+    for v in (2, 4, 6, 8):
+        if 32 * v >= hv:
+            out.append((f"w{v}", mk(_abi.KS_KERNEL_WARP_ROW, v, 128)))
+            if op == "softmax":
+                out.append((f"w{v}n", mk(_abi.KS_KERNEL_WARP_ROW, v, 128, flags=npf)))
+    for v in (1, 2, 4):
+        b = up32(-(-hv // v))
+        if b <= 512:
+            out.append((f"c{v}", mk(_abi.KS_KERNEL_CTA_ROW, v, b)))
+            if op == "softmax" and v == 4:
+                out.append(("c4n", mk(_abi.KS_KERNEL_CTA_ROW, 4, b, flags=npf)))
+    return out
+
+
+def run_ops_bands(args) -> int:
+    """The measurement behind the next operators' width bands (one JSON line per operator, dtype
+    and width; not the contract's line): every candidate of op_band_candidates() and the default
+    launch, through the *_planned entry points, in two contexts: steady (the same plan launched
+    back to back after 5 untimed launches) and right after one launch of a kernel that leaves a
+    large shared-memory carveout, as a GEMM would (the RMSNorm staged ring with 196 KiB of shared
+    memory; each launch timed alone). 384 MiB per input tensor, N(0,1) rows (SwiGLU gates N(0,4));
+    the plans alternate over --plan-sweep-rounds rounds and the median is kept, as a fraction of
+    the measured copy peak. A band takes the plan whose worse context scores best
+    (--ops-bands-table)."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    st = torch.cuda.current_stream(dev)
+    s = st.cuda_stream
+    peak = measured_peaks()["hbm_gbs"]
+    sms = device_facts(dev)["sm_count"]
+    codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
+    op_codes = {"silu_and_mul": _abi.OP_SILU_AND_MUL, "softmax": _abi.OP_SOFTMAX,
+                "layer_norm": _abi.OP_LAYER_NORM}
+    # the carveout kernel: RMSNorm through the staged ring, 6 stages of 2048 bf16 vectors
+    xa = synth.cast(synth.normal_dev((256, 16384), 1, dev), "bf16")
+    ya, wa = torch.empty_like(xa), synth.weight(16384, "bf16").to(dev)
+    ring = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 512, 6)
+    pre = lambda: _abi.check(_abi.ks_rms_norm_planned(ya.data_ptr(), xa.data_ptr(), wa.data_ptr(),
+                                                      256, 16384, 1e-5, _abi.KS_DTYPE_BF16, ring, s))
+
+    def steady(fn, n=30):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for _ in range(5):
+            fn()
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n * 1e-3
+
+    def after(fn, n=12):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(n):
+            pre()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b) * 1e-3
+        return tot / n
+
+    ops = args.ops_bands_ops.split(",")
+    for op in ops:
+        widths = ([int(v) for v in args.plan_sweep_widths.split(",")] if args.plan_sweep_widths
+                  else OPS_BAND_WIDTHS[op])
+        for dt in args.plan_sweep_dtypes.split(","):
+            elem = 4 if dt == "fp32" else 2
+            code = codes[dt]
+            for hv in widths:
+                H = hv * 16 // elem
+                if op == "silu_and_mul":
+                    R = (384 << 20) // (2 * H * elem)
+                    x = synth.cast(synth.normal_dev((R, 2 * H), synth.SEED_X, dev, std=2.0), dt)
+                    y = torch.empty((R, H), dtype=x.dtype, device=dev)
+                    nb = 3 * R * H * elem
+                    run = lambda p: _abi.ks_silu_and_mul_planned(y.data_ptr(), x.data_ptr(), R, H,
+                                                                 code, p, s)
+                    default = lambda: _abi.check(_abi.ks_silu_and_mul(y.data_ptr(), x.data_ptr(),
+                                                                      R, H, code, s))
+                else:
+                    R = (384 << 20) // (H * elem)
+                    x = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), dt)
+                    y = torch.empty_like(x)
+                    if op == "softmax":
+                        nb = 2 * R * H * elem
+                        run = lambda p: _abi.ks_softmax_planned(y.data_ptr(), x.data_ptr(), R, H,
+                                                                code, p, s)
+                        default = lambda: _abi.check(_abi.ks_softmax(y.data_ptr(), x.data_ptr(),
+                                                                     R, H, code, s))
+                    else:
+                        w = synth.weight(H, dt).to(dev)
+                        bias = synth.cast(synth.normal_np((H,), 7, std=0.1), dt).to(dev)
+                        nb = 2 * R * H * elem + 2 * H * elem
+                        run = lambda p: _abi.ks_layer_norm_planned(
+                            y.data_ptr(), x.data_ptr(), w.data_ptr(), bias.data_ptr(), R, H, 1e-5,
+                            code, p, s)
+                        default = lambda: _abi.check(_abi.ks_layer_norm(
+                            y.data_ptr(), x.data_ptr(), w.data_ptr(), bias.data_ptr(), R, H, 1e-5,
+                            code, s))
+                fns = [("default", default)]
+                for name, p in op_band_candidates(op, hv):
+                    if run(p) == _abi.KS_SUCCESS:  # a plan that does not fit is left out
+                        fns.append((name, (lambda p=p: _abi.check(run(p)))))
+                _, dp = _abi.ks_plan_launch(op_codes[op], R, H, code, True, sms, 0)
+                line = {"ops_bands": op, "dtype": dt, "hv": hv, "hidden": H, "rows": R,
+                        "default_plan": {k: dp.as_dict()[k] for k in ("kernel_name", "vec_per_thread",
+                                                                       "block", "flags")}}
+                for ctx in ("steady", "after_ring"):
+                    res = {name: [] for name, _ in fns}
+                    for _ in range(args.plan_sweep_rounds):
+                        for name, fn in fns:
+                            t = steady(fn) if ctx == "steady" else after(fn)
+                            res[name].append(nb / t / 1e9 / peak)
+                    line[ctx] = {k: round(statistics.median(v), 4) for k, v in res.items()}
+                print(json.dumps(line), flush=True)
+                del x, y
+                torch.cuda.empty_cache()
+    st_, flags = _abi.ks_device_faults(clear=False)
+    if st_ != _abi.KS_SUCCESS or flags:
+        print(json.dumps({"ops_bands": "device faults", "status": st_, "flags": flags}))
+        return 1
+    return 0
+
+
+def ops_bands_table(jsonl_path: str) -> str:
+    """A markdown table from an --ops-bands run: per operator, dtype and width, the default
+    launch's score and the best candidate's, each the worse of its two contexts."""
+    rows = []
+    for ln in open(jsonl_path):
+        if not ln.startswith('{"ops_bands"'):
+            continue
+        d = json.loads(ln)
+        if "steady" not in d:
+            continue
+        score = {k: min(d["steady"][k], d.get("after_ring", d["steady"]).get(k, 0.0))
+                 for k in d["steady"]}
+        best = max(score, key=score.get)
+        dp = d["default_plan"]
+        rows.append(f"| {d['ops_bands']} | {d['dtype']} | {d['hv']} | {dp['kernel_name']} v{dp['vec_per_thread']} "
+                    f"b{dp['block']}{' n' if dp['flags'] & 1 else ''} | {score['default']:.3f} | "
+                    f"{best} | {score[best]:.3f} | {score[best] - score['default']:+.3f} |")
+    head = ("| op | dtype | vectors | default plan | default score | best | best score | best - "
+            "default |\n|---|---|---|---|---|---|---|---|")
+    return head + "\n" + "\n".join(rows)
+
+
 def run_ops_scan(args) -> int:
     """The next operators' default launches over row widths (one JSON line per dtype and width;
     not the contract's line): Softmax, LayerNorm (weight and bias) and SwiGLU on rows of
@@ -1450,6 +1629,11 @@ def main() -> int:
     ap.add_argument("--sweep", action="store_true",
                     help="print the configuration sweeps, one JSON line per case, and exit")
     ap.add_argument("--sweep-samples", type=int, default=15)
+    ap.add_argument("--ops-bands", action="store_true",
+                    help="time the next operators' band candidates in two contexts (tuning)")
+    ap.add_argument("--ops-bands-ops", default="softmax,layer_norm,silu_and_mul")
+    ap.add_argument("--ops-bands-table", metavar="JSONL",
+                    help="print the markdown table of an --ops-bands run")
     ap.add_argument("--kernel-times", action="store_true",
                     help="every stated configuration a fixed number of times, for an ncu launch list")
     ap.add_argument("--kernel-time-launches", type=int, default=5)
@@ -1481,6 +1665,11 @@ def main() -> int:
         return run_sweep(args)
     if args.kernel_times:
         return run_kernel_times(args)
+    if args.ops_bands:
+        return run_ops_bands(args)
+    if args.ops_bands_table:
+        print(ops_bands_table(args.ops_bands_table))
+        return 0
     if args.kernel_times_table:
         print(kernel_times_table(*args.kernel_times_table))
         return 0

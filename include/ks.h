@@ -108,12 +108,17 @@ const char *ks_last_error(void);
  * depends on the dtype (the heuristic was set per dtype from a sweep of every variant), the row
  * width in 16-byte vectors and the row count; grid is an upper bound when cluster >= 2 (the
  * launch caps whole clusters by what the device can hold resident).
- *   op              0 = rms_norm, 1 = fused_add_rms_norm.
+ *   op              0 = rms_norm, 1 = fused_add_rms_norm, 2 = silu_and_mul (hidden = d, the
+ *                   output row's width), 3 = softmax, 4 = layer_norm.
  *   aligned16       non-zero when every pointer of the call is 16-byte aligned.
  *   sm_count        multiprocessors of the device (152 on GB300).
  *   blocks_per_sm   resident CTAs per SM for the chosen kernel (0: plan the CTA shape only and
- *                   leave grid at the number of CTAs one pass over the rows needs).
- * On success *plan describes the launch the entry points would make.
+ *                   leave grid at the number of CTAs one pass over the rows needs). Ops 2..4
+ *                   ignore it and leave grid 0: their launches size the grid from the kernel's
+ *                   occupancy on the device.
+ * On success *plan describes the launch the entry points would make. For ops 0 and 1 the L2
+ * budget of the two-pass kernels is taken as 96 MiB (about three quarters of a GB300's L2);
+ * the entry points use three quarters of the device's own L2.
  */
 typedef struct ks_plan {
     int32_t kernel;         /* KS_KERNEL_* below */
@@ -154,15 +159,35 @@ enum {
     KS_KERNEL_CLUSTER_ROW = 5, /* one cluster of `cluster` CTAs per row (few wide rows): each CTA
                                   holds a slice in registers and reduces it, partials exchanged
                                   in distributed shared memory */
-    KS_KERNEL_TWOPASS_ROW = 6  /* one CTA per row, any width: the row read twice with 16-byte
+    KS_KERNEL_TWOPASS_ROW = 6, /* one CTA per row, any width: the row read twice with 16-byte
                                   vectors (sum of squares, then outputs; the second pass from
                                   L2), vec_per_thread (2 or 4) vectors per thread in flight per
                                   step; the grid is capped so the rows in flight fit in L2,
                                   down to one CTA per SM. With cluster >= 2 each row is split
                                   over a cluster: CTA q runs both passes on its slice of
                                   ceil(hv / cluster) vectors and the slice sums meet in
-                                  distributed shared memory, one cluster barrier per row */
+                                  distributed shared memory, one cluster barrier per row.
+                                  Softmax and LayerNorm: their multi-pass wide kernel */
+    KS_KERNEL_FLAT = 7         /* SwiGLU only: a grid-stride walk over all rows' vectors */
 };
+
+/*
+ * What the kernel codes mean for the next operators (ks_silu_and_mul_planned,
+ * ks_softmax_planned, ks_layer_norm_planned; ks_plan_launch with op 2..4):
+ *   SwiGLU     KS_KERNEL_FLAT (block <= 256), KS_KERNEL_CTA_ROW (the row-structured kernel,
+ *              its block fitted to the row with at most `block` threads, 32..256),
+ *              KS_KERNEL_SCALAR (element loads, block <= 256).
+ *   Softmax,   KS_KERNEL_WARP_ROW (a warp per row, vec_per_thread 2, 4, 6 or 8, block / 32
+ *   LayerNorm  rows per CTA, block <= 128), KS_KERNEL_CTA_ROW (vec_per_thread 1, 2 or 4,
+ *              block <= 512, block * vec_per_thread >= the row's vectors),
+ *              KS_KERNEL_BULK_ROW (LayerNorm only: the staged ring, vec_per_thread 4,
+ *              `stages` 2..8), KS_KERNEL_TWOPASS_ROW (the multi-pass wide kernel, vec_per_thread
+ *              4, block <= 1024 for Softmax and 512 for LayerNorm), KS_KERNEL_SCALAR
+ *              (element loads, block <= 1024).
+ * KS_PLAN_NO_PREFETCH picks the variant that loads each row when it comes: Softmax warp rows at
+ * any vector count and CTA rows at 4 vectors (LayerNorm always prefetches; the flag is refused
+ * there). A grid > 0 caps the CTAs launched; 0 sizes the grid from the occupancy.
+ */
 
 ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t dtype,
                            int32_t aligned16, int32_t sm_count, int32_t blocks_per_sm,
@@ -313,6 +338,24 @@ ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, k
 ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const void *bias,
                           int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype,
                           ks_stream_t stream);
+
+/*
+ * The three operators above with an explicit launch plan instead of the built-in choice (a
+ * tuning hook, as ks_rms_norm_planned is for RMSNorm: a plan from ks_plan_launch with op 2, 3 or
+ * 4, edited; the kernel codes as listed after the KS_KERNEL_* enum). Arguments, semantics and
+ * errors are those of the plain entry points, plus KS_ERR_INVALID_ARGUMENT, before any CUDA
+ * call, for a NULL plan or one that does not fit the call (an unknown kernel for the operator, a
+ * vector kernel on rows or pointers that are not 16-byte aligned, a team that does not cover the
+ * row, a block or ring outside the kernel's bounds, a variant that does not exist). The plan is
+ * read, never written; its derived fields are recomputed.
+ */
+ks_status_t ks_silu_and_mul_planned(void *out, const void *x, int64_t rows, int64_t d,
+                                    ks_dtype_t dtype, const ks_plan_t *plan, ks_stream_t stream);
+ks_status_t ks_softmax_planned(void *out, const void *x, int64_t rows, int64_t hidden,
+                               ks_dtype_t dtype, const ks_plan_t *plan, ks_stream_t stream);
+ks_status_t ks_layer_norm_planned(void *out, const void *x, const void *weight, const void *bias,
+                                  int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype,
+                                  const ks_plan_t *plan, ks_stream_t stream);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int32_t ks_version(void);

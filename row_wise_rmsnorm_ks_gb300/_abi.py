@@ -16,9 +16,11 @@ LIB_PATH = os.path.join(_HERE, "_build", "libks.so")
 KS_DTYPE_F32, KS_DTYPE_F16, KS_DTYPE_BF16 = 0, 1, 2
 KS_SUCCESS, KS_ERR_INVALID_ARGUMENT, KS_ERR_UNSUPPORTED_DTYPE, KS_ERR_OVERLAP, KS_ERR_CUDA = range(5)
 (KS_KERNEL_NONE, KS_KERNEL_WARP_ROW, KS_KERNEL_CTA_ROW, KS_KERNEL_SCALAR, KS_KERNEL_BULK_ROW,
- KS_KERNEL_CLUSTER_ROW, KS_KERNEL_TWOPASS_ROW) = range(7)
+ KS_KERNEL_CLUSTER_ROW, KS_KERNEL_TWOPASS_ROW, KS_KERNEL_FLAT) = range(8)
 KERNEL_NAMES = {0: "none", 1: "warp_row", 2: "cta_row", 3: "scalar", 4: "bulk_row",
-                5: "cluster_row", 6: "twopass_row"}
+                5: "cluster_row", 6: "twopass_row", 7: "flat"}
+# ks_plan_launch's op codes
+OP_RMS_NORM, OP_FUSED_ADD_RMS_NORM, OP_SILU_AND_MUL, OP_SOFTMAX, OP_LAYER_NORM = range(5)
 KS_FAULT_WAIT_TIMEOUT = 1
 KS_PLAN_NO_PREFETCH = 1
 KS_PLAN_PDL = 2
@@ -30,6 +32,7 @@ EXPORTED = ("ks_rms_norm", "ks_fused_add_rms_norm", "ks_status_string", "ks_last
             "ks_device_faults", "ks_rms_norm_host", "ks_fused_add_rms_norm_host",
             "ks_host_chunk_rows", "ks_fused_add_rms_norm_host_noalloc", "ks_set_launch_options",
             "ks_get_launch_options", "ks_silu_and_mul", "ks_softmax", "ks_layer_norm",
+            "ks_silu_and_mul_planned", "ks_softmax_planned", "ks_layer_norm_planned",
             "ks_version")
 
 
@@ -114,6 +117,12 @@ def load(path: str | None = None):
         lib.ks_softmax.restype = ctypes.c_int
         lib.ks_layer_norm.argtypes = [vp, vp, vp, vp, i64, i64, f32, ctypes.c_int, vp]
         lib.ks_layer_norm.restype = ctypes.c_int
+        lib.ks_silu_and_mul_planned.argtypes = [vp, vp, i64, i64, ctypes.c_int, PP, vp]
+        lib.ks_silu_and_mul_planned.restype = ctypes.c_int
+        lib.ks_softmax_planned.argtypes = [vp, vp, i64, i64, ctypes.c_int, PP, vp]
+        lib.ks_softmax_planned.restype = ctypes.c_int
+        lib.ks_layer_norm_planned.argtypes = [vp, vp, vp, vp, i64, i64, f32, ctypes.c_int, PP, vp]
+        lib.ks_layer_norm_planned.restype = ctypes.c_int
         lib.ks_version.argtypes = []
         lib.ks_version.restype = i32
         _lib = lib
@@ -219,6 +228,23 @@ def ks_softmax(out: int, x: int, rows: int, hidden: int, dtype: int, stream: int
 def ks_layer_norm(out: int, x: int, weight: int | None, bias: int | None, rows: int, hidden: int,
                   eps: float, dtype: int, stream: int | None) -> int:
     return load().ks_layer_norm(out, x, weight, bias, rows, hidden, eps, dtype, stream)
+
+
+def ks_silu_and_mul_planned(out: int, x: int, rows: int, d: int, dtype: int, plan: ks_plan_t,
+                            stream: int | None) -> int:
+    return load().ks_silu_and_mul_planned(out, x, rows, d, dtype, ctypes.byref(plan), stream)
+
+
+def ks_softmax_planned(out: int, x: int, rows: int, hidden: int, dtype: int, plan: ks_plan_t,
+                       stream: int | None) -> int:
+    return load().ks_softmax_planned(out, x, rows, hidden, dtype, ctypes.byref(plan), stream)
+
+
+def ks_layer_norm_planned(out: int, x: int, weight: int | None, bias: int | None, rows: int,
+                          hidden: int, eps: float, dtype: int, plan: ks_plan_t,
+                          stream: int | None) -> int:
+    return load().ks_layer_norm_planned(out, x, weight, bias, rows, hidden, eps, dtype,
+                                        ctypes.byref(plan), stream)
 
 
 def ks_version() -> int:

@@ -501,7 +501,7 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
     memset(p, 0, sizeof *p);
     const int elem = elem_bytes(dtype);
     if (elem == 0) return fail(KS_ERR_UNSUPPORTED_DTYPE, "dtype code %d is not a ks_dtype_t", (int)dtype);
-    if (op != 0 && op != 1) return fail(KS_ERR_INVALID_ARGUMENT, "op must be 0 or 1");
+    if (op != 0 && op != 1) return fail(KS_ERR_INVALID_ARGUMENT, "op must be 0 to 4");
     if (hidden <= 0 || rows < 0 || sm_count <= 0 || blocks_per_sm < 0)
         return fail(KS_ERR_INVALID_ARGUMENT, "bad plan arguments");
     if (rows == 0) {
@@ -672,6 +672,12 @@ ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t 
                            ks_plan_t *plan) {
     const int e = ks::elem_bytes(dtype);
     if (e == 0) return ks::fail(KS_ERR_UNSUPPORTED_DTYPE, "dtype code %d is not a ks_dtype_t", (int)dtype);
+    if (op >= 2 && op <= 4) {
+        if (!plan) return ks::fail(KS_ERR_INVALID_ARGUMENT, "plan pointer is NULL");
+        if (hidden <= 0 || rows < 0 || sm_count <= 0)
+            return ks::fail(KS_ERR_INVALID_ARGUMENT, "bad plan arguments");
+        return ks::op_plan(op, rows, hidden, dtype, aligned16 != 0, sm_count, plan);
+    }
     return ks::plan(op, rows, hidden, dtype, aligned16 != 0, sm_count, blocks_per_sm, 0, plan);
 }
 

@@ -52,6 +52,11 @@ bool launch_pdl_enabled();
 ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
                  int sm_count, int blocks_per_sm, int64_t l2_bytes, ks_plan_t *p);
 
+// The next operators' default launch plan (op 2 SwiGLU with hidden = d, 3 Softmax, 4 LayerNorm),
+// pure host code; grid left 0 (sized from the occupancy at launch).
+ks_status_t op_plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
+                    int sm_count, ks_plan_t *p);
+
 // Per-dtype launchers (one translation unit each). `blocks_per_sm` queries the occupancy of the
 // kernel the plan names; `max_clusters` how many of its clusters can be resident at once (plans
 // with cluster >= 2; 0 if the query fails); `launch` enqueues it.

@@ -974,14 +974,12 @@ int row_vec_plan(int64_t hv, int *block) {
     return v;
 }
 
-// Rows wider than the register kernels hold take the wide multi-pass kernels (marked by this
-// vector count), 4 vectors per thread per step. Small CTAs keep more rows in flight per SM;
+// Rows wider than the register kernels hold take the wide multi-pass kernels, 4 vectors per
+// thread per step. Small CTAs keep more rows in flight per SM;
 // measured on GB300 (bf16, HBM-bound rows), the best block grows with the width: Softmax 128
 // threads up to 3072 vectors, 256 up to 6144, 512 beyond (0.66-0.87 of the copy peak, against
 // 0.62-0.79 at a fixed 512); LayerNorm 128 up to 3072, 256 up to 12288, 512 beyond (0.52-0.86,
 // against 0.38-0.62).
-constexpr int kWideRows = 16;
-
 int wide_row_block(int64_t hv, bool layer_norm) {
     if (hv <= 3072) return 128;
     if (hv <= (layer_norm ? 12288 : 6144)) return 256;
@@ -1005,119 +1003,73 @@ ks_status_t check_common(int64_t rows, int64_t width, ks_dtype_t dtype, int *e) 
     return KS_SUCCESS;
 }
 
-cudaError_t launch(const void *f, dim3 grid, dim3 block, void **args, cudaStream_t s) {
-    if (launch_pdl_enabled()) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = block;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        return cudaLaunchKernelExC(&cfg, f, args);
-    }
-    return cudaLaunchKernel(f, grid, block, args, 0, s);
+// ------------------------------------------------------------------------ launch plans
+//
+// The next operators' launches are described by ks_plan_t as well (include/ks.h), so that
+// ks_plan_launch reports the heuristic's choice and the *_planned entry points take an explicit
+// one (the tuning hook behind bench.py --ops-bands):
+//   SwiGLU     KS_KERNEL_FLAT         the flat walk over all rows' vectors (block <= 256)
+//              KS_KERNEL_CTA_ROW      the row-structured kernel, its block fitted to the row with
+//                                     at most `block` (32..256) threads
+//              KS_KERNEL_SCALAR       element loads (any width and alignment; block <= 256)
+//   Softmax,   KS_KERNEL_WARP_ROW     a warp per row, 2/4/6/8 vectors per lane, block/32 rows
+//   LayerNorm                         per CTA (block 32..128)
+//              KS_KERNEL_CTA_ROW      a CTA per row, 1/2/4 vectors per thread (block <= 512)
+//              KS_KERNEL_BULK_ROW     LayerNorm: rows through the staged ring, 4 vectors per
+//                                     thread, `stages` 2..8 rows
+//              KS_KERNEL_TWOPASS_ROW  the multi-pass wide kernel, 4 vectors a step per thread
+//                                     (block <= 1024 Softmax, 512 LayerNorm)
+//              KS_KERNEL_SCALAR       element loads (any width and alignment; block <= 1024)
+// KS_PLAN_NO_PREFETCH selects the register kernels' variant that loads each row when it comes:
+// Softmax warp rows at any vector count and CTA rows at 4 vectors (LayerNorm always prefetches).
+// KS_PLAN_PDL: programmatic dependent launch. A plan's grid > 0 caps the CTAs launched.
+
+constexpr int kOpSilu = 2, kOpSoftmax = 3, kOpLayerNorm = 4;  // ks_plan_launch's op codes
+
+ks_plan_t op_plan_of(int kernel, int v, int block, bool prefetch, int stages = 0) {
+    ks_plan_t p;
+    memset(&p, 0, sizeof p);
+    p.kernel = kernel;
+    p.vec_per_thread = v;
+    p.block = block;
+    p.team = kernel == KS_KERNEL_WARP_ROW ? 32 : block;
+    p.flags = prefetch ? 0 : KS_PLAN_NO_PREFETCH;
+    p.stages = stages;
+    return p;
 }
 
-// SwiGLU launch shapes. kSiluRows: the row-structured kernel with its block fitted to the row,
-// at most `max_block` threads; kSiluFlat: the flat walk over all rows' vectors; kSiluScalar:
-// element loads (rows that cannot be vectorised).
-enum SiluKind { kSiluScalar, kSiluRows, kSiluFlat };
+bool op_prefetch(const ks_plan_t &p) { return !(p.flags & KS_PLAN_NO_PREFETCH); }
 
-struct SiluPlan {
-    SiluKind kind;
-    int max_block;
-};
-
-// Measured on GB300 over widths of 16..2048 vectors (144..512 in steps of 8 to 32), many rows,
-// each plan timed in steady state and right after a kernel with a large shared-memory carveout
-// (as after a GEMM), the worse of the two kept. The flat walk held 0.81-0.88 of the copy peak for
-// 16-bit types at every width and 0.93-0.98 for fp32, whose rows it serves best throughout. The
-// row-structured kernel beats it for 16-bit rows of 160 and 192 vectors (0.88-0.93) and of
-// 288..447 (0.86-0.94), and from 448 vectors with its block capped at 96 threads (0.86-0.95;
-// with 128..256-thread CTAs some of those widths fell to 0.77-0.84, e.g. bf16 dv = 1024: 0.82);
-// at the other widths below 288 it fell as low as 0.59.
-SiluPlan silu_plan(bool vec, int64_t dv, ks_dtype_t dtype) {
-    if (!vec) return {kSiluScalar, 256};
-    if (dtype == KS_DTYPE_F32) return {kSiluFlat, 256};
-    if (dv >= 448) return {kSiluRows, 96};
-    if (dv >= 288 || dv == 160 || dv == 192) return {kSiluRows, 256};
-    return {kSiluFlat, 256};
+int scalar_block(int64_t width, int max_block) {
+    int b = (int)round_up64(ceil_div64(width, 8), 32);
+    return b < 32 ? 32 : (b > max_block ? max_block : b);
 }
 
-template <typename T>
-cudaError_t silu_dispatch(SiluPlan plan, void *out, const void *x, int64_t rows, int64_t d,
-                          int sms, cudaStream_t s) {
-    const SiluKind kind = plan.kind;
-    int64_t nr = rows, dd = kind == kSiluScalar ? d : d / Elem<T>::kPerVec;
-    void *args[] = {&out, const_cast<void **>(&x), &nr, &dd};
-    if (kind == kSiluFlat) {
-        // a persistent grid of as many 256-thread CTAs as are resident at once (fewer if the
-        // vectors run out), two vectors per thread per iteration
-        const void *f = (const void *)silu_mul_flat_kernel<T>;
-        const int n = cached_occupancy(f, 256, 0);
-        int64_t grid = ceil_div64(rows * dd, 512);
-        grid = grid > (int64_t)sms * n ? (int64_t)sms * n : grid;
-        return launch(f, dim3((unsigned)grid), dim3(256), args, s);
-    }
-    if (kind == kSiluRows) {
-        // gx CTAs across a row, each of bx threads covering two vectors a thread (bx a multiple
-        // of 32, at most plan.max_block); narrow rows stack 256 / bx rows per CTA; as many CTAs
-        // as are resident at once (a CTA left for a second wave of this persistent grid would
-        // start only when a first-wave one has finished all its rows)
-        const void *f = (const void *)silu_mul_rows_kernel<T>;
-        const int64_t gx = ceil_div64(dd, 2 * (int64_t)plan.max_block);
-        const int bx = (int)round_up64(ceil_div64(dd, 2 * gx), 32);
-        int64_t by = 256 / bx;
-        by = by > rows ? rows : by;
-        int64_t gy = ceil_div64(rows, by);
-        const int64_t cap = (int64_t)sms * cached_occupancy(f, bx * (int)by, 0) / gx;
-        gy = gy > cap ? cap : gy;
-        gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
-        return launch(f, dim3((unsigned)gx, (unsigned)gy), dim3((unsigned)bx, (unsigned)by), args, s);
-    }
-    // scalar: enough CTAs to cover a row once; rows: fill ~8 waves of SMs
-    int64_t gx = ceil_div64(d, 256);
-    gx = gx < 1 ? 1 : gx;
-    int64_t gy = (int64_t)sms * 8 / gx;
-    gy = gy < 1 ? 1 : (gy > rows ? rows : gy);
-    gy = gy > 65535 ? 65535 : gy;
-    return launch((const void *)silu_mul_scalar_kernel<T>, dim3((unsigned)gx, (unsigned)gy),
-                  dim3(256), args, s);
-}
-
-// A register-row launch for Softmax and LayerNorm: V 16-byte vectors per thread, one CTA of
-// `block` threads per row or (warp) one warp per row with block / 32 rows per CTA; prefetch:
-// load the next row before reducing the current one. v == kWideRows: the multi-pass wide kernel;
-// v == 0: the scalar kernel. Warp plans launch 128-thread CTAs (the warp kernels' launch bound,
-// which leaves them up to 255 registers for two rows of up to 8 vectors a lane).
-struct RegPlan {
-    int v;
-    int block;
-    bool warp;
-    bool prefetch;
-};
-
-// Grid of a register-row launch: as many CTAs as are resident at once, no more than the rows
-// need.
-int64_t reg_grid(const void *f, const RegPlan &p, size_t smem, int64_t rows, int sms) {
-    const int n = cached_occupancy(f, p.block, smem);
-    const int64_t per_cta = p.warp ? p.block / 32 : 1;
-    const int64_t need = ceil_div64(rows, per_cta);
-    const int64_t grid = (int64_t)sms * n;
-    return grid > need ? need : grid;
+// SwiGLU. Measured on GB300 over widths of 16..2048 vectors (144..512 in steps of 8 to 32), many
+// rows, each plan timed in steady state and right after a kernel with a large shared-memory
+// carveout (as after a GEMM), the worse of the two kept. The flat walk held 0.81-0.88 of the copy
+// peak for 16-bit types at every width and 0.93-0.98 for fp32, whose rows it serves best
+// throughout. The row-structured kernel beats it for 16-bit rows of 160 and 192 vectors
+// (0.88-0.93) and of 288..447 (0.86-0.94), and from 448 vectors with its block capped at 96
+// threads (0.86-0.95; with 128..256-thread CTAs some of those widths fell to 0.77-0.84, e.g. bf16
+// dv = 1024: 0.82); at the other widths below 288 it fell as low as 0.59.
+ks_plan_t silu_plan(bool vec, int64_t dv, ks_dtype_t dtype) {
+    if (!vec) return op_plan_of(KS_KERNEL_SCALAR, 0, 256, true);
+    if (dtype == KS_DTYPE_F32) return op_plan_of(KS_KERNEL_FLAT, 2, 256, true);
+    if (dv >= 448) return op_plan_of(KS_KERNEL_CTA_ROW, 2, 96, true);
+    if (dv >= 288 || dv == 160 || dv == 192) return op_plan_of(KS_KERNEL_CTA_ROW, 2, 256, true);
+    return op_plan_of(KS_KERNEL_FLAT, 2, 256, true);
 }
 
 // Width bands for many rows (more rows than SMs) of at most 256 vectors, measured on GB300 per
 // dtype, each plan timed in steady state and right after a kernel with a large shared-memory
-// carveout, the worse of the two kept: rows up to `hi` vectors take one warp per row at `v`
-// vectors per lane (kind 'w'), a CTA per row at 4 vectors with prefetch (kind 'c'), or the
-// general rule (kind 'g'). A CTA per row of 33..64 threads, most of them idle or split across
-// two partly filled warps, paid two CTA barriers per row; warp rows reduce with shuffles alone
-// and fill their lanes. Gains over the general rule at the narrowest widths were 20-39 points of
-// the copy peak (Softmax bf16 72 vectors: 0.52 -> 0.91; LayerNorm fp16 96 vectors: 0.53 -> 0.85).
+// carveout, the worse of the two kept (bench.py --ops-bands re-runs that measurement): rows up
+// to `hi` vectors take one warp per row at `v` vectors per lane (kind 'w'), a CTA per row at 4
+// vectors with prefetch (kind 'c'), or the general rule (kind 'g'). A CTA per row of 33..64
+// threads, most of them idle or split across two partly filled warps, paid two CTA barriers per
+// row; warp rows reduce with shuffles alone and fill their lanes. Gains over the general rule at
+// the narrowest widths were 20-39 points of the copy peak (Softmax bf16 72 vectors: 0.52 -> 0.91;
+// LayerNorm fp16 96 vectors: 0.53 -> 0.85).
 struct Band {
     int16_t hi;
     char kind;
@@ -1143,94 +1095,247 @@ constexpr Band kLayerNormF32[] = {{63, 'w', 2, true}, {64, 'g', 0, true}, {128, 
 
 // Applies the band of a row of hv vectors to p (the general rule's plan) when there are more rows
 // than SMs; warp plans take 128-thread CTAs (4 rows each).
-void apply_band(const Band *bands, int64_t hv, int64_t rows, int sms, RegPlan *p) {
+void apply_band(const Band *bands, int64_t hv, int64_t rows, int sms, ks_plan_t *p) {
     if (rows <= sms || hv > 256) return;
     const Band *b = bands;
     while (hv > b->hi) ++b;
-    if (b->kind == 'w') {
-        *p = RegPlan{b->v, 128, true, b->prefetch};
-    } else if (b->kind == 'c') {
-        *p = RegPlan{b->v, (int)round_up64(ceil_div64(hv, b->v), 32), false, b->prefetch};
-    }
+    if (b->kind == 'w')
+        *p = op_plan_of(KS_KERNEL_WARP_ROW, b->v, 128, b->prefetch);
+    else if (b->kind == 'c')
+        *p = op_plan_of(KS_KERNEL_CTA_ROW, b->v, (int)round_up64(ceil_div64(hv, b->v), 32), b->prefetch);
 }
 
 // Softmax: rows of up to 512 threads x V vectors in registers (V from row_vec_plan; at 4 vectors
 // no prefetch up to 1024 vectors: measured on GB300 (bf16, HBM-bound rows) 0.92-0.97 of the copy
 // peak for rows of 128..1024 vectors against 0.85-0.93 with it; beyond, prefetch wins), the wide
 // kernel for wider rows, the scalar kernel for rows that cannot be vectorised; many rows of at
-// most 256 vectors by the bands above.
-RegPlan softmax_plan(bool aligned, int64_t width, int64_t rows, int sms, ks_dtype_t dtype) {
-    RegPlan p{0, 0, false, true};
-    if (!aligned) return p;
-    p.v = row_vec_plan(width, &p.block);
-    if (p.v == 0) {
-        p.v = kWideRows;
-        p.block = wide_row_block(width, false);
-    } else if (p.v == 4) {
-        p.prefetch = width > 1024;
-    }
+// most 256 vectors by the bands above. `width` is in 16-byte vectors when aligned, else elements.
+ks_plan_t softmax_plan(bool aligned, int64_t width, int64_t rows, int sms, ks_dtype_t dtype) {
+    if (!aligned) return op_plan_of(KS_KERNEL_SCALAR, 0, scalar_block(width, 1024), true);
+    int block = 0;
+    const int v = row_vec_plan(width, &block);
+    ks_plan_t p = v == 0 ? op_plan_of(KS_KERNEL_TWOPASS_ROW, 4, wide_row_block(width, false), true)
+                         : op_plan_of(KS_KERNEL_CTA_ROW, v, block, v != 4 || width > 1024);
     apply_band(dtype == KS_DTYPE_F32 ? kSoftmax32 : kSoftmax16, width, rows, sms, &p);
     return p;
-}
-
-// LayerNorm: register rows (V from row_vec_plan, next row always prefetched: without it the two
-// reductions per row left it at 0.50-0.66 of the copy peak), the staged ring and the wide kernel
-// for many wider rows (layer_norm_dispatch), the scalar kernel for rows that cannot be
-// vectorised; many rows of at most 256 vectors by the bands above.
-RegPlan layer_norm_plan(bool aligned, int64_t hv, int64_t rows, int sms, ks_dtype_t dtype) {
-    RegPlan p{0, 0, false, true};
-    if (!aligned) return p;
-    p.v = row_vec_plan(hv, &p.block);
-    if (p.v == 0) {
-        p.v = kWideRows;
-        p.block = wide_row_block(hv, true);  // at most 512: the kernel's bound
-    }
-    apply_band(dtype == KS_DTYPE_BF16 ? kLayerNormBf16
-               : dtype == KS_DTYPE_F16 ? kLayerNormF16 : kLayerNormF32, hv, rows, sms, &p);
-    return p;
-}
-
-template <typename T>
-cudaError_t softmax_dispatch(RegPlan p, void *out, const void *x, int64_t rows, int64_t width,
-                             int sms, cudaStream_t s) {
-    int64_t nr = rows, wd = width;
-    void *args[] = {&out, const_cast<void **>(&x), &nr, &wd};
-    const void *f = nullptr;
-    if (p.warp) {
-        if (32 * (int64_t)p.v < width) return cudaErrorInvalidConfiguration;  // a warp must cover the row
-        switch (p.v) {
-        case 2: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 2, true, true>
-                               : (const void *)softmax_vec_kernel<T, 2, false, true>; break;
-        case 4: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 4, true, true>
-                               : (const void *)softmax_vec_kernel<T, 4, false, true>; break;
-        case 6: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 6, true, true>
-                               : (const void *)softmax_vec_kernel<T, 6, false, true>; break;
-        case 8: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 8, true, true>
-                               : (const void *)softmax_vec_kernel<T, 8, false, true>; break;
-        default: return cudaErrorInvalidConfiguration;
-        }
-    } else {
-        switch (p.v) {
-        case 1: f = (const void *)softmax_vec_kernel<T, 1, true>; break;
-        case 2: f = (const void *)softmax_vec_kernel<T, 2, true>; break;
-        case 4: f = p.prefetch ? (const void *)softmax_vec_kernel<T, 4, true>
-                               : (const void *)softmax_vec_kernel<T, 4, false>; break;
-        case kWideRows: f = (const void *)softmax_wide_kernel<T, 4>; break;
-        default:
-            f = (const void *)softmax_scalar_kernel<T>;
-            p.block = (int)round_up64(ceil_div64(width, 8), 32);
-            p.block = p.block < 32 ? 32 : (p.block > 1024 ? 1024 : p.block);
-        }
-    }
-    int64_t grid = reg_grid(f, p, 0, rows, sms);
-    if (p.v == kWideRows && grid > wide_grid_cap(width, sms)) grid = wide_grid_cap(width, sms);
-    return launch(f, dim3((unsigned)grid), dim3(p.block), args, s);
 }
 
 // Bytes of rows in each CTA's LayerNorm ring (a tuning constant, set from a GB300 measurement).
 #ifndef KS_LN_RING_BYTES
 #define KS_LN_RING_BYTES (64 * 1024)
 #endif
+
+// LayerNorm: register rows (V from row_vec_plan, next row always prefetched: without it the two
+// reductions per row left it at 0.50-0.66 of the copy peak), the wide kernel for wider rows, the
+// scalar kernel for rows that cannot be vectorised; many rows of at most 256 vectors by the bands
+// above. Many rows (at least 4 per SM) wider than 512 vectors: the staged ring (KS_LN_RING_BYTES
+// of rows per CTA, 2..8 stages) keeps enough bytes in flight, where the register kernel measured
+// faster up to 512 vectors (0.74-0.82 of the copy peak against 0.65-0.69 for the ring). Between
+// 1024 and 2048 vectors the ring's CTA (a thread per 4 vectors, ~105 registers for 16-bit types)
+// leaves one CTA of 8-14 warps per SM; the wide kernel's 128-thread CTAs keep more warps resident
+// and measured faster on GB300 for many rows: bf16 1280..1792 vectors 0.76-0.83 of the copy peak
+// against 0.65-0.78, fp32 1024..1792 0.88-0.95 against 0.76-0.86 (at 1024 bf16 vectors the ring
+// measured 0.96 against 0.81, so 16-bit rows start above it).
+ks_plan_t layer_norm_plan(bool aligned, int64_t hv, int64_t hidden, int64_t rows, int sms,
+                          ks_dtype_t dtype) {
+    if (!aligned) return op_plan_of(KS_KERNEL_SCALAR, 0, scalar_block(hidden, 1024), true);
+    int block = 0;
+    const int v = row_vec_plan(hv, &block);
+    ks_plan_t p = v == 0 ? op_plan_of(KS_KERNEL_TWOPASS_ROW, 4, wide_row_block(hv, true), true)
+                         : op_plan_of(KS_KERNEL_CTA_ROW, v, block, true);
+    apply_band(dtype == KS_DTYPE_BF16 ? kLayerNormBf16
+               : dtype == KS_DTYPE_F16 ? kLayerNormF16 : kLayerNormF32, hv, rows, sms, &p);
+    if (p.kernel == KS_KERNEL_CTA_ROW && v == 4 && hv > 512 && rows >= 4 * (int64_t)sms) {
+        if (hv < 2048 && hv >= (dtype == KS_DTYPE_F32 ? 1024 : 1025)) {
+            p = op_plan_of(KS_KERNEL_TWOPASS_ROW, 4, 128, true);
+        } else {
+            const int64_t n = (KS_LN_RING_BYTES) / (hv * 16);
+            p = op_plan_of(KS_KERNEL_BULK_ROW, 4, block, true, (int)(n < 2 ? 2 : (n > 8 ? 8 : n)));
+        }
+    }
+    return p;
+}
+
+// The ring's dynamic shared memory: its mbarriers, then `stages` rows of hv vectors.
+size_t ln_ring_smem(int stages, int64_t hv) { return 128 + (size_t)stages * (size_t)hv * 16; }
+
+// Checks an explicit plan for op (2 SwiGLU, 3 Softmax, 4 LayerNorm) against the call, before any
+// CUDA call; `vec` tells whether the rows and pointers take 16-byte vectors, `width` is the row's
+// width in 16-byte vectors when they do (for SwiGLU the output row's), `elems` in elements.
+ks_status_t op_check(int op, ks_plan_t &p, bool vec, int64_t width, int64_t elems) {
+    if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL))
+        return fail(KS_ERR_INVALID_ARGUMENT, "unknown plan flags 0x%x", (unsigned)p.flags);
+    if (p.block < 32 || p.block % 32 != 0)
+        return fail(KS_ERR_INVALID_ARGUMENT, "plan block %d is not a positive multiple of 32", p.block);
+    if (p.kernel != KS_KERNEL_SCALAR && !vec)
+        return fail(KS_ERR_INVALID_ARGUMENT, "vector kernel needs 16-byte rows and pointers");
+    const bool pf = op_prefetch(p);
+    p.cluster = 0;
+    p.smem_bytes = 0;
+    if (op == kOpSilu) {
+        if (p.block > 256) return fail(KS_ERR_INVALID_ARGUMENT, "SwiGLU block > 256");
+        if (p.kernel != KS_KERNEL_FLAT && p.kernel != KS_KERNEL_CTA_ROW && p.kernel != KS_KERNEL_SCALAR)
+            return fail(KS_ERR_INVALID_ARGUMENT, "SwiGLU takes the flat, row or scalar kernel");
+        p.stages = 0;
+        p.team = p.block;
+        return KS_SUCCESS;
+    }
+    const bool ln = op == kOpLayerNorm;
+    if (p.kernel != KS_KERNEL_BULK_ROW) p.stages = 0;
+    switch (p.kernel) {
+    case KS_KERNEL_WARP_ROW:
+        if (p.vec_per_thread != 2 && p.vec_per_thread != 4 && p.vec_per_thread != 6 &&
+            p.vec_per_thread != 8)
+            return fail(KS_ERR_INVALID_ARGUMENT, "warp rows take 2, 4, 6 or 8 vectors per lane");
+        if (32LL * p.vec_per_thread < width || p.block > 128)
+            return fail(KS_ERR_INVALID_ARGUMENT, "warp-row plan does not cover the row or block > 128");
+        if (ln && !pf) return fail(KS_ERR_INVALID_ARGUMENT, "LayerNorm rows always prefetch");
+        p.team = 32;
+        return KS_SUCCESS;
+    case KS_KERNEL_CTA_ROW:
+        if (p.vec_per_thread != 1 && p.vec_per_thread != 2 && p.vec_per_thread != 4)
+            return fail(KS_ERR_INVALID_ARGUMENT, "CTA rows take 1, 2 or 4 vectors per thread");
+        if ((int64_t)p.block * p.vec_per_thread < width || p.block > 512)
+            return fail(KS_ERR_INVALID_ARGUMENT, "CTA-row plan does not cover the row or block > 512");
+        if (!pf && (ln || p.vec_per_thread != 4))
+            return fail(KS_ERR_INVALID_ARGUMENT, "no variant without prefetch for this plan");
+        break;
+    case KS_KERNEL_BULK_ROW:
+        if (!ln) return fail(KS_ERR_INVALID_ARGUMENT, "the staged ring is LayerNorm's");
+        if (p.vec_per_thread != 4 || (int64_t)p.block * 4 < width || p.block > 512)
+            return fail(KS_ERR_INVALID_ARGUMENT, "ring plan: 4 vectors per thread covering the row, block <= 512");
+        if (p.stages < 2 || p.stages > 8 || ln_ring_smem(p.stages, width) > 226 * 1024)
+            return fail(KS_ERR_INVALID_ARGUMENT, "ring of %d stages does not fit", p.stages);
+        p.smem_bytes = (int32_t)ln_ring_smem(p.stages, width);
+        break;
+    case KS_KERNEL_TWOPASS_ROW:
+        if (p.vec_per_thread != 4 || p.block > (ln ? 512 : 1024))
+            return fail(KS_ERR_INVALID_ARGUMENT, "wide kernel: 4 vectors a step, block <= %d", ln ? 512 : 1024);
+        break;
+    case KS_KERNEL_SCALAR:
+        if (p.block > 1024) return fail(KS_ERR_INVALID_ARGUMENT, "scalar block > 1024");
+        p.vec_per_thread = 0;
+        break;
+    default:
+        return fail(KS_ERR_INVALID_ARGUMENT, "kernel %d is not one of this operator's", p.kernel);
+    }
+    (void)elems;
+    p.team = p.block;
+    return KS_SUCCESS;
+}
+
+// A launch with programmatic dependent launch when `pdl`.
+cudaError_t launch_ex(const void *f, dim3 grid, dim3 block, size_t smem, void **args,
+                      cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, f, args);
+}
+
+int64_t cap_grid(int64_t grid, const ks_plan_t &p) {
+    return (p.grid > 0 && grid > p.grid) ? p.grid : grid;
+}
+
+template <typename T>
+cudaError_t silu_dispatch(const ks_plan_t &p, void *out, const void *x, int64_t rows, int64_t d,
+                          int sms, cudaStream_t s, bool pdl) {
+    int64_t nr = rows, dd = p.kernel == KS_KERNEL_SCALAR ? d : d / Elem<T>::kPerVec;
+    void *args[] = {&out, const_cast<void **>(&x), &nr, &dd};
+    if (p.kernel == KS_KERNEL_FLAT) {
+        // a persistent grid of as many CTAs as are resident at once (fewer if the vectors run
+        // out), two vectors per thread per iteration
+        const void *f = (const void *)silu_mul_flat_kernel<T>;
+        const int n = cached_occupancy(f, p.block, 0);
+        int64_t grid = ceil_div64(rows * dd, 2 * (int64_t)p.block);
+        grid = cap_grid(grid > (int64_t)sms * n ? (int64_t)sms * n : grid, p);
+        return launch_ex(f, dim3((unsigned)grid), dim3(p.block), 0, args, s, pdl);
+    }
+    if (p.kernel == KS_KERNEL_CTA_ROW) {
+        // gx CTAs across a row, each of bx threads covering two vectors a thread (bx a multiple
+        // of 32, at most p.block); narrow rows stack 256 / bx rows per CTA; as many CTAs as are
+        // resident at once (a CTA left for a second wave of this persistent grid would start only
+        // when a first-wave one has finished all its rows)
+        const void *f = (const void *)silu_mul_rows_kernel<T>;
+        const int64_t gx = ceil_div64(dd, 2 * (int64_t)p.block);
+        const int bx = (int)round_up64(ceil_div64(dd, 2 * gx), 32);
+        int64_t by = 256 / bx;
+        by = by > rows ? rows : by;
+        int64_t gy = ceil_div64(rows, by);
+        int64_t cap = (int64_t)sms * cached_occupancy(f, bx * (int)by, 0) / gx;
+        if (p.grid > 0 && cap > p.grid / gx) cap = p.grid / gx;
+        gy = gy > cap ? cap : gy;
+        gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
+        return launch_ex(f, dim3((unsigned)gx, (unsigned)gy), dim3((unsigned)bx, (unsigned)by), 0,
+                         args, s, pdl);
+    }
+    // scalar: enough CTAs to cover a row once; rows: fill ~8 waves of SMs
+    int64_t gx = ceil_div64(d, p.block);
+    gx = gx < 1 ? 1 : gx;
+    int64_t gy = (int64_t)sms * 8 / gx;
+    if (p.grid > 0 && gy > p.grid / gx) gy = p.grid / gx;
+    gy = gy < 1 ? 1 : (gy > rows ? rows : gy);
+    gy = gy > 65535 ? 65535 : gy;
+    return launch_ex((const void *)silu_mul_scalar_kernel<T>, dim3((unsigned)gx, (unsigned)gy),
+                     dim3(p.block), 0, args, s, pdl);
+}
+
+// Grid of a register-row launch: as many CTAs as are resident at once, no more than the rows
+// need (warp plans: block / 32 rows per CTA), no more than the plan's grid when it gives one.
+int64_t reg_grid(const void *f, const ks_plan_t &p, size_t smem, int64_t rows, int sms) {
+    const int n = cached_occupancy(f, p.block, smem);
+    const int64_t per_cta = p.kernel == KS_KERNEL_WARP_ROW ? p.block / 32 : 1;
+    const int64_t need = ceil_div64(rows, per_cta);
+    const int64_t grid = (int64_t)sms * n;
+    return cap_grid(grid > need ? need : grid, p);
+}
+
+template <typename T>
+cudaError_t softmax_dispatch(const ks_plan_t &p, void *out, const void *x, int64_t rows,
+                             int64_t width, int sms, cudaStream_t s, bool pdl) {
+    int64_t nr = rows, wd = width;
+    void *args[] = {&out, const_cast<void **>(&x), &nr, &wd};
+    const bool pf = op_prefetch(p);
+    const void *f = nullptr;
+    switch (p.kernel) {
+    case KS_KERNEL_WARP_ROW:
+        switch (p.vec_per_thread) {
+        case 2: f = pf ? (const void *)softmax_vec_kernel<T, 2, true, true>
+                       : (const void *)softmax_vec_kernel<T, 2, false, true>; break;
+        case 4: f = pf ? (const void *)softmax_vec_kernel<T, 4, true, true>
+                       : (const void *)softmax_vec_kernel<T, 4, false, true>; break;
+        case 6: f = pf ? (const void *)softmax_vec_kernel<T, 6, true, true>
+                       : (const void *)softmax_vec_kernel<T, 6, false, true>; break;
+        case 8: f = pf ? (const void *)softmax_vec_kernel<T, 8, true, true>
+                       : (const void *)softmax_vec_kernel<T, 8, false, true>; break;
+        default: return cudaErrorInvalidConfiguration;
+        }
+        break;
+    case KS_KERNEL_CTA_ROW:
+        switch (p.vec_per_thread) {
+        case 1: f = (const void *)softmax_vec_kernel<T, 1, true>; break;
+        case 2: f = (const void *)softmax_vec_kernel<T, 2, true>; break;
+        case 4: f = pf ? (const void *)softmax_vec_kernel<T, 4, true>
+                       : (const void *)softmax_vec_kernel<T, 4, false>; break;
+        default: return cudaErrorInvalidConfiguration;
+        }
+        break;
+    case KS_KERNEL_TWOPASS_ROW: f = (const void *)softmax_wide_kernel<T, 4>; break;
+    case KS_KERNEL_SCALAR: f = (const void *)softmax_scalar_kernel<T>; break;
+    default: return cudaErrorInvalidConfiguration;
+    }
+    int64_t grid = reg_grid(f, p, 0, rows, sms);
+    if (p.kernel == KS_KERNEL_TWOPASS_ROW && grid > wide_grid_cap(width, sms))
+        grid = wide_grid_cap(width, sms);
+    return launch_ex(f, dim3((unsigned)grid), dim3(p.block), 0, args, s, pdl);
+}
 
 // The instantiation of a LayerNorm kernel for the weight/bias combination of the call.
 template <typename T, typename K>
@@ -1244,93 +1349,110 @@ const void *layer_norm_pick(int affine, K none, K weight, K bias, K both) {
 }
 
 template <typename T>
-cudaError_t layer_norm_dispatch(RegPlan p, void *out, const void *x, const void *w,
+cudaError_t layer_norm_dispatch(const ks_plan_t &p, void *out, const void *x, const void *w,
                                 const void *b, int64_t rows, int64_t hidden, int64_t hv,
-                                float eps, int sms, cudaStream_t s) {
-    int v = p.v, block = p.block;
-    if (p.warp && 32 * (int64_t)v < hv) return cudaErrorInvalidConfiguration;  // a warp must cover the row
+                                float eps, int sms, cudaStream_t s, bool pdl) {
     int64_t nr = rows, hd = hidden, hvv = hv;
     float ep = eps;
-    const void *f;
+    int stages = p.stages;
     void *vec_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
                         const_cast<void **>(&b), &nr, &hd, &hvv, &ep};
     void *sc_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
                        const_cast<void **>(&b), &nr, &hd, &ep};
-    void **args = vec_args;
-    // Many rows wider than 512 vectors: the staged ring (KS_LN_RING_BYTES of rows per CTA, 2..8
-    // stages) keeps enough bytes in flight; otherwise the register kernel, which measured faster
-    // for rows of at most 512 vectors (0.74-0.82 of the copy peak against 0.65-0.69 for the ring).
-    // Between 1024 and 2048 vectors the ring's CTA (a thread per 4 vectors, ~105 registers for
-    // 16-bit types) leaves one CTA of 8-14 warps per SM; the wide kernel's 128-thread CTAs keep
-    // more warps resident and measured faster on GB300 for many rows: bf16 1280..1792 vectors
-    // 0.76-0.83 of the copy peak against 0.65-0.78, fp32 1024..1792 0.88-0.95 against 0.76-0.86
-    // (at 1024 bf16 vectors the ring measured 0.96 against 0.81, so 16-bit rows start above it).
-    int stages = 0;
-    if (!p.warp && v == 4 && hv > 512 && rows >= 4 * (int64_t)sms) {
-        if (hv < 2048 && hv >= (sizeof(T) == 4 ? 1024 : 1025)) {
-            v = kWideRows;
-            block = 128;
-        } else {
-            int64_t n_st = (KS_LN_RING_BYTES) / (hv * 16);
-            stages = (int)(n_st < 2 ? 2 : (n_st > 8 ? 8 : n_st));
-        }
-    }
     void *bulk_args[] = {&out, const_cast<void **>(&x), const_cast<void **>(&w),
                          const_cast<void **>(&b), &nr, &hd, &hvv, &ep, &stages};
+    void **args = vec_args;
     size_t smem = 0;
     const int affine = (w ? kAffineWeight : 0) | (b ? kAffineBias : 0);
-    switch (p.warp ? -v : (stages ? 8 : v)) {
-    case -2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0, true>, layer_norm_vec_kernel<T, 2, 1, true>,
-                                    layer_norm_vec_kernel<T, 2, 2, true>, layer_norm_vec_kernel<T, 2, 3, true>); break;
-    case -4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0, true>, layer_norm_vec_kernel<T, 4, 1, true>,
-                                    layer_norm_vec_kernel<T, 4, 2, true>, layer_norm_vec_kernel<T, 4, 3, true>); break;
-    case -6: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 6, 0, true>, layer_norm_vec_kernel<T, 6, 1, true>,
-                                    layer_norm_vec_kernel<T, 6, 2, true>, layer_norm_vec_kernel<T, 6, 3, true>); break;
-    case -8: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 8, 0, true>, layer_norm_vec_kernel<T, 8, 1, true>,
-                                    layer_norm_vec_kernel<T, 8, 2, true>, layer_norm_vec_kernel<T, 8, 3, true>); break;
-    case 1: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 1, 0>, layer_norm_vec_kernel<T, 1, 1>,
-                                   layer_norm_vec_kernel<T, 1, 2>, layer_norm_vec_kernel<T, 1, 3>); break;
-    case 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0>, layer_norm_vec_kernel<T, 2, 1>,
-                                   layer_norm_vec_kernel<T, 2, 2>, layer_norm_vec_kernel<T, 2, 3>); break;
-    case 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0>, layer_norm_vec_kernel<T, 4, 1>,
-                                   layer_norm_vec_kernel<T, 4, 2>, layer_norm_vec_kernel<T, 4, 3>); break;
-    case kWideRows:
+    const void *f = nullptr;
+    switch (p.kernel) {
+    case KS_KERNEL_WARP_ROW:
+        switch (p.vec_per_thread) {
+        case 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0, true>, layer_norm_vec_kernel<T, 2, 1, true>,
+                                       layer_norm_vec_kernel<T, 2, 2, true>, layer_norm_vec_kernel<T, 2, 3, true>); break;
+        case 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0, true>, layer_norm_vec_kernel<T, 4, 1, true>,
+                                       layer_norm_vec_kernel<T, 4, 2, true>, layer_norm_vec_kernel<T, 4, 3, true>); break;
+        case 6: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 6, 0, true>, layer_norm_vec_kernel<T, 6, 1, true>,
+                                       layer_norm_vec_kernel<T, 6, 2, true>, layer_norm_vec_kernel<T, 6, 3, true>); break;
+        case 8: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 8, 0, true>, layer_norm_vec_kernel<T, 8, 1, true>,
+                                       layer_norm_vec_kernel<T, 8, 2, true>, layer_norm_vec_kernel<T, 8, 3, true>); break;
+        default: return cudaErrorInvalidConfiguration;
+        }
+        break;
+    case KS_KERNEL_CTA_ROW:
+        switch (p.vec_per_thread) {
+        case 1: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 1, 0>, layer_norm_vec_kernel<T, 1, 1>,
+                                       layer_norm_vec_kernel<T, 1, 2>, layer_norm_vec_kernel<T, 1, 3>); break;
+        case 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0>, layer_norm_vec_kernel<T, 2, 1>,
+                                       layer_norm_vec_kernel<T, 2, 2>, layer_norm_vec_kernel<T, 2, 3>); break;
+        case 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0>, layer_norm_vec_kernel<T, 4, 1>,
+                                       layer_norm_vec_kernel<T, 4, 2>, layer_norm_vec_kernel<T, 4, 3>); break;
+        default: return cudaErrorInvalidConfiguration;
+        }
+        break;
+    case KS_KERNEL_TWOPASS_ROW:
         f = layer_norm_pick<T>(affine, layer_norm_wide_kernel<T, 4, 0>, layer_norm_wide_kernel<T, 4, 1>,
                                layer_norm_wide_kernel<T, 4, 2>, layer_norm_wide_kernel<T, 4, 3>);
         break;
-    case 8:
+    case KS_KERNEL_BULK_ROW:
         f = layer_norm_pick<T>(affine, layer_norm_bulk_kernel<T, 4, 0>, layer_norm_bulk_kernel<T, 4, 1>,
                                layer_norm_bulk_kernel<T, 4, 2>, layer_norm_bulk_kernel<T, 4, 3>);
         args = bulk_args;
-        smem = 128 + (size_t)stages * (size_t)hv * 16;
+        smem = ln_ring_smem(stages, hv);
         break;
-    default:
+    case KS_KERNEL_SCALAR:
         f = layer_norm_pick<T>(affine, layer_norm_scalar_kernel<T, 0>, layer_norm_scalar_kernel<T, 1>,
                                layer_norm_scalar_kernel<T, 2>, layer_norm_scalar_kernel<T, 3>);
         args = sc_args;
-        block = (int)round_up64(ceil_div64(hidden, 8), 32);
-        block = block < 32 ? 32 : (block > 1024 ? 1024 : block);
+        break;
+    default: return cudaErrorInvalidConfiguration;
     }
     // allow the largest ring the device takes beside the kernel's static shared memory
     if (smem > 0 && !allow_dynamic_smem(f, smem)) return cudaErrorInvalidConfiguration;
-    p.v = v;
-    p.block = block;
     int64_t grid = reg_grid(f, p, smem, rows, sms);
-    if (v == kWideRows && !stages && grid > wide_grid_cap(hv, sms)) grid = wide_grid_cap(hv, sms);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = launch_pdl_enabled() ? 1 : 0;
-    return cudaLaunchKernelExC(&cfg, f, args);
+    if (p.kernel == KS_KERNEL_TWOPASS_ROW && grid > wide_grid_cap(hv, sms)) grid = wide_grid_cap(hv, sms);
+    return launch_ex(f, dim3((unsigned)grid), dim3(p.block), smem, args, s, pdl);
+}
+
+// The default plan of op (2 SwiGLU, 3 Softmax, 4 LayerNorm) for a call; for SwiGLU `hidden` is
+// the output row's width d. Pure host code.
+ks_plan_t op_default_plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
+                          int sms) {
+    const int e = elem_bytes(dtype);
+    const bool vec = aligned16 && (hidden * e) % 16 == 0;
+    const int64_t hv = vec ? hidden * e / 16 : 0;
+    if (op == kOpSilu) return silu_plan(vec, hv, dtype);
+    if (op == kOpSoftmax) return softmax_plan(vec, vec ? hv : hidden, rows, sms, dtype);
+    return layer_norm_plan(vec, hv, hidden, rows, sms, dtype);
+}
+
+// The launch plan a call runs: `forced` checked against the call, or the default plan.
+ks_status_t resolve_op_plan(int op, const ks_plan_t *forced, int64_t rows, int64_t hidden,
+                            ks_dtype_t dtype, bool aligned16, int sms, ks_plan_t *p, bool *pdl) {
+    if (!forced) {
+        *p = op_default_plan(op, rows, hidden, dtype, aligned16, sms);
+        *pdl = launch_pdl_enabled();
+        return KS_SUCCESS;
+    }
+    *p = *forced;
+    const int e = elem_bytes(dtype);
+    const bool vec = aligned16 && (hidden * e) % 16 == 0;
+    *pdl = (p->flags & KS_PLAN_PDL) != 0;
+    return op_check(op, *p, vec, vec ? hidden * e / 16 : 0, hidden);
 }
 
 }  // namespace
+
+ks_status_t op_plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
+                    int sm_count, ks_plan_t *p) {
+    if (rows == 0) {
+        memset(p, 0, sizeof *p);
+        p->kernel = KS_KERNEL_NONE;
+        return KS_SUCCESS;
+    }
+    *p = op_default_plan(op, rows, hidden, dtype, aligned16, sm_count);
+    return KS_SUCCESS;
+}
 
 int fault_flags_ops(bool clear) { return fault_flags_t(clear); }
 
@@ -1338,10 +1460,10 @@ int fault_flags_ops(bool clear) { return fault_flags_t(clear); }
 
 using namespace ks;
 
-extern "C" {
+namespace {
 
-ks_status_t ks_silu_and_mul(void *out, const void *x, int64_t rows, int64_t d, ks_dtype_t dtype,
-                            ks_stream_t stream) {
+ks_status_t silu_and_mul(void *out, const void *x, int64_t rows, int64_t d, ks_dtype_t dtype,
+                         const ks_plan_t *forced, ks_stream_t stream) {
     int e = 0;
     ks_status_t st = check_common(rows, d, dtype, &e);
     if (st != KS_SUCCESS) return st;
@@ -1351,23 +1473,27 @@ ks_status_t ks_silu_and_mul(void *out, const void *x, int64_t rows, int64_t d, k
         return fail(KS_ERR_INVALID_ARGUMENT, "a pointer is not aligned to the %d-byte element", e);
     if (overlaps(out, rows * d * e, x, rows * 2 * d * e))
         return fail(KS_ERR_OVERLAP, "out and x storage overlap");
+    const bool al = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0;
+    ks_plan_t p;
+    bool pdl = false;
+    if (forced && (st = resolve_op_plan(kOpSilu, forced, rows, d, dtype, al, 1, &p, &pdl)) != KS_SUCCESS)
+        return st;
     int sms = 0;
     if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
-    const bool vec = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0 && (d * e) % 16 == 0;
-    const SiluPlan plan = silu_plan(vec, vec ? d * e / 16 : 0, dtype);
+    if (!forced) resolve_op_plan(kOpSilu, nullptr, rows, d, dtype, al, sms, &p, &pdl);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce;
     switch (dtype) {
-    case KS_DTYPE_BF16: ce = silu_dispatch<__nv_bfloat16>(plan, out, x, rows, d, sms, s); break;
-    case KS_DTYPE_F16: ce = silu_dispatch<__half>(plan, out, x, rows, d, sms, s); break;
-    default: ce = silu_dispatch<float>(plan, out, x, rows, d, sms, s); break;
+    case KS_DTYPE_BF16: ce = silu_dispatch<__nv_bfloat16>(p, out, x, rows, d, sms, s, pdl); break;
+    case KS_DTYPE_F16: ce = silu_dispatch<__half>(p, out, x, rows, d, sms, s, pdl); break;
+    default: ce = silu_dispatch<float>(p, out, x, rows, d, sms, s, pdl); break;
     }
     if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
     return KS_SUCCESS;
 }
 
-ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, ks_dtype_t dtype,
-                       ks_stream_t stream) {
+ks_status_t softmax(void *out, const void *x, int64_t rows, int64_t hidden, ks_dtype_t dtype,
+                    const ks_plan_t *forced, ks_stream_t stream) {
     int e = 0;
     ks_status_t st = check_common(rows, hidden, dtype, &e);
     if (st != KS_SUCCESS) return st;
@@ -1378,25 +1504,31 @@ ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, k
     const int64_t nbytes = rows * hidden * e;
     if (out != x && overlaps(out, nbytes, x, nbytes))
         return fail(KS_ERR_OVERLAP, "out partially overlaps x (only out == x is allowed)");
+    const bool al = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0;
+    ks_plan_t p;
+    bool pdl = false;
+    if (forced && (st = resolve_op_plan(kOpSoftmax, forced, rows, hidden, dtype, al, 1, &p, &pdl)) != KS_SUCCESS)
+        return st;
     int sms = 0;
     if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
-    const bool aligned = (((uintptr_t)out | (uintptr_t)x) & 15u) == 0 && (hidden * e) % 16 == 0;
-    const int64_t width = aligned ? hidden * e / 16 : hidden;
-    const RegPlan p = softmax_plan(aligned, width, rows, sms, dtype);
+    if (!forced) resolve_op_plan(kOpSoftmax, nullptr, rows, hidden, dtype, al, sms, &p, &pdl);
+    // the vector kernels take the row's width in 16-byte vectors, the scalar kernel in elements
+    const bool vec = al && (hidden * e) % 16 == 0 && p.kernel != KS_KERNEL_SCALAR;
+    const int64_t width = vec ? hidden * e / 16 : hidden;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce;
     switch (dtype) {
-    case KS_DTYPE_BF16: ce = softmax_dispatch<__nv_bfloat16>(p, out, x, rows, width, sms, s); break;
-    case KS_DTYPE_F16: ce = softmax_dispatch<__half>(p, out, x, rows, width, sms, s); break;
-    default: ce = softmax_dispatch<float>(p, out, x, rows, width, sms, s); break;
+    case KS_DTYPE_BF16: ce = softmax_dispatch<__nv_bfloat16>(p, out, x, rows, width, sms, s, pdl); break;
+    case KS_DTYPE_F16: ce = softmax_dispatch<__half>(p, out, x, rows, width, sms, s, pdl); break;
+    default: ce = softmax_dispatch<float>(p, out, x, rows, width, sms, s, pdl); break;
     }
     if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
     return KS_SUCCESS;
 }
 
-ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const void *bias,
-                          int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype,
-                          ks_stream_t stream) {
+ks_status_t layer_norm(void *out, const void *x, const void *weight, const void *bias,
+                       int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype,
+                       const ks_plan_t *forced, ks_stream_t stream) {
     int e = 0;
     ks_status_t st = check_common(rows, hidden, dtype, &e);
     if (st != KS_SUCCESS) return st;
@@ -1411,21 +1543,64 @@ ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const vo
         return fail(KS_ERR_OVERLAP, "out partially overlaps x (only out == x is allowed)");
     if ((weight && overlaps(out, nbytes, weight, pbytes)) || (bias && overlaps(out, nbytes, bias, pbytes)))
         return fail(KS_ERR_OVERLAP, "out overlaps weight or bias storage");
+    const uintptr_t a = (uintptr_t)out | (uintptr_t)x | (uintptr_t)weight | (uintptr_t)bias;
+    const bool al = (a & 15u) == 0;
+    ks_plan_t p;
+    bool pdl = false;
+    if (forced && (st = resolve_op_plan(kOpLayerNorm, forced, rows, hidden, dtype, al, 1, &p, &pdl)) != KS_SUCCESS)
+        return st;
     int sms = 0;
     if ((st = sm_count(&sms)) != KS_SUCCESS) return st;
-    const uintptr_t al = (uintptr_t)out | (uintptr_t)x | (uintptr_t)weight | (uintptr_t)bias;
-    const bool aligned = (al & 15u) == 0 && (hidden * e) % 16 == 0;
+    if (!forced) resolve_op_plan(kOpLayerNorm, nullptr, rows, hidden, dtype, al, sms, &p, &pdl);
     const int64_t hv = hidden * e / 16;
-    const RegPlan p = layer_norm_plan(aligned, hv, rows, sms, dtype);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t ce;
     switch (dtype) {
-    case KS_DTYPE_BF16: ce = layer_norm_dispatch<__nv_bfloat16>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
-    case KS_DTYPE_F16: ce = layer_norm_dispatch<__half>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
-    default: ce = layer_norm_dispatch<float>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s); break;
+    case KS_DTYPE_BF16: ce = layer_norm_dispatch<__nv_bfloat16>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s, pdl); break;
+    case KS_DTYPE_F16: ce = layer_norm_dispatch<__half>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s, pdl); break;
+    default: ce = layer_norm_dispatch<float>(p, out, x, weight, bias, rows, hidden, hv, eps, sms, s, pdl); break;
     }
     if (ce != cudaSuccess) return fail(KS_ERR_CUDA, "launch: %s", cudaGetErrorString(ce));
     return KS_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" {
+
+ks_status_t ks_silu_and_mul(void *out, const void *x, int64_t rows, int64_t d, ks_dtype_t dtype,
+                            ks_stream_t stream) {
+    return silu_and_mul(out, x, rows, d, dtype, nullptr, stream);
+}
+
+ks_status_t ks_silu_and_mul_planned(void *out, const void *x, int64_t rows, int64_t d,
+                                    ks_dtype_t dtype, const ks_plan_t *plan, ks_stream_t stream) {
+    if (!plan) return fail(KS_ERR_INVALID_ARGUMENT, "plan is NULL");
+    return silu_and_mul(out, x, rows, d, dtype, plan, stream);
+}
+
+ks_status_t ks_softmax(void *out, const void *x, int64_t rows, int64_t hidden, ks_dtype_t dtype,
+                       ks_stream_t stream) {
+    return softmax(out, x, rows, hidden, dtype, nullptr, stream);
+}
+
+ks_status_t ks_softmax_planned(void *out, const void *x, int64_t rows, int64_t hidden,
+                               ks_dtype_t dtype, const ks_plan_t *plan, ks_stream_t stream) {
+    if (!plan) return fail(KS_ERR_INVALID_ARGUMENT, "plan is NULL");
+    return softmax(out, x, rows, hidden, dtype, plan, stream);
+}
+
+ks_status_t ks_layer_norm(void *out, const void *x, const void *weight, const void *bias,
+                          int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype,
+                          ks_stream_t stream) {
+    return layer_norm(out, x, weight, bias, rows, hidden, eps, dtype, nullptr, stream);
+}
+
+ks_status_t ks_layer_norm_planned(void *out, const void *x, const void *weight, const void *bias,
+                                  int64_t rows, int64_t hidden, float eps, ks_dtype_t dtype,
+                                  const ks_plan_t *plan, ks_stream_t stream) {
+    if (!plan) return fail(KS_ERR_INVALID_ARGUMENT, "plan is NULL");
+    return layer_norm(out, x, weight, bias, rows, hidden, eps, dtype, plan, stream);
 }
 
 }  // extern "C"

@@ -334,7 +334,7 @@ def test_persistent_grid_is_capped_by_residency():
 
 def test_empty_plan_and_bad_arguments():
     assert plan(0, 0, 64).kernel == _abi.KS_KERNEL_NONE
-    st, _ = _abi.ks_plan_launch(2, 1, 64, BF16, True, 152, 0)
+    st, _ = _abi.ks_plan_launch(5, 1, 64, BF16, True, 152, 0)
     assert st == _abi.KS_ERR_INVALID_ARGUMENT
     st, _ = _abi.ks_plan_launch(0, 1, 0, BF16, True, 152, 0)
     assert st == _abi.KS_ERR_INVALID_ARGUMENT
@@ -611,3 +611,82 @@ def test_every_width_gets_a_valid_plan(dtype, op):
                     assert p.block * p.vec_per_thread >= slice_ and (p.cluster - 1) * slice_ < hv
                 else:
                     raise AssertionError(f"unexpected kernel {p.kernel} for {rows} x {hidden}")
+
+
+# ------------------------------------------------------------- the next operators' launch plans
+
+def op_plan(op, rows, hidden, dtype=BF16, aligned=True, sms=152):
+    st, p = _abi.ks_plan_launch(op, rows, hidden, dtype, aligned, sms, 0)
+    assert st == _abi.KS_SUCCESS, _abi.ks_last_error()
+    return p
+
+
+def test_next_op_plans_follow_the_bands():
+    """ks_plan_launch reports the next operators' plans: the width bands for many narrow rows,
+    the general rules otherwise, the scalar kernel for rows that cannot be vectorised."""
+    SM, LN, SW = _abi.OP_SOFTMAX, _abi.OP_LAYER_NORM, _abi.OP_SILU_AND_MUL
+    # Softmax 16-bit: rows of 64..127 vectors take warp rows at 4 vectors a lane, prefetching
+    p = op_plan(SM, 1000, 72 * 8)
+    assert (p.kernel, p.vec_per_thread, p.block, p.flags) == (WARP, 4, 128, 0)
+    # ... but not in the latency regime (rows <= SMs): a CTA per row
+    assert op_plan(SM, 100, 72 * 8).kernel == CTA
+    # Softmax fp32 rows of 177..216 vectors: CTA rows at 4 vectors with prefetch
+    p = op_plan(SM, 1000, 200 * 4, F32)
+    assert (p.kernel, p.vec_per_thread, p.flags) == (CTA, 4, 0) and p.block == 64
+    # Softmax rows of 128..1024 vectors: CTA rows at 4 vectors without prefetch; wider prefetch
+    p = op_plan(SM, 1000, 512 * 8)
+    assert (p.kernel, p.vec_per_thread, p.block, p.flags) == (CTA, 4, 128, _abi.KS_PLAN_NO_PREFETCH)
+    assert op_plan(SM, 1000, 1536 * 8).flags == 0
+    # rows wider than 2048 vectors: the wide multi-pass kernel
+    p = op_plan(SM, 1000, 4096 * 8)
+    assert (p.kernel, p.vec_per_thread, p.block) == (TWO, 4, 256)
+    # LayerNorm fp16 rows of 65..128 vectors: warp rows at 4 vectors
+    p = op_plan(LN, 1000, 96 * 8, F16)
+    assert (p.kernel, p.vec_per_thread, p.flags) == (WARP, 4, 0)
+    # LayerNorm many rows of 1024 bf16 vectors: the staged ring; 1280: the wide kernel's 128 threads
+    p = op_plan(LN, 32768, 1024 * 8)
+    assert (p.kernel, p.vec_per_thread, p.block, p.stages) == (BULK, 4, 256, 4)
+    p = op_plan(LN, 32768, 1280 * 8)
+    assert (p.kernel, p.block) == (TWO, 128)
+    # SwiGLU: fp32 the flat walk; 16-bit rows of >= 448 vectors the row kernel capped at 96
+    assert op_plan(SW, 1000, 4096, F32).kernel == _abi.KS_KERNEL_FLAT
+    p = op_plan(SW, 1000, 1024 * 8)
+    assert (p.kernel, p.block) == (CTA, 96)
+    assert op_plan(SW, 1000, 64 * 8).kernel == _abi.KS_KERNEL_FLAT
+    # rows that cannot be vectorised
+    for op in (SM, LN, SW):
+        assert op_plan(op, 10, 1001).kernel == _abi.KS_KERNEL_SCALAR
+        assert op_plan(op, 10, 1024, aligned=False).kernel == _abi.KS_KERNEL_SCALAR
+    assert op_plan(SM, 0, 1024).kernel == _abi.KS_KERNEL_NONE
+
+
+def test_next_op_planned_entry_points_check_the_plan():
+    """Explicit plans for SwiGLU, Softmax and LayerNorm are arguments: checked before any CUDA
+    call."""
+    a, b = FAKE, FAKE + (1 << 30)
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    mk = _abi.make_plan
+    NP = _abi.KS_PLAN_NO_PREFETCH
+    rows, h = 64, 4096  # 512 bf16 vectors
+    for p in (mk(WARP, 8, 128),                      # a warp covers 256 vectors, not 512
+              mk(CTA, 4, 64),                        # 64 x 4 < 512
+              mk(CTA, 2, 512, flags=NP),             # no CTA-row variant without prefetch at 2
+              mk(CTA, 4, 1024),                      # block over 512
+              mk(BULK, 4, 128, 2),                   # the ring is LayerNorm's
+              mk(TWO, 2, 256),                       # the wide kernel steps 4 vectors
+              mk(_abi.KS_KERNEL_FLAT, 2, 256),       # SwiGLU's
+              mk(CTA, 4, 100),                       # not a multiple of 32
+              mk(CTA, 4, 128, flags=8)):             # unknown flag
+        assert _abi.ks_softmax_planned(a, b, rows, h, BF16, p, None) == E
+    assert _abi.ks_softmax_planned(a, b + 2, rows, h, BF16, mk(CTA, 4, 128), None) == E  # unaligned
+    for p in (mk(WARP, 4, 128, flags=NP),            # LayerNorm always prefetches
+              mk(BULK, 4, 128, 1),                   # one stage
+              mk(BULK, 4, 64, 2),                    # 64 x 4 < 512 vectors
+              mk(TWO, 4, 1024)):                     # the LayerNorm wide kernel is bounded at 512
+        assert _abi.ks_layer_norm_planned(a, b, None, None, rows, h, 1e-5, BF16, p, None) == E
+    # a ring too large for shared memory: 8 stages of 2048 vectors (256 KiB)
+    p = mk(BULK, 4, 512, 8)
+    assert _abi.ks_layer_norm_planned(a, b, None, None, rows, 16384, 1e-5, BF16, p, None) == E
+    for p in (mk(WARP, 4, 128), mk(_abi.KS_KERNEL_FLAT, 2, 512), mk(CTA, 2, 288)):
+        assert _abi.ks_silu_and_mul_planned(a, b, rows, h, BF16, p, None) == E
+    assert _abi.load().ks_softmax_planned(a, b, rows, h, BF16, None, None) == E
