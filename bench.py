@@ -1357,9 +1357,10 @@ OPS_BAND_WIDTHS = {
 
 def op_band_candidates(op: str, hv: int):
     """The launch plans the next operators' width bands choose among for a row of hv vectors:
-    wV / wVn (a warp per row, V vectors a lane, with / without prefetch; where a warp covers the
-    row), cV / cVn (a CTA per row, V vectors a thread), and for SwiGLU flatB (the flat walk on
-    B-thread CTAs) and rowsB (the row kernel with at most B threads)."""
+    tTvV / tTvVn (a team of T = 8 or 16 lanes per row, V vectors a lane, with / without
+    prefetch; where the team covers the row), wV / wVn (a warp per row), cV / cVn (a CTA per
+    row, V vectors a thread), and for SwiGLU flatB (the flat walk on B-thread CTAs) and rowsB
+    (the row kernel with at most B threads)."""
     from row_wise_rmsnorm_ks_gb300 import _abi
 
     up32 = lambda n: -(-n // 32) * 32
@@ -1371,6 +1372,13 @@ def op_band_candidates(op: str, hv: int):
                 ("flat128", mk(_abi.KS_KERNEL_FLAT, 2, 128))]
         out += [(f"rows{b}", mk(_abi.KS_KERNEL_CTA_ROW, 2, b)) for b in (96, 128, 256)]
         return out
+    for team in (8, 16):  # teams of 8 or 16 lanes: 4 or 2 rows per warp
+        for v in (2, 4):
+            if team * v >= hv and team * (v - 2) < hv:
+                out.append((f"t{team}v{v}", mk(_abi.KS_KERNEL_WARP_ROW, v, 128, team=team)))
+                if op == "softmax":
+                    out.append((f"t{team}v{v}n", mk(_abi.KS_KERNEL_WARP_ROW, v, 128, flags=npf,
+                                                    team=team)))
     for v in (2, 4, 6, 8):
         if 32 * v >= hv:
             out.append((f"w{v}", mk(_abi.KS_KERNEL_WARP_ROW, v, 128)))
@@ -1483,7 +1491,7 @@ def run_ops_bands(args) -> int:
                 _, dp = _abi.ks_plan_launch(op_codes[op], R, H, code, True, sms, 0)
                 line = {"ops_bands": op, "dtype": dt, "hv": hv, "hidden": H, "rows": R,
                         "default_plan": {k: dp.as_dict()[k] for k in ("kernel_name", "vec_per_thread",
-                                                                       "block", "flags")}}
+                                                                       "block", "flags", "team")}}
                 for ctx in ("steady", "after_ring"):
                     res = {name: [] for name, _ in fns}
                     for _ in range(args.plan_sweep_rounds):
@@ -1521,6 +1529,71 @@ def ops_bands_table(jsonl_path: str) -> str:
     head = ("| op | dtype | vectors | default plan | default score | best | best score | best - "
             "default |\n|---|---|---|---|---|---|---|---|")
     return head + "\n" + "\n".join(rows)
+
+
+def band_of(name: str, default_plan: dict, op: str, hv: int):
+    """(kind, v, prefetch, team) of a band-candidate name, the library's Band fields; 'default'
+    maps the launch the library made to the same fields, 'g' when it is the general rule."""
+    import re
+    if name == "default":
+        k, v, npf = default_plan["kernel_name"], default_plan["vec_per_thread"], default_plan["flags"] & 1
+        if k == "warp_row":
+            return ("w", v, not npf, default_plan.get("team", 32) or 32)
+        gen_v = 1 if hv < 64 else (2 if hv < 128 else 4)
+        gen_pf = True if op == "layer_norm" else (gen_v != 4 or hv > 1024)
+        if k == "cta_row" and v == gen_v and (not npf) == gen_pf:
+            return ("g", 0, gen_pf, 32)
+        return ("c", v, not npf, 32)
+    m = re.fullmatch(r"t(\d+)v(\d)(n?)", name)
+    if m:
+        return ("w", int(m.group(2)), not m.group(3), int(m.group(1)))
+    m = re.fullmatch(r"([wc])(\d)(n?)", name)
+    return (m.group(1), int(m.group(2)), not m.group(3), 32)
+
+
+def derive_bands(jsonl_path: str, op: str, dtypes, min_gain: float = 0.01):
+    """Width bands for op from an --ops-bands run, by one rule: at each measured width, score
+    every candidate by its worse context, and over `dtypes` (the dtypes that share one table) by
+    its worst dtype; keep the library's current plan unless another candidate scores at least
+    `min_gain` (a point of the copy peak) higher, then take the best. Consecutive widths with the
+    same plan merge into one band reaching to the last of them. Returns [(hi, kind, v, prefetch,
+    team)], closed by the general rule."""
+    by_w = {}
+    for ln in open(jsonl_path):
+        if not ln.startswith('{"ops_bands"'):
+            continue
+        d = json.loads(ln)
+        if d["ops_bands"] != op or d["dtype"] not in dtypes or "steady" not in d:
+            continue
+        sc = {k: min(d["steady"][k], d.get("after_ring", d["steady"]).get(k, 0.0)) for k in d["steady"]}
+        by_w.setdefault(d["hv"], {})[d["dtype"]] = (sc, d["default_plan"])
+    bands = []
+    for hv in sorted(by_w):
+        per = by_w[hv]
+        if set(per) != set(dtypes):
+            continue
+        names = set.intersection(*(set(sc) for sc, _ in per.values()))
+        worst = {n: min(per[dt][0][n] for dt in per) for n in names}
+        cur = band_of("default", per[dtypes[0]][1], op, hv)
+        best = max(worst, key=worst.get)
+        pick = cur if worst[best] - worst["default"] < min_gain else band_of(best, None, op, hv)
+        if bands and bands[-1][1:] == pick:
+            bands[-1] = (hv,) + pick
+        else:
+            bands.append((hv,) + pick)
+    bands.append((32767, "g", 0, True, 32))
+    return bands
+
+
+def bands_cpp(name: str, bands) -> str:
+    """The bands as the library's C++ table."""
+    def one(b):
+        hi, kind, v, pf, team = b
+        hi_s = "kBandEnd" if hi == 32767 else str(hi)
+        pf_s = "true" if pf else "false"
+        return (f"{{{hi_s}, '{kind}', {v}, {pf_s}, {team}}}" if team != 32
+                else f"{{{hi_s}, '{kind}', {v}, {pf_s}}}")
+    return f"constexpr Band {name}[] = {{" + ", ".join(one(b) for b in bands) + "};"
 
 
 def run_ops_scan(args) -> int:
@@ -1634,6 +1707,8 @@ def main() -> int:
     ap.add_argument("--ops-bands-ops", default="softmax,layer_norm,silu_and_mul")
     ap.add_argument("--ops-bands-table", metavar="JSONL",
                     help="print the markdown table of an --ops-bands run")
+    ap.add_argument("--ops-bands-derive", metavar="JSONL",
+                    help="print the Softmax and LayerNorm band tables an --ops-bands run implies")
     ap.add_argument("--kernel-times", action="store_true",
                     help="every stated configuration a fixed number of times, for an ncu launch list")
     ap.add_argument("--kernel-time-launches", type=int, default=5)
@@ -1669,6 +1744,14 @@ def main() -> int:
         return run_ops_bands(args)
     if args.ops_bands_table:
         print(ops_bands_table(args.ops_bands_table))
+        return 0
+    if args.ops_bands_derive:
+        for name, op, dts in (("kSoftmax16", "softmax", ["bf16", "fp16"]),
+                              ("kSoftmax32", "softmax", ["fp32"]),
+                              ("kLayerNormBf16", "layer_norm", ["bf16"]),
+                              ("kLayerNormF16", "layer_norm", ["fp16"]),
+                              ("kLayerNormF32", "layer_norm", ["fp32"])):
+            print(bands_cpp(name, derive_bands(args.ops_bands_derive, op, dts)))
         return 0
     if args.kernel_times_table:
         print(kernel_times_table(*args.kernel_times_table))

@@ -63,16 +63,30 @@ __device__ __forceinline__ float cta_max(float v, float (*red)[32], int &slot) {
     return m;
 }
 
-// Reductions over a row's team: a warp (kWarp: shuffles only, no barrier, so the warps of a CTA
-// work on their own rows independently) or the whole CTA.
-template <bool kWarp>
+// Reductions over a row's team: kTeam lanes of a warp (32, 16 or 8: shuffles only, no barrier, so
+// the teams of a CTA work on their own rows independently; a team of 8 or 16 lanes is an aligned
+// group of lanes, so xor offsets below kTeam stay inside it) or, with kTeam = 0, the whole CTA.
+// Every lane of the warp must take part (full-warp shuffles).
+template <int kTeam>
 __device__ __forceinline__ float team_sum(float v, float (*red)[32], int &slot) {
-    return kWarp ? warp_sum(v) : cta_sum(v, red, slot);
+    if constexpr (kTeam == 0) {
+        return cta_sum(v, red, slot);
+    } else {
+#pragma unroll
+        for (int o = kTeam / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        return v;
+    }
 }
 
-template <bool kWarp>
+template <int kTeam>
 __device__ __forceinline__ float team_max(float v, float (*red)[32], int &slot) {
-    return kWarp ? warp_max(v) : cta_max(v, red, slot);
+    if constexpr (kTeam == 0) {
+        return cta_max(v, red, slot);
+    } else {
+#pragma unroll
+        for (int o = kTeam / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+        return v;
+    }
 }
 
 // e^v. For 16-bit outputs the SFU-based intrinsic (error a few fp32 ulps, growing with |v|,
@@ -288,15 +302,16 @@ __global__ void __launch_bounds__(256) silu_mul_scalar_kernel(void *out, const v
 
 // ------------------------------------------------------------------------------ Softmax
 
-// One CTA per row (or with kWarp one warp per row, the CTA's warps on rows of their own), V
-// 16-byte vectors per thread held in registers; persistent over rows. With
+// One CTA per row (or, with kTeam = 32, 16 or 8, a team of that many lanes of a warp per row, the
+// teams on rows of their own; 8- and 16-lane teams put several narrow rows in one warp, so its
+// lanes are not idle), V 16-byte vectors per thread held in registers; persistent over rows. With
 // kPrefetch the next row's vectors are loaded before the current row's two reductions; without
 // it each row is loaded when its turn comes (fewer registers, more resident warps: faster up to
 // 1024 vectors per row on GB300, slower beyond). The maximum is a plain fmaxf (NaN-ignoring): a
 // NaN or +inf in the row still makes the sum, and so every output, NaN, and a row of only -inf
 // still gets max -inf and z = NaN, so the contract's non-finite rules hold.
-template <typename T, int V, bool kPrefetch, bool kWarp = false>
-__global__ void __launch_bounds__(kWarp ? 128 : 512)
+template <typename T, int V, bool kPrefetch, int kTeam = 0>
+__global__ void __launch_bounds__(kTeam ? 128 : 512)
     softmax_vec_kernel(void *out, const void *x, int64_t rows, int64_t hv) {
     using E = Elem<T>;
     constexpr int P = E::kPerVec / 2;
@@ -309,12 +324,16 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
     allow_dependents_launch();
     const uint4 *xg = static_cast<const uint4 *>(x);
     uint4 *og = static_cast<uint4 *>(out);
-    const int t = kWarp ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
-    const int g = kWarp ? 32 : (int)blockDim.x;
-    const int teams = kWarp ? (int)(blockDim.x >> 5) : 1;
+    const int t = kTeam ? (int)(threadIdx.x & (kTeam - 1)) : (int)threadIdx.x;
+    const int g = kTeam ? kTeam : (int)blockDim.x;
+    const int teams = kTeam ? (int)(blockDim.x / kTeam) : 1;
     const int64_t stride = (int64_t)gridDim.x * teams;
     int slot = 0;
-    int64_t row = (int64_t)blockIdx.x * teams + (kWarp ? (int)(threadIdx.x >> 5) : 0);
+    int64_t row = (int64_t)blockIdx.x * teams + (kTeam ? (int)(threadIdx.x / kTeam) : 0);
+    // Every lane of a warp runs the iterations of the warp's first row, so that all of them take
+    // part in the team shuffles; a team of a sub-warp whose row is past the end works on zeros
+    // and stores nothing.
+    int64_t lead = kTeam ? (int64_t)blockIdx.x * teams + (int)(threadIdx.x >> 5) * (32 / kTeam) : row;
     uint4 cur[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) {
@@ -322,7 +341,8 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
         cur[k] = (kPrefetch && row < rows && c < hv) ? __ldcs(xg + row * hv + c)
                                                      : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (; row < rows; row += stride) {
+    for (; lead < rows; lead += stride, row += stride) {
+        const bool active = row < rows;
         const int64_t next = row + stride;
         uint4 nxt[V];
 #pragma unroll
@@ -331,7 +351,7 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
             if (kPrefetch)
                 nxt[k] = (next < rows && c < hv) ? __ldcs(xg + next * hv + c) : make_uint4(0u, 0u, 0u, 0u);
             else
-                cur[k] = (c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
+                cur[k] = (active && c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
         }
         float2 f[V][P];
         float m = -INFINITY;
@@ -344,7 +364,7 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
                 for (int i = 0; i < P; ++i) m = fmaxf(fmaxf(m, f[k][i].x), f[k][i].y);
             }
         }
-        m = team_max<kWarp>(m, red, slot);
+        m = team_max<kTeam>(m, red, slot);
         // For m = +-inf or NaN, z (or the folded bias) is NaN or -inf where the formula's is,
         // which gives the contract's NaN rows and masked entries; such rows take the exact form.
         const float neg_m = -m;
@@ -376,7 +396,7 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
                 }
             }
         }
-        const float sum = team_sum<kWarp>(
+        const float sum = team_sum<kTeam>(
             __fadd_rn(__fadd_rn(s[0].x, s[0].y), __fadd_rn(s[1].x, s[1].y)), red, slot);
         // e / sum as e * (1 / sum): one correctly rounded reciprocal per row, then a product
         // per element (within 1 fp32 ulp of the quotient)
@@ -385,7 +405,7 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512)
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
+            if (active && c < hv) {
 #pragma unroll
                 for (int i = 0; i < P; ++i) f[k][i] = pair_mul<kPair>(f[k][i], inv2);
                 __stcs(og + row * hv + c, E::pack2(f[k]));
@@ -431,8 +451,9 @@ __global__ void __launch_bounds__(1024) softmax_scalar_kernel(void *out, const v
 // did not hoist it out of the unrolled loop).
 constexpr int kAffineWeight = 1, kAffineBias = 2;
 
-// One CTA per row (or with kWarp one warp per row, the CTA's warps on rows of their own), V
-// 16-byte vectors per thread in registers, persistent over rows; the weight and bias slices a
+// One CTA per row (or with kTeam = 32, 16 or 8 a team of that many lanes of a warp per row, as in
+// softmax_vec_kernel), V 16-byte vectors per thread in registers, persistent over rows; the
+// weight and bias slices a
 // thread needs stay in registers for every row it visits, and the next row's vectors are loaded
 // before the current row's two reductions. (Measured on GB300 at [32768,
 // 8192] bf16: 74 % of the copy peak; weight and bias in shared memory, with or without the
@@ -490,8 +511,8 @@ __device__ __forceinline__ uint4 ln_out(const uint4 &v, const uint4 &wv, const u
     return Elem<T>::pack2(f);
 }
 
-template <typename T, int V, int kAffine, bool kWarp = false>
-__global__ void __launch_bounds__(kWarp ? 128 : 512) layer_norm_vec_kernel(void *out, const void *x,
+template <typename T, int V, int kAffine, int kTeam = 0>
+__global__ void __launch_bounds__(kTeam ? 128 : 512) layer_norm_vec_kernel(void *out, const void *x,
                                                              const void *w, const void *b,
                                                              int64_t rows, int64_t hidden,
                                                              int64_t hv, float eps) {
@@ -501,9 +522,9 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512) layer_norm_vec_kernel(void 
     allow_dependents_launch();
     const uint4 *xg = static_cast<const uint4 *>(x);
     uint4 *og = static_cast<uint4 *>(out);
-    const int t = kWarp ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
-    const int g = kWarp ? 32 : (int)blockDim.x;
-    const int teams = kWarp ? (int)(blockDim.x >> 5) : 1;
+    const int t = kTeam ? (int)(threadIdx.x & (kTeam - 1)) : (int)threadIdx.x;
+    const int g = kTeam ? kTeam : (int)blockDim.x;
+    const int teams = kTeam ? (int)(blockDim.x / kTeam) : 1;
     const int64_t stride = (int64_t)gridDim.x * teams;
     const float h = (float)hidden;
     // Weight and bias slices: in registers for every row a thread visits, except bf16 warp rows
@@ -513,7 +534,7 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512) layer_norm_vec_kernel(void 
     // on GB300 0.76 -> 0.94 of the copy peak at 96 vectors, 0.74 -> 0.94 at 160, 0.80 -> 0.92 at
     // 192; for bf16 at 8 vectors and for fp16 and fp32, whose rows already held more warps, it
     // measured up to 8 points slower.
-    constexpr bool kSmemAffine = kWarp && std::is_same<T, __nv_bfloat16>::value && V <= 6;
+    constexpr bool kSmemAffine = kTeam && std::is_same<T, __nv_bfloat16>::value && V <= 6;
     uint4 wv[V], bv[V];
     __shared__ uint4 sw[kSmemAffine && kW ? 32 * V : 1], sb[kSmemAffine && kB ? 32 * V : 1];
     if (kSmemAffine) {
@@ -532,14 +553,17 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512) layer_norm_vec_kernel(void 
         }
     }
     int slot = 0;
-    int64_t row = (int64_t)blockIdx.x * teams + (kWarp ? (int)(threadIdx.x >> 5) : 0);
+    int64_t row = (int64_t)blockIdx.x * teams + (kTeam ? (int)(threadIdx.x / kTeam) : 0);
+    // every lane of a warp runs the iterations of the warp's first row (see softmax_vec_kernel)
+    int64_t lead = kTeam ? (int64_t)blockIdx.x * teams + (int)(threadIdx.x >> 5) * (32 / kTeam) : row;
     uint4 xv[V];
 #pragma unroll
     for (int k = 0; k < V; ++k) {
         const int64_t c = t + (int64_t)k * g;
         xv[k] = (row < rows && c < hv) ? __ldcs(xg + row * hv + c) : make_uint4(0u, 0u, 0u, 0u);
     }
-    for (; row < rows; row += stride) {
+    for (; lead < rows; lead += stride, row += stride) {
+        const bool active = row < rows;
         const int64_t next = row + stride;
         uint4 nxt[V];
 #pragma unroll
@@ -550,18 +574,18 @@ __global__ void __launch_bounds__(kWarp ? 128 : 512) layer_norm_vec_kernel(void 
         float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
         for (int k = 0; k < V; ++k) ln_add_sum<T>(xv[k], s2);
-        const float mean = __fdiv_rn(team_sum<kWarp>(ln_total(s2), red, slot), h);
+        const float mean = __fdiv_rn(team_sum<kTeam>(ln_total(s2), red, slot), h);
         float2 q2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
         for (int k = 0; k < V; ++k)
             if (t + (int64_t)k * g < hv) ln_add_sq<T>(xv[k], -mean, q2);
-        const float var = __fdiv_rn(team_sum<kWarp>(ln_total(q2), red, slot), h);
+        const float var = __fdiv_rn(team_sum<kTeam>(ln_total(q2), red, slot), h);
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
         const float shift = -__fmul_rn(mean, rstd);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            if (c < hv) {
+            if (active && c < hv) {
                 const uint4 wk = kSmemAffine ? (kW ? sw[c] : make_uint4(0u, 0u, 0u, 0u)) : wv[k];
                 const uint4 bk = kSmemAffine ? (kB ? sb[c] : make_uint4(0u, 0u, 0u, 0u)) : bv[k];
                 __stcs(og + row * hv + c, ln_out<T, kAffine>(xv[k], wk, bk, rstd, shift));
@@ -1026,13 +1050,13 @@ ks_status_t check_common(int64_t rows, int64_t width, ks_dtype_t dtype, int *e) 
 
 constexpr int kOpSilu = 2, kOpSoftmax = 3, kOpLayerNorm = 4;  // ks_plan_launch's op codes
 
-ks_plan_t op_plan_of(int kernel, int v, int block, bool prefetch, int stages = 0) {
+ks_plan_t op_plan_of(int kernel, int v, int block, bool prefetch, int stages = 0, int team = 32) {
     ks_plan_t p;
     memset(&p, 0, sizeof p);
     p.kernel = kernel;
     p.vec_per_thread = v;
     p.block = block;
-    p.team = kernel == KS_KERNEL_WARP_ROW ? 32 : block;
+    p.team = kernel == KS_KERNEL_WARP_ROW ? team : block;
     p.flags = prefetch ? 0 : KS_PLAN_NO_PREFETCH;
     p.stages = stages;
     return p;
@@ -1045,53 +1069,45 @@ int scalar_block(int64_t width, int max_block) {
     return b < 32 ? 32 : (b > max_block ? max_block : b);
 }
 
-// SwiGLU. Measured on GB300 over widths of 16..2048 vectors (144..512 in steps of 8 to 32), many
-// rows, each plan timed in steady state and right after a kernel with a large shared-memory
-// carveout (as after a GEMM), the worse of the two kept. The flat walk held 0.81-0.88 of the copy
-// peak for 16-bit types at every width and 0.93-0.98 for fp32, whose rows it serves best
-// throughout. The row-structured kernel beats it for 16-bit rows of 160 and 192 vectors
-// (0.88-0.93) and of 288..447 (0.86-0.94), and from 448 vectors with its block capped at 96
-// threads (0.86-0.95; with 128..256-thread CTAs some of those widths fell to 0.77-0.84, e.g. bf16
-// dv = 1024: 0.82); at the other widths below 288 it fell as low as 0.59.
+// SwiGLU, from bench.py --ops-bands (widths of 16..2048 vectors, many rows, each plan timed in
+// steady state and right after a kernel with a large shared-memory carveout, the worse of the
+// two kept). The row-structured kernel, its CTAs fitted to the row, reads 0.92-0.94 of the copy
+// peak for 16-bit rows whose width is a multiple of 32 vectors and 0.95-0.97 for fp32 rows of
+// multiples of 64; at other widths it falls to 0.6-0.8, where the flat walk on 128-thread CTAs
+// holds 0.85-0.89 (16-bit) and 0.94-0.95 (fp32) at every width (on 256-thread CTAs 2-4 points
+// less for 16-bit).
 ks_plan_t silu_plan(bool vec, int64_t dv, ks_dtype_t dtype) {
     if (!vec) return op_plan_of(KS_KERNEL_SCALAR, 0, 256, true);
-    if (dtype == KS_DTYPE_F32) return op_plan_of(KS_KERNEL_FLAT, 2, 256, true);
-    if (dv >= 448) return op_plan_of(KS_KERNEL_CTA_ROW, 2, 96, true);
-    if (dv >= 288 || dv == 160 || dv == 192) return op_plan_of(KS_KERNEL_CTA_ROW, 2, 256, true);
-    return op_plan_of(KS_KERNEL_FLAT, 2, 256, true);
+    if (dv % (dtype == KS_DTYPE_F32 ? 64 : 32) == 0) return op_plan_of(KS_KERNEL_CTA_ROW, 2, 256, true);
+    return op_plan_of(KS_KERNEL_FLAT, 2, 128, true);
 }
 
-// Width bands for many rows (more rows than SMs) of at most 256 vectors, measured on GB300 per
-// dtype, each plan timed in steady state and right after a kernel with a large shared-memory
-// carveout, the worse of the two kept (bench.py --ops-bands re-runs that measurement): rows up
-// to `hi` vectors take one warp per row at `v` vectors per lane (kind 'w'), a CTA per row at 4
-// vectors with prefetch (kind 'c'), or the general rule (kind 'g'). A CTA per row of 33..64
-// threads, most of them idle or split across two partly filled warps, paid two CTA barriers per
-// row; warp rows reduce with shuffles alone and fill their lanes. Gains over the general rule at
-// the narrowest widths were 20-39 points of the copy peak (Softmax bf16 72 vectors: 0.52 -> 0.91;
-// LayerNorm fp16 96 vectors: 0.53 -> 0.85).
+// Width bands for many rows (more rows than SMs) of at most 256 vectors: rows up to `hi` vectors
+// take a team of `team` lanes per row at `v` vectors per lane (kind 'w'; 8- and 16-lane teams put
+// 4 or 2 rows in a warp), a CTA per row at `v` vectors (kind 'c'), or the general rule (kind
+// 'g'); `prefetch` as the name says. The tables are printed by
+//   python bench.py --ops-bands-derive <the JSON lines of bench.py --ops-bands>
+// from a GB300 run of --ops-bands over 8..256 vectors: at each width every candidate is scored by
+// the worse of two contexts (steady, and right after a kernel with a large shared-memory
+// carveout) and by its worst dtype among those that share the table; the previous plan is kept
+// unless another scores a point of the copy peak higher. Warp rows reduce with shuffles alone and
+// fill their lanes, where a CTA per row of 33..64 threads, most of them idle, paid two CTA
+// barriers per row; sub-warp teams took rows of 8..56 vectors from 0.18-0.90 to 0.68-0.96 (e.g.
+// Softmax bf16 16 vectors 0.42 -> 0.94, LayerNorm fp16 32 vectors 0.60 -> 0.94).
 struct Band {
     int16_t hi;
     char kind;
     int8_t v;
     bool prefetch;
+    int8_t team = 32;  // lanes per row of a 'w' band
 };
 
 constexpr int16_t kBandEnd = 32767;
-constexpr Band kSoftmax16[] = {{32, 'w', 2, false}, {63, 'w', 2, true}, {127, 'w', 4, true},
-                               {128, 'g', 0, false}, {192, 'w', 6, false}, {224, 'w', 8, false},
-                               {kBandEnd, 'g', 0, false}};
-constexpr Band kSoftmax32[] = {{44, 'w', 2, false}, {52, 'w', 2, true}, {63, 'w', 4, false},
-                               {64, 'g', 0, false}, {80, 'w', 4, true}, {128, 'w', 4, false},
-                               {168, 'w', 6, false}, {176, 'g', 0, false}, {216, 'c', 4, true},
-                               {256, 'w', 8, false}, {kBandEnd, 'g', 0, false}};
-constexpr Band kLayerNormBf16[] = {{64, 'w', 2, true}, {127, 'w', 4, true}, {128, 'g', 0, true},
-                                   {192, 'w', 6, true}, {256, 'w', 8, true},
-                                   {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormF16[] = {{64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true},
-                                  {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormF32[] = {{63, 'w', 2, true}, {64, 'g', 0, true}, {128, 'w', 4, true},
-                                  {192, 'w', 6, true}, {224, 'w', 8, true}, {kBandEnd, 'g', 0, true}};
+constexpr Band kSoftmax16[] = {{16, 'w', 2, true, 8}, {20, 'w', 4, false, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {45, 'w', 4, false, 16}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {112, 'w', 4, true}, {127, 'c', 4, false}, {129, 'w', 6, true}, {144, 'w', 6, false}, {169, 'w', 8, true}, {225, 'w', 8, false}, {256, 'g', 0, false}, {kBandEnd, 'g', 0, true}};
+constexpr Band kSoftmax32[] = {{8, 'w', 2, false, 8}, {12, 'w', 2, true, 8}, {20, 'w', 2, false, 16}, {28, 'w', 4, false, 8}, {32, 'w', 2, false}, {33, 'w', 4, false, 16}, {40, 'w', 2, false}, {53, 'w', 4, false, 16}, {56, 'w', 4, false}, {63, 'w', 4, true}, {64, 'g', 0, true}, {65, 'w', 4, false}, {72, 'w', 4, true}, {81, 'w', 6, false}, {96, 'w', 6, true}, {112, 'w', 8, false}, {127, 'c', 4, false}, {128, 'w', 4, false}, {129, 'w', 8, false}, {144, 'w', 8, true}, {168, 'w', 6, false}, {176, 'g', 0, false}, {177, 'c', 4, false}, {192, 'w', 6, false}, {208, 'c', 4, false}, {225, 'c', 4, true}, {256, 'w', 8, false}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormBf16[] = {{16, 'w', 2, true, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {64, 'w', 4, true, 16}, {127, 'w', 4, true}, {192, 'w', 6, true}, {256, 'w', 8, true}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF16[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {56, 'w', 4, true, 16}, {64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true}, {256, 'g', 0, true}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF32[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'c', 2, true}, {64, 'w', 4, true, 16}, {112, 'w', 4, true}, {127, 'c', 4, true}, {169, 'w', 6, true}, {225, 'w', 8, true}, {256, 'g', 0, true}, {kBandEnd, 'g', 0, true}};
 
 // Applies the band of a row of hv vectors to p (the general rule's plan) when there are more rows
 // than SMs; warp plans take 128-thread CTAs (4 rows each).
@@ -1100,7 +1116,7 @@ void apply_band(const Band *bands, int64_t hv, int64_t rows, int sms, ks_plan_t 
     const Band *b = bands;
     while (hv > b->hi) ++b;
     if (b->kind == 'w')
-        *p = op_plan_of(KS_KERNEL_WARP_ROW, b->v, 128, b->prefetch);
+        *p = op_plan_of(KS_KERNEL_WARP_ROW, b->v, 128, b->prefetch, 0, b->team);
     else if (b->kind == 'c')
         *p = op_plan_of(KS_KERNEL_CTA_ROW, b->v, (int)round_up64(ceil_div64(hv, b->v), 32), b->prefetch);
 }
@@ -1184,13 +1200,17 @@ ks_status_t op_check(int op, ks_plan_t &p, bool vec, int64_t width, int64_t elem
     if (p.kernel != KS_KERNEL_BULK_ROW) p.stages = 0;
     switch (p.kernel) {
     case KS_KERNEL_WARP_ROW:
-        if (p.vec_per_thread != 2 && p.vec_per_thread != 4 && p.vec_per_thread != 6 &&
-            p.vec_per_thread != 8)
-            return fail(KS_ERR_INVALID_ARGUMENT, "warp rows take 2, 4, 6 or 8 vectors per lane");
-        if (32LL * p.vec_per_thread < width || p.block > 128)
+        if (p.team == 0) p.team = 32;
+        if (p.team != 32 && p.team != 16 && p.team != 8)
+            return fail(KS_ERR_INVALID_ARGUMENT, "warp-row teams are 32, 16 or 8 lanes (got %d)", p.team);
+        if (p.team == 32 ? (p.vec_per_thread != 2 && p.vec_per_thread != 4 &&
+                            p.vec_per_thread != 6 && p.vec_per_thread != 8)
+                         : (p.vec_per_thread != 2 && p.vec_per_thread != 4))
+            return fail(KS_ERR_INVALID_ARGUMENT, "warp rows take 2, 4, 6 or 8 vectors per lane "
+                        "(teams of 8 or 16 lanes: 2 or 4)");
+        if ((int64_t)p.team * p.vec_per_thread < width || p.block > 128)
             return fail(KS_ERR_INVALID_ARGUMENT, "warp-row plan does not cover the row or block > 128");
         if (ln && !pf) return fail(KS_ERR_INVALID_ARGUMENT, "LayerNorm rows always prefetch");
-        p.team = 32;
         return KS_SUCCESS;
     case KS_KERNEL_CTA_ROW:
         if (p.vec_per_thread != 1 && p.vec_per_thread != 2 && p.vec_per_thread != 4)
@@ -1264,8 +1284,18 @@ cudaError_t silu_dispatch(const ks_plan_t &p, void *out, const void *x, int64_t 
         // resident at once (a CTA left for a second wave of this persistent grid would start only
         // when a first-wave one has finished all its rows)
         const void *f = (const void *)silu_mul_rows_kernel<T>;
-        const int64_t gx = ceil_div64(dd, 2 * (int64_t)p.block);
-        const int bx = (int)round_up64(ceil_div64(dd, 2 * gx), 32);
+        // the fewest CTAs across the row whose threads leave the fewest idle: 576 vectors run as
+        // 3 CTAs of 96 threads (no idle thread) rather than 2 of 160 (64 idle), which measured
+        // 0.93 against 0.90 of the copy peak
+        int64_t gx = ceil_div64(dd, 2 * (int64_t)p.block);
+        int bx = (int)round_up64(ceil_div64(dd, 2 * gx), 32);
+        for (int64_t g2 = gx + 1; g2 <= 4 * gx && 2 * gx * bx > dd; ++g2) {
+            const int b2 = (int)round_up64(ceil_div64(dd, 2 * g2), 32);
+            if (2 * g2 * b2 < 2 * gx * bx) {
+                gx = g2;
+                bx = b2;
+            }
+        }
         int64_t by = 256 / bx;
         by = by > rows ? rows : by;
         int64_t gy = ceil_div64(rows, by);
@@ -1291,7 +1321,7 @@ cudaError_t silu_dispatch(const ks_plan_t &p, void *out, const void *x, int64_t 
 // need (warp plans: block / 32 rows per CTA), no more than the plan's grid when it gives one.
 int64_t reg_grid(const void *f, const ks_plan_t &p, size_t smem, int64_t rows, int sms) {
     const int n = cached_occupancy(f, p.block, smem);
-    const int64_t per_cta = p.kernel == KS_KERNEL_WARP_ROW ? p.block / 32 : 1;
+    const int64_t per_cta = p.kernel == KS_KERNEL_WARP_ROW ? p.block / p.team : 1;
     const int64_t need = ceil_div64(rows, per_cta);
     const int64_t grid = (int64_t)sms * n;
     return cap_grid(grid > need ? need : grid, p);
@@ -1306,15 +1336,23 @@ cudaError_t softmax_dispatch(const ks_plan_t &p, void *out, const void *x, int64
     const void *f = nullptr;
     switch (p.kernel) {
     case KS_KERNEL_WARP_ROW:
-        switch (p.vec_per_thread) {
-        case 2: f = pf ? (const void *)softmax_vec_kernel<T, 2, true, true>
-                       : (const void *)softmax_vec_kernel<T, 2, false, true>; break;
-        case 4: f = pf ? (const void *)softmax_vec_kernel<T, 4, true, true>
-                       : (const void *)softmax_vec_kernel<T, 4, false, true>; break;
-        case 6: f = pf ? (const void *)softmax_vec_kernel<T, 6, true, true>
-                       : (const void *)softmax_vec_kernel<T, 6, false, true>; break;
-        case 8: f = pf ? (const void *)softmax_vec_kernel<T, 8, true, true>
-                       : (const void *)softmax_vec_kernel<T, 8, false, true>; break;
+        switch (p.team * 16 + p.vec_per_thread) {
+        case 32 * 16 + 2: f = pf ? (const void *)softmax_vec_kernel<T, 2, true, 32>
+                                 : (const void *)softmax_vec_kernel<T, 2, false, 32>; break;
+        case 32 * 16 + 4: f = pf ? (const void *)softmax_vec_kernel<T, 4, true, 32>
+                                 : (const void *)softmax_vec_kernel<T, 4, false, 32>; break;
+        case 32 * 16 + 6: f = pf ? (const void *)softmax_vec_kernel<T, 6, true, 32>
+                                 : (const void *)softmax_vec_kernel<T, 6, false, 32>; break;
+        case 32 * 16 + 8: f = pf ? (const void *)softmax_vec_kernel<T, 8, true, 32>
+                                 : (const void *)softmax_vec_kernel<T, 8, false, 32>; break;
+        case 16 * 16 + 2: f = pf ? (const void *)softmax_vec_kernel<T, 2, true, 16>
+                                 : (const void *)softmax_vec_kernel<T, 2, false, 16>; break;
+        case 16 * 16 + 4: f = pf ? (const void *)softmax_vec_kernel<T, 4, true, 16>
+                                 : (const void *)softmax_vec_kernel<T, 4, false, 16>; break;
+        case 8 * 16 + 2: f = pf ? (const void *)softmax_vec_kernel<T, 2, true, 8>
+                                : (const void *)softmax_vec_kernel<T, 2, false, 8>; break;
+        case 8 * 16 + 4: f = pf ? (const void *)softmax_vec_kernel<T, 4, true, 8>
+                                : (const void *)softmax_vec_kernel<T, 4, false, 8>; break;
         default: return cudaErrorInvalidConfiguration;
         }
         break;
@@ -1367,15 +1405,23 @@ cudaError_t layer_norm_dispatch(const ks_plan_t &p, void *out, const void *x, co
     const void *f = nullptr;
     switch (p.kernel) {
     case KS_KERNEL_WARP_ROW:
-        switch (p.vec_per_thread) {
-        case 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0, true>, layer_norm_vec_kernel<T, 2, 1, true>,
-                                       layer_norm_vec_kernel<T, 2, 2, true>, layer_norm_vec_kernel<T, 2, 3, true>); break;
-        case 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0, true>, layer_norm_vec_kernel<T, 4, 1, true>,
-                                       layer_norm_vec_kernel<T, 4, 2, true>, layer_norm_vec_kernel<T, 4, 3, true>); break;
-        case 6: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 6, 0, true>, layer_norm_vec_kernel<T, 6, 1, true>,
-                                       layer_norm_vec_kernel<T, 6, 2, true>, layer_norm_vec_kernel<T, 6, 3, true>); break;
-        case 8: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 8, 0, true>, layer_norm_vec_kernel<T, 8, 1, true>,
-                                       layer_norm_vec_kernel<T, 8, 2, true>, layer_norm_vec_kernel<T, 8, 3, true>); break;
+        switch (p.team * 16 + p.vec_per_thread) {
+        case 32 * 16 + 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0, 32>, layer_norm_vec_kernel<T, 2, 1, 32>,
+                                                 layer_norm_vec_kernel<T, 2, 2, 32>, layer_norm_vec_kernel<T, 2, 3, 32>); break;
+        case 32 * 16 + 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0, 32>, layer_norm_vec_kernel<T, 4, 1, 32>,
+                                                 layer_norm_vec_kernel<T, 4, 2, 32>, layer_norm_vec_kernel<T, 4, 3, 32>); break;
+        case 32 * 16 + 6: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 6, 0, 32>, layer_norm_vec_kernel<T, 6, 1, 32>,
+                                                 layer_norm_vec_kernel<T, 6, 2, 32>, layer_norm_vec_kernel<T, 6, 3, 32>); break;
+        case 32 * 16 + 8: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 8, 0, 32>, layer_norm_vec_kernel<T, 8, 1, 32>,
+                                                 layer_norm_vec_kernel<T, 8, 2, 32>, layer_norm_vec_kernel<T, 8, 3, 32>); break;
+        case 16 * 16 + 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0, 16>, layer_norm_vec_kernel<T, 2, 1, 16>,
+                                                 layer_norm_vec_kernel<T, 2, 2, 16>, layer_norm_vec_kernel<T, 2, 3, 16>); break;
+        case 16 * 16 + 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0, 16>, layer_norm_vec_kernel<T, 4, 1, 16>,
+                                                 layer_norm_vec_kernel<T, 4, 2, 16>, layer_norm_vec_kernel<T, 4, 3, 16>); break;
+        case 8 * 16 + 2: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 2, 0, 8>, layer_norm_vec_kernel<T, 2, 1, 8>,
+                                                layer_norm_vec_kernel<T, 2, 2, 8>, layer_norm_vec_kernel<T, 2, 3, 8>); break;
+        case 8 * 16 + 4: f = layer_norm_pick<T>(affine, layer_norm_vec_kernel<T, 4, 0, 8>, layer_norm_vec_kernel<T, 4, 1, 8>,
+                                                layer_norm_vec_kernel<T, 4, 2, 8>, layer_norm_vec_kernel<T, 4, 3, 8>); break;
         default: return cudaErrorInvalidConfiguration;
         }
         break;

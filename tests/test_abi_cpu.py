@@ -630,9 +630,16 @@ def test_next_op_plans_follow_the_bands():
     assert (p.kernel, p.vec_per_thread, p.block, p.flags) == (WARP, 4, 128, 0)
     # ... but not in the latency regime (rows <= SMs): a CTA per row
     assert op_plan(SM, 100, 72 * 8).kernel == CTA
-    # Softmax fp32 rows of 177..216 vectors: CTA rows at 4 vectors with prefetch
+    # Softmax fp32 rows of 193..208 vectors: CTA rows at 4 vectors without prefetch
     p = op_plan(SM, 1000, 200 * 4, F32)
-    assert (p.kernel, p.vec_per_thread, p.flags) == (CTA, 4, 0) and p.block == 64
+    assert (p.kernel, p.vec_per_thread, p.flags) == (CTA, 4, _abi.KS_PLAN_NO_PREFETCH)
+    assert p.block == 64
+    # Softmax 16-bit rows of at most 16 vectors: teams of 8 lanes at 2 vectors, 4 rows a warp
+    p = op_plan(SM, 1000, 16 * 8)
+    assert (p.kernel, p.team, p.vec_per_thread, p.block) == (WARP, 8, 2, 128)
+    # LayerNorm fp16 rows of 33..56 vectors: teams of 16 lanes at 4 vectors
+    p = op_plan(LN, 1000, 40 * 8, F16)
+    assert (p.kernel, p.team, p.vec_per_thread) == (WARP, 16, 4)
     # Softmax rows of 128..1024 vectors: CTA rows at 4 vectors without prefetch; wider prefetch
     p = op_plan(SM, 1000, 512 * 8)
     assert (p.kernel, p.vec_per_thread, p.block, p.flags) == (CTA, 4, 128, _abi.KS_PLAN_NO_PREFETCH)
@@ -648,11 +655,15 @@ def test_next_op_plans_follow_the_bands():
     assert (p.kernel, p.vec_per_thread, p.block, p.stages) == (BULK, 4, 256, 4)
     p = op_plan(LN, 32768, 1280 * 8)
     assert (p.kernel, p.block) == (TWO, 128)
-    # SwiGLU: fp32 the flat walk; 16-bit rows of >= 448 vectors the row kernel capped at 96
-    assert op_plan(SW, 1000, 4096, F32).kernel == _abi.KS_KERNEL_FLAT
+    # SwiGLU: the row kernel for rows of a multiple of 32 vectors (fp32: 64), else the flat walk
+    # on 128-thread CTAs
     p = op_plan(SW, 1000, 1024 * 8)
-    assert (p.kernel, p.block) == (CTA, 96)
-    assert op_plan(SW, 1000, 64 * 8).kernel == _abi.KS_KERNEL_FLAT
+    assert (p.kernel, p.block) == (CTA, 256)
+    assert op_plan(SW, 1000, 64 * 8).kernel == CTA
+    p = op_plan(SW, 1000, 65 * 8)
+    assert (p.kernel, p.block) == (_abi.KS_KERNEL_FLAT, 128)
+    assert op_plan(SW, 1000, 128 * 4, F32).kernel == CTA
+    assert op_plan(SW, 1000, 96 * 4, F32).kernel == _abi.KS_KERNEL_FLAT
     # rows that cannot be vectorised
     for op in (SM, LN, SW):
         assert op_plan(op, 10, 1001).kernel == _abi.KS_KERNEL_SCALAR
@@ -690,3 +701,36 @@ def test_next_op_planned_entry_points_check_the_plan():
     for p in (mk(WARP, 4, 128), mk(_abi.KS_KERNEL_FLAT, 2, 512), mk(CTA, 2, 288)):
         assert _abi.ks_silu_and_mul_planned(a, b, rows, h, BF16, p, None) == E
     assert _abi.load().ks_softmax_planned(a, b, rows, h, BF16, None, None) == E
+
+
+@pytest.mark.parametrize("dtype", [BF16, F16, F32])
+def test_every_next_op_plan_is_a_valid_launch(dtype):
+    """Every row width from 1 to 600 vectors, few and many rows: each default plan of Softmax,
+    LayerNorm and SwiGLU obeys the rules the planned entry points enforce (a team that covers the
+    row, a block within the kernel's bound, a variant that exists), so the default path never
+    builds a launch the library would refuse."""
+    per = 4 if dtype == F32 else 8
+    for rows in (7, 152, 153, 5000):
+        for hv in range(1, 601):
+            for op in (_abi.OP_SOFTMAX, _abi.OP_LAYER_NORM, _abi.OP_SILU_AND_MUL):
+                p = op_plan(op, rows, hv * per, dtype)
+                assert p.block % 32 == 0 and 32 <= p.block <= 1024, (op, rows, hv, p.as_dict())
+                npf = bool(p.flags & _abi.KS_PLAN_NO_PREFETCH)
+                if op == _abi.OP_SILU_AND_MUL:
+                    assert p.kernel in (_abi.KS_KERNEL_FLAT, CTA) and p.block <= 256
+                    continue
+                if p.kernel == WARP:
+                    assert p.team in (8, 16, 32) and p.block <= 128 and p.block % p.team == 0
+                    assert p.vec_per_thread in ((2, 4, 6, 8) if p.team == 32 else (2, 4))
+                    assert p.team * p.vec_per_thread >= hv, (op, rows, hv)
+                    assert not (npf and op == _abi.OP_LAYER_NORM)
+                elif p.kernel == CTA:
+                    assert p.vec_per_thread in (1, 2, 4) and p.block <= 512
+                    assert p.block * p.vec_per_thread >= hv, (op, rows, hv)
+                    assert not npf or (op == _abi.OP_SOFTMAX and p.vec_per_thread == 4)
+                elif p.kernel == BULK:
+                    assert op == _abi.OP_LAYER_NORM and p.vec_per_thread == 4 and 2 <= p.stages <= 8
+                    assert p.block * 4 >= hv and 128 + p.stages * hv * 16 <= 226 * 1024
+                else:
+                    assert p.kernel == TWO and p.vec_per_thread == 4
+                    assert p.block <= (512 if op == _abi.OP_LAYER_NORM else 1024)

@@ -241,8 +241,9 @@ def test_layer_norm_rows_wider_than_registers(cuda_device, dtype, rows, h, affin
 
 # Row widths in 16-byte vectors at the edges of the measured plan bands for many rows (warp rows
 # at 2, 4, 6 or 8 vectors per lane, CTA rows, the general rule), for every dtype.
-BAND_HV = [16, 32, 33, 44, 45, 52, 53, 63, 64, 65, 72, 80, 81, 127, 128, 129, 168, 169, 176, 177,
-           192, 193, 216, 217, 224, 225, 256, 257]
+BAND_HV = [1, 2, 7, 8, 9, 12, 13, 16, 17, 20, 21, 28, 29, 32, 33, 40, 41, 44, 45, 52, 53, 54,
+           56, 57, 63, 64, 65, 72, 73, 80, 81, 82, 96, 97, 112, 113, 127, 128, 129, 130, 144, 145,
+           168, 169, 170, 176, 177, 178, 192, 193, 208, 209, 216, 217, 224, 225, 226, 256, 257]
 
 
 def _elems(dt, hv):
@@ -288,11 +289,11 @@ def test_layer_norm_at_plan_band_edges(cuda_device, dtype, hv, affine):
 
 
 @pytest.mark.parametrize("dtype", DT)
-@pytest.mark.parametrize("dv", [64, 159, 160, 161, 191, 192, 193, 256, 287, 288, 447, 448, 512,
-                                1024, 1280, 2048])
+@pytest.mark.parametrize("dv", [16, 31, 32, 33, 64, 96, 128, 159, 160, 161, 191, 192, 193, 256, 287,
+                                288, 447, 448, 512, 576, 640, 1024, 1280, 2048])
 def test_silu_and_mul_at_plan_band_edges(cuda_device, dtype, dv):
     """SwiGLU on many rows at the edges of its launch shapes: the flat walk, and the row kernel
-    with its block fitted to the row (at most 256 or 96 threads)."""
+    with its CTAs fitted to the row (at most 256 threads, the fewest idle)."""
     dt = synth.dtype_of(dtype)
     d = _elems(dt, dv)
     rows = 700 if dv <= 512 else 150

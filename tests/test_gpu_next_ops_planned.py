@@ -28,8 +28,10 @@ def _vectors(dt, hidden):
 
 
 # Softmax / LayerNorm variants: (name, kernel, vectors per thread, block or None for "fitted",
-# flags, stages)
+# flags, stages[, lanes per row for warp rows])
 ROW_VARIANTS = [
+    ("t8v2", A.KS_KERNEL_WARP_ROW, 2, 128, 0, 0, 8), ("t8v4n", A.KS_KERNEL_WARP_ROW, 4, 96, NP, 0, 8),
+    ("t16v2n", A.KS_KERNEL_WARP_ROW, 2, 64, NP, 0, 16), ("t16v4", A.KS_KERNEL_WARP_ROW, 4, 128, 0, 0, 16),
     ("w2", A.KS_KERNEL_WARP_ROW, 2, 128, 0, 0), ("w2n", A.KS_KERNEL_WARP_ROW, 2, 64, NP, 0),
     ("w4", A.KS_KERNEL_WARP_ROW, 4, 128, 0, 0), ("w4n", A.KS_KERNEL_WARP_ROW, 4, 96, NP, 0),
     ("w6", A.KS_KERNEL_WARP_ROW, 6, 128, 0, 0), ("w8n", A.KS_KERNEL_WARP_ROW, 8, 128, NP, 0),
@@ -45,11 +47,12 @@ ROW_VARIANTS = [
 
 
 def _row_plan(variant, op, dt, hidden):
-    name, kernel, v, block, flags, stages = variant
+    name, kernel, v, block, flags, stages = variant[:6]
+    team = variant[6] if len(variant) > 6 else 32
     hv = _vectors(dt, hidden)
     if kernel != A.KS_KERNEL_SCALAR and (hidden * (4 if dt == torch.float32 else 2)) % 16:
         return None
-    if kernel == A.KS_KERNEL_WARP_ROW and 32 * v < hv:
+    if kernel == A.KS_KERNEL_WARP_ROW and team * v < hv:
         return None
     if block is None:
         block = max(32, _up32(-(-hv // v)))
@@ -61,10 +64,13 @@ def _row_plan(variant, op, dt, hidden):
         return None
     if kernel == A.KS_KERNEL_TWOPASS_ROW and op == "layer_norm" and block > 512:
         return None
-    return A.make_plan(kernel, v, block, stages, flags=flags)
+    return A.make_plan(kernel, v, block, stages, flags=flags, team=team)
 
 
-SHAPES = [(333, 512), (1001, 1000), (77, 2056), (45, 4096), (9, 20480)]
+# ragged row counts (not a multiple of a CTA's teams, so some teams of a warp have no row), widths
+# of 8..64 vectors for the sub-warp teams, wider ones for the rest
+SHAPES = [(333, 512), (1001, 1000), (77, 2056), (45, 4096), (9, 20480), (1003, 64), (7, 128),
+          (517, 248), (2001, 256)]
 
 
 @pytest.mark.parametrize("variant", ROW_VARIANTS, ids=[v[0] for v in ROW_VARIANTS])
