@@ -1109,7 +1109,8 @@ def plan_candidates(op: str, hv: int, elem: int):
     p2/n2/p4/n4 (CTA per row, 2 or 4 vectors per thread, with/without prefetch), b2 (staged ring,
     2 stages), tBuU (the two-pass kernel, B threads, U vectors per thread per step; rows of at
     least 512 vectors), sCbBuU (the two-pass kernel split over a cluster of C CTAs; rows of at
-    least 1024 vectors), both also with a trailing n (no L2 prefetch of the next row), and for
+    least 1024 vectors), both also with a trailing n (no L2 prefetch of the row), sCbBuUp (the
+    split kernel with two rows in flight per cluster, no prefetch), and for
     rows wider than 2048 vectors cC (register-resident cluster of C CTAs, 4 vectors per thread)
     and bCsS (staged ring split over C CTAs, S stages)."""
     from row_wise_rmsnorm_ks_gb300 import _abi
@@ -1149,6 +1150,8 @@ def plan_candidates(op: str, hv: int, elem: int):
                                                                   blk, cluster=c)))
                     out.append((f"s{c}b{blk}u{u}n", _abi.make_plan(
                         _abi.KS_KERNEL_TWOPASS_ROW, u, blk, cluster=c, flags=npf)))
+                    out.append((f"s{c}b{blk}u{u}p", _abi.make_plan(
+                        _abi.KS_KERNEL_TWOPASS_ROW, u, blk, 2, cluster=c, flags=npf)))
     if hv > 2048:
         for c in (2, 4, 8):
             sl = -(-hv // c)

@@ -166,7 +166,9 @@ enum {
                                   down to one CTA per SM. With cluster >= 2 each row is split
                                   over a cluster: CTA q runs both passes on its slice of
                                   ceil(hv / cluster) vectors and the slice sums meet in
-                                  distributed shared memory, one cluster barrier per row.
+                                  distributed shared memory, one cluster barrier per row;
+                                  stages 2 keeps two rows in flight per cluster (the next
+                                  row's first pass in the same loop as this row's second).
                                   Softmax and LayerNorm: their multi-pass wide kernel */
     KS_KERNEL_FLAT = 7         /* SwiGLU only: a grid-stride walk over all rows' vectors */
 };

@@ -91,7 +91,8 @@ constexpr int kSmemLimit = 226 * 1024;  // dynamic ring; static smem and reserve
 // one-CTA-per-row kernel never drops below one CTA per SM (for rows of 16384 vectors and more,
 // measured: a full grid with some L2 misses beats fewer CTAs, 0.66-0.81 of the copy peak
 // against 0.39-0.68 for fused rows).
-int64_t twopass_l2_budget(int64_t l2_bytes) { return l2_bytes > 0 ? l2_bytes / 4 * 3 : 96ll << 20; }
+constexpr int64_t kDefaultL2Bytes = 128ll << 20;  // when no device size is given
+int64_t twopass_l2_budget(int64_t l2_bytes) { return (l2_bytes > 0 ? l2_bytes : kDefaultL2Bytes) / 4 * 3; }
 
 int64_t twopass_grid_cap(int64_t hv, bool fused, int sm_count, int64_t l2_bytes) {
     const int64_t per_cta = hv * 16 * (fused ? 2 : 1);
@@ -100,11 +101,12 @@ int64_t twopass_grid_cap(int64_t hv, bool fused, int sm_count, int64_t l2_bytes)
 }
 
 // Clusters of the split two-pass kernel: no more than keep their rows in flight (one per
-// cluster) within the L2 budget; then as few as give every cluster the same number of rows (a
+// cluster, two for the pipelined kernel) within the L2 budget; then as few as give every cluster the same number of rows (a
 // last wave that only some clusters run leaves the others' SMs idle), e.g. 768 rows on 152
 // resident clusters run as 6 rows on each of 128 clusters instead of 5 or 6 on 152.
-int64_t split_clusters(int64_t rows, int64_t resident, int64_t hv, bool fused, int64_t l2_bytes) {
-    const int64_t row_bytes = hv * 16 * (fused ? 2 : 1);
+int64_t split_clusters(int64_t rows, int64_t resident, int64_t hv, bool fused, int rows_in_flight,
+                       int64_t l2_bytes) {
+    const int64_t row_bytes = hv * 16 * (fused ? 2 : 1) * (rows_in_flight > 1 ? rows_in_flight : 1);
     int64_t n = twopass_l2_budget(l2_bytes) / (row_bytes > 0 ? row_bytes : 1);
     n = n < resident ? n : resident;
     n = n < rows ? n : rows;
@@ -122,7 +124,11 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
     const int64_t hv = vec_ok ? hidden / per_vec : 0;
     if (p.block < 32 || p.block % 32 != 0)
         return fail(KS_ERR_INVALID_ARGUMENT, "plan block %d is not a positive multiple of 32", p.block);
-    p.stages = p.kernel == KS_KERNEL_BULK_ROW ? p.stages : 0;
+    const bool split_req = p.kernel == KS_KERNEL_TWOPASS_ROW && p.cluster >= 2;
+    if (split_req && (p.stages < 0 || p.stages > 2))
+        return fail(KS_ERR_INVALID_ARGUMENT, "split two-pass plan: stages 0, 1 (one row in flight) or 2 "
+                    "(two rows), got %d", p.stages);
+    p.stages = (p.kernel == KS_KERNEL_BULK_ROW || split_req) ? p.stages : 0;
     p.smem_bytes = 0;
     const bool split_bulk = p.kernel == KS_KERNEL_BULK_ROW && p.cluster >= 2;
     const bool split_twopass = p.kernel == KS_KERNEL_TWOPASS_ROW && p.cluster >= 2;
@@ -334,7 +340,7 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
         }
         if (p.kernel == KS_KERNEL_TWOPASS_ROW && !(forced && forced->grid > 0)) {
             const int64_t n = split_clusters(rows, p.grid / p.cluster, hidden / (16 / e), fused,
-                                             slot.l2_bytes);
+                                             p.stages == 2 ? 2 : 1, slot.l2_bytes);
             p.grid = n * p.cluster;
             p.rows_per_pass = n;
         }
@@ -476,21 +482,25 @@ void twopass_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
     p->team = p->block;
 }
 
-// Many wide rows: the two-pass kernel split over a cluster of C = clamp(hv / 4096, 2, 8) CTAs,
-// so each CTA's slice is about 4096 vectors (64 KiB a tensor), read 1024 vectors a step: plain
-// rows by 256 threads at 4 vectors with each slice asked into L2 as the row starts, fused rows by
-// 512 threads at 2 without. Measured on GB300 (plan sweep, 384 MiB per tensor, bf16/fp16/fp32):
-// plain rows of 16384 and 32768 vectors 0.83-0.86 of the copy peak, fused rows of 8192 0.86-0.93,
-// 16384 0.84-0.91 and 32768 0.79-0.86, against 0.66-0.81 with one CTA per row (whose last wave,
-// at 10 rows per CTA, left SMs idle, and whose rows in flight outgrew L2 for fused rows).
+// Many wide rows: the two-pass kernel split over a cluster. Measured on GB300 (plan sweep, 384 MiB
+// per tensor, bf16/fp16), against 0.66-0.81 of the copy peak with one CTA per row (whose last wave,
+// at 10 rows per CTA, left SMs idle, and whose rows in flight outgrew L2 for fused rows):
+//  * plain rows: C = clamp(hv / 4096, 2, 8) CTAs, slices of about 4096 vectors (64 KiB) read 1024
+//    vectors a step by 256 threads at 4 vectors, each slice asked into L2 as the row starts;
+//    0.83-0.86 at 16384 and 32768 vectors (two rows in flight measured 0.79-0.87, no better);
+//  * fused rows: C = clamp(hv / 2048, 2, 8) CTAs, slices of about 2048 vectors, 512 threads at 2
+//    vectors, two rows in flight per cluster (the next row's first pass in the loop of this row's
+//    second, so every CTA reads DRAM and writes together); 0.93-0.95 at 8192 vectors, 0.91-0.93 at
+//    16384 and 32768, against 0.80-0.90 with one row in flight.
 void split_row(ks_plan_t *p, int64_t hv, bool fused) {
-    const int64_t c = hv / 4096;
+    const int64_t c = hv / (fused ? 2048 : 4096);
     p->kernel = KS_KERNEL_TWOPASS_ROW;
     p->cluster = (int32_t)(c < 2 ? 2 : (c > 8 ? 8 : c));
     p->vec_per_thread = fused ? 2 : 4;
     p->block = fused ? 512 : 256;
     p->team = p->block * p->cluster;
     p->flags = fused ? KS_PLAN_NO_PREFETCH : 0;
+    p->stages = fused ? 2 : 0;
 }
 
 }  // namespace
@@ -579,8 +589,12 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         p->vec_per_thread = slice <= 512 ? 1 : (slice <= 1024 ? 2 : 4);
         p->block = (int32_t)round_up(ceil_div(slice, p->vec_per_thread), 32);
         p->team = p->block * 8;
-    } else if (vec_ok && (hv > 8192 || (fused && hv > 4096))) {
-        // Very wide rows, more of them: the two-pass kernel split over a cluster.
+    } else if (vec_ok && (hv > 8192 || (fused && hv > 4096)) &&
+               rows * hv * 32 > (l2_bytes > 0 ? l2_bytes : kDefaultL2Bytes)) {
+        // Very wide rows, more than L2 holds: the two-pass kernel split over a cluster. (Rows that
+        // fit in L2 run faster one CTA per row: a probe of 76..1216 rows measured the one-CTA
+        // kernel ahead up to about the L2 size, e.g. fused 8192-vector rows 0.82 against 0.76 at
+        // 456 rows, 112 MiB, and the split kernels ahead beyond, 0.86 against 0.79 at 912 rows.)
         split_row(p, hv, fused);
     } else if (vec_ok && hv > 2048) {
         // Wider rows, more of them: the two-pass kernel (no width limit; the second pass from L2).
@@ -596,7 +610,7 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         const int64_t cap = (int64_t)sm_count * blocks_per_sm / p->cluster;
         if (blocks_per_sm > 0 && clusters > cap) clusters = cap < 1 ? 1 : cap;
         if (p->kernel == KS_KERNEL_TWOPASS_ROW)
-            clusters = split_clusters(rows, clusters, hv, fused, l2_bytes);
+            clusters = split_clusters(rows, clusters, hv, fused, p->stages == 2 ? 2 : 1, l2_bytes);
         p->grid = clusters * p->cluster;
         p->rows_per_pass = clusters;
         return KS_SUCCESS;

@@ -649,8 +649,152 @@ __global__ void __launch_bounds__(kMaxBlock) rows_split_kernel(const RowArgs a) 
     cluster.sync();  // no CTA leaves while a peer may still write its sums here
 }
 
+// The split two-pass scheme with two rows in flight per cluster: each CTA's one loop over its
+// slice reads the *next* row (its first pass, from DRAM: the sum of squares) and re-reads the
+// current row (its second pass, from L2: the outputs), so every CTA keeps DRAM reads and writes
+// in flight together, where the one-row kernel alternates a read-only pass with a
+// read-and-write one, all clusters in step. The next row's slice sums meet in distributed shared
+// memory during the following loop: the cluster barrier's arrive follows the loop, its wait
+// comes after the next loop's first loads. Two alternating slots hold a row's slice sums: CTA q
+// writes slot (j+1) % 2 of a peer only after the barrier of row j, which the peer reaches only
+// once it has read slot (j - 1) % 2. Rows in flight are two per cluster (the grid's L2 cap
+// counts them).
+template <typename T, bool kFused, int U, int kMaxBlock>
+__global__ void __launch_bounds__(kMaxBlock) rows_split_pipe_kernel(const RowArgs a) {
+    namespace cg = cooperative_groups;
+    using E = Elem<T>;
+    constexpr int P = E::kPerVec / 2;
+    __shared__ float red[32];
+    __shared__ float part[2][8];
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int q = (int)cluster.block_rank();
+    const int g = blockDim.x, t = threadIdx.x;
+    const int64_t hv = a.hv;
+    const int64_t S = (hv + C - 1) / C;
+    const int64_t lo = q * S;
+    const int64_t hi = (lo + S < hv) ? lo + S : hv;
+    const int64_t chunk = (int64_t)g * U;
+    const float h = (float)a.hidden;
+    const uint4 *xg = static_cast<const uint4 *>(a.x);
+    uint4 *og = static_cast<uint4 *>(a.out);
+    uint4 *rg = static_cast<uint4 *>(a.res);
+    const uint4 *wg = static_cast<const uint4 *>(a.w);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    grid_dependency_wait();
+    allow_dependents_launch();
+    const int64_t nclusters = gridDim.x / C;
+    int64_t row = blockIdx.x / C;
+
+    // The CTA's slice sum (warps in order) into slot `s` of every CTA of the cluster, then the
+    // arrive of that row's cluster barrier.
+    auto publish = [&](float v, int s) {
+        const float wsum = warp_sum(v);
+        if ((t & 31) == 0) red[t >> 5] = wsum;
+        __syncthreads();
+        if (t < C) {
+            float cta = 0.0f;
+            for (int i = 0; i < (g >> 5); ++i) cta += red[i];
+            *cluster.map_shared_rank(&part[s][q], t) = cta;
+        }
+        cluster.barrier_arrive();
+    };
+
+    // Start: every CTA of the cluster has started before any writes into a peer (the wait below);
+    // then the first row's first pass alone.
+    cluster.barrier_arrive();
+    if (row < a.rows) {
+        PairSumSq<E::kPairMath> acc;
+        const uint4 *xr = xg + row * hv;
+        const uint4 *rr = kFused ? rg + row * hv : nullptr;
+        for (int64_t c0 = lo + t; c0 < hi; c0 += chunk) {
+            uint4 xv[U], rv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                xv[u] = c < hi ? xr[c] : zero;
+                if (kFused) rv[u] = c < hi ? rr[c] : zero;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float2 f[P];
+                row_values<T, kFused>(xv[u], rv[u], f);
+                acc.add(f);
+            }
+        }
+        cluster.barrier_wait();
+        publish(acc.total(), 0);
+    } else {
+        cluster.barrier_wait();
+    }
+
+    for (int j = 0; row < a.rows; row += nclusters, ++j) {
+        const int64_t nxt = row + nclusters;
+        const bool more = nxt < a.rows;  // uniform over the cluster
+        const uint4 *xr = xg + row * hv;
+        uint4 *rr = kFused ? rg + row * hv : nullptr;
+        uint4 *orow = og + row * hv;
+        const uint4 *xn = xg + nxt * hv;
+        const uint4 *rn = kFused ? rg + nxt * hv : nullptr;
+        PairSumSq<E::kPairMath> acc;
+        uint4 xv[U], rv[U], wv[U], xw[U], rw[U];
+        // one step's loads: the next row's vectors (DRAM) and this row's (L2) with the weight
+        auto load = [&](int64_t c0) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                const bool in = c < hi;
+                xw[u] = (more && in) ? xn[c] : zero;
+                if (kFused) rw[u] = (more && in) ? rn[c] : zero;
+                xv[u] = in ? __ldcs(xr + c) : zero;
+                if (kFused) rv[u] = in ? __ldcs(rr + c) : zero;
+                wv[u] = in ? __ldg(wg + c) : zero;
+            }
+        };
+        // one step's work: the next row's sum of squares, this row's outputs
+        auto step = [&](int64_t c0, float scale) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float2 f[P];
+                row_values<T, kFused>(xw[u], rw[u], f);
+                acc.add(f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + (int64_t)u * g;
+                if (c < hi) {
+                    float2 f[P];
+                    row_values<T, kFused>(xv[u], rv[u], f);
+                    if (kFused) __stcs(rr + c, E::pack2(f));
+                    __stcs(orow + c, scaled_weighted<T>(f, scale, wv[u]));
+                }
+            }
+        };
+        // the first step's loads need no scale: issue them before this row's barrier wait
+        int64_t c0 = lo + t;
+        load(c0);
+        cluster.barrier_wait();
+        float ss = 0.0f;
+        for (int r = 0; r < C; ++r) ss += part[j & 1][r];
+        const float scale = row_scale(ss, h, a.eps);
+        step(c0, scale);
+        for (c0 += chunk; c0 < hi; c0 += chunk) {
+            load(c0);
+            step(c0, scale);
+        }
+        if (more) publish(acc.total(), (j + 1) & 1);
+    }
+    cluster.sync();  // no CTA leaves while a peer may still write its sums here
+}
+
 template <typename T, bool kFused, int U>
-const void *pick_split(int block) {
+const void *pick_split(int block, bool pipelined) {
+    if (pipelined) {
+        if (block <= 256) return (const void *)rows_split_pipe_kernel<T, kFused, U, 256>;
+        if (block <= 512) return (const void *)rows_split_pipe_kernel<T, kFused, U, 512>;
+        return (const void *)rows_split_pipe_kernel<T, kFused, U, 1024>;
+    }
     if (block <= 256) return (const void *)rows_split_kernel<T, kFused, U, 256>;
     if (block <= 512) return (const void *)rows_split_kernel<T, kFused, U, 512>;
     return (const void *)rows_split_kernel<T, kFused, U, 1024>;
@@ -1032,8 +1176,8 @@ const void *pick_kernel(const ks_plan_t &p) {
     case KS_KERNEL_TWOPASS_ROW:
         if (p.cluster >= 2) {
             switch (p.vec_per_thread) {
-            case 2: return pick_split<T, kFused, 2>(p.block);
-            case 4: return pick_split<T, kFused, 4>(p.block);
+            case 2: return pick_split<T, kFused, 2>(p.block, p.stages == 2);
+            case 4: return pick_split<T, kFused, 4>(p.block, p.stages == 2);
             default: return nullptr;
             }
         }

@@ -378,13 +378,15 @@ def test_rows_wider_than_registers_take_the_two_pass_kernel(hidden, dtype):
         assert p.vec_per_thread == (2 if op else 4)
         if hv > 8192 or (op and hv > 4096):
             # many rows of more than 8192 vectors (fused: 4096): split over a cluster of
-            # hv / 4096 CTAs (2..8), slices of about 4096 vectors; whole clusters, as many as the
-            # SMs hold, each with the same number of rows; plain rows prefetch each slice to L2
-            c = min(8, max(2, hv // 4096))
+            # hv / 4096 CTAs (fused: hv / 2048; 2..8); whole clusters, as many as the SMs hold,
+            # each with the same number of rows; plain rows prefetch each slice to L2, fused rows
+            # keep two rows in flight per cluster
+            c = min(8, max(2, hv // (2048 if op else 4096)))
             assert p.cluster == c and p.team == p.block * c
             assert p.block == (512 if op else 256)
             assert p.flags == (_abi.KS_PLAN_NO_PREFETCH if op else 0)
-            n = 152 // c
+            assert p.stages == (2 if op else 0)
+            n = min(152 // c, (96 << 20) // (hv * 16 * (4 if op else 1)))
             waves = -(-65536 // n)
             assert p.grid == -(-65536 // waves) * c
             continue
@@ -423,6 +425,7 @@ def test_split_two_pass_plans_are_checked():
     E = _abi.KS_ERR_INVALID_ARGUMENT
     mk = _abi.make_plan
     for p in (mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, 256, cluster=9),    # cluster over 8
+              mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, 256, 3, cluster=4),  # rows in flight: 1 or 2
               mk(_abi.KS_KERNEL_TWOPASS_ROW, 3, 256, cluster=4),    # unsupported vector count
               mk(_abi.KS_KERNEL_TWOPASS_ROW, 2, 2048, cluster=4)):  # block over 1024
         assert _abi.ks_rms_norm_planned(a, b, w, 64, 32768, 1e-6, BF16, p, None) == E

@@ -279,12 +279,13 @@ def _variant_plan(name, hidden, elem):
     if name.startswith("twopass"):  # twopass_b<block>_u<vectors per step>
         block, u = name.split("_b")[1].split("_u")
         return A.make_plan(A.KS_KERNEL_TWOPASS_ROW, int(u), int(block))
-    if name.startswith("split"):  # split_c<cluster>_b<block>_u<vectors per step>
+    if name.startswith("split"):  # split[p]_c<cluster>_b<block>_u<vectors per step>
         c = int(name.split("_c")[1].split("_")[0])
         block, u = name.split("_b")[1].split("_u")
         if (c - 1) * -(-hv // c) >= hv:
             return None
-        return A.make_plan(A.KS_KERNEL_TWOPASS_ROW, int(u), int(block), cluster=c)
+        stages = 2 if name.startswith("splitp") else 0  # splitp: two rows in flight per cluster
+        return A.make_plan(A.KS_KERNEL_TWOPASS_ROW, int(u), int(block), stages, cluster=c)
     flags = A.KS_PLAN_NO_PREFETCH if name.endswith("_np") else 0
     if name.startswith("warp_row"):
         v = next((v for v in (1, 2, 4, 6, 8) if 32 * v >= hv), None)
@@ -312,7 +313,8 @@ VARIANTS = ["warp_row", "warp_row_np", "cta_row_v2", "cta_row_v2_np", "cta_row_v
             "bulk_row_c3_s1", "bulk_row_c8_s3", "cluster_row_c2", "cluster_row_c3",
             "cluster_row_c8", "twopass_b256_u4", "twopass_b512_u2", "twopass_b1024_u4",
             "twopass_b96_u2", "split_c2_b256_u4", "split_c3_b96_u2", "split_c4_b512_u2",
-            "split_c8_b1024_u2", "scalar"]
+            "split_c8_b1024_u2", "splitp_c2_b256_u4", "splitp_c3_b96_u2", "splitp_c4_b512_u2",
+            "splitp_c8_b1024_u2", "scalar"]
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -390,6 +392,43 @@ def test_rows_wider_than_registers_match_oracle(cuda_device, op, dtype, hidden, 
         ref_x, ref_r, _ = oracle.fused_add_rms_norm(x, r, wt, 1e-6)
         assert bits_equal(rd.cpu(), ref_r), name
         compare_output(xd.cpu(), ref_x, dt, hidden, name)
+    st, flags = A.ks_device_faults(clear=True)
+    assert st == A.KS_SUCCESS and flags == 0
+
+
+@pytest.mark.parametrize("op,dtype,rows,hidden", [
+    ("fused_add_rms_norm", "bf16", 1203, 65536),   # 8192 vectors: the split kernel, two rows in flight
+    ("fused_add_rms_norm", "fp16", 605, 131072),   # 16384 vectors, cluster of 8
+    ("rms_norm", "bf16", 701, 131072),             # 16384 vectors: the split kernel with L2 prefetch
+    ("rms_norm", "fp32", 1001, 32768),             # 8192 fp32 vectors: one CTA per row
+    ("fused_add_rms_norm", "fp32", 333, 65536)])   # 16384 fp32 vectors
+def test_wide_rows_past_l2_through_the_heuristic(cuda_device, op, dtype, rows, hidden):
+    """Many rows wider than 4096-8192 vectors whose tensors exceed L2, through the default entry
+    points (the split kernels the heuristic picks there), ragged row counts: sampled rows against
+    the oracle, and the fused residual on every row against torch's rounded sum."""
+    from row_wise_rmsnorm_ks_gb300 import _abi as A
+    dt = synth.dtype_of(dtype)
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    code = {torch.bfloat16: A.KS_DTYPE_BF16, torch.float16: A.KS_DTYPE_F16,
+            torch.float32: A.KS_DTYPE_F32}[dt]
+    p = A.ks_plan_launch(0 if op == "rms_norm" else 1, rows, hidden, code, True, sms, 1)[1]
+    assert p.kernel == A.KS_KERNEL_TWOPASS_ROW
+    x = synth.cast(synth.student_t3_dev((rows, hidden), 97, cuda_device), dt)
+    wt = synth.weight(hidden, dt).to(cuda_device)
+    idx = sample_rows(rows, k=12)
+    name = f"wide past L2 {op} {dtype} [{rows},{hidden}] cluster {p.cluster} stages {p.stages}"
+    if op == "rms_norm":
+        y = ks.rms_norm(x, wt, 1e-6)
+        ref, _ = oracle.rms_norm(x[idx].cpu(), wt.cpu(), 1e-6)
+        compare_output(y[idx].cpu(), ref, dt, hidden, name)
+    else:
+        r = synth.cast(synth.normal_dev((rows, hidden), 98, cuda_device, std=2.0), dt)
+        x_in, r_in = x.clone(), r.clone()
+        ks.fused_add_rms_norm(x, r, wt, 1e-6)
+        assert bits_equal(r, (x_in.float() + r_in.float()).to(dt)), name
+        ref_x, ref_r, _ = oracle.fused_add_rms_norm(x_in[idx].cpu(), r_in[idx].cpu(), wt.cpu(), 1e-6)
+        assert bits_equal(r[idx].cpu(), ref_r), name
+        compare_output(x[idx].cpu(), ref_x, dt, hidden, name)
     st, flags = A.ks_device_faults(clear=True)
     assert st == A.KS_SUCCESS and flags == 0
 
