@@ -1266,7 +1266,7 @@ def run_plan_contexts(args) -> int:
     sms = device_facts(dev)["sm_count"]
     codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
     keep = ("w4", "w4n", "w6", "w6n", "w8", "w8n", "p2", "n2", "p4", "n4", "t256u4", "t512u2",
-            "b2")
+            "t256u4n", "t512u2n", "b2")
 
     def steady(fn, n=30):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -1599,6 +1599,127 @@ def bands_cpp(name: str, bands) -> str:
     return f"constexpr Band {name}[] = {{" + ", ".join(one(b) for b in bands) + "};"
 
 
+# The launch codes of the library's band table for many rows of 97..2048 16-byte vectors: W / w a
+# warp per row with / without prefetch (4 vectors per lane up to 128 vectors, 6 up to 192, 8 up to
+# 256), T / t a CTA per row at 2 vectors per thread with / without prefetch, F / f the same at 4,
+# R the staged ring of 2 stages, P the two-pass kernel in its default shape (no L2 prefetch).
+PLAN_BAND_CODES = "WwTtFfRP"
+PLAN_BAND_LO, PLAN_BAND_HI = 97, 2048
+
+
+def plan_band_candidate(code: str, op: str, dtype: str, hv: int):
+    """The plan-contexts candidate a band code launches at width hv (None where it does not
+    apply: warp rows past 256 vectors)."""
+    if code in "Ww":
+        if hv > 256:
+            return None
+        return f"w{4 if hv <= 128 else (6 if hv <= 192 else 8)}" + ("" if code == "W" else "n")
+    if code == "P":
+        return "t512u2n" if (op == "fused_add_rms_norm" and dtype != "fp32") else "t256u4n"
+    return {"T": "p2", "t": "n2", "F": "p4", "f": "n4", "R": "b2"}[code]
+
+
+def plan_bands_record(jsonl_paths, sm_count: int) -> dict:
+    """The measured record behind the band table, from one or more --plan-contexts runs: per dtype
+    and op, the widths, the row counts, and for every band code its score at each width (the worse
+    of its two contexts, as thousandths of the measured copy peak; the mean over runs that
+    measured the width)."""
+    acc = {}
+    for path in jsonl_paths:
+        for ln in open(path):
+            if not ln.startswith('{"plan_contexts"'):
+                continue
+            d = json.loads(ln)
+            if "steady" not in d or not (PLAN_BAND_LO <= d["hv"] <= PLAN_BAND_HI):
+                continue
+            sc = {k: min(d["steady"][k], d.get("after_ring", d["steady"]).get(k, 0.0))
+                  for k in d["steady"]}
+            key = f"{d['plan_contexts']}/{d['op']}"
+            slot = acc.setdefault(key, {}).setdefault(d["hv"], {"rows": d["rows"], "runs": []})
+            slot["runs"].append({c: sc.get(plan_band_candidate(c, d["op"], d["plan_contexts"],
+                                                               d["hv"])) for c in PLAN_BAND_CODES})
+    tables = {}
+    for key, by_w in sorted(acc.items()):
+        hvs = sorted(by_w)
+        t = {"hv": hvs, "rows": [by_w[h]["rows"] for h in hvs]}
+        for c in PLAN_BAND_CODES:
+            col = []
+            for h in hvs:
+                vals = [r[c] for r in by_w[h]["runs"] if r[c] is not None]
+                col.append(round(1000 * sum(vals) / len(vals)) if vals else None)
+            t[c] = col
+        tables[key] = t
+    return {"what": "RMSNorm launch-plan scores for many rows of 97..2048 16-byte vectors",
+            "score": "worse of steady state and after a large-shared-memory kernel, thousandths "
+                     "of the measured copy peak, mean over runs",
+            "sm_count": sm_count, "runs": len(jsonl_paths), "tables": tables}
+
+
+def derive_plan_bands(record: dict, tol: int = 10) -> dict:
+    """The band table a record implies, by one rule: the fewest bands over the measured widths
+    such that at every width the band's code scores within `tol` thousandths (a point of the copy
+    peak) of that width's best code. Built left to right, each band as wide as the codes common
+    to its widths allow (which gives the fewest bands), and among those codes the one with the
+    best mean score. A band reaches to its last measured width (the last band to 2048 vectors);
+    widths between two measured ones take the next band. The staged ring and the two-pass kernel
+    need at least 4 rows per SM, so their bands also name a fallback: the one-pass code with the
+    best mean score over the band's widths. Returns {"dtype/op": [(hi, code, fallback)]}."""
+    out = {}
+    for key, t in record["tables"].items():
+        hvs = t["hv"]
+        ok = []
+        for i in range(len(hvs)):
+            sc = {c: t[c][i] for c in PLAN_BAND_CODES if t[c][i] is not None}
+            best = max(sc.values())
+            ok.append({c for c, v in sc.items() if v >= best - tol})
+        bands, i = [], 0
+        while i < len(hvs):
+            common, j = set(ok[i]), i
+            while j + 1 < len(hvs) and common & ok[j + 1]:
+                common &= ok[j + 1]
+                j += 1
+            mean = lambda c, lo=i, hi=j: sum(t[c][k] for k in range(lo, hi + 1)) / (hi - lo + 1)
+            code = max(sorted(common), key=mean)
+            fb = code
+            if code in "RP":
+                one = [c for c in "WwTtFf" if all(t[c][k] is not None for k in range(i, j + 1))]
+                fb = max(one, key=mean)
+            bands.append((hvs[j], code, fb))
+            i = j + 1
+        bands[-1] = (PLAN_BAND_HI, bands[-1][1], bands[-1][2])
+        out[key] = bands
+    return out
+
+
+PLAN_BAND_TABLES = (("fp32", "kRowBandsF32"), ("fp16", "kRowBandsF16"), ("bf16", "kRowBandsBf16"))
+
+
+def plan_bands_cpp(bands: dict) -> str:
+    """The band table as the library's C++ source (one array per dtype and op)."""
+    lines = []
+    for dt, name in PLAN_BAND_TABLES:
+        for op, suffix in (("rms_norm", "Plain"), ("fused_add_rms_norm", "Fused")):
+            body = ", ".join(f"{{{hi}, '{c}', '{fb}'}}" for hi, c, fb in bands[f"{dt}/{op}"])
+            lines.append(f"constexpr RowBand {name}{suffix}[] = {{{body}}};")
+    return "\n".join(lines)
+
+
+def plan_bands_table(record: dict) -> str:
+    """A markdown table of a record: per dtype, op and width, the derived band's code and score
+    against the best code's."""
+    bands = derive_plan_bands(record)
+    rows = []
+    for key, t in record["tables"].items():
+        for i, hv in enumerate(t["hv"]):
+            code = next(c for hi, c, _ in bands[key] if hv <= hi)
+            sc = {c: t[c][i] for c in PLAN_BAND_CODES if t[c][i] is not None}
+            best = max(sc, key=sc.get)
+            rows.append(f"| {key} | {hv} | {code} | {sc[code] / 1000:.3f} | {best} | "
+                        f"{sc[best] / 1000:.3f} |")
+    return ("| dtype/op | vectors | band code | score | best code | best score |\n"
+            "|---|---|---|---|---|---|\n" + "\n".join(rows))
+
+
 def run_ops_scan(args) -> int:
     """The next operators' default launches over row widths (one JSON line per dtype and width;
     not the contract's line): Softmax, LayerNorm (weight and bias) and SwiGLU on rows of
@@ -1712,6 +1833,15 @@ def main() -> int:
                     help="print the markdown table of an --ops-bands run")
     ap.add_argument("--ops-bands-derive", metavar="JSONL",
                     help="print the Softmax and LayerNorm band tables an --ops-bands run implies")
+    ap.add_argument("--plan-bands-record", nargs="+", metavar="JSONL",
+                    help="print the JSON record of one or more --plan-contexts runs (the data the "
+                         "RMSNorm band table is derived from)")
+    ap.add_argument("--plan-bands-derive", metavar="JSON",
+                    help="print the RMSNorm band table a --plan-bands-record record implies")
+    ap.add_argument("--plan-bands-table", metavar="JSON",
+                    help="print the markdown table of a --plan-bands-record record")
+    ap.add_argument("--record-sm-count", type=int, default=0,
+                    help="the SM count of the box the runs were taken on (default: this GPU's)")
     ap.add_argument("--kernel-times", action="store_true",
                     help="every stated configuration a fixed number of times, for an ncu launch list")
     ap.add_argument("--kernel-time-launches", type=int, default=5)
@@ -1758,6 +1888,19 @@ def main() -> int:
         return 0
     if args.kernel_times_table:
         print(kernel_times_table(*args.kernel_times_table))
+        return 0
+    if args.plan_bands_record:
+        sms = args.record_sm_count
+        if sms <= 0:
+            import torch
+            sms = device_facts(torch.device("cuda", 0))["sm_count"]
+        print(json.dumps(plan_bands_record(args.plan_bands_record, sms), separators=(",", ":")))
+        return 0
+    if args.plan_bands_derive:
+        print(plan_bands_cpp(derive_plan_bands(json.load(open(args.plan_bands_derive)))))
+        return 0
+    if args.plan_bands_table:
+        print(plan_bands_table(json.load(open(args.plan_bands_table))))
         return 0
     if args.plan_sweep:
         return run_plan_sweep(args)

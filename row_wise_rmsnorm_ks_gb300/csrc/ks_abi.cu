@@ -370,63 +370,92 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 
 
 // Host heuristic (after the pages' rule of sizing the launch from the row width: Triton
-// Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"), set from sweeps of
-// every variant on GB300 at HBM-bound row counts (384 MiB per tensor), each plan timed in steady
-// state and right after a kernel with a large shared-memory carveout, the worse of the two kept:
-// rows of 129..384 16-byte vectors in steps of 8 (two runs averaged), 416..2048 in steps of 32.
-//  * rows of at most 128 vectors (bf16/fp16 H <= 1024, fp32 H <= 512): one warp per row, 1/2/4
-//    vectors per lane, next row prefetched, up to 8 rows per CTA but never fewer CTAs than SMs
+// Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"):
+//  * rows of at most 96 vectors (bf16/fp16 H <= 768, fp32 H <= 384), and of at most 128 when
+//    there are no more rows than SMs: one warp per row, 1/2/4 vectors per lane (the fewest that
+//    cover the row), next row prefetched, up to 8 rows per CTA but never fewer CTAs than SMs
 //    when the rows allow it;
-//  * many rows of 129..384 vectors: the plan of kNarrowPlans for the row's 8-vector bucket
-//    (a warp per row at 6 or 8 vectors per lane for most plain rows up to 256 vectors, where a
-//    CTA row of 33..64 threads pays a barrier per row for 4 vectors a thread; CTA rows otherwise);
-//  * rows of up to 2048 vectors (bf16/fp16 H <= 16384, fp32 H <= 8192): one CTA per row, as wide
-//    as the row needs (a multiple of 32 threads). Which variant sustains the most bandwidth
-//    depends on the width, and the sweep picks:
-//      plain: 4 vectors per thread, no prefetch, except at the widths where that plan dips and
-//        the prefetching one does not (bf16 512, 640 and 1184..1280 vectors: 4 vectors with
-//        prefetch; fp32 512 and 640: 2 vectors with prefetch); 16-bit rows wider than 1536
-//        vectors and fp32 rows of 1537..1696 take the two-pass kernel;
-//      fused: no prefetch, 2 vectors per thread for rows of at most 768 vectors and for 961..1152
-//        vectors, 4 vectors per thread for 769..960 and 1153..1536, and for 16-bit rows of
-//        545..672. Wider rows: bf16 prefetches at 4 vectors per thread (from 1473) and takes the
-//        two-pass kernel from 1985; fp16 takes the staged ring (2 stages) up to 1696 vectors when
-//        there are enough rows, the two-pass kernel beyond; fp32 takes the two-pass kernel at
-//        769..928 and from 1409, and 2 vectors per thread at 929..960. The two-pass switches that
-//        came from the dense sweep (bf16 fused from 1985, fp32 fused at 769..928 and 1409..1536,
-//        fp32 plain at 1537..1696) need at least 4 rows per SM, as the sweep had: with fewer rows,
-//        e.g. 333 bf16 fused rows of 2048 vectors, the one-pass plan measured faster (7.5 against
-//        7.9 us a launch under graph replay), so those take the previous rules.
-//    In the latency regime (rows <= SMs, so each CTA gets at most one row) prefetch has nothing
-//    to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows) go to a cluster of 8
-//    CTAs per row, plain rows of at most 1024 vectors take 2 vectors per thread, and the rest 4
-//    (a graph-replay sweep of 1..333 rows found no gain in warp rows there);
+//  * many rows (more than SMs) of 97..2048 vectors (bf16/fp16 H <= 16384, fp32 H <= 8192): the
+//    band table below, one per dtype and op, generated from a plan-contexts sweep (warp rows,
+//    CTA rows at 2 or 4 vectors per thread with and without prefetch, the staged ring and the
+//    two-pass kernel, each timed in two contexts); the ring and the two-pass kernel only with at
+//    least 4 rows per SM, the band's one-pass fallback otherwise;
+//  * latency regime (rows <= SMs, so each CTA gets at most one row) of 129..2048 vectors:
+//    prefetch has nothing to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows)
+//    go to a cluster of 8 CTAs per row, plain rows of at most 1024 vectors take 2 vectors per
+//    thread, and the rest 4 (a graph-replay sweep of 1..333 rows found no gain in warp rows
+//    there);
 //  * rows wider than 2048 vectors (bf16/fp16 H > 16384, fp32 H > 8192): the two-pass kernel,
 //    one CTA per row reading it twice (the second time from L2), any width; few rows (at most
-//    SMs/8) of up to 16384 vectors split over a cluster of 8 CTAs instead;
+//    SMs/8) of up to 16384 vectors split over a cluster of 8 CTAs instead, and rows that outgrow
+//    L2 together over a cluster of 2..8 CTAs (split_row);
 //  * anything else (H not a multiple of the vector, unaligned pointers): the scalar two-pass
 //    kernel.
 // The grid is persistent: at most sm_count * blocks_per_sm CTAs (for cluster plans, whole
 // clusters, which the launch caps again by the device's count of resident clusters; for the
-// two-pass kernel, no more CTAs than keep their rows in flight within 96 MiB of L2, but at
-// least one per SM).
+// two-pass kernel, no more CTAs than keep their rows in flight within 3/4 of the device's L2,
+// but at least one per SM).
 namespace {
 
-// Many rows of 129..384 vectors: one plan per 8-vector bucket (bucket b holds rows of
-// 129 + 8b .. 136 + 8b vectors), measured at the bucket's widest row. A plan switched away from
-// the general rules only where another won by at least a point of the copy peak in both
-// contexts (steady, and after a large-carveout kernel). Codes: W / w a warp per row with (W) or
-// without (w) prefetch, 6 vectors per lane up to 192 vectors and 8 up to 256, 4 rows per
-// 128-thread CTA; T / t a CTA per row at 2 vectors per thread with / without prefetch; F / f the
-// same at 4 vectors. Indexed [dtype code][op].
-constexpr int kNarrowLo = 129, kNarrowHi = 384, kNarrowStep = 8;
-const char *const kNarrowPlans[3][2] = {
-    // fp32: plain, fused
-    {"wwwffffWfWWWWWWTfffffffffffffffT", "tttTTTTTtTTTTTTWtttTTTTTtttTTTTT"},
-    // fp16
-    {"wwwwwwwffffffffWffffffffffffffff", "wttttfffttttttTTtttttttttttttttt"},
-    // bf16
-    {"wWWWWWWfwffffWWWffffffffffffffff", "tttttFFFFttttttttttttttFtttttttt"},
+// Many rows of 97..2048 vectors: one band table per dtype and op. A band covers the widths up to
+// its `hi` (from the previous band's hi + 1) and names a launch:
+//   W / w  a warp per row with / without prefetch: 4 vectors per lane up to 128 vectors (up to 8
+//          rows per 256-thread CTA), 6 up to 192 and 8 up to 256 (4 rows per 128-thread CTA);
+//   T / t  a CTA per row at 2 vectors per thread, with / without prefetch;
+//   F / f  the same at 4 vectors per thread;
+//   R      the staged ring, 2 stages;
+//   P      the two-pass kernel in its default shape;
+// and a fallback for fewer than 4 rows per SM, where the ring and the two-pass kernel have too
+// few rows to keep busy (the fallback is the code itself for the one-pass launches).
+// The tables are generated, not edited: a plan-contexts sweep on GB300 times every launch at each
+// measured width in two contexts (steady state, and right after a kernel with a large
+// shared-memory carveout), a plan's score is the worse of the two, and the tables are the fewest
+// bands such that at every measured width the band's launch scores within a point of the copy
+// peak of the best launch there (bench.py --plan-bands-record / --plan-bands-derive; the
+// measured record is committed beside the kernel profiles, and a CPU test re-derives the tables
+// from it and checks every default plan against it).
+struct RowBand {
+    int32_t hi;     // the band's widest row, in 16-byte vectors
+    char code;      // the launch
+    char fallback;  // the launch with fewer than 4 rows per SM
+};
+constexpr int64_t kBandLo = 97, kBandHi = 2048;
+// BEGIN GENERATED ROW BANDS
+constexpr RowBand kRowBandsF32Plain[] = {{108, 'f', 'f'}, {124, 'W', 'W'}, {128, 'F', 'F'}, {152, 'w', 'w'}, {200, 'f', 'f'}, {248, 'W', 'W'}, {256, 'T', 'T'}, {480, 'f', 'f'}, {512, 'T', 'T'}, {608, 'f', 'f'}, {640, 'T', 'T'}, {992, 'f', 'f'}, {1344, 'P', 'f'}, {1536, 'f', 'f'}, {1888, 'P', 'f'}, {2048, 'f', 'f'}};
+constexpr RowBand kRowBandsF32Fused[] = {{116, 'W', 'W'}, {128, 'F', 'F'}, {152, 't', 't'}, {192, 'T', 'T'}, {208, 't', 't'}, {248, 'T', 'T'}, {256, 'W', 'W'}, {296, 't', 't'}, {320, 'T', 'T'}, {360, 't', 't'}, {384, 'T', 'T'}, {416, 't', 't'}, {512, 'F', 'F'}, {768, 't', 't'}, {960, 'P', 't'}, {1152, 't', 't'}, {1600, 'f', 'f'}, {2048, 'P', 'f'}};
+constexpr RowBand kRowBandsF16Plain[] = {{112, 'w', 'w'}, {124, 'f', 'f'}, {128, 'W', 'W'}, {188, 'w', 'w'}, {192, 'f', 'f'}, {200, 'w', 'w'}, {248, 'f', 'f'}, {256, 'W', 'W'}, {1536, 'f', 'f'}, {2048, 'P', 'f'}};
+constexpr RowBand kRowBandsF16Fused[] = {{112, 't', 't'}, {128, 'W', 'W'}, {136, 'w', 'w'}, {176, 't', 't'}, {196, 'f', 'f'}, {248, 't', 't'}, {256, 'T', 'T'}, {576, 't', 't'}, {672, 'f', 'f'}, {768, 't', 't'}, {992, 'f', 'f'}, {1152, 't', 't'}, {1536, 'f', 'f'}, {1824, 'R', 't'}, {2048, 'P', 't'}};
+constexpr RowBand kRowBandsBf16Plain[] = {{108, 'w', 'w'}, {124, 'W', 'W'}, {128, 'T', 'T'}, {144, 'w', 'w'}, {192, 'W', 'W'}, {208, 'w', 'w'}, {240, 'f', 'f'}, {256, 'W', 'W'}, {480, 'f', 'f'}, {512, 'F', 'F'}, {576, 'f', 'f'}, {640, 'F', 'F'}, {736, 'f', 'f'}, {768, 'F', 'F'}, {1152, 'f', 'f'}, {1280, 'F', 'F'}, {1536, 'f', 'f'}, {2048, 'P', 'f'}};
+constexpr RowBand kRowBandsBf16Fused[] = {{128, 't', 't'}, {136, 'w', 'w'}, {168, 't', 't'}, {200, 'F', 'F'}, {312, 't', 't'}, {320, 'F', 'F'}, {576, 't', 't'}, {672, 'f', 'f'}, {864, 'F', 'F'}, {992, 'f', 'f'}, {1152, 't', 't'}, {1472, 'f', 'f'}, {2048, 'F', 'F'}};
+// END GENERATED ROW BANDS
+
+// Whether a table is well formed: widths rising to kBandHi, warp launches only where a warp
+// covers the row, fallbacks one-pass launches, every code known.
+template <size_t N>
+constexpr bool bands_ok(const RowBand (&b)[N]) {
+    for (size_t i = 0; i < N; ++i) {
+        if (b[i].hi < kBandLo || b[i].hi > kBandHi || (i > 0 && b[i].hi <= b[i - 1].hi)) return false;
+        const char c = b[i].code, f = b[i].fallback;
+        bool known = false, one_pass = false;
+        for (const char k : {'W', 'w', 'T', 't', 'F', 'f'}) {
+            known = known || c == k;
+            one_pass = one_pass || f == k;
+        }
+        if (!(known || c == 'R' || c == 'P') || !one_pass) return false;
+        if (known && f != c) return false;
+        if ((c == 'W' || c == 'w' || f == 'W' || f == 'w') && b[i].hi > 256) return false;
+    }
+    return b[N - 1].hi == kBandHi;
+}
+static_assert(bands_ok(kRowBandsF32Plain) && bands_ok(kRowBandsF32Fused) &&
+                  bands_ok(kRowBandsF16Plain) && bands_ok(kRowBandsF16Fused) &&
+                  bands_ok(kRowBandsBf16Plain) && bands_ok(kRowBandsBf16Fused),
+              "a row band table is malformed");
+// Indexed [dtype code][op].
+const RowBand *const kRowBands[3][2] = {
+    {kRowBandsF32Plain, kRowBandsF32Fused},
+    {kRowBandsF16Plain, kRowBandsF16Fused},
+    {kRowBandsBf16Plain, kRowBandsBf16Fused},
 };
 
 void cta_row(ks_plan_t *p, int64_t hv, int v, bool prefetch) {
@@ -435,21 +464,6 @@ void cta_row(ks_plan_t *p, int64_t hv, int v, bool prefetch) {
     p->block = (int32_t)round_up(ceil_div(hv, v), 32);
     p->team = p->block;
     p->flags = prefetch ? 0 : KS_PLAN_NO_PREFETCH;
-}
-
-// The kNarrowPlans plan for a row of hv (129..384) vectors; returns the rows each CTA handles.
-int64_t narrow_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
-    const char c = kNarrowPlans[(int)dtype][fused ? 1 : 0][(hv - kNarrowLo) / kNarrowStep];
-    if (c == 'W' || c == 'w') {
-        p->kernel = KS_KERNEL_WARP_ROW;
-        p->vec_per_thread = hv <= 192 ? 6 : 8;
-        p->team = 32;
-        p->block = 128;
-        p->flags = c == 'W' ? 0 : KS_PLAN_NO_PREFETCH;
-        return 4;
-    }
-    cta_row(p, hv, (c == 'T' || c == 't') ? 2 : 4, c == 'T' || c == 'F');
-    return 1;
 }
 
 void bulk_row(ks_plan_t *p, int64_t hv, bool fused, int64_t stages) {
@@ -480,6 +494,47 @@ void twopass_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
         p->block = hv <= 4096 ? 512 : 1024;
     }
     p->team = p->block;
+}
+
+// The band plan for many rows (more than SMs) of 97..2048 vectors; returns the rows each CTA
+// handles.
+int64_t band_row(ks_plan_t *p, int64_t hv, int64_t rows, int sm_count, bool fused,
+                 ks_dtype_t dtype) {
+    const RowBand *b = kRowBands[(int)dtype][fused ? 1 : 0];
+    while (hv > b->hi) ++b;
+    const char c = rows >= 4 * (int64_t)sm_count ? b->code : b->fallback;
+    switch (c) {
+    case 'W':
+    case 'w': {
+        p->kernel = KS_KERNEL_WARP_ROW;
+        p->team = 32;
+        p->flags = c == 'W' ? 0 : KS_PLAN_NO_PREFETCH;
+        if (hv <= 128) {
+            p->vec_per_thread = 4;
+            int64_t teams = ceil_div(rows, sm_count);
+            teams = teams < 1 ? 1 : (teams > 8 ? 8 : teams);
+            p->block = (int32_t)(32 * teams);
+            return teams;
+        }
+        p->vec_per_thread = hv <= 192 ? 6 : 8;
+        p->block = 128;
+        return 4;
+    }
+    case 'T':
+    case 't':
+        cta_row(p, hv, 2, c == 'T');
+        return 1;
+    case 'F':
+    case 'f':
+        cta_row(p, hv, 4, c == 'F');
+        return 1;
+    case 'R':
+        bulk_row(p, hv, fused, 2);
+        return 1;
+    default:
+        twopass_row(p, hv, fused, dtype);
+        return 1;
+    }
 }
 
 // Many wide rows: the two-pass kernel split over a cluster. Measured on GB300 (plan sweep, 384 MiB
@@ -522,14 +577,9 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
     const int per_vec = 16 / elem;
     const bool vec_ok = aligned16 && hidden % per_vec == 0;
     const int64_t hv = vec_ok ? hidden / per_vec : 0;
-    const bool ring_rows = rows >= 4 * (int64_t)sm_count;  // enough rows to keep a ring busy
-    const bool bf16 = dtype == KS_DTYPE_BF16, f16 = dtype == KS_DTYPE_F16;
-    // Many rows of 97..128 vectors: a CTA per row with prefetch beat a warp per row for bf16 plain
-    // (2 vectors per thread: 0.96 of the copy peak against 0.92) and fp16 fused (4 vectors: 0.97-0.99
-    // against 0.95-0.98), whatever kernel ran before.
-    const bool cta_narrow = rows > sm_count && hv > 96 && ((bf16 && !fused) || (f16 && fused));
     int64_t rows_per_cta = 1;
-    if (vec_ok && hv <= 128 && !cta_narrow) {
+    if (vec_ok && (hv < kBandLo || (hv <= 128 && rows <= sm_count))) {
+        // Narrow rows: a warp per row, the fewest vectors per lane that cover it.
         p->kernel = KS_KERNEL_WARP_ROW;
         p->vec_per_thread = hv <= 32 ? 1 : (hv <= 64 ? 2 : 4);
         p->team = 32;
@@ -551,35 +601,8 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
             cta_row(p, hv, 4, fused);
         }
     } else if (vec_ok && hv <= 2048) {
-        // Many rows.
-        const bool f32 = dtype == KS_DTYPE_F32;
-        if (hv <= 128) {  // cta_narrow
-            cta_row(p, hv, fused ? 4 : 2, true);
-        } else if (hv <= kNarrowHi) {
-            rows_per_cta = narrow_row(p, hv, fused, dtype);
-        } else if (!fused) {
-            if (f32 && (hv == 512 || hv == 640))
-                cta_row(p, hv, 2, true);
-            else if ((hv > 1536 && !f32) || (f32 && ring_rows && hv > 1536 && hv <= 1696))
-                twopass_row(p, hv, false, dtype);
-            else
-                cta_row(p, hv, 4, bf16 && (hv == 512 || hv == 640 || (hv >= 1184 && hv <= 1280)));
-        } else if (f32 && ring_rows && ((hv > 768 && hv <= 928) || hv > 1408)) {
-            twopass_row(p, hv, true, dtype);
-        } else if (f32 && hv > 928 && hv <= 960) {
-            cta_row(p, hv, 2, false);
-        } else if (!f32 && hv > 544 && hv <= 672) {
-            cta_row(p, hv, 4, false);
-        } else if (hv <= 1472 || (!bf16 && hv <= 1536)) {
-            const bool two = hv <= 768 || (hv > 960 && hv <= 1152);
-            cta_row(p, hv, two ? 2 : 4, false);
-        } else if (bf16 && (hv <= 1984 || !ring_rows)) {
-            cta_row(p, hv, 4, true);
-        } else if (f16 && hv <= 1696 && ring_rows) {
-            bulk_row(p, hv, true, 2);
-        } else {
-            twopass_row(p, hv, true, dtype);
-        }
+        // Many rows: the measured band table.
+        rows_per_cta = band_row(p, hv, rows, sm_count, fused, dtype);
     } else if (vec_ok && hv > 2048 && rows * 8 <= sm_count && hv <= 16384) {
         // Few rows wider than one CTA's registers: each row split over a cluster of 8 CTAs (the
         // register-resident cluster kernel), so the row's bytes come in over 8 SMs.

@@ -118,123 +118,18 @@ def plan(op, rows, hidden, dtype=BF16, aligned=True, sms=152, bps=0):
     return p
 
 
-@pytest.mark.parametrize("op,hidden,dtype,v", [(0, 256, BF16, 1), (0, 512, BF16, 2), (0, 1024, F16, 4),
-                                               (1, 1024, BF16, 4), (0, 512, F32, 4)])
+@pytest.mark.parametrize("op,hidden,dtype,v", [(0, 256, BF16, 1), (0, 512, BF16, 2), (0, 768, F16, 4),
+                                               (1, 768, BF16, 4), (0, 384, F32, 4)])
 def test_narrow_rows_take_warp_per_row(op, hidden, dtype, v):
     p = plan(op, 32768, hidden, dtype)
     assert p.kernel == _abi.KS_KERNEL_WARP_ROW and p.vec_per_thread == v and p.team == 32
     assert p.block == 256  # 8 rows per CTA once there are enough rows
 
 
-# The measured exceptions for 16-bit rows with many rows (op, hidden, dtype) -> (vectors per thread,
-# prefetch), and the neighbouring widths that keep the general rule.
 NO_PF = _abi.KS_PLAN_NO_PREFETCH
 CTA, BULK, TWO = _abi.KS_KERNEL_CTA_ROW, _abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_TWOPASS_ROW
-EXCEPTIONS = [
-    ((0, 1024, BF16), (2, True)),     # 128 vectors: CTA at 2 vectors, not a warp
-    ((1, 1024, F16), (4, True)),
-    ((0, 2304, BF16), (4, False)),    # 288 vectors (H = 2304): no prefetch (it lost 10 points)
-    ((0, 3072, BF16), (4, False)),    # 384: general rule
-    ((0, 4096, BF16), (4, True)),     # 512
-    ((0, 5120, BF16), (4, True)),     # 640
-    ((0, 6144, BF16), (4, False)),    # 768: general rule
-    ((0, 8192, BF16), (4, False)),    # 1024: general rule (the headline shape)
-    ((0, 10240, BF16), (4, True)),    # 1280
-    ((0, 10496, BF16), (4, False)),   # 1312: no prefetch (it lost 19 points)
-    ((0, 4352, BF16), (4, False)),    # 544: no prefetch
-    ((0, 4096, F16), (4, False)),     # fp16 plain keeps the general rule
-    ((1, 1536, BF16), (4, True)),     # 192
-    ((1, 1536, F16), (4, False)),
-    ((1, 2048, F16), (2, True)),      # 256
-    ((1, 2048, BF16), (2, False)),    # general rule
-    ((1, 12288, BF16), (4, True)),    # 1536
-    ((1, 8192, BF16), (2, False)),    # general rule (the headline shape)
-    ((1, 5120, BF16), (4, False)),    # 640 vectors, fused: 4 without prefetch
-    ((1, 5120, F16), (4, False)),
-    ((1, 4096, F16), (2, False)),     # 512: general rule
-    ((1, 4864, BF16), (4, False)),    # 608 vectors, fused: 4 without prefetch
-    ((1, 2304, F16), (2, False)),     # 288 vectors, fp16 fused: no prefetch (+8 points)
-]
-
-
-@pytest.mark.parametrize("args,want", EXCEPTIONS)
-def test_measured_16bit_plan_exceptions(args, want):
-    op, hidden, dtype = args
-    p = plan(op, 32768, hidden, dtype)
-    assert p.kernel == _abi.KS_KERNEL_CTA_ROW
-    assert (p.vec_per_thread, not (p.flags & NO_PF)) == want
-
-
-def test_bf16_fused_prefetch_starts_at_1473_vectors():
-    p = plan(1, 32768, 11776, BF16)  # 1472 vectors: the general rule (4 vectors, no prefetch)
-    assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags & NO_PF
-    for hidden in (11784, 12288, 15872):  # 1473, 1536, 1984 vectors: prefetch at 4 vectors
-        p = plan(1, 32768, hidden, BF16)
-        assert p.kernel == CTA and p.vec_per_thread == 4 and not (p.flags & NO_PF)
-    for hidden in (15880, 16384):  # 1985, 2048 vectors: the two-pass kernel
-        p = plan(1, 32768, hidden, BF16)
-        assert (p.kernel, p.vec_per_thread, p.block) == (TWO, 2, 512)
-        p = plan(1, 333, hidden, BF16)  # fewer than 4 rows per SM: the one-pass plan stays
-        assert p.kernel == CTA and p.vec_per_thread == 4 and not (p.flags & NO_PF)
-
-
-def test_fp32_two_pass_switches_need_many_rows():
-    for hidden, rows, want in ((3200, 32768, TWO), (3200, 333, CTA),     # fused, 800 vectors
-                               (6000, 32768, TWO), (6000, 333, CTA)):    # fused, 1500 vectors
-        assert plan(1, rows, hidden, F32).kernel == want, (hidden, rows)
-    assert plan(0, 32768, 6400, F32).kernel == TWO   # plain, 1600 vectors
-    assert plan(0, 333, 6400, F32).kernel == CTA
-
-
-# Many rows of 129..384 vectors: the measured per-bucket table. (op, hidden, dtype) ->
-# (kernel, vectors per thread or lane, prefetch).
 WARP = _abi.KS_KERNEL_WARP_ROW
-NARROW = [
-    ((0, 1088, BF16), (WARP, 6, False)),   # 136 vectors
-    ((0, 1280, BF16), (WARP, 6, True)),    # 160 (H = 1280)
-    ((0, 1536, BF16), (CTA, 4, False)),    # 192 (H = 1536): the CTA row stays
-    ((0, 2048, BF16), (WARP, 8, True)),    # 256
-    ((0, 1280, F16), (WARP, 6, False)),
-    ((0, 2048, F16), (WARP, 8, True)),
-    ((0, 640, F32), (CTA, 4, False)),      # 160 fp32 vectors
-    ((0, 896, F32), (WARP, 8, True)),      # 224
-    ((0, 1024, F32), (CTA, 2, True)),      # 256
-    ((0, 1280, F32), (CTA, 4, False)),     # 320
-    ((1, 1792, BF16), (CTA, 2, False)),    # 224
-    ((1, 2560, BF16), (CTA, 4, True)),     # 320 (H = 2560)
-    ((1, 1088, F16), (WARP, 6, False)),    # 136
-    ((1, 1792, F16), (CTA, 2, False)),     # 224
-    ((1, 2048, F32), (CTA, 2, False)),     # 512 fp32 vectors: general rule (above the table)
-    ((1, 1024, F32), (WARP, 8, True)),     # 256
-    ((1, 1088, F32), (CTA, 2, False)),     # 272
-]
-
-
-@pytest.mark.parametrize("args,want", NARROW)
-def test_narrow_rows_take_the_measured_table(args, want):
-    op, hidden, dtype = args
-    p = plan(op, 32768, hidden, dtype)
-    kernel, v, pf = want
-    assert (p.kernel, p.vec_per_thread, not (p.flags & NO_PF)) == (kernel, v, pf)
-    if kernel == WARP:
-        assert p.team == 32 and p.block == 128 and p.rows_per_pass == p.grid * 4
-
-
-@pytest.mark.parametrize("dtype", [BF16, F16, F32])
-@pytest.mark.parametrize("op", [0, 1])
-def test_every_narrow_width_gets_a_plan_the_library_accepts(dtype, op):
-    # the rules of the planned entry points' check, for every width the table covers
-    per = 4 if dtype == F32 else 8
-    for hv in range(129, 385):
-        p = plan(op, 32768, hv * per, dtype, bps=4)
-        if p.kernel == WARP:
-            assert p.vec_per_thread in (6, 8) and 32 * p.vec_per_thread >= hv
-            assert p.block == 128 and p.team == 32
-        else:
-            assert p.kernel == CTA and p.vec_per_thread in (2, 4)
-            assert p.block * p.vec_per_thread >= hv and p.block % 32 == 0
-            assert p.block <= (1024 if p.vec_per_thread == 2 else 512)
-        assert p.grid == 152 * 4
+# (Many rows of 97..2048 vectors take the measured band table: tests/test_plan_bands_cpu.py.)
 
 
 def test_few_rows_keep_the_latency_rules():
@@ -247,53 +142,6 @@ def test_few_rows_keep_the_latency_rules():
 def test_warp_per_row_spreads_few_rows_over_sms():
     p = plan(0, 128, 1024)
     assert p.block == 32 and p.grid == 128  # 128 rows on 128 SMs
-
-
-# bf16 widths and the plan the sweep picks at HBM-bound row counts: (kernel, vectors/thread,
-# prefetch) for the fused op, then for the plain op.
-WIDE_BF16 = [
-    (1536, (CTA, 4, True), (CTA, 4, False)),
-    (4096, (CTA, 2, False), (CTA, 4, True)),
-    (5120, (CTA, 4, False), (CTA, 4, True)),
-    (7168, (CTA, 4, False), (CTA, 4, False)),
-    (8192, (CTA, 2, False), (CTA, 4, False)),
-    (9216, (CTA, 2, False), (CTA, 4, False)),
-    (12288, (CTA, 4, True), (CTA, 4, False)),
-    (13312, (CTA, 4, True), (TWO, 4, 256)),
-    (14336, (CTA, 4, True), (TWO, 4, 256)),
-    (16384, (TWO, 2, 512), (TWO, 4, 256)),
-]
-
-
-@pytest.mark.parametrize("hidden,fused_plan,plain_plan", WIDE_BF16)
-def test_wide_rows_take_cta_per_row(hidden, fused_plan, plain_plan):
-    for op, want in ((1, fused_plan), (0, plain_plan)):
-        p = plan(op, 32768, hidden)
-        kernel, v, third = want
-        assert (p.kernel, p.vec_per_thread) == (kernel, v), (op, hidden)
-        assert p.team == p.block and p.stages == 0
-        if kernel == TWO:  # (TWO, vectors per step, block)
-            assert p.block == third and p.flags == _abi.KS_PLAN_NO_PREFETCH
-        else:  # (CTA, vectors per thread, prefetch)
-            assert p.block == -(-hidden // (8 * v) // 32) * 32
-            assert p.vec_per_thread * 8 * p.block >= hidden
-            assert p.flags == (0 if third else _abi.KS_PLAN_NO_PREFETCH)
-    # few rows: never a staged ring
-    assert plan(0, 100, hidden).kernel in (CTA, TWO)
-    assert plan(1, 300, hidden).kernel in (CTA, TWO)
-
-
-def test_fp16_and_fp32_wide_rows():
-    p = plan(1, 32768, 13312, dtype=F16)  # 1664 vectors: the staged ring
-    assert p.kernel == BULK and p.stages == 2 and p.block == 416
-    p = plan(1, 32768, 14336, dtype=F16)  # 1792 vectors: two-pass, 2 vectors on 512 threads
-    assert (p.kernel, p.vec_per_thread, p.block) == (TWO, 2, 512)
-    p = plan(1, 32768, 7168, dtype=F16)
-    assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags == _abi.KS_PLAN_NO_PREFETCH
-    p = plan(0, 32768, 7168, dtype=F32)  # 1792 vectors of fp32, plain: registers
-    assert p.kernel == CTA and p.vec_per_thread == 4 and p.flags == _abi.KS_PLAN_NO_PREFETCH
-    p = plan(1, 32768, 7168, dtype=F32)  # fused: two-pass, 4 vectors on 256 threads
-    assert (p.kernel, p.vec_per_thread, p.block) == (TWO, 4, 256)
 
 
 def test_latency_regime_keeps_one_row_per_cta_plans():
@@ -309,10 +157,14 @@ def test_fp32_counts_four_elements_per_vector():
     # 4096 fp32 = 1024 vectors: few rows take 2 vectors per thread (512 threads)
     p = plan(0, 10, 4096, dtype=F32)
     assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 512 and p.vec_per_thread == 2
-    p = plan(1, 1000, 4096, dtype=F32)  # 1024 vectors, fused: 2 vectors per thread
-    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.block == 512 and p.vec_per_thread == 2
-    p = plan(0, 32768, 1024, dtype=F32)  # 256 vectors: 2 vectors, next row prefetched
-    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.vec_per_thread == 2 and p.flags == 0
+    # many rows of 1024 fp32 = 256 vectors: whatever launch the band table names covers exactly
+    # 256 vectors (a warp at 8 vectors per lane, or a CTA with no idle warp)
+    for op in (0, 1):
+        p = plan(op, 32768, 1024, dtype=F32)
+        if p.kernel == _abi.KS_KERNEL_WARP_ROW:
+            assert p.vec_per_thread == 8
+        else:
+            assert p.kernel == CTA and p.block * p.vec_per_thread == 256
 
 
 @pytest.mark.parametrize("hidden,aligned", [(17, True), (1001, True), (4096, False),

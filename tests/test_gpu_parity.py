@@ -111,23 +111,36 @@ def test_edge_widths(cuda_device, hidden, dtype, op):
     run_and_check(w, cuda_device)
 
 
-# Row widths (16-byte vectors) at which the launch heuristic changes plan for many rows: the
-# edges of the measured 8-vector buckets of rows of 129..384 vectors, the widths with their own
-# rule above them, and the edges of the two-pass and staged ranges.
-PLAN_EDGE_HV = [129, 136, 137, 160, 184, 185, 192, 193, 200, 224, 232, 233, 248, 256, 257, 288,
-                320, 384, 385, 512, 544, 545, 608, 640, 672, 800, 928, 929, 960, 1184, 1280,
-                1312, 1408, 1409, 1440, 1537, 1568, 1696, 1697, 1984, 1985, 2048]
+def _band_edges():
+    """(dtype, op, hv) at every width where the launch heuristic's band table for many rows
+    switches launch (a band's last width and the next one), from the committed measured record
+    the table is generated from, plus both ends of the table."""
+    import json
+    import os
+
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "profiles", "plan_bands_rms_norm.json")) as f:
+        bands = bench.derive_plan_bands(json.load(f))
+    out = []
+    for key, bl in sorted(bands.items()):
+        dt, op = key.split("/")
+        hvs = {bench.PLAN_BAND_LO, bench.PLAN_BAND_HI}
+        for hi, _, _ in bl[:-1]:
+            hvs |= {hi, hi + 1}
+        out += [(dt, op, hv) for hv in sorted(hvs)]
+    return out
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
-@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
-@pytest.mark.parametrize("hv", PLAN_EDGE_HV)
-def test_default_plans_at_heuristic_edges(cuda_device, hv, op, dtype):
-    """The default entry points on many rows (333: more rows than SMs, and ragged) at every
-    width where the launch heuristic switches plan, so each plan it can pick is checked."""
+@pytest.mark.parametrize("dtype,op,hv", _band_edges())
+@pytest.mark.parametrize("rows", [333, 701])
+def test_default_plans_at_heuristic_edges(cuda_device, hv, op, dtype, rows):
+    """The default entry points on many rows at every width where the launch heuristic switches
+    plan, so each plan it can pick is checked: 333 rows (more than SMs, fewer than 4 per SM, so
+    bands of the staged ring and the two-pass kernel take their one-pass fallback) and 701 (at
+    least 4 per SM: those bands' own launch); both ragged."""
     dt = synth.dtype_of(dtype)
     hidden = hv * (4 if dt == torch.float32 else 8)
-    rows = 333
     x = synth.cast(synth.normal_np((rows, hidden), 41), dt)
     wt = synth.weight(hidden, dt)
     r = synth.cast(synth.normal_np((rows, hidden), 42, std=2.0), dt) if op != "rms_norm" else None

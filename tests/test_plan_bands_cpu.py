@@ -1,0 +1,166 @@
+"""The RMSNorm launch heuristic's band table for many rows of 97..2048 16-byte vectors, against the
+measured record it is generated from (no GPU: the plan is host code).
+
+The record (profiles/plan_bands_rms_norm.json) holds, per dtype, op and measured width, the score
+of every launch the table can name (the worse of steady state and right after a large-shared-
+memory kernel, in thousandths of the measured copy peak). The tests check that the library's table
+is exactly what the committed rule derives from it, that the library's default plan at every
+measured width scores within 2 points of that width's best launch, and that each band code
+launches what it names.
+"""
+import json
+import os
+import re
+
+import pytest
+
+import bench
+from row_wise_rmsnorm_ks_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+RECORD = os.path.join(ROOT, "profiles", "plan_bands_rms_norm.json")
+SOURCE = os.path.join(ROOT, "row_wise_rmsnorm_ks_gb300", "csrc", "ks_abi.cu")
+DTYPES = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
+OPS = {"rms_norm": 0, "fused_add_rms_norm": 1}
+NO_PF = _abi.KS_PLAN_NO_PREFETCH
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    try:
+        return _abi.load()
+    except OSError as e:
+        pytest.skip(f"libks.so not built: {e}")
+
+
+@pytest.fixture(scope="module")
+def record():
+    with open(RECORD) as f:
+        return json.load(f)
+
+
+def plan(op, rows, hidden, dtype, sms, bps=0):
+    st, p = _abi.ks_plan_launch(op, rows, hidden, dtype, True, sms, bps)
+    assert st == _abi.KS_SUCCESS, _abi.ks_last_error()
+    return p
+
+
+def code_of(p):
+    """The band code of a library plan."""
+    if p.kernel == _abi.KS_KERNEL_WARP_ROW:
+        return "w" if p.flags & NO_PF else "W"
+    if p.kernel == _abi.KS_KERNEL_CTA_ROW:
+        c = {2: "T", 4: "F"}[p.vec_per_thread]
+        return c.lower() if p.flags & NO_PF else c
+    if p.kernel == _abi.KS_KERNEL_BULK_ROW:
+        return "R"
+    if p.kernel == _abi.KS_KERNEL_TWOPASS_ROW and p.cluster <= 1:
+        return "P"
+    raise AssertionError(f"not a band launch: {p.as_dict()}")
+
+
+def up32(n):
+    return -(-n // 32) * 32
+
+
+def hidden_of(dt, hv):
+    return hv * (4 if dt == "fp32" else 8)
+
+
+def test_record_covers_every_dtype_and_op(record):
+    assert set(record["tables"]) == {f"{d}/{o}" for d in DTYPES for o in OPS}
+    for key, t in record["tables"].items():
+        assert t["hv"] == sorted(t["hv"]) and t["hv"][0] <= 100 and t["hv"][-1] == 2048, key
+        assert min(t["rows"]) >= 4 * record["sm_count"], key  # every width measured with many rows
+        for c in bench.PLAN_BAND_CODES:
+            assert len(t[c]) == len(t["hv"]), (key, c)
+
+
+def test_library_table_is_the_derivation_of_the_record(record):
+    src = open(SOURCE).read()
+    m = re.search(r"// BEGIN GENERATED ROW BANDS\n(.*?)\n// END GENERATED ROW BANDS", src, re.S)
+    assert m, "generated block not found"
+    assert m.group(1) == bench.plan_bands_cpp(bench.derive_plan_bands(record))
+
+
+def test_default_plan_within_two_points_of_the_measured_best(record):
+    sms = record["sm_count"]
+    worst = []
+    for key, t in record["tables"].items():
+        dt, op = key.split("/")
+        for i, hv in enumerate(t["hv"]):
+            p = plan(OPS[op], t["rows"][i], hidden_of(dt, hv), DTYPES[dt], sms)
+            c = code_of(p)
+            scores = {k: t[k][i] for k in bench.PLAN_BAND_CODES if t[k][i] is not None}
+            assert t[c][i] is not None, (key, hv, c)
+            loss = max(scores.values()) - t[c][i]
+            worst.append((loss, key, hv, c, max(scores, key=scores.get)))
+            assert loss <= 20, (key, hv, c, scores)
+    # and the derivation's own tolerance holds everywhere: a point of the copy peak
+    assert max(worst)[0] <= 10, max(worst)
+
+
+def test_derivation_rule_on_a_small_record():
+    """The rule on a hand-made record: fewest bands within the tolerance, best mean among the
+    codes a band allows, the fallback of a two-pass band, the last band to 2048 vectors."""
+    n = None
+    t = {"hv": [100, 200, 300, 400], "rows": [10 ** 5] * 4,
+         #      a narrow warp row, then CTA rows, then the two-pass kernel
+         "W": [950, 900, n, n], "w": [940, 800, n, n], "T": [800, 945, 900, 850],
+         "t": [700, 940, 930, 800], "F": [600, 700, 800, 880], "f": [600, 700, 800, 870],
+         "R": [n, n, n, n], "P": [n, 500, 700, 960]}
+    bands = bench.derive_plan_bands({"tables": {"bf16/rms_norm": t}})["bf16/rms_norm"]
+    # 100: W (w within a point too); 200: T or t (within a point), not W (45 below);
+    # 300: t (T is 30 below); 400: P, falling back to F (the better one-pass code there)
+    assert bands == [(100, "W", "W"), (300, "t", "t"), (2048, "P", "F")]
+
+
+@pytest.mark.parametrize("dt", list(DTYPES))
+@pytest.mark.parametrize("op", list(OPS))
+def test_every_band_width_gets_a_plan_the_library_accepts(dt, op):
+    # what each code launches, for every width of the table, with many rows (4 CTAs per SM)
+    for hv in range(97, 2049):
+        p = plan(OPS[op], 32768, hidden_of(dt, hv), DTYPES[dt], 152, bps=4)
+        c = code_of(p)
+        if c in "Ww":
+            v = 4 if hv <= 128 else (6 if hv <= 192 else 8)
+            assert (p.vec_per_thread, p.team) == (v, 32) and 32 * v >= hv
+            assert p.block == (256 if v == 4 else 128)
+            assert p.rows_per_pass == p.grid * p.block // 32
+        elif c in "TtFf":
+            v = 2 if c in "Tt" else 4
+            assert p.vec_per_thread == v and p.block == up32(-(-hv // v))
+            assert p.block <= (1024 if v == 2 else 512) and p.team == p.block
+        elif c == "R":
+            assert p.stages == 2 and p.vec_per_thread == 4 and p.block * 4 >= hv
+        else:
+            assert p.flags == NO_PF and p.block in (256, 512)
+        assert p.grid <= 152 * 4
+
+
+def test_ring_and_two_pass_need_four_rows_per_sm(record):
+    """Bands of the staged ring or the two-pass kernel take their one-pass fallback with fewer
+    than 4 rows per SM."""
+    bands = bench.derive_plan_bands(record)
+    seen = 0
+    for key, bl in bands.items():
+        dt, op = key.split("/")
+        for hv, code, fb in bl:
+            many = plan(OPS[op], 4 * 152, hidden_of(dt, hv), DTYPES[dt], 152)
+            few = plan(OPS[op], 4 * 152 - 1, hidden_of(dt, hv), DTYPES[dt], 152)
+            assert code_of(many) == code, (key, hv)
+            assert code_of(few) == fb, (key, hv)
+            seen += code in "RP"
+    assert seen >= 1  # the record has at least one such band
+
+
+def test_latency_regime_and_narrow_rows_are_outside_the_table():
+    # at most SMs rows: the latency rules (warp rows up to 128 vectors, CTA rows beyond)
+    p = plan(0, 152, 1024, _abi.KS_DTYPE_BF16, 152)
+    assert p.kernel == _abi.KS_KERNEL_WARP_ROW and p.vec_per_thread == 4
+    p = plan(0, 152, 1032, _abi.KS_DTYPE_BF16, 152)  # 129 vectors
+    assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.vec_per_thread == 2
+    # rows of at most 96 vectors: a warp per row at any row count
+    for hv in (8, 32, 64, 96):
+        p = plan(1, 10 ** 5, hv * 8, _abi.KS_DTYPE_F16, 152)
+        assert p.kernel == _abi.KS_KERNEL_WARP_ROW and 32 * p.vec_per_thread >= hv
