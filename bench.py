@@ -27,6 +27,7 @@ import hashlib
 import io
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -64,10 +65,14 @@ def l2_note(rows: int, hidden: int, l2_bytes: int) -> str:
 FALLBACK_HBM_GBS = 6800.0
 C2C_NOMINAL_GBS = 900.0  # NVLink-C2C between Grace and the GPU, both directions together
 # what decides the recorded launches' DRAM traffic: the kernels, and the plan code that picks
-# their launch shape (a change to either invalidates the record)
+# their launch shape (a change to either invalidates the record). The generated band table is
+# left out of the hash: the record names each launch's plan instead, checked against the plan
+# the library picks now, so re-deriving bands of other widths keeps the record.
 KERNEL_SOURCES = ["row_wise_rmsnorm_ks_gb300/csrc/ks_kernels.cuh",
                   "row_wise_rmsnorm_ks_gb300/csrc/ks_ptx.cuh",
                   "row_wise_rmsnorm_ks_gb300/csrc/ks_abi.cu"]
+GENERATED_BANDS = re.compile(r"// BEGIN GENERATED ROW BANDS\n.*?// END GENERATED ROW BANDS", re.S)
+PLAN_FIELDS = ("kernel", "vec_per_thread", "team", "block", "flags", "cluster", "stages")
 TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "ncu_dram_traffic.json")
 
 
@@ -127,7 +132,7 @@ def kernel_source_sha() -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
         with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
-            h.update(code_only(f.read()).encode())
+            h.update(code_only(GENERATED_BANDS.sub("", f.read())).encode())
     return h.hexdigest()[:16]
 
 
@@ -140,10 +145,11 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback 6.8 TB/s"}
 
 
-def recorded_traffic(op: str, rows: int = FULL_ROWS, hidden: int = FULL_HIDDEN):
+def recorded_traffic(op: str, rows: int = FULL_ROWS, hidden: int = FULL_HIDDEN, plan=None):
     """Per-launch DRAM bytes (ncu dram__bytes_read.sum + dram__bytes_write.sum) from the
-    committed record, if it was taken on the current kernel and plan sources and the launch has
-    the recorded shape (else None)."""
+    committed record, if it was taken on the current kernel and plan sources, the launch has the
+    recorded shape, and `plan` (the library's plan for it now, a ks_plan_t) is the recorded one
+    (else None)."""
     if not os.path.exists(TRAFFIC_RECORD):
         return None
     with open(TRAFFIC_RECORD) as f:
@@ -152,6 +158,8 @@ def recorded_traffic(op: str, rows: int = FULL_ROWS, hidden: int = FULL_HIDDEN):
         return None
     ent = rec.get("launches", {}).get(op)
     if not ent or [rows, hidden] != ent.get("shape"):
+        return None
+    if plan is None or ent.get("plan") != {k: getattr(plan, k) for k in PLAN_FIELDS}:
         return None
     return int(ent["dram_read_bytes"]) + int(ent["dram_write_bytes"])
 
@@ -333,7 +341,8 @@ def run_ks(args) -> int:
             print(json.dumps({"error": "parity check failed; no timing published",
                               "parity": cpu["parity"]}))
             return 1
-        traffic = recorded_traffic("fused_add_rms_norm", R, H)
+        traffic = recorded_traffic("fused_add_rms_norm", R, H, _abi.ks_plan_launch(
+            1, R, H, _abi.KS_DTYPE_BF16, True, facts["sm_count"], 0)[1])
         result = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -1104,7 +1113,10 @@ def run_kernel_times(args) -> int:
 
 def plan_candidates(op: str, hv: int, elem: int):
     """Every launch plan the heuristic chooses among for a row of hv 16-byte vectors, named as in
-    the plan-sweep tables: w4/w4n (warp per row, 4 vectors per lane, with/without prefetch;
+    the plan-sweep tables: w1/w1n, w2/w2n, w4/w4n (warp per row, 1, 2 or 4 vectors per lane for
+    rows of at most 32, 64 or 128 vectors, with/without prefetch; t8vV/t8vVn and t16vV/t16vVn:
+    8- or 16-lane teams, several rows per warp, at the fewest of 1, 2 or 4 vectors per lane that
+    cover rows of at most 32 or 64 vectors;
     w6/w6n and w8/w8n: 6 or 8 vectors per lane for rows of 129..192 and 193..256 vectors),
     p2/n2/p4/n4 (CTA per row, 2 or 4 vectors per thread, with/without prefetch), b2 (staged ring,
     2 stages), tBuU (the two-pass kernel, B threads, U vectors per thread per step; rows of at
@@ -1118,10 +1130,17 @@ def plan_candidates(op: str, hv: int, elem: int):
     up32 = lambda n: -(-n // 32) * 32
     fused = op == "fused_add_rms_norm"
     out = []
-    if hv <= 128:
-        out += [("w4", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, 4, 256)),
-                ("w4n", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, 4, 256,
-                                       flags=_abi.KS_PLAN_NO_PREFETCH))]
+    for v in (1, 2, 4):  # a warp per row, 8 rows per 256-thread CTA
+        if hv <= 32 * v:
+            out += [(f"w{v}", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, v, 256)),
+                    (f"w{v}n", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, v, 256,
+                                              flags=_abi.KS_PLAN_NO_PREFETCH))]
+    for team in (8, 16):  # sub-warp teams at the fewest vectors per lane that cover the row
+        v = next((v for v in (1, 2, 4) if team * v >= hv), None)
+        if v:
+            out += [(f"t{team}v{v}", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, v, 256, team=team)),
+                    (f"t{team}v{v}n", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, v, 256, team=team,
+                                                     flags=_abi.KS_PLAN_NO_PREFETCH))]
     for v in (6, 8):  # a warp covers rows of up to 32 * v vectors; 4 rows per 128-thread CTA
         if 32 * (v - 2) < hv <= 32 * v:
             out += [(f"w{v}", _abi.make_plan(_abi.KS_KERNEL_WARP_ROW, v, 128)),
@@ -1265,7 +1284,8 @@ def run_plan_contexts(args) -> int:
     peak = measured_peaks()["hbm_gbs"]
     sms = device_facts(dev)["sm_count"]
     codes = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
-    keep = ("w4", "w4n", "w6", "w6n", "w8", "w8n", "p2", "n2", "p4", "n4", "t256u4", "t512u2",
+    keep = ("w1", "w1n", "w2", "w2n", "w4", "w4n", "w6", "w6n", "t8v1", "t8v1n", "t8v2", "t8v2n",
+            "t8v4", "t8v4n", "t16v1", "t16v1n", "t16v2", "t16v2n", "t16v4", "t16v4n", "w8", "w8n", "p2", "n2", "p4", "n4", "t256u4", "t512u2",
             "t256u4n", "t512u2n", "b2")
 
     def steady(fn, n=30):
@@ -1599,21 +1619,28 @@ def bands_cpp(name: str, bands) -> str:
     return f"constexpr Band {name}[] = {{" + ", ".join(one(b) for b in bands) + "};"
 
 
-# The launch codes of the library's band table for many rows of 97..2048 16-byte vectors: W / w a
-# warp per row with / without prefetch (4 vectors per lane up to 128 vectors, 6 up to 192, 8 up to
-# 256), T / t a CTA per row at 2 vectors per thread with / without prefetch, F / f the same at 4,
-# R the staged ring of 2 stages, P the two-pass kernel in its default shape (no L2 prefetch).
-PLAN_BAND_CODES = "WwTtFfRP"
-PLAN_BAND_LO, PLAN_BAND_HI = 97, 2048
+# The launch codes of the library's band table for many rows of 1..2048 16-byte vectors (lower
+# case: without prefetch): E / e an 8-lane team per row (rows of at most 32 vectors) and H / h a
+# 16-lane team (at most 64), at the fewest of 1, 2 or 4 vectors per lane that cover the row;
+# W / w a warp per row at the fewest of 1, 2, 4, 6 or 8 vectors per lane (at most 256 vectors);
+# T / t a CTA per row at 2 vectors per thread, F / f the same at 4; R the staged ring of 2
+# stages; P the two-pass kernel in its default shape (no L2 prefetch).
+PLAN_BAND_CODES = "EeHhWwTtFfRP"
+PLAN_BAND_ONE_PASS = "EeHhWwTtFf"
+PLAN_BAND_LO, PLAN_BAND_HI = 1, 2048
 
 
 def plan_band_candidate(code: str, op: str, dtype: str, hv: int):
     """The plan-contexts candidate a band code launches at width hv (None where it does not
-    apply: warp rows past 256 vectors)."""
+    apply: teams and warp rows that cannot cover the row)."""
+    sfx = "n" if code.islower() else ""
+    if code in "EeHh":
+        team = 8 if code in "Ee" else 16
+        v = next((v for v in (1, 2, 4) if team * v >= hv), None)
+        return f"t{team}v{v}{sfx}" if v else None
     if code in "Ww":
-        if hv > 256:
-            return None
-        return f"w{4 if hv <= 128 else (6 if hv <= 192 else 8)}" + ("" if code == "W" else "n")
+        v = next((v for v in (1, 2, 4, 6, 8) if 32 * v >= hv), None)
+        return f"w{v}{sfx}" if v else None
     if code == "P":
         return "t512u2n" if (op == "fused_add_rms_norm" and dtype != "fp32") else "t256u4n"
     return {"T": "p2", "t": "n2", "F": "p4", "f": "n4", "R": "b2"}[code]
@@ -1649,7 +1676,7 @@ def plan_bands_record(jsonl_paths, sm_count: int) -> dict:
                 col.append(round(1000 * sum(vals) / len(vals)) if vals else None)
             t[c] = col
         tables[key] = t
-    return {"what": "RMSNorm launch-plan scores for many rows of 97..2048 16-byte vectors",
+    return {"what": "RMSNorm launch-plan scores for many rows of 1..2048 16-byte vectors",
             "score": "worse of steady state and after a large-shared-memory kernel, thousandths "
                      "of the measured copy peak, mean over runs",
             "sm_count": sm_count, "runs": len(jsonl_paths), "tables": tables}
@@ -1667,6 +1694,7 @@ def derive_plan_bands(record: dict, tol: int = 10) -> dict:
     out = {}
     for key, t in record["tables"].items():
         hvs = t["hv"]
+        t = {c: t.get(c, [None] * len(hvs)) for c in PLAN_BAND_CODES}  # a code not measured
         ok = []
         for i in range(len(hvs)):
             sc = {c: t[c][i] for c in PLAN_BAND_CODES if t[c][i] is not None}
@@ -1682,7 +1710,8 @@ def derive_plan_bands(record: dict, tol: int = 10) -> dict:
             code = max(sorted(common), key=mean)
             fb = code
             if code in "RP":
-                one = [c for c in "WwTtFf" if all(t[c][k] is not None for k in range(i, j + 1))]
+                one = [c for c in PLAN_BAND_ONE_PASS
+                       if all(t[c][k] is not None for k in range(i, j + 1))]
                 fb = max(one, key=mean)
             bands.append((hvs[j], code, fb))
             i = j + 1

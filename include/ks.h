@@ -123,9 +123,12 @@ const char *ks_last_error(void);
 typedef struct ks_plan {
     int32_t kernel;         /* KS_KERNEL_* below */
     int32_t vec_per_thread; /* 16-byte vectors per thread and tensor (vector kernels): warp
-                               rows 1, 2, 4, 6 or 8; CTA rows 2 or 4; staged rows 4; cluster
-                               rows 1, 2 or 4; two-pass 2 or 4 per step */
-    int32_t team;           /* threads per row: 32 (warp per row) or block (CTA per row) */
+                               rows 1, 2, 4, 6 or 8 (teams of 8 or 16 lanes: 1, 2 or 4); CTA
+                               rows 2 or 4; staged rows 4; cluster rows 1, 2 or 4; two-pass 2
+                               or 4 per step */
+    int32_t team;           /* threads per row: for warp rows 8, 16 or 32 lanes (several rows
+                               per warp below 32; an explicit plan's 0 means 32), else block
+                               (CTA per row) or block * cluster */
     int32_t block;          /* threads per CTA */
     int64_t grid;           /* CTAs launched */
     int64_t rows_per_pass;  /* rows in flight per pass over the grid (grid * rows per CTA) */
@@ -200,7 +203,8 @@ ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t 
  * tuning hook: a plan from ks_plan_launch, edited). Semantics, arguments and errors are those of
  * ks_rms_norm / ks_fused_add_rms_norm, plus KS_ERR_INVALID_ARGUMENT when the plan does not fit
  * the call: a vector kernel on unaligned pointers or on a width that is not a multiple of 16
- * bytes, team * vec_per_thread vectors short of the row, a block that is not a multiple of 32 or
+ * bytes, team * vec_per_thread vectors short of the row, a warp-row team other than 8, 16 or 32
+ * lanes (or more than 4 vectors a lane on a team of 8 or 16), a block that is not a multiple of 32 or
  * exceeds the kernel's bound (warp rows 256, CTA rows 1024 at 2 vectors and 512 at 4, staged
  * rows 512, cluster rows 512, scalar 1024), a staged ring (stages 1..16) over 226 KB of shared
  * memory (per CTA: stages * slice * 16 bytes, twice that for the fused op), or a cluster outside

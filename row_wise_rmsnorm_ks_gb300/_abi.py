@@ -158,7 +158,7 @@ def ks_plan_launch(op: int, rows: int, hidden: int, dtype: int, aligned16: bool,
 def make_plan(kernel: int, vec_per_thread: int, block: int, stages: int = 0,
               grid: int = 0, flags: int = 0, cluster: int = 0, team: int = 0) -> ks_plan_t:
     """A plan for the *_planned entry points (derived fields are recomputed by the library;
-    `team` is read only for the next operators' warp rows: lanes per row, 8, 16 or 32)."""
+    `team` is read for warp rows: lanes per row, 8, 16 or 32, 0 meaning 32)."""
     p = ks_plan_t()
     p.kernel, p.vec_per_thread, p.block, p.stages, p.grid, p.flags, p.cluster, p.team = (
         kernel, vec_per_thread, block, stages, grid, flags, cluster, team)

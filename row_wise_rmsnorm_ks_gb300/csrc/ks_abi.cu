@@ -142,10 +142,14 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
         if (p.vec_per_thread != 1 && p.vec_per_thread != 2 && p.vec_per_thread != 4 &&
             p.vec_per_thread != 6 && p.vec_per_thread != 8)
             return fail(KS_ERR_INVALID_ARGUMENT, "warp-row kernel takes 1, 2, 4, 6 or 8 vectors");
-        if (32LL * p.vec_per_thread < hv || p.block > 256)
+        if (p.team == 0) p.team = 32;  // a plan made without a team: a warp per row
+        if (p.team != 8 && p.team != 16 && p.team != 32)
+            return fail(KS_ERR_INVALID_ARGUMENT, "warp-row team must be 8, 16 or 32 lanes (got %d)", p.team);
+        if (p.team < 32 && p.vec_per_thread > 4)
+            return fail(KS_ERR_INVALID_ARGUMENT, "8- and 16-lane teams take 1, 2 or 4 vectors per lane");
+        if ((int64_t)p.team * p.vec_per_thread < hv || p.block > 256)
             return fail(KS_ERR_INVALID_ARGUMENT, "warp-row plan does not cover the row or block > 256");
-        p.team = 32;
-        rows_per_cta = p.block / 32;
+        rows_per_cta = p.block / p.team;
         break;
     case KS_KERNEL_CTA_ROW:
     case KS_KERNEL_BULK_ROW: {
@@ -371,15 +375,13 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 
 // Host heuristic (after the pages' rule of sizing the launch from the row width: Triton
 // Kernels, "Kernels" table, rmsnorm row; Kernscope, "Triton CUDA backend"):
-//  * rows of at most 96 vectors (bf16/fp16 H <= 768, fp32 H <= 384), and of at most 128 when
-//    there are no more rows than SMs: one warp per row, 1/2/4 vectors per lane (the fewest that
-//    cover the row), next row prefetched, up to 8 rows per CTA but never fewer CTAs than SMs
-//    when the rows allow it;
-//  * many rows (more than SMs) of 97..2048 vectors (bf16/fp16 H <= 16384, fp32 H <= 8192): the
-//    band table below, one per dtype and op, generated from a plan-contexts sweep (warp rows,
-//    CTA rows at 2 or 4 vectors per thread with and without prefetch, the staged ring and the
-//    two-pass kernel, each timed in two contexts); the ring and the two-pass kernel only with at
-//    least 4 rows per SM, the band's one-pass fallback otherwise;
+//  * many rows (more than SMs) of 1..2048 vectors (bf16/fp16 H <= 16384, fp32 H <= 8192): the
+//    band table below, one per dtype and op, generated from a plan-contexts sweep (8- and 16-lane
+//    teams and warps per row, CTA rows at 2 or 4 vectors per thread, each with and without
+//    prefetch, the staged ring and the two-pass kernel, each timed in two contexts); the ring and
+//    the two-pass kernel only with at least 4 rows per SM, the band's one-pass fallback otherwise;
+//  * at most SMs rows of at most 128 vectors: one warp per row, 1/2/4 vectors per lane (the
+//    fewest that cover the row), next row prefetched, one row per CTA;
 //  * latency regime (rows <= SMs, so each CTA gets at most one row) of 129..2048 vectors:
 //    prefetch has nothing to fetch: the widest fused rows (>= 1792 vectors, at most SMs/8 rows)
 //    go to a cluster of 8 CTAs per row, plain rows of at most 1024 vectors take 2 vectors per
@@ -397,10 +399,14 @@ ks_status_t run(bool fused, void *out, const void *x, void *res, const void *w, 
 // but at least one per SM).
 namespace {
 
-// Many rows of 97..2048 vectors: one band table per dtype and op. A band covers the widths up to
+// Many rows of 1..2048 vectors: one band table per dtype and op. A band covers the widths up to
 // its `hi` (from the previous band's hi + 1) and names a launch:
-//   W / w  a warp per row with / without prefetch: 4 vectors per lane up to 128 vectors (up to 8
-//          rows per 256-thread CTA), 6 up to 192 and 8 up to 256 (4 rows per 128-thread CTA);
+//   E / e  an 8-lane team per row with / without prefetch (4 rows per warp), at the fewest of 1,
+//          2 or 4 vectors per lane that cover the row (rows of at most 32 vectors);
+//   H / h  the same with 16-lane teams (2 rows per warp; rows of at most 64 vectors);
+//   W / w  a warp per row at the fewest of 1, 2, 4, 6 or 8 vectors per lane that cover the row:
+//          up to 8 warps per 256-thread CTA at 1, 2 or 4 vectors (rows of at most 128 vectors),
+//          4 rows per 128-thread CTA at 6 or 8;
 //   T / t  a CTA per row at 2 vectors per thread, with / without prefetch;
 //   F / f  the same at 4 vectors per thread;
 //   R      the staged ring, 2 stages;
@@ -419,31 +425,35 @@ struct RowBand {
     char code;      // the launch
     char fallback;  // the launch with fewer than 4 rows per SM
 };
-constexpr int64_t kBandLo = 97, kBandHi = 2048;
+constexpr int64_t kBandLo = 1, kBandHi = 2048;
 // BEGIN GENERATED ROW BANDS
-constexpr RowBand kRowBandsF32Plain[] = {{108, 'f', 'f'}, {124, 'W', 'W'}, {128, 'F', 'F'}, {152, 'w', 'w'}, {200, 'f', 'f'}, {248, 'W', 'W'}, {256, 'T', 'T'}, {480, 'f', 'f'}, {512, 'T', 'T'}, {608, 'f', 'f'}, {640, 'T', 'T'}, {992, 'f', 'f'}, {1344, 'P', 'f'}, {1536, 'f', 'f'}, {1888, 'P', 'f'}, {2048, 'f', 'f'}};
-constexpr RowBand kRowBandsF32Fused[] = {{116, 'W', 'W'}, {128, 'F', 'F'}, {152, 't', 't'}, {192, 'T', 'T'}, {208, 't', 't'}, {248, 'T', 'T'}, {256, 'W', 'W'}, {296, 't', 't'}, {320, 'T', 'T'}, {360, 't', 't'}, {384, 'T', 'T'}, {416, 't', 't'}, {512, 'F', 'F'}, {768, 't', 't'}, {960, 'P', 't'}, {1152, 't', 't'}, {1600, 'f', 'f'}, {2048, 'P', 'f'}};
-constexpr RowBand kRowBandsF16Plain[] = {{112, 'w', 'w'}, {124, 'f', 'f'}, {128, 'W', 'W'}, {188, 'w', 'w'}, {192, 'f', 'f'}, {200, 'w', 'w'}, {248, 'f', 'f'}, {256, 'W', 'W'}, {1536, 'f', 'f'}, {2048, 'P', 'f'}};
-constexpr RowBand kRowBandsF16Fused[] = {{112, 't', 't'}, {128, 'W', 'W'}, {136, 'w', 'w'}, {176, 't', 't'}, {196, 'f', 'f'}, {248, 't', 't'}, {256, 'T', 'T'}, {576, 't', 't'}, {672, 'f', 'f'}, {768, 't', 't'}, {992, 'f', 'f'}, {1152, 't', 't'}, {1536, 'f', 'f'}, {1824, 'R', 't'}, {2048, 'P', 't'}};
-constexpr RowBand kRowBandsBf16Plain[] = {{108, 'w', 'w'}, {124, 'W', 'W'}, {128, 'T', 'T'}, {144, 'w', 'w'}, {192, 'W', 'W'}, {208, 'w', 'w'}, {240, 'f', 'f'}, {256, 'W', 'W'}, {480, 'f', 'f'}, {512, 'F', 'F'}, {576, 'f', 'f'}, {640, 'F', 'F'}, {736, 'f', 'f'}, {768, 'F', 'F'}, {1152, 'f', 'f'}, {1280, 'F', 'F'}, {1536, 'f', 'f'}, {2048, 'P', 'f'}};
-constexpr RowBand kRowBandsBf16Fused[] = {{128, 't', 't'}, {136, 'w', 'w'}, {168, 't', 't'}, {200, 'F', 'F'}, {312, 't', 't'}, {320, 'F', 'F'}, {576, 't', 't'}, {672, 'f', 'f'}, {864, 'F', 'F'}, {992, 'f', 'f'}, {1152, 't', 't'}, {1472, 'f', 'f'}, {2048, 'F', 'F'}};
+constexpr RowBand kRowBandsF32Plain[] = {{4, 'e', 'e'}, {8, 'E', 'E'}, {14, 'e', 'e'}, {16, 'E', 'E'}, {24, 'e', 'e'}, {32, 'E', 'E'}, {52, 'h', 'h'}, {64, 'H', 'H'}, {108, 'w', 'w'}, {124, 'W', 'W'}, {128, 'F', 'F'}, {152, 'w', 'w'}, {200, 'f', 'f'}, {248, 'W', 'W'}, {256, 'T', 'T'}, {480, 'f', 'f'}, {512, 'T', 'T'}, {608, 'f', 'f'}, {640, 'T', 'T'}, {992, 'f', 'f'}, {1344, 'P', 'f'}, {1536, 'f', 'f'}, {1888, 'P', 'f'}, {2048, 'f', 'f'}};
+constexpr RowBand kRowBandsF32Fused[] = {{7, 'e', 'e'}, {8, 'E', 'E'}, {14, 'e', 'e'}, {16, 'E', 'E'}, {24, 'e', 'e'}, {32, 'E', 'E'}, {44, 'h', 'h'}, {64, 'H', 'H'}, {76, 'w', 'w'}, {92, 't', 't'}, {116, 'W', 'W'}, {128, 'F', 'F'}, {152, 't', 't'}, {192, 'T', 'T'}, {208, 't', 't'}, {248, 'T', 'T'}, {256, 'W', 'W'}, {296, 't', 't'}, {320, 'T', 'T'}, {360, 't', 't'}, {384, 'T', 'T'}, {416, 't', 't'}, {512, 'F', 'F'}, {768, 't', 't'}, {960, 'P', 't'}, {1152, 't', 't'}, {1600, 'f', 'f'}, {2048, 'P', 'f'}};
+constexpr RowBand kRowBandsF16Plain[] = {{14, 'e', 'e'}, {16, 'E', 'E'}, {28, 'e', 'e'}, {32, 'E', 'E'}, {60, 'h', 'h'}, {64, 'H', 'H'}, {112, 'w', 'w'}, {124, 'f', 'f'}, {128, 'W', 'W'}, {188, 'w', 'w'}, {192, 'f', 'f'}, {200, 'w', 'w'}, {248, 'f', 'f'}, {256, 'W', 'W'}, {1536, 'f', 'f'}, {2048, 'P', 'f'}};
+constexpr RowBand kRowBandsF16Fused[] = {{14, 'e', 'e'}, {16, 'E', 'E'}, {20, 'e', 'e'}, {24, 'h', 'h'}, {32, 'E', 'E'}, {44, 'h', 'h'}, {52, 'w', 'w'}, {64, 'H', 'H'}, {84, 'w', 'w'}, {92, 'f', 'f'}, {112, 't', 't'}, {128, 'W', 'W'}, {136, 'w', 'w'}, {176, 't', 't'}, {196, 'f', 'f'}, {248, 't', 't'}, {256, 'T', 'T'}, {576, 't', 't'}, {672, 'f', 'f'}, {768, 't', 't'}, {992, 'f', 'f'}, {1152, 't', 't'}, {1536, 'f', 'f'}, {1824, 'R', 't'}, {2048, 'P', 't'}};
+constexpr RowBand kRowBandsBf16Plain[] = {{14, 'e', 'e'}, {16, 'E', 'E'}, {28, 'e', 'e'}, {32, 'H', 'H'}, {60, 'h', 'h'}, {64, 'W', 'W'}, {108, 'w', 'w'}, {124, 'W', 'W'}, {128, 'T', 'T'}, {144, 'w', 'w'}, {192, 'W', 'W'}, {208, 'w', 'w'}, {240, 'f', 'f'}, {256, 'W', 'W'}, {480, 'f', 'f'}, {512, 'F', 'F'}, {576, 'f', 'f'}, {640, 'F', 'F'}, {736, 'f', 'f'}, {768, 'F', 'F'}, {1152, 'f', 'f'}, {1280, 'F', 'F'}, {1536, 'f', 'f'}, {2048, 'P', 'f'}};
+constexpr RowBand kRowBandsBf16Fused[] = {{12, 'e', 'e'}, {16, 'E', 'E'}, {20, 'e', 'e'}, {24, 'E', 'E'}, {32, 'H', 'H'}, {40, 'h', 'h'}, {64, 'H', 'H'}, {84, 'w', 'w'}, {128, 'W', 'W'}, {136, 'w', 'w'}, {168, 't', 't'}, {200, 'F', 'F'}, {312, 't', 't'}, {320, 'F', 'F'}, {576, 't', 't'}, {672, 'f', 'f'}, {864, 'F', 'F'}, {992, 'f', 'f'}, {1152, 't', 't'}, {1472, 'f', 'f'}, {2048, 'F', 'F'}};
 // END GENERATED ROW BANDS
 
-// Whether a table is well formed: widths rising to kBandHi, warp launches only where a warp
-// covers the row, fallbacks one-pass launches, every code known.
+// The widest row (in vectors) a one-pass code's launch covers (0: not a one-pass code).
+constexpr int64_t code_reach(char c) {
+    return (c == 'E' || c == 'e') ? 32
+         : (c == 'H' || c == 'h') ? 64
+         : (c == 'W' || c == 'w') ? 256
+         : (c == 'T' || c == 't' || c == 'F' || c == 'f') ? kBandHi : 0;
+}
+
+// Whether a table is well formed: widths rising to kBandHi, team and warp launches only where
+// they cover the row, fallbacks one-pass launches, every code known.
 template <size_t N>
 constexpr bool bands_ok(const RowBand (&b)[N]) {
     for (size_t i = 0; i < N; ++i) {
         if (b[i].hi < kBandLo || b[i].hi > kBandHi || (i > 0 && b[i].hi <= b[i - 1].hi)) return false;
         const char c = b[i].code, f = b[i].fallback;
-        bool known = false, one_pass = false;
-        for (const char k : {'W', 'w', 'T', 't', 'F', 'f'}) {
-            known = known || c == k;
-            one_pass = one_pass || f == k;
-        }
-        if (!(known || c == 'R' || c == 'P') || !one_pass) return false;
-        if (known && f != c) return false;
-        if ((c == 'W' || c == 'w' || f == 'W' || f == 'w') && b[i].hi > 256) return false;
+        const bool one_pass = code_reach(c) > 0;
+        if (!(one_pass || c == 'R' || c == 'P') || code_reach(f) == 0) return false;
+        if (one_pass && f != c) return false;
+        if ((one_pass && b[i].hi > code_reach(c)) || b[i].hi > code_reach(f)) return false;
     }
     return b[N - 1].hi == kBandHi;
 }
@@ -496,7 +506,7 @@ void twopass_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
     p->team = p->block;
 }
 
-// The band plan for many rows (more than SMs) of 97..2048 vectors; returns the rows each CTA
+// The band plan for many rows (more than SMs) of 1..2048 vectors; returns the rows each CTA
 // handles.
 int64_t band_row(ks_plan_t *p, int64_t hv, int64_t rows, int sm_count, bool fused,
                  ks_dtype_t dtype) {
@@ -504,21 +514,28 @@ int64_t band_row(ks_plan_t *p, int64_t hv, int64_t rows, int sm_count, bool fuse
     while (hv > b->hi) ++b;
     const char c = rows >= 4 * (int64_t)sm_count ? b->code : b->fallback;
     switch (c) {
+    case 'E':
+    case 'e':
+    case 'H':
+    case 'h':
     case 'W':
     case 'w': {
         p->kernel = KS_KERNEL_WARP_ROW;
-        p->team = 32;
-        p->flags = c == 'W' ? 0 : KS_PLAN_NO_PREFETCH;
-        if (hv <= 128) {
-            p->vec_per_thread = 4;
-            int64_t teams = ceil_div(rows, sm_count);
-            teams = teams < 1 ? 1 : (teams > 8 ? 8 : teams);
-            p->block = (int32_t)(32 * teams);
-            return teams;
+        p->team = (c == 'E' || c == 'e') ? 8 : ((c == 'H' || c == 'h') ? 16 : 32);
+        p->flags = (c == 'E' || c == 'H' || c == 'W') ? 0 : KS_PLAN_NO_PREFETCH;
+        int v = 1;
+        while ((int64_t)p->team * v < hv) v = v < 4 ? 2 * v : v + 2;  // 1, 2, 4, 6, 8
+        p->vec_per_thread = v;
+        if (v >= 6) {
+            p->block = 128;
+            return 4;
         }
-        p->vec_per_thread = hv <= 192 ? 6 : 8;
-        p->block = 128;
-        return 4;
+        // up to 8 warps per CTA, but never fewer CTAs than SMs when the rows allow it
+        const int64_t per_warp = 32 / p->team;
+        int64_t warps = ceil_div(rows, (int64_t)sm_count * per_warp);
+        warps = warps < 1 ? 1 : (warps > 8 ? 8 : warps);
+        p->block = (int32_t)(32 * warps);
+        return warps * per_warp;
     }
     case 'T':
     case 't':
@@ -578,8 +595,8 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
     const bool vec_ok = aligned16 && hidden % per_vec == 0;
     const int64_t hv = vec_ok ? hidden / per_vec : 0;
     int64_t rows_per_cta = 1;
-    if (vec_ok && (hv < kBandLo || (hv <= 128 && rows <= sm_count))) {
-        // Narrow rows: a warp per row, the fewest vectors per lane that cover it.
+    if (vec_ok && hv <= 128 && rows <= sm_count) {
+        // Few narrow rows: a warp per row, the fewest vectors per lane that cover it.
         p->kernel = KS_KERNEL_WARP_ROW;
         p->vec_per_thread = hv <= 32 ? 1 : (hv <= 64 ? 2 : 4);
         p->team = 32;
@@ -600,7 +617,7 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         } else {
             cta_row(p, hv, 4, fused);
         }
-    } else if (vec_ok && hv <= 2048) {
+    } else if (vec_ok && hv <= kBandHi) {
         // Many rows: the measured band table.
         rows_per_cta = band_row(p, hv, rows, sm_count, fused, dtype);
     } else if (vec_ok && hv > 2048 && rows * 8 <= sm_count && hv <= 16384) {

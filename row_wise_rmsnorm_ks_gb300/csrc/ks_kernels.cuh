@@ -177,15 +177,21 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Sum over a team: one warp (kWarpTeam) or the whole CTA. Every thread of the team returns the
-// same value (the per-warp sums are added in warp order). `red` is one of two alternating
-// 32-float slots: a warp can only write a slot again after passing the barrier of the row in
-// between, which every warp reaches only after it has read this row's slot, so one barrier per
-// row suffices.
-template <bool kWarpTeam>
+// Sum over a team: kTeam lanes of a warp (8, 16 or 32; an aligned group of lanes, so the xor
+// offsets below kTeam stay inside it; shuffles only, every lane of the warp taking part) or, with
+// kTeam = 0, the whole CTA. Every thread of the team returns the same value (the per-warp sums
+// are added in warp order). `red` is one of two alternating 32-float slots: a warp can only
+// write a slot again after passing the barrier of the row in between, which every warp reaches
+// only after it has read this row's slot, so one barrier per row suffices.
+template <int kTeam>
 __device__ __forceinline__ float team_sum(float v, float *red) {
+    if constexpr (kTeam == 8 || kTeam == 16) {
+#pragma unroll
+        for (int o = kTeam / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+        return v;
+    }
     v = warp_sum(v);
-    if (kWarpTeam) return v;
+    if (kTeam == 32) return v;
     const int warp = threadIdx.x >> 5;
     if ((threadIdx.x & 31) == 0) red[warp] = v;
     __syncthreads();
@@ -304,10 +310,13 @@ __device__ __forceinline__ void opaque(uint4 &v) {
 // One row of the vector kernel, its vectors already in registers (xc, and rc for the fused op):
 // the sum of squares (the fused op also forms s and stores cast(s) into the residual), the team
 // reduction through `red`, then normalise, weight, cast and store.
-template <typename T, int V, bool kFused, bool kWarpTeam, bool kOpaque>
+// One row's work for one thread of its team: vectors t, t + g, ... of the row, already loaded
+// into xc (and rc). An inactive team (a sub-warp team past the last row, whose warp still takes
+// part in the shuffles) computes on zeros and stores nothing.
+template <typename T, int V, bool kFused, int kTeam, bool kOpaque>
 __device__ __forceinline__ void vec_row(const RowArgs &a, int64_t row, int t, int g,
                                         uint4 (&xc)[V], uint4 (&rc)[V], uint4 (&wv)[V],
-                                        float *red) {
+                                        float *red, bool active) {
     using E = Elem<T>;
     constexpr int P = E::kPerVec / 2;
     const int64_t hv = a.hv;
@@ -321,11 +330,11 @@ __device__ __forceinline__ void vec_row(const RowArgs &a, int64_t row, int t, in
         if (c < hv) {
             float2 f[P];
             row_values<T, kFused>(xc[k], rc[k], f);
-            if (kFused) __stcs(rg + c, E::pack2(f));
+            if (kFused && active) __stcs(rg + c, E::pack2(f));
             acc.add(f);
         }
     }
-    const float ss = team_sum<kWarpTeam>(acc.total(), red);
+    const float ss = team_sum<kTeam>(acc.total(), red);
     const float scale = row_scale(ss, (float)a.hidden, a.eps);
 
     if (kOpaque) {
@@ -339,7 +348,7 @@ __device__ __forceinline__ void vec_row(const RowArgs &a, int64_t row, int t, in
 #pragma unroll
     for (int k = 0; k < V; ++k) {
         const int64_t c = t + (int64_t)k * g;
-        if (c < hv) {
+        if (c < hv && active) {
             float2 f[P];
             row_values<T, kFused>(xc[k], rc[k], f);
             __stcs(og + c, scaled_weighted<T>(f, scale, wv[k]));
@@ -347,23 +356,27 @@ __device__ __forceinline__ void vec_row(const RowArgs &a, int64_t row, int t, in
     }
 }
 
-// One team (a warp, or the whole CTA) per row; row r's 16-byte vector c (of hv) is handled by
-// thread c % G of the team, as its (c / G)-th vector. Teams stride over rows by the number of
-// teams in the grid. With kPrefetch a team loads its next row while it works on the current one
-// and moves it into the current buffer at the end of the row. (Writing the loop body out twice
-// for two buffers used in turn, with no copy, measured 2-20 points slower for bf16 on GB300 and
-// no faster for fp16.) Without it, each row is loaded when its turn comes, and the raw vectors
-// are hidden from the optimiser across the reduction (measured: this helps without prefetch,
-// costs with it).
-template <typename T, int V, bool kFused, bool kWarpTeam, bool kPrefetch>
-__global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
+// One team per row: kTeam lanes of a warp (8, 16 or 32) or, with kTeam = 0, the whole CTA. Row
+// r's 16-byte vector c (of hv) is handled by thread c % G of the team (G its size), as its
+// (c / G)-th vector. Teams stride over rows by the number of teams in the grid. A warp of 8- or
+// 16-lane teams holds several consecutive rows and runs as long as its first row does (the
+// shuffles of a team's sum need every lane of the warp), its teams past the last row inactive.
+// With kPrefetch a team loads its next row while it works on the current one and moves it into
+// the current buffer at the end of the row. (Writing the loop body out twice for two buffers
+// used in turn, with no copy, measured 2-20 points slower for bf16 on GB300 and no faster for
+// fp16.) Without it, each row is loaded when its turn comes, and the raw vectors are hidden from
+// the optimiser across the reduction (measured: this helps without prefetch, costs with it).
+template <typename T, int V, bool kFused, int kTeam, bool kPrefetch>
+__global__ void __launch_bounds__(VecBound<V, kTeam != 0>::value)
     rows_vec_kernel(const RowArgs a) {
+    static_assert(kTeam == 0 || kTeam == 8 || kTeam == 16 || kTeam == 32, "team of 8, 16 or 32 lanes");
+    constexpr bool kSub = kTeam == 8 || kTeam == 16;
     __shared__ float red[2][32];
 
-    const int g = kWarpTeam ? 32 : (int)blockDim.x;
-    const int t = kWarpTeam ? (int)(threadIdx.x & 31) : (int)threadIdx.x;
-    const int teams = kWarpTeam ? (int)(blockDim.x >> 5) : 1;
-    const int team = kWarpTeam ? (int)(threadIdx.x >> 5) : 0;
+    const int g = kTeam ? kTeam : (int)blockDim.x;
+    const int t = kTeam ? (int)(threadIdx.x & (kTeam - 1)) : (int)threadIdx.x;
+    const int teams = kTeam ? (int)(blockDim.x / kTeam) : 1;
+    const int team = kTeam ? (int)(threadIdx.x / kTeam) : 0;
     const int64_t hv = a.hv;
 
     const uint4 *xg = static_cast<const uint4 *>(a.x);
@@ -382,26 +395,31 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
     }
 
     int64_t row = (int64_t)blockIdx.x * teams + team;
+    // the first row of this thread's warp (its own row for warp and CTA teams)
+    int64_t lead = kSub ? row - (team & (32 / (kSub ? kTeam : 32) - 1)) : row;
     const int64_t stride = (int64_t)gridDim.x * teams;
     if (!kPrefetch) {
         int parity = 0;
-        for (; row < a.rows; row += stride) {
+        for (; lead < a.rows; lead += stride, row += stride) {
+            const bool active = !kSub || row < a.rows;
             uint4 xc[V], rc[V];
-            load_row<V>(xg + row * hv, t, g, hv, xc);
-            if (kFused) load_row<V>(rg + row * hv, t, g, hv, rc);
-            vec_row<T, V, kFused, kWarpTeam, true>(a, row, t, g, xc, rc, wv, red[parity]);
+            load_row<V>(xg + row * hv, t, g, active ? hv : 0, xc);
+            if (kFused) load_row<V>(rg + row * hv, t, g, active ? hv : 0, rc);
+            vec_row<T, V, kFused, kTeam, true>(a, row, t, g, xc, rc, wv, red[parity], active);
             parity ^= 1;
         }
         return;
     }
 
     uint4 xc[V], rc[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) xc[k] = rc[k] = make_uint4(0u, 0u, 0u, 0u);
     if (row < a.rows) {
         load_row<V>(xg + row * hv, t, g, hv, xc);
         if (kFused) load_row<V>(rg + row * hv, t, g, hv, rc);
     }
     int parity = 0;
-    while (row < a.rows) {
+    while (lead < a.rows) {
         const int64_t next = row + stride;
         uint4 xn[V], rn[V];
 #pragma unroll
@@ -410,9 +428,11 @@ __global__ void __launch_bounds__(VecBound<V, kWarpTeam>::value)
             load_row<V>(xg + next * hv, t, g, hv, xn);
             if (kFused) load_row<V>(rg + next * hv, t, g, hv, rn);
         }
-        vec_row<T, V, kFused, kWarpTeam, false>(a, row, t, g, xc, rc, wv, red[parity]);
+        vec_row<T, V, kFused, kTeam, false>(a, row, t, g, xc, rc, wv, red[parity],
+                                            !kSub || row < a.rows);
         parity ^= 1;
         row = next;
+        lead += stride;
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             xc[k] = xn[k];
@@ -483,7 +503,7 @@ __global__ void __launch_bounds__(kMaxBlock) rows_twopass_kernel(const RowArgs a
                 acc.add(f);
             }
         }
-        const float ss = team_sum<false>(acc.total(), red[parity]);
+        const float ss = team_sum<0>(acc.total(), red[parity]);
         parity ^= 1;
         const float scale = row_scale(ss, (float)a.hidden, a.eps);
         uint4 *orow = og + row * hv;
@@ -833,7 +853,7 @@ __global__ void __launch_bounds__(1024) rows_scalar_kernel(const RowArgs a) {
             if (kFused) v[0] = __fadd_rn(v[0], E::load1(a.res, base + j));
             acc.add(v);
         }
-        const float ss = team_sum<false>(acc.total(), red[parity]);
+        const float ss = team_sum<0>(acc.total(), red[parity]);
         parity ^= 1;
         const float scale = row_scale(ss, h, a.eps);
         for (int64_t j = threadIdx.x; j < H; j += blockDim.x) {
@@ -1143,32 +1163,50 @@ __global__ void __launch_bounds__(512) rows_cluster_kernel(const RowArgs a) {
 
 // ----------------------------------------------------------------------- kernel selection
 
+// Sub-warp team kernels: 8 or 16 lanes per row, V vectors per lane.
+template <typename T, int V, bool kFused>
+const void *pick_team(int team, bool pf) {
+    if (team == 8)
+        return pf ? (const void *)rows_vec_kernel<T, V, kFused, 8, true>
+                  : (const void *)rows_vec_kernel<T, V, kFused, 8, false>;
+    return pf ? (const void *)rows_vec_kernel<T, V, kFused, 16, true>
+              : (const void *)rows_vec_kernel<T, V, kFused, 16, false>;
+}
+
 template <typename T, bool kFused>
 const void *pick_kernel(const ks_plan_t &p) {
     switch (p.kernel) {
     case KS_KERNEL_WARP_ROW: {
         const bool pf = !(p.flags & KS_PLAN_NO_PREFETCH);
+        if (p.team == 8 || p.team == 16) {
+            switch (p.vec_per_thread) {
+            case 1: return pick_team<T, 1, kFused>(p.team, pf);
+            case 2: return pick_team<T, 2, kFused>(p.team, pf);
+            case 4: return pick_team<T, 4, kFused>(p.team, pf);
+            default: return nullptr;
+            }
+        }
         switch (p.vec_per_thread) {
-        case 1: return pf ? (const void *)rows_vec_kernel<T, 1, kFused, true, true>
-                          : (const void *)rows_vec_kernel<T, 1, kFused, true, false>;
-        case 2: return pf ? (const void *)rows_vec_kernel<T, 2, kFused, true, true>
-                          : (const void *)rows_vec_kernel<T, 2, kFused, true, false>;
-        case 4: return pf ? (const void *)rows_vec_kernel<T, 4, kFused, true, true>
-                          : (const void *)rows_vec_kernel<T, 4, kFused, true, false>;
-        case 6: return pf ? (const void *)rows_vec_kernel<T, 6, kFused, true, true>
-                          : (const void *)rows_vec_kernel<T, 6, kFused, true, false>;
-        case 8: return pf ? (const void *)rows_vec_kernel<T, 8, kFused, true, true>
-                          : (const void *)rows_vec_kernel<T, 8, kFused, true, false>;
+        case 1: return pf ? (const void *)rows_vec_kernel<T, 1, kFused, 32, true>
+                          : (const void *)rows_vec_kernel<T, 1, kFused, 32, false>;
+        case 2: return pf ? (const void *)rows_vec_kernel<T, 2, kFused, 32, true>
+                          : (const void *)rows_vec_kernel<T, 2, kFused, 32, false>;
+        case 4: return pf ? (const void *)rows_vec_kernel<T, 4, kFused, 32, true>
+                          : (const void *)rows_vec_kernel<T, 4, kFused, 32, false>;
+        case 6: return pf ? (const void *)rows_vec_kernel<T, 6, kFused, 32, true>
+                          : (const void *)rows_vec_kernel<T, 6, kFused, 32, false>;
+        case 8: return pf ? (const void *)rows_vec_kernel<T, 8, kFused, 32, true>
+                          : (const void *)rows_vec_kernel<T, 8, kFused, 32, false>;
         default: return nullptr;
         }
     }
     case KS_KERNEL_CTA_ROW: {
         const bool pf = !(p.flags & KS_PLAN_NO_PREFETCH);
         switch (p.vec_per_thread) {
-        case 2: return pf ? (const void *)rows_vec_kernel<T, 2, kFused, false, true>
-                          : (const void *)rows_vec_kernel<T, 2, kFused, false, false>;
-        case 4: return pf ? (const void *)rows_vec_kernel<T, 4, kFused, false, true>
-                          : (const void *)rows_vec_kernel<T, 4, kFused, false, false>;
+        case 2: return pf ? (const void *)rows_vec_kernel<T, 2, kFused, 0, true>
+                          : (const void *)rows_vec_kernel<T, 2, kFused, 0, false>;
+        case 4: return pf ? (const void *)rows_vec_kernel<T, 4, kFused, 0, true>
+                          : (const void *)rows_vec_kernel<T, 4, kFused, 0, false>;
         default: return nullptr;
         }
     }

@@ -120,10 +120,10 @@ def plan(op, rows, hidden, dtype=BF16, aligned=True, sms=152, bps=0):
 
 @pytest.mark.parametrize("op,hidden,dtype,v", [(0, 256, BF16, 1), (0, 512, BF16, 2), (0, 768, F16, 4),
                                                (1, 768, BF16, 4), (0, 384, F32, 4)])
-def test_narrow_rows_take_warp_per_row(op, hidden, dtype, v):
-    p = plan(op, 32768, hidden, dtype)
+def test_few_narrow_rows_take_warp_per_row(op, hidden, dtype, v):
+    p = plan(op, 100, hidden, dtype)  # at most SMs rows: a warp per row, one row per CTA
     assert p.kernel == _abi.KS_KERNEL_WARP_ROW and p.vec_per_thread == v and p.team == 32
-    assert p.block == 256  # 8 rows per CTA once there are enough rows
+    assert p.block == 32 and p.grid == 100
 
 
 NO_PF = _abi.KS_PLAN_NO_PREFETCH
@@ -330,6 +330,12 @@ def test_planned_entry_points_reject_plans_that_do_not_fit():
     ]
     for p in bad:
         assert _abi.ks_rms_norm_planned(a, b, w, 64, 8192, 1e-6, BF16, p, None) == E
+    # warp-row teams: 8, 16 or 32 lanes, at most 4 vectors a lane below 32 (rows of 8 vectors)
+    for team, v in ((4, 2), (12, 1), (24, 1), (8, 6), (16, 8)):
+        p = mk(_abi.KS_KERNEL_WARP_ROW, v, 64, team=team)
+        assert _abi.ks_rms_norm_planned(a, b, w, 64, 64, 1e-6, BF16, p, None) == E, (team, v)
+    p = mk(_abi.KS_KERNEL_WARP_ROW, 1, 64, team=8)  # 8 lanes x 1 vector < 9 vectors
+    assert _abi.ks_rms_norm_planned(a, b, w, 64, 72, 1e-6, BF16, p, None) == E
     # a vector plan on an unaligned pointer
     p = mk(_abi.KS_KERNEL_CTA_ROW, 4, 256)
     assert _abi.ks_rms_norm_planned(a, b + 2, w, 64, 8192, 1e-6, BF16, p, None) == E

@@ -103,8 +103,6 @@ def test_kernel_hash_ignores_comments_and_layout():
 def test_recorded_traffic_only_for_the_recorded_shape():
     """The committed ncu bytes are per launch of the full workload: a smaller --rows/--hidden
     case reports no traffic, and its config names its own shape."""
-    full = bench.recorded_traffic("fused_add_rms_norm")
-    assert full is None or full > 0
     assert bench.recorded_traffic("fused_add_rms_norm", 8192, 8192) is None
     assert bench.recorded_traffic("rms_norm", bench.FULL_ROWS, 4096) is None
     assert "[8192,8192]" in bench.workload(8192, 8192) and "128 MiB" in bench.workload(8192, 8192)
@@ -116,23 +114,52 @@ def test_recorded_traffic_only_for_the_recorded_shape():
 
 def test_recorded_traffic_follows_the_sources(tmp_path, monkeypatch):
     """The DRAM-traffic record is data: it is used only while the kernel and plan sources hash
-    to the value it was taken on, and only for the shape it records."""
+    to the value it was taken on, only for the shape it records, and only while the library
+    picks the recorded plan for that shape."""
     import json
+    from row_wise_rmsnorm_ks_gb300 import _abi
+    try:
+        _abi.load()
+    except OSError as e:
+        pytest.skip(f"libks.so not built: {e}")
+    R, H = bench.FULL_ROWS, bench.FULL_HIDDEN
+    now = _abi.ks_plan_launch(1, R, H, _abi.KS_DTYPE_BF16, True, 152, 0)[1]
+    plan = {k: getattr(now, k) for k in bench.PLAN_FIELDS}
     rec = {"sources_sha": bench.kernel_source_sha(),
-           "launches": {"fused_add_rms_norm": {"shape": [bench.FULL_ROWS, bench.FULL_HIDDEN],
+           "launches": {"fused_add_rms_norm": {"shape": [R, H], "plan": plan,
                                                "dram_read_bytes": 1000,
                                                "dram_write_bytes": 900}}}
     path = tmp_path / "traffic.json"
     path.write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(path))
-    assert bench.recorded_traffic("fused_add_rms_norm") == 1900
-    assert bench.recorded_traffic("rms_norm") is None
-    assert bench.recorded_traffic("fused_add_rms_norm", 4096, bench.FULL_HIDDEN) is None
+    assert bench.recorded_traffic("fused_add_rms_norm", R, H, now) == 1900
+    assert bench.recorded_traffic("fused_add_rms_norm", R, H) is None  # no plan to check
+    other = _abi.ks_plan_launch(1, R, H, _abi.KS_DTYPE_BF16, True, 152, 0)[1]
+    other.vec_per_thread = 4
+    assert bench.recorded_traffic("fused_add_rms_norm", R, H, other) is None
+    assert bench.recorded_traffic("rms_norm", R, H, now) is None
+    assert bench.recorded_traffic("fused_add_rms_norm", 4096, H, now) is None
     rec["sources_sha"] = "0" * 16
     path.write_text(json.dumps(rec))
-    assert bench.recorded_traffic("fused_add_rms_norm") is None
-    # the plan code is part of the hash
+    assert bench.recorded_traffic("fused_add_rms_norm", R, H, now) is None
+    # the plan code is part of the hash, but not its generated band table
     assert any(s.endswith("ks_abi.cu") for s in bench.KERNEL_SOURCES)
+    src = "int a;\n// BEGIN GENERATED ROW BANDS\nint b;\n// END GENERATED ROW BANDS\nint c;\n"
+    assert bench.code_only(bench.GENERATED_BANDS.sub("", src)) == "int a; int c;"
+
+
+def test_committed_traffic_record_is_current():
+    """The committed record matches the current sources and the library's headline plans, so
+    the bench line carries its traffic."""
+    from row_wise_rmsnorm_ks_gb300 import _abi
+    try:
+        _abi.load()
+    except OSError as e:
+        pytest.skip(f"libks.so not built: {e}")
+    R, H = bench.FULL_ROWS, bench.FULL_HIDDEN
+    for op, code in (("rms_norm", 0), ("fused_add_rms_norm", 1)):
+        now = _abi.ks_plan_launch(code, R, H, _abi.KS_DTYPE_BF16, True, 152, 0)[1]
+        assert bench.recorded_traffic(op, R, H, now) is not None, op
 
 
 def test_host_cpu_model_names_the_cpu():

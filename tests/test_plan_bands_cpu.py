@@ -1,4 +1,4 @@
-"""The RMSNorm launch heuristic's band table for many rows of 97..2048 16-byte vectors, against the
+"""The RMSNorm launch heuristic's band table for many rows of 1..2048 16-byte vectors, against the
 measured record it is generated from (no GPU: the plan is host code).
 
 The record (profiles/plan_bands_rms_norm.json) holds, per dtype, op and measured width, the score
@@ -48,7 +48,8 @@ def plan(op, rows, hidden, dtype, sms, bps=0):
 def code_of(p):
     """The band code of a library plan."""
     if p.kernel == _abi.KS_KERNEL_WARP_ROW:
-        return "w" if p.flags & NO_PF else "W"
+        c = {8: "E", 16: "H", 32: "W"}[p.team]
+        return c.lower() if p.flags & NO_PF else c
     if p.kernel == _abi.KS_KERNEL_CTA_ROW:
         c = {2: "T", 4: "F"}[p.vec_per_thread]
         return c.lower() if p.flags & NO_PF else c
@@ -70,7 +71,7 @@ def hidden_of(dt, hv):
 def test_record_covers_every_dtype_and_op(record):
     assert set(record["tables"]) == {f"{d}/{o}" for d in DTYPES for o in OPS}
     for key, t in record["tables"].items():
-        assert t["hv"] == sorted(t["hv"]) and t["hv"][0] <= 100 and t["hv"][-1] == 2048, key
+        assert t["hv"] == sorted(t["hv"]) and t["hv"][0] == 1 and t["hv"][-1] == 2048, key
         assert min(t["rows"]) >= 4 * record["sm_count"], key  # every width measured with many rows
         for c in bench.PLAN_BAND_CODES:
             assert len(t[c]) == len(t["hv"]), (key, c)
@@ -119,14 +120,15 @@ def test_derivation_rule_on_a_small_record():
 @pytest.mark.parametrize("op", list(OPS))
 def test_every_band_width_gets_a_plan_the_library_accepts(dt, op):
     # what each code launches, for every width of the table, with many rows (4 CTAs per SM)
-    for hv in range(97, 2049):
+    for hv in range(1, 2049):
         p = plan(OPS[op], 32768, hidden_of(dt, hv), DTYPES[dt], 152, bps=4)
         c = code_of(p)
-        if c in "Ww":
-            v = 4 if hv <= 128 else (6 if hv <= 192 else 8)
-            assert (p.vec_per_thread, p.team) == (v, 32) and 32 * v >= hv
-            assert p.block == (256 if v == 4 else 128)
-            assert p.rows_per_pass == p.grid * p.block // 32
+        if c in "EeHhWw":
+            team = {"E": 8, "H": 16, "W": 32}[c.upper()]
+            v = next(v for v in (1, 2, 4, 6, 8) if team * v >= hv)  # the fewest that cover
+            assert (p.vec_per_thread, p.team) == (v, team)
+            assert p.block == (256 if v <= 4 else 128)
+            assert p.rows_per_pass == p.grid * p.block // team
         elif c in "TtFf":
             v = 2 if c in "Tt" else 4
             assert p.vec_per_thread == v and p.block == up32(-(-hv // v))
@@ -154,13 +156,24 @@ def test_ring_and_two_pass_need_four_rows_per_sm(record):
     assert seen >= 1  # the record has at least one such band
 
 
-def test_latency_regime_and_narrow_rows_are_outside_the_table():
+def test_latency_regime_is_outside_the_table():
     # at most SMs rows: the latency rules (warp rows up to 128 vectors, CTA rows beyond)
-    p = plan(0, 152, 1024, _abi.KS_DTYPE_BF16, 152)
-    assert p.kernel == _abi.KS_KERNEL_WARP_ROW and p.vec_per_thread == 4
+    for hv in (1, 8, 64, 128):
+        p = plan(0, 152, hv * 8, _abi.KS_DTYPE_BF16, 152)
+        assert p.kernel == _abi.KS_KERNEL_WARP_ROW and p.team == 32 and p.block == 32
+        assert p.vec_per_thread == next(v for v in (1, 2, 4) if 32 * v >= hv)
     p = plan(0, 152, 1032, _abi.KS_DTYPE_BF16, 152)  # 129 vectors
     assert p.kernel == _abi.KS_KERNEL_CTA_ROW and p.vec_per_thread == 2
-    # rows of at most 96 vectors: a warp per row at any row count
-    for hv in (8, 32, 64, 96):
-        p = plan(1, 10 ** 5, hv * 8, _abi.KS_DTYPE_F16, 152)
-        assert p.kernel == _abi.KS_KERNEL_WARP_ROW and 32 * p.vec_per_thread >= hv
+
+
+def test_team_rows_spread_over_sms():
+    """Sub-warp teams hold 4 (8 lanes) or 2 (16 lanes) rows per warp: a CTA takes up to 8 warps
+    of rows, but never so many that fewer CTAs than SMs get rows."""
+    for rows in (153, 1000, 4864, 10 ** 6):
+        for dt, hv in (("bf16", 8), ("bf16", 40), ("fp32", 16)):
+            p = plan(0, rows, hidden_of(dt, hv), DTYPES[dt], 152)
+            assert p.kernel == _abi.KS_KERNEL_WARP_ROW and p.team in (8, 16)
+            per_warp = 32 // p.team
+            warps = min(8, max(1, -(-rows // (152 * per_warp))))
+            assert p.block == 32 * warps
+            assert p.grid == -(-rows // (warps * per_warp))
