@@ -1382,8 +1382,9 @@ def op_band_candidates(op: str, hv: int):
     """The launch plans the next operators' width bands choose among for a row of hv vectors:
     tTvV / tTvVn (a team of T = 8 or 16 lanes per row, V vectors a lane, with / without
     prefetch; where the team covers the row), wV / wVn (a warp per row), cV / cVn (a CTA per
-    row, V vectors a thread), and for SwiGLU flatB (the flat walk on B-thread CTAs) and rowsB
-    (the row kernel with at most B threads)."""
+    row, V vectors a thread), for rows wider than 256 vectors xB (the wide multi-pass kernel on
+    B threads) and for LayerNorm rS (the staged ring of S rows per CTA), and for SwiGLU flatB
+    (the flat walk on B-thread CTAs) and rowsB (the row kernel with at most B threads)."""
     from row_wise_rmsnorm_ks_gb300 import _abi
 
     up32 = lambda n: -(-n // 32) * 32
@@ -1413,6 +1414,16 @@ def op_band_candidates(op: str, hv: int):
             out.append((f"c{v}", mk(_abi.KS_KERNEL_CTA_ROW, v, b)))
             if op == "softmax" and v == 4:
                 out.append(("c4n", mk(_abi.KS_KERNEL_CTA_ROW, 4, b, flags=npf)))
+    if hv > 256:
+        # the wide multi-pass kernel at B threads (xB), and for LayerNorm the staged ring of S
+        # rows per CTA (rS) where its CTA covers the row and the ring fits
+        for blk in (128, 256, 512):
+            out.append((f"x{blk}", mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, blk)))
+        b = up32(-(-hv // 4))
+        if op == "layer_norm" and b <= 512:
+            for st in (2, 3, 4, 6, 8):
+                if 128 + st * hv * 16 <= 226 * 1024:
+                    out.append((f"r{st}", mk(_abi.KS_KERNEL_BULK_ROW, 4, b, st)))
     return out
 
 
@@ -1514,7 +1525,8 @@ def run_ops_bands(args) -> int:
                 _, dp = _abi.ks_plan_launch(op_codes[op], R, H, code, True, sms, 0)
                 line = {"ops_bands": op, "dtype": dt, "hv": hv, "hidden": H, "rows": R,
                         "default_plan": {k: dp.as_dict()[k] for k in ("kernel_name", "vec_per_thread",
-                                                                       "block", "flags", "team")}}
+                                                                       "block", "flags", "team",
+                                                                       "stages")}}
                 for ctx in ("steady", "after_ring"):
                     res = {name: [] for name, _ in fns}
                     for _ in range(args.plan_sweep_rounds):
@@ -1554,66 +1566,110 @@ def ops_bands_table(jsonl_path: str) -> str:
     return head + "\n" + "\n".join(rows)
 
 
+LN_RING_BYTES = 64 * 1024  # the library's LayerNorm ring: rows of this many bytes per CTA
+
+
 def band_of(name: str, default_plan: dict, op: str, hv: int):
-    """(kind, v, prefetch, team) of a band-candidate name, the library's Band fields; 'default'
-    maps the launch the library made to the same fields, 'g' when it is the general rule."""
+    """(kind, v, prefetch, team, block) of a band-candidate name, the library's Band fields;
+    'default' maps the launch the library made to the same fields, 'g' when it is the general
+    rule's CTA row. Kinds: w (a team of `team` lanes per row), c (a CTA per row), r (the
+    LayerNorm staged ring, v = its stages), x (the wide multi-pass kernel on `block` threads)."""
     import re
     if name == "default":
         k, v, npf = default_plan["kernel_name"], default_plan["vec_per_thread"], default_plan["flags"] & 1
         if k == "warp_row":
-            return ("w", v, not npf, default_plan.get("team", 32) or 32)
+            return ("w", v, not npf, default_plan.get("team", 32) or 32, 0)
+        if k == "twopass_row":
+            return ("x", 4, True, 32, default_plan["block"])
+        if k == "bulk_row":
+            st = default_plan.get("stages") or max(2, min(8, LN_RING_BYTES // (hv * 16)))
+            return ("r", st, True, 32, 0)
         gen_v = 1 if hv < 64 else (2 if hv < 128 else 4)
         gen_pf = True if op == "layer_norm" else (gen_v != 4 or hv > 1024)
         if k == "cta_row" and v == gen_v and (not npf) == gen_pf:
-            return ("g", 0, gen_pf, 32)
-        return ("c", v, not npf, 32)
+            return ("g", 0, gen_pf, 32, 0)
+        return ("c", v, not npf, 32, 0)
     m = re.fullmatch(r"t(\d+)v(\d)(n?)", name)
     if m:
-        return ("w", int(m.group(2)), not m.group(3), int(m.group(1)))
+        return ("w", int(m.group(2)), not m.group(3), int(m.group(1)), 0)
+    m = re.fullmatch(r"x(\d+)", name)
+    if m:
+        return ("x", 4, True, 32, int(m.group(1)))
+    m = re.fullmatch(r"r(\d)", name)
+    if m:
+        return ("r", int(m.group(1)), True, 32, 0)
     m = re.fullmatch(r"([wc])(\d)(n?)", name)
-    return (m.group(1), int(m.group(2)), not m.group(3), 32)
+    return (m.group(1), int(m.group(2)), not m.group(3), 32, 0)
 
 
-def derive_bands(jsonl_path: str, op: str, dtypes, min_gain: float = 0.01):
-    """Width bands for op from an --ops-bands run, by one rule: at each measured width, score
-    every candidate by its worse context, and over `dtypes` (the dtypes that share one table) by
-    its worst dtype; keep the library's current plan unless another candidate scores at least
-    `min_gain` (a point of the copy peak) higher, then take the best. Consecutive widths with the
-    same plan merge into one band reaching to the last of them. Returns [(hi, kind, v, prefetch,
-    team)], closed by the general rule."""
+def ops_bands_record(jsonl_paths) -> dict:
+    """The measured record behind the Softmax and LayerNorm width bands, from --ops-bands runs:
+    per operator, dtype and width, every candidate's score (the worse of its two contexts, in
+    thousandths of the measured copy peak) and the band the library's default launch was. A width
+    measured by several runs keeps the last."""
+    lines = {}
+    for path in jsonl_paths:
+        for ln in open(path):
+            if not ln.startswith('{"ops_bands"'):
+                continue
+            d = json.loads(ln)
+            if d["ops_bands"] not in ("softmax", "layer_norm") or "steady" not in d:
+                continue
+            sc = {k: round(1000 * min(d["steady"][k], d.get("after_ring", d["steady"]).get(k, 0.0)))
+                  for k in d["steady"]}
+            lines[(d["ops_bands"], d["dtype"], d["hv"])] = {
+                "op": d["ops_bands"], "dtype": d["dtype"], "hv": d["hv"],
+                "default_band": list(band_of("default", d["default_plan"], d["ops_bands"], d["hv"])),
+                "scores": sc}
+    return {"what": "Softmax and LayerNorm launch scores per width, many rows",
+            "score": "worse of steady state and after a large-shared-memory kernel, thousandths "
+                     "of the measured copy peak",
+            "lines": [lines[k] for k in sorted(lines)]}
+
+
+def derive_bands(record: dict, op: str, dtypes, min_gain: int = 10):
+    """Width bands for op from a record of --ops-bands runs, by one rule: at each measured width,
+    score every candidate by its worse context, and over `dtypes` (the dtypes that share one
+    table) by its worst dtype; keep the library's current plan unless another candidate scores at
+    least `min_gain` thousandths (a point of the copy peak) higher, then take the best. Consecutive
+    widths with the same plan merge into one band reaching to the last of them. Returns
+    [(hi, kind, v, prefetch, team, block)], closed by the general rule."""
     by_w = {}
-    for ln in open(jsonl_path):
-        if not ln.startswith('{"ops_bands"'):
-            continue
-        d = json.loads(ln)
-        if d["ops_bands"] != op or d["dtype"] not in dtypes or "steady" not in d:
-            continue
-        sc = {k: min(d["steady"][k], d.get("after_ring", d["steady"]).get(k, 0.0)) for k in d["steady"]}
-        by_w.setdefault(d["hv"], {})[d["dtype"]] = (sc, d["default_plan"])
+    for ln in record["lines"]:
+        if ln["op"] == op and ln["dtype"] in dtypes:
+            by_w.setdefault(ln["hv"], {})[ln["dtype"]] = ln
     bands = []
     for hv in sorted(by_w):
         per = by_w[hv]
         if set(per) != set(dtypes):
             continue
-        names = set.intersection(*(set(sc) for sc, _ in per.values()))
-        worst = {n: min(per[dt][0][n] for dt in per) for n in names}
-        cur = band_of("default", per[dtypes[0]][1], op, hv)
-        best = max(worst, key=worst.get)
+        names = set.intersection(*(set(ln["scores"]) for ln in per.values()))
+        worst = {n: min(per[dt]["scores"][n] for dt in per) for n in names}
+        cur = tuple(per[dtypes[0]]["default_band"])
+        best = max(sorted(worst), key=worst.get)
         pick = cur if worst[best] - worst["default"] < min_gain else band_of(best, None, op, hv)
         if bands and bands[-1][1:] == pick:
             bands[-1] = (hv,) + pick
         else:
             bands.append((hv,) + pick)
-    bands.append((32767, "g", 0, True, 32))
+    bands.append((32767, "g", 0, True, 32, 0))
     return bands
+
+
+OPS_BAND_TABLES = (("kSoftmax16", "softmax", ["bf16", "fp16"]), ("kSoftmax32", "softmax", ["fp32"]),
+                   ("kLayerNormBf16", "layer_norm", ["bf16"]),
+                   ("kLayerNormF16", "layer_norm", ["fp16"]),
+                   ("kLayerNormF32", "layer_norm", ["fp32"]))
 
 
 def bands_cpp(name: str, bands) -> str:
     """The bands as the library's C++ table."""
     def one(b):
-        hi, kind, v, pf, team = b
+        hi, kind, v, pf, team, block = b
         hi_s = "kBandEnd" if hi == 32767 else str(hi)
         pf_s = "true" if pf else "false"
+        if block:
+            return f"{{{hi_s}, '{kind}', {v}, {pf_s}, {team}, {block}}}"
         return (f"{{{hi_s}, '{kind}', {v}, {pf_s}, {team}}}" if team != 32
                 else f"{{{hi_s}, '{kind}', {v}, {pf_s}}}")
     return f"constexpr Band {name}[] = {{" + ", ".join(one(b) for b in bands) + "};"
@@ -1860,8 +1916,12 @@ def main() -> int:
     ap.add_argument("--ops-bands-ops", default="softmax,layer_norm,silu_and_mul")
     ap.add_argument("--ops-bands-table", metavar="JSONL",
                     help="print the markdown table of an --ops-bands run")
-    ap.add_argument("--ops-bands-derive", metavar="JSONL",
-                    help="print the Softmax and LayerNorm band tables an --ops-bands run implies")
+    ap.add_argument("--ops-bands-record", nargs="+", metavar="JSONL",
+                    help="print the JSON record of one or more --ops-bands runs (the data the "
+                         "Softmax and LayerNorm band tables are derived from)")
+    ap.add_argument("--ops-bands-derive", metavar="JSON",
+                    help="print the Softmax and LayerNorm band tables an --ops-bands-record "
+                         "record implies")
     ap.add_argument("--plan-bands-record", nargs="+", metavar="JSONL",
                     help="print the JSON record of one or more --plan-contexts runs (the data the "
                          "RMSNorm band table is derived from)")
@@ -1907,13 +1967,13 @@ def main() -> int:
     if args.ops_bands_table:
         print(ops_bands_table(args.ops_bands_table))
         return 0
+    if args.ops_bands_record:
+        print(json.dumps(ops_bands_record(args.ops_bands_record), separators=(",", ":")))
+        return 0
     if args.ops_bands_derive:
-        for name, op, dts in (("kSoftmax16", "softmax", ["bf16", "fp16"]),
-                              ("kSoftmax32", "softmax", ["fp32"]),
-                              ("kLayerNormBf16", "layer_norm", ["bf16"]),
-                              ("kLayerNormF16", "layer_norm", ["fp16"]),
-                              ("kLayerNormF32", "layer_norm", ["fp32"])):
-            print(bands_cpp(name, derive_bands(args.ops_bands_derive, op, dts)))
+        rec = json.load(open(args.ops_bands_derive))
+        for name, op, dts in OPS_BAND_TABLES:
+            print(bands_cpp(name, derive_bands(rec, op, dts)))
         return 0
     if args.kernel_times_table:
         print(kernel_times_table(*args.kernel_times_table))

@@ -418,7 +418,7 @@ namespace {
 // shared-memory carveout), a plan's score is the worse of the two, and the tables are the fewest
 // bands such that at every measured width the band's launch scores within a point of the copy
 // peak of the best launch there (bench.py --plan-bands-record / --plan-bands-derive; the
-// measured record is committed beside the kernel profiles, and a CPU test re-derives the tables
+// measured record is committed in bands/ beside this file, and a CPU test re-derives the tables
 // from it and checks every default plan against it).
 struct RowBand {
     int32_t hi;     // the band's widest row, in 16-byte vectors

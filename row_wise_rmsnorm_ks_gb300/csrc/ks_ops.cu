@@ -915,6 +915,7 @@ __global__ void __launch_bounds__(512) layer_norm_wide_kernel(void *out, const v
 // ------------------------------------------------------------------------ launch planning
 
 int g_sm_count[64];
+int g_l2_bytes[64];  // 0 when the query failed
 std::once_flag g_sm_once[64];
 
 // Per-device launch facts, cached: without the cache every launch would repeat the same
@@ -976,6 +977,10 @@ ks_status_t sm_count(int *out) {
     cudaError_t err = cudaSuccess;
     std::call_once(g_sm_once[dev], [&] {
         err = cudaDeviceGetAttribute(&g_sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (cudaDeviceGetAttribute(&g_l2_bytes[dev], cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
+            g_l2_bytes[dev] = 0;
+            (void)cudaGetLastError();
+        }
     });
     if (err != cudaSuccess || g_sm_count[dev] <= 0)
         return fail(KS_ERR_CUDA, "querying the SM count failed");
@@ -1010,10 +1015,19 @@ int wide_row_block(int64_t hv, bool layer_norm) {
     return 512;
 }
 
+// The L2 size of the current device as sm_count() cached it (0 when unknown).
+int64_t device_l2_bytes() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    return g_l2_bytes[dev];
+}
+
 // The wide kernels re-read each row from L2: no more CTAs than keep their rows in flight within
-// 96 MiB of it, but at least one per SM (as for the two-pass RMSNorm kernel).
+// three quarters of it (of a GB300's 128 MiB when the size is unknown), but at least one per SM
+// (as for the two-pass RMSNorm kernel).
 int64_t wide_grid_cap(int64_t hv, int sms) {
-    const int64_t cap = (96ll << 20) / (hv * 16);
+    const int64_t l2 = device_l2_bytes();
+    const int64_t cap = (l2 > 0 ? l2 : (128ll << 20)) / 4 * 3 / (hv * 16);
     return cap < sms ? sms : cap;
 }
 
@@ -1082,43 +1096,64 @@ ks_plan_t silu_plan(bool vec, int64_t dv, ks_dtype_t dtype) {
     return op_plan_of(KS_KERNEL_FLAT, 2, 128, true);
 }
 
-// Width bands for many rows (more rows than SMs) of at most 256 vectors: rows up to `hi` vectors
+// Width bands for many rows (more rows than SMs) of up to 4096 vectors: rows up to `hi` vectors
 // take a team of `team` lanes per row at `v` vectors per lane (kind 'w'; 8- and 16-lane teams put
-// 4 or 2 rows in a warp), a CTA per row at `v` vectors (kind 'c'), or the general rule (kind
-// 'g'); `prefetch` as the name says. The tables are printed by
-//   python bench.py --ops-bands-derive <the JSON lines of bench.py --ops-bands>
-// from a GB300 run of --ops-bands over 8..256 vectors: at each width every candidate is scored by
-// the worse of two contexts (steady, and right after a kernel with a large shared-memory
-// carveout) and by its worst dtype among those that share the table; the previous plan is kept
-// unless another scores a point of the copy peak higher. Warp rows reduce with shuffles alone and
-// fill their lanes, where a CTA per row of 33..64 threads, most of them idle, paid two CTA
-// barriers per row; sub-warp teams took rows of 8..56 vectors from 0.18-0.90 to 0.68-0.96 (e.g.
-// Softmax bf16 16 vectors 0.42 -> 0.94, LayerNorm fp16 32 vectors 0.60 -> 0.94).
+// 4 or 2 rows in a warp), a CTA per row at `v` vectors (kind 'c'), the LayerNorm staged ring of
+// `v` rows per CTA (kind 'r'), the wide multi-pass kernel on `block` threads (kind 'x'), or the
+// general rule (kind 'g'); `prefetch` as the name says. The tables are generated, not edited:
+//   python bench.py --ops-bands-record <JSON lines of bench.py --ops-bands> > record.json
+//   python bench.py --ops-bands-derive record.json
+// from GB300 runs of --ops-bands (8..256 and 288..4096 vectors; the record is committed as
+// bands/softmax_layer_norm_bands.json beside this file, and a CPU test re-derives the tables
+// from it): at each width every
+// candidate is scored by the worse of two contexts (steady, and right after a kernel with a
+// large shared-memory carveout) and by its worst dtype among those that share the table; the
+// previous plan is kept unless another scores a point of the copy peak higher. Warp rows reduce
+// with shuffles alone and fill their lanes, where a CTA per row of 33..64 threads, most of them
+// idle, paid two CTA barriers per row; sub-warp teams took rows of 8..56 vectors from 0.18-0.90
+// to 0.68-0.96 (e.g. Softmax bf16 16 vectors 0.42 -> 0.94, LayerNorm fp16 32 vectors 0.60 ->
+// 0.94). Past 256 vectors the ring took bf16 LayerNorm rows of 257..512 vectors (0.66-0.87 ->
+// 0.73-0.95) and fp32 rows at several widths (e.g. 1152 vectors 0.80 -> 0.93).
 struct Band {
     int16_t hi;
     char kind;
-    int8_t v;
+    int8_t v;            // vectors per lane or thread; for an 'r' band, the ring's stages
     bool prefetch;
-    int8_t team = 32;  // lanes per row of a 'w' band
+    int8_t team = 32;    // lanes per row of a 'w' band
+    int16_t block = 0;   // threads per CTA of an 'x' band
 };
 
 constexpr int16_t kBandEnd = 32767;
-constexpr Band kSoftmax16[] = {{16, 'w', 2, true, 8}, {20, 'w', 4, false, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {45, 'w', 4, false, 16}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {112, 'w', 4, true}, {127, 'c', 4, false}, {129, 'w', 6, true}, {144, 'w', 6, false}, {169, 'w', 8, true}, {225, 'w', 8, false}, {256, 'g', 0, false}, {kBandEnd, 'g', 0, true}};
-constexpr Band kSoftmax32[] = {{8, 'w', 2, false, 8}, {12, 'w', 2, true, 8}, {20, 'w', 2, false, 16}, {28, 'w', 4, false, 8}, {32, 'w', 2, false}, {33, 'w', 4, false, 16}, {40, 'w', 2, false}, {53, 'w', 4, false, 16}, {56, 'w', 4, false}, {63, 'w', 4, true}, {64, 'g', 0, true}, {65, 'w', 4, false}, {72, 'w', 4, true}, {81, 'w', 6, false}, {96, 'w', 6, true}, {112, 'w', 8, false}, {127, 'c', 4, false}, {128, 'w', 4, false}, {129, 'w', 8, false}, {144, 'w', 8, true}, {168, 'w', 6, false}, {176, 'g', 0, false}, {177, 'c', 4, false}, {192, 'w', 6, false}, {208, 'c', 4, false}, {225, 'c', 4, true}, {256, 'w', 8, false}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormBf16[] = {{16, 'w', 2, true, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {64, 'w', 4, true, 16}, {127, 'w', 4, true}, {192, 'w', 6, true}, {256, 'w', 8, true}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormF16[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {56, 'w', 4, true, 16}, {64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true}, {256, 'g', 0, true}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormF32[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'c', 2, true}, {64, 'w', 4, true, 16}, {112, 'w', 4, true}, {127, 'c', 4, true}, {169, 'w', 6, true}, {225, 'w', 8, true}, {256, 'g', 0, true}, {kBandEnd, 'g', 0, true}};
+constexpr int64_t kRingSmemLimit = 226 * 1024;  // dynamic shared memory a ring CTA may take
+// BEGIN GENERATED OP BANDS
+constexpr Band kSoftmax16[] = {{16, 'w', 2, true, 8}, {20, 'w', 4, false, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {45, 'w', 4, false, 16}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {112, 'w', 4, true}, {127, 'c', 4, false}, {129, 'w', 6, true}, {144, 'w', 6, false}, {169, 'w', 8, true}, {225, 'w', 8, false}, {512, 'g', 0, false}, {576, 'c', 4, true}, {640, 'g', 0, false}, {704, 'c', 4, true}, {768, 'g', 0, false}, {896, 'c', 4, true}, {1024, 'g', 0, false}, {2048, 'g', 0, true}, {2560, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kSoftmax32[] = {{8, 'w', 2, false, 8}, {12, 'w', 2, true, 8}, {20, 'w', 2, false, 16}, {28, 'w', 4, false, 8}, {32, 'w', 2, false}, {33, 'w', 4, false, 16}, {40, 'w', 2, false}, {53, 'w', 4, false, 16}, {56, 'w', 4, false}, {63, 'w', 4, true}, {64, 'g', 0, true}, {65, 'w', 4, false}, {72, 'w', 4, true}, {81, 'w', 6, false}, {96, 'w', 6, true}, {112, 'w', 8, false}, {127, 'c', 4, false}, {128, 'w', 4, false}, {129, 'w', 8, false}, {144, 'w', 8, true}, {168, 'w', 6, false}, {176, 'g', 0, false}, {177, 'c', 4, false}, {192, 'w', 6, false}, {208, 'c', 4, false}, {225, 'c', 4, true}, {256, 'w', 8, false}, {288, 'g', 0, false}, {320, 'c', 2, true}, {448, 'c', 4, true}, {512, 'c', 2, true}, {576, 'g', 0, false}, {640, 'c', 4, true}, {704, 'g', 0, false}, {768, 'c', 4, true}, {896, 'g', 0, false}, {1024, 'c', 4, true}, {1536, 'c', 4, false}, {1792, 'g', 0, true}, {2048, 'c', 4, false}, {2560, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormBf16[] = {{16, 'w', 2, true, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {64, 'w', 4, true, 16}, {127, 'w', 4, true}, {192, 'w', 6, true}, {256, 'w', 8, true}, {384, 'r', 2, true}, {448, 'r', 4, true}, {576, 'r', 2, true}, {640, 'r', 6, true}, {768, 'r', 5, true}, {1024, 'r', 4, true}, {1792, 'x', 4, true, 32, 128}, {2048, 'r', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF16[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {56, 'w', 4, true, 16}, {64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true}, {448, 'g', 0, true}, {512, 'r', 3, true}, {576, 'c', 4, true}, {640, 'r', 6, true}, {896, 'c', 4, true}, {1024, 'r', 4, true}, {1792, 'x', 4, true, 32, 128}, {2048, 'c', 4, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF32[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'c', 2, true}, {64, 'w', 4, true, 16}, {112, 'w', 4, true}, {127, 'c', 4, true}, {169, 'w', 6, true}, {225, 'w', 8, true}, {256, 'g', 0, true}, {288, 'r', 2, true}, {320, 'c', 2, true}, {512, 'g', 0, true}, {576, 'r', 2, true}, {640, 'c', 4, true}, {704, 'r', 6, true}, {768, 'c', 4, true}, {1024, 'x', 4, true, 32, 128}, {1152, 'r', 3, true}, {1408, 'r', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+// END GENERATED OP BANDS
 
 // Applies the band of a row of hv vectors to p (the general rule's plan) when there are more rows
-// than SMs; warp plans take 128-thread CTAs (4 rows each).
+// than SMs; warp plans take 128-thread CTAs (4 rows each). The staged ring ('r') and the wide
+// kernel ('x') were measured with many rows: on rows a register kernel can hold (at most 2048
+// vectors) they apply only with at least 4 rows per SM, as the general rule's do.
 void apply_band(const Band *bands, int64_t hv, int64_t rows, int sms, ks_plan_t *p) {
-    if (rows <= sms || hv > 256) return;
+    if (rows <= sms) return;
     const Band *b = bands;
     while (hv > b->hi) ++b;
-    if (b->kind == 'w')
+    const bool many = rows >= 4 * (int64_t)sms;
+    const int64_t ring_block = round_up64(ceil_div64(hv, 4), 32);
+    if (b->kind == 'w') {
         *p = op_plan_of(KS_KERNEL_WARP_ROW, b->v, 128, b->prefetch, 0, b->team);
-    else if (b->kind == 'c')
-        *p = op_plan_of(KS_KERNEL_CTA_ROW, b->v, (int)round_up64(ceil_div64(hv, b->v), 32), b->prefetch);
+    } else if (b->kind == 'c') {
+        const int64_t block = round_up64(ceil_div64(hv, b->v), 32);
+        if (block <= 512) *p = op_plan_of(KS_KERNEL_CTA_ROW, b->v, (int)block, b->prefetch);
+    } else if (b->kind == 'r') {
+        if (many && ring_block <= 512 && 128 + (int64_t)b->v * hv * 16 <= kRingSmemLimit)
+            *p = op_plan_of(KS_KERNEL_BULK_ROW, 4, (int)ring_block, true, b->v);
+    } else if (b->kind == 'x') {
+        if (many || hv > 2048) *p = op_plan_of(KS_KERNEL_TWOPASS_ROW, 4, b->block, true);
+    }
 }
 
 // Softmax: rows of up to 512 threads x V vectors in registers (V from row_vec_plan; at 4 vectors
@@ -1159,8 +1194,6 @@ ks_plan_t layer_norm_plan(bool aligned, int64_t hv, int64_t hidden, int64_t rows
     const int v = row_vec_plan(hv, &block);
     ks_plan_t p = v == 0 ? op_plan_of(KS_KERNEL_TWOPASS_ROW, 4, wide_row_block(hv, true), true)
                          : op_plan_of(KS_KERNEL_CTA_ROW, v, block, true);
-    apply_band(dtype == KS_DTYPE_BF16 ? kLayerNormBf16
-               : dtype == KS_DTYPE_F16 ? kLayerNormF16 : kLayerNormF32, hv, rows, sms, &p);
     if (p.kernel == KS_KERNEL_CTA_ROW && v == 4 && hv > 512 && rows >= 4 * (int64_t)sms) {
         if (hv < 2048 && hv >= (dtype == KS_DTYPE_F32 ? 1024 : 1025)) {
             p = op_plan_of(KS_KERNEL_TWOPASS_ROW, 4, 128, true);
@@ -1169,6 +1202,8 @@ ks_plan_t layer_norm_plan(bool aligned, int64_t hv, int64_t hidden, int64_t rows
             p = op_plan_of(KS_KERNEL_BULK_ROW, 4, block, true, (int)(n < 2 ? 2 : (n > 8 ? 8 : n)));
         }
     }
+    apply_band(dtype == KS_DTYPE_BF16 ? kLayerNormBf16
+               : dtype == KS_DTYPE_F16 ? kLayerNormF16 : kLayerNormF32, hv, rows, sms, &p);
     return p;
 }
 
@@ -1224,7 +1259,7 @@ ks_status_t op_check(int op, ks_plan_t &p, bool vec, int64_t width, int64_t elem
         if (!ln) return fail(KS_ERR_INVALID_ARGUMENT, "the staged ring is LayerNorm's");
         if (p.vec_per_thread != 4 || (int64_t)p.block * 4 < width || p.block > 512)
             return fail(KS_ERR_INVALID_ARGUMENT, "ring plan: 4 vectors per thread covering the row, block <= 512");
-        if (p.stages < 2 || p.stages > 8 || ln_ring_smem(p.stages, width) > 226 * 1024)
+        if (p.stages < 2 || p.stages > 8 || (int64_t)ln_ring_smem(p.stages, width) > kRingSmemLimit)
             return fail(KS_ERR_INVALID_ARGUMENT, "ring of %d stages does not fit", p.stages);
         p.smem_bytes = (int32_t)ln_ring_smem(p.stages, width);
         break;

@@ -288,6 +288,50 @@ def test_layer_norm_at_plan_band_edges(cuda_device, dtype, hv, affine):
     _ln_check(y, ref, dt, h, f"layer_norm band {dtype} [1001,{h}] affine={affine}")
 
 
+def _wide_band_edges():
+    """(op, dtype, hv) at every edge of the Softmax and LayerNorm width bands past 256 vectors
+    (each band's last width and the next), from the committed measured record the band tables
+    are generated from."""
+    import json
+    import os
+
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "row_wise_rmsnorm_ks_gb300", "csrc", "bands",
+                           "softmax_layer_norm_bands.json")) as f:
+        rec = json.load(f)
+    out = set()
+    for _, op, dts in bench.OPS_BAND_TABLES:
+        bands = bench.derive_bands(rec, op, dts)
+        for hi, *_ in bands[:-1]:
+            if hi >= 256:
+                for dt in dts:
+                    out |= {(op, dt, hi), (op, dt, hi + 1)}
+    return sorted(out)
+
+
+@pytest.mark.parametrize("op,dtype,hv", _wide_band_edges())
+def test_wide_band_edges(cuda_device, op, dtype, hv):
+    """Many rows (1001: at least 4 per SM, so the ring and wide-kernel bands apply) at each edge of
+    the bands past 256 vectors; LayerNorm with weight and bias and a constant row."""
+    dt = synth.dtype_of(dtype)
+    h = _elems(dt, hv)
+    if op == "softmax":
+        x = synth.cast(synth.normal_np((1001, h), 814, std=3.0), dt)
+        y = ks.softmax(x.to(cuda_device)).cpu()
+        ref, _ = oracle.softmax(x)
+        compare_output(y, ref, dt, h, f"softmax wide band edge {dtype} hv={hv}")
+    else:
+        x = synth.cast(synth.normal_np((1001, h), 815) + 0.25, dt)
+        x[9] = 0.75  # a constant row
+        w, b = _affine("both", h, dt, 816)
+        y = ks.layer_norm(x.to(cuda_device), _dev(w, cuda_device), _dev(b, cuda_device), 1e-5).cpu()
+        ref, _ = oracle.layer_norm(x, w, b, 1e-5)
+        _ln_check(y, ref, dt, h, f"layer_norm wide band edge {dtype} hv={hv}")
+    st, flags = _abi.ks_device_faults(clear=False)
+    assert st == _abi.KS_SUCCESS and flags == 0
+
+
 @pytest.mark.parametrize("dtype", DT)
 @pytest.mark.parametrize("dv", [16, 31, 32, 33, 64, 96, 128, 159, 160, 161, 191, 192, 193, 256, 287,
                                 288, 447, 448, 512, 576, 640, 1024, 1280, 2048])

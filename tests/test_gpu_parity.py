@@ -120,7 +120,8 @@ def _band_edges():
 
     import bench
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    with open(os.path.join(root, "profiles", "plan_bands_rms_norm.json")) as f:
+    with open(os.path.join(root, "row_wise_rmsnorm_ks_gb300", "csrc", "bands",
+                           "rms_norm_plan_bands.json")) as f:
         bands = bench.derive_plan_bands(json.load(f))
     out = []
     for key, bl in sorted(bands.items()):

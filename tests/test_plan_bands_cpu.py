@@ -1,7 +1,7 @@
 """The RMSNorm launch heuristic's band table for many rows of 1..2048 16-byte vectors, against the
 measured record it is generated from (no GPU: the plan is host code).
 
-The record (profiles/plan_bands_rms_norm.json) holds, per dtype, op and measured width, the score
+The record (csrc/bands/rms_norm_plan_bands.json) holds, per dtype, op and measured width, the score
 of every launch the table can name (the worse of steady state and right after a large-shared-
 memory kernel, in thousandths of the measured copy peak). The tests check that the library's table
 is exactly what the committed rule derives from it, that the library's default plan at every
@@ -18,7 +18,8 @@ import bench
 from row_wise_rmsnorm_ks_gb300 import _abi
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-RECORD = os.path.join(ROOT, "profiles", "plan_bands_rms_norm.json")
+BANDS = os.path.join(ROOT, "row_wise_rmsnorm_ks_gb300", "csrc", "bands")
+RECORD = os.path.join(BANDS, "rms_norm_plan_bands.json")
 SOURCE = os.path.join(ROOT, "row_wise_rmsnorm_ks_gb300", "csrc", "ks_abi.cu")
 DTYPES = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}
 OPS = {"rms_norm": 0, "fused_add_rms_norm": 1}
@@ -177,3 +178,51 @@ def test_team_rows_spread_over_sms():
             warps = min(8, max(1, -(-rows // (152 * per_warp))))
             assert p.block == 32 * warps
             assert p.grid == -(-rows // (warps * per_warp))
+
+
+def test_next_op_tables_are_the_derivation_of_their_record():
+    """The Softmax and LayerNorm width bands in the library are exactly what the committed rule
+    derives from the committed record of --ops-bands runs."""
+    with open(os.path.join(BANDS, "softmax_layer_norm_bands.json")) as f:
+        rec = json.load(f)
+    src = open(os.path.join(ROOT, "row_wise_rmsnorm_ks_gb300", "csrc", "ks_ops.cu")).read()
+    m = re.search(r"// BEGIN GENERATED OP BANDS\n(.*?)\n// END GENERATED OP BANDS", src, re.S)
+    assert m, "generated block not found"
+    want = "\n".join(bench.bands_cpp(name, bench.derive_bands(rec, op, dts))
+                     for name, op, dts in bench.OPS_BAND_TABLES)
+    assert m.group(1) == want
+
+
+def test_next_op_default_plans_follow_the_record():
+    """At every width the record measured with many rows, the library's default Softmax or
+    LayerNorm plan is the derived band's launch, and scores within 2 points of the measured best
+    in its worst dtype."""
+    with open(os.path.join(BANDS, "softmax_layer_norm_bands.json")) as f:
+        rec = json.load(f)
+    codes = {"softmax": _abi.OP_SOFTMAX, "layer_norm": _abi.OP_LAYER_NORM}
+    for _, op, dts in bench.OPS_BAND_TABLES:
+        bands = bench.derive_bands(rec, op, dts)
+        by_w = {}
+        for ln in rec["lines"]:
+            if ln["op"] == op and ln["dtype"] in dts:
+                by_w.setdefault(ln["hv"], {})[ln["dtype"]] = ln
+        for hv, per in by_w.items():
+            band = next(b for b in bands if hv <= b[0])
+            if band[1] == "g":
+                continue  # the general rule: checked by the plan tests
+            name = {"w": (f"t{band[4]}v{band[2]}" if band[4] != 32 else f"w{band[2]}")
+                         + ("" if band[3] else "n"),
+                    "c": f"c{band[2]}" + ("" if band[3] else "n"),
+                    "r": f"r{band[2]}", "x": f"x{band[5]}"}[band[1]]
+            for dt, ln in per.items():
+                p = _abi.ks_plan_launch(codes[op], 100000, hidden_of(dt, hv), DTYPES[dt], True,
+                                        152, 0)[1]
+                kind = {_abi.KS_KERNEL_WARP_ROW: "w", _abi.KS_KERNEL_CTA_ROW: "c",
+                        _abi.KS_KERNEL_BULK_ROW: "r", _abi.KS_KERNEL_TWOPASS_ROW: "x"}[p.kernel]
+                assert kind == band[1], (op, dt, hv, band, p.as_dict())
+                if all(name in l2["scores"] for l2 in per.values()):
+                    # scored as the rule scores: each candidate by its worst dtype
+                    names = set.intersection(*(set(l2["scores"]) for l2 in per.values()))
+                    best = max(min(l2["scores"][n] for l2 in per.values()) for n in names)
+                    assert min(l2["scores"][name] for l2 in per.values()) >= best - 20, \
+                        (op, hv, name)
