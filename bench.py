@@ -1124,7 +1124,8 @@ def plan_candidates(op: str, hv: int, elem: int):
     least 1024 vectors), both also with a trailing n (no L2 prefetch of the row), sCbBuUp (the
     split kernel with two rows in flight per cluster, no prefetch), and for
     rows wider than 2048 vectors cC (register-resident cluster of C CTAs, 4 vectors per thread)
-    and bCsS (staged ring split over C CTAs, S stages)."""
+    and bCsS / bCsSv8 (the staged kernel split over C CTAs, S stages, 4 or 8 vectors per
+    thread)."""
     from row_wise_rmsnorm_ks_gb300 import _abi
 
     up32 = lambda n: -(-n // 32) * 32
@@ -1175,13 +1176,16 @@ def plan_candidates(op: str, hv: int, elem: int):
         for c in (2, 4, 8):
             sl = -(-hv // c)
             b = up32(-(-sl // 4))
-            if b > 512:
-                continue
-            out.append((f"c{c}", _abi.make_plan(_abi.KS_KERNEL_CLUSTER_ROW, 4, b, cluster=c)))
-            for st in (2, 3):
-                if 128 + st * sl * 16 * (2 if fused else 1) <= 226 * 1024:
-                    out.append((f"b{c}s{st}", _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, b, st,
-                                                             cluster=c)))
+            if b <= 512:
+                out.append((f"c{c}", _abi.make_plan(_abi.KS_KERNEL_CLUSTER_ROW, 4, b, cluster=c)))
+            for vv in ((4,) if fused else (4, 8)):
+                b = up32(-(-sl // vv))
+                if b > 512:
+                    continue
+                for st in (2, 3, 4):
+                    if 128 + st * sl * 16 * (2 if fused else 1) <= 226 * 1024:
+                        out.append((f"b{c}s{st}" + ("v8" if vv == 8 else ""), _abi.make_plan(
+                            _abi.KS_KERNEL_BULK_ROW, vv, b, st, cluster=c)))
     return out
 
 
@@ -1262,6 +1266,54 @@ def run_plan_sweep(args) -> int:
         print(json.dumps({"plan_sweep": "device faults", "status": st, "flags": flags}))
         return 1
     return 0
+
+
+def run_plan_probe(args) -> int:
+    """One plan-sweep candidate (--plan-probe NAME, named as in plan_candidates) launched
+    --probe-launches times through the planned entry point on --rows x --hidden (--probe-dtype,
+    --probe-op), N(0,1) inputs, then one JSON line with the mean event time per launch (not the
+    contract's line). A fixed small workload for a profiler to capture one kernel of."""
+    import torch
+
+    from row_wise_rmsnorm_ks_gb300 import _abi, synth
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    dt, op, R, H = args.probe_dtype, args.probe_op, args.rows, args.hidden
+    elem = 4 if dt == "fp32" else 2
+    code = {"bf16": _abi.KS_DTYPE_BF16, "fp16": _abi.KS_DTYPE_F16, "fp32": _abi.KS_DTYPE_F32}[dt]
+    plans = dict(plan_candidates(op, H * elem // 16, elem))
+    if args.plan_probe not in plans:
+        print(json.dumps({"plan_probe": args.plan_probe, "error": "no such candidate at this width",
+                          "candidates": sorted(plans)}))
+        return 2
+    p = plans[args.plan_probe]
+    x = synth.cast(synth.normal_dev((R, H), synth.SEED_X, dev), dt)
+    w = synth.weight(H, dt).to(dev)
+    y = torch.empty_like(x)
+    r = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev), dt) if op != "rms_norm" else None
+    def launch():
+        if op == "rms_norm":
+            return _abi.ks_rms_norm_planned(y.data_ptr(), x.data_ptr(), w.data_ptr(), R, H, 1e-5,
+                                            code, p, s)
+        return _abi.ks_fused_add_rms_norm_planned(x.data_ptr(), r.data_ptr(), w.data_ptr(), R, H,
+                                                  1e-5, code, p, s)
+    _abi.check(launch())  # untimed: the first launch sets the kernel's attributes up
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.probe_launches):
+        _abi.check(launch())
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / args.probe_launches
+    st, flags = _abi.ks_device_faults(clear=False)
+    nb = algorithmic_bytes(op, R, H, elem)
+    print(json.dumps({"plan_probe": args.plan_probe, "op": op, "dtype": dt, "rows": R, "hidden": H,
+                      "plan": p.as_dict(), "us_per_launch": us,
+                      "frac_of_peak": nb / (us * 1e-6) / 1e9 / measured_peaks()["hbm_gbs"],
+                      "faults": [st, flags]}))
+    return 0 if (st == _abi.KS_SUCCESS and flags == 0) else 1
 
 
 def run_plan_contexts(args) -> int:
@@ -1776,6 +1828,109 @@ def derive_plan_bands(record: dict, tol: int = 10) -> dict:
     return out
 
 
+WIDE_LO, WIDE_HI = 2049, 32768  # the wide band table: many rows, tensors larger than L2
+
+
+def wide_plan_fields(name: str):
+    """(kernel, cluster, block, v, stages, flags) of a plan-sweep candidate name for rows wider
+    than 2048 vectors (block 0: fitted to the slice, ceil(ceil(hv / cluster) / v) rounded up to a
+    warp): tBuU[n] the two-pass kernel, sCbBuU[n|p] split over a cluster (p: two rows in
+    flight), cC the register-resident cluster kernel, bCsS[v8] the staged kernel."""
+    import re
+    from row_wise_rmsnorm_ks_gb300 import _abi
+    npf = _abi.KS_PLAN_NO_PREFETCH
+    m = re.fullmatch(r"t(\d+)u(\d)(n?)", name)
+    if m:
+        return (_abi.KS_KERNEL_TWOPASS_ROW, 0, int(m.group(1)), int(m.group(2)), 0,
+                npf if m.group(3) else 0)
+    m = re.fullmatch(r"s(\d)b(\d+)u(\d)([np]?)", name)
+    if m:
+        return (_abi.KS_KERNEL_TWOPASS_ROW, int(m.group(1)), int(m.group(2)), int(m.group(3)),
+                2 if m.group(4) == "p" else 0, npf if m.group(4) else 0)
+    m = re.fullmatch(r"c(\d)", name)
+    if m:
+        return (_abi.KS_KERNEL_CLUSTER_ROW, int(m.group(1)), 0, 4, 0, 0)
+    m = re.fullmatch(r"b(\d)s(\d)(v8)?", name)
+    if m:
+        return (_abi.KS_KERNEL_BULK_ROW, int(m.group(1)), 0, 8 if m.group(3) else 4,
+                int(m.group(2)), 0)
+    return None
+
+
+def wide_bands_record(log_paths, sm_count: int) -> dict:
+    """The measured record behind the wide band table, from --plan-sweep runs: per dtype, op and
+    width (2049..32768 vectors), the candidates within 5 points of that width's best (thousandths
+    of the measured copy peak; a candidate further behind can never be a band's launch under a
+    one-point rule) and the default's score. A width measured by several runs keeps the mean."""
+    acc = {}
+    for path in log_paths:
+        for ln in open(path):
+            if not ln.startswith('{"plan_sweep"'):
+                continue
+            d = json.loads(ln)
+            if "default" not in d or not (WIDE_LO <= d["hv"] <= WIDE_HI):
+                continue
+            key = (f"{d['plan_sweep']}/{d['op']}", d["hv"])
+            slot = acc.setdefault(key, {"rows": d["rows"], "runs": []})
+            slot["runs"].append({k: v for k, v in d.items() if isinstance(v, float)})
+    tables = {}
+    for (key, hv), slot in sorted(acc.items()):
+        names = set.intersection(*(set(r) for r in slot["runs"]))
+        mean = {n: round(1000 * sum(r[n] for r in slot["runs"]) / len(slot["runs"])) for n in names}
+        best = max(v for n, v in mean.items() if n != "default")
+        keep = {n: v for n, v in mean.items()
+                if n == "default" or (v >= best - 50 and wide_plan_fields(n))}
+        tables.setdefault(key, []).append({"hv": hv, "rows": slot["rows"], "scores": keep})
+    return {"what": "RMSNorm launch-plan scores for many rows of 2049..32768 16-byte vectors, "
+                    "tensors larger than L2",
+            "score": "thousandths of the measured copy peak, back-to-back launches, mean over runs; "
+                     "candidates within 5 points of the best, and the default",
+            "sm_count": sm_count, "runs": len(log_paths), "tables": tables}
+
+
+def derive_wide_bands(record: dict, tol: int = 10) -> dict:
+    """The wide band table a record implies, by the rule of derive_plan_bands: the fewest bands
+    such that at every measured width the band's launch scores within `tol` thousandths of that
+    width's best; each band as wide as the launches common to its widths allow, the launch with
+    the best mean among them; the last band reaching to 32768 vectors. Returns
+    {"dtype/op": [(hi, name)]}."""
+    out = {}
+    for key, lines in record["tables"].items():
+        ok = []
+        for ln in lines:
+            sc = {n: v for n, v in ln["scores"].items() if n != "default"}
+            best = max(sc.values())
+            ok.append({n for n, v in sc.items() if v >= best - tol})
+        bands, i = [], 0
+        while i < len(lines):
+            common, j = set(ok[i]), i
+            while j + 1 < len(lines) and common & ok[j + 1]:
+                common &= ok[j + 1]
+                j += 1
+            mean = lambda n, lo=i, hi=j: sum(lines[k]["scores"][n] for k in range(lo, hi + 1))
+            name = max(sorted(common), key=mean)
+            bands.append((lines[j]["hv"], name))
+            i = j + 1
+        bands[-1] = (WIDE_HI, bands[-1][1])
+        out[key] = bands
+    return out
+
+
+WIDE_BAND_TABLES = (("fp32", "kWideBandsF32"), ("fp16", "kWideBandsF16"), ("bf16", "kWideBandsBf16"))
+
+
+def wide_bands_cpp(bands: dict) -> str:
+    """The wide band table as the library's C++ source: {hi, kernel, cluster, block (0: fitted),
+    vectors per thread, stages, flags}, one array per dtype and op."""
+    lines = []
+    for dt, name in WIDE_BAND_TABLES:
+        for op, suffix in (("rms_norm", "Plain"), ("fused_add_rms_norm", "Fused")):
+            body = ", ".join("{%d, %d, %d, %d, %d, %d, %d}" % ((hi,) + wide_plan_fields(n))
+                             for hi, n in bands[f"{dt}/{op}"])
+            lines.append(f"constexpr WideBand {name}{suffix}[] = {{{body}}};")
+    return "\n".join(lines)
+
+
 PLAN_BAND_TABLES = (("fp32", "kRowBandsF32"), ("fp16", "kRowBandsF16"), ("bf16", "kRowBandsBf16"))
 
 
@@ -1929,6 +2084,17 @@ def main() -> int:
                     help="print the RMSNorm band table a --plan-bands-record record implies")
     ap.add_argument("--plan-bands-table", metavar="JSON",
                     help="print the markdown table of a --plan-bands-record record")
+    ap.add_argument("--plan-probe", metavar="NAME",
+                    help="launch one plan-sweep candidate a few times on --rows x --hidden and exit "
+                         "(a fixed workload for a profiler)")
+    ap.add_argument("--probe-launches", type=int, default=4)
+    ap.add_argument("--probe-dtype", default="bf16", choices=["bf16", "fp16", "fp32"])
+    ap.add_argument("--probe-op", default="rms_norm", choices=["rms_norm", "fused_add_rms_norm"])
+    ap.add_argument("--wide-bands-record", nargs="+", metavar="LOG",
+                    help="print the JSON record of one or more --plan-sweep runs over rows wider "
+                         "than 2048 vectors (the data the wide band table is derived from)")
+    ap.add_argument("--wide-bands-derive", metavar="JSON",
+                    help="print the wide band table a --wide-bands-record record implies")
     ap.add_argument("--record-sm-count", type=int, default=0,
                     help="the SM count of the box the runs were taken on (default: this GPU's)")
     ap.add_argument("--kernel-times", action="store_true",
@@ -1985,6 +2151,16 @@ def main() -> int:
             sms = device_facts(torch.device("cuda", 0))["sm_count"]
         print(json.dumps(plan_bands_record(args.plan_bands_record, sms), separators=(",", ":")))
         return 0
+    if args.wide_bands_record:
+        sms = args.record_sm_count
+        if sms <= 0:
+            import torch
+            sms = device_facts(torch.device("cuda", 0))["sm_count"]
+        print(json.dumps(wide_bands_record(args.wide_bands_record, sms), separators=(",", ":")))
+        return 0
+    if args.wide_bands_derive:
+        print(wide_bands_cpp(derive_wide_bands(json.load(open(args.wide_bands_derive)))))
+        return 0
     if args.plan_bands_derive:
         print(plan_bands_cpp(derive_plan_bands(json.load(open(args.plan_bands_derive)))))
         return 0
@@ -1995,6 +2171,8 @@ def main() -> int:
         return run_plan_sweep(args)
     if args.plan_contexts:
         return run_plan_contexts(args)
+    if args.plan_probe:
+        return run_plan_probe(args)
     if args.ops_scan:
         return run_ops_scan(args)
     return run_ks(args)

@@ -124,8 +124,8 @@ typedef struct ks_plan {
     int32_t kernel;         /* KS_KERNEL_* below */
     int32_t vec_per_thread; /* 16-byte vectors per thread and tensor (vector kernels): warp
                                rows 1, 2, 4, 6 or 8 (teams of 8 or 16 lanes: 1, 2 or 4); CTA
-                               rows 2 or 4; staged rows 4; cluster rows 1, 2 or 4; two-pass 2
-                               or 4 per step */
+                               rows 2 or 4; staged rows 4 (split over a cluster, also 8 for the
+                               plain op); cluster rows 1, 2 or 4; two-pass 2 or 4 per step */
     int32_t team;           /* threads per row: for warp rows 8, 16 or 32 lanes (several rows
                                per warp below 32; an explicit plan's 0 means 32), else block
                                (CTA per row) or block * cluster */
@@ -157,8 +157,9 @@ enum {
                                bulk asynchronous copies, 4 vectors per thread; with cluster >= 2
                                the row is split over a cluster, each CTA streaming its slice of
                                ceil(hv / cluster) vectors through its own ring, partial sums
-                               exchanged in distributed shared memory (rows too wide for one
-                               CTA's registers) */
+                               sent to every CTA of the cluster by asynchronous shared-memory
+                               stores that complete on the receiver's mbarrier (rows too wide
+                               for one CTA's registers) */
     KS_KERNEL_CLUSTER_ROW = 5, /* one cluster of `cluster` CTAs per row (few wide rows): each CTA
                                   holds a slice in registers and reduces it, partials exchanged
                                   in distributed shared memory */

@@ -155,7 +155,9 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
     case KS_KERNEL_BULK_ROW: {
         if (!vec_ok) return fail(KS_ERR_INVALID_ARGUMENT, "vector kernel needs 16-byte rows and pointers");
         const bool bulk = p.kernel == KS_KERNEL_BULK_ROW;
-        if (bulk ? p.vec_per_thread != 4 : (p.vec_per_thread != 2 && p.vec_per_thread != 4))
+        // the staged ring: 4 vectors per thread; split over a cluster, also 8 for the plain op
+        const bool bulk_v = p.vec_per_thread == 4 || (split_bulk && !fused && p.vec_per_thread == 8);
+        if (bulk ? !bulk_v : (p.vec_per_thread != 2 && p.vec_per_thread != 4))
             return fail(KS_ERR_INVALID_ARGUMENT, "unsupported vectors per thread %d", p.vec_per_thread);
         if (split_bulk && p.cluster > 8)
             return fail(KS_ERR_INVALID_ARGUMENT, "cluster of %d CTAs (2..8 supported)", p.cluster);
@@ -575,6 +577,90 @@ void split_row(ks_plan_t *p, int64_t hv, bool fused) {
     p->stages = fused ? 2 : 0;
 }
 
+// Many rows wider than 2048 vectors whose tensors exceed L2: one band table per dtype and op,
+// generated from a plan sweep on GB300 (384 MiB per tensor, every launch timed back to back) by
+// the rule of the narrow tables (the fewest bands within a point of each measured width's best),
+// over the one-CTA two-pass kernel, the two-pass kernel split over a cluster, the
+// register-resident cluster kernel and the staged kernel split over a cluster. A band names a
+// full launch: kernel, CTAs per cluster (0: one CTA per row), block (0: fitted to the slice,
+// ceil(ceil(hv / cluster) / v) rounded up to a warp), vectors per thread (per step), stages and
+// flags (bench.py --wide-bands-record / --wide-bands-derive; the measured record is committed in
+// bands/ beside this file, and a CPU test re-derives the tables from it).
+struct WideBand {
+    int32_t hi;
+    int8_t kernel;
+    int8_t cluster;
+    int16_t block;
+    int8_t v;
+    int8_t stages;
+    int8_t flags;
+};
+constexpr int64_t kWideLo = 2049, kWideHi = 32768;
+// BEGIN GENERATED WIDE BANDS
+constexpr WideBand kWideBandsF32Plain[] = {{2560, 6, 0, 256, 4, 0, 1}, {2816, 6, 0, 512, 4, 0, 0}, {3584, 6, 0, 512, 4, 0, 1}, {4096, 4, 2, 0, 8, 4, 0}, {4608, 4, 2, 0, 8, 3, 0}, {7168, 6, 0, 512, 4, 0, 1}, {9216, 4, 4, 0, 8, 4, 0}, {10240, 4, 4, 0, 8, 2, 0}, {12288, 4, 8, 0, 4, 2, 0}, {32768, 4, 8, 0, 8, 2, 0}};
+constexpr WideBand kWideBandsF32Fused[] = {{2816, 4, 2, 0, 4, 2, 0}, {4096, 6, 0, 512, 2, 0, 1}, {6144, 4, 4, 0, 4, 2, 0}, {8192, 4, 8, 0, 4, 2, 0}, {16384, 4, 8, 0, 4, 3, 0}, {28672, 6, 8, 512, 2, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
+constexpr WideBand kWideBandsF16Plain[] = {{2304, 4, 4, 0, 8, 2, 0}, {3072, 6, 0, 256, 4, 0, 1}, {4096, 6, 0, 512, 4, 0, 0}, {5120, 6, 0, 512, 2, 0, 0}, {7168, 4, 2, 0, 8, 2, 0}, {8192, 4, 4, 0, 4, 2, 0}, {14336, 4, 8, 0, 8, 2, 0}, {16384, 4, 4, 0, 8, 2, 0}, {20480, 6, 4, 256, 4, 2, 1}, {28672, 6, 8, 256, 4, 0, 0}, {32768, 4, 8, 0, 8, 2, 0}};
+constexpr WideBand kWideBandsF16Fused[] = {{2560, 6, 0, 512, 2, 0, 1}, {3072, 4, 2, 0, 4, 2, 0}, {4608, 6, 0, 512, 2, 0, 1}, {5120, 6, 0, 1024, 2, 0, 0}, {7168, 4, 4, 0, 4, 3, 0}, {8192, 4, 8, 0, 4, 3, 0}, {10240, 6, 2, 512, 2, 0, 1}, {14336, 6, 4, 512, 2, 2, 1}, {16384, 4, 8, 0, 4, 2, 0}, {28672, 6, 8, 512, 2, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
+constexpr WideBand kWideBandsBf16Plain[] = {{2304, 6, 0, 512, 2, 0, 0}, {2560, 4, 2, 0, 8, 4, 0}, {3072, 6, 0, 256, 4, 0, 1}, {3584, 6, 0, 512, 4, 0, 0}, {4096, 6, 0, 512, 2, 0, 1}, {4608, 6, 0, 512, 4, 0, 0}, {5120, 4, 4, 0, 8, 4, 0}, {8192, 4, 4, 0, 4, 2, 0}, {9216, 4, 8, 0, 8, 2, 0}, {10240, 4, 8, 0, 8, 4, 0}, {14336, 4, 4, 0, 8, 2, 0}, {16384, 4, 8, 0, 4, 2, 0}, {20480, 6, 4, 512, 2, 0, 0}, {28672, 6, 8, 256, 4, 0, 0}, {32768, 4, 8, 0, 8, 2, 0}};
+constexpr WideBand kWideBandsBf16Fused[] = {{2304, 4, 8, 0, 4, 2, 0}, {2816, 4, 2, 0, 4, 2, 0}, {3072, 6, 0, 512, 2, 0, 1}, {4608, 4, 8, 0, 4, 2, 0}, {5120, 4, 8, 0, 4, 4, 0}, {7168, 4, 4, 0, 4, 2, 0}, {14336, 6, 4, 512, 2, 2, 1}, {16384, 4, 8, 0, 4, 3, 0}, {28672, 6, 8, 512, 2, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
+// END GENERATED WIDE BANDS
+
+// Whether a wide table is well formed: widths rising to kWideHi, kernels that take rows this
+// wide, clusters of 2..8 CTAs where the kernel splits rows.
+template <size_t N>
+constexpr bool wide_bands_ok(const WideBand (&b)[N]) {
+    for (size_t i = 0; i < N; ++i) {
+        if (b[i].hi < kWideLo || b[i].hi > kWideHi || (i > 0 && b[i].hi <= b[i - 1].hi)) return false;
+        const int k = b[i].kernel, c = b[i].cluster;
+        const bool split = k == KS_KERNEL_BULK_ROW || k == KS_KERNEL_CLUSTER_ROW ||
+                           (k == KS_KERNEL_TWOPASS_ROW && c != 0);
+        if (k != KS_KERNEL_TWOPASS_ROW && k != KS_KERNEL_BULK_ROW && k != KS_KERNEL_CLUSTER_ROW)
+            return false;
+        if (split && (c < 2 || c > 8)) return false;
+        if (k == KS_KERNEL_TWOPASS_ROW && (b[i].block <= 0 || (b[i].v != 2 && b[i].v != 4))) return false;
+        if (k == KS_KERNEL_BULK_ROW && (b[i].block != 0 || b[i].stages < 1 || (b[i].v != 4 && b[i].v != 8)))
+            return false;
+    }
+    return b[N - 1].hi == kWideHi;
+}
+static_assert(wide_bands_ok(kWideBandsF32Plain) && wide_bands_ok(kWideBandsF32Fused) &&
+                  wide_bands_ok(kWideBandsF16Plain) && wide_bands_ok(kWideBandsF16Fused) &&
+                  wide_bands_ok(kWideBandsBf16Plain) && wide_bands_ok(kWideBandsBf16Fused),
+              "a wide band table is malformed");
+// Indexed [dtype code][op].
+const WideBand *const kWideBands[3][2] = {
+    {kWideBandsF32Plain, kWideBandsF32Fused},
+    {kWideBandsF16Plain, kWideBandsF16Fused},
+    {kWideBandsBf16Plain, kWideBandsBf16Fused},
+};
+
+// The wide band plan for a row of hv (2049..32768) vectors. Returns false when the band's launch
+// does not fit this width (a fitted block over 512 threads or a ring over the shared-memory
+// limit), and the caller keeps the general rules.
+bool wide_band_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
+    const WideBand *b = kWideBands[(int)dtype][fused ? 1 : 0];
+    while (hv > b->hi) ++b;
+    const int C = b->cluster;
+    const int64_t slice = C >= 2 ? ceil_div(hv, C) : hv;
+    if (C >= 2 && (C - 1) * slice >= hv) return false;  // a CTA without vectors
+    int64_t block = b->block;
+    if (block == 0) block = round_up(ceil_div(slice, b->v), 32);
+    if (block > (b->kernel == KS_KERNEL_TWOPASS_ROW ? 1024 : 512)) return false;
+    if (b->kernel == KS_KERNEL_BULK_ROW) {
+        const int64_t smem = kRingHeader + (int64_t)b->stages * slice * 16 * (fused ? 2 : 1);
+        if (smem > kSmemLimit || (fused && b->v != 4)) return false;
+        p->smem_bytes = (int32_t)smem;
+    }
+    p->kernel = b->kernel;
+    p->cluster = C;
+    p->block = (int32_t)block;
+    p->vec_per_thread = b->v;
+    p->stages = b->stages;
+    p->flags = b->flags;
+    p->team = p->block * (C >= 2 ? C : 1);
+    return true;
+}
+
 }  // namespace
 
 ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool aligned16,
@@ -629,6 +715,10 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         p->vec_per_thread = slice <= 512 ? 1 : (slice <= 1024 ? 2 : 4);
         p->block = (int32_t)round_up(ceil_div(slice, p->vec_per_thread), 32);
         p->team = p->block * 8;
+    } else if (vec_ok && hv <= kWideHi && rows >= 4 * (int64_t)sm_count &&
+               rows * hv * 32 > (l2_bytes > 0 ? l2_bytes : kDefaultL2Bytes) &&
+               wide_band_row(p, hv, fused, dtype)) {
+        // Many wide rows past L2: the measured wide band table.
     } else if (vec_ok && (hv > 8192 || (fused && hv > 4096)) &&
                rows * hv * 32 > (l2_bytes > 0 ? l2_bytes : kDefaultL2Bytes)) {
         // Very wide rows, more than L2 holds: the two-pass kernel split over a cluster. (Rows that
@@ -651,6 +741,8 @@ ks_status_t plan(int op, int64_t rows, int64_t hidden, ks_dtype_t dtype, bool al
         if (blocks_per_sm > 0 && clusters > cap) clusters = cap < 1 ? 1 : cap;
         if (p->kernel == KS_KERNEL_TWOPASS_ROW)
             clusters = split_clusters(rows, clusters, hv, fused, p->stages == 2 ? 2 : 1, l2_bytes);
+        else  // as few clusters as give every cluster the same number of rows
+            clusters = ceil_div(rows, ceil_div(rows, clusters));
         p->grid = clusters * p->cluster;
         p->rows_per_pass = clusters;
         return KS_SUCCESS;

@@ -1161,6 +1161,183 @@ __global__ void __launch_bounds__(512) rows_cluster_kernel(const RowArgs a) {
     cluster.sync();  // peers may still be reading this CTA's partials
 }
 
+// Rows too wide for one CTA, staged through shared memory: each row split over a cluster of C
+// CTAs, CTA q's slice of ceil(hv / C) vectors streamed from global memory by bulk asynchronous
+// copies (one issuing thread, L2 evict-first, completing on the stage's mbarrier) into a ring of
+// `stages` shared-memory stages, so up to `stages` rows per CTA are in flight and the DRAM reads
+// do not wait for the SM. Every thread copies its V vectors of a stage into registers (the
+// fused op forms s = x + r there and writes the residual), so the stage is free after the row's
+// CTA barrier and is refilled at once with the row `stages` iterations ahead.
+// The slice sums meet without a cluster barrier: each CTA sends its sum (and a time-out flag)
+// to every CTA of the cluster with an asynchronous shared-memory store that completes as
+// transaction bytes on the receiver's mbarrier for the row, and each CTA waits on its own
+// barrier for C of them. (A cluster barrier's arrive has release semantics: every thread first
+// waits for its previous row's global stores to be acknowledged, which ncu showed as the top
+// stall.) Two barriers and slots alternate by row: a CTA sends row j + 2's sum only after it
+// has received every peer's row j + 1 sum, which each peer sends only after reading its row j
+// slots. Every wait is bounded. After a time-out (here, or a peer's flag) the CTA records
+// KS_FAULT_WAIT_TIMEOUT and keeps exchanging flags for the remaining rows without touching rows
+// or stages, so every store a peer sends is still awaited before any CTA leaves; then it waits
+// (bounded) for its own copies in flight. Thread 0 tracks the stages with a copy in flight and
+// the parity each completes with.
+template <typename T, int V, bool kFused>
+__global__ void __launch_bounds__(512) rows_stage_split_kernel(const RowArgs a) {
+    namespace cg = cooperative_groups;
+    using E = Elem<T>;
+    constexpr int P = E::kPerVec / 2;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[2][32];
+    __shared__ __align__(8) uint32_t part[2][8][2];  // per row slot: (sum bits, flag) by rank
+    __shared__ __align__(8) uint64_t pbar[2];          // completes when C sums have arrived
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int q = (int)cluster.block_rank();
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *ring = smem + 128;
+    const int g = blockDim.x, t = threadIdx.x;
+    const int64_t hv = a.hv;
+    const int64_t S = (hv + C - 1) / C;
+    const int64_t lo = q * S;
+    const int64_t nv = (lo + S < hv ? lo + S : hv) - lo;  // this CTA's vectors (>= 1)
+    const int stages = a.stages;
+    const uint32_t copy_bytes = (uint32_t)(nv * 16);
+    const uint32_t slot_bytes = (uint32_t)(S * 16);  // the residual's slice follows the x slice
+    const uint32_t stage_bytes = kFused ? 2u * slot_bytes : slot_bytes;
+    const float h = (float)a.hidden;
+    const int64_t first = blockIdx.x / C;
+    const int64_t step = gridDim.x / C;
+    const uint4 *xg = static_cast<const uint4 *>(a.x) + lo;
+    uint4 *og = static_cast<uint4 *>(a.out) + lo;
+    uint4 *rg = kFused ? static_cast<uint4 *>(a.res) + lo : nullptr;
+
+    grid_dependency_wait();
+    allow_dependents_launch();
+    uint4 wv[V];
+    {
+        const uint4 *wg = static_cast<const uint4 *>(a.w) + lo;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            wv[k] = (c < nv) ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    if (t == 0) {
+        for (int i = 0; i < stages; ++i) mbar_init(&bars[i], 1);
+        mbar_init(&pbar[0], 1);
+        mbar_init(&pbar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // every CTA of the cluster has started and set up its barriers before any CTA sends to it
+    cluster.barrier_arrive();
+    cluster.barrier_wait();
+
+    uint64_t policy = 0;
+    uint32_t pending = 0;  // thread 0: stages with a copy in flight
+    uint32_t wphase = 0;   // bit i: the parity stage i's next copy completes with
+    auto issue = [&](int st, int64_t r) {
+        unsigned char *dst = ring + (size_t)st * stage_bytes;
+        mbar_arrive_expect_tx(&bars[st], kFused ? 2u * copy_bytes : copy_bytes);
+        bulk_g2s(dst, xg + r * hv, copy_bytes, &bars[st], policy);
+        if (kFused) bulk_g2s(dst + slot_bytes, rg + r * hv, copy_bytes, &bars[st], policy);
+        pending |= 1u << st;
+    };
+    if (t == 0) {
+        policy = l2_evict_first_policy();
+        for (int i = 0; i < stages; ++i) {
+            const int64_t r = first + (int64_t)i * step;
+            if (r >= a.rows) break;
+            issue(i, r);
+        }
+    }
+
+    int st = 0;
+    uint32_t it = 0;
+    bool fault = false;
+    for (int64_t row = first; row < a.rows; row += step, ++it) {
+        const int p = (int)(it & 1u);
+        bool ok = true;
+        uint4 xv[V], rv[V];
+        PairSumSq<E::kPairMath> acc;
+        if (!fault) {
+            ok = mbar_wait_bounded(&bars[st], (wphase >> st) & 1u);
+            const unsigned char *sx = ring + (size_t)st * stage_bytes;
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const int64_t c = t + (int64_t)k * g;
+                const bool in = ok && c < nv;
+                xv[k] = in ? ld_shared_v4(sx + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+                if (kFused) rv[k] = in ? ld_shared_v4(sx + slot_bytes + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < V; ++k) {
+                const int64_t c = t + (int64_t)k * g;
+                if (ok && c < nv) {
+                    float2 f[P];
+                    row_values<T, kFused>(xv[k], rv[k], f);
+                    if (kFused) __stcs(rg + row * hv + c, E::pack2(f));
+                    acc.add(f);
+                }
+            }
+        }
+        const float wsum = warp_sum(acc.total());
+        if ((t & 31) == 0) red[p][t >> 5] = wsum;
+        // every thread has its stage data in registers: the stage is free
+        const bool bad = __syncthreads_or(!ok || fault);
+        if (!fault && ok) wphase ^= 1u << st;
+        if (t == 0) {
+            if (!fault && ok) pending &= ~(1u << st);
+            const int64_t ahead = row + (int64_t)stages * step;
+            if (!bad && ahead < a.rows) issue(st, ahead);
+            mbar_arrive_expect_tx(&pbar[p], (uint32_t)C * 8u);
+        }
+        if (t < C) {
+            float cta = 0.0f;
+            for (int i = 0; i < (g >> 5); ++i) cta += red[p][i];
+            st_async_v2(cluster_map(&part[p][q][0], (uint32_t)t), __float_as_uint(cta), bad ? 1u : 0u,
+                        cluster_map(&pbar[p], (uint32_t)t));
+        }
+        const bool got = mbar_wait_bounded(&pbar[p], (it >> 1) & 1u);
+        float ss = 0.0f;
+        uint32_t any_bad = got ? 0u : 1u;
+        for (int r = 0; r < C; ++r) {
+            ss += __uint_as_float(part[p][r][0]);
+            any_bad |= part[p][r][1];
+        }
+        // every thread has read this row's slots before any thread's next row (whose sends
+        // into the other slot pair follow this row's barrier anyway)
+        if (__syncthreads_or(any_bad != 0u) || fault) {
+            fault = true;
+            continue;
+        }
+        const float scale = row_scale(ss, h, a.eps);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            opaque(xv[k]);
+            if (kFused) opaque(rv[k]);
+            opaque(wv[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            if (c < nv) {
+                float2 f[P];
+                row_values<T, kFused>(xv[k], rv[k], f);
+                __stcs(og + row * hv + c, scaled_weighted<T>(f, scale, wv[k]));
+            }
+        }
+        if (++st == stages) st = 0;
+    }
+    if (fault && t == 0) {
+        atomicOr(&g_fault_flags, kFaultWaitTimeout);
+        // the copies this CTA issued that have not completed, before its shared memory goes
+        for (int i = 0; i < stages; ++i)
+            if ((pending >> i) & 1u) mbar_wait_bounded(&bars[i], (wphase >> i) & 1u);
+    }
+    cluster.sync();
+}
+
 // ----------------------------------------------------------------------- kernel selection
 
 // Sub-warp team kernels: 8 or 16 lanes per row, V vectors per lane.
@@ -1225,9 +1402,13 @@ const void *pick_kernel(const ks_plan_t &p) {
         default: return nullptr;
         }
     case KS_KERNEL_BULK_ROW:
+        if (p.cluster >= 2) {
+            if (p.vec_per_thread == 4) return (const void *)rows_stage_split_kernel<T, 4, kFused>;
+            if (p.vec_per_thread == 8 && !kFused) return (const void *)rows_stage_split_kernel<T, 8, false>;
+            return nullptr;
+        }
         if (p.vec_per_thread != 4) return nullptr;
-        return p.cluster >= 2 ? (const void *)rows_bulk_kernel<T, 4, kFused, true>
-                              : (const void *)rows_bulk_kernel<T, 4, kFused, false>;
+        return (const void *)rows_bulk_kernel<T, 4, kFused, false>;
     case KS_KERNEL_CLUSTER_ROW:
         switch (p.vec_per_thread) {
         case 1: return (const void *)rows_cluster_kernel<T, 1, kFused>;

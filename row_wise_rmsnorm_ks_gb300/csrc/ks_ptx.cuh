@@ -102,6 +102,22 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// The address of this CTA's shared variable `p` in the shared memory of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+
+// An 8-byte store into a cluster peer's shared memory (addresses from cluster_map) that completes
+// as 8 transaction bytes on the peer's mbarrier `bar`: no fence, no cluster barrier; the peer sees
+// the bytes once its wait on that barrier's phase returns.
+__device__ __forceinline__ void st_async_v2(uint32_t addr, uint32_t a, uint32_t b, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+                 ::"r"(addr), "r"(a), "r"(b), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"

@@ -221,37 +221,23 @@ def test_plan_invariants_over_a_sweep(dtype):
 @pytest.mark.parametrize("hidden,dtype", [(20000, BF16), (32768, BF16), (65536, BF16),
                                           (131072, BF16), (140000, BF16), (12288, F32),
                                           (16384, F32), (32768, F32)])
-def test_rows_wider_than_registers_take_the_two_pass_kernel(hidden, dtype):
+def test_wide_rows_outside_the_band_table(hidden, dtype):
+    """Rows wider than 2048 vectors that the wide band table does not cover (it takes many rows,
+    at least 4 per SM, whose tensors exceed L2; tests/test_plan_bands_cpu.py checks it): rows
+    that fit in L2 take one CTA per row and two passes, with a grid that keeps the rows in flight
+    within L2; three rows take the register-resident cluster kernel."""
     e = 4 if dtype == F32 else 2
     hv = hidden * e // 16
     for op in (0, 1):
-        p = plan(op, 65536, hidden, dtype=dtype, bps=1)
-        assert p.kernel == _abi.KS_KERNEL_TWOPASS_ROW
-        assert p.vec_per_thread == (2 if op else 4)
-        if hv > 8192 or (op and hv > 4096):
-            # many rows of more than 8192 vectors (fused: 4096): split over a cluster of
-            # hv / 4096 CTAs (fused: hv / 2048; 2..8); whole clusters, as many as the SMs hold,
-            # each with the same number of rows; plain rows prefetch each slice to L2, fused rows
-            # keep two rows in flight per cluster
-            c = min(8, max(2, hv // (2048 if op else 4096)))
-            assert p.cluster == c and p.team == p.block * c
-            assert p.block == (512 if op else 256)
-            assert p.flags == (_abi.KS_PLAN_NO_PREFETCH if op else 0)
-            assert p.stages == (2 if op else 0)
-            n = min(152 // c, (96 << 20) // (hv * 16 * (4 if op else 1)))
-            waves = -(-65536 // n)
-            assert p.grid == -(-65536 // waves) * c
+        rows = max(153, (100 << 20) // (hv * 32))  # more rows than SMs, x and y within L2
+        if rows * hv * 32 > (128 << 20):
             continue
-        # many rows: one CTA per row, two passes over the row (the second from L2)
-        assert p.cluster == 0 and p.team == p.block and p.flags == _abi.KS_PLAN_NO_PREFETCH
-        if op:
-            assert p.block == (512 if hv <= 4096 else 1024)
-        else:
-            assert p.block == (256 if hv <= 4096 else 512 if hv <= 8192 else 1024)
+        p = plan(op, rows, hidden, dtype=dtype, bps=1)
+        assert p.kernel == _abi.KS_KERNEL_TWOPASS_ROW and p.cluster == 0
+        assert p.vec_per_thread == (4 if (not op or (dtype == F32 and hv <= 2048)) else 2)
+        assert p.team == p.block and p.flags == _abi.KS_PLAN_NO_PREFETCH
         # the grid keeps the rows in flight within 96 MiB of L2, but takes at least every SM
-        assert p.grid == min(152, max(152, (96 << 20) // (hv * 16 * (2 if op else 1))))
-        p2 = plan(op, 65536, hidden, dtype=dtype, bps=4)
-        assert p2.grid == min(608, max(152, (96 << 20) // (hv * 16 * (2 if op else 1))))
+        assert p.grid == min(rows, 152, max(152, (96 << 20) // (hv * 16 * (2 if op else 1))))
         # few rows: the register-resident cluster kernel, 8 CTAs per row (up to 16384 vectors)
         p = plan(op, 3, hidden, dtype=dtype, bps=1)
         if hv <= 16384:
@@ -259,6 +245,21 @@ def test_rows_wider_than_registers_take_the_two_pass_kernel(hidden, dtype):
             assert p.block * p.vec_per_thread * 8 >= hv and p.grid == 24
         else:
             assert p.kernel == _abi.KS_KERNEL_TWOPASS_ROW and p.grid == 3
+
+
+@pytest.mark.parametrize("op", [0, 1])
+def test_rows_past_the_wide_table_take_the_split_kernel(op):
+    """Many rows wider than 32768 vectors whose tensors exceed L2: the two-pass kernel split over
+    a cluster of 8 CTAs (plain: slice prefetch, one row in flight; fused: two rows in flight),
+    whole clusters, each with the same number of rows."""
+    hidden, hv, rows = 300000, 37500, 4096
+    p = plan(op, rows, hidden, dtype=BF16, bps=1)
+    assert p.kernel == _abi.KS_KERNEL_TWOPASS_ROW and p.cluster == 8
+    assert p.team == p.block * 8 and p.block == (512 if op else 256)
+    assert p.flags == (_abi.KS_PLAN_NO_PREFETCH if op else 0) and p.stages == (2 if op else 0)
+    n = min(152 // 8, (96 << 20) // (hv * 16 * (4 if op else 1)))
+    waves = -(-rows // n)
+    assert p.grid == -(-rows // waves) * 8
 
 
 def test_two_pass_plans_are_checked():
@@ -462,9 +463,12 @@ def test_every_width_gets_a_valid_plan(dtype, op):
                         assert p.cluster <= 8 and p.grid % p.cluster == 0
                         assert (p.cluster - 1) * slice_ < hv, (rows, hidden)
                 elif p.kernel == BULK:
-                    assert p.vec_per_thread == 4 and p.block <= 512 and 1 <= p.stages <= 16
-                    assert p.block * 4 >= hv and p.smem_bytes <= 226 * 1024
-                    assert p.cluster in (0, 1)
+                    C = p.cluster if p.cluster >= 2 else 1
+                    slice_ = -(-hv // C)
+                    assert p.block <= 512 and 1 <= p.stages <= 16 and C <= 8
+                    assert p.vec_per_thread == 4 or (p.vec_per_thread == 8 and op == 0 and C >= 2)
+                    assert p.block * p.vec_per_thread >= slice_ and (C - 1) * slice_ < hv
+                    assert p.smem_bytes <= 226 * 1024 and p.grid % C == 0
                 elif p.kernel == _abi.KS_KERNEL_CLUSTER_ROW:
                     assert 2 <= p.cluster <= 8 and p.grid % p.cluster == 0
                     assert p.vec_per_thread in (1, 2, 4) and p.block <= 512

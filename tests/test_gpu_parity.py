@@ -150,6 +150,49 @@ def test_default_plans_at_heuristic_edges(cuda_device, hv, op, dtype, rows):
     run_and_check(w, cuda_device)
 
 
+def _wide_band_edges():
+    """(dtype, op, hv) at every edge of the wide band table (rows of 2049..32768 vectors whose
+    tensors exceed L2), from the committed measured record the table is generated from."""
+    import json
+    import os
+
+    import bench
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with open(os.path.join(root, "row_wise_rmsnorm_ks_gb300", "csrc", "bands",
+                           "rms_norm_wide_bands.json")) as f:
+        bands = bench.derive_wide_bands(json.load(f))
+    out = []
+    for key, bl in sorted(bands.items()):
+        dt, op = key.split("/")
+        hvs = {bench.WIDE_LO, bench.WIDE_HI}
+        for hi, _ in bl[:-1]:
+            hvs |= {hi, hi + 1}
+        out += [(dt, op, hv) for hv in sorted(hvs)]
+    return out
+
+
+@pytest.mark.parametrize("dtype,op,hv", _wide_band_edges())
+def test_wide_band_edges(cuda_device, dtype, op, hv):
+    """The default entry points at every width where the wide band table switches launch, with
+    enough rows (ragged) that the tensors exceed L2, as the table requires: the staged kernel,
+    the split and one-CTA two-pass kernels and the cluster kernel, each at its band's edges.
+    Sampled rows against the oracle; the fused op's residual on every row against the rounded
+    sum, computed with torch on the device."""
+    dt = synth.dtype_of(dtype)
+    hidden = hv * (4 if dt == torch.float32 else 8)
+    rows = max(4 * 152 + 1, -(-(160 << 20) // (hv * 32)) + 3)
+    w = synth.prefill_device(op, rows, hidden, dtype, cuda_device)
+    x_in = w.x.clone()
+    r_in = w.residual.clone() if w.residual is not None else None
+    out = run_and_check(w, cuda_device, rows_idx=sample_rows(rows, k=12),
+                        name=f"wide band edge {op} {dtype} [{rows},{hidden}]")
+    if op != "rms_norm":
+        assert bits_equal(out["r"], (x_in.float() + r_in.float()).to(dt))
+    from row_wise_rmsnorm_ks_gb300 import _abi as A
+    st, flags = A.ks_device_faults(clear=True)
+    assert st == A.KS_SUCCESS and flags == 0
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm"])
 def test_unaligned_pointers(cuda_device, dtype, op):
@@ -308,12 +351,15 @@ def _variant_plan(name, hidden, elem):
     block = max(32, up32(-(-hv // v)))
     if block > (1024 if v == 2 else 512):
         return None
-    if name.startswith("bulk_row"):
-        stages = int(name.split("_s")[1])
+    if name.startswith("bulk_row"):  # bulk_row[_c<cluster>]_s<stages>[_v8]
+        stages = int(name.split("_s")[1].split("_")[0])
         if "_c" in name:  # the ring split over a cluster: each CTA stages its slice
             c = int(name.split("_c")[1].split("_")[0])
-            block = max(32, up32(-(-(-(-hv // c)) // 4)))
-            return A.make_plan(A.KS_KERNEL_BULK_ROW, 4, block, stages, cluster=c)
+            vv = 8 if name.endswith("_v8") else 4
+            block = max(32, up32(-(-(-(-hv // c)) // vv)))
+            if block > 512:
+                return None
+            return A.make_plan(A.KS_KERNEL_BULK_ROW, vv, block, stages, cluster=c)
         return A.make_plan(A.KS_KERNEL_BULK_ROW, 4, block, stages)
     if name.startswith("cluster_row"):
         c = int(name.split("_c")[1])
@@ -324,7 +370,8 @@ def _variant_plan(name, hidden, elem):
 
 VARIANTS = ["warp_row", "warp_row_np", "cta_row_v2", "cta_row_v2_np", "cta_row_v4",
             "cta_row_v4_np", "bulk_row_s1", "bulk_row_s2", "bulk_row_s5", "bulk_row_c2_s2",
-            "bulk_row_c3_s1", "bulk_row_c8_s3", "cluster_row_c2", "cluster_row_c3",
+            "bulk_row_c3_s1", "bulk_row_c8_s3", "bulk_row_c2_s2_v8", "bulk_row_c3_s3_v8",
+            "bulk_row_c8_s4_v8", "cluster_row_c2", "cluster_row_c3",
             "cluster_row_c8", "twopass_b256_u4", "twopass_b512_u2", "twopass_b1024_u4",
             "twopass_b96_u2", "split_c2_b256_u4", "split_c3_b96_u2", "split_c4_b512_u2",
             "split_c8_b1024_u2", "splitp_c2_b256_u4", "splitp_c3_b96_u2", "splitp_c4_b512_u2",
@@ -343,6 +390,8 @@ def test_every_kernel_variant_matches_oracle(cuda_device, variant, dtype, op, ro
     plan = _variant_plan(variant, hidden, elem)
     if plan is None:
         pytest.skip("variant does not fit this width")
+    if variant.endswith("_v8") and op != "rms_norm":
+        pytest.skip("8 vectors per thread: the plain op's staged kernel only")
     if plan.kernel == A.KS_KERNEL_BULK_ROW:
         hv = hidden * elem // 16
         stage = -(-hv // max(plan.cluster, 1)) * 16 * (2 if op != "rms_norm" else 1)
@@ -418,15 +467,15 @@ def test_rows_wider_than_registers_match_oracle(cuda_device, op, dtype, hidden, 
     ("fused_add_rms_norm", "fp32", 333, 65536)])   # 16384 fp32 vectors
 def test_wide_rows_past_l2_through_the_heuristic(cuda_device, op, dtype, rows, hidden):
     """Many rows wider than 4096-8192 vectors whose tensors exceed L2, through the default entry
-    points (the split kernels the heuristic picks there), ragged row counts: sampled rows against
-    the oracle, and the fused residual on every row against torch's rounded sum."""
+    points (the wide band table's staged or split kernels there), ragged row counts: sampled rows
+    against the oracle, and the fused residual on every row against torch's rounded sum."""
     from row_wise_rmsnorm_ks_gb300 import _abi as A
     dt = synth.dtype_of(dtype)
     sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
     code = {torch.bfloat16: A.KS_DTYPE_BF16, torch.float16: A.KS_DTYPE_F16,
             torch.float32: A.KS_DTYPE_F32}[dt]
     p = A.ks_plan_launch(0 if op == "rms_norm" else 1, rows, hidden, code, True, sms, 1)[1]
-    assert p.kernel == A.KS_KERNEL_TWOPASS_ROW
+    assert p.kernel in (A.KS_KERNEL_TWOPASS_ROW, A.KS_KERNEL_BULK_ROW) and p.cluster in (0, 2, 4, 8)
     x = synth.cast(synth.student_t3_dev((rows, hidden), 97, cuda_device), dt)
     wt = synth.weight(hidden, dt).to(cuda_device)
     idx = sample_rows(rows, k=12)

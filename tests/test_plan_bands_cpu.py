@@ -226,3 +226,69 @@ def test_next_op_default_plans_follow_the_record():
                     best = max(min(l2["scores"][n] for l2 in per.values()) for n in names)
                     assert min(l2["scores"][name] for l2 in per.values()) >= best - 20, \
                         (op, hv, name)
+
+
+WIDE = os.path.join(BANDS, "rms_norm_wide_bands.json")
+
+
+def test_wide_tables_are_the_derivation_of_their_record():
+    with open(WIDE) as f:
+        rec = json.load(f)
+    src = open(SOURCE).read()
+    m = re.search(r"// BEGIN GENERATED WIDE BANDS\n(.*?)\n// END GENERATED WIDE BANDS", src, re.S)
+    assert m, "generated block not found"
+    assert m.group(1) == bench.wide_bands_cpp(bench.derive_wide_bands(rec))
+
+
+def _wide_name(p, hv):
+    """The plan-sweep candidate name of a library plan for a row of hv vectors."""
+    K = _abi
+    npf = p.flags & NO_PF
+    if p.kernel == K.KS_KERNEL_TWOPASS_ROW and p.cluster < 2:
+        return f"t{p.block}u{p.vec_per_thread}" + ("n" if npf else "")
+    if p.kernel == K.KS_KERNEL_TWOPASS_ROW:
+        sfx = "p" if p.stages == 2 else ("n" if npf else "")
+        return f"s{p.cluster}b{p.block}u{p.vec_per_thread}{sfx}"
+    if p.kernel == K.KS_KERNEL_CLUSTER_ROW:
+        return f"c{p.cluster}"
+    if p.kernel == K.KS_KERNEL_BULK_ROW and p.cluster >= 2:
+        return f"b{p.cluster}s{p.stages}" + ("v8" if p.vec_per_thread == 8 else "")
+    raise AssertionError(p.as_dict())
+
+
+def test_wide_default_plans_within_two_points_of_the_measured_best():
+    with open(WIDE) as f:
+        rec = json.load(f)
+    for key, lines in rec["tables"].items():
+        dt, op = key.split("/")
+        for ln in lines:
+            p = plan(OPS[op], ln["rows"], hidden_of(dt, ln["hv"]), DTYPES[dt], rec["sm_count"])
+            name = _wide_name(p, ln["hv"])
+            sc = {n: v for n, v in ln["scores"].items() if n != "default"}
+            assert name in sc, (key, ln["hv"], name)
+            assert sc[name] >= max(sc.values()) - 20, (key, ln["hv"], name, max(sc.values()))
+
+
+@pytest.mark.parametrize("dt", list(DTYPES))
+@pytest.mark.parametrize("op", list(OPS))
+def test_every_wide_width_gets_a_plan_the_library_accepts(dt, op):
+    """Every width of the wide table, with many rows past L2: the plan meets the rules the planned
+    entry points check (covered slices, no CTA without vectors, blocks and rings within bounds,
+    clusters of 2..8, whole clusters in the grid)."""
+    fused = op != "rms_norm"
+    for hv in range(2049, 32769, 3):
+        rows = max(4 * 152, -(-(160 << 20) // (hv * 32)) + 1)
+        p = plan(OPS[op], rows, hidden_of(dt, hv), DTYPES[dt], 152, bps=1)
+        C = p.cluster if p.cluster >= 2 else 1
+        sl = -(-hv // C)
+        assert (C - 1) * sl < hv
+        if p.kernel == _abi.KS_KERNEL_TWOPASS_ROW:
+            assert p.vec_per_thread in (2, 4) and p.block <= 1024
+        else:
+            assert p.kernel in (_abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_CLUSTER_ROW), p.as_dict()
+            assert 2 <= C <= 8 and p.block <= 512 and p.block * p.vec_per_thread >= sl
+            if p.kernel == _abi.KS_KERNEL_BULK_ROW:
+                assert p.vec_per_thread == 4 or (p.vec_per_thread == 8 and not fused)
+                assert p.smem_bytes == 128 + p.stages * sl * 16 * (2 if fused else 1)
+                assert p.smem_bytes <= 226 * 1024
+        assert p.grid % C == 0 and p.grid >= C
