@@ -597,12 +597,12 @@ struct WideBand {
 };
 constexpr int64_t kWideLo = 2049, kWideHi = 32768;
 // BEGIN GENERATED WIDE BANDS
-constexpr WideBand kWideBandsF32Plain[] = {{2560, 6, 0, 256, 4, 0, 1}, {2816, 6, 0, 512, 4, 0, 0}, {3584, 6, 0, 512, 4, 0, 1}, {4096, 4, 2, 0, 8, 4, 0}, {4608, 4, 2, 0, 8, 3, 0}, {7168, 6, 0, 512, 4, 0, 1}, {9216, 4, 4, 0, 8, 4, 0}, {10240, 4, 4, 0, 8, 2, 0}, {12288, 4, 8, 0, 4, 2, 0}, {32768, 4, 8, 0, 8, 2, 0}};
-constexpr WideBand kWideBandsF32Fused[] = {{2816, 4, 2, 0, 4, 2, 0}, {4096, 6, 0, 512, 2, 0, 1}, {6144, 4, 4, 0, 4, 2, 0}, {8192, 4, 8, 0, 4, 2, 0}, {16384, 4, 8, 0, 4, 3, 0}, {28672, 6, 8, 512, 2, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
-constexpr WideBand kWideBandsF16Plain[] = {{2304, 4, 4, 0, 8, 2, 0}, {3072, 6, 0, 256, 4, 0, 1}, {4096, 6, 0, 512, 4, 0, 0}, {5120, 6, 0, 512, 2, 0, 0}, {7168, 4, 2, 0, 8, 2, 0}, {8192, 4, 4, 0, 4, 2, 0}, {14336, 4, 8, 0, 8, 2, 0}, {16384, 4, 4, 0, 8, 2, 0}, {20480, 6, 4, 256, 4, 2, 1}, {28672, 6, 8, 256, 4, 0, 0}, {32768, 4, 8, 0, 8, 2, 0}};
-constexpr WideBand kWideBandsF16Fused[] = {{2560, 6, 0, 512, 2, 0, 1}, {3072, 4, 2, 0, 4, 2, 0}, {4608, 6, 0, 512, 2, 0, 1}, {5120, 6, 0, 1024, 2, 0, 0}, {7168, 4, 4, 0, 4, 3, 0}, {8192, 4, 8, 0, 4, 3, 0}, {10240, 6, 2, 512, 2, 0, 1}, {14336, 6, 4, 512, 2, 2, 1}, {16384, 4, 8, 0, 4, 2, 0}, {28672, 6, 8, 512, 2, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
-constexpr WideBand kWideBandsBf16Plain[] = {{2304, 6, 0, 512, 2, 0, 0}, {2560, 4, 2, 0, 8, 4, 0}, {3072, 6, 0, 256, 4, 0, 1}, {3584, 6, 0, 512, 4, 0, 0}, {4096, 6, 0, 512, 2, 0, 1}, {4608, 6, 0, 512, 4, 0, 0}, {5120, 4, 4, 0, 8, 4, 0}, {8192, 4, 4, 0, 4, 2, 0}, {9216, 4, 8, 0, 8, 2, 0}, {10240, 4, 8, 0, 8, 4, 0}, {14336, 4, 4, 0, 8, 2, 0}, {16384, 4, 8, 0, 4, 2, 0}, {20480, 6, 4, 512, 2, 0, 0}, {28672, 6, 8, 256, 4, 0, 0}, {32768, 4, 8, 0, 8, 2, 0}};
-constexpr WideBand kWideBandsBf16Fused[] = {{2304, 4, 8, 0, 4, 2, 0}, {2816, 4, 2, 0, 4, 2, 0}, {3072, 6, 0, 512, 2, 0, 1}, {4608, 4, 8, 0, 4, 2, 0}, {5120, 4, 8, 0, 4, 4, 0}, {7168, 4, 4, 0, 4, 2, 0}, {14336, 6, 4, 512, 2, 2, 1}, {16384, 4, 8, 0, 4, 3, 0}, {28672, 6, 8, 512, 2, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
+constexpr WideBand kWideBandsF32Plain[] = {{2560, 6, 0, 256, 4, 0, 1}, {2816, 6, 0, 512, 4, 0, 0}, {3584, 6, 0, 512, 4, 0, 1}, {4608, 4, 2, 0, 8, 4, 0}, {7168, 6, 0, 512, 4, 0, 1}, {9216, 4, 4, 0, 8, 4, 0}, {10240, 4, 4, 0, 8, 2, 0}, {14336, 6, 4, 512, 2, 0, 0}, {20480, 6, 4, 512, 2, 0, 1}, {32768, 4, 8, 0, 8, 2, 0}};
+constexpr WideBand kWideBandsF32Fused[] = {{2304, 4, 2, 0, 4, 2, 0}, {3072, 6, 0, 512, 2, 0, 1}, {4096, 6, 2, 256, 4, 2, 1}, {5120, 4, 4, 0, 4, 2, 0}, {6144, 4, 8, 0, 4, 2, 0}, {8192, 6, 4, 256, 4, 2, 1}, {10240, 6, 4, 512, 2, 2, 1}, {16384, 4, 8, 0, 4, 3, 0}, {20480, 6, 8, 512, 2, 2, 1}, {28672, 6, 8, 256, 4, 2, 1}, {32768, 6, 4, 512, 4, 2, 1}};
+constexpr WideBand kWideBandsF16Plain[] = {{2304, 4, 4, 0, 8, 2, 0}, {3072, 6, 0, 256, 4, 0, 1}, {4096, 6, 0, 512, 4, 0, 0}, {5120, 6, 0, 512, 2, 0, 0}, {7168, 4, 2, 0, 8, 2, 0}, {8192, 6, 2, 256, 4, 2, 1}, {14336, 4, 8, 0, 8, 2, 0}, {24576, 6, 4, 256, 4, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
+constexpr WideBand kWideBandsF16Fused[] = {{2560, 6, 0, 512, 2, 0, 1}, {3072, 4, 2, 0, 4, 2, 0}, {3584, 4, 8, 0, 4, 4, 0}, {5120, 6, 2, 512, 2, 2, 1}, {7168, 4, 4, 0, 4, 3, 0}, {12288, 6, 4, 512, 2, 2, 1}, {14336, 6, 4, 256, 4, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
+constexpr WideBand kWideBandsBf16Plain[] = {{2304, 6, 0, 512, 2, 0, 0}, {2560, 4, 2, 0, 8, 4, 0}, {3072, 6, 0, 256, 4, 0, 1}, {3584, 6, 0, 512, 4, 0, 0}, {4096, 6, 0, 512, 2, 0, 1}, {4608, 6, 0, 512, 4, 0, 0}, {5120, 4, 4, 0, 8, 4, 0}, {8192, 4, 4, 0, 4, 2, 0}, {9216, 4, 8, 0, 8, 2, 0}, {10240, 4, 8, 0, 8, 4, 0}, {14336, 4, 4, 0, 8, 2, 0}, {16384, 4, 8, 0, 4, 2, 0}, {28672, 6, 4, 512, 2, 2, 1}, {32768, 4, 8, 0, 8, 2, 0}};
+constexpr WideBand kWideBandsBf16Fused[] = {{2304, 4, 8, 0, 4, 2, 0}, {2816, 4, 2, 0, 4, 2, 0}, {3072, 6, 0, 512, 2, 0, 1}, {3584, 6, 2, 512, 2, 2, 1}, {4096, 6, 2, 256, 4, 2, 1}, {5120, 6, 2, 512, 2, 2, 1}, {7168, 4, 8, 0, 4, 2, 0}, {10240, 6, 4, 512, 2, 2, 1}, {14336, 6, 4, 256, 4, 2, 1}, {16384, 4, 8, 0, 4, 3, 0}, {28672, 6, 8, 512, 2, 2, 1}, {32768, 6, 4, 512, 4, 2, 1}};
 // END GENERATED WIDE BANDS
 
 // Whether a wide table is well formed: widths rising to kWideHi, kernels that take rows this

@@ -538,29 +538,88 @@ const void *pick_twopass(int block) {
     return (const void *)rows_twopass_kernel<T, kFused, U, 1024>;
 }
 
+// ------------------------------------------------------- slice sums across a cluster
+
+// A row's slice sums across a cluster of C CTAs (C <= 8) without a cluster barrier per row: each
+// CTA's first C threads send the CTA's sum and a flag to every CTA of the cluster with an
+// asynchronous shared-memory store that completes as 8 transaction bytes on the receiver's
+// mbarrier for that row, and every CTA waits (bounded) on its own barrier for C of them. (A
+// cluster barrier's arrive has release semantics: every thread would first wait for its
+// earlier global stores to be acknowledged.) Rows alternate between two slots and barriers;
+// slot s is used every other row, so the n-th use of a slot completes with parity n & 1. A CTA
+// may send a row's sum into a slot only after every thread of it has read that slot's previous
+// row, and after its peers set their barriers up (the kernels' start barrier).
+struct ClusterSums {
+    uint32_t part[2][8][2];  // (sum bits, flag) by sending rank
+    uint64_t bar[2];
+};
+
+// Thread 0, before the kernel's start cluster barrier.
+__device__ __forceinline__ void sums_init(ClusterSums &cs) {
+    mbar_init(&cs.bar[0], 1);
+    mbar_init(&cs.bar[1], 1);
+    fence_mbar_init();
+}
+
+// Sends this CTA's sum `v` (valid in threads t < C) with `flag` for slot `slot`, and arms this
+// CTA's barrier of the slot for the C sums it receives. Every thread of the CTA must have read
+// the slot's previous row before this call.
+__device__ __forceinline__ void sums_send(ClusterSums &cs, int slot, float v, uint32_t flag,
+                                          int q, int C, int t) {
+    if (t == 0) mbar_arrive_expect_tx(&cs.bar[slot], (uint32_t)C * 8u);
+    if (t < C)
+        st_async_v2(cluster_map(&cs.part[slot][q][0], (uint32_t)t), __float_as_uint(v), flag,
+                    cluster_map(&cs.bar[slot], (uint32_t)t));
+}
+
+// Waits for slot `slot`'s use with parity `parity`; on return `sum` adds the C sums in rank order
+// and the result says whether they all arrived with a zero flag.
+__device__ __forceinline__ bool sums_wait(ClusterSums &cs, int slot, uint32_t parity, int C,
+                                          float &sum) {
+    const bool got = mbar_wait_bounded(&cs.bar[slot], parity);
+    uint32_t bad = got ? 0u : 1u;
+    float ss = 0.0f;
+    for (int r = 0; r < C; ++r) {
+        ss += __uint_as_float(cs.part[slot][r][0]);
+        bad |= cs.part[slot][r][1];
+    }
+    sum = ss;
+    return bad == 0u;
+}
+
 // ------------------------------------------------------------ split two-pass row kernel
 
 // The two-pass scheme with each row split over a thread-block cluster of C CTAs (2..8): CTA q of
 // a cluster takes the contiguous slice [q*S, min((q+1)*S, hv)) of S = ceil(hv / C) vectors of
 // every row its cluster visits, forms the slice's sum of squares (default L2 policy), and writes
 // the slice's outputs from a second read of it (evict-first, from L2). Between the two passes
-// the slice sums meet: the CTA's first C threads each write the CTA's sum into one peer's
-// shared memory (distributed shared memory), one cluster barrier per row makes them visible,
-// and every CTA adds the C sums in rank order, so all CTAs of a row agree on its scale. The
-// barrier's arrive and wait are split, with the first loads of the second pass issued between
-// them, so its latency overlaps those loads.
+// the slice sums meet through ClusterSums (asynchronous stores into every CTA's slot for the row,
+// completing on its mbarrier), and every CTA adds the C sums in rank order, so all CTAs of a row
+// agree on its scale. The first loads of the second pass are issued before the wait, so its
+// latency overlaps them. The wait is bounded: after a time-out (here, or a peer's flag) the CTAs
+// record KS_FAULT_WAIT_TIMEOUT and keep exchanging flags for the remaining rows without touching
+// rows, so every store a peer sends is still awaited before any CTA leaves.
 //
 // Against one CTA per row this keeps each unit of work to a slice: a persistent grid of whole
 // rows leaves SMs idle in its last wave when the rows per CTA are few (10.1 rows per CTA run as
 // 11 waves), and the rows a CTA-per-row grid has in flight at once grow with the width until
 // the second pass misses L2; here the rows in flight are one per cluster.
+// Resident CTAs per SM the launch bound asks of the split kernel: the plain op at 2 vectors per
+// step fits in 40 registers, three 512-thread CTAs (six of 256) per SM; the compiler's own
+// choice took 64 and two.
+template <bool kFused, int U, int kMaxBlock>
+struct SplitMinBlocks {
+    static constexpr int value = (!kFused && U == 2 && kMaxBlock <= 512) ? 1536 / kMaxBlock : 1;
+};
+
 template <typename T, bool kFused, int U, int kMaxBlock>
-__global__ void __launch_bounds__(kMaxBlock) rows_split_kernel(const RowArgs a) {
+__global__ void __launch_bounds__(kMaxBlock, (SplitMinBlocks<kFused, U, kMaxBlock>::value))
+    rows_split_kernel(const RowArgs a) {
     namespace cg = cooperative_groups;
     using E = Elem<T>;
     constexpr int P = E::kPerVec / 2;
     __shared__ float red[32];
-    __shared__ float part[2][8];  // a row's slice sums from every CTA of the cluster, by rank
+    __shared__ __align__(8) ClusterSums cs;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
@@ -578,17 +637,18 @@ __global__ void __launch_bounds__(kMaxBlock) rows_split_kernel(const RowArgs a) 
     const uint4 *wg = static_cast<const uint4 *>(a.w);
     grid_dependency_wait();
     allow_dependents_launch();
-    // A peer's shared memory may be written only once that peer has started: every CTA arrives
-    // here and waits (before its first write into a peer) for all of its cluster to arrive. The
-    // row loop runs the same rows on every CTA of a cluster, so `started` is uniform.
+    if (t == 0) sums_init(cs);
+    // every CTA of the cluster has set its barriers up before any CTA sends to it
     cluster.barrier_arrive();
-    bool started = false;
+    cluster.barrier_wait();
     const int64_t nclusters = gridDim.x / C;
     // With prefetch, the whole slice of a row is asked into L2 by the copy engine as the row
     // starts, so the DRAM reads of all the first pass's steps are in flight at once.
     const bool prefetch = a.l2_prefetch != 0;
-    int parity = 0;
-    for (int64_t row = blockIdx.x / C; row < a.rows; row += nclusters) {
+    bool fault = false;
+    uint32_t j = 0;
+    int64_t row = blockIdx.x / C;
+    for (; row < a.rows; row += nclusters, ++j) {
         const uint4 *xr = xg + row * hv;
         uint4 *rr = kFused ? rg + row * hv : nullptr;
         if (prefetch) prefetch_slice<kFused>(xr, rr, lo, hi, t);
@@ -608,23 +668,16 @@ __global__ void __launch_bounds__(kMaxBlock) rows_split_kernel(const RowArgs a) 
                 acc.add(f);
             }
         }
-        // The CTA's slice sum (warps in order) into slot `parity` of every CTA of the cluster.
-        // `red` is free again once every thread has passed the previous row's cluster barrier;
-        // slot `parity` of a peer is written again two rows on, after a barrier that the peer
-        // reaches only once it has read this row's sums.
+        // the CTA's slice sum (warps in order); every thread has read the slot this row reuses
+        // (two rows back) before this barrier
         const float wsum = warp_sum(acc.total());
         if ((t & 31) == 0) red[t >> 5] = wsum;
         __syncthreads();
-        if (!started) {
-            cluster.barrier_wait();
-            started = true;
-        }
-        if (t < C) {
-            float cta = 0.0f;
+        float cta = 0.0f;
+        if (t < C)
             for (int i = 0; i < (g >> 5); ++i) cta += red[i];
-            *cluster.map_shared_rank(&part[parity][q], t) = cta;
-        }
-        cluster.barrier_arrive();
+        const int slot = (int)(j & 1u);
+        sums_send(cs, slot, cta, 0u, q, C, t);
         uint4 *orow = og + row * hv;
         uint4 xv[U], rv[U], wv[U];
         int64_t c0 = lo + t;
@@ -637,10 +690,14 @@ __global__ void __launch_bounds__(kMaxBlock) rows_split_kernel(const RowArgs a) 
             if (kFused) rv[u] = in ? __ldcs(rr + c) : make_uint4(0u, 0u, 0u, 0u);
             wv[u] = in ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
         }
-        cluster.barrier_wait();
         float ss = 0.0f;
-        for (int r = 0; r < C; ++r) ss += part[parity][r];
-        parity ^= 1;
+        const bool good = sums_wait(cs, slot, (j >> 1) & 1u, C, ss);
+        // (red is written again only after the next row's first pass, which every thread
+        // reaches after this barrier)
+        if (!__syncthreads_and(good)) {
+            fault = true;
+            break;
+        }
         const float scale = row_scale(ss, h, a.eps);
         for (; c0 < hi; c0 += chunk) {
             if (c0 != lo + t) {
@@ -665,27 +722,37 @@ __global__ void __launch_bounds__(kMaxBlock) rows_split_kernel(const RowArgs a) 
             }
         }
     }
-    if (!started) cluster.barrier_wait();
-    cluster.sync();  // no CTA leaves while a peer may still write its sums here
+    if (fault) {
+        // the remaining rows' exchanges with a flag, touching no row, so that every store a peer
+        // sends here is still awaited before this CTA leaves
+        for (row += nclusters, ++j; row < a.rows; row += nclusters, ++j) {
+            __syncthreads();  // every thread has read the slot's previous row
+            float ss = 0.0f;
+            sums_send(cs, (int)(j & 1u), 0.0f, 1u, q, C, t);
+            (void)sums_wait(cs, (int)(j & 1u), (j >> 1) & 1u, C, ss);
+        }
+        if (t == 0) atomicOr(&g_fault_flags, kFaultWaitTimeout);
+    }
+    cluster.sync();
 }
 
 // The split two-pass scheme with two rows in flight per cluster: each CTA's one loop over its
 // slice reads the *next* row (its first pass, from DRAM: the sum of squares) and re-reads the
 // current row (its second pass, from L2: the outputs), so every CTA keeps DRAM reads and writes
 // in flight together, where the one-row kernel alternates a read-only pass with a
-// read-and-write one, all clusters in step. The next row's slice sums meet in distributed shared
-// memory during the following loop: the cluster barrier's arrive follows the loop, its wait
-// comes after the next loop's first loads. Two alternating slots hold a row's slice sums: CTA q
-// writes slot (j+1) % 2 of a peer only after the barrier of row j, which the peer reaches only
-// once it has read slot (j - 1) % 2. Rows in flight are two per cluster (the grid's L2 cap
-// counts them).
+// read-and-write one, all clusters in step. The next row's slice sums are sent through
+// ClusterSums after the loop, and awaited after the next loop's first loads. Rows alternate
+// between the two slots: row k's sums use slot k % 2, so a CTA sends row k + 1's sums only after
+// every thread of it has read row k - 1's. Rows in flight are two per cluster (the grid's L2 cap
+// counts them). After a time-out the CTAs keep exchanging flags without touching rows, as in the
+// one-row kernel.
 template <typename T, bool kFused, int U, int kMaxBlock>
 __global__ void __launch_bounds__(kMaxBlock) rows_split_pipe_kernel(const RowArgs a) {
     namespace cg = cooperative_groups;
     using E = Elem<T>;
     constexpr int P = E::kPerVec / 2;
     __shared__ float red[32];
-    __shared__ float part[2][8];
+    __shared__ __align__(8) ClusterSums cs;
 
     cg::cluster_group cluster = cg::this_cluster();
     const int C = (int)cluster.num_blocks();
@@ -704,28 +771,27 @@ __global__ void __launch_bounds__(kMaxBlock) rows_split_pipe_kernel(const RowArg
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     grid_dependency_wait();
     allow_dependents_launch();
+    if (t == 0) sums_init(cs);
     const int64_t nclusters = gridDim.x / C;
     int64_t row = blockIdx.x / C;
 
-    // The CTA's slice sum (warps in order) into slot `s` of every CTA of the cluster, then the
-    // arrive of that row's cluster barrier.
-    auto publish = [&](float v, int s) {
+    // The CTA's slice sum (warps in order) sent as row k's sums (slot k % 2). The barrier also
+    // orders every thread's reads of row k - 2's slot, and of `red`, before the sends.
+    auto publish = [&](float v, uint32_t k, uint32_t flag) {
         const float wsum = warp_sum(v);
         if ((t & 31) == 0) red[t >> 5] = wsum;
         __syncthreads();
-        if (t < C) {
-            float cta = 0.0f;
+        float cta = 0.0f;
+        if (t < C)
             for (int i = 0; i < (g >> 5); ++i) cta += red[i];
-            *cluster.map_shared_rank(&part[s][q], t) = cta;
-        }
-        cluster.barrier_arrive();
+        sums_send(cs, (int)(k & 1u), cta, flag, q, C, t);
     };
 
-    // Start: every CTA of the cluster has started before any writes into a peer (the wait below);
-    // then the first row's first pass alone.
+    // Start: the first row's first pass alone, while the cluster's barriers are being set up;
+    // every CTA has set its barriers up before any CTA sends to it.
     cluster.barrier_arrive();
+    PairSumSq<E::kPairMath> acc0;
     if (row < a.rows) {
-        PairSumSq<E::kPairMath> acc;
         const uint4 *xr = xg + row * hv;
         const uint4 *rr = kFused ? rg + row * hv : nullptr;
         for (int64_t c0 = lo + t; c0 < hi; c0 += chunk) {
@@ -740,16 +806,16 @@ __global__ void __launch_bounds__(kMaxBlock) rows_split_pipe_kernel(const RowArg
             for (int u = 0; u < U; ++u) {
                 float2 f[P];
                 row_values<T, kFused>(xv[u], rv[u], f);
-                acc.add(f);
+                acc0.add(f);
             }
         }
-        cluster.barrier_wait();
-        publish(acc.total(), 0);
-    } else {
-        cluster.barrier_wait();
     }
+    cluster.barrier_wait();
+    if (row < a.rows) publish(acc0.total(), 0u, 0u);
 
-    for (int j = 0; row < a.rows; row += nclusters, ++j) {
+    bool fault = false;
+    uint32_t j = 0;
+    for (; row < a.rows; row += nclusters, ++j) {
         const int64_t nxt = row + nclusters;
         const bool more = nxt < a.rows;  // uniform over the cluster
         const uint4 *xr = xg + row * hv;
@@ -791,21 +857,35 @@ __global__ void __launch_bounds__(kMaxBlock) rows_split_pipe_kernel(const RowArg
                 }
             }
         };
-        // the first step's loads need no scale: issue them before this row's barrier wait
+        // the first step's loads need no scale: issue them before this row's wait
         int64_t c0 = lo + t;
         load(c0);
-        cluster.barrier_wait();
         float ss = 0.0f;
-        for (int r = 0; r < C; ++r) ss += part[j & 1][r];
+        const bool good = sums_wait(cs, (int)(j & 1u), (j >> 1) & 1u, C, ss);
+        if (!__syncthreads_and(good)) {
+            fault = true;
+            break;
+        }
         const float scale = row_scale(ss, h, a.eps);
         step(c0, scale);
         for (c0 += chunk; c0 < hi; c0 += chunk) {
             load(c0);
             step(c0, scale);
         }
-        if (more) publish(acc.total(), (j + 1) & 1);
+        if (more) publish(acc.total(), j + 1u, 0u);
     }
-    cluster.sync();  // no CTA leaves while a peer may still write its sums here
+    if (fault) {
+        // The remaining rows' exchanges with a flag, touching no row, so that every store a peer
+        // sends here is still awaited before this CTA leaves: row k + 1's sums are sent before
+        // row k + 1's wait, as in the loop.
+        for (row += nclusters, ++j; row < a.rows; row += nclusters, ++j) {
+            publish(0.0f, j, 1u);
+            float ss = 0.0f;
+            (void)sums_wait(cs, (int)(j & 1u), (j >> 1) & 1u, C, ss);
+        }
+        if (t == 0) atomicOr(&g_fault_flags, kFaultWaitTimeout);
+    }
+    cluster.sync();
 }
 
 template <typename T, bool kFused, int U>
@@ -877,60 +957,40 @@ __global__ void __launch_bounds__(1024) rows_scalar_kernel(const RowArgs a) {
 // barrier in the CTA reduction is also the point after which the stage is free, so thread 0
 // refills it with the row `stages` iterations ahead right after that barrier.
 //
-// kCluster: rows too wide for one CTA's registers are split over a thread-block cluster of C
-// CTAs. CTA rank q owns the row's vectors [q*S, min(hv, (q+1)*S)), S = ceil(hv / C), and streams
-// that slice through its own ring; each CTA publishes its partial sum of squares (and whether a
-// wait of its timed out) in its shared memory, and after one cluster barrier every thread adds
-// the C partials in rank order through distributed shared memory, so the whole cluster computes
-// one scale. Partials alternate between two slots per row (a CTA overwrites a slot only after the
-// next row's cluster barrier, which its peers reach only after reading it). Stages are refilled
-// only after the cluster barrier, once the row is known to be good everywhere.
-//
-// Shared memory: 128 bytes of barriers, then stages x (1 or 2) x S*16 bytes.
-// Every wait is bounded: on a time-out the CTA records kFaultWaitTimeout; the CTA (with kCluster,
-// the whole cluster, which learns of it at the row's cluster barrier) stops at that row, each CTA
-// waits (bounded) for the copies it still has in flight, and returns.
-template <typename T, int V, bool kFused, bool kCluster>
+// Shared memory: 128 bytes of barriers, then stages x (1 or 2) x hv*16 bytes.
+// Every wait is bounded: on a time-out the CTA records kFaultWaitTimeout, stops at that row,
+// waits (bounded) for the copies it still has in flight, and returns. (Rows too wide for one CTA
+// take the staged split kernel below, which splits each row over a cluster.)
+template <typename T, int V, bool kFused>
 __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
-    namespace cg = cooperative_groups;
     using E = Elem<T>;
     constexpr int P = E::kPerVec / 2;
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[2][32];
-    __shared__ float part[2];
-    __shared__ int bad_slot[2];
 
-    int C = 1, q = 0;
-    if (kCluster) {
-        cg::cluster_group cluster = cg::this_cluster();
-        C = (int)cluster.num_blocks();
-        q = (int)cluster.block_rank();
-    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     unsigned char *ring = smem + 128;
     const int g = blockDim.x;
     const int t = threadIdx.x;
     const int64_t hv = a.hv;
-    const int64_t S = kCluster ? (hv + C - 1) / C : hv;
-    const int64_t lo = kCluster ? q * S : 0;
-    const int64_t nv = (lo + S < hv ? lo + S : hv) - lo;  // this CTA's vectors (>= 1)
+    const int64_t nv = hv;
     const int stages = a.stages;
     const uint32_t copy_bytes = (uint32_t)(nv * 16);
-    const uint32_t slot_bytes = (uint32_t)(S * 16);  // the residual's slice follows the x slice
+    const uint32_t slot_bytes = copy_bytes;  // the residual's row follows the x row
     const uint32_t stage_bytes = kFused ? 2u * slot_bytes : slot_bytes;
     const float h = (float)a.hidden;
-    const int64_t first = kCluster ? blockIdx.x / C : blockIdx.x;
-    const int64_t step = kCluster ? gridDim.x / C : gridDim.x;
+    const int64_t first = blockIdx.x;
+    const int64_t step = gridDim.x;
 
-    const uint4 *xg = static_cast<const uint4 *>(a.x) + lo;
-    uint4 *og = static_cast<uint4 *>(a.out) + lo;
-    uint4 *rg = kFused ? static_cast<uint4 *>(a.res) + lo : nullptr;
+    const uint4 *xg = static_cast<const uint4 *>(a.x);
+    uint4 *og = static_cast<uint4 *>(a.out);
+    uint4 *rg = kFused ? static_cast<uint4 *>(a.res) : nullptr;
 
     grid_dependency_wait();
     allow_dependents_launch();
     uint4 wv[V];
     {
-        const uint4 *wg = static_cast<const uint4 *>(a.w) + lo;
+        const uint4 *wg = static_cast<const uint4 *>(a.w);
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
@@ -992,41 +1052,16 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
         // The CTA barrier of this row: partial sums are visible, every thread has its stage data
         // in registers (so the stage may be refilled), and a time-out anywhere is seen by all.
         const bool bad = __syncthreads_or(!ok);
-        float ss = 0.0f;
-        const int nw = g >> 5;
-        if (!kCluster) {
-            if (bad) {
-                fault = true;
-                break;
-            }
-            if (t == 0) {
-                const int64_t ahead = row + (int64_t)stages * step;
-                if (ahead < a.rows) issue(s, ahead);
-            }
-            for (int i = 0; i < nw; ++i) ss += red[parity][i];
-        } else {
-            cg::cluster_group cluster = cg::this_cluster();
-            if (t == 0) {
-                float cta = 0.0f;
-                for (int i = 0; i < nw; ++i) cta += red[parity][i];
-                part[parity] = cta;
-                bad_slot[parity] = bad ? 1 : 0;
-            }
-            cluster.sync();  // every CTA's partial and time-out flag for this row is published
-            int any_bad = 0;
-            for (int r = 0; r < C; ++r) {
-                ss += *cluster.map_shared_rank(&part[parity], r);
-                any_bad |= *cluster.map_shared_rank(&bad_slot[parity], r);
-            }
-            if (any_bad) {
-                fault = true;
-                break;
-            }
-            if (t == 0) {
-                const int64_t ahead = row + (int64_t)stages * step;
-                if (ahead < a.rows) issue(s, ahead);
-            }
+        if (bad) {
+            fault = true;
+            break;
         }
+        if (t == 0) {
+            const int64_t ahead = row + (int64_t)stages * step;
+            if (ahead < a.rows) issue(s, ahead);
+        }
+        float ss = 0.0f;
+        for (int i = 0; i < (g >> 5); ++i) ss += red[parity][i];
         parity ^= 1;
         const float scale = row_scale(ss, h, a.eps);
 
@@ -1063,7 +1098,6 @@ __global__ void __launch_bounds__(512) rows_bulk_kernel(const RowArgs a) {
             }
         }
     }
-    if (kCluster) cg::this_cluster().sync();  // peers may still be reading this CTA's partials
 }
 
 // ------------------------------------------------------------------ cluster row kernel
@@ -1408,7 +1442,7 @@ const void *pick_kernel(const ks_plan_t &p) {
             return nullptr;
         }
         if (p.vec_per_thread != 4) return nullptr;
-        return (const void *)rows_bulk_kernel<T, 4, kFused, false>;
+        return (const void *)rows_bulk_kernel<T, 4, kFused>;
     case KS_KERNEL_CLUSTER_ROW:
         switch (p.vec_per_thread) {
         case 1: return (const void *)rows_cluster_kernel<T, 1, kFused>;
