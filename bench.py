@@ -1435,7 +1435,8 @@ def op_band_candidates(op: str, hv: int):
     tTvV / tTvVn (a team of T = 8 or 16 lanes per row, V vectors a lane, with / without
     prefetch; where the team covers the row), wV / wVn (a warp per row), cV / cVn (a CTA per
     row, V vectors a thread), for rows wider than 256 vectors xB (the wide multi-pass kernel on
-    B threads) and for LayerNorm rS (the staged ring of S rows per CTA), and for SwiGLU flatB
+    B threads) and for LayerNorm rS / rSa (the staged ring of S rows per CTA, with the weight and
+    bias rows in registers / in shared memory), and for SwiGLU flatB
     (the flat walk on B-thread CTAs) and rowsB (the row kernel with at most B threads)."""
     from row_wise_rmsnorm_ks_gb300 import _abi
 
@@ -1476,6 +1477,10 @@ def op_band_candidates(op: str, hv: int):
             for st in (2, 3, 4, 6, 8):
                 if 128 + st * hv * 16 <= 226 * 1024:
                     out.append((f"r{st}", mk(_abi.KS_KERNEL_BULK_ROW, 4, b, st)))
+                # rSa: the weight and bias rows in shared memory beside the ring
+                if 128 + (st + 2) * hv * 16 <= 226 * 1024:
+                    out.append((f"r{st}a", mk(_abi.KS_KERNEL_BULK_ROW, 4, b, st,
+                                               flags=_abi.KS_PLAN_AFFINE_SMEM)))
     return out
 
 
@@ -1635,10 +1640,13 @@ def band_of(name: str, default_plan: dict, op: str, hv: int):
             return ("x", 4, True, 32, default_plan["block"])
         if k == "bulk_row":
             st = default_plan.get("stages") or max(2, min(8, LN_RING_BYTES // (hv * 16)))
-            return ("r", st, True, 32, 0)
+            return ("R" if default_plan["flags"] & 4 else "r", st, True, 32, 0)
         gen_v = 1 if hv < 64 else (2 if hv < 128 else 4)
         gen_pf = True if op == "layer_norm" else (gen_v != 4 or hv > 1024)
-        if k == "cta_row" and v == gen_v and (not npf) == gen_pf:
+        # for many LayerNorm rows wider than 512 vectors the general rule is the ring or the
+        # wide kernel, so a CTA row there is a band of its own
+        gen_cta = not (op == "layer_norm" and hv > 512)
+        if k == "cta_row" and v == gen_v and (not npf) == gen_pf and gen_cta:
             return ("g", 0, gen_pf, 32, 0)
         return ("c", v, not npf, 32, 0)
     m = re.fullmatch(r"t(\d+)v(\d)(n?)", name)
@@ -1647,18 +1655,37 @@ def band_of(name: str, default_plan: dict, op: str, hv: int):
     m = re.fullmatch(r"x(\d+)", name)
     if m:
         return ("x", 4, True, 32, int(m.group(1)))
-    m = re.fullmatch(r"r(\d)", name)
+    m = re.fullmatch(r"r(\d)(a?)", name)
     if m:
-        return ("r", int(m.group(1)), True, 32, 0)
+        return ("R" if m.group(2) else "r", int(m.group(1)), True, 32, 0)
     m = re.fullmatch(r"([wc])(\d)(n?)", name)
     return (m.group(1), int(m.group(2)), not m.group(3), 32, 0)
+
+
+def ops_candidate_name(plan: dict, hv: int) -> str:
+    """The --ops-bands candidate name of a Softmax or LayerNorm launch plan (as the JSON lines
+    report it): w / tTEAMv (warp rows), c (CTA rows), r (the LayerNorm ring, its stages; a: the
+    weight and bias rows in shared memory), x (the wide kernel, its block); n: no prefetch. hv:
+    the row's width in 16-byte vectors (older runs did not report the ring's stages)."""
+    k, v, n = plan["kernel_name"], plan["vec_per_thread"], "n" if plan["flags"] & 1 else ""
+    if k == "warp_row":
+        team = plan.get("team") or 32
+        return (f"w{v}" if team == 32 else f"t{team}v{v}") + n
+    if k == "cta_row":
+        return f"c{v}{n}"
+    if k == "bulk_row":
+        st = plan.get("stages") or max(2, min(8, LN_RING_BYTES // (hv * 16)))
+        return f"r{st}" + ("a" if plan["flags"] & 4 else "")
+    if k == "twopass_row":
+        return f"x{plan['block']}"
+    return k
 
 
 def ops_bands_record(jsonl_paths) -> dict:
     """The measured record behind the Softmax and LayerNorm width bands, from --ops-bands runs:
     per operator, dtype and width, every candidate's score (the worse of its two contexts, in
-    thousandths of the measured copy peak) and the band the library's default launch was. A width
-    measured by several runs keeps the last."""
+    thousandths of the measured copy peak), the band the library's default launch was and that
+    launch's candidate name. A width measured by several runs keeps the last."""
     lines = {}
     for path in jsonl_paths:
         for ln in open(path):
@@ -1672,6 +1699,7 @@ def ops_bands_record(jsonl_paths) -> dict:
             lines[(d["ops_bands"], d["dtype"], d["hv"])] = {
                 "op": d["ops_bands"], "dtype": d["dtype"], "hv": d["hv"],
                 "default_band": list(band_of("default", d["default_plan"], d["ops_bands"], d["hv"])),
+                "default_name": ops_candidate_name(d["default_plan"], d["hv"]),
                 "scores": sc}
     return {"what": "Softmax and LayerNorm launch scores per width, many rows",
             "score": "worse of steady state and after a large-shared-memory kernel, thousandths "

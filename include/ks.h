@@ -147,6 +147,10 @@ typedef struct ks_plan {
  * the stream finishes; it waits for that kernel's writes before its first memory access. */
 #define KS_PLAN_NO_PREFETCH 1
 #define KS_PLAN_PDL 2
+/* KS_PLAN_AFFINE_SMEM (LayerNorm's staged ring only): the weight and bias rows live in the CTA's
+ * shared memory beside the ring instead of in every thread's registers (fewer registers, so more
+ * resident CTAs); the ring's shared memory grows by a row per array given. */
+#define KS_PLAN_AFFINE_SMEM 4
 
 enum {
     KS_KERNEL_NONE = 0,     /* rows == 0: nothing is launched */

@@ -24,6 +24,7 @@ OP_RMS_NORM, OP_FUSED_ADD_RMS_NORM, OP_SILU_AND_MUL, OP_SOFTMAX, OP_LAYER_NORM =
 KS_FAULT_WAIT_TIMEOUT = 1
 KS_PLAN_NO_PREFETCH = 1
 KS_PLAN_PDL = 2
+KS_PLAN_AFFINE_SMEM = 4
 KS_LAUNCH_PDL = 1
 
 # Every symbol include/ks.h declares (checked by the CPU test of the boundary).

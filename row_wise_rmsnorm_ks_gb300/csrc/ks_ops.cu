@@ -604,7 +604,10 @@ __global__ void __launch_bounds__(kTeam ? 128 : 512) layer_norm_vec_kernel(void 
 // (Reading the stage in all three passes instead freed registers but measured slower.) Waits
 // are bounded (about 2 s); on a time-out the CTA records KS_FAULT_WAIT_TIMEOUT, drains its copies
 // in flight (bounded) and returns.
-template <typename T, int V, int kAffine>
+// kSmemWB: the weight and bias slices live in shared memory after the ring (filled once per
+// CTA) instead of in every thread's registers, 8 registers per vector a thread holds each, so
+// CTAs of 288..448 threads fit twice per SM.
+template <typename T, int V, int kAffine, bool kSmemWB = false>
 __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const void *x,
                                                               const void *w, const void *b,
                                                               int64_t rows, int64_t hidden,
@@ -622,12 +625,23 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
     const float h = (float)hidden;
     const uint32_t row_bytes = (uint32_t)(hv * 16);
     const int64_t step = gridDim.x;
-    uint4 wv[V], bv[V];
+    // with kSmemWB: [ring][weight row, if any][bias row, if any]
+    unsigned char *sw = ring + (size_t)stages * row_bytes;
+    unsigned char *sb = sw + (kW ? row_bytes : 0u);
+    constexpr int VW = kSmemWB ? 1 : V;
+    uint4 wv[VW], bv[VW];
+    if (kSmemWB) {
+        for (int64_t c = t; c < hv; c += g) {
+            if (kW) *reinterpret_cast<uint4 *>(sw + c * 16) = __ldg(static_cast<const uint4 *>(w) + c);
+            if (kB) *reinterpret_cast<uint4 *>(sb + c * 16) = __ldg(static_cast<const uint4 *>(b) + c);
+        }
+    } else {
 #pragma unroll
-    for (int k = 0; k < V; ++k) {
-        const int64_t c = t + (int64_t)k * g;
-        wv[k] = (kW && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
-        bv[k] = (kB && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < VW; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            wv[k] = (kW && c < hv) ? __ldg(static_cast<const uint4 *>(w) + c) : make_uint4(0u, 0u, 0u, 0u);
+            bv[k] = (kB && c < hv) ? __ldg(static_cast<const uint4 *>(b) + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
     }
     uint64_t policy = 0;
     if (t == 0) {
@@ -685,15 +699,23 @@ __global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const v
         const float var = __fdiv_rn(cta_sum(ln_total(q2), red, slot), h);
         const float rstd = __frsqrt_rn(__fadd_rn(var, eps));
         const float shift = -__fmul_rn(mean, rstd);
+        if (!kSmemWB) {
 #pragma unroll
-        for (int k = 0; k < V; ++k) {  // unpack weight and bias per row, not hoisted as floats
-            opaque(wv[k]);
-            opaque(bv[k]);
+            for (int k = 0; k < VW; ++k) {  // unpack weight and bias per row, not hoisted as floats
+                opaque(wv[k]);
+                opaque(bv[k]);
+            }
         }
 #pragma unroll
         for (int k = 0; k < V; ++k) {
             const int64_t c = t + (int64_t)k * g;
-            if (c < hv) __stcs(og + row * hv + c, ln_out<T, kAffine>(xv[k], wv[k], bv[k], rstd, shift));
+            if (c < hv) {
+                const uint4 wk = kSmemWB ? (kW ? ld_shared_v4(sw + c * 16) : make_uint4(0u, 0u, 0u, 0u))
+                                         : wv[kSmemWB ? 0 : k];
+                const uint4 bk = kSmemWB ? (kB ? ld_shared_v4(sb + c * 16) : make_uint4(0u, 0u, 0u, 0u))
+                                         : bv[kSmemWB ? 0 : k];
+                __stcs(og + row * hv + c, ln_out<T, kAffine>(xv[k], wk, bk, rstd, shift));
+            }
         }
         if (++st == stages) {
             st = 0;
@@ -1100,7 +1122,9 @@ ks_plan_t silu_plan(bool vec, int64_t dv, ks_dtype_t dtype) {
 // take a team of `team` lanes per row at `v` vectors per lane (kind 'w'; 8- and 16-lane teams put
 // 4 or 2 rows in a warp), a CTA per row at `v` vectors (kind 'c'), the LayerNorm staged ring of
 // `v` rows per CTA (kind 'r'), the wide multi-pass kernel on `block` threads (kind 'x'), or the
-// general rule (kind 'g'); `prefetch` as the name says. The tables are generated, not edited:
+// LayerNorm ring with the weight and bias in shared memory (kind 'R', plan flag
+// KS_PLAN_AFFINE_SMEM), the general rule (kind 'g'); `prefetch` as the name says. The tables are
+// generated, not edited:
 //   python bench.py --ops-bands-record <JSON lines of bench.py --ops-bands> > record.json
 //   python bench.py --ops-bands-derive record.json
 // from GB300 runs of --ops-bands (8..256 and 288..4096 vectors; the record is committed as
@@ -1128,9 +1152,9 @@ constexpr int64_t kRingSmemLimit = 226 * 1024;  // dynamic shared memory a ring 
 // BEGIN GENERATED OP BANDS
 constexpr Band kSoftmax16[] = {{16, 'w', 2, true, 8}, {20, 'w', 4, false, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {45, 'w', 4, false, 16}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {112, 'w', 4, true}, {127, 'c', 4, false}, {129, 'w', 6, true}, {144, 'w', 6, false}, {169, 'w', 8, true}, {225, 'w', 8, false}, {512, 'g', 0, false}, {576, 'c', 4, true}, {640, 'g', 0, false}, {704, 'c', 4, true}, {768, 'g', 0, false}, {896, 'c', 4, true}, {1024, 'g', 0, false}, {2048, 'g', 0, true}, {2560, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
 constexpr Band kSoftmax32[] = {{8, 'w', 2, false, 8}, {12, 'w', 2, true, 8}, {20, 'w', 2, false, 16}, {28, 'w', 4, false, 8}, {32, 'w', 2, false}, {33, 'w', 4, false, 16}, {40, 'w', 2, false}, {53, 'w', 4, false, 16}, {56, 'w', 4, false}, {63, 'w', 4, true}, {64, 'g', 0, true}, {65, 'w', 4, false}, {72, 'w', 4, true}, {81, 'w', 6, false}, {96, 'w', 6, true}, {112, 'w', 8, false}, {127, 'c', 4, false}, {128, 'w', 4, false}, {129, 'w', 8, false}, {144, 'w', 8, true}, {168, 'w', 6, false}, {176, 'g', 0, false}, {177, 'c', 4, false}, {192, 'w', 6, false}, {208, 'c', 4, false}, {225, 'c', 4, true}, {256, 'w', 8, false}, {288, 'g', 0, false}, {320, 'c', 2, true}, {448, 'c', 4, true}, {512, 'c', 2, true}, {576, 'g', 0, false}, {640, 'c', 4, true}, {704, 'g', 0, false}, {768, 'c', 4, true}, {896, 'g', 0, false}, {1024, 'c', 4, true}, {1536, 'c', 4, false}, {1792, 'g', 0, true}, {2048, 'c', 4, false}, {2560, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormBf16[] = {{16, 'w', 2, true, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {64, 'w', 4, true, 16}, {127, 'w', 4, true}, {192, 'w', 6, true}, {256, 'w', 8, true}, {384, 'r', 2, true}, {448, 'r', 4, true}, {576, 'r', 2, true}, {640, 'r', 6, true}, {768, 'r', 5, true}, {1024, 'r', 4, true}, {1792, 'x', 4, true, 32, 128}, {2048, 'r', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormF16[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {56, 'w', 4, true, 16}, {64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true}, {448, 'g', 0, true}, {512, 'r', 3, true}, {576, 'c', 4, true}, {640, 'r', 6, true}, {896, 'c', 4, true}, {1024, 'r', 4, true}, {1792, 'x', 4, true, 32, 128}, {2048, 'c', 4, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormF32[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'c', 2, true}, {64, 'w', 4, true, 16}, {112, 'w', 4, true}, {127, 'c', 4, true}, {169, 'w', 6, true}, {225, 'w', 8, true}, {256, 'g', 0, true}, {288, 'r', 2, true}, {320, 'c', 2, true}, {512, 'g', 0, true}, {576, 'r', 2, true}, {640, 'c', 4, true}, {704, 'r', 6, true}, {768, 'c', 4, true}, {1024, 'x', 4, true, 32, 128}, {1152, 'r', 3, true}, {1408, 'r', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormBf16[] = {{16, 'w', 2, true, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {64, 'w', 4, true, 16}, {127, 'w', 4, true}, {192, 'w', 6, true}, {256, 'w', 8, true}, {384, 'r', 2, true}, {448, 'r', 4, true}, {640, 'r', 2, true}, {704, 'R', 3, true}, {768, 'R', 2, true}, {1024, 'r', 4, true}, {1792, 'R', 2, true}, {2048, 'r', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF16[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {56, 'w', 4, true, 16}, {64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true}, {448, 'g', 0, true}, {512, 'r', 3, true}, {576, 'c', 4, true}, {640, 'r', 6, true}, {704, 'R', 3, true}, {768, 'R', 2, true}, {896, 'c', 4, true}, {1024, 'r', 4, true}, {1280, 'R', 2, true}, {1408, 'x', 4, true, 32, 128}, {1792, 'R', 2, true}, {2048, 'c', 4, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF32[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'c', 2, true}, {64, 'w', 4, true, 16}, {112, 'w', 4, true}, {127, 'c', 4, true}, {169, 'w', 6, true}, {225, 'w', 8, true}, {256, 'g', 0, true}, {288, 'r', 2, true}, {320, 'c', 2, true}, {352, 'r', 6, true}, {512, 'g', 0, true}, {576, 'r', 2, true}, {640, 'c', 4, true}, {704, 'R', 4, true}, {768, 'c', 4, true}, {896, 'x', 4, true, 32, 128}, {1024, 'r', 6, true}, {1152, 'R', 3, true}, {1408, 'r', 2, true}, {1792, 'x', 4, true, 32, 128}, {2048, 'R', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
 // END GENERATED OP BANDS
 
 // Applies the band of a row of hv vectors to p (the general rule's plan) when there are more rows
@@ -1148,9 +1172,12 @@ void apply_band(const Band *bands, int64_t hv, int64_t rows, int sms, ks_plan_t 
     } else if (b->kind == 'c') {
         const int64_t block = round_up64(ceil_div64(hv, b->v), 32);
         if (block <= 512) *p = op_plan_of(KS_KERNEL_CTA_ROW, b->v, (int)block, b->prefetch);
-    } else if (b->kind == 'r') {
-        if (many && ring_block <= 512 && 128 + (int64_t)b->v * hv * 16 <= kRingSmemLimit)
+    } else if (b->kind == 'r' || b->kind == 'R') {
+        const int64_t affine = b->kind == 'R' ? 2 * hv * 16 : 0;  // weight and bias rows
+        if (many && ring_block <= 512 && 128 + (int64_t)b->v * hv * 16 + affine <= kRingSmemLimit) {
             *p = op_plan_of(KS_KERNEL_BULK_ROW, 4, (int)ring_block, true, b->v);
+            if (b->kind == 'R') p->flags |= KS_PLAN_AFFINE_SMEM;
+        }
     } else if (b->kind == 'x') {
         if (many || hv > 2048) *p = op_plan_of(KS_KERNEL_TWOPASS_ROW, 4, b->block, true);
     }
@@ -1214,8 +1241,10 @@ size_t ln_ring_smem(int stages, int64_t hv) { return 128 + (size_t)stages * (siz
 // CUDA call; `vec` tells whether the rows and pointers take 16-byte vectors, `width` is the row's
 // width in 16-byte vectors when they do (for SwiGLU the output row's), `elems` in elements.
 ks_status_t op_check(int op, ks_plan_t &p, bool vec, int64_t width, int64_t elems) {
-    if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL))
+    if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL | KS_PLAN_AFFINE_SMEM))
         return fail(KS_ERR_INVALID_ARGUMENT, "unknown plan flags 0x%x", (unsigned)p.flags);
+    if ((p.flags & KS_PLAN_AFFINE_SMEM) && !(op == kOpLayerNorm && p.kernel == KS_KERNEL_BULK_ROW))
+        return fail(KS_ERR_INVALID_ARGUMENT, "KS_PLAN_AFFINE_SMEM is for LayerNorm's staged ring");
     if (p.block < 32 || p.block % 32 != 0)
         return fail(KS_ERR_INVALID_ARGUMENT, "plan block %d is not a positive multiple of 32", p.block);
     if (p.kernel != KS_KERNEL_SCALAR && !vec)
@@ -1259,9 +1288,14 @@ ks_status_t op_check(int op, ks_plan_t &p, bool vec, int64_t width, int64_t elem
         if (!ln) return fail(KS_ERR_INVALID_ARGUMENT, "the staged ring is LayerNorm's");
         if (p.vec_per_thread != 4 || (int64_t)p.block * 4 < width || p.block > 512)
             return fail(KS_ERR_INVALID_ARGUMENT, "ring plan: 4 vectors per thread covering the row, block <= 512");
-        if (p.stages < 2 || p.stages > 8 || (int64_t)ln_ring_smem(p.stages, width) > kRingSmemLimit)
-            return fail(KS_ERR_INVALID_ARGUMENT, "ring of %d stages does not fit", p.stages);
-        p.smem_bytes = (int32_t)ln_ring_smem(p.stages, width);
+        {
+            // with the weight and bias in shared memory too (counted for both)
+            const int64_t affine = (p.flags & KS_PLAN_AFFINE_SMEM) ? 2 * width * 16 : 0;
+            if (p.stages < 2 || p.stages > 8 ||
+                (int64_t)ln_ring_smem(p.stages, width) + affine > kRingSmemLimit)
+                return fail(KS_ERR_INVALID_ARGUMENT, "ring of %d stages does not fit", p.stages);
+            p.smem_bytes = (int32_t)(ln_ring_smem(p.stages, width) + affine);
+        }
         break;
     case KS_KERNEL_TWOPASS_ROW:
         if (p.vec_per_thread != 4 || p.block > (ln ? 512 : 1024))
@@ -1476,10 +1510,18 @@ cudaError_t layer_norm_dispatch(const ks_plan_t &p, void *out, const void *x, co
                                layer_norm_wide_kernel<T, 4, 2>, layer_norm_wide_kernel<T, 4, 3>);
         break;
     case KS_KERNEL_BULK_ROW:
-        f = layer_norm_pick<T>(affine, layer_norm_bulk_kernel<T, 4, 0>, layer_norm_bulk_kernel<T, 4, 1>,
-                               layer_norm_bulk_kernel<T, 4, 2>, layer_norm_bulk_kernel<T, 4, 3>);
+        if (p.flags & KS_PLAN_AFFINE_SMEM) {
+            f = layer_norm_pick<T>(affine, layer_norm_bulk_kernel<T, 4, 0, true>,
+                                   layer_norm_bulk_kernel<T, 4, 1, true>,
+                                   layer_norm_bulk_kernel<T, 4, 2, true>,
+                                   layer_norm_bulk_kernel<T, 4, 3, true>);
+            smem = ln_ring_smem(stages, hv) + (size_t)((w ? 1 : 0) + (b ? 1 : 0)) * (size_t)hv * 16;
+        } else {
+            f = layer_norm_pick<T>(affine, layer_norm_bulk_kernel<T, 4, 0>, layer_norm_bulk_kernel<T, 4, 1>,
+                                   layer_norm_bulk_kernel<T, 4, 2>, layer_norm_bulk_kernel<T, 4, 3>);
+            smem = ln_ring_smem(stages, hv);
+        }
         args = bulk_args;
-        smem = ln_ring_smem(stages, hv);
         break;
     case KS_KERNEL_SCALAR:
         f = layer_norm_pick<T>(affine, layer_norm_scalar_kernel<T, 0>, layer_norm_scalar_kernel<T, 1>,

@@ -515,10 +515,13 @@ def test_next_op_plans_follow_the_bands():
     # LayerNorm fp16 rows of 65..128 vectors: warp rows at 4 vectors
     p = op_plan(LN, 1000, 96 * 8, F16)
     assert (p.kernel, p.vec_per_thread, p.flags) == (WARP, 4, 0)
-    # LayerNorm many rows of 1024 bf16 vectors: the staged ring; 1280: the wide kernel's 128 threads
+    # LayerNorm many rows of 1024 bf16 vectors: the staged ring; 1280: a 2-stage ring with the
+    # weight and bias rows in shared memory; 2560: the wide kernel's 128 threads
     p = op_plan(LN, 32768, 1024 * 8)
-    assert (p.kernel, p.vec_per_thread, p.block, p.stages) == (BULK, 4, 256, 4)
+    assert (p.kernel, p.vec_per_thread, p.block, p.stages, p.flags) == (BULK, 4, 256, 4, 0)
     p = op_plan(LN, 32768, 1280 * 8)
+    assert (p.kernel, p.block, p.stages, p.flags) == (BULK, 320, 2, _abi.KS_PLAN_AFFINE_SMEM)
+    p = op_plan(LN, 32768, 2560 * 8)
     assert (p.kernel, p.block) == (TWO, 128)
     # SwiGLU: the row kernel for rows of a multiple of 32 vectors (fp32: 64), else the flat walk
     # on 128-thread CTAs
@@ -534,6 +537,25 @@ def test_next_op_plans_follow_the_bands():
         assert op_plan(op, 10, 1001).kernel == _abi.KS_KERNEL_SCALAR
         assert op_plan(op, 10, 1024, aligned=False).kernel == _abi.KS_KERNEL_SCALAR
     assert op_plan(SM, 0, 1024).kernel == _abi.KS_KERNEL_NONE
+
+
+def test_affine_smem_flag_only_for_the_layer_norm_ring():
+    """KS_PLAN_AFFINE_SMEM is refused on any plan but LayerNorm's staged ring, and a ring whose
+    stages plus the weight and bias rows exceed shared memory is refused (before any CUDA call;
+    every plan here is invalid, so the fake pointers are never used)."""
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    a, b, c = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    F = _abi.KS_PLAN_AFFINE_SMEM
+    # RMSNorm: an unknown flag
+    p = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 256, 2, flags=F)
+    assert _abi.ks_rms_norm_planned(a, b, c, 64, 8192, 1e-6, BF16, p, None) == E
+    # Softmax and LayerNorm CTA rows: not the ring
+    p = _abi.make_plan(_abi.KS_KERNEL_CTA_ROW, 4, 256, flags=F)
+    assert _abi.ks_softmax_planned(a, b, 64, 8192, BF16, p, None) == E
+    assert _abi.ks_layer_norm_planned(a, b, None, None, 64, 8192, 1e-5, BF16, p, None) == E
+    # LayerNorm ring of 2048 vectors: 6 stages fit alone (192 KiB), not with two more rows
+    p = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 512, 6, flags=F)
+    assert _abi.ks_layer_norm_planned(a, b, None, None, 64, 16384, 1e-5, BF16, p, None) == E
 
 
 def test_next_op_planned_entry_points_check_the_plan():

@@ -39,6 +39,8 @@ ROW_VARIANTS = [
     ("c1", A.KS_KERNEL_CTA_ROW, 1, None, 0, 0), ("c2", A.KS_KERNEL_CTA_ROW, 2, None, 0, 0),
     ("c4", A.KS_KERNEL_CTA_ROW, 4, None, 0, 0), ("c4n", A.KS_KERNEL_CTA_ROW, 4, None, NP, 0),
     ("ring2", A.KS_KERNEL_BULK_ROW, 4, None, 0, 2), ("ring5", A.KS_KERNEL_BULK_ROW, 4, None, 0, 5),
+    ("ring2a", A.KS_KERNEL_BULK_ROW, 4, None, A.KS_PLAN_AFFINE_SMEM, 2),
+    ("ring4a", A.KS_KERNEL_BULK_ROW, 4, None, A.KS_PLAN_AFFINE_SMEM, 4),
     ("wide128", A.KS_KERNEL_TWOPASS_ROW, 4, 128, 0, 0),
     ("wide512", A.KS_KERNEL_TWOPASS_ROW, 4, 512, 0, 0),
     ("wide1024", A.KS_KERNEL_TWOPASS_ROW, 4, 1024, 0, 0),
@@ -60,7 +62,9 @@ def _row_plan(variant, op, dt, hidden):
             return None
     if op == "layer_norm" and flags & NP:
         return None  # LayerNorm always prefetches
-    if kernel == A.KS_KERNEL_BULK_ROW and (op != "layer_norm" or 128 + stages * hv * 16 > 226 * 1024):
+    affine_rows = 2 if flags & A.KS_PLAN_AFFINE_SMEM else 0
+    if kernel == A.KS_KERNEL_BULK_ROW and (op != "layer_norm" or
+                                           128 + (stages + affine_rows) * hv * 16 > 226 * 1024):
         return None
     if kernel == A.KS_KERNEL_TWOPASS_ROW and op == "layer_norm" and block > 512:
         return None
@@ -104,15 +108,19 @@ def _ln_check(out, ref, dt, h, name):
 @pytest.mark.parametrize("variant", ROW_VARIANTS, ids=[v[0] for v in ROW_VARIANTS])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("rows,hidden", SHAPES)
-@pytest.mark.parametrize("affine", ["both", "none"])
+@pytest.mark.parametrize("affine", ["both", "none", "weight", "bias"])
 def test_layer_norm_every_variant(cuda_device, variant, dtype, rows, hidden, affine):
     dt = synth.dtype_of(dtype)
     plan = _row_plan(variant, "layer_norm", dt, hidden)
     if plan is None:
         pytest.skip("variant does not fit this width")
+    if affine in ("weight", "bias") and not plan.flags & A.KS_PLAN_AFFINE_SMEM:
+        # one of the two rows: for the ring that holds them in shared memory, where the bias row
+        # sits after the weight row only when there is one
+        pytest.skip("weight-only and bias-only: the shared-memory affine ring")
     x = synth.cast(synth.normal_np((rows, hidden), 872) + 0.25, dt)
-    w = synth.weight(hidden, dt) if affine == "both" else None
-    b = synth.cast(synth.normal_np((hidden,), 873, std=0.1), dt) if affine == "both" else None
+    w = synth.weight(hidden, dt) if affine in ("both", "weight") else None
+    b = synth.cast(synth.normal_np((hidden,), 873, std=0.1), dt) if affine in ("both", "bias") else None
     xd = x.to(cuda_device)
     yd = torch.empty_like(xd)
     wd = w.to(cuda_device) if w is not None else None
