@@ -1125,7 +1125,8 @@ def plan_candidates(op: str, hv: int, elem: int):
     split kernel with two rows in flight per cluster, no prefetch), and for
     rows wider than 2048 vectors cC (register-resident cluster of C CTAs, 4 vectors per thread)
     and bCsS / bCsSv8 (the staged kernel split over C CTAs, S stages, 4 or 8 vectors per
-    thread)."""
+    thread; bCsS[v8]m, the plain op: the rows kept in shared memory, two in flight, C up to
+    16)."""
     from row_wise_rmsnorm_ks_gb300 import _abi
 
     up32 = lambda n: -(-n // 32) * 32
@@ -1173,19 +1174,25 @@ def plan_candidates(op: str, hv: int, elem: int):
                     out.append((f"s{c}b{blk}u{u}p", _abi.make_plan(
                         _abi.KS_KERNEL_TWOPASS_ROW, u, blk, 2, cluster=c, flags=npf)))
     if hv > 2048:
-        for c in (2, 4, 8):
+        for c in (2, 4, 8, 16):
             sl = -(-hv // c)
             b = up32(-(-sl // 4))
-            if b <= 512:
+            if b <= 512 and c <= 8:
                 out.append((f"c{c}", _abi.make_plan(_abi.KS_KERNEL_CLUSTER_ROW, 4, b, cluster=c)))
             for vv in ((4,) if fused else (4, 8)):
                 b = up32(-(-sl // vv))
-                if b > 512:
+                # the shared-memory rows kernel takes up to 1024 threads at 4 vectors
+                if b > (1024 if vv == 4 and not fused else 512):
                     continue
-                for st in (2, 3, 4):
+                for st in ((2, 3, 4) if c <= 8 and b <= 512 else ()):
                     if 128 + st * sl * 16 * (2 if fused else 1) <= 226 * 1024:
                         out.append((f"b{c}s{st}" + ("v8" if vv == 8 else ""), _abi.make_plan(
                             _abi.KS_KERNEL_BULK_ROW, vv, b, st, cluster=c)))
+                for st in (() if fused else (2, 3, 4, 6)):  # rows kept in shared memory
+                    if 128 + st * sl * 16 <= 226 * 1024:
+                        out.append((f"b{c}s{st}" + ("v8" if vv == 8 else "") + "m", _abi.make_plan(
+                            _abi.KS_KERNEL_BULK_ROW, vv, b, st, cluster=c,
+                            flags=_abi.KS_PLAN_SMEM_ROWS)))
     return out
 
 
@@ -1230,7 +1237,7 @@ def run_plan_sweep(args) -> int:
             r = synth.cast(synth.normal_dev((R, H), synth.SEED_RESIDUAL, dev), dt)
             y = torch.empty_like(x)
             w = synth.weight(H, dt).to(dev)
-            for op in ("rms_norm", "fused_add_rms_norm"):
+            for op in args.plan_sweep_ops.split(","):
                 nb = algorithmic_bytes(op, R, H, elem)
                 fns = []
                 for name, p in [("default", None)] + plan_candidates(op, hv, elem):
@@ -1863,7 +1870,8 @@ def wide_plan_fields(name: str):
     """(kernel, cluster, block, v, stages, flags) of a plan-sweep candidate name for rows wider
     than 2048 vectors (block 0: fitted to the slice, ceil(ceil(hv / cluster) / v) rounded up to a
     warp): tBuU[n] the two-pass kernel, sCbBuU[n|p] split over a cluster (p: two rows in
-    flight), cC the register-resident cluster kernel, bCsS[v8] the staged kernel."""
+    flight), cC the register-resident cluster kernel, bCsS[v8][m] the staged kernel (m: the rows
+    kept in shared memory)."""
     import re
     from row_wise_rmsnorm_ks_gb300 import _abi
     npf = _abi.KS_PLAN_NO_PREFETCH
@@ -1878,10 +1886,10 @@ def wide_plan_fields(name: str):
     m = re.fullmatch(r"c(\d)", name)
     if m:
         return (_abi.KS_KERNEL_CLUSTER_ROW, int(m.group(1)), 0, 4, 0, 0)
-    m = re.fullmatch(r"b(\d)s(\d)(v8)?", name)
+    m = re.fullmatch(r"b(\d+)s(\d)(v8)?(m?)", name)
     if m:
         return (_abi.KS_KERNEL_BULK_ROW, int(m.group(1)), 0, 8 if m.group(3) else 4,
-                int(m.group(2)), 0)
+                int(m.group(2)), _abi.KS_PLAN_SMEM_ROWS if m.group(4) else 0)
     return None
 
 
@@ -1889,9 +1897,11 @@ def wide_bands_record(log_paths, sm_count: int) -> dict:
     """The measured record behind the wide band table, from --plan-sweep runs: per dtype, op and
     width (2049..32768 vectors), the candidates within 5 points of that width's best (thousandths
     of the measured copy peak; a candidate further behind can never be a band's launch under a
-    one-point rule) and the default's score. A width measured by several runs keeps the mean."""
+    one-point rule) and the default's score. A width measured several times in one run keeps the
+    mean; a later run that measured a width replaces the earlier runs' lines for it (a run may
+    measure candidates the earlier ones did not)."""
     acc = {}
-    for path in log_paths:
+    for i, path in enumerate(log_paths):
         for ln in open(path):
             if not ln.startswith('{"plan_sweep"'):
                 continue
@@ -1899,7 +1909,9 @@ def wide_bands_record(log_paths, sm_count: int) -> dict:
             if "default" not in d or not (WIDE_LO <= d["hv"] <= WIDE_HI):
                 continue
             key = (f"{d['plan_sweep']}/{d['op']}", d["hv"])
-            slot = acc.setdefault(key, {"rows": d["rows"], "runs": []})
+            slot = acc.get(key)
+            if slot is None or slot["run"] != i:
+                slot = acc[key] = {"rows": d["rows"], "runs": [], "run": i}
             slot["runs"].append({k: v for k, v in d.items() if isinstance(v, float)})
     tables = {}
     for (key, hv), slot in sorted(acc.items()):
@@ -1920,13 +1932,15 @@ def derive_wide_bands(record: dict, tol: int = 10) -> dict:
     """The wide band table a record implies, by the rule of derive_plan_bands: the fewest bands
     such that at every measured width the band's launch scores within `tol` thousandths of that
     width's best; each band as wide as the launches common to its widths allow, the launch with
-    the best mean among them; the last band reaching to 32768 vectors. Returns
-    {"dtype/op": [(hi, name)]}."""
+    the best mean among them; the last band reaching to 32768 vectors. Only portable cluster
+    sizes (at most 8 CTAs) are candidates, so the default launch never depends on the device
+    placing a larger cluster. Returns {"dtype/op": [(hi, name)]}."""
     out = {}
     for key, lines in record["tables"].items():
         ok = []
         for ln in lines:
-            sc = {n: v for n, v in ln["scores"].items() if n != "default"}
+            sc = {n: v for n, v in ln["scores"].items()
+                  if n != "default" and wide_plan_fields(n)[1] <= 8}
             best = max(sc.values())
             ok.append({n for n, v in sc.items() if v >= best - tol})
         bands, i = [], 0
@@ -2140,6 +2154,8 @@ def main() -> int:
                          "state and right after a large-shared-memory kernel, and exit")
     ap.add_argument("--plan-sweep-rounds", type=int, default=3)
     ap.add_argument("--plan-sweep-dtypes", default="bf16,fp16,fp32")
+    ap.add_argument("--plan-sweep-ops", default="rms_norm,fused_add_rms_norm",
+                    help="--plan-sweep: the operators, comma-separated")
     ap.add_argument("--plan-sweep-widths", default="",
                     help="comma-separated row widths in 16-byte vectors (default: the full grid)")
     ap.add_argument("--next-rows", type=int, default=32768,

@@ -137,7 +137,8 @@ typedef struct ks_plan {
     int32_t flags;          /* KS_PLAN_* bits below */
     int32_t cluster;        /* CTAs per cluster, one cluster per row: the cluster-row kernel
                                (2..8), or the staged or two-pass kernel split over a cluster
-                               (2..8; 0 or 1: one CTA per row); 0 for the other kernels */
+                               (2..8, the staged kernel with KS_PLAN_SMEM_ROWS 2..16; 0 or 1:
+                               one CTA per row); 0 for the other kernels */
 } ks_plan_t;
 
 /* Plan flags. KS_PLAN_NO_PREFETCH: the register kernels (warp and CTA rows) load each row when
@@ -151,6 +152,12 @@ typedef struct ks_plan {
  * shared memory beside the ring instead of in every thread's registers (fewer registers, so more
  * resident CTAs); the ring's shared memory grows by a row per array given. */
 #define KS_PLAN_AFFINE_SMEM 4
+/* KS_PLAN_SMEM_ROWS (RMSNorm without the residual, the staged kernel split over a cluster, 2 or
+ * more stages): each row slice stays in its shared-memory stage through both passes instead of
+ * moving into registers, and the CTA keeps two rows in flight, so one row's cluster exchange
+ * overlaps the next row's sum of squares. vec_per_thread (4 or 8) then sizes only the weight
+ * slice each thread holds. */
+#define KS_PLAN_SMEM_ROWS 8
 
 enum {
     KS_KERNEL_NONE = 0,     /* rows == 0: nothing is launched */
@@ -213,10 +220,12 @@ ks_status_t ks_plan_launch(int32_t op, int64_t rows, int64_t hidden, ks_dtype_t 
  * exceeds the kernel's bound (warp rows 256, CTA rows 1024 at 2 vectors and 512 at 4, staged
  * rows 512, cluster rows 512, scalar 1024), a staged ring (stages 1..16) over 226 KB of shared
  * memory (per CTA: stages * slice * 16 bytes, twice that for the fused op), or a cluster outside
- * 2..8 CTAs whose slices (ceil(hv / cluster) vectors, at most block * vec_per_thread each) do not
- * cover the row or leave a CTA without vectors. grid <= 0 lets the library size the persistent
- * grid; cluster grids are whole clusters, capped by the number the device can hold resident at
- * once. smem_bytes and rows_per_pass are recomputed. The plan is read, never written.
+ * 2..8 CTAs (2..16 with KS_PLAN_SMEM_ROWS) whose slices (ceil(hv / cluster) vectors, at most
+ * block * vec_per_thread each) do not cover the row or leave a CTA without vectors; a plan the
+ * device cannot hold resident (e.g. a cluster of 16 it cannot place) gives KS_ERR_CUDA before any
+ * launch. grid <= 0 lets the library size the persistent grid; cluster grids are whole clusters,
+ * capped by the number the device can hold resident at once. smem_bytes and rows_per_pass are
+ * recomputed. The plan is read, never written.
  */
 ks_status_t ks_rms_norm_planned(void *out, const void *x, const void *weight, int64_t rows,
                                 int64_t hidden, float eps, ks_dtype_t dtype,

@@ -25,6 +25,7 @@ KS_FAULT_WAIT_TIMEOUT = 1
 KS_PLAN_NO_PREFETCH = 1
 KS_PLAN_PDL = 2
 KS_PLAN_AFFINE_SMEM = 4
+KS_PLAN_SMEM_ROWS = 8
 KS_LAUNCH_PDL = 1
 
 # Every symbol include/ks.h declares (checked by the CPU test of the boundary).

@@ -75,13 +75,18 @@ std::unordered_map<uint64_t, int> g_occ;  // occupancy facts per (device, kernel
 
 // Key of an occupancy fact: the device, what is asked (CTAs per SM or resident clusters), and
 // every plan field that selects the kernel or changes its residency.
+// Every field that selects the kernel or its resources: shared memory below 256 KiB (18 bits),
+// block up to 1024 (11), stages (5), flags (4), cluster up to 16 (5), vectors per thread up to 8
+// (4), kernel (3), op, dtype, the query kind, the warp-row team (8, 16 or a full warp) and the
+// device.
 uint64_t occ_key(int dev, ks_dtype_t d, bool fused, const ks_plan_t &p, bool clusters) {
-    return ((uint64_t)(dev & 0x3F) << 58) | ((uint64_t)clusters << 57) |
-           ((uint64_t)(d & 0x3) << 55) | ((uint64_t)fused << 54) |
-           ((uint64_t)(p.kernel & 0x7) << 51) | ((uint64_t)(p.vec_per_thread & 0x7) << 48) |
-           ((uint64_t)(p.cluster & 0xF) << 44) | ((uint64_t)(p.flags & 0x3) << 42) |
-           ((uint64_t)(p.stages & 0x1F) << 37) | ((uint64_t)(p.block & 0x7FF) << 26) |
-           (uint64_t)(p.smem_bytes & 0x3FFFFFF);
+    const uint64_t team = p.kernel == KS_KERNEL_WARP_ROW ? (p.team == 8 ? 1u : (p.team == 16 ? 2u : 0u)) : 0u;
+    return ((uint64_t)(dev & 0x3F) << 56) | (team << 54) | ((uint64_t)clusters << 53) |
+           ((uint64_t)(d & 0x3) << 51) | ((uint64_t)fused << 50) |
+           ((uint64_t)(p.kernel & 0x7) << 47) | ((uint64_t)(p.vec_per_thread & 0xF) << 43) |
+           ((uint64_t)(p.cluster & 0x1F) << 38) | ((uint64_t)(p.flags & 0xF) << 34) |
+           ((uint64_t)(p.stages & 0x1F) << 29) | ((uint64_t)(p.block & 0x7FF) << 18) |
+           (uint64_t)(p.smem_bytes & 0x3FFFF);
 }
 
 constexpr int kSmemLimit = 226 * 1024;  // dynamic ring; static smem and reserve fit in 227 KB
@@ -133,8 +138,11 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
     const bool split_bulk = p.kernel == KS_KERNEL_BULK_ROW && p.cluster >= 2;
     const bool split_twopass = p.kernel == KS_KERNEL_TWOPASS_ROW && p.cluster >= 2;
     p.cluster = (p.kernel == KS_KERNEL_CLUSTER_ROW || split_bulk || split_twopass) ? p.cluster : 0;
-    if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL))
+    if (p.flags & ~(KS_PLAN_NO_PREFETCH | KS_PLAN_PDL | KS_PLAN_SMEM_ROWS))
         return fail(KS_ERR_INVALID_ARGUMENT, "unknown plan flags 0x%x", (unsigned)p.flags);
+    if ((p.flags & KS_PLAN_SMEM_ROWS) && !(split_bulk && !fused && p.stages >= 2))
+        return fail(KS_ERR_INVALID_ARGUMENT, "KS_PLAN_SMEM_ROWS: the plain op's staged kernel split "
+                    "over a cluster, 2 or more stages");
     int64_t rows_per_cta = 1;
     switch (p.kernel) {
     case KS_KERNEL_WARP_ROW:
@@ -159,13 +167,16 @@ ks_status_t check_plan(ks_plan_t &p, bool fused, int64_t rows, int64_t hidden, i
         const bool bulk_v = p.vec_per_thread == 4 || (split_bulk && !fused && p.vec_per_thread == 8);
         if (bulk ? !bulk_v : (p.vec_per_thread != 2 && p.vec_per_thread != 4))
             return fail(KS_ERR_INVALID_ARGUMENT, "unsupported vectors per thread %d", p.vec_per_thread);
-        if (split_bulk && p.cluster > 8)
-            return fail(KS_ERR_INVALID_ARGUMENT, "cluster of %d CTAs (2..8 supported)", p.cluster);
+        if (split_bulk && p.cluster > ((p.flags & KS_PLAN_SMEM_ROWS) ? 16 : 8))
+            return fail(KS_ERR_INVALID_ARGUMENT, "cluster of %d CTAs (2..8 supported; 2..16 with "
+                        "KS_PLAN_SMEM_ROWS)", p.cluster);
         const int C = split_bulk ? p.cluster : 1;
         const int64_t slice = ceil_div(hv, C);
         if ((C - 1) * slice >= hv)
             return fail(KS_ERR_INVALID_ARGUMENT, "a cluster of %d leaves a CTA without vectors", C);
-        const int bound = bulk ? 512 : (p.vec_per_thread == 2 ? 1024 : 512);
+        // the shared-memory rows kernel holds only the weight in registers: 1024 threads at 4
+        const bool smem_rows = (p.flags & KS_PLAN_SMEM_ROWS) && p.vec_per_thread == 4;
+        const int bound = bulk ? (smem_rows ? 1024 : 512) : (p.vec_per_thread == 2 ? 1024 : 512);
         if ((int64_t)p.block * p.vec_per_thread < slice || p.block > bound)
             return fail(KS_ERR_INVALID_ARGUMENT, "CTA-row plan does not cover the row or block > %d", bound);
         p.team = p.block * C;
@@ -597,16 +608,17 @@ struct WideBand {
 };
 constexpr int64_t kWideLo = 2049, kWideHi = 32768;
 // BEGIN GENERATED WIDE BANDS
-constexpr WideBand kWideBandsF32Plain[] = {{2560, 6, 0, 256, 4, 0, 1}, {2816, 6, 0, 512, 4, 0, 0}, {3584, 6, 0, 512, 4, 0, 1}, {4608, 4, 2, 0, 8, 4, 0}, {7168, 6, 0, 512, 4, 0, 1}, {9216, 4, 4, 0, 8, 4, 0}, {10240, 4, 4, 0, 8, 2, 0}, {14336, 6, 4, 512, 2, 0, 0}, {20480, 6, 4, 512, 2, 0, 1}, {32768, 4, 8, 0, 8, 2, 0}};
+constexpr WideBand kWideBandsF32Plain[] = {{2304, 6, 0, 256, 4, 0, 1}, {2560, 4, 2, 0, 8, 3, 8}, {2816, 6, 0, 512, 4, 0, 0}, {3584, 4, 4, 0, 8, 2, 8}, {4096, 4, 2, 0, 8, 4, 0}, {4608, 4, 2, 0, 8, 3, 0}, {5120, 4, 2, 0, 4, 4, 8}, {6144, 4, 2, 0, 4, 3, 8}, {7168, 4, 8, 0, 4, 4, 8}, {9216, 4, 4, 0, 8, 4, 0}, {10240, 4, 8, 0, 4, 4, 8}, {12288, 4, 4, 0, 4, 4, 8}, {14336, 4, 4, 0, 4, 3, 8}, {16384, 4, 8, 0, 8, 3, 8}, {20480, 6, 4, 512, 2, 0, 0}, {32768, 4, 8, 0, 8, 2, 0}};
 constexpr WideBand kWideBandsF32Fused[] = {{2304, 4, 2, 0, 4, 2, 0}, {3072, 6, 0, 512, 2, 0, 1}, {4096, 6, 2, 256, 4, 2, 1}, {5120, 4, 4, 0, 4, 2, 0}, {6144, 4, 8, 0, 4, 2, 0}, {8192, 6, 4, 256, 4, 2, 1}, {10240, 6, 4, 512, 2, 2, 1}, {16384, 4, 8, 0, 4, 3, 0}, {20480, 6, 8, 512, 2, 2, 1}, {28672, 6, 8, 256, 4, 2, 1}, {32768, 6, 4, 512, 4, 2, 1}};
-constexpr WideBand kWideBandsF16Plain[] = {{2304, 4, 4, 0, 8, 2, 0}, {3072, 6, 0, 256, 4, 0, 1}, {4096, 6, 0, 512, 4, 0, 0}, {5120, 6, 0, 512, 2, 0, 0}, {7168, 4, 2, 0, 8, 2, 0}, {8192, 6, 2, 256, 4, 2, 1}, {14336, 4, 8, 0, 8, 2, 0}, {24576, 6, 4, 256, 4, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
+constexpr WideBand kWideBandsF16Plain[] = {{2304, 4, 4, 0, 8, 2, 0}, {3072, 6, 0, 256, 4, 0, 1}, {4096, 6, 0, 512, 4, 0, 0}, {5120, 6, 0, 512, 2, 0, 0}, {7168, 4, 2, 0, 8, 2, 0}, {8192, 4, 2, 0, 8, 3, 8}, {14336, 4, 8, 0, 8, 2, 0}, {16384, 4, 4, 0, 8, 3, 8}, {24576, 6, 4, 256, 4, 2, 1}, {28672, 6, 4, 512, 2, 0, 0}, {32768, 4, 8, 0, 8, 2, 0}};
 constexpr WideBand kWideBandsF16Fused[] = {{2560, 6, 0, 512, 2, 0, 1}, {3072, 4, 2, 0, 4, 2, 0}, {3584, 4, 8, 0, 4, 4, 0}, {5120, 6, 2, 512, 2, 2, 1}, {7168, 4, 4, 0, 4, 3, 0}, {12288, 6, 4, 512, 2, 2, 1}, {14336, 6, 4, 256, 4, 2, 1}, {32768, 6, 8, 256, 4, 2, 1}};
-constexpr WideBand kWideBandsBf16Plain[] = {{2304, 6, 0, 512, 2, 0, 0}, {2560, 4, 2, 0, 8, 4, 0}, {3072, 6, 0, 256, 4, 0, 1}, {3584, 6, 0, 512, 4, 0, 0}, {4096, 6, 0, 512, 2, 0, 1}, {4608, 6, 0, 512, 4, 0, 0}, {5120, 4, 4, 0, 8, 4, 0}, {8192, 4, 4, 0, 4, 2, 0}, {9216, 4, 8, 0, 8, 2, 0}, {10240, 4, 8, 0, 8, 4, 0}, {14336, 4, 4, 0, 8, 2, 0}, {16384, 4, 8, 0, 4, 2, 0}, {28672, 6, 4, 512, 2, 2, 1}, {32768, 4, 8, 0, 8, 2, 0}};
+constexpr WideBand kWideBandsBf16Plain[] = {{2304, 6, 0, 512, 2, 0, 0}, {2560, 4, 2, 0, 8, 4, 0}, {2816, 6, 0, 256, 4, 0, 1}, {3072, 4, 2, 0, 8, 4, 8}, {3584, 6, 0, 512, 4, 0, 0}, {4096, 4, 4, 0, 8, 4, 8}, {4608, 4, 4, 0, 8, 3, 8}, {5120, 4, 4, 0, 8, 4, 0}, {6144, 4, 4, 0, 8, 4, 8}, {7168, 4, 2, 0, 8, 3, 8}, {8192, 4, 2, 0, 4, 3, 8}, {10240, 4, 8, 0, 8, 3, 8}, {14336, 4, 4, 0, 8, 2, 0}, {16384, 4, 4, 0, 4, 3, 8}, {28672, 6, 4, 512, 2, 2, 1}, {32768, 4, 8, 0, 8, 2, 0}};
 constexpr WideBand kWideBandsBf16Fused[] = {{2304, 4, 8, 0, 4, 2, 0}, {2816, 4, 2, 0, 4, 2, 0}, {3072, 6, 0, 512, 2, 0, 1}, {3584, 6, 2, 512, 2, 2, 1}, {4096, 6, 2, 256, 4, 2, 1}, {5120, 6, 2, 512, 2, 2, 1}, {7168, 4, 8, 0, 4, 2, 0}, {10240, 6, 4, 512, 2, 2, 1}, {14336, 6, 4, 256, 4, 2, 1}, {16384, 4, 8, 0, 4, 3, 0}, {28672, 6, 8, 512, 2, 2, 1}, {32768, 6, 4, 512, 4, 2, 1}};
 // END GENERATED WIDE BANDS
 
 // Whether a wide table is well formed: widths rising to kWideHi, kernels that take rows this
-// wide, clusters of 2..8 CTAs where the kernel splits rows.
+// wide, clusters of 2..8 CTAs where the kernel splits rows (2..16 for the shared-memory rows
+// kernel).
 template <size_t N>
 constexpr bool wide_bands_ok(const WideBand (&b)[N]) {
     for (size_t i = 0; i < N; ++i) {
@@ -616,7 +628,8 @@ constexpr bool wide_bands_ok(const WideBand (&b)[N]) {
                            (k == KS_KERNEL_TWOPASS_ROW && c != 0);
         if (k != KS_KERNEL_TWOPASS_ROW && k != KS_KERNEL_BULK_ROW && k != KS_KERNEL_CLUSTER_ROW)
             return false;
-        if (split && (c < 2 || c > 8)) return false;
+        const int cmax = (k == KS_KERNEL_BULK_ROW && (b[i].flags & KS_PLAN_SMEM_ROWS)) ? 16 : 8;
+        if (split && (c < 2 || c > cmax)) return false;
         if (k == KS_KERNEL_TWOPASS_ROW && (b[i].block <= 0 || (b[i].v != 2 && b[i].v != 4))) return false;
         if (k == KS_KERNEL_BULK_ROW && (b[i].block != 0 || b[i].stages < 1 || (b[i].v != 4 && b[i].v != 8)))
             return false;
@@ -645,7 +658,9 @@ bool wide_band_row(ks_plan_t *p, int64_t hv, bool fused, ks_dtype_t dtype) {
     if (C >= 2 && (C - 1) * slice >= hv) return false;  // a CTA without vectors
     int64_t block = b->block;
     if (block == 0) block = round_up(ceil_div(slice, b->v), 32);
-    if (block > (b->kernel == KS_KERNEL_TWOPASS_ROW ? 1024 : 512)) return false;
+    const bool wide_block = b->kernel == KS_KERNEL_TWOPASS_ROW ||
+                            (b->kernel == KS_KERNEL_BULK_ROW && (b->flags & KS_PLAN_SMEM_ROWS) && b->v == 4);
+    if (block > (wide_block ? 1024 : 512)) return false;
     if (b->kernel == KS_KERNEL_BULK_ROW) {
         const int64_t smem = kRingHeader + (int64_t)b->stages * slice * 16 * (fused ? 2 : 1);
         if (smem > kSmemLimit || (fused && b->v != 4)) return false;

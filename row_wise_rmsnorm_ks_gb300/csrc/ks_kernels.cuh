@@ -1372,6 +1372,170 @@ __global__ void __launch_bounds__(512) rows_stage_split_kernel(const RowArgs a) 
     cluster.sync();
 }
 
+// Plain rows too wide for one CTA, kept in shared memory through both passes. As in
+// rows_stage_split_kernel, each row is split over a cluster of C CTAs (here up to 16, a
+// non-portable cluster size the launch opts into) and CTA q's slice streams
+// into a ring of `stages` shared-memory stages by bulk asynchronous copies; here the slice is not
+// copied into registers. The first pass sums its squares from the stage and the second reads it
+// again from there, so a thread holds only its V weight vectors, and the loop keeps two rows in
+// flight: iteration j forms row j's slice sum and sends it to the cluster, then waits for row
+// j - 1's sums, writes row j - 1's outputs from its stage and hands that stage to the row
+// `stages` iterations ahead (stages >= 2). The wait for one row's sums so overlaps the next
+// row's first pass, where the one-row loop leaves the SM without work for a cluster round trip
+// per row. With two rows in flight, a CTA may send row j's sum while a peer has yet to read its
+// row j - 3 slots, so the sum slots and their mbarriers cycle over four rows: a CTA sends row j
+// only after it has received every peer's row j - 2 sum, which each peer sends only after its
+// threads have read their row j - 4 slots. Waits are bounded, with the fault path of
+// rows_stage_split_kernel: after a time-out (here, or a peer's flag) the CTA keeps sending flags
+// and waiting for the remaining rows without touching rows or stages, then waits (bounded) for
+// its own copies in flight. Only the weight lives in registers, so at 4 vectors a thread the CTA
+// may have up to 1024 threads: the throughput of these rows grows with the threads per SM.
+template <typename T, int V>
+__global__ void __launch_bounds__(V >= 8 ? 512 : 1024) rows_stage_pipe_kernel(const RowArgs a) {
+    namespace cg = cooperative_groups;
+    using E = Elem<T>;
+    constexpr int P = E::kPerVec / 2;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[2][32];
+    __shared__ __align__(8) uint32_t part[4][16][2];  // per row slot: (sum bits, flag) by rank
+    __shared__ __align__(8) uint64_t pbar[4];           // completes when C sums have arrived
+
+    cg::cluster_group cluster = cg::this_cluster();
+    const int C = (int)cluster.num_blocks();
+    const int q = (int)cluster.block_rank();
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    unsigned char *ring = smem + 128;
+    const int g = blockDim.x, t = threadIdx.x;
+    const int64_t hv = a.hv;
+    const int64_t S = (hv + C - 1) / C;
+    const int64_t lo = q * S;
+    const int64_t nv = (lo + S < hv ? lo + S : hv) - lo;  // this CTA's vectors (>= 1)
+    const int stages = a.stages;
+    const uint32_t copy_bytes = (uint32_t)(nv * 16);
+    const uint32_t stage_bytes = (uint32_t)(S * 16);
+    const float h = (float)a.hidden;
+    const int64_t first = blockIdx.x / C;
+    const int64_t step = gridDim.x / C;
+    const int64_t n = first < a.rows ? (a.rows - 1 - first) / step + 1 : 0;  // the cluster's rows
+    const uint4 *xg = static_cast<const uint4 *>(a.x) + lo;
+    uint4 *og = static_cast<uint4 *>(a.out) + lo;
+
+    grid_dependency_wait();
+    allow_dependents_launch();
+    uint4 wv[V];
+    {
+        const uint4 *wg = static_cast<const uint4 *>(a.w) + lo;
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const int64_t c = t + (int64_t)k * g;
+            wv[k] = (c < nv) ? __ldg(wg + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    if (t == 0) {
+        for (int i = 0; i < stages; ++i) mbar_init(&bars[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&pbar[i], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // every CTA of the cluster has started and set up its barriers before any CTA sends to it
+    cluster.barrier_arrive();
+    cluster.barrier_wait();
+
+    uint64_t policy = 0;
+    uint32_t pending = 0;  // thread 0: stages with a copy in flight
+    uint32_t wphase = 0;   // bit i: the parity stage i's next copy completes with
+    auto issue = [&](int st, int64_t r) {
+        mbar_arrive_expect_tx(&bars[st], copy_bytes);
+        bulk_g2s(ring + (size_t)st * stage_bytes, xg + r * hv, copy_bytes, &bars[st], policy);
+        pending |= 1u << st;
+    };
+    if (t == 0) {
+        policy = l2_evict_first_policy();
+        for (int i = 0; i < stages && i < n; ++i) issue(i, first + (int64_t)i * step);
+    }
+
+    int sa = 0, sb = 0;  // the stages of the rows in the first and in the second pass
+    bool fault = false;
+    for (int64_t j = 0; j <= n; ++j) {
+        if (j < n) {  // first pass of row j
+            const int p = (int)(j & 1), sl = (int)(j & 3);
+            bool ok = true;
+            PairSumSq<E::kPairMath> acc;
+            if (!fault) {
+                ok = mbar_wait_bounded(&bars[sa], (wphase >> sa) & 1u);
+                if (ok) {
+                    const unsigned char *sx = ring + (size_t)sa * stage_bytes;
+#pragma unroll
+                    for (int k = 0; k < V; ++k) {
+                        const int64_t c = t + (int64_t)k * g;
+                        if (c < nv) {
+                            float2 f[P];
+                            const uint4 xv = ld_shared_v4(sx + c * 16);
+                            row_values<T, false>(xv, xv, f);
+                            acc.add(f);
+                        }
+                    }
+                }
+            }
+            const float wsum = warp_sum(acc.total());
+            if ((t & 31) == 0) red[p][t >> 5] = wsum;
+            const bool bad = __syncthreads_or(!ok || fault);
+            if (!fault && ok) wphase ^= 1u << sa;
+            if (t == 0) {
+                if (!fault && ok) pending &= ~(1u << sa);
+                mbar_arrive_expect_tx(&pbar[sl], (uint32_t)C * 8u);
+            }
+            if (t < C) {
+                float cta = 0.0f;
+                for (int i = 0; i < (g >> 5); ++i) cta += red[p][i];
+                st_async_v2(cluster_map(&part[sl][q][0], (uint32_t)t), __float_as_uint(cta),
+                            bad ? 1u : 0u, cluster_map(&pbar[sl], (uint32_t)t));
+            }
+            fault = bad;
+            if (++sa == stages) sa = 0;
+        }
+        if (j >= 1) {  // second pass of row j - 1
+            const int64_t jb = j - 1;
+            const int sl = (int)(jb & 3);
+            const bool got = mbar_wait_bounded(&pbar[sl], (uint32_t)(jb >> 2) & 1u);
+            float ss = 0.0f;
+            uint32_t any_bad = got ? 0u : 1u;
+            for (int r = 0; r < C; ++r) {
+                ss += __uint_as_float(part[sl][r][0]);
+                any_bad |= part[sl][r][1];
+            }
+            if (!fault && any_bad == 0u) {
+                const int64_t row = first + jb * step;
+                const float scale = row_scale(ss, h, a.eps);
+                const unsigned char *sx = ring + (size_t)sb * stage_bytes;
+#pragma unroll
+                for (int k = 0; k < V; ++k) {
+                    const int64_t c = t + (int64_t)k * g;
+                    if (c < nv) {
+                        float2 f[P];
+                        const uint4 xv = ld_shared_v4(sx + c * 16);
+                        row_values<T, false>(xv, xv, f);
+                        __stcs(og + row * hv + c, scaled_weighted<T>(f, scale, wv[k]));
+                    }
+                }
+            }
+            // every thread has read the stage and this row's slots: the stage goes to the row
+            // `stages` iterations ahead
+            const bool bad = __syncthreads_or(fault || any_bad != 0u);
+            if (t == 0 && !bad && jb + stages < n) issue(sb, first + (jb + stages) * step);
+            fault = bad;
+            if (++sb == stages) sb = 0;
+        }
+    }
+    if (fault && t == 0) {
+        atomicOr(&g_fault_flags, kFaultWaitTimeout);
+        // the copies this CTA issued that have not completed, before its shared memory goes
+        for (int i = 0; i < stages; ++i)
+            if ((pending >> i) & 1u) mbar_wait_bounded(&bars[i], (wphase >> i) & 1u);
+    }
+    cluster.sync();
+}
+
 // ----------------------------------------------------------------------- kernel selection
 
 // Sub-warp team kernels: 8 or 16 lanes per row, V vectors per lane.
@@ -1436,6 +1600,12 @@ const void *pick_kernel(const ks_plan_t &p) {
         default: return nullptr;
         }
     case KS_KERNEL_BULK_ROW:
+        if (p.cluster >= 2 && (p.flags & KS_PLAN_SMEM_ROWS)) {
+            if (kFused) return nullptr;
+            if (p.vec_per_thread == 4) return (const void *)rows_stage_pipe_kernel<T, 4>;
+            if (p.vec_per_thread == 8) return (const void *)rows_stage_pipe_kernel<T, 8>;
+            return nullptr;
+        }
         if (p.cluster >= 2) {
             if (p.vec_per_thread == 4) return (const void *)rows_stage_split_kernel<T, 4, kFused>;
             if (p.vec_per_thread == 8 && !kFused) return (const void *)rows_stage_split_kernel<T, 8, false>;
@@ -1476,6 +1646,10 @@ int blocks_per_sm_t(const ks_plan_t &p, bool fused) {
         if (p.smem_bytes > max_dynamic ||
             cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dynamic) !=
                 cudaSuccess)
+            return -1;
+        // clusters of more than 8 CTAs (the shared-memory rows kernel) are a non-portable size
+        if (p.cluster > 8 &&
+            cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             return -1;
     }
     int n = 0;

@@ -465,7 +465,12 @@ def test_every_width_gets_a_valid_plan(dtype, op):
                 elif p.kernel == BULK:
                     C = p.cluster if p.cluster >= 2 else 1
                     slice_ = -(-hv // C)
-                    assert p.block <= 512 and 1 <= p.stages <= 16 and C <= 8
+                    # the shared-memory rows kernel (plain op, split) runs up to 1024 threads
+                    # at 4 vectors and needs 2 stages
+                    smem_rows = bool(p.flags & _abi.KS_PLAN_SMEM_ROWS)
+                    assert not smem_rows or (op == 0 and C >= 2 and p.stages >= 2)
+                    bound = 1024 if smem_rows and p.vec_per_thread == 4 else 512
+                    assert p.block <= bound and 1 <= p.stages <= 16 and C <= 8
                     assert p.vec_per_thread == 4 or (p.vec_per_thread == 8 and op == 0 and C >= 2)
                     assert p.block * p.vec_per_thread >= slice_ and (C - 1) * slice_ < hv
                     assert p.smem_bytes <= 226 * 1024 and p.grid % C == 0
@@ -556,6 +561,32 @@ def test_affine_smem_flag_only_for_the_layer_norm_ring():
     # LayerNorm ring of 2048 vectors: 6 stages fit alone (192 KiB), not with two more rows
     p = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 512, 6, flags=F)
     assert _abi.ks_layer_norm_planned(a, b, None, None, 64, 16384, 1e-5, BF16, p, None) == E
+
+
+def test_smem_rows_flag_only_for_the_plain_split_ring():
+    """KS_PLAN_SMEM_ROWS is refused on the fused op, on a staged ring of one CTA per row or of
+    one stage, and on any other kernel (before any CUDA call; every plan here is invalid, so the
+    fake pointers are never used)."""
+    E = _abi.KS_ERR_INVALID_ARGUMENT
+    a, b, c = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    F = _abi.KS_PLAN_SMEM_ROWS
+    good = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 256, 2, flags=F, cluster=4)
+    assert _abi.ks_fused_add_rms_norm_planned(a, b, c, 64, 32768, 1e-6, BF16, good, None) == E
+    for p in (_abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 512, 2, flags=F),
+              _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 256, 1, flags=F, cluster=4),
+              _abi.make_plan(_abi.KS_KERNEL_TWOPASS_ROW, 4, 256, flags=F, cluster=4),
+              _abi.make_plan(_abi.KS_KERNEL_CTA_ROW, 4, 512, flags=F),
+              # clusters past 8 CTAs only with the flag, and never past 16
+              _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 128, 2, cluster=16),
+              _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 128, 2, flags=F, cluster=17),
+              # blocks past 512 threads only with the flag at 4 vectors, and never past 1024
+              _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 1024, 2, cluster=2),
+              _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 8, 1024, 2, flags=F, cluster=2),
+              _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 1056, 2, flags=F, cluster=2)):
+        assert _abi.ks_rms_norm_planned(a, b, c, 64, 32768, 1e-6, BF16, p, None) == E
+    # the next operators take no such flag
+    p = _abi.make_plan(_abi.KS_KERNEL_CTA_ROW, 4, 256, flags=F)
+    assert _abi.ks_softmax_planned(a, b, 64, 8192, BF16, p, None) == E
 
 
 def test_next_op_planned_entry_points_check_the_plan():

@@ -278,7 +278,8 @@ def _wide_name(p, hv):
     if p.kernel == K.KS_KERNEL_CLUSTER_ROW:
         return f"c{p.cluster}"
     if p.kernel == K.KS_KERNEL_BULK_ROW and p.cluster >= 2:
-        return f"b{p.cluster}s{p.stages}" + ("v8" if p.vec_per_thread == 8 else "")
+        return (f"b{p.cluster}s{p.stages}" + ("v8" if p.vec_per_thread == 8 else "")
+                + ("m" if p.flags & K.KS_PLAN_SMEM_ROWS else ""))
     raise AssertionError(p.as_dict())
 
 
@@ -299,8 +300,9 @@ def test_wide_default_plans_within_two_points_of_the_measured_best():
 @pytest.mark.parametrize("op", list(OPS))
 def test_every_wide_width_gets_a_plan_the_library_accepts(dt, op):
     """Every width of the wide table, with many rows past L2: the plan meets the rules the planned
-    entry points check (covered slices, no CTA without vectors, blocks and rings within bounds,
-    clusters of 2..8, whole clusters in the grid)."""
+    entry points check (covered slices, no CTA without vectors, blocks and rings within bounds:
+    512 threads, 1024 for the shared-memory rows kernel at 4 vectors; portable clusters of 2..8,
+    whole clusters in the grid)."""
     fused = op != "rms_norm"
     for hv in range(2049, 32769, 3):
         rows = max(4 * 152, -(-(160 << 20) // (hv * 32)) + 1)
@@ -312,7 +314,10 @@ def test_every_wide_width_gets_a_plan_the_library_accepts(dt, op):
             assert p.vec_per_thread in (2, 4) and p.block <= 1024
         else:
             assert p.kernel in (_abi.KS_KERNEL_BULK_ROW, _abi.KS_KERNEL_CLUSTER_ROW), p.as_dict()
-            assert 2 <= C <= 8 and p.block <= 512 and p.block * p.vec_per_thread >= sl
+            smem_rows = p.kernel == _abi.KS_KERNEL_BULK_ROW and p.flags & _abi.KS_PLAN_SMEM_ROWS
+            bound = 1024 if smem_rows and p.vec_per_thread == 4 else 512
+            assert 2 <= C <= 8 and p.block <= bound and p.block * p.vec_per_thread >= sl
+            assert not smem_rows or (not fused and p.stages >= 2)
             if p.kernel == _abi.KS_KERNEL_BULK_ROW:
                 assert p.vec_per_thread == 4 or (p.vec_per_thread == 8 and not fused)
                 assert p.smem_bytes == 128 + p.stages * sl * 16 * (2 if fused else 1)
