@@ -778,13 +778,76 @@ __global__ void __launch_bounds__(1024) layer_norm_scalar_kernel(void *out, cons
 // as the register kernels above. The first passes load with the default L2 policy, the last with
 // evict-first (last use).
 
+// Softmax, second pass: this thread's sum of the exponentials of its vectors of row xr (four
+// running sums, element e of a vector feeding lane e % 2 of sum (e / 2) % 2, added in a fixed
+// order at the end). The exponential's form (kFold) is a template argument, chosen once per row,
+// so the loop computes one form per element.
+template <typename T, int U, bool kFold>
+__device__ __forceinline__ float softmax_wide_sum(const uint4 *xr, int64_t hv, int t, int g,
+                                                  float neg_m, float bias) {
+    using E = Elem<T>;
+    constexpr int P = E::kPerVec / 2;
+    constexpr bool kPair = E::kPairMath;
+    const int64_t chunk = (int64_t)g * U;
+    float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = c0 + (int64_t)u * g;
+            v[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (c0 + (int64_t)u * g < hv) {
+                float2 f[P];
+                E::unpack2(v[u], f);
+#pragma unroll
+                for (int i = 0; i < P; ++i)
+                    s2[i & 1] = pair_add<kPair>(s2[i & 1], softmax_exp_pair<T, kPair, kFold>(f[i], neg_m, bias));
+            }
+        }
+    }
+    return __fadd_rn(__fadd_rn(s2[0].x, s2[0].y), __fadd_rn(s2[1].x, s2[1].y));
+}
+
+// Softmax, last pass: the outputs of row xr into orow (last use of the row: evict-first loads).
+template <typename T, int U, bool kFold>
+__device__ __forceinline__ void softmax_wide_out(const uint4 *xr, uint4 *orow, int64_t hv, int t,
+                                                 int g, float neg_m, float bias, float inv) {
+    using E = Elem<T>;
+    constexpr int P = E::kPerVec / 2;
+    constexpr bool kPair = E::kPairMath;
+    const int64_t chunk = (int64_t)g * U;
+    const float2 inv2 = make_float2(inv, inv);
+    for (int64_t c0 = t; c0 < hv; c0 += chunk) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = c0 + (int64_t)u * g;
+            v[u] = c < hv ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t c = c0 + (int64_t)u * g;
+            if (c < hv) {
+                float2 f[P];
+                E::unpack2(v[u], f);
+#pragma unroll
+                for (int i = 0; i < P; ++i)
+                    f[i] = pair_mul<kPair>(softmax_exp_pair<T, kPair, kFold>(f[i], neg_m, bias), inv2);
+                __stcs(orow + c, E::pack2(f));
+            }
+        }
+    }
+}
+
 // Softmax: max, sum of exponentials, outputs.
 template <typename T, int U>
 __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const void *x,
                                                             int64_t rows, int64_t hv) {
     using E = Elem<T>;
     constexpr int P = E::kPerVec / 2;
-    constexpr bool kPair = E::kPairMath;
     __shared__ float red[2][32];
     grid_dependency_wait();
     allow_dependents_launch();
@@ -816,54 +879,15 @@ __global__ void __launch_bounds__(1024) softmax_wide_kernel(void *out, const voi
         m = cta_max(m, red, slot);
         const float neg_m = -m;
         const float bias = __fmaf_rn(neg_m, kLog2e, 64.0f);
-        const bool fold = fabsf(m) <= kSoftmaxFoldMax;  // see softmax_exp_pair
-        float2 s2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = c0 + (int64_t)u * g;
-                v[u] = c < hv ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (c0 + (int64_t)u * g < hv) {
-                    float2 f[P];
-                    E::unpack2(v[u], f);
-#pragma unroll
-                    for (int i = 0; i < P; ++i)
-                        s2[i & 1] = pair_add<kPair>(
-                            s2[i & 1], fold ? softmax_exp_pair<T, kPair, true>(f[i], neg_m, bias)
-                                            : softmax_exp_pair<T, kPair, false>(f[i], neg_m, bias));
-                }
-            }
-        }
-        const float inv = __frcp_rn(
-            cta_sum(__fadd_rn(__fadd_rn(s2[0].x, s2[0].y), __fadd_rn(s2[1].x, s2[1].y)), red, slot));
-        const float2 inv2 = make_float2(inv, inv);
+        const bool fold = fabsf(m) <= kSoftmaxFoldMax;  // see softmax_exp_pair; uniform per row
+        const float part = fold ? softmax_wide_sum<T, U, true>(xr, hv, t, g, neg_m, bias)
+                                : softmax_wide_sum<T, U, false>(xr, hv, t, g, neg_m, bias);
+        const float inv = __frcp_rn(cta_sum(part, red, slot));
         uint4 *orow = og + row * hv;
-        for (int64_t c0 = t; c0 < hv; c0 += chunk) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = c0 + (int64_t)u * g;
-                v[u] = c < hv ? __ldcs(xr + c) : make_uint4(0u, 0u, 0u, 0u);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int64_t c = c0 + (int64_t)u * g;
-                if (c < hv) {
-                    float2 f[P];
-                    E::unpack2(v[u], f);
-#pragma unroll
-                    for (int i = 0; i < P; ++i)
-                        f[i] = pair_mul<kPair>(fold ? softmax_exp_pair<T, kPair, true>(f[i], neg_m, bias)
-                                                    : softmax_exp_pair<T, kPair, false>(f[i], neg_m, bias),
-                                               inv2);
-                    __stcs(orow + c, E::pack2(f));
-                }
-            }
-        }
+        if (fold)
+            softmax_wide_out<T, U, true>(xr, orow, hv, t, g, neg_m, bias, inv);
+        else
+            softmax_wide_out<T, U, false>(xr, orow, hv, t, g, neg_m, bias, inv);
     }
 }
 
