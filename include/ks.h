@@ -180,8 +180,9 @@ enum {
                                   step; the grid is capped so the rows in flight fit in L2,
                                   down to one CTA per SM. With cluster >= 2 each row is split
                                   over a cluster: CTA q runs both passes on its slice of
-                                  ceil(hv / cluster) vectors and the slice sums meet in
-                                  distributed shared memory, one cluster barrier per row;
+                                  ceil(hv / cluster) vectors and the slice sums reach every
+                                  CTA of the cluster by asynchronous shared-memory stores that
+                                  complete on the receiver's mbarrier;
                                   stages 2 keeps two rows in flight per cluster (the next
                                   row's first pass in the same loop as this row's second).
                                   Softmax and LayerNorm: their multi-pass wide kernel */
