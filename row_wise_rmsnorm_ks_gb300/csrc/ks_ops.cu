@@ -220,9 +220,13 @@ __global__ void __launch_bounds__(256) silu_mul_rows_kernel(void *out, const voi
 // Flat: the output [rows, dv] walked as one run of rows * dv vectors, grid-stride, two vectors
 // per thread per iteration, so every thread has work whatever the row width (a 256-thread block
 // laid across a row of 64 vectors left 7 of its 8 warps idle: bf16 d = 512 ran at 0.54 of the
-// copy peak). It spends more integer instructions per vector than the row-structured kernel.
-// Output vector i is input vector i + row * dv of the gate half (row = i / dv) and dv further on
-// of the up half; each thread divides once, then carries (row, column) forward by the stride.
+// copy peak). Output vector i is input vector i + row * dv of the gate half (row = i / dv) and dv
+// further on of the up half. Each thread divides once, then carries the column forward with
+// either the input index (16-bit types: a stride of 2 * step vectors moves it by 2 * step +
+// (2 * step / dv) * dv, and by dv more when the column wraps past the row's end, no multiply per
+// vector) or the row, the index formed from it per vector (fp32). Measured on GB300 at 48..1400
+// vectors: carrying the index read 0.92-0.94 of the copy peak for 16-bit types against 0.83-0.87
+// carrying the row, but 0.85-0.86 for fp32 against 0.92-0.94.
 template <typename T>
 __global__ void __launch_bounds__(256) silu_mul_flat_kernel(void *out, const void *x, int64_t rows,
                                                            int64_t dv) {
@@ -236,17 +240,23 @@ __global__ void __launch_bounds__(256) silu_mul_flat_kernel(void *out, const voi
     const int64_t step = (int64_t)gridDim.x * blockDim.x;
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= total) return;
-    // (row, column) of flat vector i, of i + step, and the increments of 2 * step
-    int64_t r0 = i / dv, c0 = i - r0 * dv;
+    constexpr bool kCarryIndex = sizeof(T) == 2;
+    // row, column and gate input index of flat vectors i and i + step, and the increments of
+    // 2 * step (one of the row and the index is carried, the other left to the compiler to drop)
+    int64_t r0 = i / dv;
+    int64_t c0 = i - r0 * dv, q0 = i + r0 * dv;
     const int64_t sr = step / dv, sc = step - sr * dv;
     const int64_t sr2 = (2 * step) / dv, sc2 = 2 * step - sr2 * dv;
-    int64_t r1 = r0 + sr, c1 = c0 + sc;
+    const int64_t dq = 2 * step + sr2 * dv;
+    int64_t c1 = c0 + sc, r1 = r0 + sr, q1 = q0 + step + sr * dv;
     if (c1 >= dv) {
         c1 -= dv;
         ++r1;
+        q1 += dv;
     }
     for (; i + step < total; i += 2 * step) {
-        const uint4 *p0 = xg + i + r0 * dv, *p1 = xg + i + step + r1 * dv;
+        const uint4 *p0 = xg + (kCarryIndex ? q0 : i + r0 * dv);
+        const uint4 *p1 = xg + (kCarryIndex ? q1 : i + step + r1 * dv);
         const uint4 g0 = __ldcs(p0), u0 = __ldcs(p0 + dv);
         const uint4 g1 = __ldcs(p1), u1 = __ldcs(p1 + dv);
         float a[N], b[N], r[N];
@@ -260,21 +270,26 @@ __global__ void __launch_bounds__(256) silu_mul_flat_kernel(void *out, const voi
 #pragma unroll
         for (int e = 0; e < N; ++e) r[e] = silu_mul<T>(a[e], b[e]);
         __stcs(og + i + step, E::pack(r));
-        r0 += sr2;
         c0 += sc2;
+        c1 += sc2;
+        if (kCarryIndex) {
+            q0 += dq;
+            q1 += dq;
+        } else {
+            r0 += sr2;
+            r1 += sr2;
+        }
         if (c0 >= dv) {
             c0 -= dv;
-            ++r0;
+            if (kCarryIndex) q0 += dv; else ++r0;
         }
-        r1 += sr2;
-        c1 += sc2;
         if (c1 >= dv) {
             c1 -= dv;
-            ++r1;
+            if (kCarryIndex) q1 += dv; else ++r1;
         }
     }
     if (i < total) {
-        const uint4 *p0 = xg + i + r0 * dv;
+        const uint4 *p0 = xg + (kCarryIndex ? q0 : i + r0 * dv);
         float a[N], b[N], r[N];
         E::unpack(__ldcs(p0), a);
         E::unpack(__ldcs(p0 + dv), b);
