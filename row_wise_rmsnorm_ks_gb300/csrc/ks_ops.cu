@@ -1189,8 +1189,8 @@ struct Band {
 constexpr int16_t kBandEnd = 32767;
 constexpr int64_t kRingSmemLimit = 226 * 1024;  // dynamic shared memory a ring CTA may take
 // BEGIN GENERATED OP BANDS
-constexpr Band kSoftmax16[] = {{16, 'w', 2, true, 8}, {20, 'w', 4, false, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {45, 'w', 4, false, 16}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {112, 'w', 4, true}, {127, 'c', 4, false}, {129, 'w', 6, true}, {144, 'w', 6, false}, {169, 'w', 8, true}, {225, 'w', 8, false}, {512, 'g', 0, false}, {576, 'c', 4, true}, {640, 'g', 0, false}, {704, 'c', 4, true}, {768, 'g', 0, false}, {896, 'c', 4, true}, {1024, 'g', 0, false}, {2048, 'g', 0, true}, {2560, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
-constexpr Band kSoftmax32[] = {{8, 'w', 2, false, 8}, {12, 'w', 2, true, 8}, {20, 'w', 2, false, 16}, {28, 'w', 4, false, 8}, {32, 'w', 2, false}, {33, 'w', 4, false, 16}, {40, 'w', 2, false}, {53, 'w', 4, false, 16}, {56, 'w', 4, false}, {63, 'w', 4, true}, {64, 'g', 0, true}, {65, 'w', 4, false}, {72, 'w', 4, true}, {81, 'w', 6, false}, {96, 'w', 6, true}, {112, 'w', 8, false}, {127, 'c', 4, false}, {128, 'w', 4, false}, {129, 'w', 8, false}, {144, 'w', 8, true}, {168, 'w', 6, false}, {176, 'g', 0, false}, {177, 'c', 4, false}, {192, 'w', 6, false}, {208, 'c', 4, false}, {225, 'c', 4, true}, {256, 'w', 8, false}, {288, 'g', 0, false}, {320, 'c', 2, true}, {448, 'c', 4, true}, {512, 'c', 2, true}, {576, 'g', 0, false}, {640, 'c', 4, true}, {704, 'g', 0, false}, {768, 'c', 4, true}, {896, 'g', 0, false}, {1024, 'c', 4, true}, {1536, 'c', 4, false}, {1792, 'g', 0, true}, {2048, 'c', 4, false}, {2560, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kSoftmax16[] = {{16, 'w', 2, true, 8}, {20, 'w', 4, false, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {45, 'w', 4, false, 16}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {112, 'w', 4, true}, {127, 'c', 4, false}, {129, 'w', 6, true}, {144, 'w', 6, false}, {169, 'w', 8, true}, {225, 'w', 8, false}, {512, 'g', 0, false}, {576, 'c', 4, true}, {640, 'g', 0, false}, {704, 'c', 4, true}, {768, 'g', 0, false}, {896, 'c', 4, true}, {1024, 'g', 0, false}, {2048, 'g', 0, true}, {2560, 'x', 4, true, 32, 128}, {6144, 'x', 4, true, 32, 256}, {8192, 'x', 4, true, 32, 512}, {kBandEnd, 'g', 0, true}};
+constexpr Band kSoftmax32[] = {{8, 'w', 2, false, 8}, {12, 'w', 2, true, 8}, {20, 'w', 2, false, 16}, {28, 'w', 4, false, 8}, {32, 'w', 2, false}, {33, 'w', 4, false, 16}, {40, 'w', 2, false}, {53, 'w', 4, false, 16}, {56, 'w', 4, false}, {63, 'w', 4, true}, {64, 'g', 0, true}, {65, 'w', 4, false}, {72, 'w', 4, true}, {81, 'w', 6, false}, {96, 'w', 6, true}, {112, 'w', 8, false}, {127, 'c', 4, false}, {128, 'w', 4, false}, {129, 'w', 8, false}, {144, 'w', 8, true}, {168, 'w', 6, false}, {176, 'g', 0, false}, {177, 'c', 4, false}, {192, 'w', 6, false}, {208, 'c', 4, false}, {225, 'c', 4, true}, {256, 'w', 8, false}, {288, 'g', 0, false}, {320, 'c', 2, true}, {448, 'c', 4, true}, {512, 'c', 2, true}, {576, 'g', 0, false}, {640, 'c', 4, true}, {704, 'g', 0, false}, {768, 'c', 4, true}, {896, 'g', 0, false}, {1024, 'c', 4, true}, {1536, 'c', 4, false}, {1792, 'g', 0, true}, {2048, 'c', 4, false}, {2560, 'x', 4, true, 32, 128}, {6144, 'x', 4, true, 32, 256}, {8192, 'x', 4, true, 32, 512}, {kBandEnd, 'g', 0, true}};
 constexpr Band kLayerNormBf16[] = {{16, 'w', 2, true, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {64, 'w', 4, true, 16}, {127, 'w', 4, true}, {192, 'w', 6, true}, {256, 'w', 8, true}, {384, 'r', 2, true}, {448, 'r', 4, true}, {640, 'r', 2, true}, {704, 'R', 3, true}, {768, 'R', 2, true}, {1024, 'r', 4, true}, {1792, 'R', 2, true}, {2048, 'r', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
 constexpr Band kLayerNormF16[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {56, 'w', 4, true, 16}, {64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true}, {448, 'g', 0, true}, {512, 'r', 3, true}, {576, 'c', 4, true}, {640, 'r', 6, true}, {704, 'R', 3, true}, {768, 'R', 2, true}, {896, 'c', 4, true}, {1024, 'r', 4, true}, {1280, 'R', 2, true}, {1408, 'x', 4, true, 32, 128}, {1792, 'R', 2, true}, {2048, 'c', 4, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
 constexpr Band kLayerNormF32[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'c', 2, true}, {64, 'w', 4, true, 16}, {112, 'w', 4, true}, {127, 'c', 4, true}, {169, 'w', 6, true}, {225, 'w', 8, true}, {256, 'g', 0, true}, {288, 'r', 2, true}, {320, 'c', 2, true}, {352, 'r', 6, true}, {512, 'g', 0, true}, {576, 'r', 2, true}, {640, 'c', 4, true}, {704, 'R', 4, true}, {768, 'c', 4, true}, {896, 'x', 4, true, 32, 128}, {1024, 'r', 6, true}, {1152, 'R', 3, true}, {1408, 'r', 2, true}, {1792, 'x', 4, true, 32, 128}, {2048, 'R', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
