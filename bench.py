@@ -1480,11 +1480,12 @@ def op_band_candidates(op: str, hv: int):
         for blk in (128, 256, 512):
             out.append((f"x{blk}", mk(_abi.KS_KERNEL_TWOPASS_ROW, 4, blk)))
         b = up32(-(-hv // 4))
-        if op == "layer_norm" and b <= 512:
+        if op == "layer_norm" and b <= 1024:
             for st in (2, 3, 4, 6, 8):
-                if 128 + st * hv * 16 <= 226 * 1024:
+                if 128 + st * hv * 16 <= 226 * 1024 and b <= 512:
                     out.append((f"r{st}", mk(_abi.KS_KERNEL_BULK_ROW, 4, b, st)))
-                # rSa: the weight and bias rows in shared memory beside the ring
+                # rSa: the weight and bias rows in shared memory beside the ring (up to 1024
+                # threads)
                 if 128 + (st + 2) * hv * 16 <= 226 * 1024:
                     out.append((f"r{st}a", mk(_abi.KS_KERNEL_BULK_ROW, 4, b, st,
                                                flags=_abi.KS_PLAN_AFFINE_SMEM)))

@@ -199,7 +199,8 @@ enum {
  *   LayerNorm  rows per CTA, block <= 128), KS_KERNEL_CTA_ROW (vec_per_thread 1, 2 or 4,
  *              block <= 512, block * vec_per_thread >= the row's vectors),
  *              KS_KERNEL_BULK_ROW (LayerNorm only: the staged ring, vec_per_thread 4,
- *              `stages` 2..8), KS_KERNEL_TWOPASS_ROW (the multi-pass wide kernel, vec_per_thread
+ *              `stages` 2..8, block * 4 >= the row's vectors, block <= 512, or 1024 with
+ *              KS_PLAN_AFFINE_SMEM), KS_KERNEL_TWOPASS_ROW (the multi-pass wide kernel, vec_per_thread
  *              4, block <= 1024 for Softmax and 512 for LayerNorm), KS_KERNEL_SCALAR
  *              (element loads, block <= 1024).
  * KS_PLAN_NO_PREFETCH picks the variant that loads each row when it comes: Softmax warp rows at

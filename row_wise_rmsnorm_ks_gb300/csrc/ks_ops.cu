@@ -621,9 +621,10 @@ __global__ void __launch_bounds__(kTeam ? 128 : 512) layer_norm_vec_kernel(void 
 // in flight (bounded) and returns.
 // kSmemWB: the weight and bias slices live in shared memory after the ring (filled once per
 // CTA) instead of in every thread's registers, 8 registers per vector a thread holds each, so
-// CTAs of 288..448 threads fit twice per SM.
+// CTAs of 288..448 threads fit twice per SM, and a CTA may have up to 1024 threads (rows of up
+// to 4096 vectors, where the ring and both rows fit in shared memory).
 template <typename T, int V, int kAffine, bool kSmemWB = false>
-__global__ void __launch_bounds__(512) layer_norm_bulk_kernel(void *out, const void *x,
+__global__ void __launch_bounds__(kSmemWB ? 1024 : 512) layer_norm_bulk_kernel(void *out, const void *x,
                                                               const void *w, const void *b,
                                                               int64_t rows, int64_t hidden,
                                                               int64_t hv, float eps, int stages) {
@@ -1191,9 +1192,9 @@ constexpr int64_t kRingSmemLimit = 226 * 1024;  // dynamic shared memory a ring 
 // BEGIN GENERATED OP BANDS
 constexpr Band kSoftmax16[] = {{16, 'w', 2, true, 8}, {20, 'w', 4, false, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {45, 'w', 4, false, 16}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {112, 'w', 4, true}, {127, 'c', 4, false}, {129, 'w', 6, true}, {144, 'w', 6, false}, {169, 'w', 8, true}, {225, 'w', 8, false}, {512, 'g', 0, false}, {576, 'c', 4, true}, {640, 'g', 0, false}, {704, 'c', 4, true}, {768, 'g', 0, false}, {896, 'c', 4, true}, {1024, 'g', 0, false}, {2048, 'g', 0, true}, {2560, 'x', 4, true, 32, 128}, {6144, 'x', 4, true, 32, 256}, {8192, 'x', 4, true, 32, 512}, {kBandEnd, 'g', 0, true}};
 constexpr Band kSoftmax32[] = {{8, 'w', 2, false, 8}, {12, 'w', 2, true, 8}, {20, 'w', 2, false, 16}, {28, 'w', 4, false, 8}, {32, 'w', 2, false}, {33, 'w', 4, false, 16}, {40, 'w', 2, false}, {53, 'w', 4, false, 16}, {56, 'w', 4, false}, {63, 'w', 4, true}, {64, 'g', 0, true}, {65, 'w', 4, false}, {72, 'w', 4, true}, {81, 'w', 6, false}, {96, 'w', 6, true}, {112, 'w', 8, false}, {127, 'c', 4, false}, {128, 'w', 4, false}, {129, 'w', 8, false}, {144, 'w', 8, true}, {168, 'w', 6, false}, {176, 'g', 0, false}, {177, 'c', 4, false}, {192, 'w', 6, false}, {208, 'c', 4, false}, {225, 'c', 4, true}, {256, 'w', 8, false}, {288, 'g', 0, false}, {320, 'c', 2, true}, {448, 'c', 4, true}, {512, 'c', 2, true}, {576, 'g', 0, false}, {640, 'c', 4, true}, {704, 'g', 0, false}, {768, 'c', 4, true}, {896, 'g', 0, false}, {1024, 'c', 4, true}, {1536, 'c', 4, false}, {1792, 'g', 0, true}, {2048, 'c', 4, false}, {2560, 'x', 4, true, 32, 128}, {6144, 'x', 4, true, 32, 256}, {8192, 'x', 4, true, 32, 512}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormBf16[] = {{16, 'w', 2, true, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {64, 'w', 4, true, 16}, {127, 'w', 4, true}, {192, 'w', 6, true}, {256, 'w', 8, true}, {384, 'r', 2, true}, {448, 'r', 4, true}, {640, 'r', 2, true}, {704, 'R', 3, true}, {768, 'R', 2, true}, {1024, 'r', 4, true}, {1792, 'R', 2, true}, {2048, 'r', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormF16[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {56, 'w', 4, true, 16}, {64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true}, {448, 'g', 0, true}, {512, 'r', 3, true}, {576, 'c', 4, true}, {640, 'r', 6, true}, {704, 'R', 3, true}, {768, 'R', 2, true}, {896, 'c', 4, true}, {1024, 'r', 4, true}, {1280, 'R', 2, true}, {1408, 'x', 4, true, 32, 128}, {1792, 'R', 2, true}, {2048, 'c', 4, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
-constexpr Band kLayerNormF32[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'c', 2, true}, {64, 'w', 4, true, 16}, {112, 'w', 4, true}, {127, 'c', 4, true}, {169, 'w', 6, true}, {225, 'w', 8, true}, {256, 'g', 0, true}, {288, 'r', 2, true}, {320, 'c', 2, true}, {352, 'r', 6, true}, {512, 'g', 0, true}, {576, 'r', 2, true}, {640, 'c', 4, true}, {704, 'R', 4, true}, {768, 'c', 4, true}, {896, 'x', 4, true, 32, 128}, {1024, 'r', 6, true}, {1152, 'R', 3, true}, {1408, 'r', 2, true}, {1792, 'x', 4, true, 32, 128}, {2048, 'R', 2, true}, {3072, 'x', 4, true, 32, 128}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormBf16[] = {{16, 'w', 2, true, 8}, {28, 'w', 4, true, 8}, {32, 'w', 2, true, 16}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'w', 2, true}, {64, 'w', 4, true, 16}, {127, 'w', 4, true}, {192, 'w', 6, true}, {256, 'w', 8, true}, {384, 'r', 2, true}, {448, 'r', 4, true}, {640, 'r', 2, true}, {704, 'R', 3, true}, {768, 'R', 2, true}, {1024, 'r', 4, true}, {1792, 'R', 2, true}, {2048, 'r', 2, true}, {2816, 'x', 4, true, 32, 128}, {3584, 'R', 2, true}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF16[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {56, 'w', 4, true, 16}, {64, 'w', 2, true}, {128, 'w', 4, true}, {192, 'w', 6, true}, {448, 'g', 0, true}, {512, 'r', 3, true}, {576, 'c', 4, true}, {640, 'r', 6, true}, {704, 'R', 3, true}, {768, 'R', 2, true}, {896, 'c', 4, true}, {1024, 'r', 4, true}, {1280, 'R', 2, true}, {1408, 'x', 4, true, 32, 128}, {1792, 'R', 2, true}, {2048, 'c', 4, true}, {3072, 'x', 4, true, 32, 128}, {3584, 'R', 2, true}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
+constexpr Band kLayerNormF32[] = {{16, 'w', 2, true, 8}, {32, 'w', 4, true, 8}, {52, 'w', 4, true, 16}, {53, 'w', 2, true}, {56, 'w', 4, true, 16}, {63, 'c', 2, true}, {64, 'w', 4, true, 16}, {112, 'w', 4, true}, {127, 'c', 4, true}, {169, 'w', 6, true}, {225, 'w', 8, true}, {256, 'g', 0, true}, {288, 'r', 2, true}, {320, 'c', 2, true}, {352, 'r', 6, true}, {512, 'g', 0, true}, {576, 'r', 2, true}, {640, 'c', 4, true}, {704, 'R', 4, true}, {768, 'c', 4, true}, {896, 'x', 4, true, 32, 128}, {1024, 'r', 6, true}, {1152, 'R', 3, true}, {1408, 'r', 2, true}, {1792, 'x', 4, true, 32, 128}, {3584, 'R', 2, true}, {4096, 'x', 4, true, 32, 256}, {kBandEnd, 'g', 0, true}};
 // END GENERATED OP BANDS
 
 // Applies the band of a row of hv vectors to p (the general rule's plan) when there are more rows
@@ -1213,7 +1214,8 @@ void apply_band(const Band *bands, int64_t hv, int64_t rows, int sms, ks_plan_t 
         if (block <= 512) *p = op_plan_of(KS_KERNEL_CTA_ROW, b->v, (int)block, b->prefetch);
     } else if (b->kind == 'r' || b->kind == 'R') {
         const int64_t affine = b->kind == 'R' ? 2 * hv * 16 : 0;  // weight and bias rows
-        if (many && ring_block <= 512 && 128 + (int64_t)b->v * hv * 16 + affine <= kRingSmemLimit) {
+        const int64_t max_block = b->kind == 'R' ? 1024 : 512;
+        if (many && ring_block <= max_block && 128 + (int64_t)b->v * hv * 16 + affine <= kRingSmemLimit) {
             *p = op_plan_of(KS_KERNEL_BULK_ROW, 4, (int)ring_block, true, b->v);
             if (b->kind == 'R') p->flags |= KS_PLAN_AFFINE_SMEM;
         }
@@ -1325,8 +1327,10 @@ ks_status_t op_check(int op, ks_plan_t &p, bool vec, int64_t width, int64_t elem
         break;
     case KS_KERNEL_BULK_ROW:
         if (!ln) return fail(KS_ERR_INVALID_ARGUMENT, "the staged ring is LayerNorm's");
-        if (p.vec_per_thread != 4 || (int64_t)p.block * 4 < width || p.block > 512)
-            return fail(KS_ERR_INVALID_ARGUMENT, "ring plan: 4 vectors per thread covering the row, block <= 512");
+        if (p.vec_per_thread != 4 || (int64_t)p.block * 4 < width ||
+            p.block > ((p.flags & KS_PLAN_AFFINE_SMEM) ? 1024 : 512))
+            return fail(KS_ERR_INVALID_ARGUMENT, "ring plan: 4 vectors per thread covering the row, "
+                        "block <= 512 (1024 with KS_PLAN_AFFINE_SMEM)");
         {
             // with the weight and bias in shared memory too (counted for both)
             const int64_t affine = (p.flags & KS_PLAN_AFFINE_SMEM) ? 2 * width * 16 : 0;

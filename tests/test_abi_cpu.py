@@ -561,6 +561,11 @@ def test_affine_smem_flag_only_for_the_layer_norm_ring():
     # LayerNorm ring of 2048 vectors: 6 stages fit alone (192 KiB), not with two more rows
     p = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 512, 6, flags=F)
     assert _abi.ks_layer_norm_planned(a, b, None, None, 64, 16384, 1e-5, BF16, p, None) == E
+    # rows of 2560 vectors: a 640-thread ring only with the flag; past 1024 threads never
+    p = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 640, 2)
+    assert _abi.ks_layer_norm_planned(a, b, None, None, 64, 20480, 1e-5, BF16, p, None) == E
+    p = _abi.make_plan(_abi.KS_KERNEL_BULK_ROW, 4, 1056, 2, flags=F)
+    assert _abi.ks_layer_norm_planned(a, b, None, None, 64, 33792, 1e-5, BF16, p, None) == E
 
 
 def test_smem_rows_flag_only_for_the_plain_split_ring():

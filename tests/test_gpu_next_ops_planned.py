@@ -58,7 +58,8 @@ def _row_plan(variant, op, dt, hidden):
         return None
     if block is None:
         block = max(32, _up32(-(-hv // v)))
-        if block > 512:
+        # up to 1024 threads for the ring with the weight and bias in shared memory
+        if block > (1024 if flags & A.KS_PLAN_AFFINE_SMEM else 512):
             return None
     if op == "layer_norm" and flags & NP:
         return None  # LayerNorm always prefetches
