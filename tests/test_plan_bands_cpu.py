@@ -323,3 +323,51 @@ def test_every_wide_width_gets_a_plan_the_library_accepts(dt, op):
                 assert p.smem_bytes == 128 + p.stages * sl * 16 * (2 if fused else 1)
                 assert p.smem_bytes <= 226 * 1024
         assert p.grid % C == 0 and p.grid >= C
+
+
+def _sweep_line(dt, hv, scores):
+    line = {"plan_sweep": dt, "op": "rms_norm", "hv": hv, "hidden": hv * 8, "rows": 1000,
+            "default_plan": {}, "default": scores["default"]}
+    line.update({k: v for k, v in scores.items() if k != "default"})
+    return json.dumps(line)
+
+
+def test_wide_record_keeps_the_last_run_per_width(tmp_path):
+    """A width measured by a later run takes that run's lines alone (it may time candidates the
+    earlier runs did not); a width measured twice in one run keeps the mean."""
+    a, b = tmp_path / "a.log", tmp_path / "b.log"
+    a.write_text("\n".join([
+        _sweep_line("bf16", 4096, {"default": 0.90, "b4s2": 0.90, "t512u2": 0.80}),
+        _sweep_line("bf16", 8192, {"default": 0.80, "b4s2": 0.85, "t512u2": 0.70}),
+        _sweep_line("bf16", 8192, {"default": 0.82, "b4s2": 0.87, "t512u2": 0.72}),
+    ]) + "\n")
+    b.write_text(_sweep_line("bf16", 4096, {"default": 0.91, "b4s2": 0.92, "b4s3m": 0.95}) + "\n")
+    rec = bench.wide_bands_record([str(a), str(b)], 152)
+    lines = {ln["hv"]: ln["scores"] for ln in rec["tables"]["bf16/rms_norm"]}
+    assert lines[4096] == {"default": 910, "b4s2": 920, "b4s3m": 950}  # the later run only
+    assert lines[8192] == {"default": 810, "b4s2": 860}  # mean of one run; t512u2 > 5 points behind
+
+
+def test_wide_derivation_takes_portable_clusters_only():
+    """A cluster of 16 is never a band's launch, however it scores: the default launch must not
+    depend on the device placing a non-portable cluster."""
+    rec = {"tables": {"bf16/rms_norm": [
+        {"hv": 4096, "rows": 1000, "scores": {"default": 900, "b16s3m": 990, "b8s2": 920}},
+        {"hv": 8192, "rows": 1000, "scores": {"default": 900, "b16s3v8m": 990, "b4s3m": 930}},
+    ]}}
+    bands = bench.derive_wide_bands(rec)["bf16/rms_norm"]
+    assert [n for _, n in bands] == ["b8s2", "b4s3m"]
+    assert bands[-1][0] == bench.WIDE_HI
+
+
+def test_candidate_names_of_default_launches():
+    """The record's default-launch names match the band sweep's candidate names for every
+    kernel kind, including a ring plan from a run that did not report its stages."""
+    name = bench.ops_candidate_name
+    assert name({"kernel_name": "warp_row", "vec_per_thread": 4, "flags": 0, "team": 32}, 100) == "w4"
+    assert name({"kernel_name": "warp_row", "vec_per_thread": 2, "flags": 1, "team": 8}, 16) == "t8v2n"
+    assert name({"kernel_name": "cta_row", "vec_per_thread": 4, "flags": 1, "block": 160}, 640) == "c4n"
+    assert name({"kernel_name": "bulk_row", "vec_per_thread": 4, "flags": 4, "stages": 2}, 1280) == "r2a"
+    # no stages reported: the ring's own rule, 64 KiB of rows per CTA (2..8 stages)
+    assert name({"kernel_name": "bulk_row", "vec_per_thread": 4, "flags": 0}, 1024) == "r4"
+    assert name({"kernel_name": "twopass_row", "vec_per_thread": 4, "flags": 0, "block": 256}, 4096) == "x256"
