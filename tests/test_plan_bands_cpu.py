@@ -371,3 +371,29 @@ def test_candidate_names_of_default_launches():
     # no stages reported: the ring's own rule, 64 KiB of rows per CTA (2..8 stages)
     assert name({"kernel_name": "bulk_row", "vec_per_thread": 4, "flags": 0}, 1024) == "r4"
     assert name({"kernel_name": "twopass_row", "vec_per_thread": 4, "flags": 0, "block": 256}, 4096) == "x256"
+
+
+def test_every_wide_band_launch_has_a_gpu_parity_variant():
+    """Each kind of launch the wide band tables name (kernel, vectors per thread, rows kept in
+    shared memory, two rows in flight) is among the explicit-plan variants the GPU parity test
+    runs on ragged shapes, so a re-derived table cannot pick a form no parity case covers."""
+    with open(os.path.join(ROOT, "tests", "test_gpu_parity.py")) as f:
+        src = f.read()
+    variants = set(re.findall(r'"((?:bulk_row|split|splitp|twopass|cluster_row)[a-z0-9_]*)"', src))
+    with open(WIDE) as f:
+        bands = bench.derive_wide_bands(json.load(f))
+    for key, table in bands.items():
+        for _, name in table:
+            kernel, cluster, block, v, stages, flags = bench.wide_plan_fields(name)
+            if kernel == _abi.KS_KERNEL_BULK_ROW:
+                smem_rows = bool(flags & _abi.KS_PLAN_SMEM_ROWS)
+                want = [x for x in variants if x.startswith("bulk_row_c")
+                        and ("_v8" in x) == (v == 8) and x.endswith("_m") == smem_rows]
+            elif kernel == _abi.KS_KERNEL_TWOPASS_ROW and cluster >= 2:
+                prefix = "splitp_" if stages == 2 else "split_"
+                want = [x for x in variants if x.startswith(prefix) and x.endswith(f"_u{v}")]
+            elif kernel == _abi.KS_KERNEL_TWOPASS_ROW:
+                want = [x for x in variants if x.startswith("twopass_") and x.endswith(f"_u{v}")]
+            else:
+                want = [x for x in variants if x.startswith("cluster_row")]
+            assert want, (key, name)
